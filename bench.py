@@ -1,0 +1,426 @@
+"""Throughput benchmark of draft-token verification on GB300.
+
+One step = one pass of the whole verification hot path over one batch:
+  * speculative-sampling verification of 64 sequences, k = 8 drafts,
+    V = 128256, bf16, T = 0.9, top-p 0.9 on target and draft rows;
+  * greedy chain verification of the same target rows (a separate copy, so
+    no kernel reads another's inputs out of L2);
+  * greedy token-tree verification of 8 trees of 60 nodes, depth <= 6,
+    V = 128256, bf16.
+Metric: verified draft positions per second (64*8 + 64*8 + 8*59 per step).
+
+Default: python bench.py [--gpus N --steps K --warmup W]; prints one JSON line.
+--impl reference times the float64 CPU oracle on a bounded sample instead.
+Under torchrun every rank runs its own batch on its own GPU (weak scaling,
+no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/sec on 1 GB300 and achieved HBM GB/s vs roofline"
+UNIT = "positions/s"
+SAMPLE = dict(B=64, k=8, V=128256, T=0.9, top_k=0, top_p=0.9)
+TREE = dict(B=8, N=60, V=128256, depth=6)
+
+
+def positions_per_step():
+    return SAMPLE["B"] * SAMPLE["k"] * 2 + TREE["B"] * (TREE["N"] - 1)
+
+
+def sample_bytes():
+    return SAMPLE["B"] * (2 * SAMPLE["k"] + 1) * SAMPLE["V"] * 2
+
+
+def greedy_bytes():
+    return SAMPLE["B"] * (SAMPLE["k"] + 1) * SAMPLE["V"] * 2
+
+
+def tree_bytes():
+    return TREE["B"] * TREE["N"] * TREE["V"] * 2
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "draft_token_verification_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads
+
+
+def make_inputs(seed_offset: int = 0):
+    s = W.config3(seed=3 + seed_offset, B=SAMPLE["B"], k=SAMPLE["k"], V=SAMPLE["V"])
+    t = W.config4(seed=4 + seed_offset, B=TREE["B"], N=TREE["N"], V=TREE["V"], max_depth=TREE["depth"])
+    return s, t
+
+
+def to_torch(arr, device=None, pin=False):
+    import torch
+
+    arr = np.ascontiguousarray(arr)
+    t = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr)
+    if arr.dtype == np.uint16:
+        t = t.view(torch.bfloat16)
+    if pin:
+        return t.pin_memory()
+    return t.to(device) if device is not None else t
+
+
+# ------------------------------------------------------------ GPU leg
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import draft_token_verification_gb300 as sv
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.build()
+    s, t = make_inputs(seed_offset=rank)
+    d = {
+        "target": to_torch(s.target, dev), "draft": to_torch(s.draft, dev), "tokens": to_torch(s.tokens, dev),
+        "uniforms": to_torch(s.uniforms, dev), "greedy_target": to_torch(s.target, dev),
+        "tree_logits": to_torch(t.logits, dev), "tree_tokens": to_torch(t.node_tokens, dev),
+        "parents": to_torch(t.parents, dev),
+    }
+    B, k = s.B, s.k
+    o = {
+        "tok": torch.empty((B, k + 1), dtype=torch.int32, device=dev), "n": torch.empty(B, dtype=torch.int32, device=dev),
+        "p": torch.empty((B, k), dtype=torch.float32, device=dev), "q": torch.empty((B, k), dtype=torch.float32, device=dev),
+        "gtok": torch.empty((B, k + 1), dtype=torch.int32, device=dev), "gn": torch.empty(B, dtype=torch.int32, device=dev),
+        "ttok": torch.empty((t.B, t.max_depth + 1), dtype=torch.int32, device=dev),
+        "tpath": torch.empty((t.B, t.max_depth + 1), dtype=torch.int32, device=dev),
+        "tn": torch.empty(t.B, dtype=torch.int32, device=dev),
+    }
+    ws = sv.Workspace(dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None, inputs=d):
+        if ev is not None:
+            ev[0].record(stream)
+        sv.spec_verify_sample(inputs["target"], inputs["draft"], inputs["tokens"], inputs["uniforms"], SAMPLE["T"],
+                              SAMPLE["top_k"], SAMPLE["top_p"], None, o["tok"], o["n"], o["p"], o["q"], ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        sv.spec_verify_tree_greedy(inputs["tree_logits"], inputs["tree_tokens"], inputs["parents"], TREE["depth"],
+                                   o["ttok"], o["tpath"], o["tn"], ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = sv.spec_get_status(ws)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        tdist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])] for e in evs])
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # acceptance statistics of the last step (MAL = accepted drafts per pass)
+    n_acc = o["n"].cpu().numpy()
+    gn = o["gn"].cpu().numpy()
+
+    # -------- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e_steps = max(3, min(20, args.steps // 50))
+    h = {key: to_torch(arr, pin=True) for key, arr in (
+        ("target", s.target), ("draft", s.draft), ("tokens", s.tokens), ("uniforms", s.uniforms),
+        ("tree_logits", t.logits), ("tree_tokens", t.node_tokens), ("parents", t.parents))}
+    host_out = {key: torch.empty(o[key].shape, dtype=o[key].dtype).pin_memory() for key in ("tok", "n", "gtok", "gn", "ttok", "tn")}
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for key, v in h.items():
+            d[key].copy_(v, non_blocking=True)
+        d_in = dict(d)
+        d_in["greedy_target"] = d["target"]
+        step(None, d_in)
+        for key, v in host_out.items():
+            v.copy_(o[key], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    status |= sv.spec_get_status(ws)
+
+    return dict(elapsed_ms=elapsed_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
+                h2d=h2d, d2h=d2h, mal=float(n_acc.mean()), greedy_mal=float(gn.mean()))
+
+
+# ------------------------------------------------------------ CPU leg
+
+
+def cpu_baseline(sample_seqs: int = 4, trees: int = 2, threads: int | None = None):
+    """The float64 oracle, as it stands, on a bounded sample of the same
+    workload: `sample_seqs` sampling + greedy sequences and `trees` trees."""
+    import oracle
+
+    s, t = make_inputs()
+    cores = threads or len(os.sched_getaffinity(0))
+    jobs = []
+    for b in range(sample_seqs):
+        jobs.append(("sample", b))
+        jobs.append(("greedy", b))
+    for b in range(trees):
+        jobs.append(("tree", b))
+
+    def run(job):
+        kind, b = job
+        sl = slice(b, b + 1)
+        if kind == "sample":
+            oracle.verify_sample(s.target[sl], s.draft[sl], s.tokens[sl], s.uniforms[sl], SAMPLE["T"],
+                                 SAMPLE["top_k"], SAMPLE["top_p"], all_rows=False)
+            return SAMPLE["k"]
+        if kind == "greedy":
+            oracle.verify_greedy(s.target[sl], s.tokens[sl])
+            return SAMPLE["k"]
+        oracle.verify_tree_greedy(t.logits[sl], t.node_tokens[sl], t.parents[sl], t.max_depth)
+        return TREE["N"] - 1
+
+    oracle.build()
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(cores) as pool:
+        positions = sum(pool.map(run, jobs))
+    dt = time.perf_counter() - t0
+    return {"value": positions / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{sample_seqs} sampling + {sample_seqs} greedy sequences (k=8, V=128256) and {trees} trees "
+                      f"(60 nodes) of the benchmark batch; {positions} positions in {dt:.2f} s"}
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_baseline()
+        steps_equiv = None
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": positions_per_step() / cb["value"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(), "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        del steps_equiv
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as tdist
+
+            tdist.destroy_process_group()
+        return
+    K = args.steps
+    per = r["per"]
+    pos = positions_per_step() * world
+    value = pos * K / (r["elapsed_ms"] / 1e3)
+    peak, peak_kind = measured_peaks()
+    t_sample = float(per[:, 0].mean()) / 1e3
+    achieved = sample_bytes() / t_sample / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": r["elapsed_ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
+        "clocks": r["clk"],
+        "e2e": {"value": pos * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 3 * K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic("sample"), "kernel": "sample_kernel<bf16, cluster 8>",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "kernels": {
+            "sample": {"us": t_sample * 1e6, "GB/s": achieved, "frac": achieved / peak,
+                       "algorithmic_bytes": sample_bytes()},
+            "greedy": {"us": float(per[:, 1].mean()) * 1e3,
+                       "GB/s": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9,
+                       "frac": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9 / peak,
+                       "algorithmic_bytes": greedy_bytes()},
+            "tree": {"us": float(per[:, 2].mean()) * 1e3,
+                     "GB/s": tree_bytes() / (float(per[:, 2].mean()) / 1e3) / 1e9,
+                     "frac": tree_bytes() / (float(per[:, 2].mean()) / 1e3) / 1e9 / peak,
+                     "algorithmic_bytes": tree_bytes()},
+        },
+        "acceptance": {"sample_mal": r["mal"], "greedy_mal": r["greedy_mal"], "k": SAMPLE["k"]},
+        "status_bits": r["status"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.destroy_process_group()
+
+
+def workload_config(world: int = 1):
+    return {
+        "workload": "sampling verify B=64 k=8 V=128256 bf16 T=0.9 top-p 0.9 (+ greedy on the same target rows) "
+                    "+ greedy tree 8x60 nodes depth<=6 V=128256 bf16",
+        "B": SAMPLE["B"], "k": SAMPLE["k"], "V": SAMPLE["V"], "tree_B": TREE["B"], "tree_N": TREE["N"],
+        "positions_per_step_per_gpu": positions_per_step(),
+        "l2": "inputs larger than L2: each kernel's inputs were last touched >= 2x L2 bytes earlier",
+        "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+        "drafts": "Gumbel-max samples of the unfiltered draft softmax at T",
+    }
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+// api.cu -- the extern "C" boundary of libspecverify.so: argument checks on
+// the host, workspace layout, launch shapes, status word and the speedup
+// calculator helpers.  Declarations and the meaning of every argument are in
+// include/spec_verify.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kChunkTarget = 16384;  // elements per CTA slice of a sampling row
+
+bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
+size_t elt_bytes(spec_dtype d) { return d == SPEC_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Rows start on 16-byte boundaries: the bulk-copy / vector-load fast path.
+int rows_aligned(const void* base, int V, spec_dtype d) {
+  return aligned16(base) && ((static_cast<size_t>(V) * elt_bytes(d)) % 16 == 0) ? 1 : 0;
+}
+
+int check_workspace(void* ws, size_t bytes, int B, int k) {
+  if (!ws) return SPEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  if (bytes < ws_layout(B, k).total) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+// Cluster size and per-CTA slice for a sampling row of V elements.
+bool sample_shape(int V, spec_dtype d, bool filter, int* cluster, int* chunk) {
+  int cs = 1;
+  while (cs < 16 && (V + cs - 1) / cs > kChunkTarget) cs *= 2;
+  int ch = ((V + cs - 1) / cs + 7) / 8 * 8;
+  const size_t smem = sample_smem_bytes(d == SPEC_BF16 ? DT_BF16 : DT_F32, ch, filter);
+  if (smem > 200 * 1024) return false;
+  *cluster = cs;
+  *chunk = ch;
+  return true;
+}
+
+int run_sample(const void* target, const void* draft, const int32_t* tokens, const float* uniforms, int B, int k,
+               int V, spec_dtype dtype, const spec_sampling_params* sp, int32_t* out_tokens, int32_t* out_n,
+               float* out_p, float* out_q, float* out_probs, void* ws, size_t ws_bytes, void* stream, int mode) {
+  if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
+  if (!sp || !target || B < 1 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (mode == MODE_SAMPLE) {
+    if (!draft || !tokens || !uniforms || !out_tokens || !out_n || k < 1 || k > SPEC_MAX_K)
+      return SPEC_ERR_INVALID_ARG;
+  } else if (!out_probs) {
+    return SPEC_ERR_INVALID_ARG;
+  }
+  if (!sp->temperature_per_seq && !(sp->temperature > 0.f && isfinite(sp->temperature))) return SPEC_ERR_INVALID_ARG;
+  if (sp->top_k < 0 || !(sp->top_p > 0.f && sp->top_p <= 1.f)) return SPEC_ERR_INVALID_ARG;
+  const size_t es = elt_bytes(dtype);
+  if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || (tokens && !aligned_to(tokens, 4)) ||
+      (uniforms && !aligned_to(uniforms, 4)))
+    return SPEC_ERR_INVALID_ARG;
+  const int rc = check_workspace(ws, ws_bytes, B, mode == MODE_SAMPLE ? k : 0);
+  if (rc != SPEC_OK) return rc;
+
+  SampleArgs a = {};
+  a.target = target;
+  a.draft = draft;
+  a.tokens = tokens;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.k = mode == MODE_SAMPLE ? k : 0;
+  a.V = V;
+  a.temperature = sp->temperature;
+  a.temperature_per_seq = sp->temperature_per_seq;
+  a.top_k = (sp->top_k > 0 && sp->top_k < V) ? sp->top_k : 0;
+  a.top_p = sp->top_p;
+  a.out_tokens = out_tokens;
+  a.out_n = out_n;
+  a.out_p = out_p;
+  a.out_q = out_q;
+  a.out_probs = out_probs;
+  const WsLayout L = ws_layout(B, a.k);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(w + L.status);
+  a.tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
+  a.recs = reinterpret_cast<UnitRec*>(w + L.s_recs);
+  a.aligned_target = rows_aligned(target, V, dtype);
+  a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
+  a.mode = mode;
+  int cluster = 1;
+  if (!sample_shape(V, dtype, a.top_k > 0 || a.top_p < 1.f, &cluster, &a.chunk)) return SPEC_ERR_UNSUPPORTED;
+  const int units = mode == MODE_SAMPLE ? B * (k + 1) : B;
+  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, cluster, units, stream);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
+// CTAs per row for the argmax kernel: slices of a multiple of 8 elements,
+// enough CTAs to cover the GPU a few times over.
+int argmax_split_len(int rows, int V) {
+  int len = 8192;
+  while (len > 1024 && static_cast<long long>(rows) * ((V + len - 1) / len) < 4 * 152) len /= 2;
+  return len;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int B, int k, int V, spec_dtype dtype) {
+  if (B < 1 || k < 0 || k > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V || !dtype_ok(dtype)) return 0;
+  return ws_layout(B, k).total;
+}
+
+int spec_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                       const float* uniforms, int B, int k, int V, spec_dtype dtype,
+                       const spec_sampling_params* params, int32_t* out_tokens, int32_t* out_num_accepted,
+                       float* out_p_draft, float* out_q_draft, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream) {
+  return run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
+                    out_num_accepted, out_p_draft, out_q_draft, nullptr, workspace, workspace_bytes, cuda_stream,
+                    MODE_SAMPLE);
+}
+
+int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype, const spec_sampling_params* params,
+                         float* out_probs, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return run_sample(logits, nullptr, nullptr, nullptr, R, 0, V, dtype, params, nullptr, nullptr, nullptr, nullptr,
+                    out_probs, workspace, workspace_bytes, cuda_stream, MODE_PROBS);
+}
+
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int k, int V,
+                       spec_dtype dtype, int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                       size_t workspace_bytes, void* cuda_stream) {
+  if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(target_logits, elt_bytes(dtype)) || !aligned_to(draft_tokens, 4)) return SPEC_ERR_INVALID_ARG;
+  const int rc = check_workspace(workspace, workspace_bytes, B, k);
+  if (rc != SPEC_OK) return rc;
+  const WsLayout L = ws_layout(B, k);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  ArgmaxArgs a = {};
+  a.logits = target_logits;
+  a.tokens = draft_tokens;
+  a.B = B;
+  a.R = k + 1;
+  a.V = V;
+  a.split_len = argmax_split_len(B * (k + 1), V);
+  a.splits = (V + a.split_len - 1) / a.split_len;
+  a.aligned = rows_aligned(target_logits, V, dtype);
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status);
+  a.slots = reinterpret_cast<unsigned long long*>(w + L.g_slots);
+  a.tickets = reinterpret_cast<uint32_t*>(w + L.g_tickets);
+  if (launch_argmax(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, false, cuda_stream) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
+int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens, const int32_t* parents, int B,
+                            int N, int V, int max_depth, spec_dtype dtype, int32_t* out_tokens, int32_t* out_path,
+                            int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream) {
+  if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
+  if (!node_logits || !node_tokens || !parents || !out_tokens || !out_path || !out_num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V || max_depth < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(node_logits, elt_bytes(dtype)) || !aligned_to(node_tokens, 4) || !aligned_to(parents, 4))
+    return SPEC_ERR_INVALID_ARG;
+  const int rc = check_workspace(workspace, workspace_bytes, B, N - 1);
+  if (rc != SPEC_OK) return rc;
+  const WsLayout L = ws_layout(B, N - 1);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  ArgmaxArgs a = {};
+  a.logits = node_logits;
+  a.tokens = node_tokens;
+  a.parents = parents;
+  a.B = B;
+  a.R = N;
+  a.V = V;
+  a.max_depth = max_depth;
+  a.split_len = argmax_split_len(B * N, V);
+  a.splits = (V + a.split_len - 1) / a.split_len;
+  a.aligned = rows_aligned(node_logits, V, dtype);
+  a.out_tokens = out_tokens;
+  a.out_path = out_path;
+  a.out_n = out_num_accepted;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status);
+  a.slots = reinterpret_cast<unsigned long long*>(w + L.g_slots);
+  a.tickets = reinterpret_cast<uint32_t*>(w + L.g_tickets);
+  if (launch_argmax(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, true, cuda_stream) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
+int spec_get_status(void* workspace, uint32_t* status, void* cuda_stream) {
+  if (!workspace || !status) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  uint32_t* dev = static_cast<uint32_t*>(workspace);
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, dev, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaMemsetAsync(dev, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  *status = host;
+  if (host & SPEC_STATUS_TIMEOUT) return SPEC_ERR_TIMEOUT;
+  return host ? SPEC_ERR_DEVICE_DATA : SPEC_OK;
+}
+
+const char* spec_error_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_DTYPE: return "unsupported dtype";
+    case SPEC_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case SPEC_ERR_LAUNCH: return "CUDA launch or copy failed";
+    case SPEC_ERR_DEVICE_DATA: return "device found invalid data (see status bits)";
+    case SPEC_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case SPEC_ERR_UNSUPPORTED: return "shape beyond the library's limits";
+    default: return "unknown error code";
+  }
+}
+
+double spec_expected_tokens(double alpha, int gamma) {
+  double e = 0.0, p = 1.0;
+  for (int i = 0; i <= gamma; ++i) {
+    e += p;
+    p *= alpha;
+  }
+  return e;
+}
+
+double spec_improvement_factor(double alpha, int gamma, double c) {
+  return spec_expected_tokens(alpha, gamma) / (static_cast<double>(gamma) * c + 1.0);
+}
+
+double spec_break_even_acceptance(int k) { return static_cast<double>(k) / static_cast<double>(k + 1); }
+
+}  // extern "C"

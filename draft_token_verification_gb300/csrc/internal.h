@@ -1,0 +1,105 @@
+// internal.h -- declarations shared by the C ABI (api.cu) and the kernels:
+// dtype codes, the workspace layout and the kernel argument blocks.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace specv {
+
+constexpr int DT_F32 = 0;
+constexpr int DT_BF16 = 1;
+
+constexpr int kThreads = 256;           // threads per CTA in every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kWindow = 1024;           // exact-value histogram bins per row
+constexpr int kMaxK = 31;
+constexpr int kMaxTreeNodes = 1024;
+
+constexpr int MODE_SAMPLE = 0;          // speculative-sampling verification
+constexpr int MODE_PROBS = 1;           // write filtered probabilities
+
+// Per (sequence, position) result of the sampling kernel, written by the CTA
+// that owns the draft token (accept, px, qx) and by the CTA that owns the
+// drawn token (drawn).
+struct UnitRec {
+  int32_t accept;
+  int32_t drawn;
+  float px;
+  float qx;
+};
+
+// Workspace layout (byte offsets), identical for every call with the same
+// (B, k).  All regions are zero between calls except the status word.
+struct WsLayout {
+  size_t status;      // uint32 status word (sticky bits)
+  size_t s_tickets;   // uint32[B]  arrivals per sequence, sampling kernel
+  size_t s_recs;      // UnitRec[B*(k+1)]
+  size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
+  size_t g_tickets;   // uint32[B]  arrivals per sequence / tree, argmax kernel
+  size_t total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int B, int k) {
+  WsLayout w;
+  const size_t units = static_cast<size_t>(B) * static_cast<size_t>(k + 1);
+  w.status = 0;
+  w.s_tickets = 256;
+  w.s_recs = align_up(w.s_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.g_slots = align_up(w.s_recs + sizeof(UnitRec) * units, 256);
+  w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
+  w.total = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  return w;
+}
+
+struct SampleArgs {
+  const void* target;          // [B][k+1][V] (MODE_PROBS: [R][V])
+  const void* draft;           // [B][k][V]
+  const int32_t* tokens;       // [B][k]
+  const float* uniforms;       // [B][k+2]
+  int B, k, V;
+  float temperature;
+  const float* temperature_per_seq;
+  int top_k;                   // already clamped: 0 = off
+  float top_p;                 // >= 1 = off
+  int32_t* out_tokens;
+  int32_t* out_n;
+  float* out_p;
+  float* out_q;
+  float* out_probs;            // MODE_PROBS output [R][V]
+  uint32_t* status;
+  uint32_t* tickets;
+  UnitRec* recs;
+  int chunk;                   // elements per CTA, multiple of 8
+  int aligned_target;          // rows start on 16-byte boundaries
+  int aligned_draft;
+  int mode;
+};
+
+struct ArgmaxArgs {
+  const void* logits;          // [B][R][V]
+  const int32_t* tokens;       // chain: drafts [B][k]; tree: node tokens [B][N]
+  const int32_t* parents;      // tree only
+  int B, R, V;                 // R rows per sequence (k+1, or N)
+  int max_depth;               // tree only
+  int splits;                  // CTAs per row
+  int split_len;               // elements per CTA, multiple of 8
+  int aligned;
+  int32_t* out_tokens;
+  int32_t* out_path;
+  int32_t* out_n;
+  uint32_t* status;
+  unsigned long long* slots;
+  uint32_t* tickets;
+};
+
+// Launchers (return a cudaError_t as int).
+int launch_sample(const SampleArgs& a, int dtype, int cluster, int units, void* stream);
+int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
+size_t sample_smem_bytes(int dtype, int chunk, bool filter);
+
+}  // namespace specv

@@ -1,0 +1,205 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so: the verification step of
+ * speculative decoding on one NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute is stated on these pages (cited by title and
+ * section):
+ *   [EIN]  Edge Inference Notes, post on speculative decoding and EAGLE-3:
+ *          "The core idea: draft, then check" (step 3, accept or correct),
+ *          "Why it changes nothing about the output" (temperature, top-k and
+ *          nucleus adjust both distributions before the test) and
+ *          "One decode round, end to end" (greedy token tree, longest agreed
+ *          path plus one correction).
+ *   [TGTG] "Towards Green Text Generation: Memory-Based Speculative
+ *          Decoding", section 2.4 "Verifier and Acceptance" (greedy chain
+ *          verification of k drafts from k+1 target rows) and section 5.1
+ *          "The Verifier Cost Model" (equation 1).
+ *   [SDSC] "Speculative Decoding Speedup Calculator", steps 1-3.
+ *
+ * Conventions shared by every entry point:
+ *   - Array arguments are DEVICE pointers owned by the caller, contiguous,
+ *     row-major, row stride V, aligned to their element size.  Rows whose
+ *     start is 16-byte aligned (V * element size a multiple of 16 and the
+ *     base 16-byte aligned) take the bulk-copy fast path; others are read
+ *     with plain loads and give the same results.
+ *   - Every call is asynchronous on `cuda_stream` (a cudaStream_t, NULL for
+ *     the legacy default stream), allocates nothing and does not synchronise.
+ *   - `workspace` is caller-owned device memory of at least
+ *     spec_verify_workspace_size(...) bytes, 256-byte aligned, ZEROED ONCE
+ *     when it is created.  Every kernel leaves it zeroed again (apart from
+ *     the status word), so it can be reused by later calls on the same
+ *     stream.  Two calls that may run concurrently need separate workspaces.
+ *   - Return codes are SPEC_OK or a negative SPEC_ERR_* value; argument
+ *     errors are detected on the host before anything is launched.  Errors
+ *     found in the data on the device (out-of-range tokens, NaN/+inf rows,
+ *     malformed parent arrays) never trap: they set bits of the status word
+ *     in the workspace, read with spec_get_status().
+ *   - Ties are broken to the lowest token index (argmax, top-k cut) and to
+ *     the lowest node index (deepest agreed tree node).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Return codes. */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)  /* null pointer, bad size, bad parameter     */
+#define SPEC_ERR_DTYPE (-2)        /* dtype is not SPEC_F32 / SPEC_BF16         */
+#define SPEC_ERR_WORKSPACE (-3)    /* workspace too small or misaligned         */
+#define SPEC_ERR_LAUNCH (-4)       /* a CUDA launch or copy failed              */
+#define SPEC_ERR_DEVICE_DATA (-5)  /* spec_get_status found a status bit set    */
+#define SPEC_ERR_TIMEOUT (-6)      /* a bounded device wait gave up             */
+#define SPEC_ERR_UNSUPPORTED (-7)  /* shape beyond the library's limits         */
+
+/* Status bits written by the device (bitwise OR, sticky until read). */
+#define SPEC_STATUS_BAD_TOKEN 1u   /* a draft token outside [0, V): rejected    */
+#define SPEC_STATUS_BAD_ROW 2u     /* a row with NaN, +inf or no finite entry,
+                                      or a per-sequence temperature <= 0        */
+#define SPEC_STATUS_BAD_PARENT 4u  /* parents[0] != -1 or parents[j] not in [0, j) */
+#define SPEC_STATUS_DEPTH 8u       /* an agreed tree node deeper than max_depth */
+#define SPEC_STATUS_TIMEOUT 16u    /* a bounded wait on a bulk copy gave up     */
+
+/* Limits. */
+#define SPEC_MAX_K 31              /* drafts per sequence                       */
+#define SPEC_MAX_TREE_NODES 1024   /* nodes per tree                            */
+#define SPEC_MAX_V (1 << 24)       /* vocabulary size                           */
+
+/*
+ * Sampling parameters ([EIN] "Why it changes nothing about the output": the
+ * same temperature and filters are applied to the target row p and to the
+ * draft row q before the accept test).
+ *   temperature          scalar T > 0, used when temperature_per_seq is NULL
+ *   temperature_per_seq  device float[B] (per sequence, or per row for
+ *                        spec_transform_probs), or NULL
+ *   top_k                0 = off, else keep the top_k highest-ranked tokens
+ *                        (rank = value descending, index ascending)
+ *   top_p                in (0, 1]; 1 = off.  Applied after top-k, on the
+ *                        renormalised top-k distribution: a token is kept iff
+ *                        the mass ranked strictly before it is < top_p.
+ */
+typedef struct {
+  float temperature;
+  const float* temperature_per_seq;
+  int top_k;
+  float top_p;
+} spec_sampling_params;
+
+/*
+ * Workspace bytes needed by spec_verify_sample / spec_verify_greedy for B
+ * sequences of k drafts, and by spec_verify_tree_greedy with k = N - 1 and
+ * spec_transform_probs with B = R rows and k = 0.  Returns 0 for sizes
+ * outside the limits.
+ */
+size_t spec_verify_workspace_size(int B, int k, int V, spec_dtype dtype);
+
+/*
+ * Speculative-sampling verification ([EIN] "The core idea: draft, then
+ * check", step 3).  For every sequence b, left to right over i = 0..k-1:
+ *   p_i = filter(softmax(target[b][i] / T)), q_i = filter(softmax(draft[b][i] / T))
+ *   accept x_i = draft_tokens[b][i]  iff  u_i * q_i(x_i) < p_i(x_i)
+ *   (i.e. with probability min(1, p/q)); stop at the first rejection, n = i.
+ *   If n < k, draw one token from max(0, p_n - q_n) / S with u_{k+1};
+ *   else draw the bonus token from p_k with u_k.  Draws take the smallest
+ *   index j whose running sum (ascending index order) exceeds u * S.
+ *   A residual of total mass 0 (reachable only through rounding) is replaced
+ *   by p_n.
+ *
+ *   target_logits     [B][k+1][V] dtype   target rows at the k+1 positions
+ *   draft_logits      [B][k][V]   dtype   draft LOGITS (q = filtered softmax
+ *                                         of draft_logits / T); a caller that
+ *                                         holds probabilities passes log q
+ *   draft_tokens      [B][k]      int32
+ *   uniforms          [B][k+2]    float   in [0, 1): u_0..u_{k-1} accept
+ *                                         tests, u_k bonus, u_{k+1} resample
+ *   B >= 1, 1 <= k <= SPEC_MAX_K, 1 <= V <= SPEC_MAX_V
+ *   params            HOST pointer
+ *   out_tokens        [B][k+1]    int32   x_0..x_{n-1}, drawn token, then -1
+ *   out_num_accepted  [B]         int32   n in [0, k]; n + 1 tokens committed
+ *   out_p_draft, out_q_draft  [B][k] float or NULL: p_i(x_i), q_i(x_i) for
+ *                     every i (computed for all positions, not only i <= n)
+ * A draft token outside [0, V) is rejected and sets SPEC_STATUS_BAD_TOKEN;
+ * a non-finite row gives drawn token -1 and sets SPEC_STATUS_BAD_ROW.
+ */
+int spec_verify_sample(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms, int B, int k,
+                       int V, spec_dtype dtype, const spec_sampling_params* params,
+                       int32_t* out_tokens, int32_t* out_num_accepted, float* out_p_draft,
+                       float* out_q_draft, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream);
+
+/*
+ * Greedy chain verification ([TGTG] section 2.4): a_i = argmax of the raw
+ * target row i (lowest index on ties; temperature and filters do not change
+ * an argmax and are not taken); n = first i < k with x_i != a_i, else k.
+ *   target_logits [B][k+1][V], draft_tokens [B][k]
+ *   out_tokens [B][k+1] = x_0..x_{n-1}, a_n, then -1; out_num_accepted [B] = n
+ */
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int k,
+                       int V, spec_dtype dtype, int32_t* out_tokens, int32_t* out_num_accepted,
+                       void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Greedy token-tree verification ([EIN] "One decode round, end to end").
+ * Node 0 of every tree is the root (the last committed token, its token is
+ * ignored); row j of node_logits is the target's distribution for the token
+ * after node j.  Node j (j >= 1) is agreed iff its parent is agreed and
+ * node_tokens[j] == argmax(row parents[j]).  The deepest agreed node d*
+ * (lowest index among equally deep ones) is committed with its path.
+ *   node_logits  [B][N][V], node_tokens [B][N], parents [B][N]
+ *                (parents[0] = -1, 0 <= parents[j] < j), 1 <= N <= 1024
+ *   max_depth    >= 1, at least the depth of every node that can be agreed
+ *   out_tokens   [B][max_depth+1]: tokens of the path root-exclusive, then
+ *                argmax(row d*), then -1
+ *   out_path     [B][max_depth+1]: node ids of the path (root excluded), -1 padded
+ *   out_num_accepted [B] = depth(d*)
+ * A malformed parent entry sets SPEC_STATUS_BAD_PARENT (that node is not
+ * agreed); an agreed node deeper than max_depth is ignored and sets
+ * SPEC_STATUS_DEPTH.
+ */
+int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
+                            const int32_t* parents, int B, int N, int V, int max_depth,
+                            spec_dtype dtype, int32_t* out_tokens, int32_t* out_path,
+                            int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream);
+
+/*
+ * The filtered, normalised distribution the accept test uses, written out
+ * for R independent rows ([EIN] "Why it changes nothing about the output").
+ *   logits [R][V] dtype -> out_probs [R][V] float (0 outside the kept set).
+ * params->temperature_per_seq, if set, is indexed by row.
+ */
+int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype,
+                         const spec_sampling_params* params, float* out_probs, void* workspace,
+                         size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Copies the status word of `workspace` to *status (host), then clears it.
+ * Synchronises with `cuda_stream`.  Returns SPEC_OK if no bit was set,
+ * SPEC_ERR_DEVICE_DATA if one was, SPEC_ERR_LAUNCH if the copy failed.
+ */
+int spec_get_status(void* workspace, uint32_t* status, void* cuda_stream);
+
+/* Static description of a return code. */
+const char* spec_error_string(int code);
+
+/* [SDSC] step 1: expected tokens per pass, 1 + a + ... + a^gamma. */
+double spec_expected_tokens(double alpha, int gamma);
+
+/* [SDSC] steps 2-3: E(alpha, gamma) / (gamma * c + 1). */
+double spec_improvement_factor(double alpha, int gamma, double c);
+
+/* [TGTG] section 5.1, equation 1: break-even acceptance k / (k + 1). */
+double spec_break_even_acceptance(int k);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

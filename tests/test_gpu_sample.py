@@ -1,0 +1,194 @@
+"""GPU parity of speculative-sampling verification against the float64 oracle.
+
+Bar (per sequence): identical accept count and committed tokens, except for
+sequences the oracle flags as within 1e-6 of a decision edge (counted; must
+stay under 1e-5 of all draws); p_i(x_i), q_i(x_i) within 1e-5 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity_utils import (BOUNDARY_BUDGET, compare_sample, lib, q_support_mask, run_sample_gpu,
+                          run_sample_oracle, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+_BOUNDARY = {"count": 0, "draws": 0}
+
+
+def _check(case, seqs=None):
+    gpu = run_sample_gpu(case)
+    orc = run_sample_oracle(case, seqs)
+    nb, draws = compare_sample(case, gpu, orc, seqs)
+    _BOUNDARY["count"] += nb
+    _BOUNDARY["draws"] += draws
+    return gpu, orc
+
+
+def test_config1_fp32_no_filter():
+    case = W.config1()
+    gpu, orc = _check(case)
+    # the same logits through greedy mode
+    g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
+    o = oracle.verify_greedy(case.target, case.tokens)
+    assert np.array_equal(g_tok.cpu().numpy(), o["tokens"]) and np.array_equal(g_n.cpu().numpy(), o["n"])
+
+
+def test_config2_topk50_bf16():
+    case = W.config2(mask_fn=q_support_mask(50, 1.0))
+    _check(case)
+
+
+@pytest.mark.parametrize("per_seq", [False, True])
+def test_config3_topp_full_size_sampled(per_seq):
+    case = W.config3(per_seq_temperature=per_seq)
+    seqs = list(range(0, case.B, 4))  # the oracle checks every 4th sequence of the full launch
+    _check(case, seqs)
+
+
+@pytest.mark.parametrize("B,k,sigma", [(1, 1, 0.5), (4, 12, 2.0), (16, 4, 4.0), (64, 8, 0.5), (128, 2, 2.0)])
+def test_config5_sweep_points(B, k, sigma):
+    case = W.config5(B, k, sigma)
+    seqs = list(range(0, B, max(1, B // 8)))
+    _check(case, seqs)
+    o = oracle.verify_greedy(case.target, case.tokens)
+    g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
+    assert np.array_equal(g_tok.cpu().numpy(), o["tokens"]) and np.array_equal(g_n.cpu().numpy(), o["n"])
+
+
+EDGE = [
+    # (B, k, V, dtype, top_k, top_p, extra)
+    (3, 1, 1, W.BF16, 0, 1.0, {}),
+    (5, 2, 7, W.BF16, 0, 1.0, {}),
+    (5, 3, 8, W.F32, 0, 1.0, {}),
+    (6, 4, 9, W.BF16, 3, 1.0, {}),
+    (6, 5, 33, W.F32, 0, 0.8, {}),
+    (8, 12, 1000, W.BF16, 20, 0.9, {}),
+    (8, 31, 257, W.BF16, 0, 0.7, {"per_seq_temperature": True}),
+    (4, 6, 4099, W.F32, 40, 0.95, {}),
+    (4, 3, 70001, W.BF16, 0, 0.5, {"temperature": 0.6}),
+    (6, 4, 2003, W.BF16, 7, 1.0, {"quantize": 0.5}),
+    (6, 4, 2003, W.BF16, 0, 0.6, {"quantize": 0.5}),
+    (6, 4, 2000, W.F32, 5, 0.8, {"quantize": 1.0}),
+    (4, 2, 5000, W.BF16, 1, 1.0, {}),
+    (4, 2, 300, W.BF16, 300, 1.0, {}),
+    (4, 2, 300, W.BF16, 0, 1e-4, {}),
+    (3, 2, 100000, W.BF16, 0, 0.95, {"sigma": 0.05}),
+]
+
+
+@pytest.mark.parametrize("B,k,V,dtype,top_k,top_p,extra", EDGE,
+                         ids=[f"B{e[0]}k{e[1]}V{e[2]}{e[3]}tk{e[4]}tp{e[5]}{''.join(e[6])}" for e in EDGE])
+def test_edge_shapes_and_filters(B, k, V, dtype, top_k, top_p, extra):
+    extra = dict(extra)
+    T = extra.pop("temperature", 1.0)
+    case = W.random_sample_case(B, k, V, dtype=dtype, seed=V + k, top_k=top_k, top_p=top_p, temperature=T,
+                                mask_fn=q_support_mask(top_k, top_p) if V <= 5000 else None, **extra)
+    _check(case)
+
+
+def test_all_equal_logits_ties_everywhere():
+    B, k, V = 4, 3, 5000
+    case = W.random_sample_case(B, k, V, seed=7, top_k=0, top_p=1.0)
+    case.target[:] = W.bf16_bits(np.full((B, k + 1, V), 1.5, np.float32))
+    d = np.full((B, k, V), 1.5, np.float32)
+    d[..., :5] = 3.0  # the draft prefers five tokens; the target is flat
+    case.draft[:] = W.bf16_bits(d)
+    case.tokens[:, 0] = np.arange(B) % 7  # some drafts inside, some outside those five
+    for top_k, top_p in ((0, 1.0), (17, 1.0), (0, 0.3), (100, 0.5)):
+        case.top_k, case.top_p = top_k, top_p
+        _check(case)
+
+
+def test_masked_minus_inf_entries():
+    case = W.random_sample_case(6, 4, 3000, seed=11, top_p=0.9)
+    rng = np.random.default_rng(0)
+    ninf = W.bf16_bits(np.array([-np.inf], np.float32))[0]
+    mask_t = rng.random(case.target.shape) < 0.3
+    mask_d = rng.random(case.draft.shape) < 0.3
+    case.target[mask_t] = ninf
+    case.draft[mask_d] = ninf
+    _check(case)
+
+
+def test_unaligned_rows_match_aligned():
+    case = W.random_sample_case(4, 3, 4096, seed=5, top_p=0.9)
+    base = run_sample_gpu(case)
+    # the same rows starting 2 bytes past a 16-byte boundary
+    sv = lib()
+    t = to_dev(np.concatenate([np.zeros(1, np.uint16), case.target.ravel()]))[1:].view(case.target.shape)
+    d = to_dev(np.concatenate([np.zeros(1, np.uint16), case.draft.ravel()]))[1:].view(case.draft.shape)
+    assert t.data_ptr() % 16 == 2
+    out = sv.spec_verify_sample(t, d, to_dev(case.tokens), to_dev(case.uniforms), 1.0, 0, 0.9)
+    for a, b in zip(base, out):
+        assert np.array_equal(a, b.cpu().numpy())
+
+
+def test_topk1_matches_greedy():
+    case = W.random_sample_case(32, 5, 20000, seed=3, top_k=1)
+    tok, n, _, _ = run_sample_gpu(case)
+    g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
+    assert np.array_equal(tok, g_tok.cpu().numpy()) and np.array_equal(n, g_n.cpu().numpy())
+
+
+def test_repeat_calls_reuse_workspace_and_are_deterministic():
+    case = W.random_sample_case(16, 6, 32000, seed=9, top_p=0.9)
+    first = run_sample_gpu(case)
+    for _ in range(3):
+        again = run_sample_gpu(case)
+        for a, b in zip(first, again):
+            assert np.array_equal(a, b)
+
+
+def test_bad_tokens_and_rows_set_status():
+    sv = lib()
+    case = W.random_sample_case(4, 3, 1000, seed=2)
+    case.tokens[0, 0] = -1
+    case.tokens[1, 1] = 1000
+    ws = sv.Workspace()
+    sv.spec_get_status(ws)
+    out = sv.spec_verify_sample(to_dev(case.target), to_dev(case.draft), to_dev(case.tokens),
+                                to_dev(case.uniforms), workspace=ws)
+    st = sv.spec_get_status(ws)
+    assert st & sv.SPEC_STATUS_BAD_TOKEN
+    n = out[1].cpu().numpy()
+    assert n[0] == 0 and n[1] <= 1
+    orc = run_sample_oracle(case)
+    assert np.array_equal(out[1].cpu().numpy(), orc["n"])
+    assert np.array_equal(out[0].cpu().numpy(), orc["tokens"])
+    nan = W.bf16_bits(np.array([np.nan], np.float32))[0]
+    case.target[2, 0, 5] = nan
+    sv.spec_verify_sample(to_dev(case.target), to_dev(case.draft), to_dev(case.tokens),
+                          to_dev(case.uniforms), workspace=ws)
+    assert sv.spec_get_status(ws) & sv.SPEC_STATUS_BAD_ROW
+    assert sv.spec_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("dtype,top_k,top_p,V", [(W.BF16, 0, 1.0, 32000), (W.BF16, 50, 1.0, 32000),
+                                                  (W.BF16, 0, 0.9, 128256), (W.F32, 10, 0.8, 5000),
+                                                  (W.BF16, 30, 0.95, 152064), (W.F32, 0, 0.95, 1001)])
+def test_transform_probs_within_tolerance(dtype, top_k, top_p, V):
+    sv = lib()
+    rng = np.random.default_rng(V + top_k)
+    R = 6
+    x = rng.normal(0, 3, (R, V)).astype(np.float32)
+    rows = W.bf16_bits(x) if dtype == W.BF16 else x
+    T = 0.8
+    got = sv.spec_transform_probs(to_dev(rows), T, top_k, top_p).cpu().numpy()
+    for r in range(R):
+        want, margin, lo, hi, ok = oracle.row_probs(rows[r], T, top_k, top_p)
+        assert ok
+        diff = np.abs(got[r] - want)
+        assert diff.max() <= 1e-5 or margin < 1e-6, (r, diff.max(), margin)
+        assert abs(got[r].sum() - 1.0) < 1e-4
+
+
+def test_boundary_draws_under_budget():
+    """Runs last in this module: boundary draws over all sampling cases above."""
+    if _BOUNDARY["draws"] == 0:
+        pytest.skip("no sampling cases ran")
+    frac = _BOUNDARY["count"] / _BOUNDARY["draws"]
+    print(f"boundary draws: {_BOUNDARY['count']} of {_BOUNDARY['draws']}")
+    assert _BOUNDARY["count"] == 0 or frac < BOUNDARY_BUDGET
