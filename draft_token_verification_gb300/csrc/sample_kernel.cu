@@ -827,6 +827,9 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
   out[n] = __ldcg(&rec[n].drawn);
   for (int i = n + 1; i <= k; ++i) out[i] = -1;
   a.out_n[b] = n;
+  // leave the workspace zeroed for the next call, whatever its shape
+  UnitRec* wrec = a.recs + static_cast<size_t>(b) * (k + 1);
+  for (int i = 0; i <= k; ++i) wrec[i] = UnitRec{0, 0, 0.f, 0.f};
   a.tickets[b] = 0u;
 }
 

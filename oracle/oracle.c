@@ -43,8 +43,8 @@
 #define OFLAG_ACCEPT_BOUNDARY 1u  /* an accept test had |u - p/q| < 1e-6     */
 #define OFLAG_DRAW_BOUNDARY 2u    /* the draw had u*S within 1e-6*S of an edge */
 #define OFLAG_DEGENERATE 4u       /* residual mass was exactly zero           */
-#define OFLAG_CUT_BOUNDARY 8u     /* a token that decided the outcome sits at a
-                                     top-p cut whose margin is below 1e-6    */
+#define OFLAG_CUT_BOUNDARY 8u     /* a consulted row's top-p cut is within 1e-6
+                                     and the other decision changes the outcome */
 #define OFLAG_BAD_TOKEN 16u       /* a draft token outside [0, V)             */
 #define OFLAG_BAD_ROW 32u         /* a row with NaN/+inf or no finite entry   */
 
@@ -88,14 +88,18 @@ static int rank_cmp(const void* a, const void* b) {
  *          and keep t iff the mass ranked before t is < top_p (top_p >= 1: off)
  *   p_t  = exp(z_t - m) / sum over kept of exp(z - m)  on kept, else 0
  *
+ * `adjust` is 0 for the rule above.  For the boundary check only, -1 keeps one
+ * token fewer and +1 one token more than the top-p rule (the neighbouring
+ * decision at the cut).
  * probs[V] receives p.  *cut_margin receives the distance |before - top_p| of
  * the last kept and the first dropped token (the smaller one); +inf when no
  * top-p cut was made.  *cut_lo / *cut_hi receive those two token ids (-1 if
- * none).  Returns 0, or -1 for a row with NaN, +inf or no finite entry.
+ * none); *near_lo / *near_hi tell whether each is within BOUNDARY_EPS.
+ * Returns 0, or -1 for a row with NaN, +inf or no finite entry.
  */
-int oracle_row_probs(const void* row, int dtype, int V, double temperature,
-                     int top_k, double top_p, double* probs, double* cut_margin,
-                     int* cut_lo, int* cut_hi) {
+static int row_probs_adj(const void* row, int dtype, int V, double temperature, int top_k,
+                         double top_p, int adjust, double* probs, double* cut_margin,
+                         int* cut_lo, int* cut_hi, int* near_lo, int* near_hi) {
   ranked_t* r = (ranked_t*)malloc(sizeof(ranked_t) * (size_t)V);
   char* kept = (char*)calloc((size_t)V, 1);
   int t, n_topk, rc = 0;
@@ -103,6 +107,8 @@ int oracle_row_probs(const void* row, int dtype, int V, double temperature,
   if (cut_margin) *cut_margin = INFINITY;
   if (cut_lo) *cut_lo = -1;
   if (cut_hi) *cut_hi = -1;
+  if (near_lo) *near_lo = 0;
+  if (near_hi) *near_hi = 0;
   for (t = 0; t < V; ++t) {
     double l = read_logit(row, dtype, (size_t)t);
     if (isnan(l) || (isinf(l) && l > 0)) rc = -1;
@@ -124,11 +130,10 @@ int oracle_row_probs(const void* row, int dtype, int V, double temperature,
   zk = 0.0;
   for (t = 0; t < n_topk; ++t) zk += exp(r[t].z - m);
   if (top_p < 1.0) {
-    int last_kept = 0;
+    int last_kept = 0, n_keep;
     before = 0.0;
     for (t = 0; t < n_topk; ++t) {
       if (!(before < top_p)) break;
-      kept[r[t].idx] = 1;
       last_kept = t;
       before += exp(r[t].z - m) / zk;
     }
@@ -139,13 +144,19 @@ int oracle_row_probs(const void* row, int dtype, int V, double temperature,
       for (s = 0; s < last_kept; ++s) b_last += exp(r[s].z - m) / zk;
       margin = fabs(top_p - b_last);
       if (cut_lo) *cut_lo = r[last_kept].idx;
+      if (near_lo) *near_lo = last_kept > 0 && margin < BOUNDARY_EPS;
       if (last_kept + 1 < n_topk) {
         double b_next = b_last + exp(r[last_kept].z - m) / zk;
+        if (near_hi) *near_hi = fabs(b_next - top_p) < BOUNDARY_EPS;
         if (fabs(b_next - top_p) < margin) margin = fabs(b_next - top_p);
         if (cut_hi) *cut_hi = r[last_kept + 1].idx;
       }
       if (cut_margin) *cut_margin = margin;
     }
+    n_keep = last_kept + 1 + adjust;
+    if (n_keep < 1) n_keep = 1;
+    if (n_keep > n_topk) n_keep = n_topk;
+    for (t = 0; t < n_keep; ++t) kept[r[t].idx] = 1;
   } else {
     for (t = 0; t < n_topk; ++t) kept[r[t].idx] = 1;
   }
@@ -157,6 +168,13 @@ int oracle_row_probs(const void* row, int dtype, int V, double temperature,
   free(r);
   free(kept);
   return 0;
+}
+
+int oracle_row_probs(const void* row, int dtype, int V, double temperature,
+                     int top_k, double top_p, double* probs, double* cut_margin,
+                     int* cut_lo, int* cut_hi) {
+  return row_probs_adj(row, dtype, V, temperature, top_k, top_p, 0, probs, cut_margin, cut_lo,
+                       cut_hi, NULL, NULL);
 }
 
 /*
@@ -183,6 +201,120 @@ static int inverse_cdf(const double* w, int V, double u, double* margin) {
   return last_pos;
 }
 
+/* The rows of one sequence, turned into distributions on first use. */
+typedef struct {
+  const void* target; /* this sequence's [k+1][V] */
+  const void* draft;  /* this sequence's [k][V]   */
+  int dtype, k, V, top_k;
+  double T, top_p;
+  double* probs[2 * 32 + 1]; /* row id: target i -> i, draft i -> k+1+i */
+  int ok[2 * 32 + 1];
+  double margin[2 * 32 + 1];
+  int near_lo[2 * 32 + 1], near_hi[2 * 32 + 1];
+} seq_rows_t;
+
+static const double* seq_row(seq_rows_t* s, int id) {
+  if (!s->probs[id]) {
+    size_t es = (s->dtype == ORACLE_BF16) ? 2 : 4;
+    const char* base = id <= s->k ? (const char*)s->target + (size_t)id * s->V * es
+                                  : (const char*)s->draft + (size_t)(id - s->k - 1) * s->V * es;
+    s->probs[id] = (double*)malloc(sizeof(double) * (size_t)s->V);
+    s->ok[id] = row_probs_adj(base, s->dtype, s->V, s->T, s->top_k, s->top_p, 0, s->probs[id],
+                              &s->margin[id], NULL, NULL, &s->near_lo[id], &s->near_hi[id]) == 0;
+  }
+  return s->probs[id];
+}
+
+static double* alt_row(seq_rows_t* s, int id, int adjust) {
+  size_t es = (s->dtype == ORACLE_BF16) ? 2 : 4;
+  const char* base = id <= s->k ? (const char*)s->target + (size_t)id * s->V * es
+                                : (const char*)s->draft + (size_t)(id - s->k - 1) * s->V * es;
+  double* p = (double*)malloc(sizeof(double) * (size_t)s->V);
+  row_probs_adj(base, s->dtype, s->V, s->T, s->top_k, s->top_p, adjust, p, NULL, NULL, NULL, NULL,
+                NULL);
+  return p;
+}
+
+typedef struct {
+  int n, drawn;
+  int tokens[33];
+  uint32_t flags;      /* accept / draw / degenerate / bad-token / bad-row bits */
+  double min_margin;
+  int consulted[2 * 32 + 1];
+  int n_consulted;
+} outcome_t;
+
+/*
+ * The left-to-right scan of [EIN] "The core idea: draft, then check", step 3,
+ * for one sequence.  Row `alt_id` (if >= 0) is replaced by `alt_probs`.
+ */
+static void scan_sequence(seq_rows_t* s, const int32_t* x, const float* u, int alt_id,
+                          const double* alt_probs, double* w, outcome_t* o) {
+  const int k = s->k, V = s->V;
+  int i, t;
+  o->flags = 0;
+  o->min_margin = INFINITY;
+  o->n_consulted = 0;
+  o->drawn = -1;
+#define ROW(id) ((id) == alt_id ? alt_probs : seq_row(s, (id)))
+  for (i = 0; i < k; ++i) {
+    const double* p = ROW(i);
+    const double* q = ROW(k + 1 + i);
+    const int ok = s->ok[i] && s->ok[k + 1 + i];
+    const int in_range = x[i] >= 0 && x[i] < V;
+    const double px = in_range ? p[x[i]] : 0.0, qx = in_range ? q[x[i]] : 0.0;
+    o->consulted[o->n_consulted++] = i;
+    o->consulted[o->n_consulted++] = k + 1 + i;
+    if (!in_range) o->flags |= OFLAG_BAD_TOKEN;
+    if (!ok) o->flags |= OFLAG_BAD_ROW;
+    if (qx > 0.0 && px < qx) {
+      double mg = fabs((double)u[i] - px / qx);
+      if (mg < o->min_margin) o->min_margin = mg;
+      if (mg < BOUNDARY_EPS) o->flags |= OFLAG_ACCEPT_BOUNDARY;
+    }
+    if (in_range && ok && (double)u[i] * qx < px) {
+      o->tokens[i] = x[i];
+      continue;
+    }
+    /* first rejection: resample from max(0, p - q) */
+    o->n = i;
+    if (ok) {
+      double sum = 0.0, mg = 0.0;
+      for (t = 0; t < V; ++t) {
+        double d = p[t] - q[t];
+        w[t] = d > 0.0 ? d : 0.0;
+        sum += w[t];
+      }
+      if (!(sum > 0.0)) {
+        o->flags |= OFLAG_DEGENERATE;
+        o->drawn = inverse_cdf(p, V, (double)u[k + 1], &mg);
+      } else {
+        o->drawn = inverse_cdf(w, V, (double)u[k + 1], &mg);
+      }
+      if (mg < BOUNDARY_EPS) o->flags |= OFLAG_DRAW_BOUNDARY;
+      if (mg < o->min_margin) o->min_margin = mg;
+    }
+    o->tokens[i] = o->drawn;
+    return;
+  }
+  /* every draft accepted: bonus token from the last target row */
+  {
+    const double* p = ROW(k);
+    double mg = 0.0;
+    o->consulted[o->n_consulted++] = k;
+    o->n = k;
+    if (!s->ok[k]) {
+      o->flags |= OFLAG_BAD_ROW;
+    } else {
+      o->drawn = inverse_cdf(p, V, (double)u[k], &mg);
+      if (mg < BOUNDARY_EPS) o->flags |= OFLAG_DRAW_BOUNDARY;
+      if (mg < o->min_margin) o->min_margin = mg;
+    }
+    o->tokens[k] = o->drawn;
+  }
+#undef ROW
+}
+
 /*
  * Speculative sampling verification ([EIN] "The core idea: draft, then
  * check", step 3 "Accept or correct"):
@@ -197,12 +329,18 @@ static int inverse_cdf(const double* w, int V, double u, double* margin) {
  *
  * Layouts: target [B][k+1][V], draft [B][k][V], tokens [B][k],
  * uniforms [B][k+2] (u_0..u_{k-1} accept tests, u_k bonus, u_{k+1} resample),
- * temperature_per_seq [B] or NULL.
+ * temperature_per_seq [B] or NULL; k <= 32.
  * Outputs: out_tokens [B][k+1] (-1 padded), out_n [B], out_p / out_q [B][k]
  * (p_i(x_i), q_i(x_i); NaN where not computed), out_flags [B] (OFLAG_*),
- * out_margin [B] (smallest decision margin met; may be NULL).
+ * out_margin [B] (smallest accept / draw margin met; may be NULL).
  * all_rows != 0 computes p_i(x_i), q_i(x_i) for every i, not only the rows
  * the scan consults.
+ *
+ * Boundary flags: a decision is "within 1e-6 of its edge" when an accept test
+ * has |u - p/q| < 1e-6, when the draw has u*S within 1e-6*S of an edge of the
+ * chosen token's interval, or when a consulted row's top-p cut has a margin
+ * below 1e-6 AND taking the neighbouring cut decision for that row changes
+ * the committed tokens.
  */
 int oracle_verify_sample(const void* target, const void* draft, int dtype,
                          const int32_t* tokens, const float* uniforms, int B, int k,
@@ -211,108 +349,61 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
                          int32_t* out_n, double* out_p, double* out_q,
                          uint32_t* out_flags, double* out_margin) {
   size_t es = (dtype == ORACLE_BF16) ? 2 : 4;
-  double* p = (double*)malloc(sizeof(double) * (size_t)V);
-  double* q = (double*)malloc(sizeof(double) * (size_t)V);
   double* w = (double*)malloc(sizeof(double) * (size_t)V);
-  int b, i, t;
+  int b, i, j;
+  if (k < 1 || k > 32) {
+    free(w);
+    return -1;
+  }
   for (b = 0; b < B; ++b) {
-    double T = temperature_per_seq ? (double)temperature_per_seq[b] : temperature;
+    seq_rows_t s;
+    outcome_t o, alt;
+    const int32_t* x = tokens + (size_t)b * k;
     const float* u = uniforms + (size_t)b * (size_t)(k + 2);
-    uint32_t flags = 0;
-    double min_margin = INFINITY;
-    int n = k, drawn = -1;
-    int decided = 0;
-    for (i = 0; i <= k; ++i) out_tokens[(size_t)b * (k + 1) + i] = -1;
-    for (i = 0; i < k; ++i) {
-      out_p[(size_t)b * k + i] = NAN;
-      out_q[(size_t)b * k + i] = NAN;
-    }
-    for (i = 0; i < k; ++i) {
-      const char* trow = (const char*)target + ((size_t)b * (k + 1) + i) * (size_t)V * es;
-      const char* drow = (const char*)draft + ((size_t)b * k + i) * (size_t)V * es;
-      double mp, mq, px, qx;
-      int x = tokens[(size_t)b * k + i];
-      int lo_p, hi_p, lo_q, hi_q, okp, okq;
-      if (decided && !all_rows) break;
-      okp = oracle_row_probs(trow, dtype, V, T, top_k, top_p, p, &mp, &lo_p, &hi_p);
-      okq = oracle_row_probs(drow, dtype, V, T, top_k, top_p, q, &mq, &lo_q, &hi_q);
-      if (x < 0 || x >= V) {
-        if (!decided) flags |= OFLAG_BAD_TOKEN;
-        px = 0.0;
-        qx = 0.0;
-      } else {
-        px = p[x];
-        qx = q[x];
+    memset(&s, 0, sizeof s);
+    s.target = (const char*)target + (size_t)b * (k + 1) * (size_t)V * es;
+    s.draft = (const char*)draft + (size_t)b * k * (size_t)V * es;
+    s.dtype = dtype;
+    s.k = k;
+    s.V = V;
+    s.top_k = top_k;
+    s.T = temperature_per_seq ? (double)temperature_per_seq[b] : temperature;
+    s.top_p = top_p;
+    scan_sequence(&s, x, u, -1, NULL, w, &o);
+    /* top-p cuts within 1e-6 of top_p: does the neighbouring decision matter? */
+    for (j = 0; j < o.n_consulted; ++j) {
+      int id = o.consulted[j], adj;
+      for (adj = -1; adj <= 1; adj += 2) {
+        double* ap;
+        int differs;
+        if (!(adj < 0 ? s.near_lo[id] : s.near_hi[id])) continue;
+        ap = alt_row(&s, id, adj);
+        scan_sequence(&s, x, u, id, ap, w, &alt);
+        differs = alt.n != o.n;
+        for (i = 0; i <= o.n && !differs; ++i) differs = alt.tokens[i] != o.tokens[i];
+        if (differs) o.flags |= OFLAG_CUT_BOUNDARY;
+        free(ap);
       }
-      if (okp != 0 || okq != 0) {
-        if (!decided) flags |= OFLAG_BAD_ROW;
+    }
+    for (i = 0; i <= k; ++i) out_tokens[(size_t)b * (k + 1) + i] = i <= o.n ? o.tokens[i] : -1;
+    out_n[b] = o.n;
+    out_flags[b] = o.flags;
+    if (out_margin) out_margin[b] = o.min_margin;
+    for (i = 0; i < k; ++i) {
+      int have = s.probs[i] && s.probs[k + 1 + i];
+      double px = NAN, qx = NAN;
+      if (all_rows || have) {
+        const double* p = seq_row(&s, i);
+        const double* q = seq_row(&s, k + 1 + i);
+        int in_range = x[i] >= 0 && x[i] < V;
+        px = in_range ? p[x[i]] : 0.0;
+        qx = in_range ? q[x[i]] : 0.0;
       }
       out_p[(size_t)b * k + i] = px;
       out_q[(size_t)b * k + i] = qx;
-      if (decided) continue;
-      {
-        int accept = (x >= 0 && x < V && okp == 0 && okq == 0) &&
-                     ((double)u[i] * qx < px);
-        if (qx > 0.0 && px < qx) {
-          double mg = fabs((double)u[i] - px / qx);
-          if (mg < min_margin) min_margin = mg;
-          if (mg < BOUNDARY_EPS) flags |= OFLAG_ACCEPT_BOUNDARY;
-        }
-        if ((x == lo_p || x == hi_p) && mp < BOUNDARY_EPS) flags |= OFLAG_CUT_BOUNDARY;
-        if ((x == lo_q || x == hi_q) && mq < BOUNDARY_EPS) flags |= OFLAG_CUT_BOUNDARY;
-        if (mp < min_margin && (x == lo_p || x == hi_p)) min_margin = mp;
-        if (mq < min_margin && (x == lo_q || x == hi_q)) min_margin = mq;
-        if (accept) {
-          out_tokens[(size_t)b * (k + 1) + i] = x;
-          continue;
-        }
-        /* first rejection: resample from max(0, p - q) */
-        n = i;
-        decided = 1;
-        if (okp == 0 && okq == 0) {
-          double s = 0.0, mg = 0.0;
-          for (t = 0; t < V; ++t) {
-            double d = p[t] - q[t];
-            w[t] = d > 0.0 ? d : 0.0;
-            s += w[t];
-          }
-          if (!(s > 0.0)) {
-            flags |= OFLAG_DEGENERATE;
-            drawn = inverse_cdf(p, V, (double)u[k + 1], &mg);
-          } else {
-            drawn = inverse_cdf(w, V, (double)u[k + 1], &mg);
-          }
-          if (mg < BOUNDARY_EPS) flags |= OFLAG_DRAW_BOUNDARY;
-          if (mg < min_margin) min_margin = mg;
-          if ((drawn == lo_p || drawn == hi_p) && mp < BOUNDARY_EPS) flags |= OFLAG_CUT_BOUNDARY;
-          if ((drawn == lo_q || drawn == hi_q) && mq < BOUNDARY_EPS) flags |= OFLAG_CUT_BOUNDARY;
-        }
-        out_tokens[(size_t)b * (k + 1) + i] = drawn;
-      }
     }
-    if (!decided) {
-      /* every draft accepted: bonus token from the last target row */
-      const char* trow = (const char*)target + ((size_t)b * (k + 1) + k) * (size_t)V * es;
-      double mp, mg = 0.0;
-      int lo_p, hi_p;
-      if (oracle_row_probs(trow, dtype, V, T, top_k, top_p, p, &mp, &lo_p, &hi_p) != 0) {
-        flags |= OFLAG_BAD_ROW;
-        drawn = -1;
-      } else {
-        drawn = inverse_cdf(p, V, (double)u[k], &mg);
-        if (mg < BOUNDARY_EPS) flags |= OFLAG_DRAW_BOUNDARY;
-        if (mg < min_margin) min_margin = mg;
-        if ((drawn == lo_p || drawn == hi_p) && mp < BOUNDARY_EPS) flags |= OFLAG_CUT_BOUNDARY;
-      }
-      n = k;
-      out_tokens[(size_t)b * (k + 1) + k] = drawn;
-    }
-    out_n[b] = n;
-    out_flags[b] = flags;
-    if (out_margin) out_margin[b] = min_margin;
+    for (i = 0; i < 2 * 32 + 1; ++i) free(s.probs[i]);
   }
-  free(p);
-  free(q);
   free(w);
   return 0;
 }

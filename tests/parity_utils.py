@@ -43,9 +43,11 @@ def run_sample_oracle(case: W.SampleCase, seqs=None):
                                 case.temperature, case.top_k, case.top_p, tps, all_rows=True)
 
 
-def _cut_boundary_at(row, T, top_k, top_p, x) -> bool:
-    _, margin, lo, hi, _ = oracle.row_probs(row, T, top_k, top_p)
-    return margin < 1e-6 and x in (lo, hi)
+def _cut_boundary_row(row, T, top_k, top_p) -> bool:
+    """The row's top-p cut is within 1e-6 of top_p: a neighbouring cut changes
+    the normalisation of every kept token."""
+    _, margin, _, _, _ = oracle.row_probs(row, T, top_k, top_p)
+    return margin < 1e-6
 
 
 def compare_sample(case: W.SampleCase, gpu, orc, seqs=None):
@@ -73,8 +75,7 @@ def compare_sample(case: W.SampleCase, gpu, orc, seqs=None):
         for j, i in zip(*np.nonzero(~(diff <= ABS_TOL_PROB))):
             b = idx[j]
             row = case.target[b, i] if name == "p" else case.draft[b, i]
-            x = int(case.tokens[b, i])
-            assert _cut_boundary_at(row, float(temps[b]), case.top_k, case.top_p, x), (
+            assert _cut_boundary_row(row, float(temps[b]), case.top_k, case.top_p), (
                 f"{name}(x) differs at seq {b} pos {i}: gpu {g[j, i]} oracle {o[j, i]}")
     draws = len(idx) * (case.k + 1)
     return int(boundary.sum()), draws

@@ -175,7 +175,8 @@ def test_transform_probs_within_tolerance(dtype, top_k, top_p, V):
     R = 6
     x = rng.normal(0, 3, (R, V)).astype(np.float32)
     rows = W.bf16_bits(x) if dtype == W.BF16 else x
-    T = 0.8
+    T = W.f32(0.8)
+    top_p = W.f32(top_p)
     got = sv.spec_transform_probs(to_dev(rows), T, top_k, top_p).cpu().numpy()
     for r in range(R):
         want, margin, lo, hi, ok = oracle.row_probs(rows[r], T, top_k, top_p)

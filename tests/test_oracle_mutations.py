@@ -13,14 +13,12 @@ from concurrent.futures import ThreadPoolExecutor
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTATIONS = [
-    ("accept test with p and q swapped", "((double)u[i] * qx < px)", "((double)u[i] * px < qx)"),
+    ("accept test with p and q swapped", "(double)u[i] * qx < px) {", "(double)u[i] * px < qx) {"),
     ("residual q - p instead of p - q", "double d = p[t] - q[t];", "double d = q[t] - p[t];"),
     ("residual without the clamp at zero", "w[t] = d > 0.0 ? d : 0.0;", "w[t] = d;"),
-    ("bonus draw uses the resample uniform", "drawn = inverse_cdf(p, V, (double)u[k], &mg);",
-     "drawn = inverse_cdf(p, V, (double)u[k + 1], &mg);"),
-    ("bonus drawn from the last draft position's row",
-     "const char* trow = (const char*)target + ((size_t)b * (k + 1) + k) * (size_t)V * es;\n      double mp, mg",
-     "const char* trow = (const char*)target + ((size_t)b * (k + 1) + k - 1) * (size_t)V * es;\n      double mp, mg"),
+    ("bonus draw uses the resample uniform", "o->drawn = inverse_cdf(p, V, (double)u[k], &mg);",
+     "o->drawn = inverse_cdf(p, V, (double)u[k + 1], &mg);"),
+    ("bonus drawn from the last draft position's row", "const double* p = ROW(k);", "const double* p = ROW(k - 1);"),
     ("temperature multiplies instead of divides", "r[t].z = l / temperature;", "r[t].z = l * temperature;"),
     ("top-p counts the token's own mass", "if (!(before < top_p)) break;",
      "if (!(before + exp(r[t].z - m) / zk < top_p) && t > 0) break;"),

@@ -60,6 +60,11 @@ def as_f32(arr: np.ndarray) -> np.ndarray:
     return bits_to_f32(arr) if arr.dtype == np.uint16 else np.asarray(arr, dtype=np.float32)
 
 
+def f32(x: float) -> float:
+    """The float32 value nearest to x, as a Python float."""
+    return float(np.float32(x))
+
+
 def _rng(ss: np.random.SeedSequence) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(ss))
 
@@ -155,10 +160,11 @@ def _finish_sample(name, dtype, L, D, T, top_k, top_p, ss, tps=None, mask_fn=Non
     target = _cast(L, dtype)
     draft = _cast(D, dtype)
     B = target.shape[0]
-    temps = tps if tps is not None else np.full(B, T, np.float32)
+    temps = tps if tps is not None else np.full(B, f32(T), np.float32)
     tokens = gumbel_drafts(draft, temps, _rng(s_tok), mask_fn)
     uniforms = _uniforms(_rng(s_u), B, target.shape[1] - 1)
-    return SampleCase(name, dtype, target, draft, tokens, uniforms, float(T), int(top_k), float(top_p),
+    # the C ABI takes temperature and top_p as float32: both sides get those values
+    return SampleCase(name, dtype, target, draft, tokens, uniforms, f32(T), int(top_k), f32(top_p),
                       tps, seed, meta or {})
 
 
