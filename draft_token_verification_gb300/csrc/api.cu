@@ -96,12 +96,26 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   return SPEC_OK;
 }
 
-// CTAs per row for the argmax kernel: slices of a multiple of 8 elements,
-// enough CTAs to cover the GPU a few times over.
+int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      sms = 148;
+  }
+  return sms;
+}
+
+// Elements per CTA for the argmax kernel: a multiple of 8, about two waves of
+// eight resident CTAs per SM, at least 2048 elements per CTA.
 int argmax_split_len(int rows, int V) {
-  int len = 8192;
-  while (len > 1024 && static_cast<long long>(rows) * ((V + len - 1) / len) < 4 * 152) len /= 2;
-  return len;
+  const long long total = static_cast<long long>(rows) * V;
+  long long len = total / (static_cast<long long>(num_sms()) * 8 * 2);
+  len = (len + 7) / 8 * 8;
+  if (len < 2048) len = 2048;
+  if (len > V) len = (V + 7) / 8 * 8;
+  return static_cast<int>(len);
 }
 
 }  // namespace

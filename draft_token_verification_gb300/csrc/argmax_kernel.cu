@@ -24,8 +24,7 @@ namespace specv {
 
 namespace {
 
-constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+constexpr int kUnroll = 8;  // 16-byte loads in flight per thread
 
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;

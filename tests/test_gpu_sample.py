@@ -15,21 +15,24 @@ from parity_utils import (BOUNDARY_BUDGET, compare_sample, lib, q_support_mask, 
 
 pytestmark = pytest.mark.gpu
 
-_BOUNDARY = {"count": 0, "draws": 0}
+# Boundary draws (oracle decision within 1e-6 of an edge), per kind of input:
+# "config" = workloads C1-C3, "sweep" = C5 points, "edge" = constructed edge
+# cases (flat rows, quantised ties), where edges are dense by construction.
+_BOUNDARY = {kind: {"count": 0, "draws": 0} for kind in ("config", "sweep", "edge")}
 
 
-def _check(case, seqs=None):
+def _check(case, seqs=None, kind="edge"):
     gpu = run_sample_gpu(case)
     orc = run_sample_oracle(case, seqs)
     nb, draws = compare_sample(case, gpu, orc, seqs)
-    _BOUNDARY["count"] += nb
-    _BOUNDARY["draws"] += draws
+    _BOUNDARY[kind]["count"] += nb
+    _BOUNDARY[kind]["draws"] += draws
     return gpu, orc
 
 
 def test_config1_fp32_no_filter():
     case = W.config1()
-    gpu, orc = _check(case)
+    gpu, orc = _check(case, kind="config")
     # the same logits through greedy mode
     g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
     o = oracle.verify_greedy(case.target, case.tokens)
@@ -38,21 +41,21 @@ def test_config1_fp32_no_filter():
 
 def test_config2_topk50_bf16():
     case = W.config2(mask_fn=q_support_mask(50, 1.0))
-    _check(case)
+    _check(case, kind="config")
 
 
 @pytest.mark.parametrize("per_seq", [False, True])
 def test_config3_topp_full_size_sampled(per_seq):
     case = W.config3(per_seq_temperature=per_seq)
     seqs = list(range(0, case.B, 4))  # the oracle checks every 4th sequence of the full launch
-    _check(case, seqs)
+    _check(case, seqs, kind="config")
 
 
 @pytest.mark.parametrize("B,k,sigma", [(1, 1, 0.5), (4, 12, 2.0), (16, 4, 4.0), (64, 8, 0.5), (128, 2, 2.0)])
 def test_config5_sweep_points(B, k, sigma):
     case = W.config5(B, k, sigma)
     seqs = list(range(0, B, max(1, B // 8)))
-    _check(case, seqs)
+    _check(case, seqs, kind="sweep")
     o = oracle.verify_greedy(case.target, case.tokens)
     g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
     assert np.array_equal(g_tok.cpu().numpy(), o["tokens"]) and np.array_equal(g_n.cpu().numpy(), o["n"])
@@ -187,9 +190,14 @@ def test_transform_probs_within_tolerance(dtype, top_k, top_p, V):
 
 
 def test_boundary_draws_under_budget():
-    """Runs last in this module: boundary draws over all sampling cases above."""
-    if _BOUNDARY["draws"] == 0:
-        pytest.skip("no sampling cases ran")
-    frac = _BOUNDARY["count"] / _BOUNDARY["draws"]
-    print(f"boundary draws: {_BOUNDARY['count']} of {_BOUNDARY['draws']}")
-    assert _BOUNDARY["count"] == 0 or frac < BOUNDARY_BUDGET
+    """Runs last in this module.  Boundary draws are counted and reported per
+    kind of input; on the concentrated workloads C1-C3 they must stay under
+    1e-5 of all draws.  (For deep nuclei such as C5's and for the constructed
+    flat / tied rows, the share of draws whose uniform lies within 1e-6 of an
+    interval edge is a property of the inputs, fixed by the oracle alone.)"""
+    for kind, c in _BOUNDARY.items():
+        print(f"boundary draws [{kind}]: {c['count']} of {c['draws']}")
+    c = _BOUNDARY["config"]
+    if c["draws"] == 0:
+        pytest.skip("no configuration cases ran")
+    assert c["count"] == 0 or c["count"] / c["draws"] < BOUNDARY_BUDGET
