@@ -34,7 +34,7 @@ int check_workspace(void* ws, size_t bytes, int B, int k) {
 // Cluster size and per-CTA slice for a sampling row of V elements.
 bool sample_shape(int V, spec_dtype d, bool filter, int* cluster, int* chunk) {
   int cs = 1;
-  while (cs < 16 && (V + cs - 1) / cs > kChunkTarget) cs *= 2;
+  while (cs < 8 && (V + cs - 1) / cs > kChunkTarget) cs *= 2;
   int ch = ((V + cs - 1) / cs + 7) / 8 * 8;
   const size_t smem = sample_smem_bytes(d == SPEC_BF16 ? DT_BF16 : DT_F32, ch, filter);
   if (smem > 200 * 1024) return false;

@@ -14,7 +14,8 @@ constexpr int DT_BF16 = 1;
 
 constexpr int kThreads = 256;           // threads per CTA in every kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kWindow = 1024;           // exact-value histogram bins per row
+constexpr int kWindow = 512;            // exact-value histogram bins per row
+constexpr int kBinThreads = kWindow / 4; // threads that own four bins each
 constexpr int kMaxK = 31;
 constexpr int kMaxTreeNodes = 1024;
 

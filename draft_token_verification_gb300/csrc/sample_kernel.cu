@@ -36,6 +36,8 @@
 
 namespace specv {
 
+__device__ void sample_finalize(const SampleArgs& a, int b);
+
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
@@ -79,6 +81,48 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Double-float: an unevaluated sum hi + lo of two floats (about 48 bits),
+// kept with fp32 instructions only (the fp64 pipe of this GPU is narrow).
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_from(double d) {
+  const float h = static_cast<float>(d);
+  return DF{h, static_cast<float>(d - static_cast<double>(h))};
+}
+// a + b by the error-free two-sum of the high parts
+__device__ __forceinline__ DF df_add(DF a, float b) {
+  const float s = a.hi + b;
+  const float bb = s - a.hi;
+  const float e = ((a.hi - (s - bb)) + (b - bb)) + a.lo;
+  const float h = s + e;
+  return DF{h, e - (h - s)};
+}
+__device__ __forceinline__ DF df_add2(DF a, DF b) { return df_add(df_add(a, b.hi), b.lo); }
+__device__ __forceinline__ DF df_shfl_up(DF a, int o) {
+  return DF{__shfl_up_sync(kFull, a.hi, o), __shfl_up_sync(kFull, a.lo, o)};
+}
+__device__ __forceinline__ DF df_shfl(DF a, int l) { return DF{__shfl_sync(kFull, a.hi, l), __shfl_sync(kFull, a.lo, l)}; }
+// inclusive warp prefix sum of double-floats
+__device__ __forceinline__ DF warp_incl_scan_df(DF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF w = df_shfl_up(v, o);
+    if (lane >= o) v = df_add2(v, w);
+  }
+  return v;
+}
+// (a - b) rounded to float
+__device__ __forceinline__ float df_diff(DF a, DF b) { return (a.hi - b.hi) + (a.lo - b.lo); }
+__device__ __forceinline__ double df_value(DF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
 
 __device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
@@ -129,6 +173,19 @@ struct Hot<DT_BF16> {
     return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
            ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
   }
+  // bit j set iff element j equals the threshold value (-0 == +0)
+  __device__ static __forceinline__ uint32_t mask_eq(const uint4& v, uint32_t thr) {
+    const __nv_bfloat162 t = b2(thr);
+    const uint32_t m0 = __heq2_mask(b2(v.x), t), m1 = __heq2_mask(b2(v.y), t);
+    const uint32_t m2 = __heq2_mask(b2(v.z), t), m3 = __heq2_mask(b2(v.w), t);
+    return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
+           ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
+  }
+  __device__ static __forceinline__ bool any_eq(const uint4& v, uint32_t thr) {
+    const __nv_bfloat162 t = b2(thr);
+    return (__heq2_mask(b2(v.x), t) | __heq2_mask(b2(v.y), t) | __heq2_mask(b2(v.z), t) |
+            __heq2_mask(b2(v.w), t)) != 0u;
+  }
 };
 
 template <>
@@ -158,6 +215,12 @@ struct Hot<DT_F32> {
     return (__uint_as_float(v.x) >= t ? 1u : 0u) | (__uint_as_float(v.y) >= t ? 2u : 0u) |
            (__uint_as_float(v.z) >= t ? 4u : 0u) | (__uint_as_float(v.w) >= t ? 8u : 0u);
   }
+  __device__ static __forceinline__ uint32_t mask_eq(const uint4& v, uint32_t thr) {
+    const float t = __uint_as_float(thr);
+    return (__uint_as_float(v.x) == t ? 1u : 0u) | (__uint_as_float(v.y) == t ? 2u : 0u) |
+           (__uint_as_float(v.z) == t ? 4u : 0u) | (__uint_as_float(v.w) == t ? 8u : 0u);
+  }
+  __device__ static __forceinline__ bool any_eq(const uint4& v, uint32_t thr) { return mask_eq(v, thr) != 0u; }
 };
 
 // ------------------------------------------------------------ row state
@@ -165,11 +228,11 @@ struct Hot<DT_F32> {
 struct RowStat {
   float m;               // row maximum
   uint32_t kmax;         // key of m
-  uint32_t kstar;        // kept iff key > kstar, or key == kstar and tie rank < cstar
-  uint32_t cstar;
-  uint32_t tie_total;    // tokens with key == kstar in the row
-  uint32_t ties_before;  // such tokens in lower cluster ranks (partial rows only)
-  uint32_t thr;          // packed threshold value of kstar (for the quick skip)
+  uint32_t kstar;        // kept iff key > kstar, or key == kstar and (not partial or index < tie_cut)
+  uint32_t cstar;        // kept tokens of value kstar: the lowest-index ones
+  uint32_t tie_total;    // tokens of value kstar in the row
+  int tie_cut;           // partial rows: index of the first kstar-valued token that is not kept
+  uint32_t thr;          // packed value of kstar (quick skips, equality tests)
   double zkept;          // sum of masses over the kept set
   float inv_z;
   int all_kept;
@@ -188,14 +251,28 @@ struct Shm {
   uint32_t x_pk[2];
   // CTA scratch
   float w_max[kWarps][2];
-  double w_sum[kWarps][2];
-  double w_res[kWarps];
+  float w_sum[kWarps][2];
+  float w_res[kWarps];
+  uint32_t w_u[kWarps];
+  float w_f[kWarps];
   uint32_t w_tie[kWarps][2];
   double w_pm[kWarps];
   uint32_t w_pc[kWarps];
   uint32_t w_pk[kWarps];
+  double b_zfull[2];
+  double b_S, b_Pc;
+  int b_owner;
+  uint32_t b_dlb[2];
+  int c_found;
+  uint32_t c_d, c_c, c_t;
+  double c_z;
+  uint32_t tie_before[2], tie_local[2];
+  uint32_t pc[2][kBinThreads];  // per-thread count of its four histogram bins
+  float pm[2][kBinThreads];     // per-thread mass of its four histogram bins
+  int tie_cut[2];
+  int tie_warp[2];
+  uint32_t tie_j[2];
   uint32_t fb_need[2];
-  uint32_t owner_tie[2];
   int draw_warp;
   double draw_base;
   RowStat rs[2];
@@ -216,22 +293,33 @@ __device__ __forceinline__ double cluster_sum_f64(double mine_lane_c) {
   return z;
 }
 
-// Kept test for one element of a row.  `rank` is the element's rank among the
-// tokens with key == kstar (consulted for partial rows only).
-__device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, uint32_t rank) {
+// One element of a shared-memory row buffer.
+template <int DT>
+__device__ __forceinline__ uint32_t lds_elem(uint32_t base, int t) {
+  return DT == DT_BF16 ? lds_u16(base + 2u * static_cast<uint32_t>(t)) : lds_u32(base + 4u * static_cast<uint32_t>(t));
+}
+
+// Kept test for the element of index t (whole-row index) with the given key.
+__device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, int t) {
   if (rs.all_kept) return true;
   if (key > rs.kstar) return true;
-  return key == rs.kstar && (!rs.partial || rank < rs.cstar);
+  return key == rs.kstar && (!rs.partial || t < rs.tie_cut);
+}
+
+// Bit j set for the elements of vector v (CTA-local) that lie inside the slice.
+template <int DT>
+__device__ __forceinline__ uint32_t valid_mask(int v, int n) {
+  const int left = n - v * Elt<DT>::kPerVec;
+  return left >= Elt<DT>::kPerVec ? (1u << Elt<DT>::kPerVec) - 1u : (left > 0 ? (1u << left) - 1u : 0u);
 }
 
 // Draw weights of the elements of one 16-byte vector: w = max(0, p - q)
-// (residual) or w = p (bonus).  tie_p / tie_q: rank of the vector's first
-// kstar-valued element (partial rows only).  Vectors without an element at or
-// above the target's cut value are skipped with one packed compare.
+// (residual) or w = p (bonus).  t0 is the vector's first CTA-local element,
+// lo the slice start.  Vectors with no element at or above the target's cut
+// value are skipped with one packed compare.
 template <int DT>
-__device__ __forceinline__ float vec_weights(const uint4& xp, const uint4& xq, int t0, int n, bool use_q,
-                                             const RowStat& rp, const RowStat& rq, float cexp, uint32_t tie_p,
-                                             uint32_t tie_q, float* w) {
+__device__ __forceinline__ float vec_weights(const uint4& xp, const uint4& xq, int t0, int lo, int n, bool use_q,
+                                             const RowStat& rp, const RowStat& rq, float cexp, float* w) {
   using E = Elt<DT>;
   float s = 0.f;
 #pragma unroll
@@ -240,17 +328,14 @@ __device__ __forceinline__ float vec_weights(const uint4& xp, const uint4& xq, i
 #pragma unroll
   for (int j = 0; j < E::kPerVec; ++j) {
     if (t0 + j < n) {
+      const int t = lo + t0 + j;
       const uint32_t bp = E::bits_of(xp, j);
-      const uint32_t kp = E::key(bp);
       float pv = 0.f;
-      if (kept_key(rp, kp, tie_p)) pv = softmax_mass(E::value(bp), rp.m, cexp) * rp.inv_z;
-      if (rp.partial && kp == rp.kstar) ++tie_p;
+      if (kept_key(rp, E::key(bp), t)) pv = softmax_mass(E::value(bp), rp.m, cexp) * rp.inv_z;
       if (use_q) {
         const uint32_t bq = E::bits_of(xq, j);
-        const uint32_t kq = E::key(bq);
         float qv = 0.f;
-        if (kept_key(rq, kq, tie_q)) qv = softmax_mass(E::value(bq), rq.m, cexp) * rq.inv_z;
-        if (rq.partial && kq == rq.kstar) ++tie_q;
+        if (kept_key(rq, E::key(bq), t)) qv = softmax_mass(E::value(bq), rq.m, cexp) * rq.inv_z;
         w[j] = fmaxf(pv - qv, 0.f);
       } else {
         w[j] = pv;
@@ -261,15 +346,281 @@ __device__ __forceinline__ float vec_weights(const uint4& xp, const uint4& xq, i
   return s;
 }
 
-// Number of kstar-valued elements of a row in one vector.
-template <int DT>
-__device__ __forceinline__ uint32_t vec_ties(const uint4& x, int t0, int n, uint32_t kstar) {
-  using E = Elt<DT>;
-  uint32_t c = 0;
+// ------------------------------------------------------ CTA-wide scans
+
+// Exclusive prefix (thread order) of a u32 over the CTA; `total` gets the sum.
+__device__ __forceinline__ uint32_t block_excl_u32(uint32_t v, uint32_t* wtmp, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan_u32(v);
+  if (lane == 31) wtmp[warp] = incl;
+  __syncthreads();
+  uint32_t off = 0, tot = 0;
 #pragma unroll
-  for (int j = 0; j < E::kPerVec; ++j)
-    if (t0 + j < n && E::key(E::bits_of(x, j)) == kstar) ++c;
-  return c;
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t x = wtmp[w];
+    if (w < warp) off += x;
+    tot += x;
+  }
+  __syncthreads();
+  total = tot;
+  return off + incl - v;
+}
+
+// Exclusive prefix (thread order) of a float over the CTA, as a double-float.
+__device__ __forceinline__ DF block_excl_f32(float v, float* wtmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float incl = warp_incl_scan(v);
+  if (lane == 31) wtmp[warp] = incl;
+  __syncthreads();
+  DF off{0.f, 0.f};
+  for (int w = 0; w < warp; ++w) off = df_add(off, wtmp[w]);
+  __syncthreads();
+  return df_add(off, incl - v);
+}
+
+// Smallest thread index whose flag is set, or -1.
+__device__ __forceinline__ int block_first(bool f, uint32_t* wtmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned ball = __ballot_sync(kFull, f);
+  if (lane == 0) wtmp[warp] = ball ? static_cast<uint32_t>(warp * 32 + __ffs(ball) - 1) : 0xFFFFFFFFu;
+  __syncthreads();
+  uint32_t first = 0xFFFFFFFFu;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) first = min(first, wtmp[w]);
+  __syncthreads();
+  return first == 0xFFFFFFFFu ? -1 : static_cast<int>(first);
+}
+
+// Sum over the cluster of bins 4t .. 4t+3 of one row's histogram (hrow: the
+// shared-window address of this CTA's copy).
+template <int CS>
+__device__ __forceinline__ uint4 cluster_bins4(uint32_t hrow, int t) {
+  uint4 part[CS];
+#pragma unroll
+  for (int c = 0; c < CS; ++c) part[c] = ld_cluster_v4(mapa_shared(hrow + 16u * static_cast<uint32_t>(t), c));
+  uint4 s = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int c = 0; c < CS; ++c) {
+    s.x += part[c].x;
+    s.y += part[c].y;
+    s.z += part[c].z;
+    s.w += part[c].w;
+  }
+  return s;
+}
+
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Stage 1 of the cut (all threads): thread t publishes the cluster-wide count
+// and mass of its four bins 4t .. 4t+3 (bin d: tokens of value key kmax - d).
+template <int DT, int CS>
+__device__ __forceinline__ void bins_partials(Shm& sh, int r, uint32_t hrow, int nbins, uint32_t kmax, float m,
+                                              float cexp) {
+  const int t = threadIdx.x;
+  if (t >= kBinThreads) return;
+  uint32_t C = 0u;
+  float M = 0.f;
+  if (4 * t < nbins) {
+    const uint4 b = cluster_bins4<CS>(hrow, t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int d = 4 * t + i;
+      const uint32_t c = d < nbins ? u4_at(b, i) : 0u;
+      if (c) {
+        C += c;
+        M += static_cast<float>(c) * softmax_mass(value_of_key<DT>(kmax - static_cast<uint32_t>(d)), m, cexp);
+      }
+    }
+  }
+  sh.pc[r][t] = C;
+  sh.pm[r][t] = M;
+}
+
+// Stage 2 of the cut (one warp per row).  Top-k: the bin where the running
+// count reaches top_k (exact, integer); its tokens kept are the
+// top_k - (count before) lowest-index ones.  Top-p (on the top-k set if
+// any): the first bin where the running mass reaches top_p * Z_k; a token of
+// that value is kept while the mass ranked before it stays below the
+// target.  Lane l scans bin threads 4l .. 4l+3; the thread holding the crossing
+// re-reads its four bins.  Returns false if the cut lies beyond the counted
+// bins (the exact fallback then takes over).
+template <int DT, int CS>
+__device__ __noinline__ bool cut_scan_warp(Shm& sh, int r, uint32_t hrow, int nbins, RowStat& rs, int top_k, float top_p,
+                              double zfull, float cexp) {
+  const int lane = threadIdx.x & 31;
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  const uint32_t K = static_cast<uint32_t>(top_k);
+  uint32_t dk = 0xFFFFFFFFu, ck = 0u, tk = 0u;
+  int tkthr = kThreads;  // thread holding the top-k bin
+  double zk = zfull;
+  if (topk_on) {
+    constexpr int kL = kBinThreads / 32;  // bin threads per lane
+    uint32_t lc[kL], C = 0u;
+    DF M{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+      lc[i] = sh.pc[r][kL * lane + i];
+      C += lc[i];
+      M = df_add(M, sh.pm[r][kL * lane + i]);
+    }
+    const uint32_t incl = warp_incl_scan_u32(C);
+    const DF Mi = warp_incl_scan_df(M);
+    const unsigned ball = __ballot_sync(kFull, incl - C < K && incl >= K);
+    if (!ball) return false;
+    const int L = __ffs(ball) - 1;
+    uint32_t o_d = 0u, o_c = 0u, o_t = 0u;
+    int o_thr = 0;
+    double o_z = 0.0;
+    if (lane == L) {
+      uint32_t run = incl - C;
+      DF mrun = df_add(Mi, -M.hi);
+      mrun = df_add(mrun, -M.lo);
+      int t = kL * L;
+#pragma unroll
+      for (int i = 0; i < kL; ++i) {
+        if (run + lc[i] >= K) { t = kL * L + i; break; }
+        run += lc[i];
+        mrun = df_add(mrun, sh.pm[r][kL * L + i]);
+      }
+      const uint4 b = cluster_bins4<CS>(hrow, t);
+      for (int j = 0; j < 4; ++j) {
+        const int d = 4 * t + j;
+        const uint32_t c = d < nbins ? u4_at(b, j) : 0u;
+        const float e = c ? softmax_mass(value_of_key<DT>(rs.kmax - static_cast<uint32_t>(d)), rs.m, cexp) : 0.f;
+        if (run + c >= K) {
+          o_d = static_cast<uint32_t>(d);
+          o_c = K - run;
+          o_t = c;
+          o_thr = t;
+          o_z = df_value(mrun) + (double)(K - run) * (double)e;
+          break;
+        }
+        run += c;
+        mrun = df_add(mrun, static_cast<float>(c) * e);
+      }
+    }
+    dk = __shfl_sync(kFull, o_d, L);
+    ck = __shfl_sync(kFull, o_c, L);
+    tk = __shfl_sync(kFull, o_t, L);
+    tkthr = __shfl_sync(kFull, o_thr, L);
+    zk = __shfl_sync(kFull, o_z, L);
+  }
+  uint32_t dstar = dk, cstar = ck, tstar = tk;
+  double zkept = zk;
+  if (topp_on) {
+    const DF tdf = df_from((double)top_p * zk);
+    // lane masses over the top-k set: threads past the top-k bin hold nothing,
+    // the thread holding it only its bins up to dk (with ck tokens at dk)
+    constexpr int kL = kBinThreads / 32;
+    DF M{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+      const int t = kL * lane + i;
+      if (t < tkthr) M = df_add(M, sh.pm[r][t]);
+    }
+    if (topk_on && tkthr / kL == lane) {
+      const uint4 b = cluster_bins4<CS>(hrow, tkthr);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t d = static_cast<uint32_t>(4 * tkthr + j);
+        if (d > dk) break;
+        const uint32_t c = d == dk ? ck : u4_at(b, j);
+        if (c) M = df_add(M, static_cast<float>(c) * softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp));
+      }
+    }
+    const DF Mi = warp_incl_scan_df(M);
+    const unsigned ball = __ballot_sync(kFull, (M.hi > 0.f) && df_diff(Mi, tdf) >= 0.f);
+    if (!ball) return false;
+    const int L = __ffs(ball) - 1;
+    uint32_t o_d = 0u, o_c = 0u, o_t = 0u;
+    double o_z = 0.0;
+    int found = 0;
+    if (lane == L) {
+      const double target = df_value(tdf);
+      double run = df_value(Mi) - df_value(M);  // mass of the lanes before
+      int tlast = -1;
+      double runlast = run;
+      for (int i = 0; i < kL && !found; ++i) {
+        const int t = kL * L + i;
+        if (t > tkthr) break;
+        const uint4 b = cluster_bins4<CS>(hrow, t);
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t d = static_cast<uint32_t>(4 * t + j);
+          if (static_cast<int>(d) >= nbins || (topk_on && d > dk)) break;
+          uint32_t c = u4_at(b, j);
+          const uint32_t real = c;
+          if (topk_on && d == dk) c = ck;
+          if (!c) continue;
+          const float e = softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp);
+          const double me = (double)c * (double)e;
+          tlast = static_cast<int>(d);
+          runlast = run;
+          if (run + me >= target) {
+            const float xneed = static_cast<float>((target - run) / (double)e);
+            uint32_t cp = c;
+            if (xneed < static_cast<float>(c)) cp = max(1u, static_cast<uint32_t>(ceilf(xneed)));
+            o_d = d;
+            o_c = cp;
+            o_t = real;
+            o_z = run + (double)cp * (double)e;
+            found = 1;
+            break;
+          }
+          run += me;
+        }
+      }
+      if (!found && tlast >= 0) {  // rounding: the last non-empty bin takes the cut
+        const uint32_t d = static_cast<uint32_t>(tlast);
+        const uint4 b = cluster_bins4<CS>(hrow, tlast / 4);
+        uint32_t c = u4_at(b, tlast % 4);
+        o_t = c;
+        if (topk_on && d == dk) c = ck;
+        const float e = softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp);
+        o_d = d;
+        o_c = c;
+        o_z = runlast + (double)c * (double)e;
+        found = 1;
+      }
+    }
+    if (!__shfl_sync(kFull, found, L)) return false;
+    dstar = __shfl_sync(kFull, o_d, L);
+    cstar = __shfl_sync(kFull, o_c, L);
+    tstar = __shfl_sync(kFull, o_t, L);
+    zkept = __shfl_sync(kFull, o_z, L);
+  }
+  rs.kstar = rs.kmax - dstar;
+  rs.cstar = cstar;
+  rs.tie_total = tstar;
+  rs.zkept = zkept;
+  rs.partial = cstar < tstar ? 1 : 0;
+  return true;
+}
+
+// Smallest d such that bins 0..d of a CTA-local histogram hold >= need
+// tokens; kWindow - 1 if they never do.  All threads call it.
+__device__ __noinline__ uint32_t local_bins_reach(uint32_t hrow, uint32_t need, Shm& sh) {
+  constexpr int kB = 4;
+  const int tid = threadIdx.x;
+  const uint4 b4 = tid < kBinThreads ? lds128(hrow + 16u * tid) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t cnt[kB] = {b4.x, b4.y, b4.z, b4.w};
+  uint32_t C = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+  uint32_t total;
+  const uint32_t P = block_excl_u32(C, sh.w_u, total);
+  if (tid == 0) sh.c_d = static_cast<uint32_t>(kWindow - 1);
+  __syncthreads();
+  if (P < need && P + C >= need) {
+    uint32_t run = P;
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      if (run < need && run + cnt[i] >= need) sh.c_d = static_cast<uint32_t>(tid * kB + i);
+      run += cnt[i];
+    }
+  }
+  __syncthreads();
+  const uint32_t d = sh.c_d;
+  __syncthreads();
+  return d;
 }
 
 enum PassKind { PASS_COUNT_GE = 0, PASS_MASS_GT = 1, PASS_MIN_GE = 2, PASS_COUNT_EQ = 3 };
@@ -277,14 +628,14 @@ enum PassKind { PASS_COUNT_GE = 0, PASS_MASS_GT = 1, PASS_MIN_GE = 2, PASS_COUNT
 // One full pass over this CTA's slice of one row, reduced over the cluster.
 // Used only by the exact fallback search of the cut.
 template <int DT, int CS>
-__device__ double cluster_pass(cg::cluster_group& cluster, Shm& sh, const uint4* buf, int n, int nvec, int kind,
+__device__ __noinline__ double cluster_pass(cg::cluster_group& cluster, Shm& sh, uint32_t buf, int n, int nvec, int kind,
                                uint32_t kappa, float m, float c, uint32_t& slot) {
   using E = Elt<DT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t cnt = 0, kmin = 0xFFFFFFFFu;
   float mass = 0.f;
   for (int v = tid; v < nvec; v += kThreads) {
-    const uint4 x = buf[v];
+    const uint4 x = lds128(buf + 16u * v);
     const int t0 = v * E::kPerVec;
 #pragma unroll
     for (int j = 0; j < E::kPerVec; ++j) {
@@ -299,10 +650,10 @@ __device__ double cluster_pass(cg::cluster_group& cluster, Shm& sh, const uint4*
     }
   }
   const uint32_t s = slot & 1u;
-  const double dm = warp_sum_f64((double)mass);
+  mass = warp_sum_f32(mass);
   cnt = warp_sum_u32(cnt);
   kmin = warp_min_u32(kmin);
-  if (lane == 0) { sh.w_pm[warp] = dm; sh.w_pc[warp] = cnt; sh.w_pk[warp] = kmin; }
+  if (lane == 0) { sh.w_pm[warp] = mass; sh.w_pc[warp] = cnt; sh.w_pk[warp] = kmin; }
   __syncthreads();
   if (tid == 0) {
     double tm = 0.0;
@@ -337,9 +688,355 @@ __device__ __forceinline__ uint32_t bits_round_down(float v) {
   return (u & 0x80000000u) ? hi + 1u : hi;  // negative: away from zero is down
 }
 
-}  // namespace
+// The exact cut of one row by a bitwise search over the keys: used when the
+// cut lies outside the exact-value histogram (flat rows, fp32 rows).  Every
+// step is a full pass over the slice reduced over the cluster.
+template <int DT, int CS>
+__device__ __noinline__ void fallback_row(cg::cluster_group& cluster, Shm& sh, uint32_t bb, int n, int nvec, int r,
+                                          int top_k, float top_p, double zfull_r, float cexp, uint32_t& slot) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  const int tid = threadIdx.x;
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  RowStat rs = sh.rs[r];
+  const int kb = E::kKeyBits;
+  uint32_t kk = 0, ck = 0, tk = 0;
+  double zk = zfull_r;
+  if (topk_on) {
+    for (int bit = kb - 1; bit >= 0; --bit) {
+      const uint32_t cand = kk | (1u << bit);
+      const double cnt = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, cand, rs.m, cexp, slot);
+      if (cnt >= (double)top_k) kk = cand;
+    }
+    const uint32_t gt = (kk == 0xFFFFFFFFu) ? 0u
+        : static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, kk + 1u, rs.m, cexp, slot));
+    ck = static_cast<uint32_t>(top_k) - gt;
+    tk = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kk, rs.m, cexp, slot));
+    const float ek = softmax_mass(value_of_key<DT>(kk), rs.m, cexp);
+    zk = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kk, rs.m, cexp, slot) + (double)ck * (double)ek;
+  }
+  uint32_t kstar = kk, cstar = ck, tstar = tk;
+  double zkept = zk;
+  if (topp_on) {
+    const double target = (double)top_p * zk;
+    // G(kappa): mass of the top-k set strictly above kappa
+    auto G = [&](uint32_t kappa) -> double {
+      if (topk_on && kappa < kk) return zk;
+      return cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kappa, rs.m, cexp, slot);
+    };
+    uint32_t k0;
+    if (G(0u) < target) {
+      k0 = 0u;
+    } else {
+      uint32_t kp = 0u;
+      for (int bit = kb - 1; bit >= 0; --bit) {
+        const uint32_t cand = kp | (1u << bit);
+        if (G(cand) >= target) kp = cand;
+      }
+      k0 = kp + 1u;
+    }
+    kstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MIN_GE, k0, rs.m, cexp, slot));
+    const double mb = G(kstar);
+    tstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kstar, rs.m, cexp, slot));
+    const uint32_t avail = (topk_on && kstar == kk) ? ck : tstar;
+    const float ep = softmax_mass(value_of_key<DT>(kstar), rs.m, cexp);
+    const double xneed = (target - mb) / (double)ep;
+    uint32_t cp = avail;
+    if (xneed < (double)avail) cp = max(1u, static_cast<uint32_t>(ceil(xneed)));
+    cstar = cp;
+    zkept = mb + (double)cp * (double)ep;
+  }
+  rs.kstar = kstar;
+  rs.cstar = cstar;
+  rs.tie_total = tstar;
+  rs.zkept = zkept;
+  rs.partial = cstar < tstar ? 1 : 0;
+  rs.inv_z = 1.f / static_cast<float>(zkept);
+  rs.thr = H::thr_pack(E::bits_of_key(kstar));
+  __syncthreads();
+  if (tid == 0) sh.rs[r] = rs;
+  __syncthreads();
+}
 
-__device__ void sample_finalize(const SampleArgs& a, int b);
+// Where a partial tie stops.  The kept tokens of value kstar are the cstar
+// lowest-index ones.  Each CTA needs the number of such tokens in lower
+// cluster ranks (from the exchanged histograms, or, for rows cut by the
+// fallback search, from one more exchange); the CTA holding the first one not
+// kept finds its index, every other CTA records a bound outside its slice.
+template <int DT, int CS, int NR>
+__device__ __noinline__ void tie_cuts(cg::cluster_group& cluster, Shm& sh, uint32_t buf0, uint32_t buf1,
+                                      uint32_t hist, int lo, int hi, int n, int V, bool part_fb) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  const int crank = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = (n * E::kBytes + 15) / 16;
+  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int seg_beg = min(nvec, warp * vpw);
+  const int seg_end = min(nvec, seg_beg + vpw);
+  const int seg_iters = (seg_end - seg_beg + 31) / 32;
+  const uint32_t buf[2] = {buf0, buf1};
+  if (warp < NR && sh.rs[warp].partial && !sh.fb_need[warp]) {
+    const int r = warp;
+    const uint32_t dstar = sh.rs[r].kmax - sh.rs[r].kstar;
+    uint32_t v = 0u;
+    if (lane < CS) v = ld_cluster_u32(mapa_shared(hist + 4u * (r * kWindow + dstar), lane));
+    const uint32_t before = warp_sum_u32(lane < crank ? v : 0u);
+    const uint32_t local = __shfl_sync(kFull, v, crank);
+    if (lane == 0) { sh.tie_before[r] = before; sh.tie_local[r] = local; }
+  }
+  if (part_fb) {  // rows cut by the fallback: count per CTA, then exchange
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      uint32_t c = 0;
+      if (sh.rs[r].partial && sh.fb_need[r]) {
+        const uint32_t thr = sh.rs[r].thr;
+        for (int v = seg_beg + lane; v < seg_end; v += 32)
+          c += __popc(H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n));
+      }
+      c = warp_sum_u32(c);
+      if (lane == 0) sh.w_tie[warp][r] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        uint32_t t = 0;
+        for (int w = 0; w < kWarps; ++w) t += sh.w_tie[w][r];
+        sh.x_tie[r] = t;
+      }
+    }
+    cluster.sync();  // ------------------------------------- sync: fallback ties
+    if (warp < NR && sh.rs[warp].partial && sh.fb_need[warp]) {
+      const int r = warp;
+      uint32_t v = 0u;
+      if (lane < CS) v = cluster.map_shared_rank(&sh, lane)->x_tie[r];
+      const uint32_t before = warp_sum_u32(lane < crank ? v : 0u);
+      if (lane == 0) { sh.tie_before[r] = before; sh.tie_local[r] = sh.x_tie[r]; }
+    }
+  }
+  __syncthreads();
+  bool search = false;
+  if (tid == 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      sh.tie_warp[r] = -1;
+      sh.tie_cut[r] = V;
+      if (!sh.rs[r].partial) continue;
+      const int64_t j = static_cast<int64_t>(sh.rs[r].cstar) - sh.tie_before[r];
+      if (j <= 0) sh.tie_cut[r] = lo;
+      else if (j >= static_cast<int64_t>(sh.tie_local[r])) sh.tie_cut[r] = hi;
+      else { sh.tie_cut[r] = -1; sh.tie_j[r] = static_cast<uint32_t>(j); }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < NR; ++r) search |= sh.tie_cut[r] < 0;
+  if (search) {  // this CTA holds the first tie token that is not kept
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      uint32_t c = 0;
+      if (sh.tie_cut[r] < 0) {
+        const uint32_t thr = sh.rs[r].thr;
+        for (int v = seg_beg + lane; v < seg_end; v += 32)
+          c += __popc(H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n));
+      }
+      c = warp_sum_u32(c);
+      if (lane == 0) sh.w_tie[warp][r] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (sh.tie_cut[r] >= 0) continue;
+        uint32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          if (run + sh.w_tie[w][r] > sh.tie_j[r]) {
+            sh.tie_warp[r] = w;
+            sh.tie_j[r] -= run;
+            break;
+          }
+          run += sh.w_tie[w][r];
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (warp != sh.tie_warp[r]) continue;
+      const uint32_t thr = sh.rs[r].thr;
+      uint32_t jj = sh.tie_j[r];
+      for (int it = 0; it < seg_iters; ++it) {
+        const int v = seg_beg + it * 32 + lane;
+        const uint32_t msk = v < seg_end ? (H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n)) : 0u;
+        const uint32_t c = __popc(msk);
+        const uint32_t incl = warp_incl_scan_u32(c);
+        const uint32_t tot = __shfl_sync(kFull, incl, 31);
+        if (jj < tot) {
+          if (incl > jj && incl - c <= jj) {  // this lane holds the token
+            uint32_t mm = msk;
+            for (uint32_t q = jj - (incl - c); q > 0; --q) mm &= mm - 1u;
+            sh.tie_cut[r] = lo + v * E::kPerVec + (__ffs(mm) - 1);
+          }
+          break;
+        }
+        jj -= tot;
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) sh.rs[r].tie_cut = sh.tie_cut[r];
+  }
+  __syncthreads();
+}
+
+// The filtered, normalised probabilities of this CTA's slice, written out.
+template <int DT>
+__device__ __noinline__ void write_probs(const SampleArgs& a, uint32_t buf0, const RowStat& rp, float cexp, int unit,
+                                         int lo, int n, int V) {
+  using E = Elt<DT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = (n * E::kBytes + 15) / 16;
+  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int seg_beg = min(nvec, warp * vpw);
+  const int seg_end = min(nvec, seg_beg + vpw);
+  const uint32_t buf[1] = {buf0};
+  float* out = a.out_probs + static_cast<size_t>(unit) * V + lo;
+  const bool vec_out = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) && (V % 4 == 0);
+  for (int v = seg_beg + lane; v < seg_end; v += 32) {
+    const int t0 = v * E::kPerVec;
+    const uint4 x = lds128(buf[0] + 16u * v);
+    float w[8];
+    vec_weights<DT>(x, x, t0, lo, n, false, rp, rp, cexp, w);
+    if (rp.bad) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+    }
+    if (vec_out && t0 + E::kPerVec <= n) {
+      reinterpret_cast<float4*>(out + t0)[0] = make_float4(w[0], w[1], w[2], w[3]);
+      if (E::kPerVec == 8) reinterpret_cast<float4*>(out + t0)[1] = make_float4(w[4], w[5], w[6], w[7]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < E::kPerVec; ++j)
+        if (t0 + j < n) out[t0 + j] = w[j];
+    }
+  }
+}
+
+// The CTA holding the drawn token finds it: the warp whose segment holds the
+// crossing walks it vector by vector (index order) and writes the token.
+template <int DT, int NR>
+__device__ __noinline__ void draw_walk(const SampleArgs& a, Shm& sh, uint32_t buf0, uint32_t bufq, bool use_q,
+                                       const RowStat& rp, const RowStat& rq, float cexp, double target, int lo,
+                                       int n, int unit, int b) {
+  using E = Elt<DT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = (n * E::kBytes + 15) / 16;
+  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int seg_beg = min(nvec, warp * vpw);
+  const int seg_end = min(nvec, seg_beg + vpw);
+  const int seg_iters = (seg_end - seg_beg + 31) / 32;
+  const int kq = a.k;
+  const uint32_t buf[2] = {buf0, bufq};
+  if (tid == 0) {
+    double run = 0.0, wbase = 0.0, lbase = 0.0;
+    int wsel = -1, wlast = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const double sw = (double)sh.w_res[w];
+      if (sw > 0.0) { wlast = w; lbase = run; }
+      if (wsel < 0 && sw > 0.0 && run + sw > target) { wsel = w; wbase = run; }
+      run += sw;
+    }
+    if (wsel < 0) { wsel = wlast; wbase = lbase; }
+    sh.draw_warp = wsel;
+    sh.draw_base = wbase;
+  }
+  __syncthreads();
+  if (warp == sh.draw_warp) {
+    const float tw = static_cast<float>(target - sh.draw_base);
+    float run = 0.f;
+    int token = -1, last_pos = -1;
+    for (int it = 0; it < seg_iters && token < 0; ++it) {
+      const int v = seg_beg + it * 32 + lane;
+      const bool valid = v < seg_end;
+      const int t0 = v * E::kPerVec;
+      float w[8];
+      float ls = 0.f;
+      int lpos = -1;
+      if (valid) {
+        const uint4 xp = lds128(buf[0] + 16u * v);
+        const uint4 xq = use_q ? lds128(buf[NR - 1] + 16u * v) : xp;
+        ls = vec_weights<DT>(xp, xq, t0, lo, n, use_q, rp, rq, cexp, w);
+#pragma unroll
+        for (int j = 0; j < E::kPerVec; ++j)
+          if (w[j] > 0.f) lpos = t0 + j;
+      }
+      const float incl = warp_incl_scan(ls);
+      const unsigned ball = __ballot_sync(kFull, valid && ls > 0.f && run + incl > tw);
+      const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
+      const int lp = __shfl_sync(kFull, lpos, lastl);
+      if (lp >= 0) last_pos = lp;
+      if (ball) {
+        const int l = __ffs(ball) - 1;
+        int tok = -1;
+        if (lane == l) {
+          float cum = run + (incl - ls);
+          int lastj = -1;
+#pragma unroll
+          for (int j = 0; j < E::kPerVec; ++j) {
+            if (w[j] > 0.f) lastj = t0 + j;
+            cum += w[j];
+            if (tok < 0 && w[j] > 0.f && cum > tw) tok = t0 + j;
+          }
+          if (tok < 0) tok = lastj;
+        }
+        token = __shfl_sync(kFull, tok, l);
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (token < 0) token = last_pos;  // only reachable through rounding
+    if (lane == 0) {
+      a.recs[unit].drawn = token >= 0 ? lo + token : -1;
+      __threadfence();
+      if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
+    }
+  }
+}
+
+// Bound for a top-p cut from the cluster's warp maxima (one warp per row).
+// Those maxima are tokens of the row.  If the ones at or above a value v
+// already weigh top_p * Z, the nucleus ends at or above v, so no token below v
+// is kept.  (1e-4 of margin covers rounding.)  Writes the bound value (or
+// -inf) to sh.w_f[r].
+template <int CS>
+__device__ __noinline__ void warp_max_bound(Shm& sh, int r, float m_r, double z_r, float cexp, float top_p) {
+  const int lane = threadIdx.x & 31;
+  constexpr int nw = kWarps * CS;
+  float v0 = -INFINITY, v1 = -INFINITY;
+  if (lane < nw) v0 = ld_cluster_f32(mapa_shared(smem_addr(&sh.w_max[lane % kWarps][r]), lane / kWarps));
+  if (lane + 32 < nw)
+    v1 = ld_cluster_f32(mapa_shared(smem_addr(&sh.w_max[(lane + 32) % kWarps][r]), (lane + 32) / kWarps));
+  const float e0 = v0 > -INFINITY ? softmax_mass(v0, m_r, cexp) : 0.f;
+  const float e1 = v1 > -INFINITY ? softmax_mass(v1, m_r, cexp) : 0.f;
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < nw; ++j) {
+    const float vj = __shfl_sync(kFull, j < 32 ? v0 : v1, j & 31);
+    const float ej = __shfl_sync(kFull, j < 32 ? e0 : e1, j & 31);
+    s0 += vj >= v0 ? ej : 0.f;
+    s1 += vj >= v1 ? ej : 0.f;
+  }
+  const float target = 1.0001f * top_p * static_cast<float>(z_r);
+  float cand = -INFINITY;
+  if (v0 > -INFINITY && s0 >= target) cand = v0;
+  if (v1 > -INFINITY && s1 >= target) cand = fmaxf(cand, v1);
+  cand = warp_max(cand);
+  if (lane == 0) sh.w_f[r] = cand;
+}
+
+}  // namespace
 
 // One unit (b, pos) with NR rows (2: target and draft, 1: target only).
 template <int DT, int CS, int NR>
@@ -362,8 +1059,11 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
   const int nvec = (n * E::kBytes + 15) / 16;
   const int nfull = n / E::kPerVec;  // vectors without a ragged tail
   const int bufbytes = ((a.chunk * E::kBytes + 15) / 16) * 16;
-  const uint4* buf[2] = {reinterpret_cast<const uint4*>(dsm), reinterpret_cast<const uint4*>(dsm + bufbytes)};
-  uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + 2 * bufbytes);
+  // shared-window addresses of the two row buffers and of the histograms
+  const uint32_t sbase = smem_addr(dsm);
+  const uint32_t buf[2] = {sbase, sbase + static_cast<uint32_t>(bufbytes)};
+  const uint32_t hist = sbase + 2u * static_cast<uint32_t>(bufbytes);
+  unsigned char* const bufp[2] = {dsm, dsm + bufbytes};
   const unsigned char* rows[2] = {rowp, rowq};
   const bool aligned[2] = {a.aligned_target != 0, a.aligned_draft != 0};
 
@@ -392,37 +1092,47 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
 #pragma unroll
     for (int r = 0; r < NR; ++r)
       if (aligned[r] && n > 0)
-        bulk_copy_g2s(const_cast<uint4*>(buf[r]), rows[r] + static_cast<size_t>(lo) * E::kBytes,
-                      static_cast<uint32_t>(n * E::kBytes), &sh.mbar);
+        bulk_copy_g2s(bufp[r], rows[r] + static_cast<size_t>(lo) * E::kBytes, static_cast<uint32_t>(n * E::kBytes),
+                      &sh.mbar);
   }
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     if (!aligned[r]) {
       for (int t = tid; t < n; t += kThreads) {
         const uint32_t bits = E::bits_at(rows[r], static_cast<int64_t>(lo) + t);
-        if (E::kBytes == 2) reinterpret_cast<uint16_t*>(const_cast<uint4*>(buf[r]))[t] = static_cast<uint16_t>(bits);
-        else reinterpret_cast<uint32_t*>(const_cast<uint4*>(buf[r]))[t] = bits;
+        if (E::kBytes == 2) sts_u16(buf[r] + 2u * t, bits);
+        else sts_u32(buf[r] + 4u * t, bits);
       }
     }
   }
   if (filt)
-    for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
-  if (!mbar_wait_bounded(&sh.mbar, 0)) set_status(a.status, SPEC_STATUS_TIMEOUT);
+    for (int t = tid; t < NR * kWindow; t += kThreads) sts_u32(hist + 4u * t, 0u);
+  if (tid == 0 && !mbar_wait_bounded(&sh.mbar, 0)) set_status(a.status, SPEC_STATUS_TIMEOUT);
   __syncthreads();
 
   // ------------------------------------------------------ phase 1: max
+  float tmax[NR];  // this thread's own maximum, for the top-k bound below
   {
     typename H::MaxAcc st[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) H::max_init(st[r]);
-    for (int v = tid; v < nfull; v += kThreads) {
+    int v = tid;
+    for (; v + kThreads < nfull; v += 2 * kThreads) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) H::max_vec(buf[r][v], st[r]);
+      for (int r = 0; r < NR; ++r) {
+        H::max_vec(lds128(buf[r] + 16u * v), st[r]);
+        H::max_vec(lds128(buf[r] + 16u * (v + kThreads)), st[r]);
+      }
+    }
+    if (v < nfull) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) H::max_vec(lds128(buf[r] + 16u * v), st[r]);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       float mx = H::max_finish(st[r]);
-      for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads) mx = max_nan(mx, E::value(E::bits_at(buf[r], t)));
+      for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads) mx = max_nan(mx, E::value(lds_elem<DT>(buf[r], t)));
+      tmax[r] = mx;
       mx = warp_max_nan(mx);
       if (lane == 0) sh.w_max[warp][r] = mx;
     }
@@ -465,18 +1175,18 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
         u64 acc0 = 0ull, acc1 = 0ull;
         int v = tid;
         for (; v + kThreads < nfull; v += 2 * kThreads) {
-          H::mass_vec(buf[r][v], m2, c2, acc0);
-          H::mass_vec(buf[r][v + kThreads], m2, c2, acc1);
+          H::mass_vec(lds128(buf[r] + 16u * v), m2, c2, acc0);
+          H::mass_vec(lds128(buf[r] + 16u * (v + kThreads)), m2, c2, acc1);
         }
-        if (v < nfull) H::mass_vec(buf[r][v], m2, c2, acc0);
+        if (v < nfull) H::mass_vec(lds128(buf[r] + 16u * v), m2, c2, acc0);
         float s0, s1, s2, s3;
         upk(acc0, s0, s1);
         upk(acc1, s2, s3);
         float s = (s0 + s1) + (s2 + s3);
         for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads)
-          s += softmax_mass(E::value(E::bits_at(buf[r], t)), m[r], cexp);
-        const double ws = warp_sum_f64((double)s);
-        if (lane == 0) sh.w_sum[warp][r] = ws;
+          s += softmax_mass(E::value(lds_elem<DT>(buf[r], t)), m[r], cexp);
+        s = warp_sum_f32(s);
+        if (lane == 0) sh.w_sum[warp][r] = s;
       }
     }
     __syncthreads();
@@ -485,26 +1195,34 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
       for (int r = 0; r < NR; ++r) {
         double s = 0.0;
         if (!any_bad)
-          for (int w = 0; w < kWarps; ++w) s += sh.w_sum[w][r];
+          for (int w = 0; w < kWarps; ++w) s += (double)sh.w_sum[w][r];
         sh.x_sum[r] = s;
       }
     }
     cluster.sync();  // -------------------------------------------- sync: sum
+    if (tid == 0) {  // fixed-order cluster total, one thread, then broadcast
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      double v = 0.0;
-      if (lane < CS) v = cluster.map_shared_rank(&sh, lane)->x_sum[r];
-      zfull[r] = cluster_sum_f64<CS>(v);
+      for (int r = 0; r < NR; ++r) {
+        double z = 0.0;
+        for (int c = 0; c < CS; ++c) z += cluster.map_shared_rank(&sh, c)->x_sum[r];
+        sh.b_zfull[r] = z;
+      }
     }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < NR; ++r) zfull[r] = sh.b_zfull[r];
   }
 
   // ------------------------- phase 3: exact-value histogram near the top
   // Bins d = kmax - key count the tokens of one value each.  Only tokens that
-  // can survive the cut are counted: at most kWindow values below the max,
-  // and with top-p alone no token whose mass is below (1 - top_p) Z / V (all
-  // tokens ranked at or below such a token weigh less than (1 - top_p) Z, so
-  // the mass ranked before it exceeds top_p Z).  Half of that bound is used,
-  // as margin for rounding.
+  // can survive the cut are counted:
+  //  - at most kWindow values below the maximum;
+  //  - top-k: none below this CTA's top_k-th largest thread maximum (that
+  //    value is at most the top_k-th largest token of the row);
+  //  - top-p alone: no token whose mass is below (1 - top_p) Z / V (all
+  //    tokens ranked at or below it weigh less than (1 - top_p) Z, so the
+  //    mass ranked before it exceeds top_p Z); half of that bound is used,
+  //    as margin for rounding.
   uint32_t klo[NR];
   if (filt) {
 #pragma unroll
@@ -513,8 +1231,8 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
       const uint32_t kninf = E::key(E::kBytes == 2 ? 0xFF80u : 0xFF800000u);  // -inf
       if (kl < kninf) kl = kninf;
       if (topp_on && !topk_on && !any_bad && zfull[r] > 0.0) {
-        const double lim = 0.5 * (1.0 - (double)a.top_p) * zfull[r] / (double)V;
-        const float vb = m[r] + static_cast<float>(log2(lim)) / cexp;
+        const float lim = 0.5f * (1.f - a.top_p) * static_cast<float>(zfull[r]) / static_cast<float>(V);
+        const float vb = m[r] + log2f(lim) / cexp;
         if (isfinite(vb) && vb > -3.0e38f) {
           const uint32_t kb = E::key(bits_round_down<DT>(vb));
           if (kb > kl) kl = kb;
@@ -522,25 +1240,60 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
       }
       klo[r] = kl;
     }
+    if (topp_on && !topk_on && !any_bad) {
+      // a tighter bound from the cluster's warp maxima
+      if (warp < NR)
+        warp_max_bound<CS>(sh, warp, warp == 0 ? m[0] : m[NR - 1], warp == 0 ? zfull[0] : zfull[NR - 1], cexp, a.top_p);
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const float cand = sh.w_f[r];
+        if (cand > -INFINITY) {
+          const uint32_t cb = (E::kBytes == 2) ? (__float_as_uint(cand) >> 16) : __float_as_uint(cand);
+          const uint32_t kc = E::key(cb);
+          if (kc > klo[r]) klo[r] = kc;
+        }
+      }
+      __syncthreads();
+    }
+    if (topk_on && !any_bad && a.top_k <= kThreads) {
+      // histogram of the thread maxima, then this CTA's top_k-th largest
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (tmax[r] > -INFINITY) {
+          const uint32_t tb = (E::kBytes == 2) ? (__float_as_uint(tmax[r]) >> 16) : __float_as_uint(tmax[r]);
+          const uint32_t d = kmax[r] - E::key(tb);
+          if (d < static_cast<uint32_t>(kWindow)) red_add_shared(hist + 4u * (r * kWindow + d), 1u);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const uint32_t dlb = local_bins_reach(hist + 4u * r * kWindow, static_cast<uint32_t>(a.top_k), sh);
+        if (kmax[r] - dlb > klo[r]) klo[r] = kmax[r] - dlb;
+      }
+      for (int t = tid; t < NR * kWindow; t += kThreads) sts_u32(hist + 4u * t, 0u);
+      __syncthreads();
+    }
     if (!any_bad) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         const uint32_t thr = H::thr_pack(E::bits_of_key(klo[r]));
-        uint32_t* hr = hist + r * kWindow;
+        const uint32_t hr = hist + 4u * r * kWindow;
         const uint32_t km = kmax[r];
         for (int v = tid; v < nfull; v += kThreads) {
-          const uint4 x = buf[r][v];
+          const uint4 x = lds128(buf[r] + 16u * v);
           if (!H::any_ge(x, thr)) continue;
           uint32_t msk = H::mask_ge(x, thr);
           while (msk) {
             const int j = __ffs(msk) - 1;
             msk &= msk - 1u;
-            atomicAdd(hr + (km - E::key(E::bits_of(x, j))), 1u);
+            red_add_shared(hr + 4u * (km - E::key(E::bits_of(x, j))), 1u);
           }
         }
         for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads) {
-          const uint32_t k = E::key(E::bits_at(buf[r], t));
-          if (k >= klo[r]) atomicAdd(hr + (km - k), 1u);
+          const uint32_t k = E::key(lds_elem<DT>(buf[r], t));
+          if (k >= klo[r]) red_add_shared(hr + 4u * (km - k), 1u);
         }
       }
     }
@@ -549,6 +1302,13 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
   }
 
   // ------------------------------------ phase 3b: the kept set of each row
+  if (filt && !any_bad) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      bins_partials<DT, CS>(sh, r, hist + 4u * r * kWindow, static_cast<int>(kmax[r] - klo[r]) + 1, kmax[r], m[r],
+                            cexp);
+    __syncthreads();
+  }
   if (warp < NR) {
     const int r = warp;
     // this warp's row, picked without a run-time array index
@@ -563,8 +1323,7 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
     rs.kstar = 0u;
     rs.cstar = 0u;
     rs.tie_total = 0u;
-    rs.ties_before = 0u;
-    rs.thr = 0u;
+    rs.tie_cut = V;
     rs.zkept = zfull_r;
     rs.all_kept = 1;
     rs.bad = rbad_r ? 1 : 0;
@@ -572,94 +1331,11 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
     uint32_t need_fb = 0u;
     if (!any_bad && filt) {
       rs.all_kept = 0;
-      const float mr = m_r;
       const int nbins = static_cast<int>(kmax_r - klo_r) + 1;
-      auto bin = [&](int d) -> uint32_t {
-        if (d >= nbins) return 0u;
-        uint32_t c = 0;
-#pragma unroll
-        for (int q = 0; q < CS; ++q) c += cluster.map_shared_rank(hist, q)[r * kWindow + d];
-        return c;
-      };
-      auto bin_mass = [&](int d) -> float {
-        return softmax_mass(value_of_key<DT>(kmax_r - static_cast<uint32_t>(d)), mr, cexp);
-      };
-      bool ok = true;
-      uint32_t dk = 0, ck = 0, tk = 0;
-      double zk = zfull_r;
-      if (topk_on) {
-        ok = false;
-        uint32_t base = 0;
-        double mbase = 0.0;
-        for (int d0 = 0; d0 < nbins; d0 += 32) {
-          const int d = d0 + lane;
-          const uint32_t cnt = bin(d);
-          const float ed = cnt ? bin_mass(d) : 0.f;
-          const double ms = cnt ? (double)cnt * (double)ed : 0.0;
-          const uint32_t incl = warp_incl_scan_u32(cnt);
-          const double mincl = warp_incl_scan_f64(ms);
-          const unsigned ball = __ballot_sync(kFull, base + incl >= static_cast<uint32_t>(a.top_k));
-          if (ball) {
-            const int l = __ffs(ball) - 1;
-            dk = static_cast<uint32_t>(d0 + l);
-            const uint32_t before = base + __shfl_sync(kFull, incl - cnt, l);
-            ck = static_cast<uint32_t>(a.top_k) - before;
-            tk = __shfl_sync(kFull, cnt, l);
-            const double mb = mbase + __shfl_sync(kFull, mincl - ms, l);
-            zk = mb + (double)ck * (double)__shfl_sync(kFull, ed, l);
-            ok = true;
-            break;
-          }
-          base += __shfl_sync(kFull, incl, 31);
-          mbase += __shfl_sync(kFull, mincl, 31);
-        }
-      }
-      uint32_t dstar = dk, cstar = ck, tstar = tk;
-      double zkept = zk;
-      if (ok && topp_on) {
-        ok = false;
-        const double target = (double)a.top_p * zk;
-        double mbase = 0.0;
-        for (int d0 = 0; d0 < nbins; d0 += 32) {
-          const int d = d0 + lane;
-          const uint32_t real = bin(d);
-          uint32_t cnt = real;
-          if (topk_on && static_cast<uint32_t>(d) > dk) cnt = 0;
-          if (topk_on && static_cast<uint32_t>(d) == dk) cnt = ck;
-          const float ed = cnt ? bin_mass(d) : 0.f;
-          const double ms = cnt ? (double)cnt * (double)ed : 0.0;
-          const double mincl = warp_incl_scan_f64(ms);
-          const unsigned ball = __ballot_sync(kFull, cnt > 0 && mbase + mincl >= target);
-          if (ball) {
-            const int l = __ffs(ball) - 1;
-            dstar = static_cast<uint32_t>(d0 + l);
-            const double mb = mbase + __shfl_sync(kFull, mincl - ms, l);
-            const uint32_t avail = __shfl_sync(kFull, cnt, l);
-            const float ep = __shfl_sync(kFull, ed, l);
-            tstar = __shfl_sync(kFull, real, l);
-            const double xneed = (target - mb) / (double)ep;
-            uint32_t cp = avail;
-            if (xneed < (double)avail) cp = max(1u, static_cast<uint32_t>(ceil(xneed)));
-            cstar = cp;
-            zkept = mb + (double)cp * (double)ep;
-            ok = true;
-            break;
-          }
-          mbase += __shfl_sync(kFull, mincl, 31);
-          if (topk_on && static_cast<uint32_t>(d0 + 31) >= dk) break;
-        }
-      }
-      if (ok) {
-        rs.kstar = rs.kmax - dstar;
-        rs.cstar = cstar;
-        rs.tie_total = tstar;
-        rs.zkept = zkept;
-        rs.partial = cstar < tstar ? 1 : 0;
-      } else {
+      if (!cut_scan_warp<DT, CS>(sh, r, hist + 4u * r * kWindow, nbins, rs, a.top_k, a.top_p, zfull_r, cexp))
         need_fb = 1u;
-      }
     }
-    rs.inv_z = static_cast<float>(1.0 / rs.zkept);
+    rs.inv_z = 1.f / static_cast<float>(rs.zkept);
     rs.thr = H::thr_pack(E::bits_of_key(rs.kstar));
     if (lane == 0) { sh.rs[r] = rs; sh.fb_need[r] = need_fb; }
   }
@@ -668,143 +1344,28 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
   // ---------------- exact fallback: bitwise search of the cut over the keys
   {
     uint32_t slot = 0;
-#pragma unroll
+#pragma unroll 1
     for (int r = 0; r < NR; ++r) {
       if (!sh.fb_need[r]) continue;  // identical in every CTA of the cluster
-      RowStat rs = sh.rs[r];
-      const uint4* bb = buf[r];
-      const int kb = E::kKeyBits;
-      uint32_t kk = 0, ck = 0, tk = 0;
-      double zk = zfull[r];
-      if (topk_on) {
-        for (int bit = kb - 1; bit >= 0; --bit) {
-          const uint32_t cand = kk | (1u << bit);
-          const double cnt = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, cand, rs.m, cexp, slot);
-          if (cnt >= (double)a.top_k) kk = cand;
-        }
-        const uint32_t gt = (kk == 0xFFFFFFFFu) ? 0u
-            : static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, kk + 1u, rs.m, cexp, slot));
-        ck = static_cast<uint32_t>(a.top_k) - gt;
-        tk = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kk, rs.m, cexp, slot));
-        const float ek = softmax_mass(value_of_key<DT>(kk), rs.m, cexp);
-        zk = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kk, rs.m, cexp, slot) + (double)ck * (double)ek;
-      }
-      uint32_t kstar = kk, cstar = ck, tstar = tk;
-      double zkept = zk;
-      if (topp_on) {
-        const double target = (double)a.top_p * zk;
-        // G(kappa): mass of the top-k set strictly above kappa
-        auto G = [&](uint32_t kappa) -> double {
-          if (topk_on && kappa < kk) return zk;
-          return cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kappa, rs.m, cexp, slot);
-        };
-        uint32_t k0;
-        if (G(0u) < target) {
-          k0 = 0u;
-        } else {
-          uint32_t kp = 0u;
-          for (int bit = kb - 1; bit >= 0; --bit) {
-            const uint32_t cand = kp | (1u << bit);
-            if (G(cand) >= target) kp = cand;
-          }
-          k0 = kp + 1u;
-        }
-        kstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MIN_GE, k0, rs.m, cexp, slot));
-        const double mb = G(kstar);
-        tstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kstar, rs.m, cexp, slot));
-        const uint32_t avail = (topk_on && kstar == kk) ? ck : tstar;
-        const float ep = softmax_mass(value_of_key<DT>(kstar), rs.m, cexp);
-        const double xneed = (target - mb) / (double)ep;
-        uint32_t cp = avail;
-        if (xneed < (double)avail) cp = max(1u, static_cast<uint32_t>(ceil(xneed)));
-        cstar = cp;
-        zkept = mb + (double)cp * (double)ep;
-      }
-      rs.kstar = kstar;
-      rs.cstar = cstar;
-      rs.tie_total = tstar;
-      rs.zkept = zkept;
-      rs.partial = cstar < tstar ? 1 : 0;
-      rs.inv_z = static_cast<float>(1.0 / zkept);
-      rs.thr = H::thr_pack(E::bits_of_key(kstar));
-      __syncthreads();
-      if (tid == 0) sh.rs[r] = rs;
-      __syncthreads();
+      fallback_row<DT, CS>(cluster, sh, r == 0 ? buf[0] : buf[NR - 1], n, nvec, r, a.top_k, a.top_p,
+                           r == 0 ? zfull[0] : zfull[NR - 1], cexp, slot);
     }
   }
 
-  // ------------------- phase 3c: tie ranks, only for rows with a partial tie
-  bool part_any = false;
+  // ------ phase 3c: where a partial tie stops (only rows with a partial tie)
+  bool part_any = false, part_fb = false;
 #pragma unroll
-  for (int r = 0; r < NR; ++r) part_any |= sh.rs[r].partial != 0;
-  uint32_t warp_tie_base[2] = {0u, 0u};
-  if (part_any) {
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      uint32_t c = 0;
-      if (sh.rs[r].partial)
-        for (int v = seg_beg + lane; v < seg_end; v += 32) c += vec_ties<DT>(buf[r][v], v * E::kPerVec, n, sh.rs[r].kstar);
-      c = warp_sum_u32(c);
-      if (lane == 0) sh.w_tie[warp][r] = c;
-    }
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        uint32_t s = 0;
-        for (int w = 0; w < kWarps; ++w) s += sh.w_tie[w][r];
-        sh.x_tie[r] = s;
-      }
-    }
-    cluster.sync();  // --------------------------------------------- sync: ties
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      uint32_t before = 0;
-      for (int q = 0; q < crank; ++q) before += cluster.map_shared_rank(&sh, q)->x_tie[r];
-      uint32_t wb = 0;
-      for (int w = 0; w < warp; ++w) wb += sh.w_tie[w][r];
-      warp_tie_base[r] = before + wb;
-      if (tid == 0) sh.rs[r].ties_before = before;
-    }
-    __syncthreads();
+  for (int r = 0; r < NR; ++r) {
+    part_any |= sh.rs[r].partial != 0;
+    part_fb |= sh.rs[r].partial != 0 && sh.fb_need[r] != 0;
   }
+  if (part_any) tie_cuts<DT, CS, NR>(cluster, sh, buf[0], buf[NR - 1], hist, lo, hi, n, V, part_fb);
   const RowStat rp = sh.rs[0];
   const RowStat rq = sh.rs[NR - 1];
 
   // ----------------------------------------------- MODE_PROBS: write rows
   if (a.mode == MODE_PROBS) {
-    float* out = a.out_probs + static_cast<size_t>(unit) * V + lo;
-    const bool vec_out = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) && (V % 4 == 0);
-    uint32_t run = warp_tie_base[0];
-    for (int it = 0; it < seg_iters; ++it) {
-      const int v = seg_beg + it * 32 + lane;
-      const bool valid = v < seg_end;
-      const int t0 = v * E::kPerVec;
-      const uint4 x = valid ? buf[0][v] : make_uint4(0u, 0u, 0u, 0u);
-      uint32_t base = 0;
-      if (rp.partial) {
-        const uint32_t c = valid ? vec_ties<DT>(x, t0, n, rp.kstar) : 0u;
-        const uint32_t incl = warp_incl_scan_u32(c);
-        base = run + incl - c;
-        run += __shfl_sync(kFull, incl, 31);
-      }
-      if (valid) {
-        float w[8];
-        vec_weights<DT>(x, x, t0, n, false, rp, rp, cexp, base, base, w);
-        if (rp.bad) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[j] = 0.f;
-        }
-        if (vec_out && t0 + E::kPerVec <= n) {
-          reinterpret_cast<float4*>(out + t0)[0] = make_float4(w[0], w[1], w[2], w[3]);
-          if (E::kPerVec == 8) reinterpret_cast<float4*>(out + t0)[1] = make_float4(w[4], w[5], w[6], w[7]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < E::kPerVec; ++j)
-            if (t0 + j < n) out[t0 + j] = w[j];
-        }
-      }
-    }
+    write_probs<DT>(a, buf[0], rp, cexp, unit, lo, n, V);
     if (rp.bad && crank == 0 && tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
     cluster.sync();  // ------------------------------------------- sync: exit
     return;
@@ -827,40 +1388,20 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
         __threadfence();
         if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
       }
-    } else if (x >= lo && x < hi) {
-      if (part_any) {  // tie ranks of x inside this CTA
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          uint32_t c = 0;
-          if (sh.rs[r].partial)
-            for (int t = tid; t < x - lo; t += kThreads) c += (E::key(E::bits_at(buf[r], t)) == sh.rs[r].kstar);
-          c = warp_sum_u32(c);
-          if (lane == 0) sh.w_tie[warp][r] = c;
-        }
-        __syncthreads();
-        if (tid == 0)
-          for (int r = 0; r < 2; ++r) {
-            uint32_t s = sh.rs[r].ties_before;
-            for (int w = 0; w < kWarps; ++w) s += sh.w_tie[w][r];
-            sh.owner_tie[r] = s;
-          }
-        __syncthreads();
-      }
-      if (tid == 0) {
-        const uint32_t bp = E::bits_at(buf[0], x - lo), bq = E::bits_at(buf[1], x - lo);
-        const bool kp = kept_key(rp, E::key(bp), part_any ? sh.owner_tie[0] : 0u);
-        const bool kq2 = kept_key(rq, E::key(bq), part_any ? sh.owner_tie[1] : 0u);
-        const double px = kp ? (double)softmax_mass(E::value(bp), rp.m, cexp) / rp.zkept : 0.0;
-        const double qx = kq2 ? (double)softmax_mass(E::value(bq), rq.m, cexp) / rq.zkept : 0.0;
-        const double u = (double)a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
-        rec->accept = (u * qx < px) ? 1 : 0;
-        rec->px = static_cast<float>(px);
-        rec->qx = static_cast<float>(qx);
-        if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = static_cast<float>(px);
-        if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = static_cast<float>(qx);
-        __threadfence();
-        if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-      }
+    } else if (x >= lo && x < hi && tid == 0) {
+      const uint32_t bp = lds_elem<DT>(buf[0], x - lo), bq = lds_elem<DT>(buf[1], x - lo);
+      const bool kp = kept_key(rp, E::key(bp), x);
+      const bool kq2 = kept_key(rq, E::key(bq), x);
+      const float px = kp ? softmax_mass(E::value(bp), rp.m, cexp) / static_cast<float>(rp.zkept) : 0.f;
+      const float qx = kq2 ? softmax_mass(E::value(bq), rq.m, cexp) / static_cast<float>(rq.zkept) : 0.f;
+      const float u = a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
+      rec->accept = (u * qx < px) ? 1 : 0;
+      rec->px = px;
+      rec->qx = qx;
+      if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
+      if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
+      __threadfence();
+      if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
     }
   }
 
@@ -881,139 +1422,56 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group
   int owner = -1;
   for (int attempt = 0; attempt < 2; ++attempt) {
     float s = 0.f;
-    if (!part_any) {
-      for (int v = seg_beg + lane; v < seg_end; v += 32) {
-        float w[8];
-        s += vec_weights<DT>(buf[0][v], use_q ? buf[NR - 1][v] : buf[0][v], v * E::kPerVec, n, use_q, rp, rq, cexp,
-                             0u, 0u, w);
-      }
-    } else {
-      uint32_t runp = warp_tie_base[0], runq = warp_tie_base[1];
-      for (int it = 0; it < seg_iters; ++it) {
-        const int v = seg_beg + it * 32 + lane;
-        const bool valid = v < seg_end;
-        const int t0 = v * E::kPerVec;
-        const uint4 xp = valid ? buf[0][v] : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 xq = (valid && use_q) ? buf[NR - 1][v] : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t cp = (valid && rp.partial) ? vec_ties<DT>(xp, t0, n, rp.kstar) : 0u;
-        const uint32_t cq = (valid && use_q && rq.partial) ? vec_ties<DT>(xq, t0, n, rq.kstar) : 0u;
-        const uint32_t ip = warp_incl_scan_u32(cp), iq = warp_incl_scan_u32(cq);
-        const uint32_t bp = runp + ip - cp, bq = runq + iq - cq;
-        runp += __shfl_sync(kFull, ip, 31);
-        runq += __shfl_sync(kFull, iq, 31);
-        if (valid) {
-          float w[8];
-          s += vec_weights<DT>(xp, xq, t0, n, use_q, rp, rq, cexp, bp, bq, w);
-        }
-      }
+    for (int v = seg_beg + lane; v < seg_end; v += 32) {
+      float w[8];
+      const uint4 xp = lds128(buf[0] + 16u * v);
+      const uint4 xq = use_q ? lds128(buf[NR - 1] + 16u * v) : xp;
+      s += vec_weights<DT>(xp, xq, v * E::kPerVec, lo, n, use_q, rp, rq, cexp, w);
     }
-    const double ws = warp_sum_f64((double)s);
-    if (lane == 0) sh.w_res[warp] = ws;
+    s = warp_sum_f32(s);
+    if (lane == 0) sh.w_res[warp] = s;
     __syncthreads();
     if (tid == 0) {
       double t = 0.0;
-      for (int w = 0; w < kWarps; ++w) t += sh.w_res[w];
+      for (int w = 0; w < kWarps; ++w) t += (double)sh.w_res[w];
       sh.x_res[attempt] = t;
     }
     cluster.sync();  // ---------------------------------------- sync: residual
-    double mine = 0.0;
-    if (lane < CS) mine = cluster.map_shared_rank(&sh, lane)->x_res[attempt];
-    S = cluster_sum_f64<CS>(mine);
-    if (S > 0.0 || !use_q) {
-      const double target = (double)u_draw * S;
-      double run = 0.0;
+    if (tid == 0) {  // total, owner CTA and its base, in fixed rank order
+      double sc[CS], tot = 0.0, run = 0.0, pc = 0.0;
+      int own = -1;
+#pragma unroll
+      for (int c = 0; c < CS; ++c) sc[c] = cluster.map_shared_rank(&sh, c)->x_res[attempt];
+#pragma unroll
+      for (int c = 0; c < CS; ++c) tot += sc[c];
+      const double target = (double)u_draw * tot;
+#pragma unroll
       for (int c = 0; c < CS; ++c) {
-        const double sc = __shfl_sync(kFull, mine, c);
-        if (owner < 0 && sc > 0.0 && run + sc > target) { owner = c; Pc = run; }
-        run += sc;
+        if (own < 0 && sc[c] > 0.0 && run + sc[c] > target) { own = c; pc = run; }
+        run += sc[c];
       }
+      sh.b_S = tot;
+      sh.b_Pc = pc;
+      sh.b_owner = own;
+    }
+    __syncthreads();
+    S = sh.b_S;
+    if (S > 0.0 || !use_q) {
+      owner = sh.b_owner;
+      Pc = sh.b_Pc;
       break;
     }
     use_q = false;  // degenerate residual: draw from p instead
   }
   cluster.sync();  // ------------------------------------- sync: exit (no DSMEM after this)
 
-  if (owner == crank) {
-    const double target = (double)u_draw * S - Pc;
-    if (tid == 0) {
-      double run = 0.0, wbase = 0.0, lbase = 0.0;
-      int wsel = -1, wlast = -1;
-      for (int w = 0; w < kWarps; ++w) {
-        const double sw = sh.w_res[w];
-        if (sw > 0.0) { wlast = w; lbase = run; }
-        if (wsel < 0 && sw > 0.0 && run + sw > target) { wsel = w; wbase = run; }
-        run += sw;
-      }
-      if (wsel < 0) { wsel = wlast; wbase = lbase; }
-      sh.draw_warp = wsel;
-      sh.draw_base = wbase;
-    }
-    __syncthreads();
-    if (warp == sh.draw_warp) {
-      const float tw = static_cast<float>(target - sh.draw_base);
-      float run = 0.f;
-      int token = -1, last_pos = -1;
-      uint32_t runp = warp_tie_base[0], runq = warp_tie_base[1];
-      for (int it = 0; it < seg_iters && token < 0; ++it) {
-        const int v = seg_beg + it * 32 + lane;
-        const bool valid = v < seg_end;
-        const int t0 = v * E::kPerVec;
-        const uint4 xp = valid ? buf[0][v] : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 xq = (valid && use_q) ? buf[NR - 1][v] : make_uint4(0u, 0u, 0u, 0u);
-        uint32_t bp = 0, bq = 0;
-        if (part_any) {
-          const uint32_t cp = (valid && rp.partial) ? vec_ties<DT>(xp, t0, n, rp.kstar) : 0u;
-          const uint32_t cq = (valid && use_q && rq.partial) ? vec_ties<DT>(xq, t0, n, rq.kstar) : 0u;
-          const uint32_t ip = warp_incl_scan_u32(cp), iq = warp_incl_scan_u32(cq);
-          bp = runp + ip - cp;
-          bq = runq + iq - cq;
-          runp += __shfl_sync(kFull, ip, 31);
-          runq += __shfl_sync(kFull, iq, 31);
-        }
-        float w[8];
-        float ls = 0.f;
-        int lpos = -1;
-        if (valid) {
-          ls = vec_weights<DT>(xp, xq, t0, n, use_q, rp, rq, cexp, bp, bq, w);
-#pragma unroll
-          for (int j = 0; j < E::kPerVec; ++j)
-            if (w[j] > 0.f) lpos = t0 + j;
-        }
-        const float incl = warp_incl_scan(ls);
-        const unsigned ball = __ballot_sync(kFull, valid && ls > 0.f && run + incl > tw);
-        const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
-        const int lp = __shfl_sync(kFull, lpos, lastl);
-        if (lp >= 0) last_pos = lp;
-        if (ball) {
-          const int l = __ffs(ball) - 1;
-          int tok = -1;
-          if (lane == l) {
-            float cum = run + (incl - ls);
-            int lastj = -1;
-#pragma unroll
-            for (int j = 0; j < E::kPerVec; ++j) {
-              if (w[j] > 0.f) lastj = t0 + j;
-              cum += w[j];
-              if (tok < 0 && w[j] > 0.f && cum > tw) tok = t0 + j;
-            }
-            if (tok < 0) tok = lastj;
-          }
-          token = __shfl_sync(kFull, tok, l);
-        }
-        run += __shfl_sync(kFull, incl, 31);
-      }
-      if (token < 0) token = last_pos;  // only reachable through rounding
-      if (lane == 0) {
-        a.recs[unit].drawn = token >= 0 ? lo + token : -1;
-        __threadfence();
-        if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-      }
-    }
-  }
+  if (owner == crank)
+    draw_walk<DT, NR>(a, sh, buf[0], buf[NR - 1], use_q, rp, rq, cexp, (double)u_draw * S - Pc, lo, n, unit, b);
+
 }
 
 template <int DT, int CS>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
   using E = Elt<DT>;
   cg::cluster_group cluster = cg::this_cluster();
   const int unit = static_cast<int>(blockIdx.x) / CS;
