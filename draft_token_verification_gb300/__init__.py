@@ -7,7 +7,7 @@ there is no CPU fallback.
 
 Entry points (same names as the C ABI in include/spec_verify.h):
   spec_verify_sample, spec_verify_greedy, spec_verify_tree_greedy,
-  spec_transform_probs, spec_get_status, spec_verify_workspace_size,
+  spec_verify_sample_noalloc, spec_transform_probs, spec_get_status, spec_verify_workspace_size,
   spec_error_string, spec_expected_tokens, spec_improvement_factor,
   spec_break_even_acceptance
 """
@@ -34,6 +34,7 @@ SPEC_ERR_LAUNCH = -4
 SPEC_ERR_DEVICE_DATA = -5
 SPEC_ERR_TIMEOUT = -6
 SPEC_ERR_UNSUPPORTED = -7
+SPEC_ERR_SCRATCH_LIMIT = -8
 
 SPEC_STATUS_BAD_TOKEN = 1
 SPEC_STATUS_BAD_ROW = 2
@@ -43,11 +44,13 @@ SPEC_STATUS_TIMEOUT = 16
 
 SPEC_MAX_K = 31
 SPEC_MAX_TREE_NODES = 1024
+SPEC_NOALLOC_MAX_B = 2048
+SPEC_NOALLOC_MAX_UNITS = 8192
 
 EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
     "spec_transform_probs", "spec_get_status", "spec_error_string", "spec_expected_tokens",
-    "spec_improvement_factor", "spec_break_even_acceptance",
+    "spec_improvement_factor", "spec_break_even_acceptance", "spec_verify_sample_noalloc",
 )
 
 
@@ -93,6 +96,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_workspace_size.restype = SZ
             L.spec_verify_sample.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, SZ, P]
             L.spec_verify_sample.restype = I
+            L.spec_verify_sample_noalloc.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, P]
+            L.spec_verify_sample_noalloc.restype = I
             L.spec_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, SZ, P]
             L.spec_verify_greedy.restype = I
             L.spec_verify_tree_greedy.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, SZ, P]
@@ -216,6 +221,34 @@ def spec_verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor, 
         _dev(out_q_draft, "out_q_draft"), ws.data_ptr(), ws.numel(), _stream(stream),
     )
     _check(rc, "spec_verify_sample")
+    return out_tokens, out_num_accepted, out_p_draft, out_q_draft
+
+
+def spec_verify_sample_noalloc(target_logits: torch.Tensor, draft_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                               uniforms: torch.Tensor, out_tokens: torch.Tensor, out_num_accepted: torch.Tensor,
+                               out_p_draft: Optional[torch.Tensor] = None, out_q_draft: Optional[torch.Tensor] = None,
+                               out_status: Optional[torch.Tensor] = None, temperature: float = 1.0, top_k: int = 0,
+                               top_p: float = 1.0, temperature_per_seq: Optional[torch.Tensor] = None, stream=None):
+    """spec_verify_sample for callers that cannot allocate device memory.
+
+    The library keeps a fixed scratch array on each device instead of taking
+    a workspace; the caller passes every output (this wrapper creates no
+    tensor).  out_status, if given, is a one-element int32/uint32-sized CUDA
+    tensor that receives this call's status bits.  Calls that overlap on the
+    GPU share the scratch and race.
+    """
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dt = _dtype_code(target_logits)
+    sp = _params(temperature, top_k, top_p, temperature_per_seq)
+    rc = lib().spec_verify_sample_noalloc(
+        _dev(target_logits, "target_logits"), _dev(draft_logits, "draft_logits", target_logits.dtype),
+        _dev(draft_tokens, "draft_tokens", torch.int32), _dev(uniforms, "uniforms", torch.float32),
+        B, k, V, dt, ctypes.byref(sp), _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(out_num_accepted, "out_num_accepted", torch.int32), _dev(out_p_draft, "out_p_draft", torch.float32),
+        _dev(out_q_draft, "out_q_draft", torch.float32), _dev(out_status, "out_status"), _stream(stream),
+    )
+    _check(rc, "spec_verify_sample_noalloc")
     return out_tokens, out_num_accepted, out_p_draft, out_q_draft
 
 

@@ -6,6 +6,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 using namespace specv;
@@ -118,6 +120,43 @@ int argmax_split_len(int rows, int V) {
   return static_cast<int>(len);
 }
 
+// ------------------------------------------------ allocation-free sampling
+// Fixed scratch for spec_verify_sample_noalloc: the workspace layout of the
+// largest shape it accepts (status word, per-sequence tickets, unit records,
+// plus the argmax slots the layout reserves).  Every GPU that loads the
+// library holds one copy until the process exits.
+constexpr size_t kNoAllocBytes = 256 + sizeof(uint32_t) * SPEC_NOALLOC_MAX_B +
+                                 (sizeof(UnitRec) + sizeof(uint64_t)) * SPEC_NOALLOC_MAX_UNITS +
+                                 sizeof(uint32_t) * SPEC_NOALLOC_MAX_B;
+constexpr int kNoAllocMaxDevices = 64;
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+// In host code this name stands for the array only as a handle for the
+// runtime; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(unsigned char** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ERR_LAUNCH;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_noalloc_ptr[dev]);
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -135,6 +174,35 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, cons
   return run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                     out_num_accepted, out_p_draft, out_q_draft, nullptr, workspace, workspace_bytes, cuda_stream,
                     MODE_SAMPLE);
+}
+
+int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                               const float* uniforms, int B, int k, int V, spec_dtype dtype,
+                               const spec_sampling_params* params, int32_t* out_tokens, int32_t* out_num_accepted,
+                               float* out_p_draft, float* out_q_draft, uint32_t* out_status, void* cuda_stream) {
+  if (B < 1 || k < 1 || k > SPEC_MAX_K) return SPEC_ERR_INVALID_ARG;
+  if (B > SPEC_NOALLOC_MAX_B || static_cast<long long>(B) * (k + 1) > SPEC_NOALLOC_MAX_UNITS)
+    return SPEC_ERR_SCRATCH_LIMIT;
+  const WsLayout L = ws_layout(B, k);
+  if (L.total > kNoAllocBytes) return SPEC_ERR_SCRATCH_LIMIT;
+  if (out_status && !aligned_to(out_status, sizeof(uint32_t))) return SPEC_ERR_INVALID_ARG;
+  unsigned char* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // The array keeps whatever the previous call left: the status word, the
+  // per-sequence tickets and the unit records must start at zero.
+  if (cudaMemsetAsync(scratch, 0, L.s_recs + sizeof(UnitRec) * static_cast<size_t>(B) * (k + 1), st) !=
+      cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  rc = run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
+                  out_num_accepted, out_p_draft, out_q_draft, nullptr, scratch, kNoAllocBytes, cuda_stream,
+                  MODE_SAMPLE);
+  if (rc != SPEC_OK) return rc;
+  if (out_status && cudaMemcpyAsync(out_status, scratch + L.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                                    st) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
 }
 
 int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype, const spec_sampling_params* params,
@@ -233,6 +301,8 @@ const char* spec_error_string(int code) {
     case SPEC_ERR_DEVICE_DATA: return "device found invalid data (see status bits)";
     case SPEC_ERR_TIMEOUT: return "a bounded device wait gave up";
     case SPEC_ERR_UNSUPPORTED: return "shape beyond the library's limits";
+    case SPEC_ERR_SCRATCH_LIMIT:
+      return "B > 2048 or B*(k+1) > 8192: beyond the fixed scratch of spec_verify_sample_noalloc";
     default: return "unknown error code";
   }
 }

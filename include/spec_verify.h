@@ -58,6 +58,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_ERR_DEVICE_DATA (-5)  /* spec_get_status found a status bit set    */
 #define SPEC_ERR_TIMEOUT (-6)      /* a bounded device wait gave up             */
 #define SPEC_ERR_UNSUPPORTED (-7)  /* shape beyond the library's limits         */
+#define SPEC_ERR_SCRATCH_LIMIT (-8) /* B or B*(k+1) beyond the fixed scratch of
+                                       spec_verify_sample_noalloc              */
 
 /* Status bits written by the device (bitwise OR, sticky until read). */
 #define SPEC_STATUS_BAD_TOKEN 1u   /* a draft token outside [0, V): rejected    */
@@ -186,6 +188,43 @@ int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype,
  * SPEC_ERR_DEVICE_DATA if one was, SPEC_ERR_LAUNCH if the copy failed.
  */
 int spec_get_status(void* workspace, uint32_t* status, void* cuda_stream);
+
+/*
+ * spec_verify_sample without a workspace: allocates nothing.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot obtain device memory for a workspace.  Examples: a serving
+ * process whose memory manager reserved nearly all of HBM for its KV-cache
+ * pool at start-up and treats any other cudaMalloc as an error; code
+ * embedded in another runtime that forbids allocating outside that
+ * runtime's own allocator; a decode loop that cannot afford the implicit
+ * device-wide synchronisation that cudaFree performs.
+ *
+ * Arguments, layouts, results and data-error behaviour are those of
+ * spec_verify_sample, except that there is no workspace and:
+ *   out_status  [1] uint32 device pointer or NULL: receives the status bits
+ *               (SPEC_STATUS_*) of this call only.
+ * Limits: B <= SPEC_NOALLOC_MAX_B and B*(k+1) <= SPEC_NOALLOC_MAX_UNITS;
+ * larger shapes return SPEC_ERR_SCRATCH_LIMIT before anything is launched.
+ *
+ * Scratch: a fixed 208.25 KiB array in the library's device memory, held on
+ * every GPU that loads the library until the process exits.  The first call
+ * on a device (with that device current) looks up the array's device
+ * address; make that first call before any stream capture.  Every call
+ * clears the part of the array it uses (cudaMemsetAsync on cuda_stream),
+ * then launches the kernel; no call allocates or frees memory.  All calls
+ * on one device share the one array: two calls whose work overlaps on the
+ * GPU (different streams, no ordering between them) race and give wrong
+ * results.  Calls on one stream are ordered and safe.
+ */
+#define SPEC_NOALLOC_MAX_B 2048
+#define SPEC_NOALLOC_MAX_UNITS 8192
+int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                               const int32_t* draft_tokens, const float* uniforms, int B,
+                               int k, int V, spec_dtype dtype,
+                               const spec_sampling_params* params, int32_t* out_tokens,
+                               int32_t* out_num_accepted, float* out_p_draft,
+                               float* out_q_draft, uint32_t* out_status, void* cuda_stream);
 
 /* Static description of a return code. */
 const char* spec_error_string(int code);
