@@ -14,8 +14,6 @@ using namespace specv;
 
 namespace {
 
-constexpr int kChunkTarget = 16384;  // elements per CTA slice of a sampling row
-
 bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 size_t elt_bytes(spec_dtype d) { return d == SPEC_BF16 ? 2 : 4; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -31,18 +29,6 @@ int check_workspace(void* ws, size_t bytes, int B, int k) {
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_WORKSPACE;
   if (bytes < ws_layout(B, k).total) return SPEC_ERR_WORKSPACE;
   return SPEC_OK;
-}
-
-// Cluster size and per-CTA slice for a sampling row of V elements.
-bool sample_shape(int V, spec_dtype d, bool filter, int* cluster, int* chunk) {
-  int cs = 1;
-  while (cs < 8 && (V + cs - 1) / cs > kChunkTarget) cs *= 2;
-  int ch = ((V + cs - 1) / cs + 7) / 8 * 8;
-  const size_t smem = sample_smem_bytes(d == SPEC_BF16 ? DT_BF16 : DT_F32, ch, filter);
-  if (smem > 200 * 1024) return false;
-  *cluster = cs;
-  *chunk = ch;
-  return true;
 }
 
 int run_sample(const void* target, const void* draft, const int32_t* tokens, const float* uniforms, int B, int k,
@@ -90,10 +76,8 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.aligned_target = rows_aligned(target, V, dtype);
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
-  int cluster = 1;
-  if (!sample_shape(V, dtype, a.top_k > 0 || a.top_p < 1.f, &cluster, &a.chunk)) return SPEC_ERR_UNSUPPORTED;
   const int units = mode == MODE_SAMPLE ? B * (k + 1) : B;
-  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, cluster, units, stream);
+  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, units, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }

@@ -15,7 +15,6 @@ constexpr int DT_BF16 = 1;
 constexpr int kThreads = 256;           // threads per CTA in every kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kWindow = 512;            // exact-value histogram bins per row
-constexpr int kBinThreads = kWindow / 4; // threads that own four bins each
 constexpr int kMaxK = 31;
 constexpr int kMaxTreeNodes = 1024;
 
@@ -75,7 +74,6 @@ struct SampleArgs {
   uint32_t* status;
   uint32_t* tickets;
   UnitRec* recs;
-  int chunk;                   // elements per CTA, multiple of 8
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;
@@ -99,8 +97,8 @@ struct ArgmaxArgs {
 };
 
 // Launchers (return a cudaError_t as int).
-int launch_sample(const SampleArgs& a, int dtype, int cluster, int units, void* stream);
+int launch_sample(const SampleArgs& a, int dtype, int units, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
-size_t sample_smem_bytes(int dtype, int chunk, bool filter);
+size_t sample_smem_bytes(int dtype, bool filter);
 
 }  // namespace specv

@@ -8,26 +8,30 @@
 // p_i(x_i); at the first rejection n one token is drawn from
 // max(0, p_n - q_n) with u_{k+1}, else a bonus token from p_k with u_k.
 //
-// How (one GPU, memory-bound): a thread-block cluster of CS CTAs owns one
-// unit (b, i).  Each CTA bulk-copies (TMA, cp.async.bulk) its 1/CS slice of
-// the target row and of the draft row into shared memory, so every logit is
-// read from HBM exactly once.  Row statistics are combined across the
-// cluster through distributed shared memory:
-//   1. the row maximum (packed bf16x2 max over shared memory);
-//   2. the sum of masses exp((l - m) / T) (packed f32x2 arithmetic), when a
-//      top-p cut needs it;
-//   3. for a top-k / top-p cut, a histogram of exact values counting only
-//      the tokens that can survive the cut (at most 1024 distinct values
-//      below the maximum; with top-p only, also no token whose mass is below
-//      (1 - top_p) * Z / V, which cannot be kept); bin masses are count x
-//      mass, so the cut, its tie count and the kept normaliser come from a
-//      short scan over the bins.  A cut outside the histogram (flat rows,
-//      fp32 rows) falls back to an exact bitwise search over the keys.
-// The accept test is done by the CTA that holds x_i; the residual (or bonus)
-// inverse-CDF draw is done speculatively for every unit, so no row is read
-// twice; vectors with no kept token are skipped with one packed compare.  The
-// CTA that holds the drawn token writes it.  The last writer of a sequence
-// (atomic ticket, no spin-wait) applies the first-rejection rule and commits.
+// How (one GPU, memory-bound).  One CTA owns one unit (b, i) and streams its
+// target row and draft row from HBM exactly once, 16-byte loads by warp
+// segments in index order.  While streaming, for each row:
+//   - masses are taken on a power-of-two lattice: with c = log2(e) / T and
+//     an integer k_t >= max(l) * c held per thread, mass(l) = 2^(l c - k_t)
+//     (one packed f32x2 fma and one ex2 per element).  Raising k_t rescales
+//     the running sum by an exact power of two, so the row sum
+//     Z = sum 2^(l c - K) (K the CTA-wide k) carries no rescaling error;
+//     2^(l c - K) / Z is the softmax of l / T.
+//   - every element within kTheta octaves of mass of the running maximum is
+//     appended to its warp's candidate list (index order; entries below the
+//     current bound are purged when a list fills).  A top-k / top-p cut
+//     within kTheta octaves of the maximum is therefore decided from the
+//     lists alone: a histogram of exact values, a four-warp scan for the cut,
+//     its tie count and the kept normaliser.  Rows whose cut lies deeper
+//     (flat rows), fp32 rows and overflowing lists take an exact bitwise
+//     search over the keys that re-reads the row.
+// The accept test reads p(x_i), q(x_i) at x_i.  The residual max(0, p - q)
+// (or the bonus p) is non-zero only on the kept set of p, which the lists
+// hold in index order: per-warp sums, a prefix over warps and a walk of one
+// list give the drawn token.  Every unit draws (the residual draw is
+// speculative), so no row is read twice on the fast path.  The last writer
+// of a sequence (atomic ticket, no spin-wait) applies the first-rejection
+// rule and commits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -43,6 +47,14 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 using u64 = unsigned long long;
 
+constexpr int kListCap = 800;                       // candidate entries per warp per row
+constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
+constexpr float kTheta = 13.f;                      // octaves of mass kept as candidates
+constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
+constexpr int kGroups = kWindow / 4;                // aligned groups of four keys
+constexpr int kScanWarps = 4;                       // warps that scan one row's histogram
+constexpr int kSegBits = 16;                        // element index within a warp segment
+
 // ------------------------------------------------------- packed f32x2 math
 
 __device__ __forceinline__ u64 pk2(uint32_t x, uint32_t y) {
@@ -54,9 +66,9 @@ __device__ __forceinline__ u64 pkf(float x, float y) { return pk2(__float_as_uin
 __device__ __forceinline__ void upk(u64 r, float& x, float& y) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
 }
-__device__ __forceinline__ u64 sub2(u64 a, u64 b) {
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
   u64 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ u64 mul2(u64 a, u64 b) {
@@ -64,17 +76,20 @@ __device__ __forceinline__ u64 mul2(u64 a, u64 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
   u64 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-// 2^x for both halves: the masses of two elements, (l - m) * log2(e) / T
-__device__ __forceinline__ u64 mass2(u64 l2, u64 m2, u64 c2) {
+// 2^(l c - k) for both halves: the lattice masses of two elements
+__device__ __forceinline__ u64 lat2(u64 l2, u64 c2, u64 nk2) {
   float x, y;
-  upk(mul2(sub2(l2, m2), c2), x, y);
+  upk(fma2(l2, c2, nk2), x, y);
   return pkf(ex2_approx(x), ex2_approx(y));
 }
+// The lattice mass of one value: every mass of the kernel goes through this
+// function or lat2 (same fma, same ex2), so they agree bit for bit.
+__device__ __forceinline__ float lat_mass(float l, float c, float k) { return ex2_approx(fmaf(l, c, -k)); }
 
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
@@ -86,6 +101,23 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_max_i32(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// 2^d for an integer d, exact (0 below the normal range).
+__device__ __forceinline__ float exp2i(int d) {
+  return d < -126 ? 0.f : __int_as_float((127 + min(d, 127)) << 23);
 }
 
 // Double-float: an unevaluated sum hi + lo of two floats (about 48 bits),
@@ -106,11 +138,11 @@ __device__ __forceinline__ DF df_add(DF a, float b) {
   return DF{h, e - (h - s)};
 }
 __device__ __forceinline__ DF df_add2(DF a, DF b) { return df_add(df_add(a, b.hi), b.lo); }
+__device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
 __device__ __forceinline__ DF df_shfl_up(DF a, int o) {
   return DF{__shfl_up_sync(kFull, a.hi, o), __shfl_up_sync(kFull, a.lo, o)};
 }
 __device__ __forceinline__ DF df_shfl(DF a, int l) { return DF{__shfl_sync(kFull, a.hi, l), __shfl_sync(kFull, a.lo, l)}; }
-// inclusive warp prefix sum of double-floats
 __device__ __forceinline__ DF warp_incl_scan_df(DF v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -120,15 +152,16 @@ __device__ __forceinline__ DF warp_incl_scan_df(DF v) {
   }
   return v;
 }
-// (a - b) rounded to float
-__device__ __forceinline__ float df_diff(DF a, DF b) { return (a.hi - b.hi) + (a.lo - b.lo); }
-__device__ __forceinline__ double df_value(DF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
-
-__device__ __forceinline__ float warp_max_nan(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(kFull, v, o));
-  return v;
+// a * b for a double-float and a float
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const float p = a.hi * b;
+  const float e = fmaf(a.hi, b, -p) + a.lo * b;
+  const float h = p + e;
+  return DF{h, e - (h - p)};
 }
+__device__ __forceinline__ bool df_lt(DF a, DF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ float df_float(DF a) { return a.hi + a.lo; }
+__device__ __forceinline__ double df_double(DF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
 
 // ------------------------------------------------- per-dtype vector kernels
 
@@ -137,35 +170,23 @@ struct Hot;
 
 template <>
 struct Hot<DT_BF16> {
-  using E = Elt<DT_BF16>;
-  struct MaxAcc {
-    __nv_bfloat162 a;
-  };
   __device__ static __forceinline__ __nv_bfloat162 b2(uint32_t w) {
     __nv_bfloat162 r;
     *reinterpret_cast<uint32_t*>(&r) = w;
     return r;
   }
-  __device__ static __forceinline__ void max_init(MaxAcc& s) { s.a = b2(0xFF80FF80u); }
-  __device__ static __forceinline__ void max_vec(const uint4& v, MaxAcc& s) {
-    s.a = __hmax2_nan(__hmax2_nan(s.a, b2(v.x)), __hmax2_nan(b2(v.y), __hmax2_nan(b2(v.z), b2(v.w))));
+  static constexpr uint32_t kPad = 0xFF80FF80u;  // -inf, -inf
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(b2(v.x), b2(v.y)), __hmax2_nan(b2(v.z), b2(v.w)));
+    return max_nan(__low2float(m), __high2float(m));
   }
-  __device__ static __forceinline__ float max_finish(const MaxAcc& s) {
-    return max_nan(__low2float(s.a), __high2float(s.a));
+  __device__ static __forceinline__ void mass_vec(const uint4& v, u64 c2, u64 nk2, u64& acc0, u64& acc1) {
+    acc0 = add2(acc0, lat2(pk2(v.x << 16, v.x & 0xFFFF0000u), c2, nk2));
+    acc1 = add2(acc1, lat2(pk2(v.y << 16, v.y & 0xFFFF0000u), c2, nk2));
+    acc0 = add2(acc0, lat2(pk2(v.z << 16, v.z & 0xFFFF0000u), c2, nk2));
+    acc1 = add2(acc1, lat2(pk2(v.w << 16, v.w & 0xFFFF0000u), c2, nk2));
   }
-  // accumulate the masses of the 8 elements into acc (two running sums)
-  __device__ static __forceinline__ void mass_vec(const uint4& v, u64 m2, u64 c2, u64& acc) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc = add2(acc, mass2(pk2(w[i] << 16, w[i] & 0xFFFF0000u), m2, c2));
-  }
-  // threshold as a packed pair of one bf16 value
   __device__ static __forceinline__ uint32_t thr_pack(uint32_t bits) { return bits | (bits << 16); }
-  __device__ static __forceinline__ bool any_ge(const uint4& v, uint32_t thr) {
-    const __nv_bfloat162 t = b2(thr);
-    return (__hge2_mask(b2(v.x), t) | __hge2_mask(b2(v.y), t) | __hge2_mask(b2(v.z), t) |
-            __hge2_mask(b2(v.w), t)) != 0u;
-  }
   __device__ static __forceinline__ uint32_t mask_ge(const uint4& v, uint32_t thr) {
     const __nv_bfloat162 t = b2(thr);
     const uint32_t m0 = __hge2_mask(b2(v.x), t), m1 = __hge2_mask(b2(v.y), t);
@@ -173,7 +194,6 @@ struct Hot<DT_BF16> {
     return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
            ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
   }
-  // bit j set iff element j equals the threshold value (-0 == +0)
   __device__ static __forceinline__ uint32_t mask_eq(const uint4& v, uint32_t thr) {
     const __nv_bfloat162 t = b2(thr);
     const uint32_t m0 = __heq2_mask(b2(v.x), t), m1 = __heq2_mask(b2(v.y), t);
@@ -181,35 +201,20 @@ struct Hot<DT_BF16> {
     return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
            ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
   }
-  __device__ static __forceinline__ bool any_eq(const uint4& v, uint32_t thr) {
-    const __nv_bfloat162 t = b2(thr);
-    return (__heq2_mask(b2(v.x), t) | __heq2_mask(b2(v.y), t) | __heq2_mask(b2(v.z), t) |
-            __heq2_mask(b2(v.w), t)) != 0u;
-  }
 };
 
 template <>
 struct Hot<DT_F32> {
-  using E = Elt<DT_F32>;
-  struct MaxAcc {
-    float a;
-  };
-  __device__ static __forceinline__ void max_init(MaxAcc& s) { s.a = -INFINITY; }
-  __device__ static __forceinline__ void max_vec(const uint4& v, MaxAcc& s) {
-    s.a = max_nan(max_nan(s.a, __uint_as_float(v.x)),
-                  max_nan(__uint_as_float(v.y), max_nan(__uint_as_float(v.z), __uint_as_float(v.w))));
+  static constexpr uint32_t kPad = 0xFF800000u;
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    return max_nan(max_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                   max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
-  __device__ static __forceinline__ float max_finish(const MaxAcc& s) { return s.a; }
-  __device__ static __forceinline__ void mass_vec(const uint4& v, u64 m2, u64 c2, u64& acc) {
-    acc = add2(acc, mass2(pk2(v.x, v.y), m2, c2));
-    acc = add2(acc, mass2(pk2(v.z, v.w), m2, c2));
+  __device__ static __forceinline__ void mass_vec(const uint4& v, u64 c2, u64 nk2, u64& acc0, u64& acc1) {
+    acc0 = add2(acc0, lat2(pk2(v.x, v.y), c2, nk2));
+    acc1 = add2(acc1, lat2(pk2(v.z, v.w), c2, nk2));
   }
   __device__ static __forceinline__ uint32_t thr_pack(uint32_t bits) { return bits; }
-  __device__ static __forceinline__ bool any_ge(const uint4& v, uint32_t thr) {
-    const float t = __uint_as_float(thr);
-    return (__uint_as_float(v.x) >= t) | (__uint_as_float(v.y) >= t) | (__uint_as_float(v.z) >= t) |
-           (__uint_as_float(v.w) >= t);
-  }
   __device__ static __forceinline__ uint32_t mask_ge(const uint4& v, uint32_t thr) {
     const float t = __uint_as_float(thr);
     return (__uint_as_float(v.x) >= t ? 1u : 0u) | (__uint_as_float(v.y) >= t ? 2u : 0u) |
@@ -220,465 +225,29 @@ struct Hot<DT_F32> {
     return (__uint_as_float(v.x) == t ? 1u : 0u) | (__uint_as_float(v.y) == t ? 2u : 0u) |
            (__uint_as_float(v.z) == t ? 4u : 0u) | (__uint_as_float(v.w) == t ? 8u : 0u);
   }
-  __device__ static __forceinline__ bool any_eq(const uint4& v, uint32_t thr) { return mask_eq(v, thr) != 0u; }
 };
 
 // ------------------------------------------------------------ row state
-
-struct RowStat {
-  float m;               // row maximum
-  uint32_t kmax;         // key of m
-  uint32_t kstar;        // kept iff key > kstar, or key == kstar and (not partial or index < tie_cut)
-  uint32_t cstar;        // kept tokens of value kstar: the lowest-index ones
-  uint32_t tie_total;    // tokens of value kstar in the row
-  int tie_cut;           // partial rows: index of the first kstar-valued token that is not kept
-  uint32_t thr;          // packed value of kstar (quick skips, equality tests)
-  double zkept;          // sum of masses over the kept set
-  float inv_z;
-  int all_kept;
-  int bad;
-  int partial;           // cstar < tie_total
-};
-
-struct Shm {
-  // exchange slots, read by the other CTAs of the cluster
-  float x_max[2];
-  double x_sum[2];
-  uint32_t x_tie[2];
-  double x_res[2];
-  double x_pm[2];
-  uint32_t x_pc[2];
-  uint32_t x_pk[2];
-  // CTA scratch
-  float w_max[kWarps][2];
-  float w_sum[kWarps][2];
-  float w_res[kWarps];
-  uint32_t w_u[kWarps];
-  float w_f[kWarps];
-  uint32_t w_tie[kWarps][2];
-  double w_pm[kWarps];
-  uint32_t w_pc[kWarps];
-  uint32_t w_pk[kWarps];
-  double b_zfull[2];
-  double b_S, b_Pc;
-  int b_owner;
-  uint32_t b_dlb[2];
-  int c_found;
-  uint32_t c_d, c_c, c_t;
-  double c_z;
-  uint32_t tie_before[2], tie_local[2];
-  uint32_t pc[2][kBinThreads];  // per-thread count of its four histogram bins
-  float pm[2][kBinThreads];     // per-thread mass of its four histogram bins
-  int tie_cut[2];
-  int tie_warp[2];
-  uint32_t tie_j[2];
-  uint32_t fb_need[2];
-  int draw_warp;
-  double draw_base;
-  RowStat rs[2];
-  alignas(8) uint64_t mbar;
-};
 
 template <int DT>
 __device__ __forceinline__ float value_of_key(uint32_t k) {
   return Elt<DT>::value(Elt<DT>::bits_of_key(k));
 }
-
-// Fixed-order sum of one double per cluster rank (lane c holds rank c's).
-template <int CS>
-__device__ __forceinline__ double cluster_sum_f64(double mine_lane_c) {
-  double z = 0.0;
-#pragma unroll
-  for (int c = 0; c < CS; ++c) z += __shfl_sync(kFull, mine_lane_c, c);
-  return z;
-}
-
-// One element of a shared-memory row buffer.
 template <int DT>
-__device__ __forceinline__ uint32_t lds_elem(uint32_t base, int t) {
-  return DT == DT_BF16 ? lds_u16(base + 2u * static_cast<uint32_t>(t)) : lds_u32(base + 4u * static_cast<uint32_t>(t));
+__device__ __forceinline__ uint32_t key_of_float(float v) {
+  const uint32_t b = (Elt<DT>::kBytes == 2) ? (__float_as_uint(v) >> 16) : __float_as_uint(v);
+  return Elt<DT>::key(b);
 }
-
-// Kept test for the element of index t (whole-row index) with the given key.
-__device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, int t) {
-  if (rs.all_kept) return true;
-  if (key > rs.kstar) return true;
-  return key == rs.kstar && (!rs.partial || t < rs.tie_cut);
-}
-
-// Bit j set for the elements of vector v (CTA-local) that lie inside the slice.
+// Smallest bf16 / fp32 value not below v (v finite), as bits.
 template <int DT>
-__device__ __forceinline__ uint32_t valid_mask(int v, int n) {
-  const int left = n - v * Elt<DT>::kPerVec;
-  return left >= Elt<DT>::kPerVec ? (1u << Elt<DT>::kPerVec) - 1u : (left > 0 ? (1u << left) - 1u : 0u);
+__device__ __forceinline__ uint32_t bits_round_up(float v) {
+  const uint32_t u = __float_as_uint(v);
+  if (DT == DT_F32) return u;
+  const uint32_t hi = u >> 16;
+  if ((u & 0xFFFFu) == 0u) return hi;
+  return (u & 0x80000000u) ? hi : hi + 1u;  // negative: toward zero is up
 }
-
-// Draw weights of the elements of one 16-byte vector: w = max(0, p - q)
-// (residual) or w = p (bonus).  t0 is the vector's first CTA-local element,
-// lo the slice start.  Vectors with no element at or above the target's cut
-// value are skipped with one packed compare.
-template <int DT>
-__device__ __forceinline__ float vec_weights(const uint4& xp, const uint4& xq, int t0, int lo, int n, bool use_q,
-                                             const RowStat& rp, const RowStat& rq, float cexp, float* w) {
-  using E = Elt<DT>;
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < E::kPerVec; ++j) w[j] = 0.f;
-  if (!rp.all_kept && !Hot<DT>::any_ge(xp, rp.thr)) return 0.f;
-#pragma unroll
-  for (int j = 0; j < E::kPerVec; ++j) {
-    if (t0 + j < n) {
-      const int t = lo + t0 + j;
-      const uint32_t bp = E::bits_of(xp, j);
-      float pv = 0.f;
-      if (kept_key(rp, E::key(bp), t)) pv = softmax_mass(E::value(bp), rp.m, cexp) * rp.inv_z;
-      if (use_q) {
-        const uint32_t bq = E::bits_of(xq, j);
-        float qv = 0.f;
-        if (kept_key(rq, E::key(bq), t)) qv = softmax_mass(E::value(bq), rq.m, cexp) * rq.inv_z;
-        w[j] = fmaxf(pv - qv, 0.f);
-      } else {
-        w[j] = pv;
-      }
-      s += w[j];
-    }
-  }
-  return s;
-}
-
-// ------------------------------------------------------ CTA-wide scans
-
-// Exclusive prefix (thread order) of a u32 over the CTA; `total` gets the sum.
-__device__ __forceinline__ uint32_t block_excl_u32(uint32_t v, uint32_t* wtmp, uint32_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t incl = warp_incl_scan_u32(v);
-  if (lane == 31) wtmp[warp] = incl;
-  __syncthreads();
-  uint32_t off = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const uint32_t x = wtmp[w];
-    if (w < warp) off += x;
-    tot += x;
-  }
-  __syncthreads();
-  total = tot;
-  return off + incl - v;
-}
-
-// Exclusive prefix (thread order) of a float over the CTA, as a double-float.
-__device__ __forceinline__ DF block_excl_f32(float v, float* wtmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float incl = warp_incl_scan(v);
-  if (lane == 31) wtmp[warp] = incl;
-  __syncthreads();
-  DF off{0.f, 0.f};
-  for (int w = 0; w < warp; ++w) off = df_add(off, wtmp[w]);
-  __syncthreads();
-  return df_add(off, incl - v);
-}
-
-// Smallest thread index whose flag is set, or -1.
-__device__ __forceinline__ int block_first(bool f, uint32_t* wtmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned ball = __ballot_sync(kFull, f);
-  if (lane == 0) wtmp[warp] = ball ? static_cast<uint32_t>(warp * 32 + __ffs(ball) - 1) : 0xFFFFFFFFu;
-  __syncthreads();
-  uint32_t first = 0xFFFFFFFFu;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) first = min(first, wtmp[w]);
-  __syncthreads();
-  return first == 0xFFFFFFFFu ? -1 : static_cast<int>(first);
-}
-
-// Sum over the cluster of bins 4t .. 4t+3 of one row's histogram (hrow: the
-// shared-window address of this CTA's copy).
-template <int CS>
-__device__ __forceinline__ uint4 cluster_bins4(uint32_t hrow, int t) {
-  uint4 part[CS];
-#pragma unroll
-  for (int c = 0; c < CS; ++c) part[c] = ld_cluster_v4(mapa_shared(hrow + 16u * static_cast<uint32_t>(t), c));
-  uint4 s = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-  for (int c = 0; c < CS; ++c) {
-    s.x += part[c].x;
-    s.y += part[c].y;
-    s.z += part[c].z;
-    s.w += part[c].w;
-  }
-  return s;
-}
-
-__device__ __forceinline__ uint32_t u4_at(const uint4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
-// Stage 1 of the cut (all threads): thread t publishes the cluster-wide count
-// and mass of its four bins 4t .. 4t+3 (bin d: tokens of value key kmax - d).
-template <int DT, int CS>
-__device__ __forceinline__ void bins_partials(Shm& sh, int r, uint32_t hrow, int nbins, uint32_t kmax, float m,
-                                              float cexp) {
-  const int t = threadIdx.x;
-  if (t >= kBinThreads) return;
-  uint32_t C = 0u;
-  float M = 0.f;
-  if (4 * t < nbins) {
-    const uint4 b = cluster_bins4<CS>(hrow, t);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int d = 4 * t + i;
-      const uint32_t c = d < nbins ? u4_at(b, i) : 0u;
-      if (c) {
-        C += c;
-        M += static_cast<float>(c) * softmax_mass(value_of_key<DT>(kmax - static_cast<uint32_t>(d)), m, cexp);
-      }
-    }
-  }
-  sh.pc[r][t] = C;
-  sh.pm[r][t] = M;
-}
-
-// Stage 2 of the cut (one warp per row).  Top-k: the bin where the running
-// count reaches top_k (exact, integer); its tokens kept are the
-// top_k - (count before) lowest-index ones.  Top-p (on the top-k set if
-// any): the first bin where the running mass reaches top_p * Z_k; a token of
-// that value is kept while the mass ranked before it stays below the
-// target.  Lane l scans bin threads 4l .. 4l+3; the thread holding the crossing
-// re-reads its four bins.  Returns false if the cut lies beyond the counted
-// bins (the exact fallback then takes over).
-template <int DT, int CS>
-__device__ __noinline__ bool cut_scan_warp(Shm& sh, int r, uint32_t hrow, int nbins, RowStat& rs, int top_k, float top_p,
-                              double zfull, float cexp) {
-  const int lane = threadIdx.x & 31;
-  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
-  const uint32_t K = static_cast<uint32_t>(top_k);
-  uint32_t dk = 0xFFFFFFFFu, ck = 0u, tk = 0u;
-  int tkthr = kThreads;  // thread holding the top-k bin
-  double zk = zfull;
-  if (topk_on) {
-    constexpr int kL = kBinThreads / 32;  // bin threads per lane
-    uint32_t lc[kL], C = 0u;
-    DF M{0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kL; ++i) {
-      lc[i] = sh.pc[r][kL * lane + i];
-      C += lc[i];
-      M = df_add(M, sh.pm[r][kL * lane + i]);
-    }
-    const uint32_t incl = warp_incl_scan_u32(C);
-    const DF Mi = warp_incl_scan_df(M);
-    const unsigned ball = __ballot_sync(kFull, incl - C < K && incl >= K);
-    if (!ball) return false;
-    const int L = __ffs(ball) - 1;
-    uint32_t o_d = 0u, o_c = 0u, o_t = 0u;
-    int o_thr = 0;
-    double o_z = 0.0;
-    if (lane == L) {
-      uint32_t run = incl - C;
-      DF mrun = df_add(Mi, -M.hi);
-      mrun = df_add(mrun, -M.lo);
-      int t = kL * L;
-#pragma unroll
-      for (int i = 0; i < kL; ++i) {
-        if (run + lc[i] >= K) { t = kL * L + i; break; }
-        run += lc[i];
-        mrun = df_add(mrun, sh.pm[r][kL * L + i]);
-      }
-      const uint4 b = cluster_bins4<CS>(hrow, t);
-      for (int j = 0; j < 4; ++j) {
-        const int d = 4 * t + j;
-        const uint32_t c = d < nbins ? u4_at(b, j) : 0u;
-        const float e = c ? softmax_mass(value_of_key<DT>(rs.kmax - static_cast<uint32_t>(d)), rs.m, cexp) : 0.f;
-        if (run + c >= K) {
-          o_d = static_cast<uint32_t>(d);
-          o_c = K - run;
-          o_t = c;
-          o_thr = t;
-          o_z = df_value(mrun) + (double)(K - run) * (double)e;
-          break;
-        }
-        run += c;
-        mrun = df_add(mrun, static_cast<float>(c) * e);
-      }
-    }
-    dk = __shfl_sync(kFull, o_d, L);
-    ck = __shfl_sync(kFull, o_c, L);
-    tk = __shfl_sync(kFull, o_t, L);
-    tkthr = __shfl_sync(kFull, o_thr, L);
-    zk = __shfl_sync(kFull, o_z, L);
-  }
-  uint32_t dstar = dk, cstar = ck, tstar = tk;
-  double zkept = zk;
-  if (topp_on) {
-    const DF tdf = df_from((double)top_p * zk);
-    // lane masses over the top-k set: threads past the top-k bin hold nothing,
-    // the thread holding it only its bins up to dk (with ck tokens at dk)
-    constexpr int kL = kBinThreads / 32;
-    DF M{0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kL; ++i) {
-      const int t = kL * lane + i;
-      if (t < tkthr) M = df_add(M, sh.pm[r][t]);
-    }
-    if (topk_on && tkthr / kL == lane) {
-      const uint4 b = cluster_bins4<CS>(hrow, tkthr);
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t d = static_cast<uint32_t>(4 * tkthr + j);
-        if (d > dk) break;
-        const uint32_t c = d == dk ? ck : u4_at(b, j);
-        if (c) M = df_add(M, static_cast<float>(c) * softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp));
-      }
-    }
-    const DF Mi = warp_incl_scan_df(M);
-    const unsigned ball = __ballot_sync(kFull, (M.hi > 0.f) && df_diff(Mi, tdf) >= 0.f);
-    if (!ball) return false;
-    const int L = __ffs(ball) - 1;
-    uint32_t o_d = 0u, o_c = 0u, o_t = 0u;
-    double o_z = 0.0;
-    int found = 0;
-    if (lane == L) {
-      const double target = df_value(tdf);
-      double run = df_value(Mi) - df_value(M);  // mass of the lanes before
-      int tlast = -1;
-      double runlast = run;
-      for (int i = 0; i < kL && !found; ++i) {
-        const int t = kL * L + i;
-        if (t > tkthr) break;
-        const uint4 b = cluster_bins4<CS>(hrow, t);
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t d = static_cast<uint32_t>(4 * t + j);
-          if (static_cast<int>(d) >= nbins || (topk_on && d > dk)) break;
-          uint32_t c = u4_at(b, j);
-          const uint32_t real = c;
-          if (topk_on && d == dk) c = ck;
-          if (!c) continue;
-          const float e = softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp);
-          const double me = (double)c * (double)e;
-          tlast = static_cast<int>(d);
-          runlast = run;
-          if (run + me >= target) {
-            const float xneed = static_cast<float>((target - run) / (double)e);
-            uint32_t cp = c;
-            if (xneed < static_cast<float>(c)) cp = max(1u, static_cast<uint32_t>(ceilf(xneed)));
-            o_d = d;
-            o_c = cp;
-            o_t = real;
-            o_z = run + (double)cp * (double)e;
-            found = 1;
-            break;
-          }
-          run += me;
-        }
-      }
-      if (!found && tlast >= 0) {  // rounding: the last non-empty bin takes the cut
-        const uint32_t d = static_cast<uint32_t>(tlast);
-        const uint4 b = cluster_bins4<CS>(hrow, tlast / 4);
-        uint32_t c = u4_at(b, tlast % 4);
-        o_t = c;
-        if (topk_on && d == dk) c = ck;
-        const float e = softmax_mass(value_of_key<DT>(rs.kmax - d), rs.m, cexp);
-        o_d = d;
-        o_c = c;
-        o_z = runlast + (double)c * (double)e;
-        found = 1;
-      }
-    }
-    if (!__shfl_sync(kFull, found, L)) return false;
-    dstar = __shfl_sync(kFull, o_d, L);
-    cstar = __shfl_sync(kFull, o_c, L);
-    tstar = __shfl_sync(kFull, o_t, L);
-    zkept = __shfl_sync(kFull, o_z, L);
-  }
-  rs.kstar = rs.kmax - dstar;
-  rs.cstar = cstar;
-  rs.tie_total = tstar;
-  rs.zkept = zkept;
-  rs.partial = cstar < tstar ? 1 : 0;
-  return true;
-}
-
-// Smallest d such that bins 0..d of a CTA-local histogram hold >= need
-// tokens; kWindow - 1 if they never do.  All threads call it.
-__device__ __noinline__ uint32_t local_bins_reach(uint32_t hrow, uint32_t need, Shm& sh) {
-  constexpr int kB = 4;
-  const int tid = threadIdx.x;
-  const uint4 b4 = tid < kBinThreads ? lds128(hrow + 16u * tid) : make_uint4(0u, 0u, 0u, 0u);
-  const uint32_t cnt[kB] = {b4.x, b4.y, b4.z, b4.w};
-  uint32_t C = cnt[0] + cnt[1] + cnt[2] + cnt[3];
-  uint32_t total;
-  const uint32_t P = block_excl_u32(C, sh.w_u, total);
-  if (tid == 0) sh.c_d = static_cast<uint32_t>(kWindow - 1);
-  __syncthreads();
-  if (P < need && P + C >= need) {
-    uint32_t run = P;
-#pragma unroll
-    for (int i = 0; i < kB; ++i) {
-      if (run < need && run + cnt[i] >= need) sh.c_d = static_cast<uint32_t>(tid * kB + i);
-      run += cnt[i];
-    }
-  }
-  __syncthreads();
-  const uint32_t d = sh.c_d;
-  __syncthreads();
-  return d;
-}
-
-enum PassKind { PASS_COUNT_GE = 0, PASS_MASS_GT = 1, PASS_MIN_GE = 2, PASS_COUNT_EQ = 3 };
-
-// One full pass over this CTA's slice of one row, reduced over the cluster.
-// Used only by the exact fallback search of the cut.
-template <int DT, int CS>
-__device__ __noinline__ double cluster_pass(cg::cluster_group& cluster, Shm& sh, uint32_t buf, int n, int nvec, int kind,
-                               uint32_t kappa, float m, float c, uint32_t& slot) {
-  using E = Elt<DT>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t cnt = 0, kmin = 0xFFFFFFFFu;
-  float mass = 0.f;
-  for (int v = tid; v < nvec; v += kThreads) {
-    const uint4 x = lds128(buf + 16u * v);
-    const int t0 = v * E::kPerVec;
-#pragma unroll
-    for (int j = 0; j < E::kPerVec; ++j) {
-      if (t0 + j < n) {
-        const uint32_t b = E::bits_of(x, j);
-        const uint32_t k = E::key(b);
-        if (kind == PASS_COUNT_GE) cnt += (k >= kappa);
-        else if (kind == PASS_COUNT_EQ) cnt += (k == kappa);
-        else if (kind == PASS_MIN_GE) { if (k >= kappa) kmin = min(kmin, k); }
-        else if (k > kappa) mass += softmax_mass(E::value(b), m, c);
-      }
-    }
-  }
-  const uint32_t s = slot & 1u;
-  mass = warp_sum_f32(mass);
-  cnt = warp_sum_u32(cnt);
-  kmin = warp_min_u32(kmin);
-  if (lane == 0) { sh.w_pm[warp] = mass; sh.w_pc[warp] = cnt; sh.w_pk[warp] = kmin; }
-  __syncthreads();
-  if (tid == 0) {
-    double tm = 0.0;
-    uint32_t tc = 0, tk = 0xFFFFFFFFu;
-    for (int w = 0; w < kWarps; ++w) { tm += sh.w_pm[w]; tc += sh.w_pc[w]; tk = min(tk, sh.w_pk[w]); }
-    sh.x_pm[s] = tm; sh.x_pc[s] = tc; sh.x_pk[s] = tk;
-  }
-  cluster.sync();
-  double res;
-  {
-    double vm = 0.0;
-    uint32_t vc = 0, vk = 0xFFFFFFFFu;
-    if (lane < CS) {
-      const Shm* peer = cluster.map_shared_rank(&sh, lane);
-      vm = peer->x_pm[s]; vc = peer->x_pc[s]; vk = peer->x_pk[s];
-    }
-    if (kind == PASS_MASS_GT) res = cluster_sum_f64<CS>(vm);
-    else if (kind == PASS_MIN_GE) res = (double)warp_min_u32(vk);
-    else res = (double)warp_sum_u32(vc);
-  }
-  ++slot;
-  return res;
-}
-
-// Largest bf16 / fp32 value not above v (v finite), as bits.
+// Largest bf16 / fp32 value not above v, as bits.
 template <int DT>
 __device__ __forceinline__ uint32_t bits_round_down(float v) {
   const uint32_t u = __float_as_uint(v);
@@ -688,41 +257,193 @@ __device__ __forceinline__ uint32_t bits_round_down(float v) {
   return (u & 0x80000000u) ? hi + 1u : hi;  // negative: away from zero is down
 }
 
-// The exact cut of one row by a bitwise search over the keys: used when the
-// cut lies outside the exact-value histogram (flat rows, fp32 rows).  Every
-// step is a full pass over the slice reduced over the cluster.
-template <int DT, int CS>
-__device__ __noinline__ void fallback_row(cg::cluster_group& cluster, Shm& sh, uint32_t bb, int n, int nvec, int r,
-                                          int top_k, float top_p, double zfull_r, float cexp, uint32_t& slot) {
+// The kept set of a row: key > kstar, or key == kstar and index < tie_cut.
+struct RowStat {
+  float c;               // log2(e) / T
+  float K;               // lattice exponent (integer) of the row: masses 2^(l c - K)
+  float m;               // row maximum
+  uint32_t kmax;         // key of m
+  uint32_t kstar;
+  int tie_cut;           // row index bound for tokens of value kstar
+  float inv_z;           // 1 / mass of the kept set
+  float zkept;
+  int all_kept;
+  int covered;           // the candidate lists hold every kept token
+  int bad;
+};
+
+__device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, int j) {
+  if (rs.all_kept) return true;
+  if (key > rs.kstar) return true;
+  return key == rs.kstar && j < rs.tie_cut;
+}
+
+template <int DT>
+__device__ __forceinline__ float prob_of(const RowStat& rs, uint32_t bits, int j) {
   using E = Elt<DT>;
-  using H = Hot<DT>;
-  const int tid = threadIdx.x;
+  return kept_key(rs, E::key(bits), j) ? lat_mass(E::value(bits), rs.c, rs.K) * rs.inv_z : 0.f;
+}
+
+struct CutOut {
+  uint32_t kstar;        // key of the last kept value
+  uint32_t keep;         // tokens of value kstar that are kept (lowest indices)
+  uint32_t total;        // tokens of value kstar in the row
+  int found;
+  DF zkept;              // mass of the kept set
+};
+
+struct Shm {
+  float w_m[kWarps][2];
+  int w_k[kWarps][2];
+  float w_z[kWarps][2];
+  uint32_t w_n[kWarps][2];     // candidate list lengths
+  uint32_t w_floor[kWarps][2]; // key above which a warp's list is complete
+  float x_m[2][kWarps][2];     // running maxima exchanged while streaming (double-buffered)
+  float w_s[kWarps];
+  float w_sp[kWarps];
+  uint32_t w_u[kWarps][2];
+  double w_d[kWarps];
+  uint32_t s_C[2][kScanWarps];
+  DF s_M[2][kScanWarps];
+  DF z[2];                     // row sums of masses
+  CutOut cutk[2];
+  CutOut cut[2];
+  uint32_t klo[2];
+  int tie_warp[2];
+  uint32_t tie_j[2];
+  int tie_cut[2];
+  RowStat rs[2];
+  int draw_warp;
+  float draw_base;
+  double red_d;
+  uint32_t red_u, red_k;
+};
+
+// 16-byte vector v of a row (elements v*kPerVec ...), -inf beyond n.
+template <int DT>
+__device__ __forceinline__ uint4 load_vec(const unsigned char* row, int v, int n, bool aligned) {
+  using E = Elt<DT>;
+  if (aligned && (v + 1) * E::kPerVec <= n) return ldg_stream(row + 16 * static_cast<size_t>(v));
+  uint32_t w[4] = {Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad};
+#pragma unroll
+  for (int j = 0; j < E::kPerVec; ++j) {
+    const int t = v * E::kPerVec + j;
+    if (t < n) {
+      const uint32_t b = E::bits_at(row, t);
+      if (E::kBytes == 2) {
+        const int q = j >> 1;
+        w[q] = (j & 1) ? ((w[q] & 0xFFFFu) | (b << 16)) : ((w[q] & 0xFFFF0000u) | b);
+      } else {
+        w[j] = b;
+      }
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Bit j set for the elements of vector v that lie inside a row of n.
+template <int DT>
+__device__ __forceinline__ uint32_t vmask(int v, int n) {
+  const int left = n - v * Elt<DT>::kPerVec;
+  return left >= Elt<DT>::kPerVec ? (1u << Elt<DT>::kPerVec) - 1u : (left > 0 ? (1u << left) - 1u : 0u);
+}
+
+// ------------------------------------------------------ CTA reductions
+
+// Fixed-order CTA sums (deterministic); every thread gets the result.
+__device__ __forceinline__ DF block_sum_df(float v, Shm& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_f32(v);
+  if (lane == 0) sh.w_s[warp] = v;
+  __syncthreads();
+  DF t{0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t = df_add(t, sh.w_s[w]);
+  __syncthreads();
+  return t;
+}
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, Shm& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_u32(v);
+  if (lane == 0) sh.w_u[warp][0] = v;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += sh.w_u[w][0];
+  __syncthreads();
+  return t;
+}
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, Shm& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_min_u32(v);
+  if (lane == 0) sh.w_u[warp][1] = v;
+  __syncthreads();
+  uint32_t t = 0xFFFFFFFFu;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t = min(t, sh.w_u[w][1]);
+  __syncthreads();
+  return t;
+}
+
+// ------------------------------------------------- exact search by passes
+
+enum PassKind { PASS_COUNT_GE = 0, PASS_MASS_GT = 1, PASS_MIN_GE = 2, PASS_COUNT_EQ = 3 };
+
+// One pass over a whole row (re-read from global memory), reduced over the
+// CTA.  Used by rows whose cut is not decided from the candidate lists.
+template <int DT>
+__device__ __noinline__ double row_pass(Shm& sh, const unsigned char* row, int V, bool aligned, int kind,
+                                        uint32_t kappa, const RowStat& rs) {
+  using E = Elt<DT>;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  uint32_t cnt = 0, kmin = 0xFFFFFFFFu;
+  float mass = 0.f;
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    const uint4 x = load_vec<DT>(row, v, V, aligned);
+#pragma unroll
+    for (int j = 0; j < E::kPerVec; ++j) {
+      if (v * E::kPerVec + j < V) {
+        const uint32_t b = E::bits_of(x, j);
+        const uint32_t k = E::key(b);
+        if (kind == PASS_COUNT_GE) cnt += (k >= kappa);
+        else if (kind == PASS_COUNT_EQ) cnt += (k == kappa);
+        else if (kind == PASS_MIN_GE) { if (k >= kappa) kmin = min(kmin, k); }
+        else if (k > kappa) mass += lat_mass(E::value(b), rs.c, rs.K);
+      }
+    }
+  }
+  if (kind == PASS_MASS_GT) return df_double(block_sum_df(mass, sh));
+  if (kind == PASS_MIN_GE) return static_cast<double>(block_min_u32(kmin, sh));
+  return static_cast<double>(block_sum_u32(cnt, sh));
+}
+
+// The exact cut of one row by a bitwise search over the keys.
+template <int DT>
+__device__ __noinline__ CutOut search_cut(Shm& sh, const unsigned char* row, int V, bool aligned, int top_k,
+                                          float top_p, const RowStat& rs, double zfull) {
   const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
-  RowStat rs = sh.rs[r];
-  const int kb = E::kKeyBits;
+  constexpr int kb = Elt<DT>::kKeyBits;
   uint32_t kk = 0, ck = 0, tk = 0;
-  double zk = zfull_r;
+  double zk = zfull;
   if (topk_on) {
     for (int bit = kb - 1; bit >= 0; --bit) {
       const uint32_t cand = kk | (1u << bit);
-      const double cnt = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, cand, rs.m, cexp, slot);
-      if (cnt >= (double)top_k) kk = cand;
+      if (row_pass<DT>(sh, row, V, aligned, PASS_COUNT_GE, cand, rs) >= (double)top_k) kk = cand;
     }
-    const uint32_t gt = (kk == 0xFFFFFFFFu) ? 0u
-        : static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_GE, kk + 1u, rs.m, cexp, slot));
+    const uint32_t gt = (kk == 0xFFFFFFFFu)
+        ? 0u : static_cast<uint32_t>(row_pass<DT>(sh, row, V, aligned, PASS_COUNT_GE, kk + 1u, rs));
     ck = static_cast<uint32_t>(top_k) - gt;
-    tk = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kk, rs.m, cexp, slot));
-    const float ek = softmax_mass(value_of_key<DT>(kk), rs.m, cexp);
-    zk = cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kk, rs.m, cexp, slot) + (double)ck * (double)ek;
+    tk = static_cast<uint32_t>(row_pass<DT>(sh, row, V, aligned, PASS_COUNT_EQ, kk, rs));
+    const float ek = lat_mass(value_of_key<DT>(kk), rs.c, rs.K);
+    zk = row_pass<DT>(sh, row, V, aligned, PASS_MASS_GT, kk, rs) + (double)ck * (double)ek;
   }
   uint32_t kstar = kk, cstar = ck, tstar = tk;
   double zkept = zk;
   if (topp_on) {
     const double target = (double)top_p * zk;
-    // G(kappa): mass of the top-k set strictly above kappa
-    auto G = [&](uint32_t kappa) -> double {
+    auto G = [&](uint32_t kappa) -> double {  // mass of the top-k set strictly above kappa
       if (topk_on && kappa < kk) return zk;
-      return cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MASS_GT, kappa, rs.m, cexp, slot);
+      return row_pass<DT>(sh, row, V, aligned, PASS_MASS_GT, kappa, rs);
     };
     uint32_t k0;
     if (G(0u) < target) {
@@ -735,249 +456,737 @@ __device__ __noinline__ void fallback_row(cg::cluster_group& cluster, Shm& sh, u
       }
       k0 = kp + 1u;
     }
-    kstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_MIN_GE, k0, rs.m, cexp, slot));
+    kstar = static_cast<uint32_t>(row_pass<DT>(sh, row, V, aligned, PASS_MIN_GE, k0, rs));
     const double mb = G(kstar);
-    tstar = static_cast<uint32_t>(cluster_pass<DT, CS>(cluster, sh, bb, n, nvec, PASS_COUNT_EQ, kstar, rs.m, cexp, slot));
+    tstar = static_cast<uint32_t>(row_pass<DT>(sh, row, V, aligned, PASS_COUNT_EQ, kstar, rs));
     const uint32_t avail = (topk_on && kstar == kk) ? ck : tstar;
-    const float ep = softmax_mass(value_of_key<DT>(kstar), rs.m, cexp);
+    const float ep = lat_mass(value_of_key<DT>(kstar), rs.c, rs.K);
     const double xneed = (target - mb) / (double)ep;
     uint32_t cp = avail;
     if (xneed < (double)avail) cp = max(1u, static_cast<uint32_t>(ceil(xneed)));
     cstar = cp;
     zkept = mb + (double)cp * (double)ep;
   }
-  rs.kstar = kstar;
-  rs.cstar = cstar;
-  rs.tie_total = tstar;
-  rs.zkept = zkept;
-  rs.partial = cstar < tstar ? 1 : 0;
-  rs.inv_z = 1.f / static_cast<float>(zkept);
-  rs.thr = H::thr_pack(E::bits_of_key(kstar));
-  __syncthreads();
-  if (tid == 0) sh.rs[r] = rs;
-  __syncthreads();
+  CutOut co;
+  co.kstar = kstar;
+  co.keep = cstar;
+  co.total = tstar;
+  co.found = 1;
+  co.zkept = df_from(zkept);
+  return co;
 }
 
-// Where a partial tie stops.  The kept tokens of value kstar are the cstar
-// lowest-index ones.  Each CTA needs the number of such tokens in lower
-// cluster ranks (from the exchanged histograms, or, for rows cut by the
-// fallback search, from one more exchange); the CTA holding the first one not
-// kept finds its index, every other CTA records a bound outside its slice.
-template <int DT, int CS, int NR>
-__device__ __noinline__ void tie_cuts(cg::cluster_group& cluster, Shm& sh, uint32_t buf0, uint32_t buf1,
-                                      uint32_t hist, int lo, int hi, int n, int V, bool part_fb) {
+// ------------------------------------------------------ segments & lists
+
+// Warp w owns vectors [seg_beg, seg_end) of a row: consecutive vectors in
+// index order (iteration, lane, element).
+struct Seg {
+  int beg, end, iters;
+};
+__device__ __forceinline__ Seg warp_seg(int nvec, int warp) {
+  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
+  Seg s;
+  s.beg = min(nvec, warp * vpw);
+  s.end = min(nvec, s.beg + vpw);
+  s.iters = (s.end - s.beg + 31) / 32;
+  return s;
+}
+
+// List entry: element index within the warp segment (high 16 bits) and the
+// element's 16-bit pattern (low 16 bits).  Lists are bf16 only.
+__device__ __forceinline__ uint32_t entry_make(uint32_t local, uint32_t bits) { return (local << 16) | bits; }
+__device__ __forceinline__ uint32_t entry_local(uint32_t e) { return e >> 16; }
+__device__ __forceinline__ uint32_t entry_bits(uint32_t e) { return e & 0xFFFFu; }
+
+// Keeps, in order, the entries of one warp's list whose key is at least
+// kthr; returns the new length.  Whole warp.
+__device__ __forceinline__ uint32_t list_purge(uint32_t* list, uint32_t len, uint32_t kthr) {
+  const int lane = threadIdx.x & 31;
+  uint32_t out = 0;
+  for (uint32_t base = 0; base < len; base += 32) {
+    const uint32_t i = base + lane;
+    const uint32_t e = i < len ? list[i] : 0u;
+    const bool keep = i < len && Elt<DT_BF16>::key(entry_bits(e)) >= kthr;
+    const unsigned ball = __ballot_sync(kFull, keep);
+    __syncwarp();
+    if (keep) list[out + __popc(ball & ((1u << lane) - 1u))] = e;
+    out += __popc(ball);
+    __syncwarp();
+  }
+  return out;
+}
+
+// Tie cut from one warp-ordered set of tokens of value kstar: every warp
+// counts its tokens (list entries or segment elements), the warp holding the
+// keep-th one (0-based) finds its row index.  Whole CTA.
+template <int DT, bool FROM_LIST>
+__device__ __noinline__ int tie_cut_of(Shm& sh, const uint32_t* list, uint32_t len, const unsigned char* row, int V,
+                                       bool aligned, uint32_t kstar, uint32_t keep) {
   using E = Elt<DT>;
   using H = Hot<DT>;
-  const int crank = static_cast<int>(cluster.block_rank());
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const uint32_t thr = H::thr_pack(E::bits_of_key(kstar));
+  uint32_t c = 0;
+  if (FROM_LIST) {
+    for (uint32_t i = lane; i < len; i += 32) c += (E::key(entry_bits(list[i])) == kstar) ? 1u : 0u;
+  } else {
+    for (int v = sg.beg + lane; v < sg.end; v += 32) {
+      const uint4 x = load_vec<DT>(row, v, V, aligned);
+      c += __popc(H::mask_eq(x, thr) & vmask<DT>(v, V));
+    }
+  }
+  c = warp_sum_u32(c);
+  if (lane == 0) sh.w_u[warp][0] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t run = 0;
+    sh.tie_warp[0] = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      if (run + sh.w_u[w][0] > keep) { sh.tie_warp[0] = w; sh.tie_j[0] = keep - run; break; }
+      run += sh.w_u[w][0];
+    }
+    sh.tie_cut[0] = V;  // all kept (only if the counts disagree)
+  }
+  __syncthreads();
+  if (warp == sh.tie_warp[0]) {
+    uint32_t jj = sh.tie_j[0];
+    const int seg_lo = sg.beg * E::kPerVec;
+    const int rounds = FROM_LIST ? static_cast<int>((len + 31) / 32) : sg.iters;
+    for (int it = 0; it < rounds; ++it) {
+      uint32_t msk = 0u;
+      int base_idx = 0;
+      if (FROM_LIST) {
+        const uint32_t i = it * 32 + lane;
+        if (i < len && E::key(entry_bits(list[i])) == kstar) {
+          msk = 1u;
+          base_idx = seg_lo + static_cast<int>(entry_local(list[i]));
+        }
+      } else {
+        const int v = sg.beg + it * 32 + lane;
+        if (v < sg.end) msk = H::mask_eq(load_vec<DT>(row, v, V, aligned), thr) & vmask<DT>(v, V);
+        base_idx = v * E::kPerVec;
+      }
+      const uint32_t cc = __popc(msk);
+      const uint32_t incl = warp_incl_scan_u32(cc);
+      const uint32_t tot = __shfl_sync(kFull, incl, 31);
+      if (jj < tot) {
+        if (incl > jj && incl - cc <= jj) {
+          uint32_t mm = msk;
+          for (uint32_t q = jj - (incl - cc); q > 0; --q) mm &= mm - 1u;
+          sh.tie_cut[0] = FROM_LIST ? base_idx : base_idx + (__ffs(mm) - 1);
+        }
+        break;
+      }
+      jj -= tot;
+    }
+  }
+  __syncthreads();
+  const int r = sh.tie_cut[0];
+  __syncthreads();
+  return r;
+}
+
+// The filtered, normalised probabilities of a row, written out.
+template <int DT>
+__device__ __noinline__ void write_probs(const unsigned char* row, int V, bool aligned, const RowStat& rp,
+                                         float* out) {
+  using E = Elt<DT>;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    const uint4 x = load_vec<DT>(row, v, V, aligned);
+#pragma unroll
+    for (int j = 0; j < E::kPerVec; ++j) {
+      const int t = v * E::kPerVec + j;
+      if (t < V) out[t] = rp.bad ? 0.f : prob_of<DT>(rp, E::bits_of(x, j), t);
+    }
+  }
+}
+
+// Draw weight of token j: max(0, p - q) (residual) or p (bonus / degenerate).
+template <int DT>
+__device__ __forceinline__ float weight_of(const RowStat& rp, const RowStat& rq, uint32_t bp, const unsigned char* rowq,
+                                           int j, bool use_q, float* pv_out) {
+  const float pv = prob_of<DT>(rp, bp, j);
+  *pv_out = pv;
+  if (!use_q || pv == 0.f) return pv;
+  const float qv = prob_of<DT>(rq, Elt<DT>::bits_at(rowq, j), j);
+  return fmaxf(pv - qv, 0.f);
+}
+
+}  // namespace
+
+// One unit (b, pos) with NR rows (2: target and draft, 1: target only).
+template <int DT, int NR>
+__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* lists, uint32_t* hist, int unit, int b,
+                                          int pos, const unsigned char* rowp, const unsigned char* rowq) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = (n * E::kBytes + 15) / 16;
-  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int seg_beg = min(nvec, warp * vpw);
-  const int seg_end = min(nvec, seg_beg + vpw);
-  const int seg_iters = (seg_end - seg_beg + 31) / 32;
-  const uint32_t buf[2] = {buf0, buf1};
-  if (warp < NR && sh.rs[warp].partial && !sh.fb_need[warp]) {
-    const int r = warp;
-    const uint32_t dstar = sh.rs[r].kmax - sh.rs[r].kstar;
-    uint32_t v = 0u;
-    if (lane < CS) v = ld_cluster_u32(mapa_shared(hist + 4u * (r * kWindow + dstar), lane));
-    const uint32_t before = warp_sum_u32(lane < crank ? v : 0u);
-    const uint32_t local = __shfl_sync(kFull, v, crank);
-    if (lane == 0) { sh.tie_before[r] = before; sh.tie_local[r] = local; }
-  }
-  if (part_fb) {  // rows cut by the fallback: count per CTA, then exchange
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      uint32_t c = 0;
-      if (sh.rs[r].partial && sh.fb_need[r]) {
-        const uint32_t thr = sh.rs[r].thr;
-        for (int v = seg_beg + lane; v < seg_end; v += 32)
-          c += __popc(H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n));
-      }
-      c = warp_sum_u32(c);
-      if (lane == 0) sh.w_tie[warp][r] = c;
-    }
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        uint32_t t = 0;
-        for (int w = 0; w < kWarps; ++w) t += sh.w_tie[w][r];
-        sh.x_tie[r] = t;
-      }
-    }
-    cluster.sync();  // ------------------------------------- sync: fallback ties
-    if (warp < NR && sh.rs[warp].partial && sh.fb_need[warp]) {
-      const int r = warp;
-      uint32_t v = 0u;
-      if (lane < CS) v = cluster.map_shared_rank(&sh, lane)->x_tie[r];
-      const uint32_t before = warp_sum_u32(lane < crank ? v : 0u);
-      if (lane == 0) { sh.tie_before[r] = before; sh.tie_local[r] = sh.x_tie[r]; }
-    }
-  }
+  const int V = a.V;
+  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
+  const bool bad_t = !(T > 0.f) || isinf(T);
+  const float c = kLog2e / T;
+  const u64 c2 = pkf(c, c);
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const unsigned char* rows[2] = {rowp, rowq};
+  const bool aligned[2] = {a.aligned_target != 0, a.aligned_draft != 0};
+  const bool topk_on = a.top_k > 0;
+  const bool topp_on = a.top_p < 1.f;
+  const bool filt = topk_on || topp_on;
+  // candidate lists: bf16 rows with a cut, segments short enough to index
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && (sg.end - sg.beg) * E::kPerVec <= (1 << kSegBits) &&
+                         ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32 * E::kPerVec <= (1 << kSegBits);
+  const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
+  uint32_t* wl[2] = {lists + (0 * kWarps + warp) * kListCap, lists + (1 * kWarps + warp) * kListCap};
+
+  if (filt)
+    for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
   __syncthreads();
-  bool search = false;
-  if (tid == 0) {
+
+  // --------------------------------------------------- phase 1: stream
+  float mt[NR];             // thread maximum
+  int kt[NR];               // thread lattice exponent
+  u64 acc0[NR], acc1[NR];   // thread sums of 2^(l c - kt)
+  float mw[NR];             // running maximum known to the warp (uniform)
+  uint32_t len[NR];         // list lengths (uniform)
+  uint32_t kthr[NR];        // current list bound, as a key (uniform)
+  uint32_t kfloor[NR];      // raised bound: the list is complete above it
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      sh.tie_warp[r] = -1;
-      sh.tie_cut[r] = V;
-      if (!sh.rs[r].partial) continue;
-      const int64_t j = static_cast<int64_t>(sh.rs[r].cstar) - sh.tie_before[r];
-      if (j <= 0) sh.tie_cut[r] = lo;
-      else if (j >= static_cast<int64_t>(sh.tie_local[r])) sh.tie_cut[r] = hi;
-      else { sh.tie_cut[r] = -1; sh.tie_j[r] = static_cast<uint32_t>(j); }
-    }
+  for (int r = 0; r < NR; ++r) {
+    mt[r] = -INFINITY;
+    kt[r] = -(1 << 30);
+    acc0[r] = 0ull;
+    acc1[r] = 0ull;
+    mw[r] = -INFINITY;
+    len[r] = 0u;
+    kthr[r] = 0u;
+    kfloor[r] = 0u;
   }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < NR; ++r) search |= sh.tie_cut[r] < 0;
-  if (search) {  // this CTA holds the first tie token that is not kept
+  // every warp runs the same number of iterations (the CTA barriers below)
+  const int iters_all = (((nvec + kWarps - 1) / kWarps + 31) / 32 * 32) / 32;
+  for (int it = 0; it < iters_all; it += 2) {
+    const int v0 = sg.beg + it * 32 + lane;
+    const int v1 = v0 + 32;
+    uint4 x[NR][2];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      uint32_t c = 0;
-      if (sh.tie_cut[r] < 0) {
-        const uint32_t thr = sh.rs[r].thr;
-        for (int v = seg_beg + lane; v < seg_end; v += 32)
-          c += __popc(H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n));
-      }
-      c = warp_sum_u32(c);
-      if (lane == 0) sh.w_tie[warp][r] = c;
+      x[r][0] = v0 < sg.end ? load_vec<DT>(rows[r], v0, V, aligned[r]) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
+      x[r][1] = v1 < sg.end ? load_vec<DT>(rows[r], v1, V, aligned[r]) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
     }
-    __syncthreads();
-    if (tid == 0) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (sh.tie_cut[r] >= 0) continue;
-        uint32_t run = 0;
-        for (int w = 0; w < kWarps; ++w) {
-          if (run + sh.w_tie[w][r] > sh.tie_j[r]) {
-            sh.tie_warp[r] = w;
-            sh.tie_j[r] -= run;
+    for (int r = 0; r < NR; ++r) {
+      float vm[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        vm[u] = H::vmax(x[r][u]);
+        const float L = vm[u] * c;
+        if (L > static_cast<float>(kt[r]) && L < 1073741824.f) {  // raise the lattice exponent (rare)
+          const int knew = static_cast<int>(ceilf(L));
+          const float s = exp2i(kt[r] - knew);
+          acc0[r] = mul2(acc0[r], pkf(s, s));
+          acc1[r] = mul2(acc1[r], pkf(s, s));
+          kt[r] = knew;
+        }
+        const float nk = -static_cast<float>(kt[r]);
+        H::mass_vec(x[r][u], c2, pkf(nk, nk), acc0[r], acc1[r]);
+        mt[r] = max_nan(mt[r], vm[u]);
+      }
+      if (use_lists) {
+        // the bound: kTheta octaves below the running maximum (at most the
+        // row maximum), never below the raised floor
+        const float m_new = warp_max_nan(max_nan(vm[0], vm[1]));
+        if (m_new > mw[r]) mw[r] = m_new;
+        {
+          const float tv = mw[r] - dtheta;
+          const uint32_t kb = tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u;
+          kthr[r] = max(kfloor[r], kb);
+        }
+        // candidates: elements at or above the bound, appended in index order
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int v = v0 + 32 * u;
+          for (;;) {
+            const float thr_v = value_of_key<DT>(kthr[r]);
+            const bool any = v < sg.end && vm[u] >= thr_v;
+            if (__ballot_sync(kFull, any) == 0u) break;
+            const uint32_t msk = any ? (H::mask_ge(x[r][u], H::thr_pack(E::bits_of_key(kthr[r]))) & vmask<DT>(v, V)) : 0u;
+            const uint32_t cnt = __popc(msk);
+            const uint32_t incl = warp_incl_scan_u32(cnt);
+            const uint32_t tot = __shfl_sync(kFull, incl, 31);
+            if (len[r] + tot > static_cast<uint32_t>(kListCap)) {
+              len[r] = list_purge(wl[r], len[r], kthr[r]);
+              if (len[r] + tot > static_cast<uint32_t>(kListCap)) {
+                // still full: raise the floor (a step toward the warp maximum)
+                const uint32_t kmw = key_of_float<DT>(mw[r]);
+                const uint32_t step = kmw > kthr[r] ? max(1u, (kmw - kthr[r]) / 8u) : 1u;
+                kfloor[r] = kthr[r] + step;
+                kthr[r] = kfloor[r];
+                continue;
+              }
+            }
+            uint32_t pos_w = len[r] + incl - cnt;
+            uint32_t mm = msk;
+            while (mm) {
+              const int j = __ffs(mm) - 1;
+              mm &= mm - 1u;
+              wl[r][pos_w++] = entry_make(static_cast<uint32_t>((v - sg.beg) * 8 + j), E::bits_of(x[r][u], j));
+            }
+            len[r] += tot;
             break;
           }
-          run += sh.w_tie[w][r];
         }
       }
     }
-    __syncthreads();
+    if (use_lists && ((it >> 1) % kSyncEvery) == kSyncEvery - 1) {
+      // share the running maxima across the CTA (fixed points: deterministic)
+      const int slot = ((it >> 1) / kSyncEvery) & 1;
+      if (lane == 0) {
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      if (warp != sh.tie_warp[r]) continue;
-      const uint32_t thr = sh.rs[r].thr;
-      uint32_t jj = sh.tie_j[r];
-      for (int it = 0; it < seg_iters; ++it) {
-        const int v = seg_beg + it * 32 + lane;
-        const uint32_t msk = v < seg_end ? (H::mask_eq(lds128(buf[r] + 16u * v), thr) & valid_mask<DT>(v, n)) : 0u;
-        const uint32_t c = __popc(msk);
-        const uint32_t incl = warp_incl_scan_u32(c);
-        const uint32_t tot = __shfl_sync(kFull, incl, 31);
-        if (jj < tot) {
-          if (incl > jj && incl - c <= jj) {  // this lane holds the token
-            uint32_t mm = msk;
-            for (uint32_t q = jj - (incl - c); q > 0; --q) mm &= mm - 1u;
-            sh.tie_cut[r] = lo + v * E::kPerVec + (__ffs(mm) - 1);
-          }
-          break;
-        }
-        jj -= tot;
+        for (int r = 0; r < NR; ++r) sh.x_m[slot][warp][r] = mw[r];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float mm = mw[r];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][r]);
+        mw[r] = mm;
       }
     }
-    __syncthreads();
   }
-  if (tid == 0) {
+  __syncwarp();
+
+  // ------------------------------------------ phase 2: row maximum and sum
 #pragma unroll
-    for (int r = 0; r < NR; ++r) sh.rs[r].tie_cut = sh.tie_cut[r];
+  for (int r = 0; r < NR; ++r) {
+    float s0, s1, s2, s3;
+    upk(acc0[r], s0, s1);
+    upk(acc1[r], s2, s3);
+    float zt = (s0 + s1) + (s2 + s3);
+    const int kw = warp_max_i32(kt[r]);
+    zt *= exp2i(kt[r] - kw);
+    zt = warp_sum_f32(zt);
+    const float mx = warp_max_nan(mt[r]);
+    if (lane == 0) {
+      sh.w_m[warp][r] = mx;
+      sh.w_k[warp][r] = kw;
+      sh.w_z[warp][r] = zt;
+      sh.w_n[warp][r] = len[r];
+      sh.w_floor[warp][r] = kfloor[r];
+    }
   }
   __syncthreads();
-}
-
-// The filtered, normalised probabilities of this CTA's slice, written out.
-template <int DT>
-__device__ __noinline__ void write_probs(const SampleArgs& a, uint32_t buf0, const RowStat& rp, float cexp, int unit,
-                                         int lo, int n, int V) {
-  using E = Elt<DT>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = (n * E::kBytes + 15) / 16;
-  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int seg_beg = min(nvec, warp * vpw);
-  const int seg_end = min(nvec, seg_beg + vpw);
-  const uint32_t buf[1] = {buf0};
-  float* out = a.out_probs + static_cast<size_t>(unit) * V + lo;
-  const bool vec_out = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) && (V % 4 == 0);
-  for (int v = seg_beg + lane; v < seg_end; v += 32) {
-    const int t0 = v * E::kPerVec;
-    const uint4 x = lds128(buf[0] + 16u * v);
-    float w[8];
-    vec_weights<DT>(x, x, t0, lo, n, false, rp, rp, cexp, w);
-    if (rp.bad) {
+  float m[NR], K[NR];
+  bool bad[NR], cov[NR];
+  bool any_bad = bad_t;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+  for (int r = 0; r < NR; ++r) {
+    float mx = -INFINITY;
+    int kk = -(1 << 30);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mx = max_nan(mx, sh.w_m[w][r]);
+      kk = max(kk, sh.w_k[w][r]);
     }
-    if (vec_out && t0 + E::kPerVec <= n) {
-      reinterpret_cast<float4*>(out + t0)[0] = make_float4(w[0], w[1], w[2], w[3]);
-      if (E::kPerVec == 8) reinterpret_cast<float4*>(out + t0)[1] = make_float4(w[4], w[5], w[6], w[7]);
-    } else {
+    DF z{0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < E::kPerVec; ++j)
-        if (t0 + j < n) out[t0 + j] = w[j];
+    for (int w = 0; w < kWarps; ++w) z = df_add(z, sh.w_z[w][r] * exp2i(sh.w_k[w][r] - kk));
+    m[r] = mx;
+    K[r] = static_cast<float>(kk);
+    // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
+    bad[r] = bad_t || !isfinite(mx) || !(fabsf(mx * c) < 1073741824.f);
+    any_bad |= bad[r];
+    cov[r] = use_lists;
+    if (tid == 0) sh.z[r] = z;
+  }
+
+  if (any_bad) {
+    if (a.mode == MODE_PROBS) {
+      float* out = a.out_probs + static_cast<size_t>(unit) * V;
+      for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
+      if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
+    } else if (tid == 0) {
+      const int kq = a.k;
+      UnitRec* rec = a.recs + unit;
+      uint32_t add = 1u;
+      uint32_t st = SPEC_STATUS_BAD_ROW;
+      rec->drawn = -1;
+      if (NR == 2) {
+        const int x = a.tokens[static_cast<size_t>(b) * kq + pos];
+        if (!(x >= 0 && x < V)) st |= SPEC_STATUS_BAD_TOKEN;
+        rec->accept = 0;
+        rec->px = 0.f;
+        rec->qx = 0.f;
+        if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = 0.f;
+        if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = 0.f;
+        add = 2u;
+      }
+      set_status(a.status, st);
+      __threadfence();
+      const uint32_t before = atomicAdd(a.tickets + b, add);
+      if (before + add == static_cast<uint32_t>(2 * kq + 1)) sample_finalize(a, b);
+    }
+    return;
+  }
+
+  // --------------------------- phase 3: histogram of the candidates' values
+  // Every element within kTheta octaves of the row maximum (key >= klo) is
+  // on a list; the histogram covers keys klo .. kmax (at most kWindow).
+  uint32_t klo[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const uint32_t kmax = key_of_float<DT>(m[r]);
+    const float tv = m[r] - dtheta;
+    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
+    const uint32_t gtop = kmax >> 2;
+    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
+    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][r]);  // every list is complete above kl
+    klo[r] = kl;
+    if (cov[r]) {
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t n_w = sh.w_n[w][r];
+        const uint32_t* lw = lists + (r * kWarps + w) * kListCap;
+        for (uint32_t i = tid; i < n_w; i += kThreads) {
+          const uint32_t k = E::key(entry_bits(lw[i]));
+          if (k >= kl) red_add_shared(smem_addr(hist + r * kWindow + (k & kSlotMask)), 1u);
+        }
+      }
     }
   }
-}
+  if (tid < 2) { sh.cut[tid].found = 0; sh.cutk[tid].found = 0; }
+  __syncthreads();
 
-// The CTA holding the drawn token finds it: the warp whose segment holds the
-// crossing walks it vector by vector (index order) and writes the token.
-template <int DT, int NR>
-__device__ __noinline__ void draw_walk(const SampleArgs& a, Shm& sh, uint32_t buf0, uint32_t bufq, bool use_q,
-                                       const RowStat& rp, const RowStat& rq, float cexp, double target, int lo,
-                                       int n, int unit, int b) {
-  using E = Elt<DT>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = (n * E::kBytes + 15) / 16;
-  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int seg_beg = min(nvec, warp * vpw);
-  const int seg_end = min(nvec, seg_beg + vpw);
-  const int seg_iters = (seg_end - seg_beg + 31) / 32;
+  // ---------------------------------------------- phase 4: the cut scan
+  if (filt) {
+    const int r_s = (NR == 2) ? (warp >> 2) : 0;
+    const int wq = warp & (kScanWarps - 1);
+    const bool scanner = ((NR == 2) || warp < kScanWarps) && (r_s == 0 ? cov[0] : cov[NR - 1]);
+    const float m_s = r_s == 0 ? m[0] : m[NR - 1];
+    const float K_s = r_s == 0 ? K[0] : K[NR - 1];
+    const uint32_t klo_s = r_s == 0 ? klo[0] : klo[NR - 1];
+    const uint32_t kmax_s = key_of_float<DT>(m_s);
+    uint32_t cnt[4] = {0u, 0u, 0u, 0u}, top = 0u, Cl = 0u, Cex = 0u;
+    float ms[4] = {0.f, 0.f, 0.f, 0.f}, Ml = 0.f;
+    DF Mex{0.f, 0.f};
+    bool valid = false;
+    if (scanner) {
+      const uint32_t gtop = kmax_s >> 2;
+      const uint32_t gi = static_cast<uint32_t>(wq * 32 + lane);
+      if (gi <= gtop) {
+        const uint32_t grp = gtop - gi;
+        top = 4u * grp + 3u;
+        if (top >= klo_s) {
+          valid = true;
+          const uint4 h4 = lds128(smem_addr(hist + r_s * kWindow + 4u * (grp & static_cast<uint32_t>(kGroups - 1))));
+          const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // keys top, top-1, top-2, top-3
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t key = top - static_cast<uint32_t>(j);
+            const uint32_t s = (key > kmax_s || key < klo_s) ? 0u : hv[j];
+            cnt[j] = s;
+            ms[j] = s ? lat_mass(value_of_key<DT>(key), c, K_s) : 0.f;
+            Cl += s;
+            Ml += static_cast<float>(s) * ms[j];
+          }
+        }
+      }
+      const uint32_t Cin = warp_incl_scan_u32(Cl);
+      const DF Min = warp_incl_scan_df(DF{Ml, 0.f});
+      Cex = Cin - Cl;
+      Mex = df_shfl_up(Min, 1);
+      if (lane == 0) Mex = DF{0.f, 0.f};
+      if (lane == 31) {
+        sh.s_C[r_s][wq] = Cin;
+        sh.s_M[r_s][wq] = Min;
+      }
+    }
+    __syncthreads();
+    uint32_t offC = 0u;
+    DF offM{0.f, 0.f}, nxtM{0.f, 0.f}, totM{0.f, 0.f};
+    if (scanner) {
+#pragma unroll
+      for (int q = 0; q < kScanWarps; ++q) {
+        const uint32_t cq = sh.s_C[r_s][q];
+        const DF mq = sh.s_M[r_s][q];
+        if (q < wq) { offC += cq; offM = df_add2(offM, mq); }
+        if (q <= wq) nxtM = df_add2(nxtM, mq);
+        totM = df_add2(totM, mq);
+      }
+    }
+    if (topk_on && scanner) {  // the value where the running count reaches top_k
+      const uint32_t Kc = static_cast<uint32_t>(a.top_k);
+      const uint32_t wC = sh.s_C[r_s][wq];
+      if (offC < Kc && offC + wC >= Kc) {
+        const uint32_t cb = offC + Cex;
+        const unsigned ball = __ballot_sync(kFull, valid && cb < Kc);
+        const int l = 31 - __clz(ball | 1u);
+        if (lane == l && valid && cb < Kc) {
+          uint32_t run = cb;
+          DF mb = df_add2(offM, Mex);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (run < Kc && run + cnt[j] >= Kc) {
+              CutOut co;
+              co.kstar = top - static_cast<uint32_t>(j);
+              co.keep = Kc - run;
+              co.total = cnt[j];
+              co.found = 1;
+              co.zkept = df_add(mb, static_cast<float>(Kc - run) * ms[j]);
+              sh.cutk[r_s] = co;
+              if (!topp_on) sh.cut[r_s] = co;
+            }
+            run += cnt[j];
+            mb = df_add(mb, static_cast<float>(cnt[j]) * ms[j]);
+          }
+        }
+      }
+    }
+    if (topk_on && topp_on) __syncthreads();
+    if (topp_on && scanner) {  // a token is kept while the mass ranked before it is below top_p * Z
+      const CutOut ck = sh.cutk[r_s];
+      if (!topk_on || ck.found) {
+        const DF target = df_mul_f(topk_on ? ck.zkept : sh.z[r_s], a.top_p);
+        const bool wlast = !df_lt(totM, target) && df_lt(offM, target) &&
+                           (wq == kScanWarps - 1 || !df_lt(nxtM, target));
+        if (wlast) {
+          const DF mbl = df_add2(offM, Mex);
+          const unsigned ball = __ballot_sync(kFull, valid && df_lt(mbl, target));
+          const int l = 31 - __clz(ball | 1u);
+          if (lane == l && valid && df_lt(mbl, target)) {
+            DF mb = mbl, mb_last{0.f, 0.f};
+            int jl = -1;
+            uint32_t cl = 0u;
+            bool done = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t key = top - static_cast<uint32_t>(j);
+              uint32_t ce = cnt[j];
+              if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
+              if (!done && ce > 0u) {
+                const DF after = df_add(mb, static_cast<float>(ce) * ms[j]);
+                jl = j;
+                cl = ce;
+                mb_last = mb;
+                if (!df_lt(after, target)) {
+                  const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
+                  uint32_t keep = static_cast<uint32_t>(ceilf(need / ms[j]));
+                  keep = max(1u, min(keep, ce));
+                  CutOut co;
+                  co.kstar = key;
+                  co.keep = keep;
+                  co.total = cnt[j];
+                  co.found = 1;
+                  co.zkept = df_add(mb, static_cast<float>(keep) * ms[j]);
+                  sh.cut[r_s] = co;
+                  done = true;
+                }
+                mb = after;
+              }
+            }
+            if (!done && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
+              CutOut co;
+              co.kstar = top - static_cast<uint32_t>(jl);
+              co.keep = cl;
+              co.total = cnt[jl];
+              co.found = 1;
+              co.zkept = df_add(mb_last, static_cast<float>(cl) * ms[jl]);
+              sh.cut[r_s] = co;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ------------------------------------ phase 5: kept set of each row
+#pragma unroll 1
+  for (int r = 0; r < NR; ++r) {
+    RowStat rs;
+    rs.c = c;
+    rs.K = r == 0 ? K[0] : K[NR - 1];
+    rs.m = r == 0 ? m[0] : m[NR - 1];
+    rs.kmax = key_of_float<DT>(rs.m);
+    rs.bad = 0;
+    rs.all_kept = filt ? 0 : 1;
+    rs.covered = (r == 0 ? cov[0] : cov[NR - 1]) ? 1 : 0;
+    rs.kstar = 0u;
+    rs.tie_cut = V;
+    float zk = df_float(sh.z[r]);
+    if (filt) {
+      CutOut co = sh.cut[r];
+      const bool from_lists = co.found != 0;
+      if (!from_lists) {
+        rs.covered = 0;
+        co = search_cut<DT>(sh, rows[r], V, aligned[r], a.top_k, a.top_p, rs, df_double(sh.z[r]));
+      }
+      rs.kstar = co.kstar;
+      zk = df_float(co.zkept);
+      if (co.keep < co.total) {
+        const uint32_t* lw = lists + (r * kWarps + warp) * kListCap;
+        rs.tie_cut = from_lists
+            ? tie_cut_of<DT, true>(sh, lw, sh.w_n[warp][r], rows[r], V, aligned[r], co.kstar, co.keep)
+            : tie_cut_of<DT, false>(sh, lw, 0u, rows[r], V, aligned[r], co.kstar, co.keep);
+      }
+    }
+    rs.zkept = zk;
+    rs.inv_z = 1.f / zk;
+    if (tid == 0) sh.rs[r] = rs;
+  }
+  __syncthreads();
+  const RowStat rp = sh.rs[0];
+  const RowStat rq = sh.rs[NR - 1];
+
+  if (a.mode == MODE_PROBS) {
+    write_probs<DT>(rows[0], V, aligned[0], rp, a.out_probs + static_cast<size_t>(unit) * V);
+    return;
+  }
+
   const int kq = a.k;
-  const uint32_t buf[2] = {buf0, bufq};
+  // ------------------------------------- phase 6: accept test at x_pos
+  if (NR == 2 && tid == 0) {
+    const int x = a.tokens[static_cast<size_t>(b) * kq + pos];
+    UnitRec* rec = a.recs + unit;
+    float px = 0.f, qx = 0.f;
+    if (x >= 0 && x < V) {
+      px = prob_of<DT>(rp, E::bits_at(rows[0], x), x);
+      qx = prob_of<DT>(rq, E::bits_at(rows[NR - 1], x), x);
+      const float u = a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
+      rec->accept = (u * qx < px) ? 1 : 0;
+    } else {
+      rec->accept = 0;
+      set_status(a.status, SPEC_STATUS_BAD_TOKEN);
+    }
+    rec->px = px;
+    rec->qx = qx;
+    if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
+    if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
+    __threadfence();
+    if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
+  }
+
+  // ------------- phase 7: residual (or bonus) by warps, in index order
+  // On the fast path each warp walks its list of p (the kept set of p is on
+  // it); otherwise its segment of the row.
+  const bool lists_p = rp.covered && !rp.all_kept;
+  const uint32_t* lp = lists + (0 * kWarps + warp) * kListCap;
+  const uint32_t np = lists_p ? sh.w_n[warp][0] : 0u;
+  const int seg_lo = sg.beg * E::kPerVec;
+  {
+    float s = 0.f, sp = 0.f;
+    if (lists_p) {
+      for (uint32_t i = lane; i < np; i += 32) {
+        const uint32_t e = lp[i];
+        const int j = seg_lo + static_cast<int>(entry_local(e));
+        float pv;
+        s += weight_of<DT>(rp, rq, entry_bits(e), rows[NR - 1], j, NR == 2, &pv);
+        sp += pv;
+      }
+    } else {
+      for (int v = sg.beg + lane; v < sg.end; v += 32) {
+        const uint4 xp = load_vec<DT>(rows[0], v, V, aligned[0]);
+        const uint4 xq = NR == 2 ? load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]) : xp;
+#pragma unroll
+        for (int j = 0; j < E::kPerVec; ++j) {
+          const int t = v * E::kPerVec + j;
+          if (t < V) {
+            const float pv = prob_of<DT>(rp, E::bits_of(xp, j), t);
+            sp += pv;
+            s += NR == 2 ? fmaxf(pv - (pv > 0.f ? prob_of<DT>(rq, E::bits_of(xq, j), t) : 0.f), 0.f) : pv;
+          }
+        }
+      }
+    }
+    s = warp_sum_f32(s);
+    sp = warp_sum_f32(sp);
+    if (lane == 0) {
+      sh.w_s[warp] = s;
+      sh.w_sp[warp] = sp;
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
-    double run = 0.0, wbase = 0.0, lbase = 0.0;
+    DF S{0.f, 0.f}, Sp{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      S = df_add(S, sh.w_s[w]);
+      Sp = df_add(Sp, sh.w_sp[w]);
+    }
+    bool use_q = NR == 2;
+    const float* ws = sh.w_s;
+    if (NR == 2 && !(S.hi > 0.f)) {  // degenerate residual: draw from p instead
+      use_q = false;
+      S = Sp;
+      ws = sh.w_sp;
+    }
+    const float u_draw = a.uniforms[static_cast<size_t>(b) * (kq + 2) + (NR == 2 ? kq + 1 : kq)];
+    const DF target = df_mul_f(S, u_draw);
+    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
     int wsel = -1, wlast = -1;
     for (int w = 0; w < kWarps; ++w) {
-      const double sw = (double)sh.w_res[w];
-      if (sw > 0.0) { wlast = w; lbase = run; }
-      if (wsel < 0 && sw > 0.0 && run + sw > target) { wsel = w; wbase = run; }
-      run += sw;
+      const float sw = ws[w];
+      const DF nxt = df_add(run, sw);
+      if (sw > 0.f) { wlast = w; lbase = run; }
+      if (wsel < 0 && sw > 0.f && df_lt(target, nxt)) { wsel = w; base = run; }
+      run = nxt;
     }
-    if (wsel < 0) { wsel = wlast; wbase = lbase; }
-    sh.draw_warp = wsel;
-    sh.draw_base = wbase;
+    if (wsel < 0) { wsel = wlast; base = lbase; }
+    sh.draw_warp = use_q ? wsel : -2 - wsel;  // -2 - w: weights are p
+    sh.draw_base = df_float(df_add2(target, df_neg(base)));
   }
   __syncthreads();
-  if (warp == sh.draw_warp) {
-    const float tw = static_cast<float>(target - sh.draw_base);
+  const int dw = sh.draw_warp;
+  const bool use_q = dw >= 0;
+  const int wsel = use_q ? dw : -2 - dw;
+  if (warp == wsel) {
+    const float tw = sh.draw_base;
     float run = 0.f;
     int token = -1, last_pos = -1;
-    for (int it = 0; it < seg_iters && token < 0; ++it) {
-      const int v = seg_beg + it * 32 + lane;
-      const bool valid = v < seg_end;
-      const int t0 = v * E::kPerVec;
+    const int rounds = lists_p ? static_cast<int>((np + 31) / 32) : sg.iters;
+    for (int it = 0; it < rounds && token < 0; ++it) {
       float w[8];
+      int idx[8];
       float ls = 0.f;
       int lpos = -1;
-      if (valid) {
-        const uint4 xp = lds128(buf[0] + 16u * v);
-        const uint4 xq = use_q ? lds128(buf[NR - 1] + 16u * v) : xp;
-        ls = vec_weights<DT>(xp, xq, t0, lo, n, use_q, rp, rq, cexp, w);
 #pragma unroll
-        for (int j = 0; j < E::kPerVec; ++j)
-          if (w[j] > 0.f) lpos = t0 + j;
+      for (int j = 0; j < 8; ++j) { w[j] = 0.f; idx[j] = -1; }
+      if (lists_p) {
+        const uint32_t i = it * 32 + lane;
+        if (i < np) {
+          const uint32_t e = lp[i];
+          float pv;
+          idx[0] = seg_lo + static_cast<int>(entry_local(e));
+          w[0] = weight_of<DT>(rp, rq, entry_bits(e), rows[NR - 1], idx[0], use_q, &pv);
+        }
+      } else {
+        const int v = sg.beg + it * 32 + lane;
+        if (v < sg.end) {
+          const uint4 xp = load_vec<DT>(rows[0], v, V, aligned[0]);
+          const uint4 xq = use_q ? load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]) : xp;
+#pragma unroll
+          for (int j = 0; j < E::kPerVec; ++j) {
+            const int t = v * E::kPerVec + j;
+            if (t < V) {
+              const float pv = prob_of<DT>(rp, E::bits_of(xp, j), t);
+              w[j] = use_q ? fmaxf(pv - (pv > 0.f ? prob_of<DT>(rq, E::bits_of(xq, j), t) : 0.f), 0.f) : pv;
+              idx[j] = t;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ls += w[j];
+        if (w[j] > 0.f) lpos = idx[j];
       }
       const float incl = warp_incl_scan(ls);
-      const unsigned ball = __ballot_sync(kFull, valid && ls > 0.f && run + incl > tw);
+      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
       const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
-      const int lp = __shfl_sync(kFull, lpos, lastl);
-      if (lp >= 0) last_pos = lp;
+      const int lp2 = __shfl_sync(kFull, lpos, lastl);
+      if (lp2 >= 0) last_pos = lp2;
       if (ball) {
         const int l = __ffs(ball) - 1;
         int tok = -1;
@@ -985,10 +1194,10 @@ __device__ __noinline__ void draw_walk(const SampleArgs& a, Shm& sh, uint32_t bu
           float cum = run + (incl - ls);
           int lastj = -1;
 #pragma unroll
-          for (int j = 0; j < E::kPerVec; ++j) {
-            if (w[j] > 0.f) lastj = t0 + j;
+          for (int j = 0; j < 8; ++j) {
+            if (w[j] > 0.f) lastj = idx[j];
             cum += w[j];
-            if (tok < 0 && w[j] > 0.f && cum > tw) tok = t0 + j;
+            if (tok < 0 && w[j] > 0.f && cum > tw) tok = idx[j];
           }
           if (tok < 0) tok = lastj;
         }
@@ -998,486 +1207,26 @@ __device__ __noinline__ void draw_walk(const SampleArgs& a, Shm& sh, uint32_t bu
     }
     if (token < 0) token = last_pos;  // only reachable through rounding
     if (lane == 0) {
-      a.recs[unit].drawn = token >= 0 ? lo + token : -1;
+      a.recs[unit].drawn = token;
       __threadfence();
       if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
     }
+  } else if (wsel < 0 && tid == 0) {  // nothing to draw from (all mass rounded away)
+    a.recs[unit].drawn = -1;
+    __threadfence();
+    if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
   }
 }
 
-// Bound for a top-p cut from the cluster's warp maxima (one warp per row).
-// Those maxima are tokens of the row.  If the ones at or above a value v
-// already weigh top_p * Z, the nucleus ends at or above v, so no token below v
-// is kept.  (1e-4 of margin covers rounding.)  Writes the bound value (or
-// -inf) to sh.w_f[r].
-template <int CS>
-__device__ __noinline__ void warp_max_bound(Shm& sh, int r, float m_r, double z_r, float cexp, float top_p) {
-  const int lane = threadIdx.x & 31;
-  constexpr int nw = kWarps * CS;
-  float v0 = -INFINITY, v1 = -INFINITY;
-  if (lane < nw) v0 = ld_cluster_f32(mapa_shared(smem_addr(&sh.w_max[lane % kWarps][r]), lane / kWarps));
-  if (lane + 32 < nw)
-    v1 = ld_cluster_f32(mapa_shared(smem_addr(&sh.w_max[(lane + 32) % kWarps][r]), (lane + 32) / kWarps));
-  const float e0 = v0 > -INFINITY ? softmax_mass(v0, m_r, cexp) : 0.f;
-  const float e1 = v1 > -INFINITY ? softmax_mass(v1, m_r, cexp) : 0.f;
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-  for (int j = 0; j < nw; ++j) {
-    const float vj = __shfl_sync(kFull, j < 32 ? v0 : v1, j & 31);
-    const float ej = __shfl_sync(kFull, j < 32 ? e0 : e1, j & 31);
-    s0 += vj >= v0 ? ej : 0.f;
-    s1 += vj >= v1 ? ej : 0.f;
-  }
-  const float target = 1.0001f * top_p * static_cast<float>(z_r);
-  float cand = -INFINITY;
-  if (v0 > -INFINITY && s0 >= target) cand = v0;
-  if (v1 > -INFINITY && s1 >= target) cand = fmaxf(cand, v1);
-  cand = warp_max(cand);
-  if (lane == 0) sh.w_f[r] = cand;
-}
-
-}  // namespace
-
-// One unit (b, pos) with NR rows (2: target and draft, 1: target only).
-template <int DT, int CS, int NR>
-__device__ __forceinline__ void unit_body(const SampleArgs& a, cg::cluster_group& cluster, Shm& sh,
-                                          unsigned char* dsm, int unit, int b, int pos,
-                                          const unsigned char* rowp, const unsigned char* rowq) {
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
   using E = Elt<DT>;
-  using H = Hot<DT>;
-  const int crank = static_cast<int>(cluster.block_rank());
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int V = a.V;
-  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
-  const bool bad_t = !(T > 0.f) || isinf(T);
-  const float cexp = kLog2e / T;
-  const u64 c2 = pkf(cexp, cexp);
-
-  const int lo = min(V, crank * a.chunk);
-  const int hi = min(V, lo + a.chunk);
-  const int n = hi - lo;
-  const int nvec = (n * E::kBytes + 15) / 16;
-  const int nfull = n / E::kPerVec;  // vectors without a ragged tail
-  const int bufbytes = ((a.chunk * E::kBytes + 15) / 16) * 16;
-  // shared-window addresses of the two row buffers and of the histograms
-  const uint32_t sbase = smem_addr(dsm);
-  const uint32_t buf[2] = {sbase, sbase + static_cast<uint32_t>(bufbytes)};
-  const uint32_t hist = sbase + 2u * static_cast<uint32_t>(bufbytes);
-  unsigned char* const bufp[2] = {dsm, dsm + bufbytes};
-  const unsigned char* rows[2] = {rowp, rowq};
-  const bool aligned[2] = {a.aligned_target != 0, a.aligned_draft != 0};
-
-  const bool topk_on = a.top_k > 0;
-  const bool topp_on = a.top_p < 1.f;
-  const bool filt = topk_on || topp_on;
-
-  // warp segment: consecutive vectors, index order (iteration, lane, element)
-  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int seg_beg = min(nvec, warp * vpw);
-  const int seg_end = min(nvec, seg_beg + vpw);
-  const int seg_iters = (seg_end - seg_beg + 31) / 32;
-
-  // ------------------------------------------------------ phase 0: load
-  if (tid == 0) {
-    mbar_init(&sh.mbar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t tx = 0;
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      if (aligned[r] && n > 0) tx += static_cast<uint32_t>(n * E::kBytes);
-    mbar_arrive_expect_tx(&sh.mbar, tx);
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      if (aligned[r] && n > 0)
-        bulk_copy_g2s(bufp[r], rows[r] + static_cast<size_t>(lo) * E::kBytes, static_cast<uint32_t>(n * E::kBytes),
-                      &sh.mbar);
-  }
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    if (!aligned[r]) {
-      for (int t = tid; t < n; t += kThreads) {
-        const uint32_t bits = E::bits_at(rows[r], static_cast<int64_t>(lo) + t);
-        if (E::kBytes == 2) sts_u16(buf[r] + 2u * t, bits);
-        else sts_u32(buf[r] + 4u * t, bits);
-      }
-    }
-  }
-  if (filt)
-    for (int t = tid; t < NR * kWindow; t += kThreads) sts_u32(hist + 4u * t, 0u);
-  if (tid == 0 && !mbar_wait_bounded(&sh.mbar, 0)) set_status(a.status, SPEC_STATUS_TIMEOUT);
-  __syncthreads();
-
-  // ------------------------------------------------------ phase 1: max
-  float tmax[NR];  // this thread's own maximum, for the top-k bound below
-  {
-    typename H::MaxAcc st[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) H::max_init(st[r]);
-    int v = tid;
-    for (; v + kThreads < nfull; v += 2 * kThreads) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        H::max_vec(lds128(buf[r] + 16u * v), st[r]);
-        H::max_vec(lds128(buf[r] + 16u * (v + kThreads)), st[r]);
-      }
-    }
-    if (v < nfull) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) H::max_vec(lds128(buf[r] + 16u * v), st[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      float mx = H::max_finish(st[r]);
-      for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads) mx = max_nan(mx, E::value(lds_elem<DT>(buf[r], t)));
-      tmax[r] = mx;
-      mx = warp_max_nan(mx);
-      if (lane == 0) sh.w_max[warp][r] = mx;
-    }
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        float m = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) m = max_nan(m, sh.w_max[w][r]);
-        sh.x_max[r] = m;
-      }
-    }
-  }
-  cluster.sync();  // ---------------------------------------------- sync: max
-  float m[NR];
-  bool rbad[NR];
-  uint32_t kmax[NR];
-  bool any_bad = bad_t;
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    float pm = -INFINITY;
-    if (lane < CS) pm = cluster.map_shared_rank(&sh, lane)->x_max[r];
-    m[r] = warp_max_nan(pm);
-    rbad[r] = bad_t || !isfinite(m[r]);  // NaN, +inf, or no finite entry
-    any_bad |= rbad[r];
-    const uint32_t mbits = (E::kBytes == 2) ? (__float_as_uint(m[r]) >> 16) : __float_as_uint(m[r]);
-    kmax[r] = E::key(mbits);
-  }
-
-  // --------------------------------------- phase 2: sum of masses (if used)
-  const bool need_sum = !topk_on;
-  double zfull[NR];
-#pragma unroll
-  for (int r = 0; r < NR; ++r) zfull[r] = 0.0;
-  if (need_sum) {
-    if (!any_bad) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const u64 m2 = pkf(m[r], m[r]);
-        u64 acc0 = 0ull, acc1 = 0ull;
-        int v = tid;
-        for (; v + kThreads < nfull; v += 2 * kThreads) {
-          H::mass_vec(lds128(buf[r] + 16u * v), m2, c2, acc0);
-          H::mass_vec(lds128(buf[r] + 16u * (v + kThreads)), m2, c2, acc1);
-        }
-        if (v < nfull) H::mass_vec(lds128(buf[r] + 16u * v), m2, c2, acc0);
-        float s0, s1, s2, s3;
-        upk(acc0, s0, s1);
-        upk(acc1, s2, s3);
-        float s = (s0 + s1) + (s2 + s3);
-        for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads)
-          s += softmax_mass(E::value(lds_elem<DT>(buf[r], t)), m[r], cexp);
-        s = warp_sum_f32(s);
-        if (lane == 0) sh.w_sum[warp][r] = s;
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        double s = 0.0;
-        if (!any_bad)
-          for (int w = 0; w < kWarps; ++w) s += (double)sh.w_sum[w][r];
-        sh.x_sum[r] = s;
-      }
-    }
-    cluster.sync();  // -------------------------------------------- sync: sum
-    if (tid == 0) {  // fixed-order cluster total, one thread, then broadcast
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        double z = 0.0;
-        for (int c = 0; c < CS; ++c) z += cluster.map_shared_rank(&sh, c)->x_sum[r];
-        sh.b_zfull[r] = z;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < NR; ++r) zfull[r] = sh.b_zfull[r];
-  }
-
-  // ------------------------- phase 3: exact-value histogram near the top
-  // Bins d = kmax - key count the tokens of one value each.  Only tokens that
-  // can survive the cut are counted:
-  //  - at most kWindow values below the maximum;
-  //  - top-k: none below this CTA's top_k-th largest thread maximum (that
-  //    value is at most the top_k-th largest token of the row);
-  //  - top-p alone: no token whose mass is below (1 - top_p) Z / V (all
-  //    tokens ranked at or below it weigh less than (1 - top_p) Z, so the
-  //    mass ranked before it exceeds top_p Z); half of that bound is used,
-  //    as margin for rounding.
-  uint32_t klo[NR];
-  if (filt) {
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      uint32_t kl = kmax[r] >= static_cast<uint32_t>(kWindow - 1) ? kmax[r] - static_cast<uint32_t>(kWindow - 1) : 0u;
-      const uint32_t kninf = E::key(E::kBytes == 2 ? 0xFF80u : 0xFF800000u);  // -inf
-      if (kl < kninf) kl = kninf;
-      if (topp_on && !topk_on && !any_bad && zfull[r] > 0.0) {
-        const float lim = 0.5f * (1.f - a.top_p) * static_cast<float>(zfull[r]) / static_cast<float>(V);
-        const float vb = m[r] + log2f(lim) / cexp;
-        if (isfinite(vb) && vb > -3.0e38f) {
-          const uint32_t kb = E::key(bits_round_down<DT>(vb));
-          if (kb > kl) kl = kb;
-        }
-      }
-      klo[r] = kl;
-    }
-    if (topp_on && !topk_on && !any_bad) {
-      // a tighter bound from the cluster's warp maxima
-      if (warp < NR)
-        warp_max_bound<CS>(sh, warp, warp == 0 ? m[0] : m[NR - 1], warp == 0 ? zfull[0] : zfull[NR - 1], cexp, a.top_p);
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float cand = sh.w_f[r];
-        if (cand > -INFINITY) {
-          const uint32_t cb = (E::kBytes == 2) ? (__float_as_uint(cand) >> 16) : __float_as_uint(cand);
-          const uint32_t kc = E::key(cb);
-          if (kc > klo[r]) klo[r] = kc;
-        }
-      }
-      __syncthreads();
-    }
-    if (topk_on && !any_bad && a.top_k <= kThreads) {
-      // histogram of the thread maxima, then this CTA's top_k-th largest
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (tmax[r] > -INFINITY) {
-          const uint32_t tb = (E::kBytes == 2) ? (__float_as_uint(tmax[r]) >> 16) : __float_as_uint(tmax[r]);
-          const uint32_t d = kmax[r] - E::key(tb);
-          if (d < static_cast<uint32_t>(kWindow)) red_add_shared(hist + 4u * (r * kWindow + d), 1u);
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const uint32_t dlb = local_bins_reach(hist + 4u * r * kWindow, static_cast<uint32_t>(a.top_k), sh);
-        if (kmax[r] - dlb > klo[r]) klo[r] = kmax[r] - dlb;
-      }
-      for (int t = tid; t < NR * kWindow; t += kThreads) sts_u32(hist + 4u * t, 0u);
-      __syncthreads();
-    }
-    if (!any_bad) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const uint32_t thr = H::thr_pack(E::bits_of_key(klo[r]));
-        const uint32_t hr = hist + 4u * r * kWindow;
-        const uint32_t km = kmax[r];
-        for (int v = tid; v < nfull; v += kThreads) {
-          const uint4 x = lds128(buf[r] + 16u * v);
-          if (!H::any_ge(x, thr)) continue;
-          uint32_t msk = H::mask_ge(x, thr);
-          while (msk) {
-            const int j = __ffs(msk) - 1;
-            msk &= msk - 1u;
-            red_add_shared(hr + 4u * (km - E::key(E::bits_of(x, j))), 1u);
-          }
-        }
-        for (int t = nfull * E::kPerVec + tid; t < n; t += kThreads) {
-          const uint32_t k = E::key(lds_elem<DT>(buf[r], t));
-          if (k >= klo[r]) red_add_shared(hr + 4u * (km - k), 1u);
-        }
-      }
-    }
-    __syncthreads();
-    cluster.sync();  // ---------------------------------------- sync: histogram
-  }
-
-  // ------------------------------------ phase 3b: the kept set of each row
-  if (filt && !any_bad) {
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      bins_partials<DT, CS>(sh, r, hist + 4u * r * kWindow, static_cast<int>(kmax[r] - klo[r]) + 1, kmax[r], m[r],
-                            cexp);
-    __syncthreads();
-  }
-  if (warp < NR) {
-    const int r = warp;
-    // this warp's row, picked without a run-time array index
-    const float m_r = r == 0 ? m[0] : m[NR - 1];
-    const uint32_t kmax_r = r == 0 ? kmax[0] : kmax[NR - 1];
-    const uint32_t klo_r = filt ? (r == 0 ? klo[0] : klo[NR - 1]) : 0u;
-    const double zfull_r = r == 0 ? zfull[0] : zfull[NR - 1];
-    const bool rbad_r = r == 0 ? rbad[0] : rbad[NR - 1];
-    RowStat rs;
-    rs.m = m_r;
-    rs.kmax = kmax_r;
-    rs.kstar = 0u;
-    rs.cstar = 0u;
-    rs.tie_total = 0u;
-    rs.tie_cut = V;
-    rs.zkept = zfull_r;
-    rs.all_kept = 1;
-    rs.bad = rbad_r ? 1 : 0;
-    rs.partial = 0;
-    uint32_t need_fb = 0u;
-    if (!any_bad && filt) {
-      rs.all_kept = 0;
-      const int nbins = static_cast<int>(kmax_r - klo_r) + 1;
-      if (!cut_scan_warp<DT, CS>(sh, r, hist + 4u * r * kWindow, nbins, rs, a.top_k, a.top_p, zfull_r, cexp))
-        need_fb = 1u;
-    }
-    rs.inv_z = 1.f / static_cast<float>(rs.zkept);
-    rs.thr = H::thr_pack(E::bits_of_key(rs.kstar));
-    if (lane == 0) { sh.rs[r] = rs; sh.fb_need[r] = need_fb; }
-  }
-  __syncthreads();
-
-  // ---------------- exact fallback: bitwise search of the cut over the keys
-  {
-    uint32_t slot = 0;
-#pragma unroll 1
-    for (int r = 0; r < NR; ++r) {
-      if (!sh.fb_need[r]) continue;  // identical in every CTA of the cluster
-      fallback_row<DT, CS>(cluster, sh, r == 0 ? buf[0] : buf[NR - 1], n, nvec, r, a.top_k, a.top_p,
-                           r == 0 ? zfull[0] : zfull[NR - 1], cexp, slot);
-    }
-  }
-
-  // ------ phase 3c: where a partial tie stops (only rows with a partial tie)
-  bool part_any = false, part_fb = false;
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    part_any |= sh.rs[r].partial != 0;
-    part_fb |= sh.rs[r].partial != 0 && sh.fb_need[r] != 0;
-  }
-  if (part_any) tie_cuts<DT, CS, NR>(cluster, sh, buf[0], buf[NR - 1], hist, lo, hi, n, V, part_fb);
-  const RowStat rp = sh.rs[0];
-  const RowStat rq = sh.rs[NR - 1];
-
-  // ----------------------------------------------- MODE_PROBS: write rows
-  if (a.mode == MODE_PROBS) {
-    write_probs<DT>(a, buf[0], rp, cexp, unit, lo, n, V);
-    if (rp.bad && crank == 0 && tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
-    cluster.sync();  // ------------------------------------------- sync: exit
-    return;
-  }
-
-  const int kq = a.k;
-  // ------------------------------------- phase 4: accept test at x_pos
-  if constexpr (NR == 2) {
-    const int x = a.tokens[static_cast<size_t>(b) * kq + pos];
-    const bool x_ok = x >= 0 && x < V;
-    UnitRec* rec = a.recs + unit;
-    if (!x_ok || any_bad) {
-      if (crank == 0 && tid == 0) {
-        rec->accept = 0;
-        rec->px = 0.f;
-        rec->qx = 0.f;
-        if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = 0.f;
-        if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = 0.f;
-        set_status(a.status, (!x_ok ? SPEC_STATUS_BAD_TOKEN : 0u) | (any_bad ? SPEC_STATUS_BAD_ROW : 0u));
-        __threadfence();
-        if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-      }
-    } else if (x >= lo && x < hi && tid == 0) {
-      const uint32_t bp = lds_elem<DT>(buf[0], x - lo), bq = lds_elem<DT>(buf[1], x - lo);
-      const bool kp = kept_key(rp, E::key(bp), x);
-      const bool kq2 = kept_key(rq, E::key(bq), x);
-      const float px = kp ? softmax_mass(E::value(bp), rp.m, cexp) / static_cast<float>(rp.zkept) : 0.f;
-      const float qx = kq2 ? softmax_mass(E::value(bq), rq.m, cexp) / static_cast<float>(rq.zkept) : 0.f;
-      const float u = a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
-      rec->accept = (u * qx < px) ? 1 : 0;
-      rec->px = px;
-      rec->qx = qx;
-      if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
-      if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
-      __threadfence();
-      if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-    }
-  }
-
-  // ------------------------- phase 5: residual (or bonus) inverse-CDF draw
-  if (any_bad) {
-    cluster.sync();  // ------------------------------------------- sync: exit
-    if (crank == 0 && tid == 0) {
-      a.recs[unit].drawn = -1;
-      set_status(a.status, SPEC_STATUS_BAD_ROW);
-      __threadfence();
-      if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-    }
-    return;
-  }
-  const float u_draw = a.uniforms[static_cast<size_t>(b) * (kq + 2) + (NR == 2 ? kq + 1 : kq)];
-  bool use_q = NR == 2;
-  double S = 0.0, Pc = 0.0;
-  int owner = -1;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    float s = 0.f;
-    for (int v = seg_beg + lane; v < seg_end; v += 32) {
-      float w[8];
-      const uint4 xp = lds128(buf[0] + 16u * v);
-      const uint4 xq = use_q ? lds128(buf[NR - 1] + 16u * v) : xp;
-      s += vec_weights<DT>(xp, xq, v * E::kPerVec, lo, n, use_q, rp, rq, cexp, w);
-    }
-    s = warp_sum_f32(s);
-    if (lane == 0) sh.w_res[warp] = s;
-    __syncthreads();
-    if (tid == 0) {
-      double t = 0.0;
-      for (int w = 0; w < kWarps; ++w) t += (double)sh.w_res[w];
-      sh.x_res[attempt] = t;
-    }
-    cluster.sync();  // ---------------------------------------- sync: residual
-    if (tid == 0) {  // total, owner CTA and its base, in fixed rank order
-      double sc[CS], tot = 0.0, run = 0.0, pc = 0.0;
-      int own = -1;
-#pragma unroll
-      for (int c = 0; c < CS; ++c) sc[c] = cluster.map_shared_rank(&sh, c)->x_res[attempt];
-#pragma unroll
-      for (int c = 0; c < CS; ++c) tot += sc[c];
-      const double target = (double)u_draw * tot;
-#pragma unroll
-      for (int c = 0; c < CS; ++c) {
-        if (own < 0 && sc[c] > 0.0 && run + sc[c] > target) { own = c; pc = run; }
-        run += sc[c];
-      }
-      sh.b_S = tot;
-      sh.b_Pc = pc;
-      sh.b_owner = own;
-    }
-    __syncthreads();
-    S = sh.b_S;
-    if (S > 0.0 || !use_q) {
-      owner = sh.b_owner;
-      Pc = sh.b_Pc;
-      break;
-    }
-    use_q = false;  // degenerate residual: draw from p instead
-  }
-  cluster.sync();  // ------------------------------------- sync: exit (no DSMEM after this)
-
-  if (owner == crank)
-    draw_walk<DT, NR>(a, sh, buf[0], buf[NR - 1], use_q, rp, rq, cexp, (double)u_draw * S - Pc, lo, n, unit, b);
-
-}
-
-template <int DT, int CS>
-__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
-  using E = Elt<DT>;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int unit = static_cast<int>(blockIdx.x) / CS;
+  const int unit = static_cast<int>(blockIdx.x);
   const int V = a.V;
   __shared__ Shm sh;
-  extern __shared__ __align__(128) unsigned char dsm[];
+  extern __shared__ __align__(16) uint32_t dsm[];
+  uint32_t* lists = dsm;                                // [2][kWarps][kListCap]
+  uint32_t* hist = dsm + 2 * kWarps * kListCap;         // [2][kWindow]
   if (a.mode == MODE_SAMPLE) {
     const int b = unit / (a.k + 1);
     const int pos = unit % (a.k + 1);
@@ -1486,14 +1235,14 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
     if (pos < a.k) {
       const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
                                   (static_cast<size_t>(b) * a.k + pos) * static_cast<size_t>(V) * E::kBytes;
-      unit_body<DT, CS, 2>(a, cluster, sh, dsm, unit, b, pos, rowp, rowq);
+      unit_body<DT, 2>(a, sh, lists, hist, unit, b, pos, rowp, rowq);
     } else {
-      unit_body<DT, CS, 1>(a, cluster, sh, dsm, unit, b, pos, rowp, nullptr);
+      unit_body<DT, 1>(a, sh, lists, hist, unit, b, pos, rowp, rowp);
     }
   } else {
     const unsigned char* rowp =
         static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-    unit_body<DT, CS, 1>(a, cluster, sh, dsm, unit, unit, 0, rowp, nullptr);
+    unit_body<DT, 1>(a, sh, lists, hist, unit, unit, 0, rowp, rowp);
   }
 }
 
@@ -1519,51 +1268,30 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
 
 // ------------------------------------------------------------------ launch
 
-template <int DT, int CS>
+size_t sample_smem_bytes(int dtype, bool filter) {
+  (void)dtype;
+  return filter ? (2 * kWarps * kListCap + 2 * kWindow) * sizeof(uint32_t) : 16;
+}
+
+template <int DT>
 static int launch_one(const SampleArgs& a, int units, size_t smem, cudaStream_t st) {
-  auto kern = sample_kernel<DT, CS>;
+  auto kern = sample_kernel<DT>;
   static size_t configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    if (CS > 8) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
     configured = smem;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * CS));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  kern<<<units, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
-size_t sample_smem_bytes(int dtype, int chunk, bool filter) {
-  const size_t es = dtype == DT_BF16 ? 2 : 4;
-  const size_t buf = (chunk * es + 15) / 16 * 16;
-  return 2 * buf + (filter ? 2 * kWindow * sizeof(uint32_t) : 0);
-}
-
-int launch_sample(const SampleArgs& a, int dtype, int cluster, int units, void* stream) {
+int launch_sample(const SampleArgs& a, int dtype, int units, void* stream) {
   const bool filter = a.top_k > 0 || a.top_p < 1.f;
-  const size_t smem = sample_smem_bytes(dtype, a.chunk, filter);
+  const size_t smem = sample_smem_bytes(dtype, filter);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define SPECV_CASE(D, C) \
-  if (dtype == D && cluster == C) return launch_one<D, C>(a, units, smem, st);
-  SPECV_CASE(DT_BF16, 1) SPECV_CASE(DT_BF16, 2) SPECV_CASE(DT_BF16, 4) SPECV_CASE(DT_BF16, 8) SPECV_CASE(DT_BF16, 16)
-  SPECV_CASE(DT_F32, 1) SPECV_CASE(DT_F32, 2) SPECV_CASE(DT_F32, 4) SPECV_CASE(DT_F32, 8) SPECV_CASE(DT_F32, 16)
-#undef SPECV_CASE
+  if (dtype == DT_BF16) return launch_one<DT_BF16>(a, units, smem, st);
+  if (dtype == DT_F32) return launch_one<DT_F32>(a, units, smem, st);
   return cudaErrorInvalidValue;
 }
 
