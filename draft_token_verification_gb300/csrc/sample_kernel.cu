@@ -47,13 +47,12 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 using u64 = unsigned long long;
 
-constexpr int kListCap = 800;                       // candidate entries per warp per row
+constexpr int kTagCap = 512;                        // candidate vector tags per warp per row
 constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
 constexpr float kTheta = 13.f;                      // octaves of mass kept as candidates
 constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
 constexpr int kGroups = kWindow / 4;                // aligned groups of four keys
 constexpr int kScanWarps = 4;                       // warps that scan one row's histogram
-constexpr int kSegBits = 16;                        // element index within a warp segment
 
 // ------------------------------------------------------- packed f32x2 math
 
@@ -292,31 +291,38 @@ struct CutOut {
   DF zkept;              // mass of the kept set
 };
 
+// Row-wide values after the stream (the same for every thread).
+struct RowG {
+  float m;               // row maximum
+  float K;               // lattice exponent
+  uint32_t kmax;         // key of m
+  uint32_t klo;          // lowest key of the scanned window
+  DF z;                  // sum of masses 2^(l c - K)
+  int active;            // the row takes part in the current scan
+};
+
 struct Shm {
   float w_m[kWarps][2];
   int w_k[kWarps][2];
   float w_z[kWarps][2];
-  uint32_t w_n[kWarps][2];     // candidate list lengths
-  uint32_t w_floor[kWarps][2]; // key above which a warp's list is complete
-  float x_m[2][kWarps][2];     // running maxima exchanged while streaming (double-buffered)
+  uint32_t w_floor[kWarps][2]; // key above which a warp's tag list is complete
+  uint32_t w_over[kWarps][2];  // a warp's gather overflowed
   float w_s[kWarps];
   float w_sp[kWarps];
   uint32_t w_u[kWarps][2];
-  double w_d[kWarps];
+  float x_m[2][kWarps][2];     // running maxima exchanged while streaming (double-buffered)
+  uint32_t xbits[2];           // the draft token's value in the target and draft rows
   uint32_t s_C[2][kScanWarps];
   DF s_M[2][kScanWarps];
-  DF z[2];                     // row sums of masses
+  RowG g[2];
   CutOut cutk[2];
   CutOut cut[2];
-  uint32_t klo[2];
   int tie_warp[2];
   uint32_t tie_j[2];
   int tie_cut[2];
   RowStat rs[2];
   int draw_warp;
   float draw_base;
-  double red_d;
-  uint32_t red_u, red_k;
 };
 
 // 16-byte vector v of a row (elements v*kPerVec ...), -inf beyond n.
@@ -478,13 +484,14 @@ __device__ __noinline__ CutOut search_cut(Shm& sh, const unsigned char* row, int
 
 // ------------------------------------------------------ segments & lists
 
-// Warp w owns vectors [seg_beg, seg_end) of a row: consecutive vectors in
-// index order (iteration, lane, element).
+// Warp w owns vectors [beg, end) of a row: consecutive vectors in index
+// order (iteration, lane, element).
 struct Seg {
   int beg, end, iters;
 };
+__device__ __forceinline__ int seg_vectors(int nvec) { return ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32; }
 __device__ __forceinline__ Seg warp_seg(int nvec, int warp) {
-  const int vpw = ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int vpw = seg_vectors(nvec);
   Seg s;
   s.beg = min(nvec, warp * vpw);
   s.end = min(nvec, s.beg + vpw);
@@ -492,35 +499,231 @@ __device__ __forceinline__ Seg warp_seg(int nvec, int warp) {
   return s;
 }
 
-// List entry: element index within the warp segment (high 16 bits) and the
-// element's 16-bit pattern (low 16 bits).  Lists are bf16 only.
-__device__ __forceinline__ uint32_t entry_make(uint32_t local, uint32_t bits) { return (local << 16) | bits; }
-__device__ __forceinline__ uint32_t entry_local(uint32_t e) { return e >> 16; }
-__device__ __forceinline__ uint32_t entry_bits(uint32_t e) { return e & 0xFFFFu; }
+// Tag of a candidate vector: its index within the warp segment (high 16
+// bits) and the key of its maximum (low 16 bits, bf16 keys).  A warp's tags
+// are kept in index order.
+__device__ __forceinline__ uint32_t tag_make(uint32_t local, uint32_t key) { return (local << 16) | key; }
+__device__ __forceinline__ uint32_t tag_local(uint32_t t) { return t >> 16; }
+__device__ __forceinline__ uint32_t tag_key(uint32_t t) { return t & 0xFFFFu; }
 
-// Keeps, in order, the entries of one warp's list whose key is at least
-// kthr; returns the new length.  Whole warp.
-__device__ __forceinline__ uint32_t list_purge(uint32_t* list, uint32_t len, uint32_t kthr) {
+// Keeps, in order, the tags whose key is at least kthr; new length.  Warp.
+__device__ __forceinline__ uint32_t tags_purge(uint32_t* tags, uint32_t len, uint32_t kthr) {
   const int lane = threadIdx.x & 31;
   uint32_t out = 0;
   for (uint32_t base = 0; base < len; base += 32) {
     const uint32_t i = base + lane;
-    const uint32_t e = i < len ? list[i] : 0u;
-    const bool keep = i < len && Elt<DT_BF16>::key(entry_bits(e)) >= kthr;
+    const uint32_t t = i < len ? tags[i] : 0u;
+    const bool keep = i < len && tag_key(t) >= kthr;
     const unsigned ball = __ballot_sync(kFull, keep);
     __syncwarp();
-    if (keep) list[out + __popc(ball & ((1u << lane) - 1u))] = e;
+    if (keep) tags[out + __popc(ball & ((1u << lane) - 1u))] = t;
     out += __popc(ball);
     __syncwarp();
   }
   return out;
 }
 
-// Tie cut from one warp-ordered set of tokens of value kstar: every warp
-// counts its tokens (list entries or segment elements), the warp holding the
-// keep-th one (0-based) finds its row index.  Whole CTA.
+// Smallest key kf >= klow such that at most half the capacity of tags
+// (listed ones, plus this lane's pending key if any) have key >= kf.  Warp.
+__device__ __noinline__ uint32_t tags_half_key(const uint32_t* tags, uint32_t len, uint32_t klow, uint32_t pend) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = kTagCap / 32;
+  uint32_t keys[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const uint32_t i = q * 32 + lane;
+    keys[q] = i < len ? tag_key(tags[i]) : 0u;
+  }
+  uint32_t lo = klow, hi = 0x10000u;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    uint32_t c = pend >= mid ? 1u : 0u;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) c += keys[q] >= mid ? 1u : 0u;
+    c = warp_sum_u32(c);
+    if (c <= static_cast<uint32_t>(kTagCap) / 2u) hi = mid;
+    else lo = mid + 1u;
+  }
+  return lo;
+}
+
+// The gathered vectors of one warp and row: its tags at or above the bound
+// (index order); the vectors themselves are read from the row on demand.
+struct GList {
+  const uint32_t* tags;
+  const unsigned char* row;
+};
+
+// Position of local vector index vi among index-ordered tags, or -1.
+__device__ __forceinline__ int glist_find(const uint32_t* tags, uint32_t len, uint32_t vi) {
+  int lo = 0, hi = static_cast<int>(len) - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const uint32_t x = tag_local(tags[mid]);
+    if (x == vi) return mid;
+    if (x < vi) lo = mid + 1;
+    else hi = mid - 1;
+  }
+  return -1;
+}
+
+// The cut of each active row from a histogram of exact keys (slot
+// key & (kWindow - 1), keys g.klo .. g.kmax): four warps per row scan groups
+// of four keys from the top with double-float prefix sums.  Top-k: where the
+// running count reaches top_k (sh.cutk); top-p (on the top-k set, if any):
+// where the running mass reaches top_p * Z, a token being kept while the
+// mass ranked before it is below the target (sh.cut).  Rows whose cut lies
+// below the window keep found = 0.  Whole CTA.
+template <int DT, int NR>
+__device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, int top_k, float top_p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  const int r_s = (NR == 2) ? (warp >> 2) : 0;
+  const int wq = warp & (kScanWarps - 1);
+  const RowG g = sh.g[r_s];
+  const bool scanner = ((NR == 2) || warp < kScanWarps) && g.active;
+  if (threadIdx.x < 2) { sh.cut[threadIdx.x].found = 0; sh.cutk[threadIdx.x].found = 0; }
+  uint32_t cnt[4] = {0u, 0u, 0u, 0u}, top = 0u, Cl = 0u, Cex = 0u;
+  float ms[4] = {0.f, 0.f, 0.f, 0.f}, Ml = 0.f;
+  DF Mex{0.f, 0.f};
+  bool valid = false;
+  if (scanner) {
+    const uint32_t gtop = g.kmax >> 2;
+    const uint32_t gi = static_cast<uint32_t>(wq * 32 + lane);
+    if (gi <= gtop) {
+      const uint32_t grp = gtop - gi;
+      top = 4u * grp + 3u;
+      if (top >= g.klo) {
+        valid = true;
+        const uint4 h4 = lds128(smem_addr(hist + r_s * kWindow + 4u * (grp & static_cast<uint32_t>(kGroups - 1))));
+        const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // keys top, top-1, top-2, top-3
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t key = top - static_cast<uint32_t>(j);
+          const uint32_t s = (key > g.kmax || key < g.klo) ? 0u : hv[j];
+          cnt[j] = s;
+          ms[j] = s ? lat_mass(value_of_key<DT>(key), c, g.K) : 0.f;
+          Cl += s;
+          Ml += static_cast<float>(s) * ms[j];
+        }
+      }
+    }
+    const uint32_t Cin = warp_incl_scan_u32(Cl);
+    const DF Min = warp_incl_scan_df(DF{Ml, 0.f});
+    Cex = Cin - Cl;
+    Mex = df_shfl_up(Min, 1);
+    if (lane == 0) Mex = DF{0.f, 0.f};
+    if (lane == 31) {
+      sh.s_C[r_s][wq] = Cin;
+      sh.s_M[r_s][wq] = Min;
+    }
+  }
+  __syncthreads();
+  uint32_t offC = 0u;
+  DF offM{0.f, 0.f}, nxtM{0.f, 0.f}, totM{0.f, 0.f};
+  if (scanner) {
+#pragma unroll
+    for (int q = 0; q < kScanWarps; ++q) {
+      const uint32_t cq = sh.s_C[r_s][q];
+      const DF mq = sh.s_M[r_s][q];
+      if (q < wq) { offC += cq; offM = df_add2(offM, mq); }
+      if (q <= wq) nxtM = df_add2(nxtM, mq);
+      totM = df_add2(totM, mq);
+    }
+  }
+  if (topk_on && scanner) {  // the value where the running count reaches top_k
+    const uint32_t Kc = static_cast<uint32_t>(top_k);
+    const uint32_t wC = sh.s_C[r_s][wq];
+    if (offC < Kc && offC + wC >= Kc) {
+      const uint32_t cb = offC + Cex;
+      const unsigned ball = __ballot_sync(kFull, valid && cb < Kc);
+      const int l = 31 - __clz(ball | 1u);
+      if (lane == l && valid && cb < Kc) {
+        uint32_t run = cb;
+        DF mb = df_add2(offM, Mex);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (run < Kc && run + cnt[j] >= Kc) {
+            CutOut co;
+            co.kstar = top - static_cast<uint32_t>(j);
+            co.keep = Kc - run;
+            co.total = cnt[j];
+            co.found = 1;
+            co.zkept = df_add(mb, static_cast<float>(Kc - run) * ms[j]);
+            sh.cutk[r_s] = co;
+            if (!topp_on) sh.cut[r_s] = co;
+          }
+          run += cnt[j];
+          mb = df_add(mb, static_cast<float>(cnt[j]) * ms[j]);
+        }
+      }
+    }
+  }
+  if (topk_on && topp_on) __syncthreads();
+  if (topp_on && scanner) {
+    const CutOut ck = sh.cutk[r_s];
+    if (!topk_on || ck.found) {
+      const DF target = df_mul_f(topk_on ? ck.zkept : g.z, top_p);
+      // (a window holding less than the target leaves the cut unfound)
+      const bool wlast = !df_lt(totM, target) && df_lt(offM, target) &&
+                         (wq == kScanWarps - 1 || !df_lt(nxtM, target));
+      if (wlast) {
+        const DF mbl = df_add2(offM, Mex);
+        const unsigned ball = __ballot_sync(kFull, valid && df_lt(mbl, target));
+        const int l = 31 - __clz(ball | 1u);
+        if (lane == l && valid && df_lt(mbl, target)) {
+          DF mb = mbl, mb_last{0.f, 0.f};
+          int jl = -1;
+          uint32_t cl = 0u;
+          bool done = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t key = top - static_cast<uint32_t>(j);
+            uint32_t ce = cnt[j];
+            if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
+            if (!done && ce > 0u) {
+              const DF after = df_add(mb, static_cast<float>(ce) * ms[j]);
+              jl = j;
+              cl = ce;
+              mb_last = mb;
+              if (!df_lt(after, target)) {
+                const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
+                uint32_t keep = static_cast<uint32_t>(ceilf(need / ms[j]));
+                keep = max(1u, min(keep, ce));
+                CutOut co;
+                co.kstar = key;
+                co.keep = keep;
+                co.total = cnt[j];
+                co.found = 1;
+                co.zkept = df_add(mb, static_cast<float>(keep) * ms[j]);
+                sh.cut[r_s] = co;
+                done = true;
+              }
+              mb = after;
+            }
+          }
+          if (!done && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
+            CutOut co;
+            co.kstar = top - static_cast<uint32_t>(jl);
+            co.keep = cl;
+            co.total = cnt[jl];
+            co.found = 1;
+            co.zkept = df_add(mb_last, static_cast<float>(cl) * ms[jl]);
+            sh.cut[r_s] = co;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Tie cut of a row: tokens of value kstar are kept in index order, the
+// first `keep` of them.  Every warp counts its tokens (in its gathered
+// vectors, or in its segment of the row re-read), the warp holding token
+// number `keep` (0-based) finds its row index.  Whole CTA.
 template <int DT, bool FROM_LIST>
-__device__ __noinline__ int tie_cut_of(Shm& sh, const uint32_t* list, uint32_t len, const unsigned char* row, int V,
+__device__ __noinline__ int tie_cut_of(Shm& sh, const GList& L, uint32_t len, const unsigned char* row, int V,
                                        bool aligned, uint32_t kstar, uint32_t keep) {
   using E = Elt<DT>;
   using H = Hot<DT>;
@@ -528,14 +731,25 @@ __device__ __noinline__ int tie_cut_of(Shm& sh, const uint32_t* list, uint32_t l
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
   const Seg sg = warp_seg(nvec, warp);
   const uint32_t thr = H::thr_pack(E::bits_of_key(kstar));
-  uint32_t c = 0;
-  if (FROM_LIST) {
-    for (uint32_t i = lane; i < len; i += 32) c += (E::key(entry_bits(list[i])) == kstar) ? 1u : 0u;
-  } else {
-    for (int v = sg.beg + lane; v < sg.end; v += 32) {
-      const uint4 x = load_vec<DT>(row, v, V, aligned);
-      c += __popc(H::mask_eq(x, thr) & vmask<DT>(v, V));
+  const int rounds = FROM_LIST ? static_cast<int>((len + 31) / 32) : sg.iters;
+  auto vec_at = [&](int it, uint4& x) -> int {
+    if (FROM_LIST) {
+      const uint32_t i = it * 32 + lane;
+      if (i >= len) return -1;
+      const int v = sg.beg + static_cast<int>(tag_local(L.tags[i]));
+      x = load_vec<DT>(L.row, v, V, aligned);
+      return v;
     }
+    const int v = sg.beg + it * 32 + lane;
+    if (v >= sg.end) return -1;
+    x = load_vec<DT>(row, v, V, aligned);
+    return v;
+  };
+  uint32_t c = 0;
+  for (int it = 0; it < rounds; ++it) {
+    uint4 x;
+    const int v = vec_at(it, x);
+    if (v >= 0) c += __popc(H::mask_eq(x, thr) & vmask<DT>(v, V));
   }
   c = warp_sum_u32(c);
   if (lane == 0) sh.w_u[warp][0] = c;
@@ -552,22 +766,10 @@ __device__ __noinline__ int tie_cut_of(Shm& sh, const uint32_t* list, uint32_t l
   __syncthreads();
   if (warp == sh.tie_warp[0]) {
     uint32_t jj = sh.tie_j[0];
-    const int seg_lo = sg.beg * E::kPerVec;
-    const int rounds = FROM_LIST ? static_cast<int>((len + 31) / 32) : sg.iters;
     for (int it = 0; it < rounds; ++it) {
-      uint32_t msk = 0u;
-      int base_idx = 0;
-      if (FROM_LIST) {
-        const uint32_t i = it * 32 + lane;
-        if (i < len && E::key(entry_bits(list[i])) == kstar) {
-          msk = 1u;
-          base_idx = seg_lo + static_cast<int>(entry_local(list[i]));
-        }
-      } else {
-        const int v = sg.beg + it * 32 + lane;
-        if (v < sg.end) msk = H::mask_eq(load_vec<DT>(row, v, V, aligned), thr) & vmask<DT>(v, V);
-        base_idx = v * E::kPerVec;
-      }
+      uint4 x;
+      const int v = vec_at(it, x);
+      const uint32_t msk = v >= 0 ? (H::mask_eq(x, thr) & vmask<DT>(v, V)) : 0u;
       const uint32_t cc = __popc(msk);
       const uint32_t incl = warp_incl_scan_u32(cc);
       const uint32_t tot = __shfl_sync(kFull, incl, 31);
@@ -575,7 +777,7 @@ __device__ __noinline__ int tie_cut_of(Shm& sh, const uint32_t* list, uint32_t l
         if (incl > jj && incl - cc <= jj) {
           uint32_t mm = msk;
           for (uint32_t q = jj - (incl - cc); q > 0; --q) mm &= mm - 1u;
-          sh.tie_cut[0] = FROM_LIST ? base_idx : base_idx + (__ffs(mm) - 1);
+          sh.tie_cut[0] = v * E::kPerVec + (__ffs(mm) - 1);
         }
         break;
       }
@@ -604,22 +806,41 @@ __device__ __noinline__ void write_probs(const unsigned char* row, int V, bool a
   }
 }
 
-// Draw weight of token j: max(0, p - q) (residual) or p (bonus / degenerate).
+// Draw weights of the elements of one vector (row index v): max(0, p - q)
+// (use_q) or p.  xq: the draft row's vector, or null when it holds no kept
+// token of q.  Returns the sum; *ps gets the sum of p.
 template <int DT>
-__device__ __forceinline__ float weight_of(const RowStat& rp, const RowStat& rq, uint32_t bp, const unsigned char* rowq,
-                                           int j, bool use_q, float* pv_out) {
-  const float pv = prob_of<DT>(rp, bp, j);
-  *pv_out = pv;
-  if (!use_q || pv == 0.f) return pv;
-  const float qv = prob_of<DT>(rq, Elt<DT>::bits_at(rowq, j), j);
-  return fmaxf(pv - qv, 0.f);
+__device__ __forceinline__ float vec_weights(const RowStat& rp, const RowStat& rq, const uint4& xp, const uint4* xq, int v,
+                                             int V, bool use_q, float* w, float* ps) {
+  using E = Elt<DT>;
+  float s = 0.f, sp = 0.f;
+  const uint32_t vm = vmask<DT>(v, V);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = 0.f;
+#pragma unroll
+  for (int j = 0; j < E::kPerVec; ++j) {
+    if ((vm >> j) & 1u) {
+      const int t = v * E::kPerVec + j;
+      const float pv = prob_of<DT>(rp, E::bits_of(xp, j), t);
+      float wj = pv;
+      if (use_q) {
+        const float qv = (xq && pv > 0.f) ? prob_of<DT>(rq, E::bits_of(*xq, j), t) : 0.f;
+        wj = fmaxf(pv - qv, 0.f);
+      }
+      w[j] = wj;
+      s += wj;
+      sp += pv;
+    }
+  }
+  *ps = sp;
+  return s;
 }
 
 }  // namespace
 
 // One unit (b, pos) with NR rows (2: target and draft, 1: target only).
 template <int DT, int NR>
-__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* lists, uint32_t* hist, int unit, int b,
+__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* tags, uint32_t* hist, int unit, int b,
                                           int pos, const unsigned char* rowp, const unsigned char* rowq) {
   using E = Elt<DT>;
   using H = Hot<DT>;
@@ -636,14 +857,22 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
   const bool topk_on = a.top_k > 0;
   const bool topp_on = a.top_p < 1.f;
   const bool filt = topk_on || topp_on;
-  // candidate lists: bf16 rows with a cut, segments short enough to index
-  const bool use_lists = DT == DT_BF16 && filt && !bad_t && (sg.end - sg.beg) * E::kPerVec <= (1 << kSegBits) &&
-                         ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32 * E::kPerVec <= (1 << kSegBits);
+  const int kq = a.k;
+  const int xtok = (NR == 2 && a.mode == MODE_SAMPLE) ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
+  // candidate tags: bf16 rows with a cut, segments short enough to index
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= 65536;
   const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
-  uint32_t* wl[2] = {lists + (0 * kWarps + warp) * kListCap, lists + (1 * kWarps + warp) * kListCap};
+  uint32_t* wt[2] = {tags + (0 * kWarps + warp) * kTagCap, tags + (1 * kWarps + warp) * kTagCap};
+  GList gl[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    gl[r].tags = wt[r];
+    gl[r].row = rows[r];
+  }
 
   if (filt)
     for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
+  if (tid < 2) sh.xbits[tid] = 0u;
   __syncthreads();
 
   // --------------------------------------------------- phase 1: stream
@@ -651,11 +880,14 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
   int kt[NR];               // thread lattice exponent
   u64 acc0[NR], acc1[NR];   // thread sums of 2^(l c - kt)
   float mw[NR];             // running maximum known to the warp (uniform)
-  uint32_t len[NR];         // list lengths (uniform)
-  uint32_t kthr[NR];        // current list bound, as a key (uniform)
-  uint32_t kfloor[NR];      // raised bound: the list is complete above it
+  uint32_t len[NR];         // tag list lengths (uniform)
+  uint32_t kthr[NR];        // current tag bound, as a key (uniform)
+  uint32_t kfloor[NR];      // raised bound: the tag list is complete above it
+  float thr_v[NR];          // value of kthr
+  int sync_no = 0;
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
+    thr_v[r] = -INFINITY;
     mt[r] = -INFINITY;
     kt[r] = -(1 << 30);
     acc0[r] = 0ull;
@@ -665,8 +897,9 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     kthr[r] = 0u;
     kfloor[r] = 0u;
   }
+  const int xv = xtok >= 0 && xtok < V ? xtok / E::kPerVec : -1;
   // every warp runs the same number of iterations (the CTA barriers below)
-  const int iters_all = (((nvec + kWarps - 1) / kWarps + 31) / 32 * 32) / 32;
+  const int iters_all = seg_vectors(nvec) / 32;
   for (int it = 0; it < iters_all; it += 2) {
     const int v0 = sg.beg + it * 32 + lane;
     const int v1 = v0 + 32;
@@ -693,56 +926,50 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
         const float nk = -static_cast<float>(kt[r]);
         H::mass_vec(x[r][u], c2, pkf(nk, nk), acc0[r], acc1[r]);
         mt[r] = max_nan(mt[r], vm[u]);
+        if (v0 + 32 * u == xv && xv < sg.end) sh.xbits[r] = E::bits_of(x[r][u], xtok - xv * E::kPerVec);
       }
       if (use_lists) {
-        // the bound: kTheta octaves below the running maximum (at most the
+        // tag bound: kTheta octaves below the running maximum (at most the
         // row maximum), never below the raised floor
         const float m_new = warp_max_nan(max_nan(vm[0], vm[1]));
-        if (m_new > mw[r]) mw[r] = m_new;
-        {
+        if (m_new > mw[r]) {
+          mw[r] = m_new;
           const float tv = mw[r] - dtheta;
-          const uint32_t kb = tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u;
-          kthr[r] = max(kfloor[r], kb);
+          kthr[r] = max(kfloor[r], tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u);
+          thr_v[r] = value_of_key<DT>(kthr[r]);
         }
-        // candidates: elements at or above the bound, appended in index order
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int v = v0 + 32 * u;
-          for (;;) {
-            const float thr_v = value_of_key<DT>(kthr[r]);
-            const bool any = v < sg.end && vm[u] >= thr_v;
-            if (__ballot_sync(kFull, any) == 0u) break;
-            const uint32_t msk = any ? (H::mask_ge(x[r][u], H::thr_pack(E::bits_of_key(kthr[r]))) & vmask<DT>(v, V)) : 0u;
-            const uint32_t cnt = __popc(msk);
-            const uint32_t incl = warp_incl_scan_u32(cnt);
-            const uint32_t tot = __shfl_sync(kFull, incl, 31);
-            if (len[r] + tot > static_cast<uint32_t>(kListCap)) {
-              len[r] = list_purge(wl[r], len[r], kthr[r]);
-              if (len[r] + tot > static_cast<uint32_t>(kListCap)) {
-                // still full: raise the floor (a step toward the warp maximum)
-                const uint32_t kmw = key_of_float<DT>(mw[r]);
-                const uint32_t step = kmw > kthr[r] ? max(1u, (kmw - kthr[r]) / 8u) : 1u;
-                kfloor[r] = kthr[r] + step;
-                kthr[r] = kfloor[r];
-                continue;
-              }
+          bool flag = v < sg.end && vm[u] >= thr_v[r];
+          unsigned ball = __ballot_sync(kFull, flag);
+          if (ball == 0u) continue;
+          uint32_t n = __popc(ball);
+          if (len[r] + n > static_cast<uint32_t>(kTagCap)) {  // full: purge to the bound, then halve
+            const uint32_t kv = flag ? key_of_float<DT>(vm[u]) : 0u;
+            len[r] = tags_purge(wt[r], len[r], kthr[r]);
+            if (len[r] + n > static_cast<uint32_t>(kTagCap) / 2u) {
+              kfloor[r] = tags_half_key(wt[r], len[r], kthr[r], kv);
+              kthr[r] = max(kthr[r], kfloor[r]);
+              thr_v[r] = value_of_key<DT>(kthr[r]);
+              len[r] = tags_purge(wt[r], len[r], kthr[r]);
+              flag = flag && kv >= kthr[r];
+              ball = __ballot_sync(kFull, flag);
+              n = __popc(ball);
             }
-            uint32_t pos_w = len[r] + incl - cnt;
-            uint32_t mm = msk;
-            while (mm) {
-              const int j = __ffs(mm) - 1;
-              mm &= mm - 1u;
-              wl[r][pos_w++] = entry_make(static_cast<uint32_t>((v - sg.beg) * 8 + j), E::bits_of(x[r][u], j));
-            }
-            len[r] += tot;
-            break;
           }
+          if (flag)
+            wt[r][len[r] + __popc(ball & ((1u << lane) - 1u))] =
+                tag_make(static_cast<uint32_t>(v - sg.beg), key_of_float<DT>(vm[u]));
+          len[r] += n;
         }
       }
     }
-    if (use_lists && ((it >> 1) % kSyncEvery) == kSyncEvery - 1) {
-      // share the running maxima across the CTA (fixed points: deterministic)
-      const int slot = ((it >> 1) / kSyncEvery) & 1;
+    const int li = it >> 1;  // loop iteration
+    if (use_lists && (li < kSyncEvery ? (li & (li + 1)) == 0 : (li % kSyncEvery) == kSyncEvery - 1)) {
+      // share the running maxima across the CTA (fixed points, denser at the
+      // start where they rise fastest: deterministic)
+      const int slot = (sync_no++) & 1;
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) sh.x_m[slot][warp][r] = mw[r];
@@ -753,7 +980,12 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
         float mm = mw[r];
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][r]);
-        mw[r] = mm;
+        if (mm > mw[r]) {
+          mw[r] = mm;
+          const float tv = mw[r] - dtheta;
+          kthr[r] = max(kfloor[r], tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u);
+          thr_v[r] = value_of_key<DT>(kthr[r]);
+        }
       }
     }
   }
@@ -774,16 +1006,14 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
       sh.w_m[warp][r] = mx;
       sh.w_k[warp][r] = kw;
       sh.w_z[warp][r] = zt;
-      sh.w_n[warp][r] = len[r];
       sh.w_floor[warp][r] = kfloor[r];
+      sh.w_over[warp][r] = 0u;
     }
   }
   __syncthreads();
-  float m[NR], K[NR];
-  bool bad[NR], cov[NR];
   bool any_bad = bad_t;
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
+  if (tid < NR) {
+    const int r = tid;
     float mx = -INFINITY;
     int kk = -(1 << 30);
 #pragma unroll
@@ -794,13 +1024,28 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     DF z{0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) z = df_add(z, sh.w_z[w][r] * exp2i(sh.w_k[w][r] - kk));
-    m[r] = mx;
-    K[r] = static_cast<float>(kk);
+    RowG g;
+    g.m = mx;
+    g.K = static_cast<float>(kk);
+    g.kmax = key_of_float<DT>(mx);
+    g.z = z;
+    // every vector whose maximum reaches klo is tagged
+    const float tv = mx - dtheta;
+    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
+    const uint32_t gtop = g.kmax >> 2;
+    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][r]);
+    g.klo = kl;
+    g.active = use_lists ? 1 : 0;
+    sh.g[r] = g;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const float mx = sh.g[r].m;
     // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
-    bad[r] = bad_t || !isfinite(mx) || !(fabsf(mx * c) < 1073741824.f);
-    any_bad |= bad[r];
-    cov[r] = use_lists;
-    if (tid == 0) sh.z[r] = z;
+    any_bad |= !isfinite(mx) || !(fabsf(mx * c) < 1073741824.f);
   }
 
   if (any_bad) {
@@ -809,14 +1054,12 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
       for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
       if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
     } else if (tid == 0) {
-      const int kq = a.k;
       UnitRec* rec = a.recs + unit;
       uint32_t add = 1u;
       uint32_t st = SPEC_STATUS_BAD_ROW;
       rec->drawn = -1;
       if (NR == 2) {
-        const int x = a.tokens[static_cast<size_t>(b) * kq + pos];
-        if (!(x >= 0 && x < V)) st |= SPEC_STATUS_BAD_TOKEN;
+        if (!(xtok >= 0 && xtok < V)) st |= SPEC_STATUS_BAD_TOKEN;
         rec->accept = 0;
         rec->px = 0.f;
         rec->qx = 0.f;
@@ -832,204 +1075,94 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     return;
   }
 
-  // --------------------------- phase 3: histogram of the candidates' values
-  // Every element within kTheta octaves of the row maximum (key >= klo) is
-  // on a list; the histogram covers keys klo .. kmax (at most kWindow).
-  uint32_t klo[NR];
+  // ---------- phase 3: a bound on the cut from the tagged vector maxima
+  // The tags hold every vector whose maximum reaches klo.  Vector maxima are
+  // tokens of the row, so the mass (or count) of the row above a value is at
+  // least that of the maxima above it: where the maxima reach the top-p
+  // target (or top_k), the row's cut lies at or above.
+  uint32_t ngat[NR];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    const uint32_t kmax = key_of_float<DT>(m[r]);
-    const float tv = m[r] - dtheta;
-    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
-    const uint32_t gtop = kmax >> 2;
-    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
-    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][r]);  // every list is complete above kl
-    klo[r] = kl;
-    if (cov[r]) {
-      for (int w = 0; w < kWarps; ++w) {
-        const uint32_t n_w = sh.w_n[w][r];
-        const uint32_t* lw = lists + (r * kWarps + w) * kListCap;
-        for (uint32_t i = tid; i < n_w; i += kThreads) {
-          const uint32_t k = E::key(entry_bits(lw[i]));
-          if (k >= kl) red_add_shared(smem_addr(hist + r * kWindow + (k & kSlotMask)), 1u);
-        }
-      }
-    }
-  }
-  if (tid < 2) { sh.cut[tid].found = 0; sh.cutk[tid].found = 0; }
-  __syncthreads();
-
-  // ---------------------------------------------- phase 4: the cut scan
-  if (filt) {
-    const int r_s = (NR == 2) ? (warp >> 2) : 0;
-    const int wq = warp & (kScanWarps - 1);
-    const bool scanner = ((NR == 2) || warp < kScanWarps) && (r_s == 0 ? cov[0] : cov[NR - 1]);
-    const float m_s = r_s == 0 ? m[0] : m[NR - 1];
-    const float K_s = r_s == 0 ? K[0] : K[NR - 1];
-    const uint32_t klo_s = r_s == 0 ? klo[0] : klo[NR - 1];
-    const uint32_t kmax_s = key_of_float<DT>(m_s);
-    uint32_t cnt[4] = {0u, 0u, 0u, 0u}, top = 0u, Cl = 0u, Cex = 0u;
-    float ms[4] = {0.f, 0.f, 0.f, 0.f}, Ml = 0.f;
-    DF Mex{0.f, 0.f};
-    bool valid = false;
-    if (scanner) {
-      const uint32_t gtop = kmax_s >> 2;
-      const uint32_t gi = static_cast<uint32_t>(wq * 32 + lane);
-      if (gi <= gtop) {
-        const uint32_t grp = gtop - gi;
-        top = 4u * grp + 3u;
-        if (top >= klo_s) {
-          valid = true;
-          const uint4 h4 = lds128(smem_addr(hist + r_s * kWindow + 4u * (grp & static_cast<uint32_t>(kGroups - 1))));
-          const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // keys top, top-1, top-2, top-3
+  for (int r = 0; r < NR; ++r) ngat[r] = 0u;
+  bool fast[NR];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t key = top - static_cast<uint32_t>(j);
-            const uint32_t s = (key > kmax_s || key < klo_s) ? 0u : hv[j];
-            cnt[j] = s;
-            ms[j] = s ? lat_mass(value_of_key<DT>(key), c, K_s) : 0.f;
-            Cl += s;
-            Ml += static_cast<float>(s) * ms[j];
-          }
-        }
-      }
-      const uint32_t Cin = warp_incl_scan_u32(Cl);
-      const DF Min = warp_incl_scan_df(DF{Ml, 0.f});
-      Cex = Cin - Cl;
-      Mex = df_shfl_up(Min, 1);
-      if (lane == 0) Mex = DF{0.f, 0.f};
-      if (lane == 31) {
-        sh.s_C[r_s][wq] = Cin;
-        sh.s_M[r_s][wq] = Min;
+  for (int r = 0; r < NR; ++r) fast[r] = false;
+  if (use_lists) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const uint32_t kl = sh.g[r].klo;
+      for (uint32_t i = lane; i < len[r]; i += 32) {
+        const uint32_t k = tag_key(wt[r][i]);
+        if (k >= kl) red_add_shared(smem_addr(hist + r * kWindow + (k & kSlotMask)), 1u);
       }
     }
     __syncthreads();
-    uint32_t offC = 0u;
-    DF offM{0.f, 0.f}, nxtM{0.f, 0.f}, totM{0.f, 0.f};
-    if (scanner) {
+    cut_scan<DT, NR>(sh, hist, c, a.top_k, a.top_p);
+    // bound (top-k: its own cut; top-p alone: the maxima's crossing)
+    uint32_t tau[NR];
 #pragma unroll
-      for (int q = 0; q < kScanWarps; ++q) {
-        const uint32_t cq = sh.s_C[r_s][q];
-        const DF mq = sh.s_M[r_s][q];
-        if (q < wq) { offC += cq; offM = df_add2(offM, mq); }
-        if (q <= wq) nxtM = df_add2(nxtM, mq);
-        totM = df_add2(totM, mq);
-      }
-    }
-    if (topk_on && scanner) {  // the value where the running count reaches top_k
-      const uint32_t Kc = static_cast<uint32_t>(a.top_k);
-      const uint32_t wC = sh.s_C[r_s][wq];
-      if (offC < Kc && offC + wC >= Kc) {
-        const uint32_t cb = offC + Cex;
-        const unsigned ball = __ballot_sync(kFull, valid && cb < Kc);
-        const int l = 31 - __clz(ball | 1u);
-        if (lane == l && valid && cb < Kc) {
-          uint32_t run = cb;
-          DF mb = df_add2(offM, Mex);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (run < Kc && run + cnt[j] >= Kc) {
-              CutOut co;
-              co.kstar = top - static_cast<uint32_t>(j);
-              co.keep = Kc - run;
-              co.total = cnt[j];
-              co.found = 1;
-              co.zkept = df_add(mb, static_cast<float>(Kc - run) * ms[j]);
-              sh.cutk[r_s] = co;
-              if (!topp_on) sh.cut[r_s] = co;
-            }
-            run += cnt[j];
-            mb = df_add(mb, static_cast<float>(cnt[j]) * ms[j]);
-          }
-        }
-      }
-    }
-    if (topk_on && topp_on) __syncthreads();
-    if (topp_on && scanner) {  // a token is kept while the mass ranked before it is below top_p * Z
-      const CutOut ck = sh.cutk[r_s];
-      if (!topk_on || ck.found) {
-        const DF target = df_mul_f(topk_on ? ck.zkept : sh.z[r_s], a.top_p);
-        const bool wlast = !df_lt(totM, target) && df_lt(offM, target) &&
-                           (wq == kScanWarps - 1 || !df_lt(nxtM, target));
-        if (wlast) {
-          const DF mbl = df_add2(offM, Mex);
-          const unsigned ball = __ballot_sync(kFull, valid && df_lt(mbl, target));
-          const int l = 31 - __clz(ball | 1u);
-          if (lane == l && valid && df_lt(mbl, target)) {
-            DF mb = mbl, mb_last{0.f, 0.f};
-            int jl = -1;
-            uint32_t cl = 0u;
-            bool done = false;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t key = top - static_cast<uint32_t>(j);
-              uint32_t ce = cnt[j];
-              if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
-              if (!done && ce > 0u) {
-                const DF after = df_add(mb, static_cast<float>(ce) * ms[j]);
-                jl = j;
-                cl = ce;
-                mb_last = mb;
-                if (!df_lt(after, target)) {
-                  const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
-                  uint32_t keep = static_cast<uint32_t>(ceilf(need / ms[j]));
-                  keep = max(1u, min(keep, ce));
-                  CutOut co;
-                  co.kstar = key;
-                  co.keep = keep;
-                  co.total = cnt[j];
-                  co.found = 1;
-                  co.zkept = df_add(mb, static_cast<float>(keep) * ms[j]);
-                  sh.cut[r_s] = co;
-                  done = true;
-                }
-                mb = after;
-              }
-            }
-            if (!done && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
-              CutOut co;
-              co.kstar = top - static_cast<uint32_t>(jl);
-              co.keep = cl;
-              co.total = cnt[jl];
-              co.found = 1;
-              co.zkept = df_add(mb_last, static_cast<float>(cl) * ms[jl]);
-              sh.cut[r_s] = co;
-            }
-          }
-        }
-      }
+    for (int r = 0; r < NR; ++r) {
+      const CutOut bo = topk_on ? sh.cutk[r] : sh.cut[r];
+      fast[r] = bo.found != 0;
+      tau[r] = bo.kstar;
     }
     __syncthreads();
+    for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
+    // the gathered vectors: the tags at or above the bound (index order kept)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (fast[r]) ngat[r] = tags_purge(wt[r], len[r], tau[r]);
+    }
+    __syncthreads();
+    // exact histogram of the gathered elements at or above the bound
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (!fast[r]) continue;
+      const uint32_t thr = H::thr_pack(E::bits_of_key(tau[r]));
+      for (uint32_t i = lane; i < ngat[r]; i += 32) {
+        const int v = sg.beg + static_cast<int>(tag_local(wt[r][i]));
+        const uint4 x = load_vec<DT>(rows[r], v, V, aligned[r]);
+        uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
+        while (msk) {
+          const int j = __ffs(msk) - 1;
+          msk &= msk - 1u;
+          red_add_shared(smem_addr(hist + r * kWindow + (E::key(E::bits_of(x, j)) & kSlotMask)), 1u);
+        }
+      }
+    }
+    if (tid < NR) {
+      sh.g[tid].klo = tau[tid];
+      sh.g[tid].active = fast[tid] ? 1 : 0;
+    }
+    __syncthreads();
+    cut_scan<DT, NR>(sh, hist, c, a.top_k, a.top_p);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) fast[r] = fast[r] && sh.cut[r].found != 0;
   }
 
-  // ------------------------------------ phase 5: kept set of each row
+  // ------------------------------------ phase 4: kept set of each row
 #pragma unroll 1
   for (int r = 0; r < NR; ++r) {
+    const RowG g = sh.g[r];
+    const bool fr = r == 0 ? fast[0] : fast[NR - 1];
     RowStat rs;
     rs.c = c;
-    rs.K = r == 0 ? K[0] : K[NR - 1];
-    rs.m = r == 0 ? m[0] : m[NR - 1];
-    rs.kmax = key_of_float<DT>(rs.m);
+    rs.K = g.K;
+    rs.m = g.m;
+    rs.kmax = g.kmax;
     rs.bad = 0;
     rs.all_kept = filt ? 0 : 1;
-    rs.covered = (r == 0 ? cov[0] : cov[NR - 1]) ? 1 : 0;
+    rs.covered = fr ? 1 : 0;
     rs.kstar = 0u;
     rs.tie_cut = V;
-    float zk = df_float(sh.z[r]);
+    float zk = df_float(g.z);
     if (filt) {
-      CutOut co = sh.cut[r];
-      const bool from_lists = co.found != 0;
-      if (!from_lists) {
-        rs.covered = 0;
-        co = search_cut<DT>(sh, rows[r], V, aligned[r], a.top_k, a.top_p, rs, df_double(sh.z[r]));
-      }
+      const CutOut co = fr ? sh.cut[r] : search_cut<DT>(sh, rows[r], V, aligned[r], a.top_k, a.top_p, rs, df_double(g.z));
       rs.kstar = co.kstar;
       zk = df_float(co.zkept);
       if (co.keep < co.total) {
-        const uint32_t* lw = lists + (r * kWarps + warp) * kListCap;
-        rs.tie_cut = from_lists
-            ? tie_cut_of<DT, true>(sh, lw, sh.w_n[warp][r], rows[r], V, aligned[r], co.kstar, co.keep)
-            : tie_cut_of<DT, false>(sh, lw, 0u, rows[r], V, aligned[r], co.kstar, co.keep);
+        rs.tie_cut = fr ? tie_cut_of<DT, true>(sh, gl[r], r == 0 ? ngat[0] : ngat[NR - 1], rows[r], V, aligned[r],
+                                               co.kstar, co.keep)
+                        : tie_cut_of<DT, false>(sh, gl[r], 0u, rows[r], V, aligned[r], co.kstar, co.keep);
       }
     }
     rs.zkept = zk;
@@ -1045,15 +1178,13 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     return;
   }
 
-  const int kq = a.k;
-  // ------------------------------------- phase 6: accept test at x_pos
+  // ------------------------------------- phase 5: accept test at x_pos
   if (NR == 2 && tid == 0) {
-    const int x = a.tokens[static_cast<size_t>(b) * kq + pos];
     UnitRec* rec = a.recs + unit;
     float px = 0.f, qx = 0.f;
-    if (x >= 0 && x < V) {
-      px = prob_of<DT>(rp, E::bits_at(rows[0], x), x);
-      qx = prob_of<DT>(rq, E::bits_at(rows[NR - 1], x), x);
+    if (xtok >= 0 && xtok < V) {
+      px = prob_of<DT>(rp, sh.xbits[0], xtok);
+      qx = prob_of<DT>(rq, sh.xbits[NR - 1], xtok);
       const float u = a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
       rec->accept = (u * qx < px) ? 1 : 0;
     } else {
@@ -1068,36 +1199,54 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
   }
 
-  // ------------- phase 7: residual (or bonus) by warps, in index order
-  // On the fast path each warp walks its list of p (the kept set of p is on
-  // it); otherwise its segment of the row.
+  // ------------- phase 6: residual (or bonus) by warps, in index order
+  // Fast path: the kept set of p lies in the warps' gathered vectors of p;
+  // the draft's vector at a gathered index is among the gathered vectors of
+  // q, or it holds no kept token of q.  Otherwise each warp re-reads its
+  // segment of the rows.
   const bool lists_p = rp.covered && !rp.all_kept;
-  const uint32_t* lp = lists + (0 * kWarps + warp) * kListCap;
-  const uint32_t np = lists_p ? sh.w_n[warp][0] : 0u;
-  const int seg_lo = sg.beg * E::kPerVec;
+  const bool lists_q = NR == 2 && rq.covered && !rq.all_kept;
+  const uint32_t np = lists_p ? ngat[0] : 0u;
+  const uint32_t nq = lists_q ? ngat[NR - 1] : 0u;
+  const int rounds = lists_p ? static_cast<int>((np + 31) / 32) : sg.iters;
+  // vector of round it (index order) for this lane, or -1
+  auto round_vec = [&](int it, bool want_q, uint4& xp, uint4& xq, bool& has_q) -> int {
+    has_q = false;
+    if (lists_p) {
+      const uint32_t i = it * 32 + lane;
+      if (i >= np) return -1;
+      const uint32_t vi = tag_local(wt[0][i]);
+      const int v = sg.beg + static_cast<int>(vi);
+      xp = load_vec<DT>(rows[0], v, V, aligned[0]);
+      if (want_q) {
+        if (lists_q) {
+          if (glist_find(wt[NR - 1], nq, vi) >= 0) {
+            xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]);
+            has_q = true;
+          }
+        } else {
+          xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]);
+          has_q = true;
+        }
+      }
+      return v;
+    }
+    const int v = sg.beg + it * 32 + lane;
+    if (v >= sg.end) return -1;
+    xp = load_vec<DT>(rows[0], v, V, aligned[0]);
+    if (want_q) { xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]); has_q = true; }
+    return v;
+  };
   {
     float s = 0.f, sp = 0.f;
-    if (lists_p) {
-      for (uint32_t i = lane; i < np; i += 32) {
-        const uint32_t e = lp[i];
-        const int j = seg_lo + static_cast<int>(entry_local(e));
-        float pv;
-        s += weight_of<DT>(rp, rq, entry_bits(e), rows[NR - 1], j, NR == 2, &pv);
-        sp += pv;
-      }
-    } else {
-      for (int v = sg.beg + lane; v < sg.end; v += 32) {
-        const uint4 xp = load_vec<DT>(rows[0], v, V, aligned[0]);
-        const uint4 xq = NR == 2 ? load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]) : xp;
-#pragma unroll
-        for (int j = 0; j < E::kPerVec; ++j) {
-          const int t = v * E::kPerVec + j;
-          if (t < V) {
-            const float pv = prob_of<DT>(rp, E::bits_of(xp, j), t);
-            sp += pv;
-            s += NR == 2 ? fmaxf(pv - (pv > 0.f ? prob_of<DT>(rq, E::bits_of(xq, j), t) : 0.f), 0.f) : pv;
-          }
-        }
+    for (int it = 0; it < rounds; ++it) {
+      uint4 xp, xq;
+      bool has_q;
+      const int v = round_vec(it, NR == 2, xp, xq, has_q);
+      if (v >= 0) {
+        float w[8], ps;
+        s += vec_weights<DT>(rp, rq, xp, has_q ? &xq : nullptr, v, V, NR == 2, w, &ps);
+        sp += ps;
       }
     }
     s = warp_sum_f32(s);
@@ -1145,42 +1294,20 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     const float tw = sh.draw_base;
     float run = 0.f;
     int token = -1, last_pos = -1;
-    const int rounds = lists_p ? static_cast<int>((np + 31) / 32) : sg.iters;
     for (int it = 0; it < rounds && token < 0; ++it) {
-      float w[8];
-      int idx[8];
+      uint4 xp, xq;
+      bool has_q;
+      const int v = round_vec(it, use_q, xp, xq, has_q);
+      float w[8], ps;
       float ls = 0.f;
       int lpos = -1;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { w[j] = 0.f; idx[j] = -1; }
-      if (lists_p) {
-        const uint32_t i = it * 32 + lane;
-        if (i < np) {
-          const uint32_t e = lp[i];
-          float pv;
-          idx[0] = seg_lo + static_cast<int>(entry_local(e));
-          w[0] = weight_of<DT>(rp, rq, entry_bits(e), rows[NR - 1], idx[0], use_q, &pv);
-        }
-      } else {
-        const int v = sg.beg + it * 32 + lane;
-        if (v < sg.end) {
-          const uint4 xp = load_vec<DT>(rows[0], v, V, aligned[0]);
-          const uint4 xq = use_q ? load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]) : xp;
+      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+      if (v >= 0) {
+        ls = vec_weights<DT>(rp, rq, xp, has_q ? &xq : nullptr, v, V, use_q, w, &ps);
 #pragma unroll
-          for (int j = 0; j < E::kPerVec; ++j) {
-            const int t = v * E::kPerVec + j;
-            if (t < V) {
-              const float pv = prob_of<DT>(rp, E::bits_of(xp, j), t);
-              w[j] = use_q ? fmaxf(pv - (pv > 0.f ? prob_of<DT>(rq, E::bits_of(xq, j), t) : 0.f), 0.f) : pv;
-              idx[j] = t;
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        ls += w[j];
-        if (w[j] > 0.f) lpos = idx[j];
+        for (int j = 0; j < 8; ++j)
+          if (w[j] > 0.f) lpos = v * E::kPerVec + j;
       }
       const float incl = warp_incl_scan(ls);
       const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
@@ -1195,9 +1322,9 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
           int lastj = -1;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (w[j] > 0.f) lastj = idx[j];
+            if (w[j] > 0.f) lastj = v * E::kPerVec + j;
             cum += w[j];
-            if (tok < 0 && w[j] > 0.f && cum > tw) tok = idx[j];
+            if (tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
           }
           if (tok < 0) tok = lastj;
         }
@@ -1225,8 +1352,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   const int V = a.V;
   __shared__ Shm sh;
   extern __shared__ __align__(16) uint32_t dsm[];
-  uint32_t* lists = dsm;                                // [2][kWarps][kListCap]
-  uint32_t* hist = dsm + 2 * kWarps * kListCap;         // [2][kWindow]
+  // dynamic shared memory: tags [2][kWarps][kTagCap], histograms [2][kWindow]
+  uint32_t* tags = dsm;
+  uint32_t* hist = tags + 2 * kWarps * kTagCap;
   if (a.mode == MODE_SAMPLE) {
     const int b = unit / (a.k + 1);
     const int pos = unit % (a.k + 1);
@@ -1235,14 +1363,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     if (pos < a.k) {
       const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
                                   (static_cast<size_t>(b) * a.k + pos) * static_cast<size_t>(V) * E::kBytes;
-      unit_body<DT, 2>(a, sh, lists, hist, unit, b, pos, rowp, rowq);
+      unit_body<DT, 2>(a, sh, tags, hist, unit, b, pos, rowp, rowq);
     } else {
-      unit_body<DT, 1>(a, sh, lists, hist, unit, b, pos, rowp, rowp);
+      unit_body<DT, 1>(a, sh, tags, hist, unit, b, pos, rowp, rowp);
     }
   } else {
     const unsigned char* rowp =
         static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-    unit_body<DT, 1>(a, sh, lists, hist, unit, unit, 0, rowp, rowp);
+    unit_body<DT, 1>(a, sh, tags, hist, unit, unit, 0, rowp, rowp);
   }
 }
 
@@ -1270,7 +1398,7 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
 
 size_t sample_smem_bytes(int dtype, bool filter) {
   (void)dtype;
-  return filter ? (2 * kWarps * kListCap + 2 * kWindow) * sizeof(uint32_t) : 16;
+  return filter ? (2 * kWarps * kTagCap + 2 * kWindow) * sizeof(uint32_t) : 16;
 }
 
 template <int DT>
