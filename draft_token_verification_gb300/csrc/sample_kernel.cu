@@ -47,7 +47,9 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 using u64 = unsigned long long;
 
-constexpr int kTagCap = 512;                        // candidate vector tags per warp per row
+constexpr int kLaneTags = 16;                       // candidate vector tags per lane per row
+constexpr int kBmapWords = 128;                     // gather bitmap words per warp per row (4096 vectors)
+constexpr int kGather = kLaneTags * 32;             // gathered vectors per warp per row (in the lane tags' place)
 constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
 constexpr float kTheta = 13.f;                      // octaves of mass kept as candidates
 constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
@@ -506,45 +508,21 @@ __device__ __forceinline__ uint32_t tag_make(uint32_t local, uint32_t key) { ret
 __device__ __forceinline__ uint32_t tag_local(uint32_t t) { return t >> 16; }
 __device__ __forceinline__ uint32_t tag_key(uint32_t t) { return t & 0xFFFFu; }
 
-// Keeps, in order, the tags whose key is at least kthr; new length.  Warp.
-__device__ __forceinline__ uint32_t tags_purge(uint32_t* tags, uint32_t len, uint32_t kthr) {
-  const int lane = threadIdx.x & 31;
+// Lane tag lists: every lane keeps the tags of the candidate vectors it
+// streamed (stream order), kLaneTags per row; tag q of a lane sits at
+// [row][warp][q][lane] (conflict-free).
+__device__ __forceinline__ uint32_t lane_tags_purge(uint32_t* L, uint32_t n, uint32_t kthr) {
   uint32_t out = 0;
-  for (uint32_t base = 0; base < len; base += 32) {
-    const uint32_t i = base + lane;
-    const uint32_t t = i < len ? tags[i] : 0u;
-    const bool keep = i < len && tag_key(t) >= kthr;
-    const unsigned ball = __ballot_sync(kFull, keep);
-    __syncwarp();
-    if (keep) tags[out + __popc(ball & ((1u << lane) - 1u))] = t;
-    out += __popc(ball);
-    __syncwarp();
+  for (uint32_t q = 0; q < n; ++q) {
+    const uint32_t t = L[32 * q];
+    if (tag_key(t) >= kthr) L[32 * (out++)] = t;
   }
   return out;
 }
-
-// Smallest key kf >= klow such that at most half the capacity of tags
-// (listed ones, plus this lane's pending key if any) have key >= kf.  Warp.
-__device__ __noinline__ uint32_t tags_half_key(const uint32_t* tags, uint32_t len, uint32_t klow, uint32_t pend) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kPer = kTagCap / 32;
-  uint32_t keys[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const uint32_t i = q * 32 + lane;
-    keys[q] = i < len ? tag_key(tags[i]) : 0u;
-  }
-  uint32_t lo = klow, hi = 0x10000u;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    uint32_t c = pend >= mid ? 1u : 0u;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) c += keys[q] >= mid ? 1u : 0u;
-    c = warp_sum_u32(c);
-    if (c <= static_cast<uint32_t>(kTagCap) / 2u) hi = mid;
-    else lo = mid + 1u;
-  }
-  return lo;
+__device__ __forceinline__ uint32_t lane_tags_min_key(const uint32_t* L, uint32_t n) {
+  uint32_t k = 0xFFFFFFFFu;
+  for (uint32_t q = 0; q < n; ++q) k = min(k, tag_key(L[32 * q]));
+  return k;
 }
 
 // The gathered vectors of one warp and row: its tags at or above the bound
@@ -840,8 +818,9 @@ __device__ __forceinline__ float vec_weights(const RowStat& rp, const RowStat& r
 
 // One unit (b, pos) with NR rows (2: target and draft, 1: target only).
 template <int DT, int NR>
-__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* tags, uint32_t* hist, int unit, int b,
-                                          int pos, const unsigned char* rowp, const unsigned char* rowq) {
+__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* ltags, uint32_t* hist, uint32_t* bmap,
+                                          int unit, int b, int pos, const unsigned char* rowp,
+                                          const unsigned char* rowq) {
   using E = Elt<DT>;
   using H = Hot<DT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -860,13 +839,17 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
   const int kq = a.k;
   const int xtok = (NR == 2 && a.mode == MODE_SAMPLE) ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
   // candidate tags: bf16 rows with a cut, segments short enough to index
-  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= 65536;
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
   const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
-  uint32_t* wt[2] = {tags + (0 * kWarps + warp) * kTagCap, tags + (1 * kWarps + warp) * kTagCap};
+  uint32_t* myl[2] = {ltags + (0 * kWarps + warp) * kLaneTags * 32 + lane,
+                      ltags + (1 * kWarps + warp) * kLaneTags * 32 + lane};
+  // a warp's gathered list replaces its lanes' tags once they are read
+  uint32_t* wg[2] = {ltags + (0 * kWarps + warp) * kGather, ltags + (1 * kWarps + warp) * kGather};
+  uint32_t* wb[2] = {bmap + (0 * kWarps + warp) * kBmapWords, bmap + (1 * kWarps + warp) * kBmapWords};
   GList gl[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    gl[r].tags = wt[r];
+    gl[r].tags = wg[r];
     gl[r].row = rows[r];
   }
 
@@ -880,22 +863,22 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
   int kt[NR];               // thread lattice exponent
   u64 acc0[NR], acc1[NR];   // thread sums of 2^(l c - kt)
   float mw[NR];             // running maximum known to the warp (uniform)
-  uint32_t len[NR];         // tag list lengths (uniform)
-  uint32_t kthr[NR];        // current tag bound, as a key (uniform)
-  uint32_t kfloor[NR];      // raised bound: the tag list is complete above it
-  float thr_v[NR];          // value of kthr
+  uint32_t cnt[NR];         // lane tag list lengths
+  uint32_t lfl[NR];         // lane floor: the lane list is complete above it
+  float lflv[NR];           // value of the lane floor
+  float thr_c[NR];          // kTheta octaves below the CTA maximum of the last exchange
   int sync_no = 0;
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    thr_v[r] = -INFINITY;
     mt[r] = -INFINITY;
     kt[r] = -(1 << 30);
     acc0[r] = 0ull;
     acc1[r] = 0ull;
     mw[r] = -INFINITY;
-    len[r] = 0u;
-    kthr[r] = 0u;
-    kfloor[r] = 0u;
+    cnt[r] = 0u;
+    lfl[r] = 0u;
+    lflv[r] = -INFINITY;
+    thr_c[r] = -INFINITY;
   }
   const int xv = xtok >= 0 && xtok < V ? xtok / E::kPerVec : -1;
   // every warp runs the same number of iterations (the CTA barriers below)
@@ -929,39 +912,29 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
         if (v0 + 32 * u == xv && xv < sg.end) sh.xbits[r] = E::bits_of(x[r][u], xtok - xv * E::kPerVec);
       }
       if (use_lists) {
-        // tag bound: kTheta octaves below the running maximum (at most the
-        // row maximum), never below the raised floor
-        const float m_new = warp_max_nan(max_nan(vm[0], vm[1]));
-        if (m_new > mw[r]) {
-          mw[r] = m_new;
-          const float tv = mw[r] - dtheta;
-          kthr[r] = max(kfloor[r], tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u);
-          thr_v[r] = value_of_key<DT>(kthr[r]);
-        }
+        // lane bound: kTheta octaves below the larger of this lane's running
+        // maximum and the CTA maximum of the last exchange (both at most the
+        // row maximum), never below the lane floor
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int v = v0 + 32 * u;
-          bool flag = v < sg.end && vm[u] >= thr_v[r];
-          unsigned ball = __ballot_sync(kFull, flag);
-          if (ball == 0u) continue;
-          uint32_t n = __popc(ball);
-          if (len[r] + n > static_cast<uint32_t>(kTagCap)) {  // full: purge to the bound, then halve
-            const uint32_t kv = flag ? key_of_float<DT>(vm[u]) : 0u;
-            len[r] = tags_purge(wt[r], len[r], kthr[r]);
-            if (len[r] + n > static_cast<uint32_t>(kTagCap) / 2u) {
-              kfloor[r] = tags_half_key(wt[r], len[r], kthr[r], kv);
-              kthr[r] = max(kthr[r], kfloor[r]);
-              thr_v[r] = value_of_key<DT>(kthr[r]);
-              len[r] = tags_purge(wt[r], len[r], kthr[r]);
-              flag = flag && kv >= kthr[r];
-              ball = __ballot_sync(kFull, flag);
-              n = __popc(ball);
+          const float lthr = fmaxf(fmaxf(thr_c[r], mt[r] - dtheta), lflv[r]);
+          if (v < sg.end && vm[u] >= lthr) {
+            bool take = true;
+            if (cnt[r] == static_cast<uint32_t>(kLaneTags)) {  // full: keep the largest of this lane
+              cnt[r] = lane_tags_purge(myl[r], cnt[r], E::key(bits_round_down<DT>(lthr)));
+              while (cnt[r] == static_cast<uint32_t>(kLaneTags)) {
+                lfl[r] = lane_tags_min_key(myl[r], cnt[r]) + 1u;
+                lflv[r] = value_of_key<DT>(lfl[r]);
+                cnt[r] = lane_tags_purge(myl[r], cnt[r], lfl[r]);
+              }
+              take = vm[u] >= lflv[r];
+            }
+            if (take) {
+              myl[r][32 * cnt[r]] = tag_make(static_cast<uint32_t>(v - sg.beg), key_of_float<DT>(vm[u]));
+              ++cnt[r];
             }
           }
-          if (flag)
-            wt[r][len[r] + __popc(ball & ((1u << lane) - 1u))] =
-                tag_make(static_cast<uint32_t>(v - sg.beg), key_of_float<DT>(vm[u]));
-          len[r] += n;
         }
       }
     }
@@ -970,9 +943,10 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
       // share the running maxima across the CTA (fixed points, denser at the
       // start where they rise fastest: deterministic)
       const int slot = (sync_no++) & 1;
-      if (lane == 0) {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) sh.x_m[slot][warp][r] = mw[r];
+      for (int r = 0; r < NR; ++r) {
+        const float wm = warp_max_nan(mt[r]);
+        if (lane == 0) sh.x_m[slot][warp][r] = fmaxf(mw[r], wm);
       }
       __syncthreads();
 #pragma unroll
@@ -982,9 +956,7 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
         for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][r]);
         if (mm > mw[r]) {
           mw[r] = mm;
-          const float tv = mw[r] - dtheta;
-          kthr[r] = max(kfloor[r], tv > -3.0e38f ? E::key(bits_round_down<DT>(tv)) : 0u);
-          thr_v[r] = value_of_key<DT>(kthr[r]);
+          thr_c[r] = mw[r] - dtheta;
         }
       }
     }
@@ -1002,11 +974,12 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     zt *= exp2i(kt[r] - kw);
     zt = warp_sum_f32(zt);
     const float mx = warp_max_nan(mt[r]);
+    const uint32_t fl = warp_max_u32(lfl[r]);
     if (lane == 0) {
       sh.w_m[warp][r] = mx;
       sh.w_k[warp][r] = kw;
       sh.w_z[warp][r] = zt;
-      sh.w_floor[warp][r] = kfloor[r];
+      sh.w_floor[warp][r] = fl;
       sh.w_over[warp][r] = 0u;
     }
   }
@@ -1076,7 +1049,7 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
   }
 
   // ---------- phase 3: a bound on the cut from the tagged vector maxima
-  // The tags hold every vector whose maximum reaches klo.  Vector maxima are
+  // The lane tags hold every vector whose maximum reaches klo.  Vector maxima are
   // tokens of the row, so the mass (or count) of the row above a value is at
   // least that of the maxima above it: where the maxima reach the top-p
   // target (or top_k), the row's cut lies at or above.
@@ -1090,8 +1063,8 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       const uint32_t kl = sh.g[r].klo;
-      for (uint32_t i = lane; i < len[r]; i += 32) {
-        const uint32_t k = tag_key(wt[r][i]);
+      for (uint32_t q = 0; q < cnt[r]; ++q) {
+        const uint32_t k = tag_key(myl[r][32 * q]);
         if (k >= kl) red_add_shared(smem_addr(hist + r * kWindow + (k & kSlotMask)), 1u);
       }
     }
@@ -1107,19 +1080,53 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     }
     __syncthreads();
     for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
-    // the gathered vectors: the tags at or above the bound (index order kept)
+    // the gathered vectors: the lanes' tags at or above the bound, marked in
+    // the warp's bitmap and read back in index order
+    const int nwords = seg_vectors(nvec) / 32;
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      if (fast[r]) ngat[r] = tags_purge(wt[r], len[r], tau[r]);
+      if (!fast[r]) continue;
+      for (int w2 = lane; w2 < nwords; w2 += 32) wb[r][w2] = 0u;
+      __syncwarp();
+      for (uint32_t q = 0; q < cnt[r]; ++q) {
+        const uint32_t t = myl[r][32 * q];
+        if (tag_key(t) >= tau[r]) atomicOr(&wb[r][tag_local(t) >> 5], 1u << (tag_local(t) & 31u));
+      }
+      __syncwarp();
+      uint32_t base = 0u;
+      for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w2 = w0 + lane;
+        const uint32_t bits = w2 < nwords ? wb[r][w2] : 0u;
+        const uint32_t cb = __popc(bits);
+        const uint32_t incl = warp_incl_scan_u32(cb);
+        uint32_t o = base + incl - cb;
+        uint32_t bb = bits;
+        while (bb) {
+          const uint32_t j = __ffs(bb) - 1u;
+          bb &= bb - 1u;
+          if (o < static_cast<uint32_t>(kGather)) wg[r][o] = tag_make(static_cast<uint32_t>(w2) * 32u + j, 0u);
+          ++o;
+        }
+        base += __shfl_sync(kFull, incl, 31);
+      }
+      ngat[r] = min(base, static_cast<uint32_t>(kGather));
+      if (lane == 0) sh.w_over[warp][r] = base > static_cast<uint32_t>(kGather) ? 1u : 0u;
     }
     __syncthreads();
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      bool ok = fast[r];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) ok = ok && sh.w_over[w][r] == 0u;
+      fast[r] = ok;
+    }
     // exact histogram of the gathered elements at or above the bound
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       if (!fast[r]) continue;
       const uint32_t thr = H::thr_pack(E::bits_of_key(tau[r]));
       for (uint32_t i = lane; i < ngat[r]; i += 32) {
-        const int v = sg.beg + static_cast<int>(tag_local(wt[r][i]));
+        const int v = sg.beg + static_cast<int>(tag_local(wg[r][i]));
         const uint4 x = load_vec<DT>(rows[r], v, V, aligned[r]);
         uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
         while (msk) {
@@ -1215,12 +1222,12 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     if (lists_p) {
       const uint32_t i = it * 32 + lane;
       if (i >= np) return -1;
-      const uint32_t vi = tag_local(wt[0][i]);
+      const uint32_t vi = tag_local(wg[0][i]);
       const int v = sg.beg + static_cast<int>(vi);
       xp = load_vec<DT>(rows[0], v, V, aligned[0]);
       if (want_q) {
         if (lists_q) {
-          if (glist_find(wt[NR - 1], nq, vi) >= 0) {
+          if (glist_find(wg[NR - 1], nq, vi) >= 0) {
             xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]);
             has_q = true;
           }
@@ -1352,9 +1359,12 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   const int V = a.V;
   __shared__ Shm sh;
   extern __shared__ __align__(16) uint32_t dsm[];
-  // dynamic shared memory: tags [2][kWarps][kTagCap], histograms [2][kWindow]
-  uint32_t* tags = dsm;
-  uint32_t* hist = tags + 2 * kWarps * kTagCap;
+  // dynamic shared memory: lane tags [2][kWarps][kLaneTags][32] (later the
+  // gathered tags [2][kWarps][kGather]), histograms [2][kWindow], gather
+  // bitmaps [2][kWarps][kBmapWords]
+  uint32_t* ltags = dsm;
+  uint32_t* hist = ltags + 2 * kWarps * kLaneTags * 32;
+  uint32_t* bmap = hist + 2 * kWindow;
   if (a.mode == MODE_SAMPLE) {
     const int b = unit / (a.k + 1);
     const int pos = unit % (a.k + 1);
@@ -1363,14 +1373,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     if (pos < a.k) {
       const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
                                   (static_cast<size_t>(b) * a.k + pos) * static_cast<size_t>(V) * E::kBytes;
-      unit_body<DT, 2>(a, sh, tags, hist, unit, b, pos, rowp, rowq);
+      unit_body<DT, 2>(a, sh, ltags, hist, bmap, unit, b, pos, rowp, rowq);
     } else {
-      unit_body<DT, 1>(a, sh, tags, hist, unit, b, pos, rowp, rowp);
+      unit_body<DT, 1>(a, sh, ltags, hist, bmap, unit, b, pos, rowp, rowp);
     }
   } else {
     const unsigned char* rowp =
         static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-    unit_body<DT, 1>(a, sh, tags, hist, unit, unit, 0, rowp, rowp);
+    unit_body<DT, 1>(a, sh, ltags, hist, bmap, unit, unit, 0, rowp, rowp);
   }
 }
 
@@ -1398,7 +1408,7 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
 
 size_t sample_smem_bytes(int dtype, bool filter) {
   (void)dtype;
-  return filter ? (2 * kWarps * kTagCap + 2 * kWindow) * sizeof(uint32_t) : 16;
+  return filter ? (2 * kWarps * kLaneTags * 32 + 2 * kWindow + 2 * kWarps * kBmapWords) * sizeof(uint32_t) : 16;
 }
 
 template <int DT>
