@@ -73,11 +73,15 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.status = reinterpret_cast<uint32_t*>(w + L.status);
   a.tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
   a.recs = reinterpret_cast<UnitRec*>(w + L.s_recs);
+  a.pair_tickets = reinterpret_cast<uint32_t*>(w + L.p_tickets);
+  a.pairs = reinterpret_cast<PairRec*>(w + L.p_recs);
   a.aligned_target = rows_aligned(target, V, dtype);
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
-  const int units = mode == MODE_SAMPLE ? B * (k + 1) : B;
-  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, units, stream);
+  // one CTA per row: target and draft rows of every draft position, then the
+  // bonus target rows (MODE_PROBS: one per row)
+  const int ctas = mode == MODE_SAMPLE ? B * (2 * k + 1) : B;
+  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, ctas, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }
@@ -109,9 +113,10 @@ int argmax_split_len(int rows, int V) {
 // largest shape it accepts (status word, per-sequence tickets, unit records,
 // plus the argmax slots the layout reserves).  Every GPU that loads the
 // library holds one copy until the process exits.
-constexpr size_t kNoAllocBytes = 256 + sizeof(uint32_t) * SPEC_NOALLOC_MAX_B +
-                                 (sizeof(UnitRec) + sizeof(uint64_t)) * SPEC_NOALLOC_MAX_UNITS +
-                                 sizeof(uint32_t) * SPEC_NOALLOC_MAX_B;
+constexpr size_t kNoAllocBytes =
+    256 + align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_B, 256) + align_up(sizeof(UnitRec) * SPEC_NOALLOC_MAX_UNITS, 256) +
+    align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_UNITS, 256) + align_up(sizeof(PairRec) * SPEC_NOALLOC_MAX_UNITS, 256) +
+    align_up(sizeof(uint64_t) * SPEC_NOALLOC_MAX_UNITS, 256) + align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_B, 256);
 constexpr int kNoAllocMaxDevices = 64;
 
 std::mutex g_noalloc_mu;
@@ -175,10 +180,9 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
   if (rc != SPEC_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   // The array keeps whatever the previous call left: the status word, the
-  // per-sequence tickets and the unit records must start at zero.
-  if (cudaMemsetAsync(scratch, 0, L.s_recs + sizeof(UnitRec) * static_cast<size_t>(B) * (k + 1), st) !=
-      cudaSuccess)
-    return SPEC_ERR_LAUNCH;
+  // per-sequence tickets, the unit records and the per-position tickets must
+  // start at zero (the position records are written before they are read).
+  if (cudaMemsetAsync(scratch, 0, L.p_recs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
   rc = run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                   out_num_accepted, out_p_draft, out_q_draft, nullptr, scratch, kNoAllocBytes, cuda_stream,
                   MODE_SAMPLE);
@@ -286,7 +290,7 @@ const char* spec_error_string(int code) {
     case SPEC_ERR_TIMEOUT: return "a bounded device wait gave up";
     case SPEC_ERR_UNSUPPORTED: return "shape beyond the library's limits";
     case SPEC_ERR_SCRATCH_LIMIT:
-      return "B > 2048 or B*(k+1) > 8192: beyond the fixed scratch of spec_verify_sample_noalloc";
+      return "B > 1024 or B*(k+1) > 1024: beyond the fixed scratch of spec_verify_sample_noalloc";
     default: return "unknown error code";
   }
 }

@@ -47,7 +47,7 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 using u64 = unsigned long long;
 
-constexpr int kLaneTags = 16;                       // candidate vector tags per lane per row
+constexpr int kLaneTags = 32;                       // candidate vector tags per lane per row
 constexpr int kBmapWords = 128;                     // gather bitmap words per warp per row (4096 vectors)
 constexpr int kGather = kLaneTags * 32;             // gathered vectors per warp per row (in the lane tags' place)
 constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
@@ -259,19 +259,17 @@ __device__ __forceinline__ uint32_t bits_round_down(float v) {
 }
 
 // The kept set of a row: key > kstar, or key == kstar and index < tie_cut.
-struct RowStat {
-  float c;               // log2(e) / T
-  float K;               // lattice exponent (integer) of the row: masses 2^(l c - K)
-  float m;               // row maximum
-  uint32_t kmax;         // key of m
-  uint32_t kstar;
-  int tie_cut;           // row index bound for tokens of value kstar
-  float inv_z;           // 1 / mass of the kept set
-  float zkept;
-  int all_kept;
-  int covered;           // the candidate lists hold every kept token
-  int bad;
+using RowStat = RowState;
+
+// The leading part of a PairRec: both rows' states and probabilities at the
+// draft token, and the length of the target row's vector list.
+struct PairHdr {
+  RowState rs[2];
+  float xprob[2];
+  uint32_t nlist;
+  uint32_t pad;
 };
+static_assert(offsetof(PairRec, list) == sizeof(PairHdr), "PairRec must start with a PairHdr");
 
 __device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, int j) {
   if (rs.all_kept) return true;
@@ -325,6 +323,8 @@ struct Shm {
   RowStat rs[2];
   int draw_warp;
   float draw_base;
+  int second;                  // this CTA finished second of its draft position
+  PairHdr pair_hdr;            // the pair's states, as read by the second finisher
 };
 
 // 16-byte vector v of a row (elements v*kPerVec ...), -inf beyond n.
@@ -502,11 +502,11 @@ __device__ __forceinline__ Seg warp_seg(int nvec, int warp) {
 }
 
 // Tag of a candidate vector: its index within the warp segment (high 16
-// bits) and the key of its maximum (low 16 bits, bf16 keys).  A warp's tags
-// are kept in index order.
+// bits) and the bf16 pattern of its maximum (low 16 bits).
 __device__ __forceinline__ uint32_t tag_make(uint32_t local, uint32_t key) { return (local << 16) | key; }
 __device__ __forceinline__ uint32_t tag_local(uint32_t t) { return t >> 16; }
-__device__ __forceinline__ uint32_t tag_key(uint32_t t) { return t & 0xFFFFu; }
+// (the tag keeps the maximum's bf16 pattern; its key orders the values)
+__device__ __forceinline__ uint32_t tag_key(uint32_t t) { return Elt<DT_BF16>::key(t & 0xFFFFu); }
 
 // Lane tag lists: every lane keeps the tags of the candidate vectors it
 // streamed (stream order), kLaneTags per row; tag q of a lane sits at
@@ -816,443 +816,62 @@ __device__ __forceinline__ float vec_weights(const RowStat& rp, const RowStat& r
 
 }  // namespace
 
-// One unit (b, pos) with NR rows (2: target and draft, 1: target only).
-template <int DT, int NR>
-__device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t* ltags, uint32_t* hist, uint32_t* bmap,
-                                          int unit, int b, int pos, const unsigned char* rowp,
-                                          const unsigned char* rowq) {
+constexpr int ROLE_P = 0;      // target row of a draft position
+constexpr int ROLE_Q = 1;      // draft row of a draft position
+constexpr int ROLE_BONUS = 2;  // target row after the last draft
+constexpr int ROLE_PROBS = 3;  // one row of spec_transform_probs
+
+// Draw weights over one CTA-wide index-ordered set of vectors, per warp
+// chunks: warp w takes entries [w n / kWarps, (w + 1) n / kWarps) of the
+// set.  `vec_at(e)` gives the row vector index of entry e.
+struct Chunk {
+  int beg, end;
+};
+__device__ __forceinline__ Chunk warp_chunk(int n, int warp) {
+  Chunk ch;
+  ch.beg = static_cast<int>((static_cast<long long>(n) * warp) / kWarps);
+  ch.end = static_cast<int>((static_cast<long long>(n) * (warp + 1)) / kWarps);
+  return ch;
+}
+
+// The residual (use_q) or target (p) draw over the vectors listed in L (row
+// vector indices, index order), or over the whole rows when L is null:
+// per-warp sums, then the warp holding u * S walks its part.  Writes the drawn
+// token (or -1) to *drawn_out from one thread.  Whole CTA.
+// G (when L is null and G is not): the CTA's own per-warp gathered tags, warp
+// w's at G + w * kGather, n in all, sh.w_u[w][0] of them in warp w.
+template <int DT>
+__device__ __noinline__ void draw_rows(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
+                                       const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
+                                       const uint32_t* L, const uint32_t* G, int n, float u_draw, int* drawn_out) {
   using E = Elt<DT>;
-  using H = Hot<DT>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int V = a.V;
-  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
-  const bool bad_t = !(T > 0.f) || isinf(T);
-  const float c = kLog2e / T;
-  const u64 c2 = pkf(c, c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
   const Seg sg = warp_seg(nvec, warp);
-  const unsigned char* rows[2] = {rowp, rowq};
-  const bool aligned[2] = {a.aligned_target != 0, a.aligned_draft != 0};
-  const bool topk_on = a.top_k > 0;
-  const bool topp_on = a.top_p < 1.f;
-  const bool filt = topk_on || topp_on;
-  const int kq = a.k;
-  const int xtok = (NR == 2 && a.mode == MODE_SAMPLE) ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
-  // candidate tags: bf16 rows with a cut, segments short enough to index
-  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
-  const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
-  uint32_t* myl[2] = {ltags + (0 * kWarps + warp) * kLaneTags * 32 + lane,
-                      ltags + (1 * kWarps + warp) * kLaneTags * 32 + lane};
-  // a warp's gathered list replaces its lanes' tags once they are read
-  uint32_t* wg[2] = {ltags + (0 * kWarps + warp) * kGather, ltags + (1 * kWarps + warp) * kGather};
-  uint32_t* wb[2] = {bmap + (0 * kWarps + warp) * kBmapWords, bmap + (1 * kWarps + warp) * kBmapWords};
-  GList gl[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    gl[r].tags = wg[r];
-    gl[r].row = rows[r];
-  }
-
-  if (filt)
-    for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
-  if (tid < 2) sh.xbits[tid] = 0u;
-  __syncthreads();
-
-  // --------------------------------------------------- phase 1: stream
-  float mt[NR];             // thread maximum
-  int kt[NR];               // thread lattice exponent
-  u64 acc0[NR], acc1[NR];   // thread sums of 2^(l c - kt)
-  float mw[NR];             // running maximum known to the warp (uniform)
-  uint32_t cnt[NR];         // lane tag list lengths
-  uint32_t lfl[NR];         // lane floor: the lane list is complete above it
-  float lflv[NR];           // value of the lane floor
-  float thr_c[NR];          // kTheta octaves below the CTA maximum of the last exchange
-  int sync_no = 0;
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    mt[r] = -INFINITY;
-    kt[r] = -(1 << 30);
-    acc0[r] = 0ull;
-    acc1[r] = 0ull;
-    mw[r] = -INFINITY;
-    cnt[r] = 0u;
-    lfl[r] = 0u;
-    lflv[r] = -INFINITY;
-    thr_c[r] = -INFINITY;
-  }
-  const int xv = xtok >= 0 && xtok < V ? xtok / E::kPerVec : -1;
-  // every warp runs the same number of iterations (the CTA barriers below)
-  const int iters_all = seg_vectors(nvec) / 32;
-  for (int it = 0; it < iters_all; it += 2) {
-    const int v0 = sg.beg + it * 32 + lane;
-    const int v1 = v0 + 32;
-    uint4 x[NR][2];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      x[r][0] = v0 < sg.end ? load_vec<DT>(rows[r], v0, V, aligned[r]) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
-      x[r][1] = v1 < sg.end ? load_vec<DT>(rows[r], v1, V, aligned[r]) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
-    }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      float vm[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        vm[u] = H::vmax(x[r][u]);
-        const float L = vm[u] * c;
-        if (L > static_cast<float>(kt[r]) && L < 1073741824.f) {  // raise the lattice exponent (rare)
-          const int knew = static_cast<int>(ceilf(L));
-          const float s = exp2i(kt[r] - knew);
-          acc0[r] = mul2(acc0[r], pkf(s, s));
-          acc1[r] = mul2(acc1[r], pkf(s, s));
-          kt[r] = knew;
-        }
-        const float nk = -static_cast<float>(kt[r]);
-        H::mass_vec(x[r][u], c2, pkf(nk, nk), acc0[r], acc1[r]);
-        mt[r] = max_nan(mt[r], vm[u]);
-        if (v0 + 32 * u == xv && xv < sg.end) sh.xbits[r] = E::bits_of(x[r][u], xtok - xv * E::kPerVec);
-      }
-      if (use_lists) {
-        // lane bound: kTheta octaves below the larger of this lane's running
-        // maximum and the CTA maximum of the last exchange (both at most the
-        // row maximum), never below the lane floor
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int v = v0 + 32 * u;
-          const float lthr = fmaxf(fmaxf(thr_c[r], mt[r] - dtheta), lflv[r]);
-          if (v < sg.end && vm[u] >= lthr) {
-            bool take = true;
-            if (cnt[r] == static_cast<uint32_t>(kLaneTags)) {  // full: keep the largest of this lane
-              cnt[r] = lane_tags_purge(myl[r], cnt[r], E::key(bits_round_down<DT>(lthr)));
-              while (cnt[r] == static_cast<uint32_t>(kLaneTags)) {
-                lfl[r] = lane_tags_min_key(myl[r], cnt[r]) + 1u;
-                lflv[r] = value_of_key<DT>(lfl[r]);
-                cnt[r] = lane_tags_purge(myl[r], cnt[r], lfl[r]);
-              }
-              take = vm[u] >= lflv[r];
-            }
-            if (take) {
-              myl[r][32 * cnt[r]] = tag_make(static_cast<uint32_t>(v - sg.beg), key_of_float<DT>(vm[u]));
-              ++cnt[r];
-            }
-          }
-        }
-      }
-    }
-    const int li = it >> 1;  // loop iteration
-    if (use_lists && (li < kSyncEvery ? (li & (li + 1)) == 0 : (li % kSyncEvery) == kSyncEvery - 1)) {
-      // share the running maxima across the CTA (fixed points, denser at the
-      // start where they rise fastest: deterministic)
-      const int slot = (sync_no++) & 1;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float wm = warp_max_nan(mt[r]);
-        if (lane == 0) sh.x_m[slot][warp][r] = fmaxf(mw[r], wm);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        float mm = mw[r];
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][r]);
-        if (mm > mw[r]) {
-          mw[r] = mm;
-          thr_c[r] = mw[r] - dtheta;
-        }
-      }
-    }
-  }
-  __syncwarp();
-
-  // ------------------------------------------ phase 2: row maximum and sum
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    float s0, s1, s2, s3;
-    upk(acc0[r], s0, s1);
-    upk(acc1[r], s2, s3);
-    float zt = (s0 + s1) + (s2 + s3);
-    const int kw = warp_max_i32(kt[r]);
-    zt *= exp2i(kt[r] - kw);
-    zt = warp_sum_f32(zt);
-    const float mx = warp_max_nan(mt[r]);
-    const uint32_t fl = warp_max_u32(lfl[r]);
-    if (lane == 0) {
-      sh.w_m[warp][r] = mx;
-      sh.w_k[warp][r] = kw;
-      sh.w_z[warp][r] = zt;
-      sh.w_floor[warp][r] = fl;
-      sh.w_over[warp][r] = 0u;
-    }
-  }
-  __syncthreads();
-  bool any_bad = bad_t;
-  if (tid < NR) {
-    const int r = tid;
-    float mx = -INFINITY;
-    int kk = -(1 << 30);
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      mx = max_nan(mx, sh.w_m[w][r]);
-      kk = max(kk, sh.w_k[w][r]);
-    }
-    DF z{0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) z = df_add(z, sh.w_z[w][r] * exp2i(sh.w_k[w][r] - kk));
-    RowG g;
-    g.m = mx;
-    g.K = static_cast<float>(kk);
-    g.kmax = key_of_float<DT>(mx);
-    g.z = z;
-    // every vector whose maximum reaches klo is tagged
-    const float tv = mx - dtheta;
-    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
-    const uint32_t gtop = g.kmax >> 2;
-    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][r]);
-    g.klo = kl;
-    g.active = use_lists ? 1 : 0;
-    sh.g[r] = g;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < NR; ++r) {
-    const float mx = sh.g[r].m;
-    // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
-    any_bad |= !isfinite(mx) || !(fabsf(mx * c) < 1073741824.f);
-  }
-
-  if (any_bad) {
-    if (a.mode == MODE_PROBS) {
-      float* out = a.out_probs + static_cast<size_t>(unit) * V;
-      for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
-      if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
-    } else if (tid == 0) {
-      UnitRec* rec = a.recs + unit;
-      uint32_t add = 1u;
-      uint32_t st = SPEC_STATUS_BAD_ROW;
-      rec->drawn = -1;
-      if (NR == 2) {
-        if (!(xtok >= 0 && xtok < V)) st |= SPEC_STATUS_BAD_TOKEN;
-        rec->accept = 0;
-        rec->px = 0.f;
-        rec->qx = 0.f;
-        if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = 0.f;
-        if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = 0.f;
-        add = 2u;
-      }
-      set_status(a.status, st);
-      __threadfence();
-      const uint32_t before = atomicAdd(a.tickets + b, add);
-      if (before + add == static_cast<uint32_t>(2 * kq + 1)) sample_finalize(a, b);
-    }
-    return;
-  }
-
-  // ---------- phase 3: a bound on the cut from the tagged vector maxima
-  // The lane tags hold every vector whose maximum reaches klo.  Vector maxima are
-  // tokens of the row, so the mass (or count) of the row above a value is at
-  // least that of the maxima above it: where the maxima reach the top-p
-  // target (or top_k), the row's cut lies at or above.
-  uint32_t ngat[NR];
-#pragma unroll
-  for (int r = 0; r < NR; ++r) ngat[r] = 0u;
-  bool fast[NR];
-#pragma unroll
-  for (int r = 0; r < NR; ++r) fast[r] = false;
-  if (use_lists) {
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      const uint32_t kl = sh.g[r].klo;
-      for (uint32_t q = 0; q < cnt[r]; ++q) {
-        const uint32_t k = tag_key(myl[r][32 * q]);
-        if (k >= kl) red_add_shared(smem_addr(hist + r * kWindow + (k & kSlotMask)), 1u);
-      }
-    }
-    __syncthreads();
-    cut_scan<DT, NR>(sh, hist, c, a.top_k, a.top_p);
-    // bound (top-k: its own cut; top-p alone: the maxima's crossing)
-    uint32_t tau[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      const CutOut bo = topk_on ? sh.cutk[r] : sh.cut[r];
-      fast[r] = bo.found != 0;
-      tau[r] = bo.kstar;
-    }
-    __syncthreads();
-    for (int t = tid; t < NR * kWindow; t += kThreads) hist[t] = 0u;
-    // the gathered vectors: the lanes' tags at or above the bound, marked in
-    // the warp's bitmap and read back in index order
-    const int nwords = seg_vectors(nvec) / 32;
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      if (!fast[r]) continue;
-      for (int w2 = lane; w2 < nwords; w2 += 32) wb[r][w2] = 0u;
-      __syncwarp();
-      for (uint32_t q = 0; q < cnt[r]; ++q) {
-        const uint32_t t = myl[r][32 * q];
-        if (tag_key(t) >= tau[r]) atomicOr(&wb[r][tag_local(t) >> 5], 1u << (tag_local(t) & 31u));
-      }
-      __syncwarp();
-      uint32_t base = 0u;
-      for (int w0 = 0; w0 < nwords; w0 += 32) {
-        const int w2 = w0 + lane;
-        const uint32_t bits = w2 < nwords ? wb[r][w2] : 0u;
-        const uint32_t cb = __popc(bits);
-        const uint32_t incl = warp_incl_scan_u32(cb);
-        uint32_t o = base + incl - cb;
-        uint32_t bb = bits;
-        while (bb) {
-          const uint32_t j = __ffs(bb) - 1u;
-          bb &= bb - 1u;
-          if (o < static_cast<uint32_t>(kGather)) wg[r][o] = tag_make(static_cast<uint32_t>(w2) * 32u + j, 0u);
-          ++o;
-        }
-        base += __shfl_sync(kFull, incl, 31);
-      }
-      ngat[r] = min(base, static_cast<uint32_t>(kGather));
-      if (lane == 0) sh.w_over[warp][r] = base > static_cast<uint32_t>(kGather) ? 1u : 0u;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      bool ok = fast[r];
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) ok = ok && sh.w_over[w][r] == 0u;
-      fast[r] = ok;
-    }
-    // exact histogram of the gathered elements at or above the bound
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      if (!fast[r]) continue;
-      const uint32_t thr = H::thr_pack(E::bits_of_key(tau[r]));
-      for (uint32_t i = lane; i < ngat[r]; i += 32) {
-        const int v = sg.beg + static_cast<int>(tag_local(wg[r][i]));
-        const uint4 x = load_vec<DT>(rows[r], v, V, aligned[r]);
-        uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
-        while (msk) {
-          const int j = __ffs(msk) - 1;
-          msk &= msk - 1u;
-          red_add_shared(smem_addr(hist + r * kWindow + (E::key(E::bits_of(x, j)) & kSlotMask)), 1u);
-        }
-      }
-    }
-    if (tid < NR) {
-      sh.g[tid].klo = tau[tid];
-      sh.g[tid].active = fast[tid] ? 1 : 0;
-    }
-    __syncthreads();
-    cut_scan<DT, NR>(sh, hist, c, a.top_k, a.top_p);
-#pragma unroll
-    for (int r = 0; r < NR; ++r) fast[r] = fast[r] && sh.cut[r].found != 0;
-  }
-
-  // ------------------------------------ phase 4: kept set of each row
-#pragma unroll 1
-  for (int r = 0; r < NR; ++r) {
-    const RowG g = sh.g[r];
-    const bool fr = r == 0 ? fast[0] : fast[NR - 1];
-    RowStat rs;
-    rs.c = c;
-    rs.K = g.K;
-    rs.m = g.m;
-    rs.kmax = g.kmax;
-    rs.bad = 0;
-    rs.all_kept = filt ? 0 : 1;
-    rs.covered = fr ? 1 : 0;
-    rs.kstar = 0u;
-    rs.tie_cut = V;
-    float zk = df_float(g.z);
-    if (filt) {
-      const CutOut co = fr ? sh.cut[r] : search_cut<DT>(sh, rows[r], V, aligned[r], a.top_k, a.top_p, rs, df_double(g.z));
-      rs.kstar = co.kstar;
-      zk = df_float(co.zkept);
-      if (co.keep < co.total) {
-        rs.tie_cut = fr ? tie_cut_of<DT, true>(sh, gl[r], r == 0 ? ngat[0] : ngat[NR - 1], rows[r], V, aligned[r],
-                                               co.kstar, co.keep)
-                        : tie_cut_of<DT, false>(sh, gl[r], 0u, rows[r], V, aligned[r], co.kstar, co.keep);
-      }
-    }
-    rs.zkept = zk;
-    rs.inv_z = 1.f / zk;
-    if (tid == 0) sh.rs[r] = rs;
-  }
-  __syncthreads();
-  const RowStat rp = sh.rs[0];
-  const RowStat rq = sh.rs[NR - 1];
-
-  if (a.mode == MODE_PROBS) {
-    write_probs<DT>(rows[0], V, aligned[0], rp, a.out_probs + static_cast<size_t>(unit) * V);
-    return;
-  }
-
-  // ------------------------------------- phase 5: accept test at x_pos
-  if (NR == 2 && tid == 0) {
-    UnitRec* rec = a.recs + unit;
-    float px = 0.f, qx = 0.f;
-    if (xtok >= 0 && xtok < V) {
-      px = prob_of<DT>(rp, sh.xbits[0], xtok);
-      qx = prob_of<DT>(rq, sh.xbits[NR - 1], xtok);
-      const float u = a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos];
-      rec->accept = (u * qx < px) ? 1 : 0;
-    } else {
-      rec->accept = 0;
-      set_status(a.status, SPEC_STATUS_BAD_TOKEN);
-    }
-    rec->px = px;
-    rec->qx = qx;
-    if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
-    if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
-    __threadfence();
-    if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-  }
-
-  // ------------- phase 6: residual (or bonus) by warps, in index order
-  // Fast path: the kept set of p lies in the warps' gathered vectors of p;
-  // the draft's vector at a gathered index is among the gathered vectors of
-  // q, or it holds no kept token of q.  Otherwise each warp re-reads its
-  // segment of the rows.
-  const bool lists_p = rp.covered && !rp.all_kept;
-  const bool lists_q = NR == 2 && rq.covered && !rq.all_kept;
-  const uint32_t np = lists_p ? ngat[0] : 0u;
-  const uint32_t nq = lists_q ? ngat[NR - 1] : 0u;
-  const int rounds = lists_p ? static_cast<int>((np + 31) / 32) : sg.iters;
-  // vector of round it (index order) for this lane, or -1
-  auto round_vec = [&](int it, bool want_q, uint4& xp, uint4& xq, bool& has_q) -> int {
-    has_q = false;
-    if (lists_p) {
-      const uint32_t i = it * 32 + lane;
-      if (i >= np) return -1;
-      const uint32_t vi = tag_local(wg[0][i]);
-      const int v = sg.beg + static_cast<int>(vi);
-      xp = load_vec<DT>(rows[0], v, V, aligned[0]);
-      if (want_q) {
-        if (lists_q) {
-          if (glist_find(wg[NR - 1], nq, vi) >= 0) {
-            xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]);
-            has_q = true;
-          }
-        } else {
-          xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]);
-          has_q = true;
-        }
-      }
-      return v;
+  const Chunk ch = warp_chunk(n, warp);
+  const bool listed = L || G;
+  const int rounds = listed ? (ch.end - ch.beg + 31) / 32 : sg.iters;
+  auto vec_of = [&](int it) -> int {
+    if (listed) {
+      const int e = ch.beg + it * 32 + lane;
+      if (e >= ch.end) return -1;
+      if (L) return static_cast<int>(__ldcg(L + e));
+      int w = 0, off = 0;  // the warp whose gathered tags hold entry e
+      while (w < kWarps - 1 && e >= off + static_cast<int>(sh.w_u[w][0])) off += sh.w_u[w++][0];
+      return warp_seg(nvec, w).beg + static_cast<int>(tag_local(G[w * kGather + (e - off)]));
     }
     const int v = sg.beg + it * 32 + lane;
-    if (v >= sg.end) return -1;
-    xp = load_vec<DT>(rows[0], v, V, aligned[0]);
-    if (want_q) { xq = load_vec<DT>(rows[NR - 1], v, V, aligned[NR - 1]); has_q = true; }
-    return v;
+    return v < sg.end ? v : -1;
   };
   {
     float s = 0.f, sp = 0.f;
     for (int it = 0; it < rounds; ++it) {
-      uint4 xp, xq;
-      bool has_q;
-      const int v = round_vec(it, NR == 2, xp, xq, has_q);
+      const int v = vec_of(it);
       if (v >= 0) {
+        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
+        const uint4 xq = want_q ? load_vec<DT>(rowq, v, V, aq) : xp;
         float w[8], ps;
-        s += vec_weights<DT>(rp, rq, xp, has_q ? &xq : nullptr, v, V, NR == 2, w, &ps);
+        s += vec_weights<DT>(rp, rq, xp, &xq, v, V, want_q, w, &ps);
         sp += ps;
       }
     }
@@ -1264,21 +883,20 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     }
   }
   __syncthreads();
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     DF S{0.f, 0.f}, Sp{0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       S = df_add(S, sh.w_s[w]);
       Sp = df_add(Sp, sh.w_sp[w]);
     }
-    bool use_q = NR == 2;
+    bool use_q = want_q;
     const float* ws = sh.w_s;
-    if (NR == 2 && !(S.hi > 0.f)) {  // degenerate residual: draw from p instead
+    if (want_q && !(S.hi > 0.f)) {  // degenerate residual: draw from p instead
       use_q = false;
       S = Sp;
       ws = sh.w_sp;
     }
-    const float u_draw = a.uniforms[static_cast<size_t>(b) * (kq + 2) + (NR == 2 ? kq + 1 : kq)];
     const DF target = df_mul_f(S, u_draw);
     DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
     int wsel = -1, wlast = -1;
@@ -1292,6 +910,7 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     if (wsel < 0) { wsel = wlast; base = lbase; }
     sh.draw_warp = use_q ? wsel : -2 - wsel;  // -2 - w: weights are p
     sh.draw_base = df_float(df_add2(target, df_neg(base)));
+    if (wsel < 0) *drawn_out = -1;  // nothing to draw from (all mass rounded away)
   }
   __syncthreads();
   const int dw = sh.draw_warp;
@@ -1302,16 +921,16 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
     float run = 0.f;
     int token = -1, last_pos = -1;
     for (int it = 0; it < rounds && token < 0; ++it) {
-      uint4 xp, xq;
-      bool has_q;
-      const int v = round_vec(it, use_q, xp, xq, has_q);
+      const int v = vec_of(it);
       float w[8], ps;
       float ls = 0.f;
       int lpos = -1;
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = 0.f;
       if (v >= 0) {
-        ls = vec_weights<DT>(rp, rq, xp, has_q ? &xq : nullptr, v, V, use_q, w, &ps);
+        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
+        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
+        ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (w[j] > 0.f) lpos = v * E::kPerVec + j;
@@ -1340,47 +959,450 @@ __device__ __forceinline__ void unit_body(const SampleArgs& a, Shm& sh, uint32_t
       run += __shfl_sync(kFull, incl, 31);
     }
     if (token < 0) token = last_pos;  // only reachable through rounding
+    if (lane == 0) *drawn_out = token;
+  }
+  __syncthreads();
+}
+
+// One row of one unit, in the given role.
+template <int DT>
+__device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t* ltags, uint32_t* hist, uint32_t* bmap,
+                                         int role, int unit, int b, int pos, int pair, const unsigned char* row) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V;
+  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
+  const bool bad_t = !(T > 0.f) || isinf(T);
+  const float c = kLog2e / T;
+  const u64 c2 = pkf(c, c);
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const bool aligned = (role == ROLE_Q ? a.aligned_draft : a.aligned_target) != 0;
+  const bool topk_on = a.top_k > 0;
+  const bool topp_on = a.top_p < 1.f;
+  const bool filt = topk_on || topp_on;
+  const int kq = a.k;
+  const bool paired = role == ROLE_P || role == ROLE_Q;
+  const int xtok = paired ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
+  // candidate tags: bf16 rows with a cut, segments short enough to index
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
+  const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
+  uint32_t* const myl = ltags + warp * kLaneTags * 32 + lane;
+  // a warp's gathered list replaces its lanes' tags once they are read
+  uint32_t* const wg = ltags + warp * kGather;
+  uint32_t* const wb = bmap + warp * kBmapWords;
+  GList gl;
+  gl.tags = wg;
+  gl.row = row;
+
+  if (filt)
+    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
+  if (tid == 0) sh.xbits[0] = 0u;
+  __syncthreads();
+
+  // --------------------------------------------------- phase 1: stream
+  float mt = -INFINITY;     // thread maximum
+  int kt = -(1 << 30);      // thread lattice exponent
+  u64 acc0 = 0ull, acc1 = 0ull;  // thread sums of 2^(l c - kt)
+  float mw = -INFINITY;     // CTA maximum of the last exchange
+  uint32_t cnt = 0u;        // lane tag list length
+  uint32_t lfl = 0u;        // lane floor: the lane list is complete above it
+  float lflv = -INFINITY;   // its value
+  float lthr = -INFINITY;   // lane bound: kTheta octaves below mw, at least the lane floor
+  int sync_no = 0;
+  const int xv = xtok >= 0 && xtok < V ? xtok / E::kPerVec : -1;
+  // every warp runs the same number of iterations (the CTA barriers below)
+  const int iters_all = seg_vectors(nvec) / 32;
+  for (int it = 0; it < iters_all; it += 4) {
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = sg.beg + (it + u) * 32 + lane;
+      x[u] = v < sg.end ? load_vec<DT>(row, v, V, aligned) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = sg.beg + (it + u) * 32 + lane;
+      const float vm = H::vmax(x[u]);
+      const float L = vm * c;
+      if (L > static_cast<float>(kt) && L < 1073741824.f) {  // raise the lattice exponent (rare)
+        const int knew = static_cast<int>(ceilf(L));
+        const float s = exp2i(kt - knew);
+        acc0 = mul2(acc0, pkf(s, s));
+        acc1 = mul2(acc1, pkf(s, s));
+        kt = knew;
+      }
+      const float nk = -static_cast<float>(kt);
+      H::mass_vec(x[u], c2, pkf(nk, nk), acc0, acc1);
+      mt = max_nan(mt, vm);
+      lthr = fmaxf(lthr, vm - dtheta);
+      if (v == xv && xv < sg.end) sh.xbits[0] = E::bits_of(x[u], xtok - xv * E::kPerVec);
+      if (use_lists) {
+        // lane bound lthr: kTheta octaves below the larger of this lane's
+        // running maximum and the CTA maximum of the last exchange (both at
+        // most the row maximum), never below the lane floor
+        if (v < sg.end && vm >= lthr) {
+          bool take = true;
+          if (cnt == static_cast<uint32_t>(kLaneTags)) {  // full: keep the largest of this lane
+            cnt = lane_tags_purge(myl, cnt, E::key(bits_round_down<DT>(lthr)));
+            while (cnt == static_cast<uint32_t>(kLaneTags)) {
+              lfl = lane_tags_min_key(myl, cnt) + 1u;
+              lflv = value_of_key<DT>(lfl);
+              cnt = lane_tags_purge(myl, cnt, lfl);
+            }
+            lthr = fmaxf(lthr, lflv);
+            take = vm >= lflv;
+          }
+          if (take) {
+            myl[32 * cnt] = (static_cast<uint32_t>(v - sg.beg) << 16) | (__float_as_uint(vm) >> 16);
+            ++cnt;
+          }
+        }
+      }
+    }
+    const int li = it >> 2;  // loop iteration
+    if (use_lists && (li < kSyncEvery ? (li & (li + 1)) == 0 : (li % kSyncEvery) == kSyncEvery - 1)) {
+      // share the running maxima across the CTA (fixed points, denser at the
+      // start where they rise fastest: deterministic)
+      const int slot = (sync_no++) & 1;
+      const float wm = warp_max_nan(mt);
+      if (lane == 0) sh.x_m[slot][warp][0] = fmaxf(mw, wm);
+      __syncthreads();
+      float mm = mw;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][0]);
+      if (mm > mw) {
+        mw = mm;
+        lthr = fmaxf(lthr, mw - dtheta);
+      }
+    }
+  }
+
+  // ------------------------------------------ phase 2: row maximum and sum
+  {
+    float s0, s1, s2, s3;
+    upk(acc0, s0, s1);
+    upk(acc1, s2, s3);
+    float zt = (s0 + s1) + (s2 + s3);
+    const int kw = warp_max_i32(kt);
+    zt *= exp2i(kt - kw);
+    zt = warp_sum_f32(zt);
+    const float mx = warp_max_nan(mt);
+    const uint32_t fl = warp_max_u32(lfl);
     if (lane == 0) {
-      a.recs[unit].drawn = token;
+      sh.w_m[warp][0] = mx;
+      sh.w_k[warp][0] = kw;
+      sh.w_z[warp][0] = zt;
+      sh.w_floor[warp][0] = fl;
+      sh.w_over[warp][0] = 0u;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float mx = -INFINITY;
+    int kk = -(1 << 30);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mx = max_nan(mx, sh.w_m[w][0]);
+      kk = max(kk, sh.w_k[w][0]);
+    }
+    DF z{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) z = df_add(z, sh.w_z[w][0] * exp2i(sh.w_k[w][0] - kk));
+    RowG g;
+    g.m = mx;
+    g.K = static_cast<float>(kk);
+    g.kmax = key_of_float<DT>(mx);
+    g.z = z;
+    // every vector whose maximum reaches klo is tagged
+    const float tv = mx - dtheta;
+    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
+    const uint32_t gtop = g.kmax >> 2;
+    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][0]);
+    g.klo = kl;
+    g.active = use_lists ? 1 : 0;
+    sh.g[0] = g;
+  }
+  __syncthreads();
+  // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
+  const bool bad = bad_t || !isfinite(sh.g[0].m) || !(fabsf(sh.g[0].m * c) < 1073741824.f);
+
+  // ---------- phase 3: a bound on the cut from the tagged vector maxima
+  // The lane tags hold every vector whose maximum reaches klo.  Vector maxima
+  // are tokens of the row, so the mass (or count) of the row above a value is
+  // at least that of the maxima above it: where the maxima reach the top-p
+  // target (or top_k), the row's cut lies at or above.
+  int ngat = 0;
+  bool fast = false;
+  if (use_lists && !bad) {
+    {
+      const uint32_t kl = sh.g[0].klo;
+      for (uint32_t q = 0; q < cnt; ++q) {
+        const uint32_t k = tag_key(myl[32 * q]);
+        if (k >= kl) red_add_shared(smem_addr(hist + (k & kSlotMask)), 1u);
+      }
+    }
+    __syncthreads();
+    cut_scan<DT, 1>(sh, hist, c, a.top_k, a.top_p);
+    // bound (top-k: its own cut; top-p alone: the maxima's crossing)
+    const CutOut bo = topk_on ? sh.cutk[0] : sh.cut[0];
+    fast = bo.found != 0;
+    const uint32_t tau = bo.kstar;
+    __syncthreads();
+    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
+    // the gathered vectors: the lanes' tags at or above the bound, marked in
+    // the warp's bitmap and read back in index order
+    if (fast) {
+      const int nwords = seg_vectors(nvec) / 32;
+      for (int w2 = lane; w2 < nwords; w2 += 32) wb[w2] = 0u;
+      __syncwarp();
+      for (uint32_t q = 0; q < cnt; ++q) {
+        const uint32_t t = myl[32 * q];
+        if (tag_key(t) >= tau) atomicOr(&wb[tag_local(t) >> 5], 1u << (tag_local(t) & 31u));
+      }
+      __syncwarp();
+      uint32_t base = 0u;
+      for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w2 = w0 + lane;
+        const uint32_t bits = w2 < nwords ? wb[w2] : 0u;
+        const uint32_t cb = __popc(bits);
+        const uint32_t incl = warp_incl_scan_u32(cb);
+        uint32_t o = base + incl - cb;
+        uint32_t bb = bits;
+        while (bb) {
+          const uint32_t j = __ffs(bb) - 1u;
+          bb &= bb - 1u;
+          if (o < static_cast<uint32_t>(kGather)) wg[o] = tag_make(static_cast<uint32_t>(w2) * 32u + j, 0u);
+          ++o;
+        }
+        base += __shfl_sync(kFull, incl, 31);
+      }
+      ngat = static_cast<int>(min(base, static_cast<uint32_t>(kGather)));
+      if (lane == 0) sh.w_over[warp][0] = base > static_cast<uint32_t>(kGather) ? 1u : 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) fast = fast && sh.w_over[w][0] == 0u;
+    // exact histogram of the gathered elements at or above the bound
+    if (fast) {
+      const uint32_t thr = H::thr_pack(E::bits_of_key(tau));
+      for (int i = lane; i < ngat; i += 32) {
+        const int v = sg.beg + static_cast<int>(tag_local(wg[i]));
+        const uint4 x = load_vec<DT>(row, v, V, aligned);
+        wg[i] = tag_make(tag_local(wg[i]), __float_as_uint(H::vmax(x)) >> 16);  // keep its maximum
+        uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
+        while (msk) {
+          const int j = __ffs(msk) - 1;
+          msk &= msk - 1u;
+          red_add_shared(smem_addr(hist + (E::key(E::bits_of(x, j)) & kSlotMask)), 1u);
+        }
+      }
+    }
+    if (tid == 0) {
+      sh.g[0].klo = tau;
+      sh.g[0].active = fast ? 1 : 0;
+    }
+    __syncthreads();
+    cut_scan<DT, 1>(sh, hist, c, a.top_k, a.top_p);
+    fast = fast && sh.cut[0].found != 0;
+  }
+
+  // ------------------------------------------ phase 4: kept set of the row
+  RowStat rs;
+  {
+    const RowG g = sh.g[0];
+    rs.c = c;
+    rs.K = g.K;
+    rs.m = g.m;
+    rs.kmax = g.kmax;
+    rs.bad = bad ? 1 : 0;
+    rs.all_kept = filt ? 0 : 1;
+    rs.covered = fast ? 1 : 0;
+    rs.kstar = 0u;
+    rs.tie_cut = V;
+    float zk = df_float(g.z);
+    if (filt && !bad) {
+      const CutOut co = fast ? sh.cut[0] : search_cut<DT>(sh, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z));
+      rs.kstar = co.kstar;
+      zk = df_float(co.zkept);
+      if (co.keep < co.total)
+        rs.tie_cut = fast ? tie_cut_of<DT, true>(sh, gl, static_cast<uint32_t>(ngat), row, V, aligned, co.kstar, co.keep)
+                          : tie_cut_of<DT, false>(sh, gl, 0u, row, V, aligned, co.kstar, co.keep);
+    }
+    rs.zkept = zk;
+    rs.inv_z = 1.f / zk;
+  }
+
+  if (role == ROLE_PROBS) {
+    float* out = a.out_probs + static_cast<size_t>(unit) * V;
+    if (bad) {
+      for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
+      if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
+    } else {
+      write_probs<DT>(row, V, aligned, rs, out);
+    }
+    return;
+  }
+
+  if (role == ROLE_BONUS) {  // the bonus token, drawn from p
+    UnitRec* rec = a.recs + unit;
+    if (bad) {
+      if (tid == 0) {
+        rec->drawn = -1;
+        set_status(a.status, SPEC_STATUS_BAD_ROW);
+      }
+    } else {
+      // the kept set lies in the gathered vectors when the cut came from them
+      const bool listed = fast && !rs.all_kept;
+      if (listed) {  // this CTA's own gathered vectors, by warps in index order
+        if (lane == 0) sh.w_u[warp][0] = static_cast<uint32_t>(ngat);
+        __syncthreads();
+        uint32_t tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += sh.w_u[w][0];
+        draw_rows<DT>(sh, rs, rs, row, row, aligned, aligned, V, false, nullptr, ltags, static_cast<int>(tot),
+                      a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq], &rec->drawn);
+      } else {
+        draw_rows<DT>(sh, rs, rs, row, row, aligned, aligned, V, false, nullptr, nullptr, 0,
+                      a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq], &rec->drawn);
+      }
+    }
+    if (tid == 0) {
       __threadfence();
       if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
     }
-  } else if (wsel < 0 && tid == 0) {  // nothing to draw from (all mass rounded away)
-    a.recs[unit].drawn = -1;
+    return;
+  }
+
+  // --------------------- a draft position: hand over to the second finisher
+  const int r = role;  // 0: target row, 1: draft row
+  PairRec* pr = a.pairs + pair;
+  if (tid == 0) {
+    pr->rs[r] = rs;
+    pr->xprob[r] = (!bad && xtok >= 0 && xtok < V) ? prob_of<DT>(rs, sh.xbits[0], xtok) : 0.f;
+  }
+  if (r == 0) {  // the target row's vectors holding kept tokens, in index order
+    uint32_t mine = 0u, nk = 0u;
+    if (fast) {
+      for (int i0 = 0; i0 < ngat; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t t = i < ngat ? wg[i] : 0u;
+        const bool keep = i < ngat && tag_key(t) >= rs.kstar;
+        const unsigned ball = __ballot_sync(kFull, keep);
+        if (keep) wg[nk + __popc(ball & ((1u << lane) - 1u))] = t;
+        nk += __popc(ball);
+        __syncwarp();
+      }
+      mine = nk;
+    }
+    if (lane == 0) sh.w_u[warp][0] = mine;
+    __syncthreads();
+    uint32_t off = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) off += sh.w_u[w][0];
+      tot += sh.w_u[w][0];
+    }
+    const bool listed = fast && !rs.all_kept && !bad && tot <= static_cast<uint32_t>(kPairList);
+    if (listed)
+      for (uint32_t i = lane; i < mine; i += 32) pr->list[off + i] = static_cast<uint32_t>(sg.beg) + tag_local(wg[i]);
+    if (tid == 0) pr->nlist = listed ? tot : kPairReread;
+  }
+  __syncthreads();
+  if (tid == 0) {
     __threadfence();
-    if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
+    sh.second = atomicAdd(a.pair_tickets + pair, 1u) == 1u ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh.second) return;
+
+  // ---------------------------- second finisher: accept test, residual draw
+  __threadfence();
+  if (tid == 0) {
+    // the other CTA's half, written before its ticket (read past L1)
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(pr);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&sh.pair_hdr);
+    for (int i = 0; i < static_cast<int>(sizeof(PairHdr) / 4); ++i) dst[i] = __ldcg(src + i);
+  }
+  __syncthreads();
+  const RowStat rp = sh.pair_hdr.rs[0];
+  const RowStat rq = sh.pair_hdr.rs[1];
+  const float px = sh.pair_hdr.xprob[0], qx = sh.pair_hdr.xprob[1];
+  const uint32_t nlist = sh.pair_hdr.nlist;
+  const unsigned char* rowp = static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
+  const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
+                              (static_cast<size_t>(b) * kq + pos) * static_cast<size_t>(V) * E::kBytes;
+  UnitRec* rec = a.recs + unit;
+  const bool xok = xtok >= 0 && xtok < V;
+  if (tid == 0) {
+    rec->accept = (!rp.bad && !rq.bad && xok) ? ((a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos] * qx < px) ? 1 : 0) : 0;
+    rec->px = px;
+    rec->qx = qx;
+    if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
+    if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
+    set_status(a.status, (xok ? 0u : SPEC_STATUS_BAD_TOKEN) | ((rp.bad || rq.bad) ? SPEC_STATUS_BAD_ROW : 0u));
+  }
+  if (rp.bad || rq.bad) {
+    if (tid == 0) rec->drawn = -1;
+  } else {
+    const float u_draw = a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq + 1];
+    if (nlist != kPairReread)
+      draw_rows<DT>(sh, rp, rq, rowp, rowq, a.aligned_target != 0, a.aligned_draft != 0, V, true, pr->list, nullptr,
+                    static_cast<int>(nlist), u_draw, &rec->drawn);
+    else
+      draw_rows<DT>(sh, rp, rq, rowp, rowq, a.aligned_target != 0, a.aligned_draft != 0, V, true, nullptr, nullptr, 0,
+                    u_draw, &rec->drawn);
+  }
+  // leave the workspace zeroed: this position's record and ticket
+  {
+    uint32_t* hdr = reinterpret_cast<uint32_t*>(pr);
+    for (int i = tid; i < static_cast<int>(sizeof(PairHdr) / 4); i += kThreads) hdr[i] = 0u;
+    if (nlist != kPairReread)
+      for (int i = tid; i < static_cast<int>(nlist); i += kThreads) pr->list[i] = 0u;
+  }
+  if (tid == 0) {
+    a.pair_tickets[pair] = 0u;
+    __threadfence();
+    if (atomicAdd(a.tickets + b, 2u) == static_cast<uint32_t>(2 * kq - 1)) sample_finalize(a, b);
   }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
   using E = Elt<DT>;
-  const int unit = static_cast<int>(blockIdx.x);
+  const int cta = static_cast<int>(blockIdx.x);
   const int V = a.V;
   __shared__ Shm sh;
   extern __shared__ __align__(16) uint32_t dsm[];
-  // dynamic shared memory: lane tags [2][kWarps][kLaneTags][32] (later the
-  // gathered tags [2][kWarps][kGather]), histograms [2][kWindow], gather
-  // bitmaps [2][kWarps][kBmapWords]
+  // dynamic shared memory: lane tags [kWarps][kLaneTags][32] (later the
+  // gathered tags [kWarps][kGather]), histogram [kWindow], gather bitmaps
+  // [kWarps][kBmapWords]
   uint32_t* ltags = dsm;
-  uint32_t* hist = ltags + 2 * kWarps * kLaneTags * 32;
-  uint32_t* bmap = hist + 2 * kWindow;
-  if (a.mode == MODE_SAMPLE) {
-    const int b = unit / (a.k + 1);
-    const int pos = unit % (a.k + 1);
-    const unsigned char* rowp =
-        static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-    if (pos < a.k) {
-      const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
-                                  (static_cast<size_t>(b) * a.k + pos) * static_cast<size_t>(V) * E::kBytes;
-      unit_body<DT, 2>(a, sh, ltags, hist, bmap, unit, b, pos, rowp, rowq);
-    } else {
-      unit_body<DT, 1>(a, sh, ltags, hist, bmap, unit, b, pos, rowp, rowp);
-    }
-  } else {
-    const unsigned char* rowp =
-        static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-    unit_body<DT, 1>(a, sh, ltags, hist, bmap, unit, unit, 0, rowp, rowp);
+  uint32_t* hist = ltags + kWarps * kLaneTags * 32;
+  uint32_t* bmap = hist + kWindow;
+  const unsigned char* tgt = static_cast<const unsigned char*>(a.target);
+  if (a.mode == MODE_PROBS) {
+    row_body<DT>(a, sh, ltags, hist, bmap, ROLE_PROBS, cta, cta, 0, 0, tgt + static_cast<size_t>(cta) * V * E::kBytes);
+    return;
+  }
+  const int k = a.k;
+  const int npairs = a.B * k;
+  if (cta < 2 * npairs) {  // a draft position: its target row (even) or draft row (odd)
+    const int pair = cta >> 1;
+    const int r = cta & 1;
+    const int b = pair / k, pos = pair % k;
+    const int unit = b * (k + 1) + pos;
+    const unsigned char* row = r == 0 ? tgt + static_cast<size_t>(unit) * V * E::kBytes
+                                      : static_cast<const unsigned char*>(a.draft) +
+                                            static_cast<size_t>(pair) * V * E::kBytes;
+    row_body<DT>(a, sh, ltags, hist, bmap, r, unit, b, pos, pair, row);
+  } else {  // the bonus position of sequence b
+    const int b = cta - 2 * npairs;
+    const int unit = b * (k + 1) + k;
+    row_body<DT>(a, sh, ltags, hist, bmap, ROLE_BONUS, unit, b, k, 0, tgt + static_cast<size_t>(unit) * V * E::kBytes);
   }
 }
 
@@ -1408,7 +1430,7 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
 
 size_t sample_smem_bytes(int dtype, bool filter) {
   (void)dtype;
-  return filter ? (2 * kWarps * kLaneTags * 32 + 2 * kWindow + 2 * kWarps * kBmapWords) * sizeof(uint32_t) : 16;
+  return filter ? (kWarps * kLaneTags * 32 + kWindow + kWarps * kBmapWords) * sizeof(uint32_t) : 16;
 }
 
 template <int DT>
