@@ -8,30 +8,42 @@
 // p_i(x_i); at the first rejection n one token is drawn from
 // max(0, p_n - q_n) with u_{k+1}, else a bonus token from p_k with u_k.
 //
-// How (one GPU, memory-bound).  One CTA owns one unit (b, i) and streams its
-// target row and draft row from HBM exactly once, 16-byte loads by warp
-// segments in index order.  While streaming, for each row:
+// How (one GPU, memory-bound).  One CTA owns one row: the target or the
+// draft row of a draft position (b, i), or the target row of the bonus
+// position (b, k); the grid is B (2k + 1) CTAs.  Each streams its row from
+// HBM once, 16-byte non-allocating loads by warp segments in index order.
+// While streaming:
 //   - masses are taken on a power-of-two lattice: with c = log2(e) / T and
 //     an integer k_t >= max(l) * c held per thread, mass(l) = 2^(l c - k_t)
 //     (one packed f32x2 fma and one ex2 per element).  Raising k_t rescales
 //     the running sum by an exact power of two, so the row sum
 //     Z = sum 2^(l c - K) (K the CTA-wide k) carries no rescaling error;
 //     2^(l c - K) / Z is the softmax of l / T.
-//   - every element within kTheta octaves of mass of the running maximum is
-//     appended to its warp's candidate list (index order; entries below the
-//     current bound are purged when a list fills).  A top-k / top-p cut
-//     within kTheta octaves of the maximum is therefore decided from the
-//     lists alone: a histogram of exact values, a four-warp scan for the cut,
-//     its tie count and the kept normaliser.  Rows whose cut lies deeper
-//     (flat rows), fp32 rows and overflowing lists take an exact bitwise
-//     search over the keys that re-reads the row.
-// The accept test reads p(x_i), q(x_i) at x_i.  The residual max(0, p - q)
-// (or the bonus p) is non-zero only on the kept set of p, which the lists
-// hold in index order: per-warp sums, a prefix over warps and a walk of one
-// list give the drawn token.  Every unit draws (the residual draw is
-// speculative), so no row is read twice on the fast path.  The last writer
-// of a sequence (atomic ticket, no spin-wait) applies the first-rejection
-// rule and commits.
+//   - candidate vectors: a lane tags every 16-byte vector whose maximum is
+//     within kTheta octaves of mass of the best maximum it knows (its own
+//     running maximum, or the CTA's, exchanged at fixed stream steps).  A tag
+//     is the vector's index in the warp segment and the bf16 pattern of its
+//     maximum.  A full lane list drops the tags below its current bound and,
+//     if still full, raises the lane's floor above its smallest tag; each
+//     list is complete above max(bound, floor).
+// After the stream the tagged maxima above those bounds give a bound on the
+// cut (vector maxima are tokens of the row, so the mass or count above a
+// value is at least that of the maxima above it).  The tagged vectors at or
+// above the bound are gathered in index order and their elements counted in
+// a histogram of exact values; a four-warp scan gives the cut, its tie count
+// and the kept normaliser.  A row the candidates do not decide re-reads
+// itself in windows of exact values from the maximum down, and past a few
+// windows (flat rows crossing zero, 32-bit keys) by a bitwise search.
+// The two CTAs of a draft position each publish their row's state and
+// probability at x_i, and the target CTA the list of its vectors holding
+// kept tokens; the second of the two to finish (pair ticket, no spin-wait)
+// applies the accept test u_i q_i(x_i) < p_i(x_i) and draws from
+// max(0, p_i - q_i) over the listed vectors (the draft row read at the same
+// indices), or over both whole rows when the list overflowed.  The bonus CTA
+// draws from p_k over its own gathered vectors.  Every position draws (the
+// residual draw is speculative), so no CTA waits on another; the last
+// finisher of a sequence (sequence ticket) applies the first-rejection rule
+// and commits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -298,6 +310,8 @@ struct RowG {
   uint32_t kmax;         // key of m
   uint32_t klo;          // lowest key of the scanned window
   DF z;                  // sum of masses 2^(l c - K)
+  uint32_t c0;           // tokens above the window (keys > kmax)
+  DF m0;                 // their mass
   int active;            // the row takes part in the current scan
 };
 
@@ -404,19 +418,29 @@ __device__ __noinline__ double row_pass(Shm& sh, const unsigned char* row, int V
                                         uint32_t kappa, const RowStat& rs) {
   using E = Elt<DT>;
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  constexpr int kU = 4;  // loads in flight per thread
   uint32_t cnt = 0, kmin = 0xFFFFFFFFu;
   float mass = 0.f;
-  for (int v = threadIdx.x; v < nvec; v += kThreads) {
-    const uint4 x = load_vec<DT>(row, v, V, aligned);
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kU * kThreads) {
+    uint4 xs[kU];
 #pragma unroll
-    for (int j = 0; j < E::kPerVec; ++j) {
-      if (v * E::kPerVec + j < V) {
-        const uint32_t b = E::bits_of(x, j);
-        const uint32_t k = E::key(b);
-        if (kind == PASS_COUNT_GE) cnt += (k >= kappa);
-        else if (kind == PASS_COUNT_EQ) cnt += (k == kappa);
-        else if (kind == PASS_MIN_GE) { if (k >= kappa) kmin = min(kmin, k); }
-        else if (k > kappa) mass += lat_mass(E::value(b), rs.c, rs.K);
+    for (int u = 0; u < kU; ++u) {
+      const int v = v0 + u * kThreads;
+      xs[u] = v < nvec ? load_vec<DT>(row, v, V, aligned) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = v0 + u * kThreads;
+#pragma unroll
+      for (int j = 0; j < E::kPerVec; ++j) {
+        if (v * E::kPerVec + j < V) {
+          const uint32_t b = E::bits_of(xs[u], j);
+          const uint32_t k = E::key(b);
+          if (kind == PASS_COUNT_GE) cnt += (k >= kappa);
+          else if (kind == PASS_COUNT_EQ) cnt += (k == kappa);
+          else if (kind == PASS_MIN_GE) { if (k >= kappa) kmin = min(kmin, k); }
+          else if (k > kappa) mass += lat_mass(E::value(b), rs.c, rs.K);
+        }
       }
     }
   }
@@ -551,16 +575,23 @@ __device__ __forceinline__ int glist_find(const uint32_t* tags, uint32_t len, ui
 // running count reaches top_k (sh.cutk); top-p (on the top-k set, if any):
 // where the running mass reaches top_p * Z, a token being kept while the
 // mass ranked before it is below the target (sh.cut).  Rows whose cut lies
-// below the window keep found = 0.  Whole CTA.
+// below the window keep found = 0.  The count and mass of the tokens above
+// the window (g.c0, g.m0) start the running sums.  With given_k the top-k
+// cut in sh.cutk is taken as found earlier and only top-p is scanned.
+// Whole CTA.
 template <int DT, int NR>
-__device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, int top_k, float top_p) {
+__device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, int top_k, float top_p,
+                                      bool given_k = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
   const int r_s = (NR == 2) ? (warp >> 2) : 0;
   const int wq = warp & (kScanWarps - 1);
   const RowG g = sh.g[r_s];
   const bool scanner = ((NR == 2) || warp < kScanWarps) && g.active;
-  if (threadIdx.x < 2) { sh.cut[threadIdx.x].found = 0; sh.cutk[threadIdx.x].found = 0; }
+  if (threadIdx.x < 2) {
+    sh.cut[threadIdx.x].found = 0;
+    if (!given_k) sh.cutk[threadIdx.x].found = 0;
+  }
   uint32_t cnt[4] = {0u, 0u, 0u, 0u}, top = 0u, Cl = 0u, Cex = 0u;
   float ms[4] = {0.f, 0.f, 0.f, 0.f}, Ml = 0.f;
   DF Mex{0.f, 0.f};
@@ -597,8 +628,8 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
     }
   }
   __syncthreads();
-  uint32_t offC = 0u;
-  DF offM{0.f, 0.f}, nxtM{0.f, 0.f}, totM{0.f, 0.f};
+  uint32_t offC = g.c0;
+  DF offM = g.m0, nxtM = g.m0, totM = g.m0;
   if (scanner) {
 #pragma unroll
     for (int q = 0; q < kScanWarps; ++q) {
@@ -609,7 +640,7 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
       totM = df_add2(totM, mq);
     }
   }
-  if (topk_on && scanner) {  // the value where the running count reaches top_k
+  if (topk_on && !given_k && scanner) {  // the value where the running count reaches top_k
     const uint32_t Kc = static_cast<uint32_t>(top_k);
     const uint32_t wC = sh.s_C[r_s][wq];
     if (offC < Kc && offC + wC >= Kc) {
@@ -694,6 +725,98 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
     }
   }
   __syncthreads();
+}
+
+// Exact counts of the row's tokens with keys in [klo, khi] (klo .. klo +
+// kWindow - 1, slot key & (kWindow - 1)), by one re-read of the row with
+// four loads in flight per thread.  Whole CTA.
+template <int DT>
+__device__ __noinline__ void window_pass(uint32_t* hist, const unsigned char* row, int V, bool aligned,
+                                         uint32_t klo, uint32_t khi) {
+  using E = Elt<DT>;
+  constexpr int kU = 4;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  for (int t = threadIdx.x; t < kWindow; t += kThreads) hist[t] = 0u;
+  __syncthreads();
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kU * kThreads) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = v0 + u * kThreads;
+      x[u] = v < nvec ? load_vec<DT>(row, v, V, aligned) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int t0 = (v0 + u * kThreads) * E::kPerVec;
+#pragma unroll
+      for (int j = 0; j < E::kPerVec; ++j) {
+        const uint32_t k = E::key(E::bits_of(x[u], j));
+        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(hist + (k & kSlotMask)), 1u);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+constexpr int kSlowWindows = 8;  // windows of kWindow keys tried before the bitwise search
+
+// The exact cut of a row that the candidate vectors do not decide: windows
+// of kWindow consecutive keys from the row maximum down, each counted by a
+// re-read of the row and scanned with the count and mass above it carried,
+// until the window holding the cut.  Top-k first; top-p then scans the same
+// windows on the top-k set.  A cut more than kSlowWindows windows down
+// takes the bitwise search.  Whole CTA; sh.g[0] is left as it was.
+template <int DT>
+__device__ __noinline__ CutOut window_cut(Shm& sh, uint32_t* hist, const unsigned char* row, int V, bool aligned,
+                                          int top_k, float top_p, const RowStat& rs, double zfull) {
+  // (32-bit keys are too fine for windows of kWindow keys)
+  if (Elt<DT>::kKeyBits > 16) return search_cut<DT>(sh, row, V, aligned, top_k, top_p, rs, zfull);
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  const RowG g0 = sh.g[0];
+  bool ok = true;
+#pragma unroll 1
+  for (int phase = 0; phase < 2 && ok; ++phase) {
+    const bool kphase = phase == 0;
+    if (kphase ? !topk_on : !topp_on) continue;
+    uint32_t hi = g0.kmax, c0 = 0u;
+    DF m0{0.f, 0.f};
+    bool found = false;
+#pragma unroll 1
+    for (int w = 0; w < kSlowWindows && !found; ++w) {
+      const uint32_t gt = hi >> 2;
+      const uint32_t lo = gt >= static_cast<uint32_t>(kGroups - 1) ? 4u * (gt - static_cast<uint32_t>(kGroups - 1)) : 0u;
+      window_pass<DT>(hist, row, V, aligned, lo, hi);
+      if (threadIdx.x == 0) {
+        RowG g = g0;
+        g.kmax = hi;
+        g.klo = lo;
+        g.c0 = c0;
+        g.m0 = m0;
+        g.active = 1;
+        sh.g[0] = g;
+      }
+      __syncthreads();
+      cut_scan<DT, 1>(sh, hist, rs.c, top_k, kphase ? 1.f : top_p, !kphase);
+      found = (kphase ? sh.cutk[0].found : sh.cut[0].found) != 0;
+      if (!found) {
+#pragma unroll
+        for (int q = 0; q < kScanWarps; ++q) {
+          c0 += sh.s_C[0][q];
+          m0 = df_add2(m0, sh.s_M[0][q]);
+        }
+        if (lo == 0u) break;
+        hi = lo - 1u;
+      }
+      __syncthreads();
+    }
+    ok = found;
+  }
+  CutOut co = sh.cut[0];
+  __syncthreads();
+  if (threadIdx.x == 0) sh.g[0] = g0;
+  __syncthreads();
+  if (!ok) co = search_cut<DT>(sh, row, V, aligned, top_k, top_p, rs, zfull);
+  return co;
 }
 
 // Tie cut of a row: tokens of value kstar are kept in index order, the
@@ -1115,6 +1238,8 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     g.K = static_cast<float>(kk);
     g.kmax = key_of_float<DT>(mx);
     g.z = z;
+    g.c0 = 0u;
+    g.m0 = DF{0.f, 0.f};
     // every vector whose maximum reaches klo is tagged
     const float tv = mx - dtheta;
     uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
@@ -1225,7 +1350,7 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     rs.tie_cut = V;
     float zk = df_float(g.z);
     if (filt && !bad) {
-      const CutOut co = fast ? sh.cut[0] : search_cut<DT>(sh, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z));
+      const CutOut co = fast ? sh.cut[0] : window_cut<DT>(sh, hist, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z));
       rs.kstar = co.kstar;
       zk = df_float(co.zkept);
       if (co.keep < co.total)

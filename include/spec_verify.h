@@ -67,7 +67,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
                                       or a per-sequence temperature <= 0        */
 #define SPEC_STATUS_BAD_PARENT 4u  /* parents[0] != -1 or parents[j] not in [0, j) */
 #define SPEC_STATUS_DEPTH 8u       /* an agreed tree node deeper than max_depth */
-#define SPEC_STATUS_TIMEOUT 16u    /* a bounded wait on a bulk copy gave up     */
+#define SPEC_STATUS_TIMEOUT 16u    /* reserved: a bounded device wait gave up   */
 
 /* Limits. */
 #define SPEC_MAX_K 31              /* drafts per sequence                       */

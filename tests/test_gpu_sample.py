@@ -116,6 +116,28 @@ def test_masked_minus_inf_entries():
     _check(case)
 
 
+# One token per row towers over an N(0, 1) rest, so the kept set reaches far
+# below the row maximum in value: beyond the candidate vectors the stream
+# keeps, down one or more windows of values, or past every window (top-p
+# 0.999 crosses zero).
+SPIKES = [
+    # (top_k, top_p, spike)
+    (50, 1.0, 30.0),
+    (0, 0.9, 12.0),
+    (40, 0.98, 25.0),
+    (40, 0.9999, 14.0),
+    (3000, 1.0, 40.0),
+    (0, 0.999, 12.0),
+]
+
+
+@pytest.mark.parametrize("top_k,top_p,spike", SPIKES)
+def test_cut_far_below_the_row_maximum(top_k, top_p, spike):
+    case = W.random_sample_case(4, 3, 50000, seed=13, sigma=1.0, noise=0.5, top_k=top_k, top_p=top_p,
+                                spike=spike)
+    _check(case)
+
+
 def test_unaligned_rows_match_aligned():
     case = W.random_sample_case(4, 3, 4096, seed=5, top_p=0.9)
     base = run_sample_gpu(case)

@@ -267,13 +267,22 @@ def config4(seed: int = 4, B: int = 8, N: int = 60, V: int = 128256, max_depth: 
 def random_sample_case(B: int, k: int, V: int, dtype: str = BF16, seed: int = 0, sigma: float = 3.0,
                        noise: float = 1.0, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,
                        per_seq_temperature: bool = False, mask_fn: Optional[MaskFn] = None,
-                       quantize: Optional[float] = None) -> SampleCase:
+                       quantize: Optional[float] = None, spike: Optional[float] = None) -> SampleCase:
     """Small random case for edge coverage.  ``quantize`` rounds logits to a grid
-    (many exact ties)."""
+    (many exact ties); ``spike`` adds that much to one random token of every
+    target row and to the same token of the draft row at that position (one
+    token towering over the rest)."""
     ss = np.random.SeedSequence([seed, B, k, V])
     s_l, s_d, s_tok, s_u, s_t = ss.spawn(5)
     L = _rng(s_l).normal(0.0, sigma, size=(B, k + 1, V)).astype(np.float32)
     D = (L[:, :k] + _rng(s_d).normal(0.0, noise, size=(B, k, V))).astype(np.float32)
+    if spike:
+        at = _rng(ss.spawn(1)[0]).integers(0, V, size=(B, k + 1))
+        for b in range(B):
+            for j in range(k + 1):
+                L[b, j, at[b, j]] += np.float32(spike)
+                if j < k:
+                    D[b, j, at[b, j]] += np.float32(spike)
     if quantize:
         L = (np.round(L / quantize) * quantize).astype(np.float32)
         D = (np.round(D / quantize) * quantize).astype(np.float32)
