@@ -86,27 +86,8 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   return SPEC_OK;
 }
 
-int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-      sms = 148;
-  }
-  return sms;
-}
-
-// Elements per CTA for the argmax kernel: a multiple of 8, about two waves of
-// eight resident CTAs per SM, at least 2048 elements per CTA.
-int argmax_split_len(int rows, int V) {
-  const long long total = static_cast<long long>(rows) * V;
-  long long len = total / (static_cast<long long>(num_sms()) * 8 * 2);
-  len = (len + 7) / 8 * 8;
-  if (len < 2048) len = 2048;
-  if (len > V) len = (V + 7) / 8 * 8;
-  return static_cast<int>(len);
-}
+// Elements of one 16-byte vector.
+int vec_elems(spec_dtype d) { return 16 / static_cast<int>(elt_bytes(d)); }
 
 // ------------------------------------------------ allocation-free sampling
 // Fixed scratch for spec_verify_sample_noalloc: the workspace layout of the
@@ -216,8 +197,7 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   a.B = B;
   a.R = k + 1;
   a.V = V;
-  a.split_len = argmax_split_len(B * (k + 1), V);
-  a.splits = (V + a.split_len - 1) / a.split_len;
+  a.nvr = (V + vec_elems(dtype) - 1) / vec_elems(dtype);
   a.aligned = rows_aligned(target_logits, V, dtype);
   a.out_tokens = out_tokens;
   a.out_n = out_num_accepted;
@@ -252,8 +232,7 @@ int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
   a.R = N;
   a.V = V;
   a.max_depth = max_depth;
-  a.split_len = argmax_split_len(B * N, V);
-  a.splits = (V + a.split_len - 1) / a.split_len;
+  a.nvr = (V + vec_elems(dtype) - 1) / vec_elems(dtype);
   a.aligned = rows_aligned(node_logits, V, dtype);
   a.out_tokens = out_tokens;
   a.out_path = out_path;

@@ -9,13 +9,18 @@
 // whose tokens all equal the argmax of their parent's row is committed, plus
 // the argmax of its last node's row.
 //
-// Both reduce to one argmax per row (lowest index on ties) followed by a tiny
-// per-sequence walk.  Each row is split over several CTAs that stream their
-// slice once with 16-byte non-allocating loads; a CTA's (value, index) winner
-// is folded into the row's slot with one 64-bit atomicMax on an order-
-// preserving packing; the last CTA of a sequence (atomic ticket, no
-// spin-wait) does the walk, writes the outputs and re-zeroes the slots.
+// Both reduce to one argmax per row (lowest index on ties, -0 equal to +0)
+// followed by a tiny per-sequence walk.  The batch's rows are laid end to end
+// as 16-byte vectors and cut into one equal range per CTA, one wave of CTAs
+// sized to the GPU; a CTA streams its range once with 16-byte non-allocating
+// loads, eight in flight per thread, and folds its (value, index) winner for
+// each row piece into the row's slot with one 64-bit atomicMax on an order-
+// preserving packing.  A per-sequence ticket counts the vectors folded in; the
+// CTA that completes a sequence (no spin-wait) does the walk, writes the
+// outputs and re-zeroes the slots.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <math.h>
 
 #include "device_common.cuh"
@@ -45,121 +50,39 @@ struct TreeShm {
   int am[kMaxTreeNodes];
   int par[kMaxTreeNodes];
   int tok[kMaxTreeNodes];
-  int depth[kMaxTreeNodes];
-  unsigned char agreed[kMaxTreeNodes];
 };
+
+__device__ __forceinline__ int warp_max_i32(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
 
 }  // namespace
 
-template <int DT, bool TREE>
-__global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
-  using E = Elt<DT>;
+// The walk of sequence b by the CTA that completed it (whole CTA; every
+// node or position in parallel, no serial chain of loads).
+template <bool TREE>
+__device__ __forceinline__ void sequence_walk(const ArgmaxArgs& a, int b) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = static_cast<int>(blockIdx.x) / a.splits;
-  const int split = static_cast<int>(blockIdx.x) % a.splits;
-  const int b = row / a.R;
-  const int lo = min(a.V, split * a.split_len);
-  const int hi = min(a.V, lo + a.split_len);
-  const unsigned char* base =
-      static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * a.V * E::kBytes;
-
-  __shared__ unsigned long long s_best[kWarps];
-  __shared__ uint32_t s_nan[kWarps];
-  __shared__ int s_last;
-
-  // ---- this thread's best over its vectors: (value, first vector holding it)
-  float best = 0.f;
-  int best_pos = -1;  // element index of the first vector (or element) holding `best`
-  uint32_t nan_seen = 0;
-  if (a.aligned) {
-    const int nvec = (hi - lo) / E::kPerVec;  // lo, hi are multiples of kPerVec (hi may be V)
-    const uint4* vp = reinterpret_cast<const uint4*>(base + static_cast<size_t>(lo) * E::kBytes);
-    for (int v0 = tid; v0 < nvec; v0 += kThreads * kUnroll) {
-      uint4 x[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * kThreads;
-        x[u] = v < nvec ? ldg_stream(vp + v) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * kThreads;
-        if (v < nvec) {
-          float vm = E::value(E::bits_of(x[u], 0));
-#pragma unroll
-          for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x[u], j)));
-          if (vm != vm) {
-            nan_seen = 1u;
-          } else if (best_pos < 0 || vm > best) {
-            best = vm;
-            best_pos = lo + v * E::kPerVec;
-          }
-        }
-      }
-    }
-    // the first element of the winning vector that equals the vector maximum
-    if (best_pos >= 0) {
-      const uint4 x = ldg_stream(reinterpret_cast<const uint4*>(base + static_cast<size_t>(best_pos) * E::kBytes));
-      int j0 = E::kPerVec - 1;
-#pragma unroll
-      for (int j = E::kPerVec - 1; j >= 0; --j)
-        if (E::value(E::bits_of(x, j)) == best) j0 = j;
-      best_pos += j0;
-    }
-  } else {
-    for (int t = lo + tid; t < hi; t += kThreads) {
-      const float v = E::value(E::bits_at(base, t));
-      if (v != v) {
-        nan_seen = 1u;
-      } else if (best_pos < 0 || v > best) {
-        best = v;
-        best_pos = t;
-      }
-    }
-  }
-  unsigned long long mine = 0ull;
-  if (best_pos >= 0) {
-    const uint32_t bits = (E::kBytes == 2) ? (__float_as_uint(best) >> 16) : __float_as_uint(best);
-    mine = pack_best(E::key(bits), best_pos);
-  }
-  mine = warp_max_u64(mine);
-  nan_seen = warp_max_u32(nan_seen);
-  if (lane == 0) { s_best[warp] = mine; s_nan[warp] = nan_seen; }
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long m = 0ull;
-    uint32_t nn = 0;
-    for (int w = 0; w < kWarps; ++w) { m = s_best[w] > m ? s_best[w] : m; nn |= s_nan[w]; }
-    if (nn) set_status(a.status, SPEC_STATUS_BAD_ROW);
-    if (m) atomicMax(a.slots + row, m);
-    __threadfence();
-    const uint32_t total = static_cast<uint32_t>(a.R * a.splits);
-    s_last = (atomicAdd(a.tickets + b, 1u) == total - 1u) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ------------------------------------------- last CTA of sequence b: walk
   unsigned long long* slots = a.slots + static_cast<size_t>(b) * a.R;
+  __shared__ int s_red[kWarps];
   if constexpr (!TREE) {
-    if (tid == 0) {
-      const int k = a.R - 1;
-      const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
-      int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
-      int n = k;
-      for (int i = 0; i <= k; ++i) {
-        const int am = unpack_index(__ldcg(slots + i));
-        if (i == k || x[i] != am) {
-          out[i] = am;
-          n = i;
-          break;
-        }
-        out[i] = am;
-      }
-      for (int i = n + 1; i <= k; ++i) out[i] = -1;
-      a.out_n[b] = n;
-    }
+    // n = the first position whose draft differs from the target's argmax
+    const int k = a.R - 1;
+    const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
+    int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
+    int first = k;
+    for (int i = tid; i < k; i += kThreads)
+      if (x[i] != unpack_index(__ldcg(slots + i))) first = min(first, i);
+    first = -warp_max_i32(-first);
+    if (lane == 0) s_red[warp] = first;
+    __syncthreads();
+    int n = k;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) n = min(n, s_red[w]);
+    for (int i = tid; i <= k; i += kThreads) out[i] = i <= n ? unpack_index(__ldcg(slots + i)) : -1;
+    if (tid == 0) a.out_n[b] = n;
   } else {
     __shared__ TreeShm ts;
     const int N = a.R;
@@ -171,33 +94,52 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
       ts.tok[j] = tok[j];
     }
     __syncthreads();
-    if (tid == 0) {
-      uint32_t st = 0;
-      if (ts.par[0] != -1) st |= SPEC_STATUS_BAD_PARENT;
-      ts.agreed[0] = 1;
-      ts.depth[0] = 0;
-      int best = 0;
-      for (int j = 1; j < N; ++j) {
-        const int p = ts.par[j];
-        ts.agreed[j] = 0;
-        ts.depth[j] = 0;
-        if (p < 0 || p >= j) {
-          st |= SPEC_STATUS_BAD_PARENT;
-          continue;
-        }
-        ts.depth[j] = ts.depth[p] + 1;
-        bool ag = ts.agreed[p] && ts.tok[j] == ts.am[p];
-        if (ag && ts.depth[j] > a.max_depth) {
-          st |= SPEC_STATUS_DEPTH;
-          ag = false;
-        }
-        ts.agreed[j] = ag ? 1 : 0;
-        if (ag && ts.depth[j] > ts.depth[best]) best = j;
+    // node j is agreed iff every node on its path from the root has a valid
+    // parent (p < j) and a token equal to its parent's argmax, and it lies at
+    // depth <= max_depth; an agreed-path node at max_depth + 1 is reported.
+    // Best: the deepest agreed node, the lowest index among equals.
+    uint32_t st = 0;
+    int key = -1;
+    for (int j = tid; j < N; j += kThreads) {
+      if (j == 0) {
+        if (ts.par[0] != -1) st |= SPEC_STATUS_BAD_PARENT;
+        key = max(key, (0 << 16) | 0xFFFF);
+        continue;
       }
+      const int pj = ts.par[j];
+      if (pj < 0 || pj >= j) st |= SPEC_STATUS_BAD_PARENT;
+      bool ok = true;  // every node from j up has a valid parent and matches its argmax
+      int d = 0;       // edges walked from j
+      for (int c = j; c != 0;) {
+        const int p = ts.par[c];
+        // an invalid parent, or j deeper than max_depth + 1 (neither kept nor reported)
+        if (p < 0 || p >= c || d > a.max_depth) {
+          ok = false;
+          break;
+        }
+        ok = ok && ts.tok[c] == ts.am[p];
+        ++d;
+        c = p;
+      }
+      if (ok && d > a.max_depth) {
+        if (d == a.max_depth + 1) st |= SPEC_STATUS_DEPTH;
+        ok = false;
+      }
+      if (ok) key = max(key, (d << 16) | (0xFFFF - j));
+    }
+    if (st) set_status(a.status, st);
+    key = warp_max_i32(key);
+    if (lane == 0) s_red[warp] = key;
+    __syncthreads();
+    if (tid == 0) {
+      int bk = -1;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) bk = max(bk, s_red[w]);
+      const int best = 0xFFFF - (bk & 0xFFFF);
       const int D = a.max_depth + 1;
       int32_t* ot = a.out_tokens + static_cast<size_t>(b) * D;
       int32_t* op = a.out_path + static_cast<size_t>(b) * D;
-      const int len = ts.depth[best];
+      const int len = bk >> 16;
       for (int i = len + 1; i < D; ++i) { ot[i] = -1; op[i] = -1; }
       ot[len] = ts.am[best];
       if (len < D) op[len] = -1;
@@ -206,7 +148,6 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
         ot[i] = ts.tok[c];
       }
       a.out_n[b] = len;
-      set_status(a.status, st);
     }
   }
   __syncthreads();
@@ -214,9 +155,134 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
   if (tid == 0) a.tickets[b] = 0u;
 }
 
-int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream) {
+template <int DT, bool TREE>
+__global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
+  using E = Elt<DT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V, nvr = a.nvr;
+  // this CTA's range of row vectors (rows laid end to end)
+  const long long units = static_cast<long long>(a.B) * a.R * nvr;
+  const long long u0 = static_cast<long long>(blockIdx.x) * units / gridDim.x;
+  const long long u1 = (static_cast<long long>(blockIdx.x) + 1) * units / gridDim.x;
+  const uint32_t seq_units = static_cast<uint32_t>(a.R) * static_cast<uint32_t>(nvr);
+
+  __shared__ unsigned long long s_best[kWarps];
+  __shared__ uint32_t s_nan[kWarps];
+  __shared__ int s_last;
+
+  for (long long us = u0; us < u1;) {
+    // the piece of one row: row vectors [v_lo, v_hi)
+    const int row = static_cast<int>(us / nvr);
+    const long long rbeg = static_cast<long long>(row) * nvr;
+    const long long ue = min(u1, rbeg + nvr);
+    const int v_lo = static_cast<int>(us - rbeg), v_hi = static_cast<int>(ue - rbeg);
+    us = ue;
+    const int b = row / a.R;
+    const unsigned char* base =
+        static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(row) * V * E::kBytes;
+
+    // ---- this thread's best: (value, its first index), vectors in index order
+    float best = 0.f;
+    int best_pos = -1;
+    uint32_t nan_seen = 0;
+    if (a.aligned) {  // whole 16-byte vectors (V is a multiple of kPerVec)
+      const uint4* vp = reinterpret_cast<const uint4*>(base);
+      for (int v0 = v_lo + tid; v0 < v_hi; v0 += kThreads * kUnroll) {
+        uint4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * kThreads;
+          x[u] = v < v_hi ? ldg_stream(vp + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * kThreads;
+          if (v < v_hi) {
+            float vm = E::value(E::bits_of(x[u], 0));
+#pragma unroll
+            for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x[u], j)));
+            if (vm != vm) {
+              nan_seen = 1u;
+            } else if (best_pos < 0 || vm > best) {
+              int j0 = E::kPerVec - 1;
+#pragma unroll
+              for (int j = E::kPerVec - 1; j >= 0; --j)
+                if (E::value(E::bits_of(x[u], j)) == vm) j0 = j;
+              best = vm;
+              best_pos = v * E::kPerVec + j0;
+            }
+          }
+        }
+      }
+    } else {
+      const int hi = min(V, v_hi * E::kPerVec);
+      for (int t = v_lo * E::kPerVec + tid; t < hi; t += kThreads) {
+        const float v = E::value(E::bits_at(base, t));
+        if (v != v) {
+          nan_seen = 1u;
+        } else if (best_pos < 0 || v > best) {
+          best = v;
+          best_pos = t;
+        }
+      }
+    }
+    unsigned long long mine = 0ull;
+    if (best_pos >= 0) {
+      // -0 and +0 compare equal: both take the key of +0
+      const uint32_t bits = best == 0.f ? 0u
+                            : (E::kBytes == 2) ? (__float_as_uint(best) >> 16) : __float_as_uint(best);
+      mine = pack_best(E::key(bits), best_pos);
+    }
+    mine = warp_max_u64(mine);
+    nan_seen = warp_max_u32(nan_seen);
+    if (lane == 0) { s_best[warp] = mine; s_nan[warp] = nan_seen; }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long m = 0ull;
+      uint32_t nn = 0;
+      for (int w = 0; w < kWarps; ++w) { m = s_best[w] > m ? s_best[w] : m; nn |= s_nan[w]; }
+      if (nn) set_status(a.status, SPEC_STATUS_BAD_ROW);
+      if (m) atomicMax(a.slots + row, m);
+      __threadfence();
+      const uint32_t mine_units = static_cast<uint32_t>(v_hi - v_lo);
+      s_last = (atomicAdd(a.tickets + b, mine_units) + mine_units == seq_units) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      sequence_walk<TREE>(a, b);
+    }
+  }
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  if (dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+int launch_argmax(const ArgmaxArgs& args, int dtype, bool tree, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const dim3 grid(static_cast<unsigned>(a.B * a.R * a.splits));
+  const void* kern = dtype == DT_BF16 ? (tree ? reinterpret_cast<const void*>(argmax_kernel<DT_BF16, true>)
+                                              : reinterpret_cast<const void*>(argmax_kernel<DT_BF16, false>))
+                                      : (tree ? reinterpret_cast<const void*>(argmax_kernel<DT_F32, true>)
+                                              : reinterpret_cast<const void*>(argmax_kernel<DT_F32, false>));
+  // one wave: resident CTAs per SM x SMs, at most one CTA per 256 row vectors
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const long long units = static_cast<long long>(args.B) * args.R * args.nvr;
+  long long g = static_cast<long long>(num_sms()) * per_sm;
+  g = std::min(g, (units + 255) / 256);
+  ArgmaxArgs a = args;
+  a.grid = static_cast<int>(std::max(1LL, g));
+  const dim3 grid(static_cast<unsigned>(a.grid));
   if (dtype == DT_BF16) {
     if (tree) argmax_kernel<DT_BF16, true><<<grid, kThreads, 0, st>>>(a);
     else argmax_kernel<DT_BF16, false><<<grid, kThreads, 0, st>>>(a);

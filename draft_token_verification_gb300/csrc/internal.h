@@ -124,8 +124,8 @@ struct ArgmaxArgs {
   const int32_t* parents;      // tree only
   int B, R, V;                 // R rows per sequence (k+1, or N)
   int max_depth;               // tree only
-  int splits;                  // CTAs per row
-  int split_len;               // elements per CTA, multiple of 8
+  int nvr;                     // 16-byte vectors per row: ceil(V / elements per vector)
+  int grid;                    // CTAs (set by the launcher)
   int aligned;
   int32_t* out_tokens;
   int32_t* out_path;
@@ -139,5 +139,6 @@ struct ArgmaxArgs {
 int launch_sample(const SampleArgs& a, int dtype, int units, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
 size_t sample_smem_bytes(int dtype, bool filter);
+int num_sms();
 
 }  // namespace specv

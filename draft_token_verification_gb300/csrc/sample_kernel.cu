@@ -1536,13 +1536,19 @@ __device__ void sample_finalize(const SampleArgs& a, int b) {
   __threadfence();
   const int k = a.k;
   const UnitRec* rec = a.recs + static_cast<size_t>(b) * (k + 1);
-  int n = k;
+  // every record is read (no early exit), so the loads overlap
+  int n = k, dn = __ldcg(&rec[k].drawn);
+#pragma unroll 4
   for (int i = 0; i < k; ++i) {
-    if (__ldcg(&rec[i].accept) == 0) { n = i; break; }
+    const int2 r = __ldcg(reinterpret_cast<const int2*>(rec + i));  // (accept, drawn)
+    if (r.x == 0 && n == k) {
+      n = i;
+      dn = r.y;
+    }
   }
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
   for (int i = 0; i < n; ++i) out[i] = a.tokens[static_cast<size_t>(b) * k + i];
-  out[n] = __ldcg(&rec[n].drawn);
+  out[n] = dn;
   for (int i = n + 1; i <= k; ++i) out[i] = -1;
   a.out_n[b] = n;
   // leave the workspace zeroed for the next call, whatever its shape
