@@ -44,8 +44,8 @@ SPEC_STATUS_TIMEOUT = 16
 
 SPEC_MAX_K = 31
 SPEC_MAX_TREE_NODES = 1024
-SPEC_NOALLOC_MAX_B = 1024
-SPEC_NOALLOC_MAX_UNITS = 1024
+SPEC_NOALLOC_MAX_B = 256
+SPEC_NOALLOC_MAX_UNITS = 256
 
 EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",

@@ -71,17 +71,19 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   const WsLayout L = ws_layout(B, a.k);
   unsigned char* w = static_cast<unsigned char*>(ws);
   a.status = reinterpret_cast<uint32_t*>(w + L.status);
-  a.tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
-  a.recs = reinterpret_cast<UnitRec*>(w + L.s_recs);
-  a.pair_tickets = reinterpret_cast<uint32_t*>(w + L.p_tickets);
-  a.pairs = reinterpret_cast<PairRec*>(w + L.p_recs);
+  a.seq_tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
+  a.draw_tickets = reinterpret_cast<uint32_t*>(w + L.d_tickets);
+  a.hdrs = reinterpret_cast<RowHdr*>(w + L.hdrs);
+  a.tags = reinterpret_cast<uint32_t*>(w + L.tags);
+  a.pubs = reinterpret_cast<RowPub*>(w + L.pubs);
+  a.csums = reinterpret_cast<float*>(w + L.csums);
+  // the draw at the first rejection: a few chunks over listed vectors, more
+  // over whole rows (no filter)
+  a.chunks = (a.top_k > 0 || a.top_p < 1.f) ? 8 : kMaxDrawChunks;
   a.aligned_target = rows_aligned(target, V, dtype);
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
-  // one CTA per row: target and draft rows of every draft position, then the
-  // bonus target rows (MODE_PROBS: one per row)
-  const int ctas = mode == MODE_SAMPLE ? B * (2 * k + 1) : B;
-  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, ctas, stream);
+  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }
@@ -90,14 +92,12 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
 int vec_elems(spec_dtype d) { return 16 / static_cast<int>(elt_bytes(d)); }
 
 // ------------------------------------------------ allocation-free sampling
-// Fixed scratch for spec_verify_sample_noalloc: the workspace layout of the
-// largest shape it accepts (status word, per-sequence tickets, unit records,
-// plus the argmax slots the layout reserves).  Every GPU that loads the
-// library holds one copy until the process exits.
-constexpr size_t kNoAllocBytes =
-    256 + align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_B, 256) + align_up(sizeof(UnitRec) * SPEC_NOALLOC_MAX_UNITS, 256) +
-    align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_UNITS, 256) + align_up(sizeof(PairRec) * SPEC_NOALLOC_MAX_UNITS, 256) +
-    align_up(sizeof(uint64_t) * SPEC_NOALLOC_MAX_UNITS, 256) + align_up(sizeof(uint32_t) * SPEC_NOALLOC_MAX_B, 256);
+// Fixed scratch for spec_verify_sample_noalloc: a bound on the workspace
+// layout of every shape it accepts (B <= SPEC_NOALLOC_MAX_B and B*(k+1) <=
+// SPEC_NOALLOC_MAX_UNITS, so at most 2 * SPEC_NOALLOC_MAX_UNITS rows).  Every
+// GPU that loads the library holds one copy until the process exits.
+constexpr size_t kNoAllocBytes = ws_bound(SPEC_NOALLOC_MAX_B, 2 * static_cast<size_t>(SPEC_NOALLOC_MAX_UNITS),
+                                          SPEC_NOALLOC_MAX_UNITS);
 constexpr int kNoAllocMaxDevices = 64;
 
 std::mutex g_noalloc_mu;
@@ -160,10 +160,9 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
   int rc = noalloc_scratch(&scratch);
   if (rc != SPEC_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  // The array keeps whatever the previous call left: the status word, the
-  // per-sequence tickets, the unit records and the per-position tickets must
-  // start at zero (the position records are written before they are read).
-  if (cudaMemsetAsync(scratch, 0, L.p_recs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  // The array keeps whatever the previous call left: the status word and the
+  // tickets must start at zero (everything else is written before it is read).
+  if (cudaMemsetAsync(scratch, 0, L.hdrs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
   rc = run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                   out_num_accepted, out_p_draft, out_q_draft, nullptr, scratch, kNoAllocBytes, cuda_stream,
                   MODE_SAMPLE);
@@ -269,7 +268,7 @@ const char* spec_error_string(int code) {
     case SPEC_ERR_TIMEOUT: return "a bounded device wait gave up";
     case SPEC_ERR_UNSUPPORTED: return "shape beyond the library's limits";
     case SPEC_ERR_SCRATCH_LIMIT:
-      return "B > 1024 or B*(k+1) > 1024: beyond the fixed scratch of spec_verify_sample_noalloc";
+      return "B > 256 or B*(k+1) > 256: beyond the fixed scratch of spec_verify_sample_noalloc";
     default: return "unknown error code";
   }
 }

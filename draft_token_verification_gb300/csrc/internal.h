@@ -21,16 +21,6 @@ constexpr int kMaxTreeNodes = 1024;
 constexpr int MODE_SAMPLE = 0;          // speculative-sampling verification
 constexpr int MODE_PROBS = 1;           // write filtered probabilities
 
-// Per (sequence, position) result of the sampling kernel, written by the CTA
-// that owns the draft token (accept, px, qx) and by the CTA that owns the
-// drawn token (drawn).
-struct UnitRec {
-  int32_t accept;
-  int32_t drawn;
-  float px;
-  float qx;
-};
-
 // The kept set and normaliser of one filtered row: token j of key (value
 // order) `key` is kept iff all_kept, or key > kstar, or key == kstar and
 // j < tie_cut; its probability is 2^(l c - K) * inv_z.
@@ -48,50 +38,84 @@ struct RowState {
   int32_t bad;
 };
 
-// What the two CTAs of a draft position (target row, draft row) hand to the
-// one of them that finishes second: each row's state and probability at the
-// draft token, and the target row's candidate vectors (index order), which
-// hold its kept set; nlist = kPairReread when they are not listed.
-constexpr int kPairList = 1024;
-constexpr uint32_t kPairReread = 0xFFFFFFFFu;
-struct PairRec {
-  RowState rs[2];
-  float xprob[2];
-  uint32_t nlist;
-  uint32_t pad;
-  uint32_t list[kPairList];
+// Sampling runs as three launches.  The stream kernel reads every row once
+// and leaves a RowHdr and its candidate tags; the tail kernel decides each
+// row's kept set from them (RowPub) and, in the last CTA of a sequence, the
+// accepted prefix n; the draw kernel draws the token at position n.
+constexpr int kTagsPerWarp = 1024;      // candidate tags per warp segment handed to the tail kernel
+constexpr int kRowTags = kWarps * kTagsPerWarp;
+
+// One row after the stream kernel.
+struct RowHdr {
+  float m;               // row maximum
+  float K;               // lattice exponent
+  float zhi, zlo;        // sum of 2^(l c - K) over the row, as a double-float
+  uint32_t kmax;         // key of m
+  uint32_t klo;          // every tag list is complete at and above this key
+  uint32_t xbits;        // the row's value at the draft token (draft positions)
+  int32_t bad;           // bad temperature, no finite maximum, or |m c| >= 2^30
+  uint32_t ntags[kWarps];  // tags at or above klo handed over per warp segment
 };
 
+// One row after the tail kernel: its kept set, its probability at the draft
+// token and, for target rows, the row vectors holding its kept tokens in
+// index order (nlist = kPubReread when they are not listed).
+constexpr int kPubList = 1024;
+constexpr uint32_t kPubReread = 0xFFFFFFFFu;
+struct RowPub {
+  RowState rs;
+  float xprob;
+  uint32_t nlist;
+  uint32_t pad[2];
+  uint32_t list[kPubList];
+};
+
+// Chunks of the draw at the first rejection: one CTA each.
+constexpr int kMaxDrawChunks = 16;
+
 // Workspace layout (byte offsets), identical for every call with the same
-// (B, k).  All regions are zero between calls except the status word (the
-// pair records are written before they are read).
+// (B, k).  Tickets are zero between calls; everything else is written before
+// it is read within a call (the status word collects sticky bits until
+// spec_get_status clears it).
 struct WsLayout {
   size_t status;      // uint32 status word (sticky bits)
-  size_t s_tickets;   // uint32[B]  arrivals per sequence, sampling kernel
-  size_t s_recs;      // UnitRec[B*(k+1)]
-  size_t p_tickets;   // uint32[B*k]  arrivals per draft position
-  size_t p_recs;      // PairRec[B*k]
+  size_t s_tickets;   // uint32[B]  rows finished per sequence, tail kernel
+  size_t d_tickets;   // uint32[B]  chunks finished per sequence, draw kernel
+  size_t hdrs;        // RowHdr[rows]
+  size_t tags;        // uint32[rows][kRowTags]
+  size_t pubs;        // RowPub[rows]
+  size_t csums;       // float4[B][kMaxDrawChunks]  per-chunk draw sums
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
-  size_t g_tickets;   // uint32[B]  arrivals per sequence / tree, argmax kernel
+  size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
   size_t total;
 };
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr WsLayout ws_layout(int B, int k) {
+// Rows of a sampling call: the k+1 target and k draft rows of each sequence
+// (k = 0: the B rows of spec_transform_probs).
+constexpr size_t sample_rows(int B, int k) { return static_cast<size_t>(B) * static_cast<size_t>(2 * k + 1); }
+
+constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   WsLayout w{};
-  const size_t units = static_cast<size_t>(B) * static_cast<size_t>(k + 1);
-  const size_t pairs = static_cast<size_t>(B) * static_cast<size_t>(k);
   w.status = 0;
   w.s_tickets = 256;
-  w.s_recs = align_up(w.s_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
-  w.p_tickets = align_up(w.s_recs + sizeof(UnitRec) * units, 256);
-  w.p_recs = align_up(w.p_tickets + sizeof(uint32_t) * pairs, 256);
-  w.g_slots = align_up(w.p_recs + sizeof(PairRec) * pairs, 256);
+  w.d_tickets = align_up(w.s_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.hdrs = align_up(w.d_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.tags = align_up(w.hdrs + sizeof(RowHdr) * rows, 256);
+  w.pubs = align_up(w.tags + sizeof(uint32_t) * kRowTags * rows, 256);
+  w.csums = align_up(w.pubs + sizeof(RowPub) * rows, 256);
+  w.g_slots = align_up(w.csums + 16 * static_cast<size_t>(kMaxDrawChunks) * static_cast<size_t>(B), 256);
   w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
   w.total = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
   return w;
 }
+constexpr WsLayout ws_layout(int B, int k) {
+  return ws_layout_of(static_cast<size_t>(B), sample_rows(B, k), static_cast<size_t>(B) * static_cast<size_t>(k + 1));
+}
+// Every region grows with its count: the layout of the largest counts bounds
+// the layouts of all smaller shapes.
+constexpr size_t ws_bound(size_t B, size_t rows, size_t units) { return ws_layout_of(B, rows, units).total; }
 
 struct SampleArgs {
   const void* target;          // [B][k+1][V] (MODE_PROBS: [R][V])
@@ -109,10 +133,13 @@ struct SampleArgs {
   float* out_q;
   float* out_probs;            // MODE_PROBS output [R][V]
   uint32_t* status;
-  uint32_t* tickets;
-  UnitRec* recs;
-  uint32_t* pair_tickets;      // [B*k]
-  PairRec* pairs;              // [B*k]
+  uint32_t* seq_tickets;       // [B]
+  uint32_t* draw_tickets;      // [B]
+  RowHdr* hdrs;                // [rows]
+  uint32_t* tags;              // [rows][kRowTags]
+  RowPub* pubs;                // [rows]
+  float* csums;                // [B][kMaxDrawChunks][4]
+  int chunks;                  // draw chunks per sequence (<= kMaxDrawChunks)
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;
@@ -135,8 +162,9 @@ struct ArgmaxArgs {
   uint32_t* tickets;
 };
 
-// Launchers (return a cudaError_t as int).
-int launch_sample(const SampleArgs& a, int dtype, int units, void* stream);
+// Launchers (return a cudaError_t as int).  launch_sample issues the stream
+// and tail kernels, and the draw kernel in MODE_SAMPLE.
+int launch_sample(const SampleArgs& a, int dtype, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
 size_t sample_smem_bytes(int dtype, bool filter);
 int num_sms();

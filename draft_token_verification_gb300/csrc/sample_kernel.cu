@@ -47,12 +47,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 
 #include "device_common.cuh"
 
 namespace specv {
-
-__device__ void sample_finalize(const SampleArgs& a, int b);
 
 namespace {
 
@@ -67,6 +66,8 @@ constexpr float kTheta = 13.f;                      // octaves of mass kept as c
 constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
 constexpr int kGroups = kWindow / 4;                // aligned groups of four keys
 constexpr int kScanWarps = 4;                       // warps that scan one row's histogram
+constexpr int kVecCacheAt = 256;                    // gathered tags before, cached vectors after (words)
+constexpr int kVecCache = (kGather - kVecCacheAt) / 4;  // cached gathered vectors per warp (192)
 
 // ------------------------------------------------------- packed f32x2 math
 
@@ -155,7 +156,6 @@ __device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
 __device__ __forceinline__ DF df_shfl_up(DF a, int o) {
   return DF{__shfl_up_sync(kFull, a.hi, o), __shfl_up_sync(kFull, a.lo, o)};
 }
-__device__ __forceinline__ DF df_shfl(DF a, int l) { return DF{__shfl_sync(kFull, a.hi, l), __shfl_sync(kFull, a.lo, l)}; }
 __device__ __forceinline__ DF warp_incl_scan_df(DF v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -273,15 +273,6 @@ __device__ __forceinline__ uint32_t bits_round_down(float v) {
 // The kept set of a row: key > kstar, or key == kstar and index < tie_cut.
 using RowStat = RowState;
 
-// The leading part of a PairRec: both rows' states and probabilities at the
-// draft token, and the length of the target row's vector list.
-struct PairHdr {
-  RowState rs[2];
-  float xprob[2];
-  uint32_t nlist;
-  uint32_t pad;
-};
-static_assert(offsetof(PairRec, list) == sizeof(PairHdr), "PairRec must start with a PairHdr");
 
 __device__ __forceinline__ bool kept_key(const RowStat& rs, uint32_t key, int j) {
   if (rs.all_kept) return true;
@@ -337,8 +328,11 @@ struct Shm {
   RowStat rs[2];
   int draw_warp;
   float draw_base;
-  int second;                  // this CTA finished second of its draft position
-  PairHdr pair_hdr;            // the pair's states, as read by the second finisher
+  int second;                  // this CTA is the last of its sequence (tail, draw kernels)
+  int draw_chunk;              // the chunk holding the draw target, or -1
+  int draw_useq;               // the draw weights are max(0, p - q)
+  int draw_token;
+  DF draw_target;              // the draw target within its chunk
 };
 
 // 16-byte vector v of a row (elements v*kPerVec ...), -inf beyond n.
@@ -554,20 +548,9 @@ __device__ __forceinline__ uint32_t lane_tags_min_key(const uint32_t* L, uint32_
 struct GList {
   const uint32_t* tags;
   const unsigned char* row;
+  const uint4* vc;  // the gathered vectors themselves (same order), or null: read from the row
 };
 
-// Position of local vector index vi among index-ordered tags, or -1.
-__device__ __forceinline__ int glist_find(const uint32_t* tags, uint32_t len, uint32_t vi) {
-  int lo = 0, hi = static_cast<int>(len) - 1;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    const uint32_t x = tag_local(tags[mid]);
-    if (x == vi) return mid;
-    if (x < vi) lo = mid + 1;
-    else hi = mid - 1;
-  }
-  return -1;
-}
 
 // The cut of each active row from a histogram of exact keys (slot
 // key & (kWindow - 1), keys g.klo .. g.kmax): four warps per row scan groups
@@ -838,7 +821,7 @@ __device__ __noinline__ int tie_cut_of(Shm& sh, const GList& L, uint32_t len, co
       const uint32_t i = it * 32 + lane;
       if (i >= len) return -1;
       const int v = sg.beg + static_cast<int>(tag_local(L.tags[i]));
-      x = load_vec<DT>(L.row, v, V, aligned);
+      x = L.vc ? L.vc[i] : load_vec<DT>(L.row, v, V, aligned);
       return v;
     }
     const int v = sg.beg + it * 32 + lane;
@@ -944,155 +927,62 @@ constexpr int ROLE_Q = 1;      // draft row of a draft position
 constexpr int ROLE_BONUS = 2;  // target row after the last draft
 constexpr int ROLE_PROBS = 3;  // one row of spec_transform_probs
 
-// Draw weights over one CTA-wide index-ordered set of vectors, per warp
-// chunks: warp w takes entries [w n / kWarps, (w + 1) n / kWarps) of the
-// set.  `vec_at(e)` gives the row vector index of entry e.
-struct Chunk {
-  int beg, end;
+// The row of CTA `cta` in the stream and tail kernels: the target (even) and
+// draft (odd) rows of every draft position, then the bonus target rows
+// (MODE_PROBS: row cta).
+struct RowRef {
+  int role, b, pos;
+  const unsigned char* row;
+  bool aligned;
 };
-__device__ __forceinline__ Chunk warp_chunk(int n, int warp) {
-  Chunk ch;
-  ch.beg = static_cast<int>((static_cast<long long>(n) * warp) / kWarps);
-  ch.end = static_cast<int>((static_cast<long long>(n) * (warp + 1)) / kWarps);
-  return ch;
-}
-
-// The residual (use_q) or target (p) draw over the vectors listed in L (row
-// vector indices, index order), or over the whole rows when L is null:
-// per-warp sums, then the warp holding u * S walks its part.  Writes the drawn
-// token (or -1) to *drawn_out from one thread.  Whole CTA.
-// G (when L is null and G is not): the CTA's own per-warp gathered tags, warp
-// w's at G + w * kGather, n in all, sh.w_u[w][0] of them in warp w.
 template <int DT>
-__device__ __noinline__ void draw_rows(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
-                                       const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
-                                       const uint32_t* L, const uint32_t* G, int n, float u_draw, int* drawn_out) {
+__device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int cta) {
   using E = Elt<DT>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
-  const Seg sg = warp_seg(nvec, warp);
-  const Chunk ch = warp_chunk(n, warp);
-  const bool listed = L || G;
-  const int rounds = listed ? (ch.end - ch.beg + 31) / 32 : sg.iters;
-  auto vec_of = [&](int it) -> int {
-    if (listed) {
-      const int e = ch.beg + it * 32 + lane;
-      if (e >= ch.end) return -1;
-      if (L) return static_cast<int>(__ldcg(L + e));
-      int w = 0, off = 0;  // the warp whose gathered tags hold entry e
-      while (w < kWarps - 1 && e >= off + static_cast<int>(sh.w_u[w][0])) off += sh.w_u[w++][0];
-      return warp_seg(nvec, w).beg + static_cast<int>(tag_local(G[w * kGather + (e - off)]));
-    }
-    const int v = sg.beg + it * 32 + lane;
-    return v < sg.end ? v : -1;
-  };
-  {
-    float s = 0.f, sp = 0.f;
-    for (int it = 0; it < rounds; ++it) {
-      const int v = vec_of(it);
-      if (v >= 0) {
-        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
-        const uint4 xq = want_q ? load_vec<DT>(rowq, v, V, aq) : xp;
-        float w[8], ps;
-        s += vec_weights<DT>(rp, rq, xp, &xq, v, V, want_q, w, &ps);
-        sp += ps;
-      }
-    }
-    s = warp_sum_f32(s);
-    sp = warp_sum_f32(sp);
-    if (lane == 0) {
-      sh.w_s[warp] = s;
-      sh.w_sp[warp] = sp;
-    }
+  const unsigned char* tgt = static_cast<const unsigned char*>(a.target);
+  const size_t rb = static_cast<size_t>(a.V) * E::kBytes;
+  RowRef r;
+  if (a.mode == MODE_PROBS) {
+    r.role = ROLE_PROBS;
+    r.b = cta;
+    r.pos = 0;
+    r.row = tgt + static_cast<size_t>(cta) * rb;
+    r.aligned = a.aligned_target != 0;
+    return r;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    DF S{0.f, 0.f}, Sp{0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      S = df_add(S, sh.w_s[w]);
-      Sp = df_add(Sp, sh.w_sp[w]);
-    }
-    bool use_q = want_q;
-    const float* ws = sh.w_s;
-    if (want_q && !(S.hi > 0.f)) {  // degenerate residual: draw from p instead
-      use_q = false;
-      S = Sp;
-      ws = sh.w_sp;
-    }
-    const DF target = df_mul_f(S, u_draw);
-    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
-    int wsel = -1, wlast = -1;
-    for (int w = 0; w < kWarps; ++w) {
-      const float sw = ws[w];
-      const DF nxt = df_add(run, sw);
-      if (sw > 0.f) { wlast = w; lbase = run; }
-      if (wsel < 0 && sw > 0.f && df_lt(target, nxt)) { wsel = w; base = run; }
-      run = nxt;
-    }
-    if (wsel < 0) { wsel = wlast; base = lbase; }
-    sh.draw_warp = use_q ? wsel : -2 - wsel;  // -2 - w: weights are p
-    sh.draw_base = df_float(df_add2(target, df_neg(base)));
-    if (wsel < 0) *drawn_out = -1;  // nothing to draw from (all mass rounded away)
+  const int k = a.k, npairs = a.B * k;
+  if (cta < 2 * npairs) {
+    const int pair = cta >> 1;
+    r.role = (cta & 1) ? ROLE_Q : ROLE_P;
+    r.b = pair / k;
+    r.pos = pair % k;
+    r.row = r.role == ROLE_P ? tgt + static_cast<size_t>(r.b * (k + 1) + r.pos) * rb
+                             : static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(pair) * rb;
+    r.aligned = (r.role == ROLE_P ? a.aligned_target : a.aligned_draft) != 0;
+  } else {
+    r.role = ROLE_BONUS;
+    r.b = cta - 2 * npairs;
+    r.pos = k;
+    r.row = tgt + static_cast<size_t>(r.b * (k + 1) + k) * rb;
+    r.aligned = a.aligned_target != 0;
   }
-  __syncthreads();
-  const int dw = sh.draw_warp;
-  const bool use_q = dw >= 0;
-  const int wsel = use_q ? dw : -2 - dw;
-  if (warp == wsel) {
-    const float tw = sh.draw_base;
-    float run = 0.f;
-    int token = -1, last_pos = -1;
-    for (int it = 0; it < rounds && token < 0; ++it) {
-      const int v = vec_of(it);
-      float w[8], ps;
-      float ls = 0.f;
-      int lpos = -1;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = 0.f;
-      if (v >= 0) {
-        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
-        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
-        ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (w[j] > 0.f) lpos = v * E::kPerVec + j;
-      }
-      const float incl = warp_incl_scan(ls);
-      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
-      const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
-      const int lp2 = __shfl_sync(kFull, lpos, lastl);
-      if (lp2 >= 0) last_pos = lp2;
-      if (ball) {
-        const int l = __ffs(ball) - 1;
-        int tok = -1;
-        if (lane == l) {
-          float cum = run + (incl - ls);
-          int lastj = -1;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (w[j] > 0.f) lastj = v * E::kPerVec + j;
-            cum += w[j];
-            if (tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
-          }
-          if (tok < 0) tok = lastj;
-        }
-        token = __shfl_sync(kFull, tok, l);
-      }
-      run += __shfl_sync(kFull, incl, 31);
-    }
-    if (token < 0) token = last_pos;  // only reachable through rounding
-    if (lane == 0) *drawn_out = token;
-  }
-  __syncthreads();
+  return r;
 }
 
-// One row of one unit, in the given role.
+// ---------------------------------------------------------- stream kernel
+// One CTA per row: stream it once (lattice masses, maximum, candidate tags),
+// then hand over the row header and the tags at or above klo.
 template <int DT>
-__device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t* ltags, uint32_t* hist, uint32_t* bmap,
-                                         int role, int unit, int b, int pos, int pair, const unsigned char* row) {
+__global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a) {
   using E = Elt<DT>;
   using H = Hot<DT>;
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  uint32_t* const ltags = dsm;  // lane tags [kWarps][kLaneTags][32]
+  const int cta = static_cast<int>(blockIdx.x);
+  const RowRef rr = row_ref<DT>(a, cta);
+  const int role = rr.role, b = rr.b, pos = rr.pos;
+  const unsigned char* const row = rr.row;
+  const bool aligned = rr.aligned;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = a.V;
   const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
@@ -1101,10 +991,7 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
   const u64 c2 = pkf(c, c);
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
   const Seg sg = warp_seg(nvec, warp);
-  const bool aligned = (role == ROLE_Q ? a.aligned_draft : a.aligned_target) != 0;
-  const bool topk_on = a.top_k > 0;
-  const bool topp_on = a.top_p < 1.f;
-  const bool filt = topk_on || topp_on;
+  const bool filt = a.top_k > 0 || a.top_p < 1.f;
   const int kq = a.k;
   const bool paired = role == ROLE_P || role == ROLE_Q;
   const int xtok = paired ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
@@ -1112,15 +999,7 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
   const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
   const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
   uint32_t* const myl = ltags + warp * kLaneTags * 32 + lane;
-  // a warp's gathered list replaces its lanes' tags once they are read
-  uint32_t* const wg = ltags + warp * kGather;
-  uint32_t* const wb = bmap + warp * kBmapWords;
-  GList gl;
-  gl.tags = wg;
-  gl.row = row;
 
-  if (filt)
-    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
   if (tid == 0) sh.xbits[0] = 0u;
   __syncthreads();
 
@@ -1255,8 +1134,130 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
   // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
   const bool bad = bad_t || !isfinite(sh.g[0].m) || !(fabsf(sh.g[0].m * c) < 1073741824.f);
 
+  // ------------- hand over: the row header and its tags at or above klo
+  {
+    const bool lists = use_lists && !bad;
+    const uint32_t kl = sh.g[0].klo;
+    uint32_t mine = 0u;
+    if (lists)
+      for (uint32_t q = 0; q < cnt; ++q) mine += tag_key(myl[32 * q]) >= kl ? 1u : 0u;
+    const uint32_t incl = warp_incl_scan_u32(mine);
+    if (lists) {
+      uint32_t* dst = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
+      uint32_t o = incl - mine;  // (at most kLaneTags * 32 = kTagsPerWarp in all)
+      for (uint32_t q = 0; q < cnt; ++q) {
+        const uint32_t t = myl[32 * q];
+        if (tag_key(t) >= kl) dst[o++] = t;
+      }
+    }
+    if (lane == 31) sh.w_u[warp][0] = lists ? incl : 0u;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const RowG g = sh.g[0];
+    RowHdr h;
+    h.m = g.m;
+    h.K = g.K;
+    h.zhi = g.z.hi;
+    h.zlo = g.z.lo;
+    h.kmax = g.kmax;
+    h.klo = g.klo;
+    h.xbits = sh.xbits[0];
+    h.bad = bad ? 1 : 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) h.ntags[w] = sh.w_u[w][0];
+    a.hdrs[cta] = h;
+  }
+}
+
+// ------------------------------------------------------------ tail kernel
+// One CTA per row, after the stream kernel: the kept set of the row from its
+// header and tags (or by re-reading the row), published with its probability
+// at the draft token and, for target rows, its kept vectors.  The last row
+// of a sequence to finish applies the first-rejection rule.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 5) tail_kernel(const SampleArgs a) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  // dynamic shared memory: tags [kWarps][kTagsPerWarp] (then the gathered
+  // tags in their place), histogram [kWindow], gather bitmaps
+  // [kWarps][kBmapWords]
+  uint32_t* const ltags = dsm;
+  uint32_t* const hist = ltags + kRowTags;
+  uint32_t* const bmap = hist + kWindow;
+  const int cta = static_cast<int>(blockIdx.x);
+  const RowRef rr = row_ref<DT>(a, cta);
+  const int role = rr.role, b = rr.b, pos = rr.pos;
+  const unsigned char* const row = rr.row;
+  const bool aligned = rr.aligned;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V;
+  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
+  const bool bad_t = !(T > 0.f) || isinf(T);
+  const float c = kLog2e / T;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const bool topk_on = a.top_k > 0;
+  const bool topp_on = a.top_p < 1.f;
+  const bool filt = topk_on || topp_on;
+  const int kq = a.k;
+  const bool paired = role == ROLE_P || role == ROLE_Q;
+  const int xtok = paired ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
+  // a warp's tags, then its gathered vectors (index order)
+  uint32_t* const wg = ltags + warp * kGather;
+  uint32_t* const wb = bmap + warp * kBmapWords;
+  GList gl;
+  gl.tags = wg;
+  gl.row = row;
+  gl.vc = nullptr;
+  // gathered vectors cached after the first kVecCacheAt words of the warp's region
+  uint4* const vc = reinterpret_cast<uint4*>(wg + kVecCacheAt);
+
+  const RowHdr* const hp = a.hdrs + cta;
+  const bool bad = hp->bad != 0;
+  const uint32_t ntag = use_lists && !bad ? hp->ntags[warp] : 0u;
+  if (tid == 0) {
+    RowG g;
+    g.m = hp->m;
+    g.K = hp->K;
+    g.kmax = hp->kmax;
+    g.klo = hp->klo;
+    g.z = DF{hp->zhi, hp->zlo};
+    g.c0 = 0u;
+    g.m0 = DF{0.f, 0.f};
+    g.active = use_lists ? 1 : 0;
+    sh.g[0] = g;
+    sh.xbits[0] = hp->xbits;
+  }
+  if (filt)
+    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
+  {  // (the handed-over tags and header are left zeroed for the next call)
+    uint32_t* src = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
+    for (uint32_t i0 = 0; i0 < ntag; i0 += 32 * 8) {  // eight loads in flight per lane
+      uint32_t t8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = i0 + 32 * u + lane;
+        t8[u] = i < ntag ? src[i] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = i0 + 32 * u + lane;
+        if (i < ntag) {
+          wg[i] = t8[u];
+          src[i] = 0u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < static_cast<int>(sizeof(RowHdr) / 4)) reinterpret_cast<uint32_t*>(a.hdrs + cta)[tid] = 0u;
+
   // ---------- phase 3: a bound on the cut from the tagged vector maxima
-  // The lane tags hold every vector whose maximum reaches klo.  Vector maxima
+  // The tags hold every vector whose maximum reaches klo.  Vector maxima
   // are tokens of the row, so the mass (or count) of the row above a value is
   // at least that of the maxima above it: where the maxima reach the top-p
   // target (or top_k), the row's cut lies at or above.
@@ -1265,8 +1266,8 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
   if (use_lists && !bad) {
     {
       const uint32_t kl = sh.g[0].klo;
-      for (uint32_t q = 0; q < cnt; ++q) {
-        const uint32_t k = tag_key(myl[32 * q]);
+      for (uint32_t i = lane; i < ntag; i += 32) {
+        const uint32_t k = tag_key(wg[i]);
         if (k >= kl) red_add_shared(smem_addr(hist + (k & kSlotMask)), 1u);
       }
     }
@@ -1278,14 +1279,14 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     const uint32_t tau = bo.kstar;
     __syncthreads();
     for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
-    // the gathered vectors: the lanes' tags at or above the bound, marked in
-    // the warp's bitmap and read back in index order
+    // the gathered vectors: the warp's tags at or above the bound, marked in
+    // its bitmap and read back in index order (in the tags' place)
     if (fast) {
       const int nwords = seg_vectors(nvec) / 32;
       for (int w2 = lane; w2 < nwords; w2 += 32) wb[w2] = 0u;
       __syncwarp();
-      for (uint32_t q = 0; q < cnt; ++q) {
-        const uint32_t t = myl[32 * q];
+      for (uint32_t i = lane; i < ntag; i += 32) {
+        const uint32_t t = wg[i];
         if (tag_key(t) >= tau) atomicOr(&wb[tag_local(t) >> 5], 1u << (tag_local(t) & 31u));
       }
       __syncwarp();
@@ -1314,9 +1315,11 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     // exact histogram of the gathered elements at or above the bound
     if (fast) {
       const uint32_t thr = H::thr_pack(E::bits_of_key(tau));
+      const bool cache = ngat <= kVecCache;
       for (int i = lane; i < ngat; i += 32) {
         const int v = sg.beg + static_cast<int>(tag_local(wg[i]));
         const uint4 x = load_vec<DT>(row, v, V, aligned);
+        if (cache) vc[i] = x;
         wg[i] = tag_make(tag_local(wg[i]), __float_as_uint(H::vmax(x)) >> 16);  // keep its maximum
         uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
         while (msk) {
@@ -1333,7 +1336,9 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     __syncthreads();
     cut_scan<DT, 1>(sh, hist, c, a.top_k, a.top_p);
     fast = fast && sh.cut[0].found != 0;
+    if (fast && ngat <= kVecCache) gl.vc = vc;
   }
+
 
   // ------------------------------------------ phase 4: kept set of the row
   RowStat rs;
@@ -1361,8 +1366,9 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     rs.inv_z = 1.f / zk;
   }
 
+
   if (role == ROLE_PROBS) {
-    float* out = a.out_probs + static_cast<size_t>(unit) * V;
+    float* out = a.out_probs + static_cast<size_t>(cta) * V;
     if (bad) {
       for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
       if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
@@ -1372,44 +1378,19 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
     return;
   }
 
-  if (role == ROLE_BONUS) {  // the bonus token, drawn from p
-    UnitRec* rec = a.recs + unit;
-    if (bad) {
-      if (tid == 0) {
-        rec->drawn = -1;
-        set_status(a.status, SPEC_STATUS_BAD_ROW);
-      }
-    } else {
-      // the kept set lies in the gathered vectors when the cut came from them
-      const bool listed = fast && !rs.all_kept;
-      if (listed) {  // this CTA's own gathered vectors, by warps in index order
-        if (lane == 0) sh.w_u[warp][0] = static_cast<uint32_t>(ngat);
-        __syncthreads();
-        uint32_t tot = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) tot += sh.w_u[w][0];
-        draw_rows<DT>(sh, rs, rs, row, row, aligned, aligned, V, false, nullptr, ltags, static_cast<int>(tot),
-                      a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq], &rec->drawn);
-      } else {
-        draw_rows<DT>(sh, rs, rs, row, row, aligned, aligned, V, false, nullptr, nullptr, 0,
-                      a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq], &rec->drawn);
-      }
-    }
-    if (tid == 0) {
-      __threadfence();
-      if (atomicAdd(a.tickets + b, 1u) == static_cast<uint32_t>(2 * kq)) sample_finalize(a, b);
-    }
-    return;
-  }
-
-  // --------------------- a draft position: hand over to the second finisher
-  const int r = role;  // 0: target row, 1: draft row
-  PairRec* pr = a.pairs + pair;
+  // ------------------------------------------------------------- publish
+  RowPub* const pub = a.pubs + cta;
   if (tid == 0) {
-    pr->rs[r] = rs;
-    pr->xprob[r] = (!bad && xtok >= 0 && xtok < V) ? prob_of<DT>(rs, sh.xbits[0], xtok) : 0.f;
+    const bool xok = xtok >= 0 && xtok < V;
+    const float xp = (!bad && paired && xok) ? prob_of<DT>(rs, sh.xbits[0], xtok) : 0.f;
+    pub->rs = rs;
+    pub->xprob = xp;
+    if (role == ROLE_P && a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = xp;
+    if (role == ROLE_Q && a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = xp;
+    const uint32_t st = (bad ? SPEC_STATUS_BAD_ROW : 0u) | ((role == ROLE_P && !xok) ? SPEC_STATUS_BAD_TOKEN : 0u);
+    if (st) set_status(a.status, st);
   }
-  if (r == 0) {  // the target row's vectors holding kept tokens, in index order
+  if (role == ROLE_P || role == ROLE_BONUS) {  // the vectors holding kept tokens, in index order
     uint32_t mine = 0u, nk = 0u;
     if (fast) {
       for (int i0 = 0; i0 < ngat; i0 += 32) {
@@ -1431,158 +1412,309 @@ __device__ __forceinline__ void row_body(const SampleArgs& a, Shm& sh, uint32_t*
       if (w < warp) off += sh.w_u[w][0];
       tot += sh.w_u[w][0];
     }
-    const bool listed = fast && !rs.all_kept && !bad && tot <= static_cast<uint32_t>(kPairList);
+    const bool listed = fast && !rs.all_kept && !bad && tot <= static_cast<uint32_t>(kPubList);
     if (listed)
-      for (uint32_t i = lane; i < mine; i += 32) pr->list[off + i] = static_cast<uint32_t>(sg.beg) + tag_local(wg[i]);
-    if (tid == 0) pr->nlist = listed ? tot : kPairReread;
+      for (uint32_t i = lane; i < mine; i += 32) pub->list[off + i] = static_cast<uint32_t>(sg.beg) + tag_local(wg[i]);
+    if (tid == 0) pub->nlist = listed ? tot : kPubReread;
   }
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    sh.second = atomicAdd(a.pair_tickets + pair, 1u) == 1u ? 1 : 0;
+    sh.second = atomicAdd(a.seq_tickets + b, 1u) == static_cast<uint32_t>(2 * kq) ? 1 : 0;
   }
   __syncthreads();
   if (!sh.second) return;
 
-  // ---------------------------- second finisher: accept test, residual draw
-  __threadfence();
+  // ------------- the last row of sequence b: the first-rejection rule
   if (tid == 0) {
-    // the other CTA's half, written before its ticket (read past L1)
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(pr);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(&sh.pair_hdr);
-    for (int i = 0; i < static_cast<int>(sizeof(PairHdr) / 4); ++i) dst[i] = __ldcg(src + i);
-  }
-  __syncthreads();
-  const RowStat rp = sh.pair_hdr.rs[0];
-  const RowStat rq = sh.pair_hdr.rs[1];
-  const float px = sh.pair_hdr.xprob[0], qx = sh.pair_hdr.xprob[1];
-  const uint32_t nlist = sh.pair_hdr.nlist;
-  const unsigned char* rowp = static_cast<const unsigned char*>(a.target) + static_cast<size_t>(unit) * V * E::kBytes;
-  const unsigned char* rowq = static_cast<const unsigned char*>(a.draft) +
-                              (static_cast<size_t>(b) * kq + pos) * static_cast<size_t>(V) * E::kBytes;
-  UnitRec* rec = a.recs + unit;
-  const bool xok = xtok >= 0 && xtok < V;
-  if (tid == 0) {
-    rec->accept = (!rp.bad && !rq.bad && xok) ? ((a.uniforms[static_cast<size_t>(b) * (kq + 2) + pos] * qx < px) ? 1 : 0) : 0;
-    rec->px = px;
-    rec->qx = qx;
-    if (a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = px;
-    if (a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = qx;
-    set_status(a.status, (xok ? 0u : SPEC_STATUS_BAD_TOKEN) | ((rp.bad || rq.bad) ? SPEC_STATUS_BAD_ROW : 0u));
-  }
-  if (rp.bad || rq.bad) {
-    if (tid == 0) rec->drawn = -1;
-  } else {
-    const float u_draw = a.uniforms[static_cast<size_t>(b) * (kq + 2) + kq + 1];
-    if (nlist != kPairReread)
-      draw_rows<DT>(sh, rp, rq, rowp, rowq, a.aligned_target != 0, a.aligned_draft != 0, V, true, pr->list, nullptr,
-                    static_cast<int>(nlist), u_draw, &rec->drawn);
-    else
-      draw_rows<DT>(sh, rp, rq, rowp, rowq, a.aligned_target != 0, a.aligned_draft != 0, V, true, nullptr, nullptr, 0,
-                    u_draw, &rec->drawn);
-  }
-  // leave the workspace zeroed: this position's record and ticket
-  {
-    uint32_t* hdr = reinterpret_cast<uint32_t*>(pr);
-    for (int i = tid; i < static_cast<int>(sizeof(PairHdr) / 4); i += kThreads) hdr[i] = 0u;
-    if (nlist != kPairReread)
-      for (int i = tid; i < static_cast<int>(nlist); i += kThreads) pr->list[i] = 0u;
-  }
-  if (tid == 0) {
-    a.pair_tickets[pair] = 0u;
     __threadfence();
-    if (atomicAdd(a.tickets + b, 2u) == static_cast<uint32_t>(2 * kq - 1)) sample_finalize(a, b);
+    const int k = kq;
+    const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
+    const float* u = a.uniforms + static_cast<size_t>(b) * (k + 2);
+    int n = k;
+    // every position is read (no early exit), so the loads overlap
+    for (int i = 0; i < k; ++i) {
+      const RowPub* pp = a.pubs + 2 * (static_cast<size_t>(b) * k + i);
+      const float px = __ldcg(&pp[0].xprob), qx = __ldcg(&pp[1].xprob);
+      const int bp = __ldcg(&pp[0].rs.bad), bq = __ldcg(&pp[1].rs.bad);
+      const bool xok = x[i] >= 0 && x[i] < V;
+      const bool acc = !bp && !bq && xok && u[i] * qx < px;
+      if (!acc && n == k) n = i;
+    }
+    int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
+    for (int i = 0; i < n; ++i) out[i] = x[i];
+    for (int i = n + 1; i <= k; ++i) out[i] = -1;  // out[n]: the draw kernel
+    a.out_n[b] = n;
+    a.seq_tickets[b] = 0u;  // left zeroed for the next call
   }
 }
 
+// -------------------------------------------------------------- the draw
+// Entries [e0, e1) of a draw: row vector L[e] (index order) when L is given,
+// else vector e itself; warp w takes the w-th of kWarps equal parts.
+struct Part {
+  int beg, end;
+};
+__device__ __forceinline__ Part warp_part(int e0, int e1, int warp) {
+  const long long m = e1 - e0;
+  Part p;
+  p.beg = e0 + static_cast<int>(m * warp / kWarps);
+  p.end = e0 + static_cast<int>(m * (warp + 1) / kWarps);
+  return p;
+}
+
+// Per-warp sums of the draw weights over entries [e0, e1): max(0, p - q)
+// (want_q) into sh.w_s and p into sh.w_sp.  Each lane sums its entries in
+// order, four loads in flight; fixed-order warp sums.  Whole CTA.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
-  using E = Elt<DT>;
-  const int cta = static_cast<int>(blockIdx.x);
-  const int V = a.V;
-  __shared__ Shm sh;
-  extern __shared__ __align__(16) uint32_t dsm[];
-  // dynamic shared memory: lane tags [kWarps][kLaneTags][32] (later the
-  // gathered tags [kWarps][kGather]), histogram [kWindow], gather bitmaps
-  // [kWarps][kBmapWords]
-  uint32_t* ltags = dsm;
-  uint32_t* hist = ltags + kWarps * kLaneTags * 32;
-  uint32_t* bmap = hist + kWindow;
-  const unsigned char* tgt = static_cast<const unsigned char*>(a.target);
-  if (a.mode == MODE_PROBS) {
-    row_body<DT>(a, sh, ltags, hist, bmap, ROLE_PROBS, cta, cta, 0, 0, tgt + static_cast<size_t>(cta) * V * E::kBytes);
-    return;
-  }
-  const int k = a.k;
-  const int npairs = a.B * k;
-  if (cta < 2 * npairs) {  // a draft position: its target row (even) or draft row (odd)
-    const int pair = cta >> 1;
-    const int r = cta & 1;
-    const int b = pair / k, pos = pair % k;
-    const int unit = b * (k + 1) + pos;
-    const unsigned char* row = r == 0 ? tgt + static_cast<size_t>(unit) * V * E::kBytes
-                                      : static_cast<const unsigned char*>(a.draft) +
-                                            static_cast<size_t>(pair) * V * E::kBytes;
-    row_body<DT>(a, sh, ltags, hist, bmap, r, unit, b, pos, pair, row);
-  } else {  // the bonus position of sequence b
-    const int b = cta - 2 * npairs;
-    const int unit = b * (k + 1) + k;
-    row_body<DT>(a, sh, ltags, hist, bmap, ROLE_BONUS, unit, b, k, 0, tgt + static_cast<size_t>(unit) * V * E::kBytes);
-  }
-}
-
-// The last writer of sequence b applies the first-rejection rule and commits.
-__device__ void sample_finalize(const SampleArgs& a, int b) {
-  __threadfence();
-  const int k = a.k;
-  const UnitRec* rec = a.recs + static_cast<size_t>(b) * (k + 1);
-  // every record is read (no early exit), so the loads overlap
-  int n = k, dn = __ldcg(&rec[k].drawn);
-#pragma unroll 4
-  for (int i = 0; i < k; ++i) {
-    const int2 r = __ldcg(reinterpret_cast<const int2*>(rec + i));  // (accept, drawn)
-    if (r.x == 0 && n == k) {
-      n = i;
-      dn = r.y;
+__device__ __noinline__ void range_sums(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
+                                        const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
+                                        const uint32_t* L, int e0, int e1) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Part pt = warp_part(e0, e1, warp);
+  constexpr int kU = 4;
+  float s = 0.f, sp = 0.f;
+  for (int e = pt.beg + lane; e < pt.end; e += 32 * kU) {
+    uint4 xp[kU], xq[kU];
+    int vv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int ee = e + 32 * u;
+      vv[u] = ee < pt.end ? (L ? static_cast<int>(L[ee]) : ee) : -1;
+      if (vv[u] >= 0) {
+        xp[u] = load_vec<DT>(rowp, vv[u], V, ap);
+        xq[u] = want_q ? load_vec<DT>(rowq, vv[u], V, aq) : xp[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (vv[u] >= 0) {
+        float w[8], ps;
+        s += vec_weights<DT>(rp, rq, xp[u], &xq[u], vv[u], V, want_q, w, &ps);
+        sp += ps;
+      }
     }
   }
-  int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
-  for (int i = 0; i < n; ++i) out[i] = a.tokens[static_cast<size_t>(b) * k + i];
-  out[n] = dn;
-  for (int i = n + 1; i <= k; ++i) out[i] = -1;
-  a.out_n[b] = n;
-  // leave the workspace zeroed for the next call, whatever its shape
-  UnitRec* wrec = a.recs + static_cast<size_t>(b) * (k + 1);
-  for (int i = 0; i <= k; ++i) wrec[i] = UnitRec{0, 0, 0.f, 0.f};
-  a.tickets[b] = 0u;
+  s = warp_sum_f32(s);
+  sp = warp_sum_f32(sp);
+  if (lane == 0) {
+    sh.w_s[warp] = s;
+    sh.w_sp[warp] = sp;
+  }
+  __syncthreads();
+}
+
+// The token at cumulative weight tw (relative to e0) over entries [e0, e1),
+// given their per-warp sums in sh (range_sums): the warp holding tw walks its
+// part in index order.  -1 when the range has no weight.  Whole CTA; every
+// thread gets the token.
+template <int DT>
+__device__ __noinline__ int range_walk(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
+                                       const unsigned char* rowq, bool ap, bool aq, int V, bool use_q, DF tw_in,
+                                       const uint32_t* L, int e0, int e1) {
+  using E = Elt<DT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    const float* ws = use_q ? sh.w_s : sh.w_sp;
+    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
+    int wsel = -1, wlast = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const float sw = ws[w];
+      const DF nxt = df_add(run, sw);
+      if (sw > 0.f) { wlast = w; lbase = run; }
+      if (wsel < 0 && sw > 0.f && df_lt(tw_in, nxt)) { wsel = w; base = run; }
+      run = nxt;
+    }
+    if (wsel < 0) { wsel = wlast; base = lbase; }
+    sh.draw_warp = wsel;
+    sh.draw_base = df_float(df_add2(tw_in, df_neg(base)));
+    sh.draw_token = -1;
+  }
+  __syncthreads();
+  if (warp == sh.draw_warp) {
+    const Part pt = warp_part(e0, e1, warp);
+    const float tw = sh.draw_base;
+    const int rounds = (pt.end - pt.beg + 31) / 32;
+    float run = 0.f;
+    int token = -1, last_pos = -1;
+    for (int it = 0; it < rounds && token < 0; ++it) {
+      const int e = pt.beg + it * 32 + lane;
+      const int v = e < pt.end ? (L ? static_cast<int>(L[e]) : e) : -1;
+      float w[8], ps;
+      float ls = 0.f;
+      int lpos = -1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+      if (v >= 0) {
+        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
+        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
+        ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (w[j] > 0.f) lpos = v * E::kPerVec + j;
+      }
+      const float incl = warp_incl_scan(ls);
+      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
+      const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
+      const int lp2 = __shfl_sync(kFull, lpos, lastl);
+      if (lp2 >= 0) last_pos = lp2;
+      if (ball) {
+        const int l = __ffs(ball) - 1;
+        int tok = -1;
+        if (lane == l) {
+          float cum = run + (incl - ls);
+          int lastj = -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (w[j] > 0.f) lastj = v * E::kPerVec + j;
+            cum += w[j];
+            if (tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
+          }
+          if (tok < 0) tok = lastj;
+        }
+        token = __shfl_sync(kFull, tok, l);
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (token < 0) token = last_pos;  // only reachable through rounding
+    if (lane == 0) sh.draw_token = token;
+  }
+  __syncthreads();
+  return sh.draw_token;
+}
+
+// ------------------------------------------------------------ draw kernel
+// After the tail kernel: sequence b's token at its first rejection n, drawn
+// from max(0, p_n - q_n) with u_{k+1} (n < k) or from p_k with u_k (n = k),
+// falling back to p_n when the residual has no mass.  a.chunks CTAs per
+// sequence each sum the weights of one chunk of the draw (the target row's
+// listed vectors, or the whole rows); the last of them picks the chunk
+// holding u * S from the chunk sums in order and walks it.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
+  using E = Elt<DT>;
+  __shared__ Shm sh;
+  const int S = a.chunks;
+  const int b = static_cast<int>(blockIdx.x) / S, s = static_cast<int>(blockIdx.x) % S;
+  const int k = a.k, V = a.V, tid = threadIdx.x;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const int n = min(max(a.out_n[b], 0), k);  // (written by the tail kernel; kept in range regardless)
+  const bool want_q = n < k;
+  const RowPub* const pp = a.pubs + (want_q ? 2 * (static_cast<size_t>(b) * k + n) : 2 * static_cast<size_t>(a.B) * k + b);
+  const RowStat rp = pp[0].rs;
+  const RowStat rq = want_q ? pp[1].rs : rp;
+  const size_t rb = static_cast<size_t>(V) * E::kBytes;
+  const unsigned char* const rowp = static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + n) * rb;
+  const unsigned char* const rowq =
+      want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
+  const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
+  const bool bad = rp.bad || (want_q && rq.bad);
+  const uint32_t nlist = pp[0].nlist;
+  const bool listed = nlist != kPubReread && !rp.all_kept;
+  const uint32_t* const L = listed ? pp[0].list : nullptr;
+  const int N = bad ? 0 : (listed ? static_cast<int>(nlist) : nvec);
+  auto chunk_beg = [&](int cc) { return static_cast<int>(static_cast<long long>(N) * cc / S); };
+
+  range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, L, chunk_beg(s), chunk_beg(s + 1));
+  if (tid == 0) {
+    DF sr{0.f, 0.f}, spp{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      sr = df_add(sr, sh.w_s[w]);
+      spp = df_add(spp, sh.w_sp[w]);
+    }
+    float* cs = a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + s) * 4;
+    cs[0] = sr.hi;
+    cs[1] = sr.lo;
+    cs[2] = spp.hi;
+    cs[3] = spp.lo;
+    __threadfence();
+    sh.second = atomicAdd(a.draw_tickets + b, 1u) == static_cast<uint32_t>(S - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh.second) return;
+
+  // ---------------------- the last chunk of sequence b: pick one, walk it
+  if (tid == 0) {
+    __threadfence();
+    const float* cs = a.csums + static_cast<size_t>(b) * kMaxDrawChunks * 4;
+    DF tr{0.f, 0.f}, tp{0.f, 0.f};
+    for (int cc = 0; cc < S; ++cc) {
+      tr = df_add2(tr, DF{__ldcg(cs + 4 * cc), __ldcg(cs + 4 * cc + 1)});
+      tp = df_add2(tp, DF{__ldcg(cs + 4 * cc + 2), __ldcg(cs + 4 * cc + 3)});
+    }
+    const bool use_q = want_q && tr.hi > 0.f;  // a residual with no mass: draw from p
+    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
+    const DF target = df_mul_f(use_q ? tr : tp, u);
+    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
+    int csel = -1, clast = -1;
+    for (int cc = 0; cc < S; ++cc) {
+      const int o = use_q ? 0 : 2;
+      const DF sc{__ldcg(cs + 4 * cc + o), __ldcg(cs + 4 * cc + o + 1)};
+      const DF nxt = df_add2(run, sc);
+      if (sc.hi > 0.f) { clast = cc; lbase = run; }
+      if (csel < 0 && sc.hi > 0.f && df_lt(target, nxt)) { csel = cc; base = run; }
+      run = nxt;
+    }
+    if (csel < 0) { csel = clast; base = lbase; }
+    sh.draw_chunk = bad ? -1 : csel;
+    sh.draw_useq = use_q ? 1 : 0;
+    sh.draw_target = df_add2(target, df_neg(base));
+  }
+  __syncthreads();
+  const int cs = sh.draw_chunk;
+  int token = -1;
+  if (cs >= 0) {
+    const bool use_q = sh.draw_useq != 0;
+    range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, L, chunk_beg(cs), chunk_beg(cs + 1));
+    token = range_walk<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, sh.draw_target, L, chunk_beg(cs),
+                           chunk_beg(cs + 1));
+  }
+  if (tid == 0) a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
+  // leave the workspace zeroed for the next call, whatever its shape: the
+  // chunk sums, the records of the sequence's rows and the ticket
+  __shared__ uint32_t s_nl[2 * kMaxK + 1];
+  const int nrows = 2 * k + 1;
+  auto row_pub = [&](int r) { return r < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + r
+                                                 : a.pubs + 2 * static_cast<size_t>(a.B) * k + b; };
+  if (tid < nrows) s_nl[tid] = row_pub(tid)->nlist;
+  __syncthreads();
+  if (tid < 4 * S) a.csums[static_cast<size_t>(b) * kMaxDrawChunks * 4 + tid] = 0.f;
+  for (int r = 0; r < nrows; ++r) {
+    const uint32_t nl = s_nl[r];
+    if (nl != kPubReread)
+      for (uint32_t i = tid; i < nl && i < static_cast<uint32_t>(kPubList); i += kThreads) row_pub(r)->list[i] = 0u;
+  }
+  constexpr int kHdrWords = static_cast<int>(offsetof(RowPub, list) / 4);
+  for (int i = tid; i < nrows * kHdrWords; i += kThreads)
+    reinterpret_cast<uint32_t*>(row_pub(i / kHdrWords))[i % kHdrWords] = 0u;
+  if (tid == 0) a.draw_tickets[b] = 0u;
 }
 
 // ------------------------------------------------------------------ launch
 
+size_t stream_smem_bytes(bool filter) { return filter ? kWarps * kLaneTags * 32 * sizeof(uint32_t) : 16; }
 size_t sample_smem_bytes(int dtype, bool filter) {
   (void)dtype;
-  return filter ? (kWarps * kLaneTags * 32 + kWindow + kWarps * kBmapWords) * sizeof(uint32_t) : 16;
+  return filter ? (kRowTags + kWindow + kWarps * kBmapWords) * sizeof(uint32_t) : 16;
 }
 
 template <int DT>
-static int launch_one(const SampleArgs& a, int units, size_t smem, cudaStream_t st) {
-  auto kern = sample_kernel<DT>;
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  kern<<<units, kThreads, smem, st>>>(a);
+static int launch_all(const SampleArgs& a, cudaStream_t st) {
+  const bool filter = a.top_k > 0 || a.top_p < 1.f;
+  const int rows = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
+  const size_t s1 = stream_smem_bytes(filter), s2 = sample_smem_bytes(DT, filter);
+  static_assert(kRowTags * 4 + (kWindow + kWarps * kBmapWords) * 4 <= 48 * 1024, "tail kernel shared memory");
+  stream_kernel<DT><<<rows, kThreads, s1, st>>>(a);
+  tail_kernel<DT><<<rows, kThreads, s2, st>>>(a);
+  if (a.mode == MODE_SAMPLE) draw_kernel<DT><<<a.B * a.chunks, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
-int launch_sample(const SampleArgs& a, int dtype, int units, void* stream) {
-  const bool filter = a.top_k > 0 || a.top_p < 1.f;
-  const size_t smem = sample_smem_bytes(dtype, filter);
+int launch_sample(const SampleArgs& a, int dtype, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == DT_BF16) return launch_one<DT_BF16>(a, units, smem, st);
-  if (dtype == DT_F32) return launch_one<DT_F32>(a, units, smem, st);
+  if (dtype == DT_BF16) return launch_all<DT_BF16>(a, st);
+  if (dtype == DT_F32) return launch_all<DT_F32>(a, st);
   return cudaErrorInvalidValue;
 }
 

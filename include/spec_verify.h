@@ -207,18 +207,18 @@ int spec_get_status(void* workspace, uint32_t* status, void* cuda_stream);
  * Limits: B <= SPEC_NOALLOC_MAX_B and B*(k+1) <= SPEC_NOALLOC_MAX_UNITS;
  * larger shapes return SPEC_ERR_SCRATCH_LIMIT before anything is launched.
  *
- * Scratch: a fixed array of about 4.2 MiB in the library's device memory, held on
+ * Scratch: a fixed array of about 18 MiB in the library's device memory, held on
  * every GPU that loads the library until the process exits.  The first call
  * on a device (with that device current) looks up the array's device
  * address; make that first call before any stream capture.  Every call
  * clears the part of the array it uses (cudaMemsetAsync on cuda_stream),
- * then launches the kernel; no call allocates or frees memory.  All calls
+ * then launches the kernels; no call allocates or frees memory.  All calls
  * on one device share the one array: two calls whose work overlaps on the
  * GPU (different streams, no ordering between them) race and give wrong
  * results.  Calls on one stream are ordered and safe.
  */
-#define SPEC_NOALLOC_MAX_B 1024
-#define SPEC_NOALLOC_MAX_UNITS 1024
+#define SPEC_NOALLOC_MAX_B 256
+#define SPEC_NOALLOC_MAX_UNITS 256
 int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
                                const int32_t* draft_tokens, const float* uniforms, int B,
                                int k, int V, spec_dtype dtype,
