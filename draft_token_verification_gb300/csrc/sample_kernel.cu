@@ -876,8 +876,9 @@ __device__ __noinline__ int tie_cut_of(Shm& sh, const GList& L, uint32_t len, co
 
 // The filtered, normalised probabilities of a row, written out.
 template <int DT>
-__device__ __noinline__ void write_probs(const unsigned char* row, int V, bool aligned, const RowStat& rp,
+__device__ __noinline__ void write_probs(const unsigned char* row, int V, bool aligned, const RowStat& rp_in,
                                          float* out) {
+  const RowStat rp = rp_in;
   using E = Elt<DT>;
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
@@ -967,6 +968,306 @@ __device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int cta) {
   }
   return r;
 }
+
+// -------------------------------------------------------------- the draw
+// Entries [e0, e1) of a draw: row vector L[e] (index order, read past L1:
+// written by another CTA of the same kernel) when L is given,
+// else vector e itself; warp w takes the w-th of kWarps equal parts.
+struct Part {
+  int beg, end;
+};
+__device__ __forceinline__ Part warp_part(int e0, int e1, int warp) {
+  const long long m = e1 - e0;
+  Part p;
+  p.beg = e0 + static_cast<int>(m * warp / kWarps);
+  p.end = e0 + static_cast<int>(m * (warp + 1) / kWarps);
+  return p;
+}
+
+// Per-warp sums of the draw weights over entries [e0, e1): max(0, p - q)
+// (want_q) into sh.w_s and p into sh.w_sp.  Each lane sums its entries in
+// order, four loads in flight; fixed-order warp sums.  Whole CTA.
+template <int DT>
+__device__ __noinline__ void range_sums(Shm& sh, const RowStat& rp_in, const RowStat& rq_in, const unsigned char* rowp,
+                                        const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
+                                        const uint32_t* L, int e0, int e1) {
+  const RowStat rp = rp_in, rq = rq_in;  // (register copies: no reloads through the references)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Part pt = warp_part(e0, e1, warp);
+  constexpr int kU = 4;
+  float s = 0.f, sp = 0.f;
+  for (int e = pt.beg + lane; e < pt.end; e += 32 * kU) {
+    uint4 xp[kU], xq[kU];
+    int vv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int ee = e + 32 * u;
+      vv[u] = ee < pt.end ? (L ? static_cast<int>(__ldcg(L + ee)) : ee) : -1;
+      if (vv[u] >= 0) {
+        xp[u] = load_vec<DT>(rowp, vv[u], V, ap);
+        xq[u] = want_q ? load_vec<DT>(rowq, vv[u], V, aq) : xp[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (vv[u] >= 0) {
+        float w[8], ps;
+        s += vec_weights<DT>(rp, rq, xp[u], &xq[u], vv[u], V, want_q, w, &ps);
+        sp += ps;
+      }
+    }
+  }
+  s = warp_sum_f32(s);
+  sp = warp_sum_f32(sp);
+  if (lane == 0) {
+    sh.w_s[warp] = s;
+    sh.w_sp[warp] = sp;
+  }
+  __syncthreads();
+}
+
+// The token at cumulative weight tw (relative to e0) over entries [e0, e1),
+// given their per-warp sums in sh (range_sums): the warp holding tw walks its
+// part in index order.  -1 when the range has no weight.  Whole CTA; every
+// thread gets the token.
+template <int DT>
+__device__ __noinline__ int range_walk(Shm& sh, const RowStat& rp_in, const RowStat& rq_in, const unsigned char* rowp,
+                                       const unsigned char* rowq, bool ap, bool aq, int V, bool use_q, DF tw_in,
+                                       const uint32_t* L, int e0, int e1) {
+  const RowStat rp = rp_in, rq = rq_in;  // (register copies: no reloads through the references)
+  using E = Elt<DT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    const float* ws = use_q ? sh.w_s : sh.w_sp;
+    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
+    int wsel = -1, wlast = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const float sw = ws[w];
+      const DF nxt = df_add(run, sw);
+      if (sw > 0.f) { wlast = w; lbase = run; }
+      if (wsel < 0 && sw > 0.f && df_lt(tw_in, nxt)) { wsel = w; base = run; }
+      run = nxt;
+    }
+    if (wsel < 0) { wsel = wlast; base = lbase; }
+    sh.draw_warp = wsel;
+    sh.draw_base = df_float(df_add2(tw_in, df_neg(base)));
+    sh.draw_token = -1;
+  }
+  __syncthreads();
+  if (warp == sh.draw_warp) {
+    const Part pt = warp_part(e0, e1, warp);
+    const float tw = sh.draw_base;
+    const int rounds = (pt.end - pt.beg + 31) / 32;
+    float run = 0.f;
+    int token = -1, last_pos = -1;
+    for (int it = 0; it < rounds && token < 0; ++it) {
+      const int e = pt.beg + it * 32 + lane;
+      const int v = e < pt.end ? (L ? static_cast<int>(__ldcg(L + e)) : e) : -1;
+      float w[8], ps;
+      float ls = 0.f;
+      int lpos = -1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = 0.f;
+      if (v >= 0) {
+        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
+        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
+        ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (w[j] > 0.f) lpos = v * E::kPerVec + j;
+      }
+      const float incl = warp_incl_scan(ls);
+      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
+      const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
+      const int lp2 = __shfl_sync(kFull, lpos, lastl);
+      if (lp2 >= 0) last_pos = lp2;
+      if (ball) {
+        const int l = __ffs(ball) - 1;
+        int tok = -1;
+        if (lane == l) {
+          float cum = run + (incl - ls);
+          int lastj = -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (w[j] > 0.f) lastj = v * E::kPerVec + j;
+            cum += w[j];
+            if (tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
+          }
+          if (tok < 0) tok = lastj;
+        }
+        token = __shfl_sync(kFull, tok, l);
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (token < 0) token = last_pos;  // only reachable through rounding
+    if (lane == 0) sh.draw_token = token;
+  }
+  __syncthreads();
+  return sh.draw_token;
+}
+
+
+// The draw over a target row's listed kept vectors (N <= kPubList entries):
+// every thread reads its entries and their vector pairs at once and keeps
+// each entry's weight sums (max(0, p - q), and p) in shared memory; per-warp
+// sums in the order of range_sums; the warp holding u * S finds the entry
+// from the kept sums and reads only that entry's vectors again to pick the
+// token (as range_walk).  idx: kPubList words, ew: 2 * kPubList floats of
+// shared memory.  Whole CTA; every thread gets the token.
+template <int DT>
+__device__ __noinline__ int draw_listed(Shm& sh, const RowStat& rp_in, const RowStat& rq_in, const unsigned char* rowp,
+                                        const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
+                                        const uint32_t* Lg, int N, float u, uint32_t* idx, float* ew) {
+  const RowStat rp = rp_in, rq = rq_in;  // (register copies: no reloads through the references)
+  using E = Elt<DT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kPer = kPubList / kThreads;  // entries per thread, two pairs of rows' vectors in flight
+#pragma unroll 1
+  for (int jb = 0; jb < kPer && tid + kThreads * jb < N; jb += 2) {
+    int vv[2];
+    uint4 xp[2], xq[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = tid + kThreads * (jb + j);
+      vv[j] = e < N ? static_cast<int>(__ldcg(Lg + e)) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (vv[j] >= 0) {
+        xp[j] = load_vec<DT>(rowp, vv[j], V, ap);
+        xq[j] = want_q ? load_vec<DT>(rowq, vv[j], V, aq) : xp[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (vv[j] >= 0) {
+        const int e = tid + kThreads * (jb + j);
+        float w[8], ps;
+        ew[2 * e] = vec_weights<DT>(rp, rq, xp[j], &xq[j], vv[j], V, want_q, w, &ps);
+        ew[2 * e + 1] = ps;
+        idx[e] = static_cast<uint32_t>(vv[j]);
+      }
+    }
+  }
+  __syncthreads();
+  const Part pt = warp_part(0, N, warp);
+  {
+    float s = 0.f, sp = 0.f;
+    for (int e = pt.beg + lane; e < pt.end; e += 32) {
+      s += ew[2 * e];
+      sp += ew[2 * e + 1];
+    }
+    s = warp_sum_f32(s);
+    sp = warp_sum_f32(sp);
+    if (lane == 0) {
+      sh.w_s[warp] = s;
+      sh.w_sp[warp] = sp;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    DF tr{0.f, 0.f}, tp{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      tr = df_add(tr, sh.w_s[w]);
+      tp = df_add(tp, sh.w_sp[w]);
+    }
+    const bool use_q = want_q && tr.hi > 0.f;  // a residual with no mass: draw from p
+    const DF target = df_mul_f(use_q ? tr : tp, u);
+    const float* ws = use_q ? sh.w_s : sh.w_sp;
+    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
+    int wsel = -1, wlast = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const float sw = ws[w];
+      const DF nxt = df_add(run, sw);
+      if (sw > 0.f) { wlast = w; lbase = run; }
+      if (wsel < 0 && sw > 0.f && df_lt(target, nxt)) { wsel = w; base = run; }
+      run = nxt;
+    }
+    if (wsel < 0) { wsel = wlast; base = lbase; }
+    sh.draw_useq = use_q ? 1 : 0;
+    sh.draw_warp = wsel;
+    sh.draw_base = df_float(df_add2(target, df_neg(base)));
+    sh.draw_token = -1;
+  }
+  __syncthreads();
+  if (warp == sh.draw_warp) {
+    const bool use_q = sh.draw_useq != 0;
+    const float tw = sh.draw_base;
+    const int o = use_q ? 0 : 1;
+    float run = 0.f, cum0 = 0.f;
+    int ecross = -1, elast = -1;
+    for (int e0 = pt.beg; e0 < pt.end && ecross < 0; e0 += 32) {
+      const int e = e0 + lane;
+      const float ls = e < pt.end ? ew[2 * e + o] : 0.f;
+      const float incl = warp_incl_scan(ls);
+      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
+      const unsigned pos = __ballot_sync(kFull, ls > 0.f);
+      if (pos) elast = e0 + 31 - __clz(pos);
+      if (ball) {
+        const int l = __ffs(ball) - 1;
+        ecross = e0 + l;
+        cum0 = __shfl_sync(kFull, run + (incl - ls), l);
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    // the entry holding the target (or, only through rounding, the last
+    // entry with weight): its elements walked in order
+    const int ee = ecross >= 0 ? ecross : elast;
+    if (lane == 0 && ee >= 0) {
+      const int v = static_cast<int>(idx[ee]);
+      const uint4 xp = load_vec<DT>(rowp, v, V, ap);
+      const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
+      float w[8], ps;
+      vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
+      int tok = -1, lastj = -1;
+      float cum = cum0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (w[j] > 0.f) lastj = v * E::kPerVec + j;
+        cum += w[j];
+        if (ecross >= 0 && tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
+      }
+      sh.draw_token = tok >= 0 ? tok : lastj;
+    }
+  }
+  __syncthreads();
+  return sh.draw_token;
+}
+
+// A row's published state, read past L1 (written by another CTA).
+__device__ __forceinline__ RowStat ldcg_rowstat(const RowStat* p) {
+  RowStat r;
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(p);
+  uint32_t* d = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(RowStat) / 4); ++i) d[i] = __ldcg(s + i);
+  return r;
+}
+
+// The records of sequence b's rows (pubs) zeroed for the next call, whatever
+// its shape.  Whole CTA; every read of them is done.
+// nl_pre: the rows' list lengths already in shared memory, or null.
+__device__ __noinline__ void clear_sequence_pubs(const SampleArgs& a, int b, const uint32_t* nl_pre) {
+  __shared__ uint32_t s_nl[2 * kMaxK + 1];
+  const int k = a.k, nrows = 2 * k + 1, tid = threadIdx.x;
+  auto row_pub = [&](int r) { return r < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + r
+                                                 : a.pubs + 2 * static_cast<size_t>(a.B) * k + b; };
+  __syncthreads();
+  if (!nl_pre && tid < nrows) s_nl[tid] = __ldcg(&row_pub(tid)->nlist);
+  __syncthreads();
+  const uint32_t* const nls = nl_pre ? nl_pre : s_nl;
+  for (int r = 0; r < nrows; ++r) {
+    const uint32_t nl = nls[r];
+    if (nl != kPubReread)
+      for (uint32_t i = tid; i < nl && i < static_cast<uint32_t>(kPubList); i += kThreads) row_pub(r)->list[i] = 0u;
+  }
+  constexpr int kHdrWords = static_cast<int>(offsetof(RowPub, list) / 4);
+  for (int i = tid; i < nrows * kHdrWords; i += kThreads)
+    reinterpret_cast<uint32_t*>(row_pub(i / kHdrWords))[i % kHdrWords] = 0u;
+}
+
+constexpr uint32_t kDrawnInTail = 0x80000000u;  // draw ticket flag: the tail kernel drew the token
 
 // ---------------------------------------------------------- stream kernel
 // One CTA per row: stream it once (lattice masses, maximum, candidate tags),
@@ -1216,9 +1517,19 @@ __global__ void __launch_bounds__(kThreads, 5) tail_kernel(const SampleArgs a) {
   // gathered vectors cached after the first kVecCacheAt words of the warp's region
   uint4* const vc = reinterpret_cast<uint4*>(wg + kVecCacheAt);
 
+  // The header and the first tags are read together (the tag area beyond a
+  // warp's count holds zeros), so one memory round trip covers most rows.
   const RowHdr* const hp = a.hdrs + cta;
+  uint32_t* const src = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
+  constexpr int kSpec = 8;  // tags per lane read ahead of the count
+  uint32_t t8[kSpec];
+  if (use_lists) {
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) t8[u] = src[32 * u + lane];
+  }
   const bool bad = hp->bad != 0;
-  const uint32_t ntag = use_lists && !bad ? hp->ntags[warp] : 0u;
+  const uint32_t ntag_raw = hp->ntags[warp];
+  const uint32_t ntag = use_lists && !bad ? ntag_raw : 0u;
   if (tid == 0) {
     RowG g;
     g.m = hp->m;
@@ -1235,19 +1546,26 @@ __global__ void __launch_bounds__(kThreads, 5) tail_kernel(const SampleArgs a) {
   if (filt)
     for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
   {  // (the handed-over tags and header are left zeroed for the next call)
-    uint32_t* src = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
-    for (uint32_t i0 = 0; i0 < ntag; i0 += 32 * 8) {  // eight loads in flight per lane
-      uint32_t t8[8];
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) {
+      const uint32_t i = 32 * u + lane;
+      if (i < ntag) {
+        wg[i] = t8[u];
+        src[i] = 0u;
+      }
+    }
+    for (uint32_t i0 = 32 * kSpec; i0 < ntag; i0 += 32 * 8) {  // the rest, eight loads in flight per lane
+      uint32_t r8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint32_t i = i0 + 32 * u + lane;
-        t8[u] = i < ntag ? src[i] : 0u;
+        r8[u] = i < ntag ? src[i] : 0u;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint32_t i = i0 + 32 * u + lane;
         if (i < ntag) {
-          wg[i] = t8[u];
+          wg[i] = r8[u];
           src[i] = 0u;
         }
       }
@@ -1426,170 +1744,78 @@ __global__ void __launch_bounds__(kThreads, 5) tail_kernel(const SampleArgs a) {
   if (!sh.second) return;
 
   // ------------- the last row of sequence b: the first-rejection rule
-  if (tid == 0) {
-    __threadfence();
+  // (every position tested by its own thread, so the reads overlap)
+  __threadfence();
+  {
     const int k = kq;
     const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
-    const float* u = a.uniforms + static_cast<size_t>(b) * (k + 2);
-    int n = k;
-    // every position is read (no early exit), so the loads overlap
-    for (int i = 0; i < k; ++i) {
-      const RowPub* pp = a.pubs + 2 * (static_cast<size_t>(b) * k + i);
+    int rej = k;  // this thread's position if it is rejected
+    if (tid < k) {
+      const RowPub* pp = a.pubs + 2 * (static_cast<size_t>(b) * k + tid);
       const float px = __ldcg(&pp[0].xprob), qx = __ldcg(&pp[1].xprob);
       const int bp = __ldcg(&pp[0].rs.bad), bq = __ldcg(&pp[1].rs.bad);
-      const bool xok = x[i] >= 0 && x[i] < V;
-      const bool acc = !bp && !bq && xok && u[i] * qx < px;
-      if (!acc && n == k) n = i;
+      const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + tid];
+      const bool xok = x[tid] >= 0 && x[tid] < V;
+      const bool acc = !bp && !bq && xok && u * qx < px;
+      if (!acc) rej = tid;
     }
+    // k <= 31: the first warp holds every position
+    if (warp == 0) {
+      const unsigned rb = __ballot_sync(kFull, rej < k);
+      if (lane == 0) sh.draw_chunk = rb ? __ffs(rb) - 1 : k;
+    }
+    __syncthreads();
+    const int n = sh.draw_chunk;
     int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
-    for (int i = 0; i < n; ++i) out[i] = x[i];
-    for (int i = n + 1; i <= k; ++i) out[i] = -1;  // out[n]: the draw kernel
-    a.out_n[b] = n;
-    a.seq_tickets[b] = 0u;  // left zeroed for the next call
+    if (tid < n) out[tid] = x[tid];
+    else if (tid > n && tid <= k) out[tid] = -1;  // out[n]: drawn below, or by the draw kernel
+    if (tid == 0) {
+      a.out_n[b] = n;
+      a.seq_tickets[b] = 0u;  // left zeroed for the next call
+    }
   }
-}
 
-// -------------------------------------------------------------- the draw
-// Entries [e0, e1) of a draw: row vector L[e] (index order) when L is given,
-// else vector e itself; warp w takes the w-th of kWarps equal parts.
-struct Part {
-  int beg, end;
-};
-__device__ __forceinline__ Part warp_part(int e0, int e1, int warp) {
-  const long long m = e1 - e0;
-  Part p;
-  p.beg = e0 + static_cast<int>(m * warp / kWarps);
-  p.end = e0 + static_cast<int>(m * (warp + 1) / kWarps);
-  return p;
-}
-
-// Per-warp sums of the draw weights over entries [e0, e1): max(0, p - q)
-// (want_q) into sh.w_s and p into sh.w_sp.  Each lane sums its entries in
-// order, four loads in flight; fixed-order warp sums.  Whole CTA.
-template <int DT>
-__device__ __noinline__ void range_sums(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
-                                        const unsigned char* rowq, bool ap, bool aq, int V, bool want_q,
-                                        const uint32_t* L, int e0, int e1) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const Part pt = warp_part(e0, e1, warp);
-  constexpr int kU = 4;
-  float s = 0.f, sp = 0.f;
-  for (int e = pt.beg + lane; e < pt.end; e += 32 * kU) {
-    uint4 xp[kU], xq[kU];
-    int vv[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int ee = e + 32 * u;
-      vv[u] = ee < pt.end ? (L ? static_cast<int>(L[ee]) : ee) : -1;
-      if (vv[u] >= 0) {
-        xp[u] = load_vec<DT>(rowp, vv[u], V, ap);
-        xq[u] = want_q ? load_vec<DT>(rowq, vv[u], V, aq) : xp[u];
-      }
+  // ------- the draw at n, here when the target row's kept vectors are listed
+  {
+    const int k = kq, n = sh.draw_chunk;
+    const bool want_q = n < k;
+    const RowPub* const pp = want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
+    const RowStat rp = ldcg_rowstat(&pp[0].rs);
+    const RowStat rq = want_q ? ldcg_rowstat(&pp[1].rs) : rp;
+    const uint32_t nlist = __ldcg(&pp[0].nlist);
+    const bool listed = !rp.bad && !(want_q && rq.bad) && nlist != kPubReread && !rp.all_kept;
+    if (!listed) return;  // the draw kernel draws over the whole rows
+    const size_t rb = static_cast<size_t>(V) * E::kBytes;
+    const unsigned char* const rowp =
+        static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + n) * rb;
+    const unsigned char* const rowq =
+        want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
+    const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
+    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
+    uint32_t* const idx = ltags;  // (the tags region is free now)
+    float* const ew = reinterpret_cast<float*>(ltags + kPubList);
+    uint32_t* const nls = ltags + 3 * kPubList;
+    if (tid < 2 * k + 1)
+      nls[tid] = __ldcg(&(tid < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + tid
+                                        : a.pubs + 2 * static_cast<size_t>(a.B) * k + b)->nlist);
+    const int token = draw_listed<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, pp[0].list, static_cast<int>(nlist), u,
+                                      idx, ew);
+    if (tid == 0) {
+      a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
+      a.draw_tickets[b] = kDrawnInTail;
     }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (vv[u] >= 0) {
-        float w[8], ps;
-        s += vec_weights<DT>(rp, rq, xp[u], &xq[u], vv[u], V, want_q, w, &ps);
-        sp += ps;
-      }
-    }
+    clear_sequence_pubs(a, b, nls);
   }
-  s = warp_sum_f32(s);
-  sp = warp_sum_f32(sp);
-  if (lane == 0) {
-    sh.w_s[warp] = s;
-    sh.w_sp[warp] = sp;
-  }
-  __syncthreads();
-}
-
-// The token at cumulative weight tw (relative to e0) over entries [e0, e1),
-// given their per-warp sums in sh (range_sums): the warp holding tw walks its
-// part in index order.  -1 when the range has no weight.  Whole CTA; every
-// thread gets the token.
-template <int DT>
-__device__ __noinline__ int range_walk(Shm& sh, const RowStat& rp, const RowStat& rq, const unsigned char* rowp,
-                                       const unsigned char* rowq, bool ap, bool aq, int V, bool use_q, DF tw_in,
-                                       const uint32_t* L, int e0, int e1) {
-  using E = Elt<DT>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    const float* ws = use_q ? sh.w_s : sh.w_sp;
-    DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
-    int wsel = -1, wlast = -1;
-    for (int w = 0; w < kWarps; ++w) {
-      const float sw = ws[w];
-      const DF nxt = df_add(run, sw);
-      if (sw > 0.f) { wlast = w; lbase = run; }
-      if (wsel < 0 && sw > 0.f && df_lt(tw_in, nxt)) { wsel = w; base = run; }
-      run = nxt;
-    }
-    if (wsel < 0) { wsel = wlast; base = lbase; }
-    sh.draw_warp = wsel;
-    sh.draw_base = df_float(df_add2(tw_in, df_neg(base)));
-    sh.draw_token = -1;
-  }
-  __syncthreads();
-  if (warp == sh.draw_warp) {
-    const Part pt = warp_part(e0, e1, warp);
-    const float tw = sh.draw_base;
-    const int rounds = (pt.end - pt.beg + 31) / 32;
-    float run = 0.f;
-    int token = -1, last_pos = -1;
-    for (int it = 0; it < rounds && token < 0; ++it) {
-      const int e = pt.beg + it * 32 + lane;
-      const int v = e < pt.end ? (L ? static_cast<int>(L[e]) : e) : -1;
-      float w[8], ps;
-      float ls = 0.f;
-      int lpos = -1;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = 0.f;
-      if (v >= 0) {
-        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
-        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
-        ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (w[j] > 0.f) lpos = v * E::kPerVec + j;
-      }
-      const float incl = warp_incl_scan(ls);
-      const unsigned ball = __ballot_sync(kFull, ls > 0.f && run + incl > tw);
-      const int lastl = 31 - __clz(__ballot_sync(kFull, lpos >= 0) | 1u);
-      const int lp2 = __shfl_sync(kFull, lpos, lastl);
-      if (lp2 >= 0) last_pos = lp2;
-      if (ball) {
-        const int l = __ffs(ball) - 1;
-        int tok = -1;
-        if (lane == l) {
-          float cum = run + (incl - ls);
-          int lastj = -1;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (w[j] > 0.f) lastj = v * E::kPerVec + j;
-            cum += w[j];
-            if (tok < 0 && w[j] > 0.f && cum > tw) tok = v * E::kPerVec + j;
-          }
-          if (tok < 0) tok = lastj;
-        }
-        token = __shfl_sync(kFull, tok, l);
-      }
-      run += __shfl_sync(kFull, incl, 31);
-    }
-    if (token < 0) token = last_pos;  // only reachable through rounding
-    if (lane == 0) sh.draw_token = token;
-  }
-  __syncthreads();
-  return sh.draw_token;
 }
 
 // ------------------------------------------------------------ draw kernel
-// After the tail kernel: sequence b's token at its first rejection n, drawn
-// from max(0, p_n - q_n) with u_{k+1} (n < k) or from p_k with u_k (n = k),
-// falling back to p_n when the residual has no mass.  a.chunks CTAs per
-// sequence each sum the weights of one chunk of the draw (the target row's
-// listed vectors, or the whole rows); the last of them picks the chunk
-// holding u * S from the chunk sums in order and walks it.
+// After the tail kernel: sequence b's token at its first rejection n when the
+// tail kernel could not draw it from listed vectors (no filter, a row the
+// candidates did not decide, a non-finite row): drawn from max(0, p_n - q_n)
+// with u_{k+1} (n < k) or from p_k with u_k (n = k), falling back to p_n
+// when the residual has no mass.  a.chunks CTAs each sum one chunk of the
+// whole rows; the last of them picks the chunk holding u * S from the chunk
+// sums in order and walks it.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   using E = Elt<DT>;
@@ -1597,10 +1823,17 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   const int S = a.chunks;
   const int b = static_cast<int>(blockIdx.x) / S, s = static_cast<int>(blockIdx.x) % S;
   const int k = a.k, V = a.V, tid = threadIdx.x;
+  if (__ldcg(a.draw_tickets + b) & kDrawnInTail) {  // drawn in the tail kernel: the last CTA resets the flag
+    if (tid == 0) {
+      const uint32_t old = atomicAdd(a.draw_tickets + b, 1u);
+      if ((old & ~kDrawnInTail) == static_cast<uint32_t>(S - 1)) a.draw_tickets[b] = 0u;
+    }
+    return;
+  }
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
   const int n = min(max(a.out_n[b], 0), k);  // (written by the tail kernel; kept in range regardless)
   const bool want_q = n < k;
-  const RowPub* const pp = a.pubs + (want_q ? 2 * (static_cast<size_t>(b) * k + n) : 2 * static_cast<size_t>(a.B) * k + b);
+  const RowPub* const pp = want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
   const RowStat rp = pp[0].rs;
   const RowStat rq = want_q ? pp[1].rs : rp;
   const size_t rb = static_cast<size_t>(V) * E::kBytes;
@@ -1609,13 +1842,11 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
       want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
   const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
   const bool bad = rp.bad || (want_q && rq.bad);
-  const uint32_t nlist = pp[0].nlist;
-  const bool listed = nlist != kPubReread && !rp.all_kept;
-  const uint32_t* const L = listed ? pp[0].list : nullptr;
-  const int N = bad ? 0 : (listed ? static_cast<int>(nlist) : nvec);
+  const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
+  const int N = bad ? 0 : nvec;
   auto chunk_beg = [&](int cc) { return static_cast<int>(static_cast<long long>(N) * cc / S); };
 
-  range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, L, chunk_beg(s), chunk_beg(s + 1));
+  range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, nullptr, chunk_beg(s), chunk_beg(s + 1));
   if (tid == 0) {
     DF sr{0.f, 0.f}, spp{0.f, 0.f};
 #pragma unroll
@@ -1634,23 +1865,25 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   __syncthreads();
   if (!sh.second) return;
 
-  // ---------------------- the last chunk of sequence b: pick one, walk it
+  // ------------------------ the last chunk of sequence b: pick one, walk it
+  __shared__ float s_cs[kMaxDrawChunks * 4];
+  __threadfence();
+  if (tid < 4 * S) s_cs[tid] = __ldcg(a.csums + static_cast<size_t>(b) * kMaxDrawChunks * 4 + tid);
+  __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const float* cs = a.csums + static_cast<size_t>(b) * kMaxDrawChunks * 4;
+    const float* cs = s_cs;
     DF tr{0.f, 0.f}, tp{0.f, 0.f};
     for (int cc = 0; cc < S; ++cc) {
-      tr = df_add2(tr, DF{__ldcg(cs + 4 * cc), __ldcg(cs + 4 * cc + 1)});
-      tp = df_add2(tp, DF{__ldcg(cs + 4 * cc + 2), __ldcg(cs + 4 * cc + 3)});
+      tr = df_add2(tr, DF{cs[4 * cc], cs[4 * cc + 1]});
+      tp = df_add2(tp, DF{cs[4 * cc + 2], cs[4 * cc + 3]});
     }
     const bool use_q = want_q && tr.hi > 0.f;  // a residual with no mass: draw from p
-    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
     const DF target = df_mul_f(use_q ? tr : tp, u);
     DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
     int csel = -1, clast = -1;
+    const int o = use_q ? 0 : 2;
     for (int cc = 0; cc < S; ++cc) {
-      const int o = use_q ? 0 : 2;
-      const DF sc{__ldcg(cs + 4 * cc + o), __ldcg(cs + 4 * cc + o + 1)};
+      const DF sc{cs[4 * cc + o], cs[4 * cc + o + 1]};
       const DF nxt = df_add2(run, sc);
       if (sc.hi > 0.f) { clast = cc; lbase = run; }
       if (csel < 0 && sc.hi > 0.f && df_lt(target, nxt)) { csel = cc; base = run; }
@@ -1666,29 +1899,16 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   int token = -1;
   if (cs >= 0) {
     const bool use_q = sh.draw_useq != 0;
-    range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, L, chunk_beg(cs), chunk_beg(cs + 1));
-    token = range_walk<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, sh.draw_target, L, chunk_beg(cs),
+    // (this CTA's own chunk keeps its per-warp sums from the pass above)
+    if (cs != s) range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, nullptr, chunk_beg(cs), chunk_beg(cs + 1));
+    token = range_walk<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, sh.draw_target, nullptr, chunk_beg(cs),
                            chunk_beg(cs + 1));
   }
   if (tid == 0) a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
-  // leave the workspace zeroed for the next call, whatever its shape: the
-  // chunk sums, the records of the sequence's rows and the ticket
-  __shared__ uint32_t s_nl[2 * kMaxK + 1];
-  const int nrows = 2 * k + 1;
-  auto row_pub = [&](int r) { return r < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + r
-                                                 : a.pubs + 2 * static_cast<size_t>(a.B) * k + b; };
-  if (tid < nrows) s_nl[tid] = row_pub(tid)->nlist;
-  __syncthreads();
+  // leave the workspace zeroed for the next call, whatever its shape
   if (tid < 4 * S) a.csums[static_cast<size_t>(b) * kMaxDrawChunks * 4 + tid] = 0.f;
-  for (int r = 0; r < nrows; ++r) {
-    const uint32_t nl = s_nl[r];
-    if (nl != kPubReread)
-      for (uint32_t i = tid; i < nl && i < static_cast<uint32_t>(kPubList); i += kThreads) row_pub(r)->list[i] = 0u;
-  }
-  constexpr int kHdrWords = static_cast<int>(offsetof(RowPub, list) / 4);
-  for (int i = tid; i < nrows * kHdrWords; i += kThreads)
-    reinterpret_cast<uint32_t*>(row_pub(i / kHdrWords))[i % kHdrWords] = 0u;
   if (tid == 0) a.draw_tickets[b] = 0u;
+  clear_sequence_pubs(a, b, nullptr);
 }
 
 // ------------------------------------------------------------------ launch
