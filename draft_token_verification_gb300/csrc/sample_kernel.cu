@@ -552,158 +552,140 @@ struct GList {
 };
 
 
-// The cut of each active row from a histogram of exact keys (slot
-// key & (kWindow - 1), keys g.klo .. g.kmax): four warps per row scan groups
-// of four keys from the top with double-float prefix sums.  Top-k: where the
-// running count reaches top_k (sh.cutk); top-p (on the top-k set, if any):
-// where the running mass reaches top_p * Z, a token being kept while the
-// mass ranked before it is below the target (sh.cut).  Rows whose cut lies
-// below the window keep found = 0.  The count and mass of the tokens above
-// the window (g.c0, g.m0) start the running sums.  With given_k the top-k
-// cut in sh.cutk is taken as found earlier and only top-p is scanned.
-// Whole CTA.
+// The cut of the row from a histogram of exact keys (slot key & (kWindow -
+// 1), keys g.klo .. g.kmax), scanned by one warp from the top: lane l holds
+// the 16 keys below 4 * (kmax >> 2) + 3 - 16 l, their counts and lattice
+// masses summed, then one warp-wide prefix (count, double-float mass).
+// Top-k: where the running count reaches top_k (sh.cutk); top-p (on the
+// top-k set, if any): where the running mass reaches top_p * Z, a token being
+// kept while the mass ranked before it is below the target (sh.cut).  The
+// lane holding a crossing walks its 16 keys.  A cut below the window leaves
+// found = 0.  The count and mass above the window (g.c0, g.m0) start the
+// running sums; the window's own totals are left in sh.s_C[0][0], sh.s_M[0][0].
+// With given_k the top-k cut in sh.cutk is taken as found earlier and only
+// top-p is scanned.  Whole CTA (one barrier).
 template <int DT, int NR>
 __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, int top_k, float top_p,
                                       bool given_k = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
-  const int r_s = (NR == 2) ? (warp >> 2) : 0;
-  const int wq = warp & (kScanWarps - 1);
-  const RowG g = sh.g[r_s];
-  const bool scanner = ((NR == 2) || warp < kScanWarps) && g.active;
-  if (threadIdx.x < 2) {
-    sh.cut[threadIdx.x].found = 0;
-    if (!given_k) sh.cutk[threadIdx.x].found = 0;
-  }
-  uint32_t cnt[4] = {0u, 0u, 0u, 0u}, top = 0u, Cl = 0u, Cex = 0u;
-  float ms[4] = {0.f, 0.f, 0.f, 0.f}, Ml = 0.f;
-  DF Mex{0.f, 0.f};
-  bool valid = false;
-  if (scanner) {
+  if (warp == 0) {
+    const RowG g = sh.g[0];
+    CutOut ck = sh.cutk[0];
+    if (!given_k) ck.found = 0;
+    __syncwarp();
+    if (lane == 0) {
+      sh.cut[0].found = 0;
+      if (!given_k) sh.cutk[0].found = 0;
+    }
+    __syncwarp();
     const uint32_t gtop = g.kmax >> 2;
-    const uint32_t gi = static_cast<uint32_t>(wq * 32 + lane);
-    if (gi <= gtop) {
-      const uint32_t grp = gtop - gi;
-      top = 4u * grp + 3u;
-      if (top >= g.klo) {
-        valid = true;
-        const uint4 h4 = lds128(smem_addr(hist + r_s * kWindow + 4u * (grp & static_cast<uint32_t>(kGroups - 1))));
-        const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // keys top, top-1, top-2, top-3
+    const uint32_t span = 4u * gtop + 3u;  // keys 0 .. span; lane l takes span - 16 l down to span - 16 l - 15
+    const uint32_t top = span - 16u * static_cast<uint32_t>(lane);
+    const bool live = g.active && span >= 16u * static_cast<uint32_t>(lane);
+    auto count_at = [&](int j) -> uint32_t {
+      if (!live || 16u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(j) > span) return 0u;
+      const uint32_t key = top - static_cast<uint32_t>(j);
+      return (key > g.kmax || key < g.klo) ? 0u : hist[key & kSlotMask];
+    };
+    uint32_t Cl = 0u;
+    float Ml = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t n = count_at(j);
+      Cl += n;
+      if (n) Ml += static_cast<float>(n) * lat_mass(value_of_key<DT>(top - static_cast<uint32_t>(j)), c, g.K);
+    }
+    const uint32_t Craw = warp_incl_scan_u32(Cl);
+    const DF Mraw = warp_incl_scan_df(DF{Ml, 0.f});
+    const uint32_t Cin = Craw + g.c0, Cex = Cin - Cl;
+    const DF Min = df_add2(g.m0, Mraw);
+    DF Mex = df_shfl_up(Min, 1);
+    if (lane == 0) Mex = g.m0;
+    if (lane == 31) {  // the window's own totals
+      sh.s_C[0][0] = Craw;
+      sh.s_M[0][0] = Mraw;
+    }
+    if (lane > 0 && lane < kScanWarps) {
+      sh.s_C[0][lane] = 0u;
+      sh.s_M[0][lane] = DF{0.f, 0.f};
+    }
+    if (topk_on && !given_k) {  // the value where the running count reaches top_k
+      const uint32_t Kc = static_cast<uint32_t>(top_k);
+      const unsigned bal = __ballot_sync(kFull, live && Cin >= Kc && Cex < Kc);
+      if (bal && lane == __ffs(bal) - 1) {
+        uint32_t run = Cex;
+        DF mb = Mex;
+        for (int j = 0; j < 16 && !ck.found; ++j) {
+          const uint32_t n = count_at(j);
+          if (!n) continue;
           const uint32_t key = top - static_cast<uint32_t>(j);
-          const uint32_t s = (key > g.kmax || key < g.klo) ? 0u : hv[j];
-          cnt[j] = s;
-          ms[j] = s ? lat_mass(value_of_key<DT>(key), c, g.K) : 0.f;
-          Cl += s;
-          Ml += static_cast<float>(s) * ms[j];
-        }
-      }
-    }
-    const uint32_t Cin = warp_incl_scan_u32(Cl);
-    const DF Min = warp_incl_scan_df(DF{Ml, 0.f});
-    Cex = Cin - Cl;
-    Mex = df_shfl_up(Min, 1);
-    if (lane == 0) Mex = DF{0.f, 0.f};
-    if (lane == 31) {
-      sh.s_C[r_s][wq] = Cin;
-      sh.s_M[r_s][wq] = Min;
-    }
-  }
-  __syncthreads();
-  uint32_t offC = g.c0;
-  DF offM = g.m0, nxtM = g.m0, totM = g.m0;
-  if (scanner) {
-#pragma unroll
-    for (int q = 0; q < kScanWarps; ++q) {
-      const uint32_t cq = sh.s_C[r_s][q];
-      const DF mq = sh.s_M[r_s][q];
-      if (q < wq) { offC += cq; offM = df_add2(offM, mq); }
-      if (q <= wq) nxtM = df_add2(nxtM, mq);
-      totM = df_add2(totM, mq);
-    }
-  }
-  if (topk_on && !given_k && scanner) {  // the value where the running count reaches top_k
-    const uint32_t Kc = static_cast<uint32_t>(top_k);
-    const uint32_t wC = sh.s_C[r_s][wq];
-    if (offC < Kc && offC + wC >= Kc) {
-      const uint32_t cb = offC + Cex;
-      const unsigned ball = __ballot_sync(kFull, valid && cb < Kc);
-      const int l = 31 - __clz(ball | 1u);
-      if (lane == l && valid && cb < Kc) {
-        uint32_t run = cb;
-        DF mb = df_add2(offM, Mex);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (run < Kc && run + cnt[j] >= Kc) {
-            CutOut co;
-            co.kstar = top - static_cast<uint32_t>(j);
-            co.keep = Kc - run;
-            co.total = cnt[j];
-            co.found = 1;
-            co.zkept = df_add(mb, static_cast<float>(Kc - run) * ms[j]);
-            sh.cutk[r_s] = co;
-            if (!topp_on) sh.cut[r_s] = co;
+          const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
+          if (run + n >= Kc) {
+            ck.kstar = key;
+            ck.keep = Kc - run;
+            ck.total = n;
+            ck.found = 1;
+            ck.zkept = df_add(mb, static_cast<float>(Kc - run) * ms);
           }
-          run += cnt[j];
-          mb = df_add(mb, static_cast<float>(cnt[j]) * ms[j]);
+          run += n;
+          mb = df_add(mb, static_cast<float>(n) * ms);
         }
+        sh.cutk[0] = ck;
+        if (!topp_on) sh.cut[0] = ck;
       }
+      const int src = bal ? __ffs(bal) - 1 : 0;
+      ck.found = __shfl_sync(kFull, ck.found, src);
+      ck.kstar = __shfl_sync(kFull, ck.kstar, src);
+      ck.keep = __shfl_sync(kFull, ck.keep, src);
+      ck.total = __shfl_sync(kFull, ck.total, src);
+      ck.zkept = DF{__shfl_sync(kFull, ck.zkept.hi, src), __shfl_sync(kFull, ck.zkept.lo, src)};
     }
-  }
-  if (topk_on && topp_on) __syncthreads();
-  if (topp_on && scanner) {
-    const CutOut ck = sh.cutk[r_s];
-    if (!topk_on || ck.found) {
+    if (topp_on && (!topk_on || ck.found)) {
       const DF target = df_mul_f(topk_on ? ck.zkept : g.z, top_p);
-      // (a window holding less than the target leaves the cut unfound)
-      const bool wlast = !df_lt(totM, target) && df_lt(offM, target) &&
-                         (wq == kScanWarps - 1 || !df_lt(nxtM, target));
-      if (wlast) {
-        const DF mbl = df_add2(offM, Mex);
-        const unsigned ball = __ballot_sync(kFull, valid && df_lt(mbl, target));
-        const int l = 31 - __clz(ball | 1u);
-        if (lane == l && valid && df_lt(mbl, target)) {
-          DF mb = mbl, mb_last{0.f, 0.f};
-          int jl = -1;
-          uint32_t cl = 0u;
-          bool done = false;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t key = top - static_cast<uint32_t>(j);
-            uint32_t ce = cnt[j];
-            if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
-            if (!done && ce > 0u) {
-              const DF after = df_add(mb, static_cast<float>(ce) * ms[j]);
-              jl = j;
-              cl = ce;
-              mb_last = mb;
-              if (!df_lt(after, target)) {
-                const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
-                uint32_t keep = static_cast<uint32_t>(ceilf(need / ms[j]));
-                keep = max(1u, min(keep, ce));
-                CutOut co;
-                co.kstar = key;
-                co.keep = keep;
-                co.total = cnt[j];
-                co.found = 1;
-                co.zkept = df_add(mb, static_cast<float>(keep) * ms[j]);
-                sh.cut[r_s] = co;
-                done = true;
-              }
-              mb = after;
-            }
+      // the first lane whose running mass reaches the target (a window
+      // holding less than the target leaves the cut unfound)
+      const unsigned bal = __ballot_sync(kFull, live && !df_lt(Min, target));
+      if (bal && lane == __ffs(bal) - 1 && df_lt(Mex, target)) {
+        CutOut cp;
+        cp.found = 0;
+        DF mb = Mex, mb_last{0.f, 0.f};
+        int jl = -1;
+        uint32_t cl = 0u, tl = 0u;
+        float msl = 0.f;
+        for (int j = 0; j < 16 && !cp.found; ++j) {
+          const uint32_t n = count_at(j);
+          const uint32_t key = top - static_cast<uint32_t>(j);
+          uint32_t ce = n;
+          if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
+          if (!ce) continue;
+          const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
+          const DF after = df_add(mb, static_cast<float>(ce) * ms);
+          jl = j;
+          cl = ce;
+          tl = n;
+          msl = ms;
+          mb_last = mb;
+          if (!df_lt(after, target)) {
+            const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
+            uint32_t keep = static_cast<uint32_t>(ceilf(need / ms));
+            keep = max(1u, min(keep, ce));
+            cp.kstar = key;
+            cp.keep = keep;
+            cp.total = n;
+            cp.found = 1;
+            cp.zkept = df_add(mb, static_cast<float>(keep) * ms);
           }
-          if (!done && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
-            CutOut co;
-            co.kstar = top - static_cast<uint32_t>(jl);
-            co.keep = cl;
-            co.total = cnt[jl];
-            co.found = 1;
-            co.zkept = df_add(mb_last, static_cast<float>(cl) * ms[jl]);
-            sh.cut[r_s] = co;
-          }
+          mb = after;
         }
+        if (!cp.found && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
+          cp.kstar = top - static_cast<uint32_t>(jl);
+          cp.keep = cl;
+          cp.total = tl;
+          cp.found = 1;
+          cp.zkept = df_add(mb_last, static_cast<float>(cl) * msl);
+        }
+        sh.cut[0] = cp;
       }
     }
   }
@@ -1477,7 +1459,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
 // at the draft token and, for target rows, its kept vectors.  The last row
 // of a sequence to finish applies the first-rejection rule.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 5) tail_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
   using E = Elt<DT>;
   using H = Hot<DT>;
   __shared__ Shm sh;
