@@ -1294,23 +1294,29 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
   uint32_t cnt = 0u;        // lane tag list length
   uint32_t lfl = 0u;        // lane floor: the lane list is complete above it
   float lflv = -INFINITY;   // its value
-  float lthr = -INFINITY;   // lane bound: kTheta octaves below mw, at least the lane floor
+  float lthr = -3.0e38f;    // lane bound: kTheta octaves below mw, at least the lane floor
+                            // (finite: the -inf padding past a segment is never tagged)
   int sync_no = 0;
-  const int xv = xtok >= 0 && xtok < V ? xtok / E::kPerVec : -1;
   // every warp runs the same number of iterations (the CTA barriers below)
   const int iters_all = seg_vectors(nvec) / 32;
+  // whole 16-byte vectors: every vector below the segment end is full
+  const bool whole = aligned && (V % E::kPerVec) == 0;
   for (int it = 0; it < iters_all; it += 4) {
     uint4 x[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = sg.beg + (it + u) * 32 + lane;
-      x[u] = v < sg.end ? load_vec<DT>(row, v, V, aligned) : make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
+      x[u] = make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
+      if (v < sg.end) x[u] = whole ? ldg_stream(row + 16 * static_cast<size_t>(v)) : load_vec<DT>(row, v, V, aligned);
     }
+    // the four vectors' maxima: one lattice-exponent check and one bound
+    // update per four vectors
+    float vmx[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = sg.beg + (it + u) * 32 + lane;
-      const float vm = H::vmax(x[u]);
-      const float L = vm * c;
+    for (int u = 0; u < 4; ++u) vmx[u] = H::vmax(x[u]);
+    const float gm = max_nan(max_nan(vmx[0], vmx[1]), max_nan(vmx[2], vmx[3]));
+    {
+      const float L = gm * c;
       if (L > static_cast<float>(kt) && L < 1073741824.f) {  // raise the lattice exponent (rare)
         const int knew = static_cast<int>(ceilf(L));
         const float s = exp2i(kt - knew);
@@ -1318,16 +1324,21 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
         acc1 = mul2(acc1, pkf(s, s));
         kt = knew;
       }
-      const float nk = -static_cast<float>(kt);
-      H::mass_vec(x[u], c2, pkf(nk, nk), acc0, acc1);
-      mt = max_nan(mt, vm);
-      lthr = fmaxf(lthr, vm - dtheta);
-      if (v == xv && xv < sg.end) sh.xbits[0] = E::bits_of(x[u], xtok - xv * E::kPerVec);
+    }
+    const float nk = -static_cast<float>(kt);
+    const u64 nk2 = pkf(nk, nk);
+    mt = max_nan(mt, gm);
+    // lane bound lthr: kTheta octaves below the larger of this lane's running
+    // maximum and the CTA maximum of the last exchange (both at most the row
+    // maximum), never below the lane floor
+    lthr = fmaxf(lthr, gm - dtheta);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = sg.beg + (it + u) * 32 + lane;
+      const float vm = vmx[u];
+      H::mass_vec(x[u], c2, nk2, acc0, acc1);
       if (use_lists) {
-        // lane bound lthr: kTheta octaves below the larger of this lane's
-        // running maximum and the CTA maximum of the last exchange (both at
-        // most the row maximum), never below the lane floor
-        if (v < sg.end && vm >= lthr) {
+        if (vm >= lthr) {
           bool take = true;
           if (cnt == static_cast<uint32_t>(kLaneTags)) {  // full: keep the largest of this lane
             cnt = lane_tags_purge(myl, cnt, E::key(bits_round_down<DT>(lthr)));
@@ -1363,6 +1374,9 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
       }
     }
   }
+
+  // the row's value at the draft token
+  if (tid == 0 && xtok >= 0 && xtok < V) sh.xbits[0] = E::bits_at(row, xtok);
 
   // ------------------------------------------ phase 2: row maximum and sum
   {
