@@ -1332,30 +1332,26 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
     // maximum and the CTA maximum of the last exchange (both at most the row
     // maximum), never below the lane floor
     lthr = fmaxf(lthr, gm - dtheta);
+    if (use_lists && cnt > static_cast<uint32_t>(kLaneTags - 4)) {
+      // (rare) room for this group's four candidates: drop the tags below the
+      // bound, then while still short of room raise the lane's floor above its
+      // smallest tag; the list stays complete above max(bound, floor)
+      cnt = lane_tags_purge(myl, cnt, E::key(bits_round_down<DT>(lthr)));
+      while (cnt > static_cast<uint32_t>(kLaneTags - 4)) {
+        lfl = lane_tags_min_key(myl, cnt) + 1u;
+        lflv = value_of_key<DT>(lfl);
+        cnt = lane_tags_purge(myl, cnt, lfl);
+      }
+      lthr = fmaxf(lthr, lflv);
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = sg.beg + (it + u) * 32 + lane;
-      const float vm = vmx[u];
       H::mass_vec(x[u], c2, nk2, acc0, acc1);
-      if (use_lists) {
-        if (vm >= lthr) {
-          bool take = true;
-          if (cnt == static_cast<uint32_t>(kLaneTags)) {  // full: keep the largest of this lane
-            cnt = lane_tags_purge(myl, cnt, E::key(bits_round_down<DT>(lthr)));
-            while (cnt == static_cast<uint32_t>(kLaneTags)) {
-              lfl = lane_tags_min_key(myl, cnt) + 1u;
-              lflv = value_of_key<DT>(lfl);
-              cnt = lane_tags_purge(myl, cnt, lfl);
-            }
-            lthr = fmaxf(lthr, lflv);
-            take = vm >= lflv;
-          }
-          if (take) {
-            myl[32 * cnt] = (static_cast<uint32_t>(v - sg.beg) << 16) | (__float_as_uint(vm) >> 16);
-            ++cnt;
-          }
-        }
-      }
+      // a candidate: one predicated store, no branch
+      const bool take = use_lists && vmx[u] >= lthr;
+      if (take) myl[32 * cnt] = (static_cast<uint32_t>(v - sg.beg) << 16) | (__float_as_uint(vmx[u]) >> 16);
+      cnt += take ? 1u : 0u;
     }
     const int li = it >> 2;  // loop iteration
     if (use_lists && (li < kSyncEvery ? (li & (li + 1)) == 0 : (li % kSyncEvery) == kSyncEvery - 1)) {
