@@ -391,9 +391,9 @@ def main():
         "clocks": r["clk"],
         "e2e": {"value": pos * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 5 * K,  # sampling: stream, tail and draw kernels; greedy; tree
+        "gpu_launches": 4 * K,  # sampling: fused stream+tail and draw kernels; greedy; tree
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic("sample"), "kernel": "sampling verify: stream_kernel + tail_kernel + draw_kernel<bf16>, timed together",
+                     "traffic": recorded_traffic("sample"), "kernel": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels": {
             "sample": {"us": t_sample * 1e6, "GB/s": achieved, "frac": achieved / peak,

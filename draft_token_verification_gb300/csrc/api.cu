@@ -77,6 +77,8 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.tags = reinterpret_cast<uint32_t*>(w + L.tags);
   a.pubs = reinterpret_cast<RowPub*>(w + L.pubs);
   a.csums = reinterpret_cast<float*>(w + L.csums);
+  a.work = reinterpret_cast<uint32_t*>(w + L.work);
+  a.done = reinterpret_cast<uint32_t*>(w + L.done);
   // the draw at the first rejection: a few chunks over listed vectors, more
   // over whole rows (no filter)
   a.chunks = (a.top_k > 0 || a.top_p < 1.f) ? 8 : kMaxDrawChunks;

@@ -81,6 +81,8 @@ struct WsLayout {
   size_t status;      // uint32 status word (sticky bits)
   size_t s_tickets;   // uint32[B]  rows finished per sequence, tail kernel
   size_t d_tickets;   // uint32[B]  chunks finished per sequence, draw kernel
+  size_t work;        // uint32[2]  fused stream/tail kernel: next work item, CTAs finished
+  size_t done;        // uint32[rows]  fused kernel: a row's stream part is published
   size_t hdrs;        // RowHdr[rows]
   size_t tags;        // uint32[rows][kRowTags]
   size_t pubs;        // RowPub[rows]
@@ -101,7 +103,9 @@ constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   w.status = 0;
   w.s_tickets = 256;
   w.d_tickets = align_up(w.s_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
-  w.hdrs = align_up(w.d_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.work = align_up(w.d_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.done = w.work + 2 * sizeof(uint32_t);
+  w.hdrs = align_up(w.done + sizeof(uint32_t) * rows, 256);
   w.tags = align_up(w.hdrs + sizeof(RowHdr) * rows, 256);
   w.pubs = align_up(w.tags + sizeof(uint32_t) * kRowTags * rows, 256);
   w.csums = align_up(w.pubs + sizeof(RowPub) * rows, 256);
@@ -140,6 +144,8 @@ struct SampleArgs {
   RowPub* pubs;                // [rows]
   float* csums;                // [B][kMaxDrawChunks][4]
   int chunks;                  // draw chunks per sequence (<= kMaxDrawChunks)
+  uint32_t* work;              // [2] fused kernel work counters
+  uint32_t* done;              // [rows] fused kernel row flags
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;

@@ -49,6 +49,8 @@
 #include <math.h>
 #include <stddef.h>
 
+#include <algorithm>
+
 #include "device_common.cuh"
 
 namespace specv {
@@ -1255,13 +1257,10 @@ constexpr uint32_t kDrawnInTail = 0x80000000u;  // draw ticket flag: the tail ke
 // One CTA per row: stream it once (lattice masses, maximum, candidate tags),
 // then hand over the row header and the tags at or above klo.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a) {
+__device__ __forceinline__ void stream_row(const SampleArgs& a, Shm& sh, uint32_t* dsm, const int cta) {
   using E = Elt<DT>;
   using H = Hot<DT>;
-  __shared__ Shm sh;
-  extern __shared__ __align__(16) uint32_t dsm[];
   uint32_t* const ltags = dsm;  // lane tags [kWarps][kLaneTags][32]
-  const int cta = static_cast<int>(blockIdx.x);
   const RowRef rr = row_ref<DT>(a, cta);
   const int role = rr.role, b = rr.b, pos = rr.pos;
   const unsigned char* const row = rr.row;
@@ -1463,24 +1462,31 @@ __global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a)
   }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  stream_row<DT>(a, sh, dsm, static_cast<int>(blockIdx.x));
+}
+
 // ------------------------------------------------------------ tail kernel
 // One CTA per row, after the stream kernel: the kept set of the row from its
 // header and tags (or by re-reading the row), published with its probability
 // at the draft token and, for target rows, its kept vectors.  The last row
 // of a sequence to finish applies the first-rejection rule.
+// timed_out: the row's header never arrived (fused kernel): the row is
+// published as bad without reading it.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
+__device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t* dsm, const int cta,
+                                         const bool timed_out) {
   using E = Elt<DT>;
   using H = Hot<DT>;
-  __shared__ Shm sh;
-  extern __shared__ __align__(16) uint32_t dsm[];
   // dynamic shared memory: tags [kWarps][kTagsPerWarp] (then the gathered
   // tags in their place), histogram [kWindow], gather bitmaps
   // [kWarps][kBmapWords]
   uint32_t* const ltags = dsm;
   uint32_t* const hist = ltags + kRowTags;
   uint32_t* const bmap = hist + kWindow;
-  const int cta = static_cast<int>(blockIdx.x);
   const RowRef rr = row_ref<DT>(a, cta);
   const int role = rr.role, b = rr.b, pos = rr.pos;
   const unsigned char* const row = rr.row;
@@ -1511,29 +1517,29 @@ __global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
 
   // The header and the first tags are read together (the tag area beyond a
   // warp's count holds zeros), so one memory round trip covers most rows.
+  // (read past L1: written by another CTA when the kernels are fused)
   const RowHdr* const hp = a.hdrs + cta;
   uint32_t* const src = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
   constexpr int kSpec = 8;  // tags per lane read ahead of the count
   uint32_t t8[kSpec];
-  if (use_lists) {
+  if (use_lists && !timed_out) {
 #pragma unroll
-    for (int u = 0; u < kSpec; ++u) t8[u] = src[32 * u + lane];
+    for (int u = 0; u < kSpec; ++u) t8[u] = __ldcg(src + 32 * u + lane);
   }
-  const bool bad = hp->bad != 0;
-  const uint32_t ntag_raw = hp->ntags[warp];
-  const uint32_t ntag = use_lists && !bad ? ntag_raw : 0u;
+  const bool bad = timed_out || __ldcg(&hp->bad) != 0;
+  const uint32_t ntag = use_lists && !bad ? __ldcg(&hp->ntags[warp]) : 0u;
   if (tid == 0) {
     RowG g;
-    g.m = hp->m;
-    g.K = hp->K;
-    g.kmax = hp->kmax;
-    g.klo = hp->klo;
-    g.z = DF{hp->zhi, hp->zlo};
+    g.m = timed_out ? 0.f : __ldcg(&hp->m);
+    g.K = timed_out ? 0.f : __ldcg(&hp->K);
+    g.kmax = timed_out ? 0u : __ldcg(&hp->kmax);
+    g.klo = timed_out ? 0u : __ldcg(&hp->klo);
+    g.z = timed_out ? DF{1.f, 0.f} : DF{__ldcg(&hp->zhi), __ldcg(&hp->zlo)};
     g.c0 = 0u;
     g.m0 = DF{0.f, 0.f};
     g.active = use_lists ? 1 : 0;
     sh.g[0] = g;
-    sh.xbits[0] = hp->xbits;
+    sh.xbits[0] = timed_out ? 0u : __ldcg(&hp->xbits);
   }
   if (filt)
     for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
@@ -1551,7 +1557,7 @@ __global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint32_t i = i0 + 32 * u + lane;
-        r8[u] = i < ntag ? src[i] : 0u;
+        r8[u] = i < ntag ? __ldcg(src + i) : 0u;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -1800,6 +1806,83 @@ __global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
   }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  tail_row<DT>(a, sh, dsm, static_cast<int>(blockIdx.x), false);
+}
+
+// ----------------------------------------------------- fused stream + tail
+// One cooperative launch of as many CTAs as fit on the GPU at once, taking
+// work items in order from a counter: the stream part of every row, then the
+// tail part of every row.  A tail item waits for its row's stream item,
+// which a running CTA took earlier and finishes without waiting on anyone;
+// the tails of the first rows thus run beside the streams of the last ones,
+// and no CTA slot idles between the two.  (Interleaving the two kinds
+// earlier measured slower.)  The wait is bounded (about kMaxPolls polls):
+// past it the row is published as bad and SPEC_STATUS_TIMEOUT is set.
+constexpr int kMaxPolls = 1 << 22;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  __shared__ int s_item, s_ok;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  const int R = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
+  const int tid = threadIdx.x;
+  for (;;) {
+    __syncthreads();  // the previous item is done with shared memory
+    if (tid == 0) s_item = static_cast<int>(atomicAdd(a.work, 1u));
+    __syncthreads();
+    const int item = s_item;
+    if (item >= 2 * R) break;
+    // item -> (stream or tail, row)
+    const int kind = item < R ? 0 : 1;
+    const int rowi = item < R ? item : item - R;
+    if (kind == 0) {
+      const int item_row = rowi;
+      stream_row<DT>(a, sh, dsm, item_row);
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        st_release_u32(a.done + item_row, 1u);
+      }
+    } else {
+      const int r = rowi;
+      if (tid == 0) {
+        int ok = 0;
+        for (int i = 0; i < kMaxPolls; ++i) {
+          if (ld_acquire_u32(a.done + r)) {
+            ok = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!ok) set_status(a.status, SPEC_STATUS_TIMEOUT);
+        a.done[r] = 0u;  // left zeroed for the next call
+        s_ok = ok;
+      }
+      __syncthreads();
+      tail_row<DT>(a, sh, dsm, r, s_ok == 0);
+    }
+  }
+  // the last CTA out leaves the counters zeroed for the next call
+  if (tid == 0 && atomicAdd(a.work + 1, 1u) == gridDim.x - 1) {
+    a.work[0] = 0u;
+    a.work[1] = 0u;
+  }
+}
+
 // ------------------------------------------------------------ draw kernel
 // After the tail kernel: sequence b's token at its first rejection n when the
 // tail kernel could not draw it from listed vectors (no filter, a row the
@@ -1917,8 +2000,26 @@ static int launch_all(const SampleArgs& a, cudaStream_t st) {
   const int rows = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
   const size_t s1 = stream_smem_bytes(filter), s2 = sample_smem_bytes(DT, filter);
   static_assert(kRowTags * 4 + (kWindow + kWarps * kBmapWords) * 4 <= 48 * 1024, "tail kernel shared memory");
-  stream_kernel<DT><<<rows, kThreads, s1, st>>>(a);
-  tail_kernel<DT><<<rows, kThreads, s2, st>>>(a);
+  // stream and tail fused in one cooperative launch when the GPU allows it
+  bool fused = false;
+  {
+    const size_t sf = s1 > s2 ? s1 : s2;
+    int per_sm = 0, dev = 0, coop = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<DT>, kThreads, sf) == cudaSuccess &&
+        per_sm > 0) {
+      const int grid = std::min(per_sm * num_sms(), 2 * rows);
+      void* params[] = {const_cast<SampleArgs*>(&a)};
+      fused = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_kernel<DT>), dim3(grid), dim3(kThreads),
+                                          params, sf, st) == cudaSuccess;
+    }
+    if (!fused) (void)cudaGetLastError();  // (clear a refused launch; the two launches below stand in)
+  }
+  if (!fused) {
+    stream_kernel<DT><<<rows, kThreads, s1, st>>>(a);
+    tail_kernel<DT><<<rows, kThreads, s2, st>>>(a);
+  }
   if (a.mode == MODE_SAMPLE) draw_kernel<DT><<<a.B * a.chunks, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
