@@ -51,7 +51,11 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
     "spec_transform_probs", "spec_get_status", "spec_error_string", "spec_expected_tokens",
     "spec_improvement_factor", "spec_break_even_acceptance", "spec_verify_sample_noalloc",
+    "spec_sample_launch_mode",
 )
+SPEC_LAUNCH_SEPARATE = 0
+SPEC_LAUNCH_FUSED = 1
+SPEC_LAUNCH_FUSED_WAIT_TEST = 2
 
 
 class SpecSamplingParams(ctypes.Structure):
@@ -114,8 +118,18 @@ def lib() -> ctypes.CDLL:
             L.spec_improvement_factor.restype = D
             L.spec_break_even_acceptance.argtypes = [I]
             L.spec_break_even_acceptance.restype = D
+            L.spec_sample_launch_mode.argtypes = [I]
+            L.spec_sample_launch_mode.restype = I
             _lib = L
     return _lib
+
+
+def spec_sample_launch_mode(mode: int) -> int:
+    """Set how the sampling entry points launch (SPEC_LAUNCH_*); returns the previous mode."""
+    rc = lib().spec_sample_launch_mode(int(mode))
+    if rc < 0:
+        raise SpecVerifyError(rc, "spec_sample_launch_mode")
+    return rc
 
 
 def error_string(code: int) -> str:

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -13,6 +14,8 @@
 using namespace specv;
 
 namespace {
+
+std::atomic<int> g_launch_mode{SPEC_LAUNCH_FUSED};
 
 bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 size_t elt_bytes(spec_dtype d) { return d == SPEC_BF16 ? 2 : 4; }
@@ -78,6 +81,7 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.pubs = reinterpret_cast<RowPub*>(w + L.pubs);
   a.csums = reinterpret_cast<float*>(w + L.csums);
   a.work = reinterpret_cast<uint32_t*>(w + L.work);
+  a.launch_mode = g_launch_mode.load();
   a.done = reinterpret_cast<uint32_t*>(w + L.done);
   // the draw at the first rejection: a few chunks over listed vectors, more
   // over whole rows (no filter)
@@ -173,6 +177,12 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
                                     st) != cudaSuccess)
     return SPEC_ERR_LAUNCH;
   return SPEC_OK;
+}
+
+int spec_sample_launch_mode(int mode) {
+  if (mode != SPEC_LAUNCH_FUSED && mode != SPEC_LAUNCH_SEPARATE && mode != SPEC_LAUNCH_FUSED_WAIT_TEST)
+    return SPEC_ERR_INVALID_ARG;
+  return g_launch_mode.exchange(mode);
 }
 
 int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype, const spec_sampling_params* params,

@@ -146,6 +146,8 @@ struct SampleArgs {
   int chunks;                  // draw chunks per sequence (<= kMaxDrawChunks)
   uint32_t* work;              // [2] fused kernel work counters
   uint32_t* done;              // [rows] fused kernel row flags
+  int launch_mode;             // SPEC_LAUNCH_*
+  int poll_limit;              // fused kernel: polls before a tail part gives up
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;

@@ -1853,7 +1853,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) 
       const int item_row = rowi;
       stream_row<DT>(a, sh, dsm, item_row);
       __syncthreads();
-      if (tid == 0) {
+      if (tid == 0 && a.launch_mode != SPEC_LAUNCH_FUSED_WAIT_TEST) {
         __threadfence();
         st_release_u32(a.done + item_row, 1u);
       }
@@ -1861,7 +1861,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) 
       const int r = rowi;
       if (tid == 0) {
         int ok = 0;
-        for (int i = 0; i < kMaxPolls; ++i) {
+        for (int i = 0; i < a.poll_limit; ++i) {
           if (ld_acquire_u32(a.done + r)) {
             ok = 1;
             break;
@@ -1995,14 +1995,16 @@ size_t sample_smem_bytes(int dtype, bool filter) {
 }
 
 template <int DT>
-static int launch_all(const SampleArgs& a, cudaStream_t st) {
+static int launch_all(const SampleArgs& args, cudaStream_t st) {
+  SampleArgs a = args;
+  a.poll_limit = a.launch_mode == SPEC_LAUNCH_FUSED_WAIT_TEST ? 64 : kMaxPolls;
   const bool filter = a.top_k > 0 || a.top_p < 1.f;
   const int rows = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
   const size_t s1 = stream_smem_bytes(filter), s2 = sample_smem_bytes(DT, filter);
   static_assert(kRowTags * 4 + (kWindow + kWarps * kBmapWords) * 4 <= 48 * 1024, "tail kernel shared memory");
   // stream and tail fused in one cooperative launch when the GPU allows it
   bool fused = false;
-  {
+  if (a.launch_mode != SPEC_LAUNCH_SEPARATE) {
     const size_t sf = s1 > s2 ? s1 : s2;
     int per_sm = 0, dev = 0, coop = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -2010,7 +2012,7 @@ static int launch_all(const SampleArgs& a, cudaStream_t st) {
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<DT>, kThreads, sf) == cudaSuccess &&
         per_sm > 0) {
       const int grid = std::min(per_sm * num_sms(), 2 * rows);
-      void* params[] = {const_cast<SampleArgs*>(&a)};
+      void* params[] = {&a};
       fused = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_kernel<DT>), dim3(grid), dim3(kThreads),
                                           params, sf, st) == cudaSuccess;
     }

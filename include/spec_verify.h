@@ -67,7 +67,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
                                       or a per-sequence temperature <= 0        */
 #define SPEC_STATUS_BAD_PARENT 4u  /* parents[0] != -1 or parents[j] not in [0, j) */
 #define SPEC_STATUS_DEPTH 8u       /* an agreed tree node deeper than max_depth */
-#define SPEC_STATUS_TIMEOUT 16u    /* reserved: a bounded device wait gave up   */
+#define SPEC_STATUS_TIMEOUT 16u    /* a bounded device wait gave up             */
 
 /* Limits. */
 #define SPEC_MAX_K 31              /* drafts per sequence                       */
@@ -225,6 +225,25 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
                                const spec_sampling_params* params, int32_t* out_tokens,
                                int32_t* out_num_accepted, float* out_p_draft,
                                float* out_q_draft, uint32_t* out_status, void* cuda_stream);
+
+/*
+ * How the sampling entry points launch their stream and tail parts, for the
+ * whole process (a setting, not a request of the pages):
+ *   SPEC_LAUNCH_FUSED     one cooperative launch whose CTAs take every row's
+ *                         stream part, then every row's tail part (the default;
+ *                         the separate launches stand in when the GPU refuses it)
+ *   SPEC_LAUNCH_SEPARATE  a stream launch, then a tail launch
+ *   SPEC_LAUNCH_FUSED_WAIT_TEST  the fused launch with the stream parts'
+ *                         completion flags withheld and a short poll limit:
+ *                         every tail part's bounded wait runs out, every row
+ *                         is published as non-finite and SPEC_STATUS_TIMEOUT
+ *                         is set (exercises the timeout path without a fault)
+ * Returns the previous mode, or SPEC_ERR_INVALID_ARG for an unknown one.
+ */
+#define SPEC_LAUNCH_FUSED 1
+#define SPEC_LAUNCH_SEPARATE 0
+#define SPEC_LAUNCH_FUSED_WAIT_TEST 2
+int spec_sample_launch_mode(int mode);
 
 /* Static description of a return code. */
 const char* spec_error_string(int code);

@@ -223,3 +223,52 @@ def test_boundary_draws_under_budget():
     if c["draws"] == 0:
         pytest.skip("no configuration cases ran")
     assert c["count"] == 0 or c["count"] / c["draws"] < BOUNDARY_BUDGET
+
+
+# The stream and tail parts of sampling run fused in one cooperative launch
+# or as two launches: both give the same results, bit for bit.
+@pytest.mark.parametrize("label", ["C3-topp", "topk-spike", "nofilter", "topk-topp"])
+def test_fused_and_separate_launches_agree(label):
+    sv = lib()
+    if label == "C3-topp":
+        case = W.config3()
+    elif label == "topk-spike":
+        case = W.random_sample_case(8, 4, 50000, seed=21, sigma=1.0, noise=0.5, top_k=50, spike=30.0)
+    elif label == "nofilter":
+        case = W.random_sample_case(16, 6, 32000, seed=22)
+    else:
+        case = W.random_sample_case(16, 5, 32000, seed=23, top_k=40, top_p=0.9)
+    prev = sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_SEPARATE)
+    try:
+        sep = run_sample_gpu(case)
+        sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_FUSED)
+        fus = run_sample_gpu(case)
+    finally:
+        sv.spec_sample_launch_mode(prev)
+    for x, y in zip(sep, fus):
+        assert np.array_equal(x, y)
+
+
+# Failure detection without a fault: with the stream parts' completion flags
+# withheld, every tail part's bounded wait runs out; the call still ends,
+# publishes every row as non-finite and sets SPEC_STATUS_TIMEOUT, and the next
+# call on the same workspace and context is correct.
+def test_fused_wait_runs_out_and_context_stays_usable():
+    sv = lib()
+    case = W.random_sample_case(6, 3, 5000, seed=24, top_p=0.9)
+    ws = sv.Workspace()
+    sv.spec_get_status(ws)
+    good = run_sample_gpu(case, workspace=ws)
+    assert sv.spec_get_status(ws) == 0
+    prev = sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_FUSED_WAIT_TEST)
+    try:
+        tok, n, _, _ = run_sample_gpu(case, workspace=ws)
+    finally:
+        sv.spec_sample_launch_mode(prev)
+    st = sv.spec_get_status(ws)
+    assert st & sv.SPEC_STATUS_TIMEOUT and st & sv.SPEC_STATUS_BAD_ROW
+    assert np.all(n == 0) and np.all(tok == -1)
+    again = run_sample_gpu(case, workspace=ws)
+    assert sv.spec_get_status(ws) == 0
+    for x, y in zip(good, again):
+        assert np.array_equal(x, y)
