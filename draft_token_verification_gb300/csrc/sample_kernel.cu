@@ -8,11 +8,13 @@
 // p_i(x_i); at the first rejection n one token is drawn from
 // max(0, p_n - q_n) with u_{k+1}, else a bonus token from p_k with u_k.
 //
-// How (one GPU, memory-bound).  One CTA owns one row: the target or the
-// draft row of a draft position (b, i), or the target row of the bonus
-// position (b, k); the grid is B (2k + 1) CTAs.  Each streams its row from
-// HBM once, 16-byte non-allocating loads by warp segments in index order.
-// While streaming:
+// How (one GPU, memory-bound).  Every row (the target and draft rows of
+// each draft position (b, i), then the bonus target rows (b, k)) has a stream
+// part and a tail part, run by one CTA each: as work items of one
+// cooperative launch (every stream part, then every tail part; a tail part
+// polls, bounded, for its row's stream part) or as two launches.
+// The stream part reads its row from HBM once, 16-byte non-allocating loads
+// by warp segments in index order:
 //   - masses are taken on a power-of-two lattice: with c = log2(e) / T and
 //     an integer k_t >= max(l) * c held per thread, mass(l) = 2^(l c - k_t)
 //     (one packed f32x2 fma and one ex2 per element).  Raising k_t rescales
@@ -23,27 +25,27 @@
 //     within kTheta octaves of mass of the best maximum it knows (its own
 //     running maximum, or the CTA's, exchanged at fixed stream steps).  A tag
 //     is the vector's index in the warp segment and the bf16 pattern of its
-//     maximum.  A full lane list drops the tags below its current bound and,
-//     if still full, raises the lane's floor above its smallest tag; each
-//     list is complete above max(bound, floor).
-// After the stream the tagged maxima above those bounds give a bound on the
-// cut (vector maxima are tokens of the row, so the mass or count above a
-// value is at least that of the maxima above it).  The tagged vectors at or
-// above the bound are gathered in index order and their elements counted in
-// a histogram of exact values; a four-warp scan gives the cut, its tie count
-// and the kept normaliser.  A row the candidates do not decide re-reads
-// itself in windows of exact values from the maximum down, and past a few
-// windows (flat rows crossing zero, 32-bit keys) by a bitwise search.
-// The two CTAs of a draft position each publish their row's state and
-// probability at x_i, and the target CTA the list of its vectors holding
-// kept tokens; the second of the two to finish (pair ticket, no spin-wait)
-// applies the accept test u_i q_i(x_i) < p_i(x_i) and draws from
-// max(0, p_i - q_i) over the listed vectors (the draft row read at the same
-// indices), or over both whole rows when the list overflowed.  The bonus CTA
-// draws from p_k over its own gathered vectors.  Every position draws (the
-// residual draw is speculative), so no CTA waits on another; the last
-// finisher of a sequence (sequence ticket) applies the first-rejection rule
-// and commits.
+//     maximum.  A lane list short of room drops the tags below its current
+//     bound and, if still short, raises the lane's floor above its smallest
+//     tag; each list is complete above max(bound, floor).
+// It hands over a row header (maximum, lattice exponent, row sum, window
+// bottom) and the tags at or above the window bottom.
+// The tail part bounds the cut from the tagged maxima (vector maxima are
+// tokens of the row, so the mass or count above a value is at least that of
+// the maxima above it), gathers the tagged vectors at or above the bound in
+// index order, counts their elements in a histogram of exact values and
+// scans it for the cut, its tie count and the kept normaliser.  A row the
+// candidates do not decide re-reads itself in windows of exact values from
+// the maximum down, and past a few windows (flat rows crossing zero, 32-bit
+// keys) by a bitwise search.  Each row publishes its state, its probability
+// at the draft token and, for target rows, its vectors holding kept tokens.
+// The last row of a sequence to finish (ticket, no spin-wait) tests
+// u_i q_i(x_i) < p_i(x_i) at every position, takes the first rejection n,
+// commits the accepted prefix and, when row n's kept vectors are listed,
+// draws the token at n from max(0, p_n - q_n) (or from p_k when n = k) over
+// them.  A draw over whole rows (no filter, or a row the candidates did not
+// decide) is left to the draw kernel, which splits the rows into chunks.
+// Only the first rejection is drawn: no residual is computed speculatively.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
