@@ -329,6 +329,7 @@ struct Shm {
   int tie_warp[2];
   uint32_t tie_j[2];
   int tie_cut[2];
+  int lead;                    // the warp that runs one-warp steps for this row
   RowStat rs[2];
   int draw_warp;
   float draw_base;
@@ -573,7 +574,7 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
                                       bool given_k = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
-  if (warp == 0) {
+  if (warp == sh.lead) {
     const RowG g = sh.g[0];
     CutOut ck = sh.cutk[0];
     if (!given_k) ck.found = 0;
@@ -595,10 +596,14 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
     uint32_t Cl = 0u;
     float Ml = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t n = count_at(j);
+    for (int j = 0; j < 16; ++j) {  // (selects, no branches)
+      const uint32_t key = top - static_cast<uint32_t>(j);
+      const bool in = live && 16u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(j) <= span &&
+                      key <= g.kmax && key >= g.klo;
+      const uint32_t n = in ? hist[key & kSlotMask] : 0u;
+      const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
       Cl += n;
-      if (n) Ml += static_cast<float>(n) * lat_mass(value_of_key<DT>(top - static_cast<uint32_t>(j)), c, g.K);
+      Ml += n ? static_cast<float>(n) * ms : 0.f;
     }
     const uint32_t Craw = warp_incl_scan_u32(Cl);
     const DF Mraw = warp_incl_scan_df(DF{Ml, 0.f});
@@ -1542,6 +1547,9 @@ __device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t*
     g.active = use_lists ? 1 : 0;
     sh.g[0] = g;
     sh.xbits[0] = timed_out ? 0u : __ldcg(&hp->xbits);
+    // one-warp steps of co-resident CTAs spread over the SM's schedulers
+    // (warp w issues from scheduler w % 4): a hashed warp per row
+    sh.lead = static_cast<int>((static_cast<uint32_t>(cta) * 2654435761u) >> 29);
   }
   if (filt)
     for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
