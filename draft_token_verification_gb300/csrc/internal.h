@@ -70,8 +70,11 @@ struct RowPub {
   uint32_t list[kPubList];
 };
 
-// Chunks of the draw at the first rejection: one CTA each.
+// Chunks of the draw at the first rejection: one CTA each.  A chunk's record:
+// its residual and p sums (two double-floats), then its per-warp sums
+// (kWarps residual, kWarps p).
 constexpr int kMaxDrawChunks = 16;
+constexpr int kChunkRec = 4 + 2 * kWarps;  // floats
 
 // Workspace layout (byte offsets), identical for every call with the same
 // (B, k).  Tickets are zero between calls; everything else is written before
@@ -86,7 +89,7 @@ struct WsLayout {
   size_t hdrs;        // RowHdr[rows]
   size_t tags;        // uint32[rows][kRowTags]
   size_t pubs;        // RowPub[rows]
-  size_t csums;       // float4[B][kMaxDrawChunks]  per-chunk draw sums
+  size_t csums;       // float[B][kMaxDrawChunks][kChunkRec]  per-chunk draw sums
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
   size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
   size_t total;
@@ -109,7 +112,7 @@ constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   w.tags = align_up(w.hdrs + sizeof(RowHdr) * rows, 256);
   w.pubs = align_up(w.tags + sizeof(uint32_t) * kRowTags * rows, 256);
   w.csums = align_up(w.pubs + sizeof(RowPub) * rows, 256);
-  w.g_slots = align_up(w.csums + 16 * static_cast<size_t>(kMaxDrawChunks) * static_cast<size_t>(B), 256);
+  w.g_slots = align_up(w.csums + sizeof(float) * kChunkRec * static_cast<size_t>(kMaxDrawChunks) * B, 256);
   w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
   w.total = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
   return w;
@@ -142,7 +145,7 @@ struct SampleArgs {
   RowHdr* hdrs;                // [rows]
   uint32_t* tags;              // [rows][kRowTags]
   RowPub* pubs;                // [rows]
-  float* csums;                // [B][kMaxDrawChunks][4]
+  float* csums;                // [B][kMaxDrawChunks][kChunkRec]
   int chunks;                  // draw chunks per sequence (<= kMaxDrawChunks)
   uint32_t* work;              // [2] fused kernel work counters
   uint32_t* done;              // [rows] fused kernel row flags

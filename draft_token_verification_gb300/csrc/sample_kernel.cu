@@ -1051,17 +1051,34 @@ __device__ __noinline__ int range_walk(Shm& sh, const RowStat& rp_in, const RowS
     const int rounds = (pt.end - pt.beg + 31) / 32;
     float run = 0.f;
     int token = -1, last_pos = -1;
-    for (int it = 0; it < rounds && token < 0; ++it) {
-      const int e = pt.beg + it * 32 + lane;
-      const int v = e < pt.end ? (L ? static_cast<int>(__ldcg(L + e)) : e) : -1;
+    constexpr int kR = 2;  // rounds whose vectors are read together
+    for (int it0 = 0; it0 < rounds && token < 0; it0 += kR) {
+    int vr[kR];
+    uint4 xpr[kR], xqr[kR];
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      const int e = pt.beg + (it0 + r) * 32 + lane;
+      vr[r] = (it0 + r < rounds && e < pt.end) ? (L ? static_cast<int>(__ldcg(L + e)) : e) : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      if (vr[r] >= 0) {
+        xpr[r] = load_vec<DT>(rowp, vr[r], V, ap);
+        xqr[r] = use_q ? load_vec<DT>(rowq, vr[r], V, aq) : xpr[r];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      if (it0 + r >= rounds || token >= 0) break;
+      const int v = vr[r];
       float w[8], ps;
       float ls = 0.f;
       int lpos = -1;
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = 0.f;
       if (v >= 0) {
-        const uint4 xp = load_vec<DT>(rowp, v, V, ap);
-        const uint4 xq = use_q ? load_vec<DT>(rowq, v, V, aq) : xp;
+        const uint4 xp = xpr[r];
+        const uint4 xq = xqr[r];
         ls = vec_weights<DT>(rp, rq, xp, &xq, v, V, use_q, w, &ps);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -1089,6 +1106,7 @@ __device__ __noinline__ int range_walk(Shm& sh, const RowStat& rp_in, const RowS
         token = __shfl_sync(kFull, tok, l);
       }
       run += __shfl_sync(kFull, incl, 31);
+    }
     }
     if (token < 0) token = last_pos;  // only reachable through rounding
     if (lane == 0) sh.draw_token = token;
@@ -1939,11 +1957,16 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
       sr = df_add(sr, sh.w_s[w]);
       spp = df_add(spp, sh.w_sp[w]);
     }
-    float* cs = a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + s) * 4;
+    float* cs = a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + s) * kChunkRec;
     cs[0] = sr.hi;
     cs[1] = sr.lo;
     cs[2] = spp.hi;
     cs[3] = spp.lo;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {  // kept for the walk of the chosen chunk
+      cs[4 + w] = sh.w_s[w];
+      cs[4 + kWarps + w] = sh.w_sp[w];
+    }
     __threadfence();
     sh.second = atomicAdd(a.draw_tickets + b, 1u) == static_cast<uint32_t>(S - 1) ? 1 : 0;
   }
@@ -1953,7 +1976,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   // ------------------------ the last chunk of sequence b: pick one, walk it
   __shared__ float s_cs[kMaxDrawChunks * 4];
   __threadfence();
-  if (tid < 4 * S) s_cs[tid] = __ldcg(a.csums + static_cast<size_t>(b) * kMaxDrawChunks * 4 + tid);
+  if (tid < 4 * S) s_cs[tid] = __ldcg(a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + tid / 4) * kChunkRec + tid % 4);
   __syncthreads();
   if (tid == 0) {
     const float* cs = s_cs;
@@ -1984,14 +2007,19 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   int token = -1;
   if (cs >= 0) {
     const bool use_q = sh.draw_useq != 0;
-    // (this CTA's own chunk keeps its per-warp sums from the pass above)
-    if (cs != s) range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, nullptr, chunk_beg(cs), chunk_beg(cs + 1));
+    // the chosen chunk's per-warp sums, as its CTA recorded them
+    if (cs != s && tid < 2 * kWarps) {
+      const float v = __ldcg(a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + cs) * kChunkRec + 4 + tid);
+      if (tid < kWarps) sh.w_s[tid] = v;
+      else sh.w_sp[tid - kWarps] = v;
+    }
+    __syncthreads();
     token = range_walk<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, sh.draw_target, nullptr, chunk_beg(cs),
                            chunk_beg(cs + 1));
   }
   if (tid == 0) a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
   // leave the workspace zeroed for the next call, whatever its shape
-  if (tid < 4 * S) a.csums[static_cast<size_t>(b) * kMaxDrawChunks * 4 + tid] = 0.f;
+  for (int i = tid; i < kChunkRec * S; i += kThreads) a.csums[static_cast<size_t>(b) * kMaxDrawChunks * kChunkRec + i] = 0.f;
   if (tid == 0) a.draw_tickets[b] = 0u;
   clear_sequence_pubs(a, b, nullptr);
 }
