@@ -1920,7 +1920,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) 
 // whole rows; the last of them picks the chunk holding u * S from the chunk
 // sums in order and walks it.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) draw_kernel(const SampleArgs a) {
   using E = Elt<DT>;
   __shared__ Shm sh;
   const int S = a.chunks;
