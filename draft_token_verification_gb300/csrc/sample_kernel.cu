@@ -68,6 +68,10 @@ constexpr int kGather = kLaneTags * 32;             // gathered vectors per warp
 constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
 constexpr float kTheta = 13.f;                      // octaves of mass kept as candidates
 constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
+// Histogram slot of a key (any kWindow consecutive keys take distinct
+// slots): the low bits are mixed with bits 4.. so that the scan's lanes,
+// which read keys 16 apart, fall in distinct shared-memory banks.
+__device__ __forceinline__ uint32_t hslot(uint32_t key) { return (key & kSlotMask) ^ ((key >> 4) & 15u); }
 constexpr int kGroups = kWindow / 4;                // aligned groups of four keys
 constexpr int kScanWarps = 4;                       // warps that scan one row's histogram
 constexpr int kVecCacheAt = 256;                    // gathered tags before, cached vectors after (words)
@@ -588,11 +592,6 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
     const uint32_t span = 4u * gtop + 3u;  // keys 0 .. span; lane l takes span - 16 l down to span - 16 l - 15
     const uint32_t top = span - 16u * static_cast<uint32_t>(lane);
     const bool live = g.active && span >= 16u * static_cast<uint32_t>(lane);
-    auto count_at = [&](int j) -> uint32_t {
-      if (!live || 16u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(j) > span) return 0u;
-      const uint32_t key = top - static_cast<uint32_t>(j);
-      return (key > g.kmax || key < g.klo) ? 0u : hist[key & kSlotMask];
-    };
     uint32_t Cl = 0u;
     float Ml = 0.f;
 #pragma unroll
@@ -600,7 +599,7 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
       const uint32_t key = top - static_cast<uint32_t>(j);
       const bool in = live && 16u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(j) <= span &&
                       key <= g.kmax && key >= g.klo;
-      const uint32_t n = in ? hist[key & kSlotMask] : 0u;
+      const uint32_t n = in ? hist[hslot(key)] : 0u;
       const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
       Cl += n;
       Ml += n ? static_cast<float>(n) * ms : 0.f;
@@ -619,82 +618,85 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
       sh.s_C[0][lane] = 0u;
       sh.s_M[0][lane] = DF{0.f, 0.f};
     }
+    // The crossing lane's 16 keys resolved by the warp: lane j < 16 takes
+    // its key j (count, mass), then one warp prefix over them.
+    auto lane_keys = [&](int xl, uint32_t& key, uint32_t& n, float& ms) {
+      const uint32_t topx = span - 16u * static_cast<uint32_t>(xl);
+      const uint32_t jj = static_cast<uint32_t>(lane);
+      key = topx - jj;
+      const bool in = lane < 16 && 16u * static_cast<uint32_t>(xl) + jj <= span && key <= g.kmax && key >= g.klo;
+      n = in ? hist[hslot(key)] : 0u;
+      ms = lat_mass(value_of_key<DT>(key), c, g.K);
+    };
     if (topk_on && !given_k) {  // the value where the running count reaches top_k
       const uint32_t Kc = static_cast<uint32_t>(top_k);
       const unsigned bal = __ballot_sync(kFull, live && Cin >= Kc && Cex < Kc);
-      if (bal && lane == __ffs(bal) - 1) {
-        uint32_t run = Cex;
-        DF mb = Mex;
-        for (int j = 0; j < 16 && !ck.found; ++j) {
-          const uint32_t n = count_at(j);
-          if (!n) continue;
-          const uint32_t key = top - static_cast<uint32_t>(j);
-          const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
-          if (run + n >= Kc) {
-            ck.kstar = key;
-            ck.keep = Kc - run;
-            ck.total = n;
-            ck.found = 1;
-            ck.zkept = df_add(mb, static_cast<float>(Kc - run) * ms);
-          }
-          run += n;
-          mb = df_add(mb, static_cast<float>(n) * ms);
+      if (bal) {  // (warp-uniform)
+        const int xl = __ffs(bal) - 1;
+        uint32_t key, n;
+        float ms;
+        lane_keys(xl, key, n, ms);
+        const uint32_t run0 = __shfl_sync(kFull, Cex, xl);
+        const DF mb0 = DF{__shfl_sync(kFull, Mex.hi, xl), __shfl_sync(kFull, Mex.lo, xl)};
+        const uint32_t ci = warp_incl_scan_u32(n);
+        const DF mi = warp_incl_scan_df(DF{n ? static_cast<float>(n) * ms : 0.f, 0.f});
+        DF me = df_shfl_up(mi, 1);
+        if (lane == 0) me = DF{0.f, 0.f};
+        const uint32_t before = run0 + ci - n;
+        const unsigned hit = __ballot_sync(kFull, n > 0u && before < Kc && before + n >= Kc);
+        if (hit && lane == __ffs(hit) - 1) {
+          ck.kstar = key;
+          ck.keep = Kc - before;
+          ck.total = n;
+          ck.found = 1;
+          ck.zkept = df_add(df_add2(mb0, me), static_cast<float>(Kc - before) * ms);
+          sh.cutk[0] = ck;
+          if (!topp_on) sh.cut[0] = ck;
         }
-        sh.cutk[0] = ck;
-        if (!topp_on) sh.cut[0] = ck;
+        const int src = hit ? __ffs(hit) - 1 : 0;
+        ck.found = __shfl_sync(kFull, hit ? 1 : 0, src);
+        ck.kstar = __shfl_sync(kFull, ck.kstar, src);
+        ck.keep = __shfl_sync(kFull, ck.keep, src);
+        ck.total = __shfl_sync(kFull, ck.total, src);
+        ck.zkept = DF{__shfl_sync(kFull, ck.zkept.hi, src), __shfl_sync(kFull, ck.zkept.lo, src)};
       }
-      const int src = bal ? __ffs(bal) - 1 : 0;
-      ck.found = __shfl_sync(kFull, ck.found, src);
-      ck.kstar = __shfl_sync(kFull, ck.kstar, src);
-      ck.keep = __shfl_sync(kFull, ck.keep, src);
-      ck.total = __shfl_sync(kFull, ck.total, src);
-      ck.zkept = DF{__shfl_sync(kFull, ck.zkept.hi, src), __shfl_sync(kFull, ck.zkept.lo, src)};
     }
     if (topp_on && (!topk_on || ck.found)) {
       const DF target = df_mul_f(topk_on ? ck.zkept : g.z, top_p);
       // the first lane whose running mass reaches the target (a window
       // holding less than the target leaves the cut unfound)
       const unsigned bal = __ballot_sync(kFull, live && !df_lt(Min, target));
-      if (bal && lane == __ffs(bal) - 1 && df_lt(Mex, target)) {
-        CutOut cp;
-        cp.found = 0;
-        DF mb = Mex, mb_last{0.f, 0.f};
-        int jl = -1;
-        uint32_t cl = 0u, tl = 0u;
-        float msl = 0.f;
-        for (int j = 0; j < 16 && !cp.found; ++j) {
-          const uint32_t n = count_at(j);
-          const uint32_t key = top - static_cast<uint32_t>(j);
-          uint32_t ce = n;
-          if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
-          if (!ce) continue;
-          const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
-          const DF after = df_add(mb, static_cast<float>(ce) * ms);
-          jl = j;
-          cl = ce;
-          tl = n;
-          msl = ms;
-          mb_last = mb;
-          if (!df_lt(after, target)) {
-            const float need = df_float(df_add(target, -mb.hi)) - mb.lo;
-            uint32_t keep = static_cast<uint32_t>(ceilf(need / ms));
+      const int xl = bal ? __ffs(bal) - 1 : 0;
+      const DF mb0 = DF{__shfl_sync(kFull, Mex.hi, xl), __shfl_sync(kFull, Mex.lo, xl)};
+      if (bal && df_lt(mb0, target)) {  // (warp-uniform)
+        uint32_t key, n;
+        float ms;
+        lane_keys(xl, key, n, ms);
+        uint32_t ce = n;
+        if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
+        const DF mi = warp_incl_scan_df(DF{ce ? static_cast<float>(ce) * ms : 0.f, 0.f});
+        DF me = df_shfl_up(mi, 1);
+        if (lane == 0) me = DF{0.f, 0.f};
+        const DF before = df_add2(mb0, me), after = df_add2(mb0, mi);
+        const unsigned hit = __ballot_sync(kFull, ce > 0u && !df_lt(after, target));
+        // (rounding may leave the crossing past these keys: then all of the last one)
+        const unsigned pos = __ballot_sync(kFull, ce > 0u);
+        const int jc = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        if (jc >= 0 && lane == jc) {
+          CutOut cp;
+          uint32_t keep = ce;
+          if (hit) {
+            const float need = df_float(df_add(target, -before.hi)) - before.lo;
+            keep = static_cast<uint32_t>(ceilf(need / ms));
             keep = max(1u, min(keep, ce));
-            cp.kstar = key;
-            cp.keep = keep;
-            cp.total = n;
-            cp.found = 1;
-            cp.zkept = df_add(mb, static_cast<float>(keep) * ms);
           }
-          mb = after;
-        }
-        if (!cp.found && jl >= 0) {  // rounding put the crossing past this lane: all of its last value
-          cp.kstar = top - static_cast<uint32_t>(jl);
-          cp.keep = cl;
-          cp.total = tl;
+          cp.kstar = key;
+          cp.keep = keep;
+          cp.total = n;
           cp.found = 1;
-          cp.zkept = df_add(mb_last, static_cast<float>(cl) * msl);
+          cp.zkept = df_add(before, static_cast<float>(keep) * ms);
+          sh.cut[0] = cp;
         }
-        sh.cut[0] = cp;
       }
     }
   }
@@ -725,7 +727,7 @@ __device__ __noinline__ void window_pass(uint32_t* hist, const unsigned char* ro
 #pragma unroll
       for (int j = 0; j < E::kPerVec; ++j) {
         const uint32_t k = E::key(E::bits_of(x[u], j));
-        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(hist + (k & kSlotMask)), 1u);
+        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(hist + hslot(k)), 1u);
       }
     }
   }
@@ -1612,7 +1614,7 @@ __device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t*
       const uint32_t kl = sh.g[0].klo;
       for (uint32_t i = lane; i < ntag; i += 32) {
         const uint32_t k = tag_key(wg[i]);
-        if (k >= kl) red_add_shared(smem_addr(hist + (k & kSlotMask)), 1u);
+        if (k >= kl) red_add_shared(smem_addr(hist + hslot(k)), 1u);
       }
     }
     __syncthreads();
@@ -1669,7 +1671,7 @@ __device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t*
         while (msk) {
           const int j = __ffs(msk) - 1;
           msk &= msk - 1u;
-          red_add_shared(smem_addr(hist + (E::key(E::bits_of(x, j)) & kSlotMask)), 1u);
+          red_add_shared(smem_addr(hist + hslot(E::key(E::bits_of(x, j)))), 1u);
         }
       }
     }
