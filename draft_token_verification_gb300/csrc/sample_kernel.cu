@@ -704,15 +704,20 @@ __device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, in
 }
 
 // Exact counts of the row's tokens with keys in [klo, khi] (klo .. klo +
-// kWindow - 1, slot key & (kWindow - 1)), by one re-read of the row with
-// four loads in flight per thread.  Whole CTA.
+// kWindow - 1, slot hslot(key)), by one re-read of the row with four loads
+// in flight per thread.  Whole CTA.
 template <int DT>
 __device__ __noinline__ void window_pass(uint32_t* hist, const unsigned char* row, int V, bool aligned,
-                                         uint32_t klo, uint32_t khi) {
+                                         uint32_t klo, uint32_t khi, uint32_t* priv) {
   using E = Elt<DT>;
   constexpr int kU = 4;
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  // each warp counts into its own copy when priv is given (fewer colliding
+  // atomics on the common values), then the copies are summed
+  uint32_t* const mine = priv ? priv + (threadIdx.x >> 5) * kWindow : hist;
   for (int t = threadIdx.x; t < kWindow; t += kThreads) hist[t] = 0u;
+  if (priv)
+    for (int t = threadIdx.x; t < kWarps * kWindow; t += kThreads) priv[t] = 0u;
   __syncthreads();
   for (int v0 = threadIdx.x; v0 < nvec; v0 += kU * kThreads) {
     uint4 x[kU];
@@ -727,11 +732,20 @@ __device__ __noinline__ void window_pass(uint32_t* hist, const unsigned char* ro
 #pragma unroll
       for (int j = 0; j < E::kPerVec; ++j) {
         const uint32_t k = E::key(E::bits_of(x[u], j));
-        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(hist + hslot(k)), 1u);
+        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(mine + hslot(k)), 1u);
       }
     }
   }
   __syncthreads();
+  if (priv) {
+    for (int t = threadIdx.x; t < kWindow; t += kThreads) {
+      uint32_t sum = 0u;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) sum += priv[w * kWindow + t];
+      hist[t] = sum;
+    }
+    __syncthreads();
+  }
 }
 
 constexpr int kSlowWindows = 8;  // windows of kWindow keys tried before the bitwise search
@@ -744,7 +758,8 @@ constexpr int kSlowWindows = 8;  // windows of kWindow keys tried before the bit
 // takes the bitwise search.  Whole CTA; sh.g[0] is left as it was.
 template <int DT>
 __device__ __noinline__ CutOut window_cut(Shm& sh, uint32_t* hist, const unsigned char* row, int V, bool aligned,
-                                          int top_k, float top_p, const RowStat& rs, double zfull) {
+                                          int top_k, float top_p, const RowStat& rs, double zfull,
+                                          uint32_t* priv) {
   // (32-bit keys are too fine for windows of kWindow keys)
   if (Elt<DT>::kKeyBits > 16) return search_cut<DT>(sh, row, V, aligned, top_k, top_p, rs, zfull);
   const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
@@ -761,7 +776,7 @@ __device__ __noinline__ CutOut window_cut(Shm& sh, uint32_t* hist, const unsigne
     for (int w = 0; w < kSlowWindows && !found; ++w) {
       const uint32_t gt = hi >> 2;
       const uint32_t lo = gt >= static_cast<uint32_t>(kGroups - 1) ? 4u * (gt - static_cast<uint32_t>(kGroups - 1)) : 0u;
-      window_pass<DT>(hist, row, V, aligned, lo, hi);
+      window_pass<DT>(hist, row, V, aligned, lo, hi, priv);
       if (threadIdx.x == 0) {
         RowG g = g0;
         g.kmax = hi;
@@ -1701,7 +1716,8 @@ __device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t*
     rs.tie_cut = V;
     float zk = df_float(g.z);
     if (filt && !bad) {
-      const CutOut co = fast ? sh.cut[0] : window_cut<DT>(sh, hist, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z));
+      const CutOut co = fast ? sh.cut[0] : window_cut<DT>(sh, hist, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z),
+                                                          use_lists ? ltags : nullptr);
       rs.kstar = co.kstar;
       zk = df_float(co.zkept);
       if (co.keep < co.total)
