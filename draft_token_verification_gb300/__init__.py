@@ -51,7 +51,7 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
     "spec_transform_probs", "spec_get_status", "spec_error_string", "spec_expected_tokens",
     "spec_improvement_factor", "spec_break_even_acceptance", "spec_verify_sample_noalloc",
-    "spec_sample_launch_mode",
+    "spec_sample_launch_mode", "spec_best_gamma",
 )
 SPEC_LAUNCH_SEPARATE = 0
 SPEC_LAUNCH_FUSED = 1
@@ -120,8 +120,19 @@ def lib() -> ctypes.CDLL:
             L.spec_break_even_acceptance.restype = D
             L.spec_sample_launch_mode.argtypes = [I]
             L.spec_sample_launch_mode.restype = I
+            L.spec_best_gamma.argtypes = [D, D, I, ctypes.POINTER(D)]
+            L.spec_best_gamma.restype = I
             _lib = L
     return _lib
+
+
+def spec_best_gamma(alpha: float, c: float, gamma_max: int = 12):
+    """The draft length in 1..gamma_max with the largest speedup: (gamma, speedup)."""
+    best = ctypes.c_double()
+    g = lib().spec_best_gamma(float(alpha), float(c), int(gamma_max), ctypes.byref(best))
+    if g < 0:
+        raise SpecVerifyError(g, "spec_best_gamma")
+    return g, best.value
 
 
 def spec_sample_launch_mode(mode: int) -> int:

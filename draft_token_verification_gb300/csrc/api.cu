@@ -300,4 +300,19 @@ double spec_improvement_factor(double alpha, int gamma, double c) {
 
 double spec_break_even_acceptance(int k) { return static_cast<double>(k) / static_cast<double>(k + 1); }
 
+int spec_best_gamma(double alpha, double c, int gamma_max, double* best_factor) {
+  if (!(alpha >= 0.0 && alpha <= 1.0) || !(c >= 0.0) || gamma_max < 1 || gamma_max > 64) return SPEC_ERR_INVALID_ARG;
+  int arg = 1;
+  double top = spec_improvement_factor(alpha, 1, c);
+  for (int g = 2; g <= gamma_max; ++g) {
+    const double f = spec_improvement_factor(alpha, g, c);
+    if (f > top) {
+      top = f;
+      arg = g;
+    }
+  }
+  if (best_factor) *best_factor = top;
+  return arg;
+}
+
 }  // extern "C"

@@ -257,6 +257,15 @@ double spec_improvement_factor(double alpha, int gamma, double c);
 /* [TGTG] section 5.1, equation 1: break-even acceptance k / (k + 1). */
 double spec_break_even_acceptance(int k);
 
+/*
+ * [SDSC] the draft-length scan: the gamma in 1..gamma_max with the largest
+ * spec_improvement_factor(alpha, gamma, c), the smallest such gamma on ties;
+ * that speedup is written to *best_factor (may be NULL).  Host only.
+ * Returns gamma, or SPEC_ERR_INVALID_ARG unless 0 <= alpha <= 1, c >= 0 and
+ * 1 <= gamma_max <= 64.
+ */
+int spec_best_gamma(double alpha, double c, int gamma_max, double* best_factor);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,6 +76,8 @@ def _load():
             lib.oracle_improvement_factor.restype = D
             lib.oracle_break_even.argtypes = [I]
             lib.oracle_break_even.restype = D
+            lib.oracle_best_gamma.argtypes = [D, D, I, ctypes.POINTER(D)]
+            lib.oracle_best_gamma.restype = I
             _lib = lib
     return _lib
 
@@ -183,3 +185,10 @@ def improvement_factor(alpha: float, gamma: int, c: float) -> float:
 
 def break_even(k: int) -> float:
     return _load().oracle_break_even(int(k))
+
+
+def best_gamma(alpha: float, c: float, gamma_max: int = 12):
+    """Speedup Calculator's draft-length scan: (gamma, speedup) of the best gamma in 1..gamma_max."""
+    best = ctypes.c_double()
+    g = _load().oracle_best_gamma(float(alpha), float(c), int(gamma_max), ctypes.byref(best))
+    return g, best.value

@@ -548,3 +548,21 @@ double oracle_improvement_factor(double alpha, int gamma, double c) {
 
 /* [TGTG] section 5.1, equation 1: break-even acceptance k / (k + 1). */
 double oracle_break_even(int k) { return (double)k / (double)(k + 1); }
+
+/*
+ * [SDSC] the draft length scan: the gamma in 1..gamma_max with the largest
+ * speedup E / (gamma*c + 1) (the first one on ties), its speedup in *best.
+ */
+int oracle_best_gamma(double alpha, double c, int gamma_max, double* best) {
+  int g, arg = 1;
+  double top = oracle_improvement_factor(alpha, 1, c);
+  for (g = 2; g <= gamma_max; ++g) {
+    double f = oracle_improvement_factor(alpha, g, c);
+    if (f > top) {
+      top = f;
+      arg = g;
+    }
+  }
+  if (best) *best = top;
+  return arg;
+}

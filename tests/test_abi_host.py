@@ -128,3 +128,16 @@ def test_binding_requires_cuda_tensors():
     x = torch.zeros(2, 3, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         sv.spec_verify_greedy(x, torch.zeros(2, 2, dtype=torch.int32), workspace=torch.zeros(1 << 16, dtype=torch.uint8))
+
+
+def test_best_gamma_matches_oracle(L):
+    import oracle
+    for alpha in (0.0, 0.3, 0.6, 0.8, 0.9, 0.97, 1.0):
+        for c in (0.0, 0.01, 0.05, 0.1, 0.3, 1.0, 1.5):
+            for gmax in (1, 5, 12):
+                g, f = sv.spec_best_gamma(alpha, c, gmax)
+                go, fo = oracle.best_gamma(alpha, c, gmax)
+                assert g == go and f == pytest.approx(fo, rel=1e-15), (alpha, c, gmax)
+    best = ctypes.c_double()
+    for bad in ((-0.1, 0.1, 12), (1.1, 0.1, 12), (0.5, -1.0, 12), (0.5, 0.1, 0), (0.5, 0.1, 65)):
+        assert L.spec_best_gamma(bad[0], bad[1], bad[2], ctypes.byref(best)) == sv.SPEC_ERR_INVALID_ARG

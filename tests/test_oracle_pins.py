@@ -454,3 +454,37 @@ def test_tree_malformed_parents_flagged():
     out = oracle.verify_tree_greedy(logits, tokens, parents, 3)
     assert out["flags"][0] & 1
     assert out["n"][0] == 2 and out["path"][0, :2].tolist() == [1, 3]
+
+
+# The calculator's draft-length scan (gamma = 1..12, the peak speedup), pinned
+# by the cases the mathematics decides without the scan:
+#  - c = 0: the speedup is E itself, which grows with gamma when alpha > 0, so
+#    the scan ends at gamma_max (alpha = 0: E = 1 for every gamma, so 1);
+#  - alpha = 0: the speedup is 1 / (gamma c + 1), falling with gamma when c > 0;
+#  - alpha = 1: E = gamma + 1 and the speedup (gamma + 1) / (gamma c + 1) rises
+#    for c < 1, falls for c > 1 and is 1 for c = 1 (ties: the smallest gamma);
+#  - the speedup at the chosen gamma is no lower than at every gamma scanned,
+#    and equals improvement_factor there.
+def test_best_gamma_special_cases():
+    assert oracle.best_gamma(0.7, 0.0, 12) == (12, pytest.approx(oracle.expected_tokens_series(0.7, 12)))
+    assert oracle.best_gamma(0.0, 0.0, 12)[0] == 1
+    for c in (0.05, 0.5, 2.0):
+        g, f = oracle.best_gamma(0.0, c, 12)
+        assert g == 1 and f == pytest.approx(1.0 / (c + 1.0), rel=1e-15)
+    assert oracle.best_gamma(1.0, 0.3, 12) == (12, pytest.approx(13.0 / (12 * 0.3 + 1.0), rel=1e-15))
+    assert oracle.best_gamma(1.0, 1.5, 12) == (1, pytest.approx(2.0 / 2.5, rel=1e-15))
+    assert oracle.best_gamma(1.0, 1.0, 12) == (1, pytest.approx(1.0, rel=1e-15))
+
+
+@pytest.mark.parametrize("alpha,c", [(0.8, 0.05), (0.6, 0.1), (0.9, 0.02), (0.5, 0.3), (0.95, 0.2)])
+def test_best_gamma_is_the_scan_peak(alpha, c):
+    g, f = oracle.best_gamma(alpha, c, 12)
+    assert 1 <= g <= 12 and f == oracle.improvement_factor(alpha, g, c)
+    for gg in range(1, 13):
+        assert oracle.improvement_factor(alpha, gg, c) <= f
+        if gg < g:
+            assert oracle.improvement_factor(alpha, gg, c) < f
+    # the speedup rises to the peak and falls after it (the page: concave in gamma)
+    vals = [oracle.improvement_factor(alpha, gg, c) for gg in range(1, 13)]
+    assert all(vals[i] < vals[i + 1] for i in range(g - 1))
+    assert all(vals[i] >= vals[i + 1] for i in range(g - 1, 11))
