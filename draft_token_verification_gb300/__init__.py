@@ -51,7 +51,7 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
     "spec_transform_probs", "spec_get_status", "spec_error_string", "spec_expected_tokens",
     "spec_improvement_factor", "spec_break_even_acceptance", "spec_verify_sample_noalloc",
-    "spec_sample_launch_mode", "spec_best_gamma",
+    "spec_sample_launch_mode", "spec_best_gamma", "spec_first_draft_check",
 )
 SPEC_LAUNCH_SEPARATE = 0
 SPEC_LAUNCH_FUSED = 1
@@ -122,6 +122,8 @@ def lib() -> ctypes.CDLL:
             L.spec_sample_launch_mode.restype = I
             L.spec_best_gamma.argtypes = [D, D, I, ctypes.POINTER(D)]
             L.spec_best_gamma.restype = I
+            L.spec_first_draft_check.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
+            L.spec_first_draft_check.restype = I
             _lib = L
     return _lib
 
@@ -296,6 +298,26 @@ def spec_verify_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor, 
     )
     _check(rc, "spec_verify_greedy")
     return out_tokens, out_num_accepted
+
+
+def spec_first_draft_check(prev_rows: torch.Tensor, draft0: torch.Tensor, out_accept=None, out_argmax=None,
+                           workspace=None, stream=None):
+    """Rejection fast path: (accept [B], argmax [B]) of the previous step's rows [B][V] against draft0 [B]."""
+    B, V = prev_rows.shape
+    dev = prev_rows.device
+    if out_accept is None:
+        out_accept = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_argmax is None:
+        out_argmax = torch.empty((B,), dtype=torch.int32, device=dev)
+    dt = _dtype_code(prev_rows)
+    ws = _workspace(workspace, spec_verify_workspace_size(B, 1, V, dt), dev)
+    rc = lib().spec_first_draft_check(
+        _dev(prev_rows, "prev_rows"), _dev(draft0, "draft0", torch.int32), B, V, dt,
+        _dev(out_accept, "out_accept", torch.int32), _dev(out_argmax, "out_argmax", torch.int32),
+        ws.data_ptr(), ws.numel(), _stream(stream),
+    )
+    _check(rc, "spec_first_draft_check")
+    return out_accept, out_argmax
 
 
 def spec_verify_tree_greedy(node_logits: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor,

@@ -220,6 +220,36 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   return SPEC_OK;
 }
 
+int spec_first_draft_check(const void* prev_rows, const int32_t* draft0, int B, int V, spec_dtype dtype,
+                           int32_t* out_accept, int32_t* out_argmax, void* workspace, size_t workspace_bytes,
+                           void* cuda_stream) {
+  if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
+  if (!prev_rows || !draft0 || !out_accept || !out_argmax) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(prev_rows, elt_bytes(dtype)) || !aligned_to(draft0, 4)) return SPEC_ERR_INVALID_ARG;
+  const int rc = check_workspace(workspace, workspace_bytes, B, 1);
+  if (rc != SPEC_OK) return rc;
+  const WsLayout L = ws_layout(B, 1);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  ArgmaxArgs a = {};
+  a.logits = prev_rows;
+  a.tokens = draft0;
+  a.B = B;
+  a.R = 1;
+  a.V = V;
+  a.first_check = 1;
+  a.nvr = (V + vec_elems(dtype) - 1) / vec_elems(dtype);
+  a.aligned = rows_aligned(prev_rows, V, dtype);
+  a.out_tokens = out_argmax;
+  a.out_n = out_accept;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status);
+  a.slots = reinterpret_cast<unsigned long long*>(w + L.g_slots);
+  a.tickets = reinterpret_cast<uint32_t*>(w + L.g_tickets);
+  if (launch_argmax(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, false, cuda_stream) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
 int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens, const int32_t* parents, int B,
                             int N, int V, int max_depth, spec_dtype dtype, int32_t* out_tokens, int32_t* out_path,
                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,

@@ -68,6 +68,16 @@ __device__ __forceinline__ void sequence_walk(const ArgmaxArgs& a, int b) {
   unsigned long long* slots = a.slots + static_cast<size_t>(b) * a.R;
   __shared__ int s_red[kWarps];
   if constexpr (!TREE) {
+    if (a.first_check) {  // the rejection fast path: one row, the first draft
+      if (tid == 0) {
+        const int am = unpack_index(__ldcg(slots));
+        a.out_tokens[b] = am;
+        a.out_n[b] = a.tokens[b] == am ? 1 : 0;
+        slots[0] = 0ull;
+        a.tickets[b] = 0u;
+      }
+      return;
+    }
     // n = the first position whose draft differs from the target's argmax
     const int k = a.R - 1;
     const int32_t* x = a.tokens + static_cast<size_t>(b) * k;

@@ -162,6 +162,7 @@ struct ArgmaxArgs {
   const int32_t* parents;      // tree only
   int B, R, V;                 // R rows per sequence (k+1, or N)
   int max_depth;               // tree only
+  int first_check;             // chain with R = 1: out_n = (tokens == argmax), out_tokens = argmax
   int nvr;                     // 16-byte vectors per row: ceil(V / elements per vector)
   int grid;                    // CTAs (set by the launcher)
   int aligned;

@@ -138,6 +138,24 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        void* cuda_stream);
 
 /*
+ * The rejection fast path ([TGTG] section 2.4, KV-cached regime): the first
+ * draft token is checked against the previous step's logits (already
+ * computed), so that the k-token verification pass runs only when it is
+ * accepted.  For every sequence b, a = argmax of prev_rows[b] (raw logits,
+ * lowest index on ties):
+ *   prev_rows   [B][V] dtype   device
+ *   draft0      [B]    int32   device: each sequence's first draft token
+ *   out_accept  [B]    int32   device: 1 iff draft0[b] == a, else 0
+ *   out_argmax  [B]    int32   device: a (the token to commit on rejection)
+ * Workspace: spec_verify_workspace_size(B, 1, V, dtype) bytes, as for
+ * spec_verify_greedy (left zeroed).  Greedy only: the pages check the first
+ * token by exact match.
+ */
+int spec_first_draft_check(const void* prev_rows, const int32_t* draft0, int B, int V,
+                           spec_dtype dtype, int32_t* out_accept, int32_t* out_argmax,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Greedy chain verification ([TGTG] section 2.4): a_i = argmax of the raw
  * target row i (lowest index on ties; temperature and filters do not change
  * an argmax and are not taken); n = first i < k with x_i != a_i, else k.
@@ -160,7 +178,9 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
  *   max_depth    >= 1, at least the depth of every node that can be agreed
  *   out_tokens   [B][max_depth+1]: tokens of the path root-exclusive, then
  *                argmax(row d*), then -1
- *   out_path     [B][max_depth+1]: node ids of the path (root excluded), -1 padded
+ *   out_path     [B][max_depth+1]: node ids of the path (root excluded), -1 padded;
+ *                for a KV cache these are the nodes to keep, node out_path[d]
+ *                moving to position d + 1 after the root
  *   out_num_accepted [B] = depth(d*)
  * A malformed parent entry sets SPEC_STATUS_BAD_PARENT (that node is not
  * agreed); an agreed node deeper than max_depth is ignored and sets

@@ -78,6 +78,8 @@ def _load():
             lib.oracle_break_even.restype = D
             lib.oracle_best_gamma.argtypes = [D, D, I, ctypes.POINTER(D)]
             lib.oracle_best_gamma.restype = I
+            lib.oracle_first_draft_check.argtypes = [P, I, P, I, I, P, P]
+            lib.oracle_first_draft_check.restype = I
             _lib = lib
     return _lib
 
@@ -152,6 +154,17 @@ def verify_greedy(target, tokens):
     out = dict(tokens=np.empty((B, k + 1), np.int32), n=np.empty(B, np.int32))
     _load().oracle_verify_greedy(_ptr(target), _dtype_code(target), _ptr(tokens), B, k, V,
                                  _ptr(out["tokens"]), _ptr(out["n"]))
+    return out
+
+
+def first_draft_check(prev_rows, draft0):
+    """Rejection fast path: prev_rows [B][V] (the previous step's logits), draft0 [B]."""
+    prev_rows = np.ascontiguousarray(prev_rows)
+    draft0 = np.ascontiguousarray(draft0, dtype=np.int32)
+    B, V = prev_rows.shape
+    out = dict(accept=np.empty(B, np.int32), argmax=np.empty(B, np.int32))
+    _load().oracle_first_draft_check(_ptr(prev_rows), _dtype_code(prev_rows), _ptr(draft0), B, V,
+                                     _ptr(out["accept"]), _ptr(out["argmax"]))
     return out
 
 

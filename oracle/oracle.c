@@ -452,6 +452,27 @@ int oracle_verify_greedy(const void* target, int dtype, const int32_t* tokens, i
 }
 
 /*
+ * The rejection fast path ([TGTG] section 2.4, KV-cached regime): the first
+ * draft token is checked against the previous step's logits, already
+ * computed; the k-token pass is needed only when it is accepted.  For every
+ * sequence b: a = argmax of prev_rows[b] (lowest index on ties);
+ * out_accept[b] = 1 iff draft0[b] == a; out_argmax[b] = a (the token to
+ * commit when draft 0 is rejected).
+ */
+int oracle_first_draft_check(const void* prev_rows, int dtype, const int32_t* draft0, int B, int V,
+                             int32_t* out_accept, int32_t* out_argmax) {
+  size_t es = (dtype == ORACLE_BF16) ? 2 : 4;
+  int b;
+  for (b = 0; b < B; ++b) {
+    const char* row = (const char*)prev_rows + (size_t)b * (size_t)V * es;
+    int a = row_argmax(row, dtype, V);
+    out_argmax[b] = a;
+    out_accept[b] = draft0[b] == a ? 1 : 0;
+  }
+  return 0;
+}
+
+/*
  * Greedy token-tree verification ([EIN] "One decode round, end to end"):
  * node j's row is the target's distribution for the token after node j
  * (node 0 is the root, the last committed token).  A node is on an agreed

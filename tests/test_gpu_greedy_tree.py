@@ -105,3 +105,20 @@ def test_tree_bad_parents_and_depth_limit_status():
     o = oracle.verify_tree_greedy(case.logits, case.node_tokens, case.parents, 2)
     assert np.array_equal(out[2].cpu().numpy(), o["n"]) and np.array_equal(out[0].cpu().numpy(), o["tokens"])
     assert sv.spec_get_status(ws) & sv.SPEC_STATUS_DEPTH
+
+
+@pytest.mark.parametrize("B,V,dtype,quantize", [(1, 1, W.BF16, None), (7, 33, W.F32, None), (64, 128256, W.BF16, None),
+                                                (32, 5000, W.BF16, 1.0), (16, 20000, W.F32, 2.0)])
+def test_first_draft_check_parity(B, V, dtype, quantize):
+    rng = np.random.default_rng(B * 7 + V)
+    x = rng.normal(0.0, 3.0, size=(B, V)).astype(np.float32)
+    if quantize:
+        x = np.round(x / quantize) * quantize
+    rows = W.bf16_bits(x) if dtype == W.BF16 else x
+    o0 = oracle.first_draft_check(rows, np.zeros(B, np.int32))
+    # about half the drafts are the argmax
+    draft0 = np.where(rng.random(B) < 0.5, o0["argmax"], rng.integers(0, V, B)).astype(np.int32)
+    o = oracle.first_draft_check(rows, draft0)
+    acc, am = lib().spec_first_draft_check(to_dev(rows), to_dev(draft0))
+    assert np.array_equal(am.cpu().numpy(), o["argmax"])
+    assert np.array_equal(acc.cpu().numpy(), o["accept"])

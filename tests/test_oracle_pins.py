@@ -488,3 +488,17 @@ def test_best_gamma_is_the_scan_peak(alpha, c):
     vals = [oracle.improvement_factor(alpha, gg, c) for gg in range(1, 13)]
     assert all(vals[i] < vals[i + 1] for i in range(g - 1))
     assert all(vals[i] >= vals[i + 1] for i in range(g - 1, 11))
+
+
+# The rejection fast path, pinned by hand-made rows: the lowest index wins a
+# tie, -0 equals +0, and a mismatching draft yields the argmax to commit.
+def test_first_draft_check_hand_rows():
+    rows = np.array([[0.0, 3.0, 1.0, 3.0],       # tie at 1 and 3: lowest index, 1
+                     [-0.0, -1.0, 0.0, -2.0],    # -0 == +0: index 0
+                     [-np.inf, -5.0, -np.inf, -7.0],
+                     [2.0, 1.0, 0.5, 9.5]], np.float32)
+    draft0 = np.array([1, 2, 1, 0], np.int32)
+    for arr in (rows, W.bf16_bits(rows)):
+        o = oracle.first_draft_check(arr, draft0)
+        assert o["argmax"].tolist() == [1, 0, 1, 3]
+        assert o["accept"].tolist() == [1, 0, 1, 0]
