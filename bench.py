@@ -163,6 +163,21 @@ def make_inputs(seed_offset: int = 0):
     return s, t
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as tdist
+
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(positions_per_rank_step: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank's positions over the slowest rank's time."""
+    return positions_per_rank_step * world * steps / (elapsed_ms / 1e3)
+
+
 def to_torch(arr, device=None, pin=False):
     import torch
 
@@ -250,9 +265,7 @@ def run_gpu(args, rank, world):
     elapsed_ms = start.elapsed_time(end)
     per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])] for e in evs])
     if dist:
-        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # acceptance statistics of the last step (MAL = accepted drafts per pass)
     n_acc = o["n"].cpu().numpy()
@@ -289,9 +302,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if dist:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
     status |= sv.spec_get_status(ws)
 
     return dict(elapsed_ms=elapsed_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
@@ -380,7 +391,7 @@ def main():
     K = args.steps
     per = r["per"]
     pos = positions_per_step() * world
-    value = pos * K / (r["elapsed_ms"] / 1e3)
+    value = job_rate(positions_per_step(), world, K, r["elapsed_ms"])
     peak, peak_kind = measured_peaks()
     t_sample = float(per[:, 0].mean()) / 1e3
     achieved = sample_bytes() / t_sample / 1e9
