@@ -37,6 +37,8 @@ FLAG_DEGENERATE = 4
 FLAG_CUT_BOUNDARY = 8
 FLAG_BAD_TOKEN = 16
 FLAG_BAD_ROW = 32
+FLAG_BAD_PARENT = 64
+FLAG_DEPTH = 128
 #: flags that mark a sequence whose outcome sits within 1e-6 of a decision edge
 BOUNDARY_FLAGS = FLAG_ACCEPT_BOUNDARY | FLAG_DRAW_BOUNDARY | FLAG_DEGENERATE | FLAG_CUT_BOUNDARY
 
@@ -68,6 +70,7 @@ def _load():
             lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P]
             lib.oracle_verify_greedy.restype = I
             lib.oracle_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P]
+            lib.oracle_verify_tree_sample.argtypes = [P, P, I, P, P, P, I, I, I, I, D, P, P, P, P, P]
             lib.oracle_verify_tree_greedy.restype = I
             for name in ("oracle_expected_tokens_series", "oracle_expected_tokens_closed"):
                 getattr(lib, name).argtypes = [D, I]
@@ -181,6 +184,35 @@ def verify_tree_greedy(logits, node_tokens, parents, max_depth):
         _ptr(logits), _dtype_code(logits), _ptr(node_tokens), _ptr(parents), B, N, V, int(max_depth),
         _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["n"]), _ptr(out["flags"]),
     )
+    return out
+
+
+def verify_tree_sample(logits, draft_logits, node_tokens, parents, uniforms, max_depth,
+                       temperature=1.0):
+    """Token-tree sampling verification.
+
+    logits, draft_logits [B][N][V] (same dtype); node_tokens, parents [B][N];
+    uniforms [B][N] float32 (u_0 the final draw, u_j the test of node j).
+    Returns tokens / path [B][max_depth+1], n [B], flags [B], margin [B].
+    """
+    logits = np.ascontiguousarray(logits)
+    draft_logits = np.ascontiguousarray(draft_logits)
+    if draft_logits.dtype != logits.dtype or draft_logits.shape != logits.shape:
+        raise ValueError("logits and draft_logits must share dtype and shape")
+    node_tokens = np.ascontiguousarray(node_tokens, dtype=np.int32)
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    B, N, V = logits.shape
+    D = max_depth + 1
+    out = dict(tokens=np.empty((B, D), np.int32), path=np.empty((B, D), np.int32),
+               n=np.empty(B, np.int32), flags=np.empty(B, np.uint32), margin=np.empty(B, np.float64))
+    rc = _load().oracle_verify_tree_sample(
+        _ptr(logits), _ptr(draft_logits), _dtype_code(logits), _ptr(node_tokens), _ptr(parents),
+        _ptr(uniforms), B, N, V, int(max_depth), float(temperature), _ptr(out["tokens"]),
+        _ptr(out["path"]), _ptr(out["n"]), _ptr(out["flags"]), _ptr(out["margin"]),
+    )
+    if rc != 0:
+        raise ValueError("oracle_verify_tree_sample rejected its arguments")
     return out
 
 

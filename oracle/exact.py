@@ -126,3 +126,53 @@ def topk_bruteforce(values: Sequence[float], top_k: int) -> frozenset:
         if best is None or tot > best[0]:
             best = (tot, s)
     return frozenset(best[1])
+
+
+def sibling_law(p: Dist, q: Dist, tokens: Sequence[int]) -> Dict[Tuple[str, int], Fraction]:
+    """Law of one tree node's outcome for fixed child tokens, tried in order.
+
+    The rule applied down the branches (Edge Inference Notes, "One decode
+    round, end to end"), with the sibling reading: a rejected child removes
+    the draft mass from the residual, r <- max(0, r - q) / S, and the next
+    child is accepted with probability min(1, r(x) / q(x)) (1 when q(x) = 0
+    and r(x) > 0).  A residual of mass 0 is replaced by p.  Keys are
+    ("accept", j) for the j-th child and ("draw", t) for a drawn token t once
+    every child is rejected.
+    """
+    law: Dict[Tuple[str, int], Fraction] = {}
+    r = list(p)
+    reach = Fraction(1)
+    for j, x in enumerate(tokens):
+        if q[x]:
+            a = min(Fraction(1), r[x] / q[x])
+        else:
+            a = Fraction(1) if r[x] > 0 else Fraction(0)
+        if a:
+            law[("accept", j)] = reach * a
+        reach *= 1 - a
+        if reach == 0:
+            return law
+        w = [max(Fraction(0), a_ - b_) for a_, b_ in zip(r, q)]
+        s = sum(w)
+        r = [x_ / s for x_ in w] if s else list(p)
+    for t, rt in enumerate(r):
+        if rt:
+            law[("draw", t)] = reach * rt
+    return law
+
+
+def first_token_law(p: Dist, q: Dist, k: int) -> Dict[int, Fraction]:
+    """Law of the first committed token when a node has k children drawn
+    independently from q and they are checked with :func:`sibling_law`."""
+    out: Dict[int, Fraction] = {}
+    V = len(p)
+    for toks in product(range(V), repeat=k):
+        pr = Fraction(1)
+        for x in toks:
+            pr *= q[x]
+        if pr == 0:
+            continue
+        for (kind, idx), m in sibling_law(p, q, toks).items():
+            t = toks[idx] if kind == "accept" else idx
+            out[t] = out.get(t, Fraction(0)) + pr * m
+    return out

@@ -47,6 +47,9 @@
                                      and the other decision changes the outcome */
 #define OFLAG_BAD_TOKEN 16u       /* a draft token outside [0, V)             */
 #define OFLAG_BAD_ROW 32u         /* a row with NaN/+inf or no finite entry   */
+#define OFLAG_BAD_PARENT 64u      /* tree: parents[0] != -1 or a parent outside [0, j) */
+#define OFLAG_DEPTH 128u          /* tree: the walk stopped at depth max_depth on a
+                                     node that has children                    */
 
 #define BOUNDARY_EPS 1e-6
 
@@ -543,6 +546,143 @@ int oracle_verify_tree_greedy(const void* logits, int dtype, const int32_t* node
   free(depth);
   free(agreed);
   free(chain);
+  return 0;
+}
+
+/*
+ * Token-tree sampling verification ([EIN] "One decode round, end to end": the
+ * accept-or-correct rule of "The core idea: draft, then check" applied down
+ * the branches of the draft tree).  Per tree b, starting at the root (node 0):
+ *
+ *   p = softmax(node_logits[v] / T), q = softmax(draft_logits[v] / T)
+ *   r = p
+ *   for each child j of v (parents[j] == v), in ascending node order:
+ *     skip j if its token is outside [0, V) or depth(v) == max_depth
+ *     accept j iff u_j * q(x_j) < r(x_j)   (probability min(1, r/q))
+ *       -> commit x_j, move to v = j, start again
+ *     else r <- max(0, r - q) / sum(max(0, r - q))   (q is unchanged)
+ *          a residual of total mass 0 is replaced by p
+ *   no child accepted: draw one token from r with u_0 (inverse CDF,
+ *   ascending index order) and stop.
+ *
+ * The pages state the rule for a chain and say only that it is applied down
+ * the branches.  The sibling rule taken here (each rejected sibling removes
+ * its draft mass from the residual, the next sibling is tested against the
+ * renormalised residual) keeps the output distributed as p when the children
+ * of a node are drawn independently from q; the tests check that property.
+ *
+ * Layouts: node_logits, draft_logits [B][N][V] (draft row v is the draft
+ * distribution the children of v were drawn from), node_tokens, parents
+ * [B][N], uniforms [B][N] (u_0 the final draw, u_j the test of node j).
+ * Outputs: out_tokens [B][max_depth+1] (path tokens, the drawn token, then
+ * -1), out_path [B][max_depth+1] (path node ids, root excluded, -1 padded),
+ * out_n [B] (accepted nodes), out_flags [B] (OFLAG_*), out_margin [B] (the
+ * smallest accept / draw margin met; may be NULL).
+ * A node whose parent entry is malformed is never a child of anything; a
+ * non-finite row at a visited node ends the walk there with drawn token -1.
+ */
+int oracle_verify_tree_sample(const void* node_logits, const void* draft_logits, int dtype,
+                              const int32_t* node_tokens, const int32_t* parents,
+                              const float* uniforms, int B, int N, int V, int max_depth,
+                              double temperature, int32_t* out_tokens, int32_t* out_path,
+                              int32_t* out_n, uint32_t* out_flags, double* out_margin) {
+  size_t es = (dtype == ORACLE_BF16) ? 2 : 4;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  int b, j, t;
+  if (N < 1 || max_depth < 1 || !(temperature > 0.0)) {
+    free(p);
+    free(q);
+    free(r);
+    return -1;
+  }
+  for (b = 0; b < B; ++b) {
+    const int32_t* par = parents + (size_t)b * N;
+    const int32_t* tok = node_tokens + (size_t)b * N;
+    const float* u = uniforms + (size_t)b * N;
+    const size_t D = (size_t)max_depth + 1;
+    uint32_t flags = 0;
+    double margin = INFINITY;
+    int v = 0, n = 0, drawn = -1;
+    if (par[0] != -1) flags |= OFLAG_BAD_PARENT;
+    for (j = 1; j < N; ++j) {
+      if (par[j] < 0 || par[j] >= j) flags |= OFLAG_BAD_PARENT;
+      if (tok[j] < 0 || tok[j] >= V) flags |= OFLAG_BAD_TOKEN;
+    }
+    for (j = 0; j < (int)D; ++j) {
+      out_tokens[(size_t)b * D + j] = -1;
+      out_path[(size_t)b * D + j] = -1;
+    }
+    for (;;) {
+      const char* prow = (const char*)node_logits + ((size_t)b * N + v) * (size_t)V * es;
+      const char* qrow = (const char*)draft_logits + ((size_t)b * N + v) * (size_t)V * es;
+      int has_child = 0, n_test = 0, accepted = -1;
+      for (j = v + 1; j < N; ++j)
+        if (par[j] == v) {
+          has_child = 1;
+          if (tok[j] >= 0 && tok[j] < V && n < max_depth) ++n_test;
+        }
+      if (has_child && n >= max_depth) flags |= OFLAG_DEPTH;
+      if (row_probs_adj(prow, dtype, V, temperature, 0, 1.0, 0, p, NULL, NULL, NULL, NULL, NULL) != 0) {
+        flags |= OFLAG_BAD_ROW;
+        break;
+      }
+      if (n_test > 0 &&
+          row_probs_adj(qrow, dtype, V, temperature, 0, 1.0, 0, q, NULL, NULL, NULL, NULL, NULL) != 0) {
+        flags |= OFLAG_BAD_ROW;
+        break;
+      }
+      for (t = 0; t < V; ++t) r[t] = p[t];
+      for (j = v + 1; j < N && n_test > 0; ++j) {
+        int x = tok[j];
+        double s;
+        if (par[j] != v || x < 0 || x >= V) continue;
+        if (q[x] > 0.0 && r[x] < q[x]) {
+          double mg = fabs((double)u[j] - r[x] / q[x]);
+          if (mg < margin) margin = mg;
+          if (mg < BOUNDARY_EPS) flags |= OFLAG_ACCEPT_BOUNDARY;
+        }
+        if ((double)u[j] * q[x] < r[x]) {
+          accepted = j;
+          break;
+        }
+        s = 0.0;
+        for (t = 0; t < V; ++t) {
+          double d = r[t] - q[t];
+          r[t] = d > 0.0 ? d : 0.0;
+          s += r[t];
+        }
+        if (s > 0.0) {
+          for (t = 0; t < V; ++t) r[t] /= s;
+        } else {
+          flags |= OFLAG_DEGENERATE;
+          for (t = 0; t < V; ++t) r[t] = p[t];
+        }
+      }
+      if (accepted >= 0) {
+        out_path[(size_t)b * D + n] = accepted;
+        out_tokens[(size_t)b * D + n] = tok[accepted];
+        ++n;
+        v = accepted;
+        continue;
+      }
+      {
+        double mg = 0.0;
+        drawn = inverse_cdf(r, V, (double)u[0], &mg);
+        if (mg < margin) margin = mg;
+        if (mg < BOUNDARY_EPS) flags |= OFLAG_DRAW_BOUNDARY;
+      }
+      break;
+    }
+    out_tokens[(size_t)b * D + n] = drawn;
+    out_n[b] = n;
+    out_flags[b] = flags;
+    if (out_margin) out_margin[b] = margin;
+  }
+  free(p);
+  free(q);
+  free(r);
   return 0;
 }
 

@@ -34,7 +34,17 @@ MUTATIONS = [
     ("tree prefers the highest index among equally deep nodes",
      "if (agreed[j] && depth[j] > depth[best]) best = j;", "if (agreed[j] && depth[j] >= depth[best]) best = j;"),
     ("expected tokens drops the last power", "for (i = 0; i <= gamma; ++i) {", "for (i = 0; i < gamma; ++i) {"),
+    ("tree sibling tested against p, not the residual", "if ((double)u[j] * q[x] < r[x]) {",
+     "if ((double)u[j] * q[x] < p[x]) {"),
+    ("tree accept test takes the draw uniform", "if ((double)u[j] * q[x] < r[x]) {",
+     "if ((double)u[0] * q[x] < r[x]) {"),
+    ("tree residual subtracts p", "double d = r[t] - q[t];", "double d = r[t] - p[t];"),
+    ("tree residual left unnormalised", "for (t = 0; t < V; ++t) r[t] /= s;", "s = s;"),
+    ("tree final draw from p", "drawn = inverse_cdf(r, V, (double)u[0], &mg);",
+     "drawn = inverse_cdf(p, V, (double)u[0], &mg);"),
 ]
+
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_tree_sample.py")
 
 
 def _run_mutated(tmp_root, src, idx, name, old, new):
@@ -48,12 +58,12 @@ def _run_mutated(tmp_root, src, idx, name, old, new):
         fh.write(src.replace(old, new))
     os.makedirs(os.path.join(d, "tests"))
     shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(d, "tests", "golden"))
-    for f in ("conftest.py", "test_oracle_pins.py"):
+    for f in ("conftest.py",) + PIN_FILES:
         shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(d, "tests", f))
     env = dict(os.environ, PYTHONPATH=d, PYTHONDONTWRITEBYTECODE="1", OMP_NUM_THREADS="1")
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "--rootdir", d,
-         os.path.join(d, "tests", "test_oracle_pins.py")],
+         *[os.path.join(d, "tests", f) for f in PIN_FILES]],
         cwd=d, env=env, capture_output=True, text=True, timeout=900,
     )
     return name, r.returncode, r.stdout[-1500:] + r.stderr[-1500:]

@@ -129,6 +129,32 @@ class SampleCase:
 
 
 @dataclass
+class TreeSampleCase:
+    name: str
+    dtype: str
+    logits: np.ndarray            # [B][N][V] target row of every node
+    draft: np.ndarray             # [B][N][V] draft row the children of every node came from
+    node_tokens: np.ndarray       # [B][N] int32 (node 0 = root, token unused)
+    parents: np.ndarray           # [B][N] int32
+    uniforms: np.ndarray          # [B][N] float32: u_0 final draw, u_j test of node j
+    max_depth: int
+    temperature: float
+    seed: int = 0
+
+    @property
+    def B(self) -> int:
+        return self.logits.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.logits.shape[1]
+
+    @property
+    def V(self) -> int:
+        return self.logits.shape[2]
+
+
+@dataclass
 class TreeCase:
     name: str
     dtype: str
@@ -309,3 +335,30 @@ def random_tree_case(B: int, N: int, V: int, max_depth: int, seed: int = 0, dtyp
         for j in range(1, N):
             tokens[b, j] = am[parents[b, j]] if rk.random() < p_match else rk.integers(0, V)
     return TreeCase(f"tree-B{B}-N{N}-V{V}", dtype, logits, tokens, parents, max_depth, seed)
+
+
+def tree_sample_case(B: int, N: int, V: int, max_depth: int, seed: int = 0, dtype: str = BF16,
+                     sigma: float = 3.0, noise: float = 1.0, temperature: float = 1.0,
+                     max_children: int = 4) -> TreeSampleCase:
+    """Draft tree for sampling verification: target rows NL ~ N(0, sigma^2),
+    draft rows DL = NL + N(0, noise^2) per node, breadth-first parents (as in
+    the greedy tree cases) and every child's token drawn from its parent's
+    draft distribution softmax(DL[parent] / T) by the Gumbel-max trick, so
+    siblings are independent draws from q."""
+    ss = np.random.SeedSequence([seed, B, N, V, max_depth, 7])
+    s_l, s_d, s_t, s_k, s_u = ss.spawn(5)
+    x = _rng(s_l).normal(0.0, sigma, size=(B, N, V)).astype(np.float32)
+    d = (x + _rng(s_d).normal(0.0, noise, size=(B, N, V))).astype(np.float32)
+    logits, draft = _cast(x, dtype), _cast(d, dtype)
+    rt = _rng(s_t)
+    parents = np.stack([tree_parents(rt, N, max_depth, max_children) for _ in range(B)])
+    rk = _rng(s_k)
+    tokens = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        rows = as_f32(draft[b]).astype(np.float64) / float(temperature)
+        for j in range(1, N):
+            g = -np.log(-np.log(rk.random(V, dtype=np.float64).clip(1e-300, None)))
+            tokens[b, j] = int(np.argmax(rows[parents[b, j]] + g))
+    uniforms = _rng(s_u).random((B, N), dtype=np.float32)
+    return TreeSampleCase(f"tree-sample-B{B}-N{N}-V{V}", dtype, logits, draft, tokens, parents, uniforms,
+                          max_depth, float(temperature), seed)
