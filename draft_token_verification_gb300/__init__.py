@@ -6,7 +6,7 @@ and the current stream.  The binding fails loudly if the library is missing:
 there is no CPU fallback.
 
 Entry points (same names as the C ABI in include/spec_verify.h):
-  spec_verify_sample, spec_verify_greedy, spec_verify_tree_greedy,
+  spec_verify_sample, spec_verify_greedy, spec_verify_tree_greedy, spec_verify_tree_sample,
   spec_verify_sample_noalloc, spec_transform_probs, spec_get_status, spec_verify_workspace_size,
   spec_error_string, spec_expected_tokens, spec_improvement_factor,
   spec_break_even_acceptance
@@ -51,7 +51,7 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
     "spec_transform_probs", "spec_get_status", "spec_error_string", "spec_expected_tokens",
     "spec_improvement_factor", "spec_break_even_acceptance", "spec_verify_sample_noalloc",
-    "spec_sample_launch_mode", "spec_best_gamma", "spec_first_draft_check",
+    "spec_sample_launch_mode", "spec_best_gamma", "spec_first_draft_check", "spec_verify_tree_sample",
 )
 SPEC_LAUNCH_SEPARATE = 0
 SPEC_LAUNCH_FUSED = 1
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_greedy.restype = I
             L.spec_verify_tree_greedy.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, SZ, P]
             L.spec_verify_tree_greedy.restype = I
+            L.spec_verify_tree_sample.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P, P, P, P, SZ, P]
+            L.spec_verify_tree_sample.restype = I
             L.spec_transform_probs.argtypes = [P, I, I, I, P, P, P, SZ, P]
             L.spec_transform_probs.restype = I
             L.spec_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -342,6 +344,37 @@ def spec_verify_tree_greedy(node_logits: torch.Tensor, node_tokens: torch.Tensor
         _dev(out_num_accepted, "out_num_accepted", torch.int32), ws.data_ptr(), ws.numel(), _stream(stream),
     )
     _check(rc, "spec_verify_tree_greedy")
+    return out_tokens, out_path, out_num_accepted
+
+
+def spec_verify_tree_sample(node_logits: torch.Tensor, draft_logits: torch.Tensor, node_tokens: torch.Tensor,
+                            parents: torch.Tensor, uniforms: torch.Tensor, max_depth: int,
+                            temperature: float = 1.0, out_tokens=None, out_path=None, out_num_accepted=None,
+                            workspace=None, stream=None):
+    """Token-tree sampling verification.  node_logits / draft_logits [B][N][V],
+    node_tokens / parents [B][N] int32, uniforms [B][N] float32 (u_0 the final
+    draw, u_j the test of node j).  Returns (tokens, path [B][max_depth+1], n [B])."""
+    B, N, V = node_logits.shape
+    if tuple(draft_logits.shape) != (B, N, V) or draft_logits.dtype != node_logits.dtype:
+        raise ValueError("draft_logits must match node_logits in shape and dtype")
+    dev = node_logits.device
+    D = int(max_depth) + 1
+    if out_tokens is None:
+        out_tokens = torch.empty((B, D), dtype=torch.int32, device=dev)
+    if out_path is None:
+        out_path = torch.empty((B, D), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    dt = _dtype_code(node_logits)
+    ws = _workspace(workspace, spec_verify_workspace_size(B, N - 1, V, dt), dev)
+    rc = lib().spec_verify_tree_sample(
+        _dev(node_logits, "node_logits"), _dev(draft_logits, "draft_logits"),
+        _dev(node_tokens, "node_tokens", torch.int32), _dev(parents, "parents", torch.int32),
+        _dev(uniforms, "uniforms", torch.float32), B, N, V, int(max_depth), dt, float(temperature),
+        _dev(out_tokens, "out_tokens", torch.int32), _dev(out_path, "out_path", torch.int32),
+        _dev(out_num_accepted, "out_num_accepted", torch.int32), ws.data_ptr(), ws.numel(), _stream(stream),
+    )
+    _check(rc, "spec_verify_tree_sample")
     return out_tokens, out_path, out_num_accepted
 
 

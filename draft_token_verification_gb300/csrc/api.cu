@@ -286,6 +286,55 @@ int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
   return SPEC_OK;
 }
 
+int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, const int32_t* node_tokens,
+                            const int32_t* parents, const float* uniforms, int B, int N, int V, int max_depth,
+                            spec_dtype dtype, float temperature, int32_t* out_tokens, int32_t* out_path,
+                            int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream) {
+  if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
+  if (!node_logits || !draft_logits || !node_tokens || !parents || !uniforms || !out_tokens || !out_path ||
+      !out_num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V || max_depth < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.f && isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  const size_t es = elt_bytes(dtype);
+  if (!aligned_to(node_logits, es) || !aligned_to(draft_logits, es) || !aligned_to(node_tokens, 4) ||
+      !aligned_to(parents, 4) || !aligned_to(uniforms, 4))
+    return SPEC_ERR_INVALID_ARG;
+  const int rc = check_workspace(workspace, workspace_bytes, B, N - 1);
+  if (rc != SPEC_OK) return rc;
+  // each CTA of a node's cluster holds 1/kTreeCl of both rows in shared memory
+  const int slice = ((V + kTreeCl - 1) / kTreeCl + 7) / 8 * 8;
+  if (tree_smem_bytes(dtype == SPEC_BF16 ? DT_BF16 : DT_F32, slice) > kTreeSmemMax) return SPEC_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(B, N - 1);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  TreeSampleArgs a = {};
+  a.logits = node_logits;
+  a.draft = draft_logits;
+  a.tokens = node_tokens;
+  a.parents = parents;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.N = N;
+  a.V = V;
+  a.max_depth = max_depth;
+  a.c = 1.4426950408889634f / temperature;  // log2(e) / T, as in the chain kernels
+  a.slice = slice;
+  a.wchunk = ((slice + kWarps - 1) / kWarps + 31) / 32 * 32;
+  a.aligned = rows_aligned(node_logits, V, dtype) && rows_aligned(draft_logits, V, dtype);
+  a.out_tokens = out_tokens;
+  a.out_path = out_path;
+  a.out_n = out_num_accepted;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status);
+  a.tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
+  a.recs = reinterpret_cast<TreeRec*>(w + L.trecs);
+  if (launch_tree_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, cuda_stream) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
 int spec_get_status(void* workspace, uint32_t* status, void* cuda_stream) {
   if (!workspace || !status) return SPEC_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);

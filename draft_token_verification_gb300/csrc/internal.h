@@ -76,6 +76,27 @@ struct RowPub {
 constexpr int kMaxDrawChunks = 16;
 constexpr int kChunkRec = 4 + 2 * kWarps;  // floats
 
+// Token-tree sampling verification runs one thread-block cluster of kTreeCl
+// CTAs per node: CTA r of the cluster holds elements [r*slice, (r+1)*slice)
+// of the node's target and draft rows in shared memory, and warp w of it the
+// chunk [w*wchunk, (w+1)*wchunk) of that slice.  A node leaves one TreeRec:
+// the first accepted child, or the residual it stops with and that
+// residual's per-chunk sums (the draw's first level).
+constexpr int kTreeCl = 8;
+constexpr int kTreeChunks = kTreeCl * kWarps;
+constexpr size_t kTreeSmemMax = 200 * 1024;  // dynamic shared memory of one tree CTA
+constexpr uint32_t kRecBad = 1u;        // a non-finite row at this node
+constexpr uint32_t kRecDepth = 2u;      // children not tested: the node is at max_depth
+constexpr uint32_t kRecDetached = 4u;   // a malformed parent on the way to the root
+struct TreeRec {
+  int32_t accepted;      // node id of the accepted child, or -1
+  uint32_t flags;        // kRec*
+  float nmp, nmq;        // -max * log2(e) / T of the target and draft rows
+  float fa, fb;          // stop residual weight: max(0, 2^(l c + nmp) fa - 2^(d c + nmq) fb)
+  int32_t pad[2];
+  double chunk[kTreeChunks];  // sums of that weight per (CTA, warp) chunk
+};
+
 // Workspace layout (byte offsets), identical for every call with the same
 // (B, k).  Tickets are zero between calls; everything else is written before
 // it is read within a call (the status word collects sticky bits until
@@ -92,6 +113,7 @@ struct WsLayout {
   size_t csums;       // float[B][kMaxDrawChunks][kChunkRec]  per-chunk draw sums
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
   size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
+  size_t trecs;       // TreeRec[B*(k+1)]  tree sampling: one record per node
   size_t total;
 };
 
@@ -114,7 +136,8 @@ constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   w.csums = align_up(w.pubs + sizeof(RowPub) * rows, 256);
   w.g_slots = align_up(w.csums + sizeof(float) * kChunkRec * static_cast<size_t>(kMaxDrawChunks) * B, 256);
   w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
-  w.total = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.trecs = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.total = align_up(w.trecs + sizeof(TreeRec) * units, 256);
   return w;
 }
 constexpr WsLayout ws_layout(int B, int k) {
@@ -156,6 +179,25 @@ struct SampleArgs {
   int mode;
 };
 
+struct TreeSampleArgs {
+  const void* logits;          // [B][N][V] target row of every node
+  const void* draft;           // [B][N][V] draft row the children of every node came from
+  const int32_t* tokens;       // [B][N]
+  const int32_t* parents;      // [B][N]
+  const float* uniforms;       // [B][N]
+  int B, N, V, max_depth;
+  float c;                     // log2(e) / T
+  int slice;                   // elements per CTA slice (multiple of 8)
+  int wchunk;                  // elements per warp chunk (multiple of 32)
+  int aligned;                 // rows start on 16-byte boundaries
+  int32_t* out_tokens;         // [B][max_depth+1]
+  int32_t* out_path;           // [B][max_depth+1]
+  int32_t* out_n;              // [B]
+  uint32_t* status;
+  uint32_t* tickets;           // [B] nodes finished per tree
+  TreeRec* recs;               // [B][N]
+};
+
 struct ArgmaxArgs {
   const void* logits;          // [B][R][V]
   const int32_t* tokens;       // chain: drafts [B][k]; tree: node tokens [B][N]
@@ -178,6 +220,9 @@ struct ArgmaxArgs {
 // and tail kernels, and the draw kernel in MODE_SAMPLE.
 int launch_sample(const SampleArgs& a, int dtype, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
+int launch_tree_sample(const TreeSampleArgs& a, int dtype, void* stream);
+// Shared-memory bytes of one tree-sampling CTA for slice `slice`.
+size_t tree_smem_bytes(int dtype, int slice);
 size_t sample_smem_bytes(int dtype, bool filter);
 int num_sms();
 

@@ -1,0 +1,652 @@
+// tree_sample_kernel.cu -- token-tree sampling verification.
+//
+// The accept-or-correct rule of speculative sampling (Edge Inference Notes,
+// post on speculative decoding and EAGLE-3, "The core idea: draft, then
+// check", step 3) applied down the branches of a draft tree ("One decode
+// round, end to end").  At a node v with target distribution p and draft
+// distribution q (temperature T), the children are tried in ascending node
+// order: child x is accepted iff u_x q(x) < r(x), where r starts as p and,
+// after each rejected child, becomes max(0, r - q) renormalised.  With
+// c_0 = 0, W_0 = 1 that residual is  r_m = max(0, p - c_m q) / W_m  with
+// c_{m+1} = c_m + W_m and W_{m+1} = sum_t max(0, p_t - c_{m+1} q_t); a mass of
+// zero puts r back to p.  When no child is accepted one token is drawn from r
+// (inverse CDF in ascending index order, uniform u_0).
+//
+// Which children a node accepts depends only on that node's rows, its
+// children's tokens and their uniforms, never on how the walk reached the
+// node.  So every node is decided independently and in parallel: one
+// thread-block cluster of kTreeCl CTAs per node holds the node's target and
+// draft rows in shared memory (CTA r a 1/kTreeCl slice of each), reduces the
+// row maxima and sums through distributed shared memory, then runs the
+// sibling loop, one residual-mass pass over the shared-memory slices per
+// rejected child.  A node that accepts no child records its stop residual's
+// per-chunk sums.  The cluster that finishes the last node of a tree (a
+// per-tree ticket) walks the accepted children from the root and draws the
+// correction at the stop node: chunk from the records, then the element
+// within the chunk from the rows.
+//
+// Masses are 2^(l c + nm) with c = log2(e)/T and nm = -max * c, one ex2 per
+// element; sums are float per lane and double across lanes, warps and CTAs,
+// always in the same order, so every CTA of a cluster takes the same
+// decisions.
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace specv {
+
+namespace {
+
+struct TreeShm {
+  double red[2][4];          // per-CTA values handed to the cluster, by round parity
+  double got[4];             // their cluster-wide combination
+  double wsum[kWarps][2];    // per-warp sums of the current pass
+  double zc[kWarps];         // per-warp sums of 2^(l c + nmp) (the c = 0 residual)
+  double wc[kWarps];         // per-warp sums of the last residual pass
+  float fmax[kWarps][2];
+  int bad[kWarps];
+  int16_t kids[kMaxTreeNodes];
+  int nk_w[kWarps];
+  int nk, has_child, depth, attached, accept, last;
+  int walk_v, walk_n, walk_ok, draw_w;
+  double draw_rem;
+};
+
+template <int DT>
+__device__ __forceinline__ bool bad_bits(uint32_t b) {
+  // NaN or +inf; -inf is an ordinary masked logit
+  if (DT == DT_BF16) return (b & 0x7F80u) == 0x7F80u && b != 0xFF80u;
+  return (b & 0x7F800000u) == 0x7F800000u && b != 0xFF800000u;
+}
+
+template <int DT>
+__device__ __forceinline__ float smem_val(uint32_t base, int i) {
+  if (DT == DT_BF16) return Elt<DT_BF16>::value(lds_u16(base + 2u * static_cast<uint32_t>(i)));
+  return __uint_as_float(lds_u32(base + 4u * static_cast<uint32_t>(i)));
+}
+
+// The residual weight of one element; the c = 0 residual (fb == 0) is the
+// target mass itself.  Used unchanged by the per-node passes and the draw.
+__device__ __forceinline__ float resid_weight(float l, float d, float c, float nmp, float nmq, float fa,
+                                              float fb) {
+  const float ep = ex2_approx(fmaf(l, c, nmp));
+  if (fb == 0.f) return ep;
+  const float eq = ex2_approx(fmaf(d, c, nmq));
+  return fmaxf(0.f, fmaf(ep, fa, -(eq * fb)));
+}
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
+  return v;  // lane 0
+}
+
+__device__ __forceinline__ float warp_max_f32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Combines the nv values thread 0 of every CTA left in sh.red[slot] across the
+// cluster, in rank order (sum, or max when is_max), into sh.got.  Every CTA
+// computes the same result bit for bit.
+__device__ void cluster_combine(TreeShm& sh, int slot, int nv, bool is_max) {
+  cg::this_cluster().sync();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    for (int i = 0; i < nv; ++i) {
+      double x = 0.0;
+      if (lane < kTreeCl) x = ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i]), lane));
+      double acc = __shfl_sync(0xFFFFFFFFu, x, 0);
+      for (int r = 1; r < kTreeCl; ++r) {
+        const double y = __shfl_sync(0xFFFFFFFFu, x, r);
+        acc = is_max ? fmax(acc, y) : acc + y;
+      }
+      if (lane == 0) sh.got[i] = acc;
+    }
+  }
+  __syncthreads();
+}
+
+// Children of node j that are tested, in ascending node order, into sh.kids
+// (sh.nk of them); sh.has_child tells whether j has any child at all.
+__device__ void collect_children(const TreeSampleArgs& a, TreeShm& sh, const int32_t* par, const int32_t* tok,
+                                 int j, bool testable) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int nk = 0, any = 0;
+  for (int base = j + 1; base < a.N; base += kThreads) {
+    const int jj = base + static_cast<int>(threadIdx.x);
+    const bool child = jj < a.N && par[jj] == j;
+    const bool ok = child && testable && tok[jj] >= 0 && tok[jj] < a.V;
+    any |= __syncthreads_or(child);
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
+    if (lane == 0) sh.nk_w[warp] = __popc(bal);
+    __syncthreads();
+    int before = nk, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) before += sh.nk_w[w];
+      total += sh.nk_w[w];
+    }
+    if (ok) sh.kids[before + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(jj);
+    nk += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    sh.nk = nk;
+    sh.has_child = any;
+  }
+  __syncthreads();
+}
+
+// Copies elements [lo, lo+len) of the target row (and of the draft row when
+// with_q) into shared memory and leaves this CTA's maxima and bad-value flags
+// in sh.red[slot] (thread 0): {max p, max q, bad p, bad q}.
+template <int DT>
+__device__ void load_slices(const TreeSampleArgs& a, TreeShm& sh, const unsigned char* prow,
+                            const unsigned char* qrow, int len, bool with_q, uint32_t sp, uint32_t sq,
+                            int slot) {
+  constexpr int E = Elt<DT>::kBytes;
+  constexpr int PV = Elt<DT>::kPerVec;
+  constexpr int kB = 4;  // vectors in flight per row and thread
+  float mp = -INFINITY, mq = -INFINITY;
+  int bp = 0, bq = 0;
+  if (a.aligned) {
+    const int nv = len / PV;  // aligned rows: len is a whole number of vectors
+    const uint4* ps = reinterpret_cast<const uint4*>(prow);
+    const uint4* qs = reinterpret_cast<const uint4*>(qrow);
+    for (int base = threadIdx.x; base < nv; base += kThreads * kB) {
+      uint4 vp[kB], vq[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = base + u * kThreads;
+        if (i < nv) {
+          vp[u] = ldg_stream(ps + i);
+          if (with_q) vq[u] = ldg_stream(qs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = base + u * kThreads;
+        if (i < nv) {
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sp + 16u * i), "r"(vp[u].x), "r"(vp[u].y),
+                       "r"(vp[u].z), "r"(vp[u].w)
+                       : "memory");
+#pragma unroll
+          for (int e = 0; e < PV; ++e) {
+            const uint32_t bits = Elt<DT>::bits_of(vp[u], e);
+            bp |= bad_bits<DT>(bits);
+            mp = fmaxf(mp, Elt<DT>::value(bits));
+          }
+          if (with_q) {
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sq + 16u * i), "r"(vq[u].x), "r"(vq[u].y),
+                         "r"(vq[u].z), "r"(vq[u].w)
+                         : "memory");
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+              const uint32_t bits = Elt<DT>::bits_of(vq[u], e);
+              bq |= bad_bits<DT>(bits);
+              mq = fmaxf(mq, Elt<DT>::value(bits));
+            }
+          }
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < len; i += kThreads) {
+      const uint32_t b1 = Elt<DT>::bits_at(prow, i);
+      bp |= bad_bits<DT>(b1);
+      mp = fmaxf(mp, Elt<DT>::value(b1));
+      if (E == 2) sts_u16(sp + 2u * i, b1); else sts_u32(sp + 4u * i, b1);
+      if (with_q) {
+        const uint32_t b2 = Elt<DT>::bits_at(qrow, i);
+        bq |= bad_bits<DT>(b2);
+        mq = fmaxf(mq, Elt<DT>::value(b2));
+        if (E == 2) sts_u16(sq + 2u * i, b2); else sts_u32(sq + 4u * i, b2);
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  mp = warp_max_f32(mp);
+  mq = warp_max_f32(mq);
+  bp = __any_sync(0xFFFFFFFFu, bp);
+  bq = __any_sync(0xFFFFFFFFu, bq);
+  if (lane == 0) {
+    sh.fmax[warp][0] = mp;
+    sh.fmax[warp][1] = mq;
+    sh.bad[warp] = bp | (bq << 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+    int bd = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      m0 = fmaxf(m0, sh.fmax[w][0]);
+      m1 = fmaxf(m1, sh.fmax[w][1]);
+      bd |= sh.bad[w];
+    }
+    sh.red[slot][0] = m0;
+    sh.red[slot][1] = m1;
+    sh.red[slot][2] = bd & 1;
+    sh.red[slot][3] = (bd >> 1) & 1;
+  }
+}
+
+// Sums over this CTA's slice, per warp chunk (lanes interleaved, float per
+// lane, double across lanes).  MODE 0: target and draft masses
+// (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
+template <int DT, int MODE>
+__device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
+                           float nmp, float nmq, float fa, float fb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wlo = warp * wchunk;
+  const int whi = min(len, wlo + wchunk);
+  float s0 = 0.f, s1 = 0.f;
+  for (int i = wlo + lane; i < whi; i += 32) {
+    const float l = smem_val<DT>(sp, i);
+    if (MODE == 0) {
+      s0 += ex2_approx(fmaf(l, c, nmp));
+      if (with_q) s1 += ex2_approx(fmaf(smem_val<DT>(sq, i), c, nmq));
+    } else {
+      s0 += resid_weight(l, smem_val<DT>(sq, i), c, nmp, nmq, fa, fb);
+    }
+  }
+  const double d0 = warp_sum_f64(static_cast<double>(s0));
+  const double d1 = MODE == 0 ? warp_sum_f64(static_cast<double>(s1)) : 0.0;
+  if (lane == 0) {
+    sh.wsum[warp][0] = d0;
+    sh.wsum[warp][1] = d1;
+  }
+  __syncthreads();
+}
+
+// The walk and the draw of tree b, by the whole CTA that finished the tree's
+// last node: follow the accepted children from the root, then draw from the
+// stop node's residual -- the chunk from its records (double prefix), the
+// warp sub-range and the element from its rows.
+template <int DT>
+__device__ void tree_draw(const TreeSampleArgs& a, TreeShm& sh, int b) {
+  constexpr int E = Elt<DT>::kBytes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int D = a.max_depth + 1;
+  int32_t* otok = a.out_tokens + static_cast<size_t>(b) * D;
+  int32_t* opath = a.out_path + static_cast<size_t>(b) * D;
+  const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
+  if (tid == 0) {
+    int v = 0, n = 0, ok = 1;
+    uint32_t st = 0;
+    for (int it = 0; it <= a.max_depth; ++it) {
+      const TreeRec* r = a.recs + static_cast<size_t>(b) * a.N + v;
+      const uint32_t fl = __ldcg(&r->flags);
+      const int acc = __ldcg(&r->accepted);
+      if (fl & (kRecBad | kRecDetached)) {
+        ok = 0;
+        st |= SPEC_STATUS_BAD_ROW;
+        break;
+      }
+      if (acc >= 0) {
+        if (n >= a.max_depth) {  // not reachable: children at max_depth are never tested
+          ok = 0;
+          break;
+        }
+        opath[n] = acc;
+        otok[n] = tok[acc];
+        ++n;
+        v = acc;
+        continue;
+      }
+      if (fl & kRecDepth) st |= SPEC_STATUS_DEPTH;
+      break;
+    }
+    if (st) atomicOr(a.status, st);
+    sh.walk_v = v;
+    sh.walk_n = n;
+    sh.walk_ok = ok;
+  }
+  __syncthreads();
+  const int v = sh.walk_v, n = sh.walk_n;
+  for (int i = tid; i < D; i += kThreads) {
+    if (i > n) otok[i] = -1;
+    if (i >= n) opath[i] = -1;
+  }
+  if (!sh.walk_ok) {
+    if (tid == 0) {
+      otok[n] = -1;
+      a.out_n[b] = n;
+    }
+    __syncthreads();
+    return;
+  }
+  const size_t g = static_cast<size_t>(b) * a.N + v;
+  const TreeRec* r = a.recs + g;
+  const float nmp = __ldcg(&r->nmp), nmq = __ldcg(&r->nmq), fa = __ldcg(&r->fa), fb = __ldcg(&r->fb);
+  const unsigned char* lrow = static_cast<const unsigned char*>(a.logits) + g * a.V * E;
+  const unsigned char* drow = static_cast<const unsigned char*>(a.draft) + g * a.V * E;
+  if (warp == 0) {
+    // chunk: lane L holds chunks 2L and 2L+1
+    const double c0 = __ldcg(&r->chunk[2 * lane]), c1 = __ldcg(&r->chunk[2 * lane + 1]);
+    double incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const double target = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N]) * total;
+    const uint32_t over = __ballot_sync(0xFFFFFFFFu, incl > target);
+    const uint32_t pos = __ballot_sync(0xFFFFFFFFu, c0 > 0.0 || c1 > 0.0);
+    int l = -1;
+    if (over) l = __ffs(over) - 1;
+    else if (pos) l = 31 - __clz(pos);
+    int ci = -1;
+    double rem = 0.0;
+    if (l >= 0) {
+      const double ex = __shfl_sync(0xFFFFFFFFu, incl - (c0 + c1), l);
+      const double a0 = __shfl_sync(0xFFFFFFFFu, c0, l), a1 = __shfl_sync(0xFFFFFFFFu, c1, l);
+      if (over) {
+        ci = (ex + a0 > target || a1 <= 0.0) ? 2 * l : 2 * l + 1;
+      } else {
+        ci = a1 > 0.0 ? 2 * l + 1 : 2 * l;
+      }
+      rem = target - (ci & 1 ? ex + a0 : ex);
+    }
+    if (lane == 0) {
+      sh.draw_w = ci;
+      sh.draw_rem = rem;
+    }
+  }
+  __syncthreads();
+  const int ci = sh.draw_w;
+  if (ci < 0) {  // no positive weight anywhere: nothing to draw from
+    if (tid == 0) {
+      otok[n] = -1;
+      a.out_n[b] = n;
+      atomicOr(a.status, SPEC_STATUS_BAD_ROW);
+    }
+    __syncthreads();
+    return;
+  }
+  const int cr = ci / kWarps, cw = ci % kWarps;
+  const int slo = cr * a.slice;
+  const int slen = max(0, min(a.V, slo + a.slice) - slo);
+  const int clo = slo + min(slen, cw * a.wchunk);
+  const int chi = slo + min(slen, (cw + 1) * a.wchunk);
+  const int sub = ((chi - clo + kWarps - 1) / kWarps + 31) / 32 * 32;
+  {
+    const int wlo = min(chi, clo + warp * sub), whi = min(chi, clo + (warp + 1) * sub);
+    float s = 0.f;
+    for (int t = wlo + lane; t < whi; t += 32)
+      s += resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
+                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp, nmq, fa, fb);
+    const double ws = warp_sum_f64(static_cast<double>(s));
+    if (lane == 0) sh.wsum[warp][0] = ws;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const double rem = sh.draw_rem;
+    double cum = 0.0;
+    int pick = -1, lastpos = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const double s = sh.wsum[w][0];
+      if (s > 0.0) lastpos = w;
+      if (cum + s > rem && s > 0.0) {
+        pick = w;
+        break;
+      }
+      cum += s;
+    }
+    if (pick < 0) {
+      pick = lastpos;
+      sh.draw_rem = INFINITY;  // past every element: the last positive one
+    } else {
+      sh.draw_rem = rem - cum;
+    }
+    sh.walk_v = pick;
+  }
+  __syncthreads();
+  const int pick = sh.walk_v;
+  if (warp == (pick < 0 ? 0 : pick)) {
+    int token = -1;
+    if (pick >= 0) {
+      const double rem = sh.draw_rem;
+      const int wlo = min(chi, clo + pick * sub), whi = min(chi, clo + (pick + 1) * sub);
+      double acc = 0.0;
+      for (int base = wlo; base < whi; base += 32) {
+        const int t = base + lane;
+        float w = 0.f;
+        if (t < whi)
+          w = resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
+                           fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp, nmq, fa, fb);
+        double incl = static_cast<double>(w);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, w > 0.f && acc + incl > rem);
+        const uint32_t pos = __ballot_sync(0xFFFFFFFFu, w > 0.f);
+        if (pos) token = base + 31 - __clz(pos);
+        if (hit) {
+          token = base + __ffs(hit) - 1;
+          break;
+        }
+        acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      otok[n] = token;
+      a.out_n[b] = n;
+      if (token < 0) atomicOr(a.status, SPEC_STATUS_BAD_ROW);
+    }
+  }
+  __syncthreads();
+}
+
+// One cluster of kTreeCl CTAs per node, clusters looping over the B*N nodes.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSampleArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ TreeShm sh;
+  constexpr int E = Elt<DT>::kBytes;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int ncl = gridDim.x / kTreeCl;
+  const int cid = blockIdx.x / kTreeCl;
+  const uint32_t sp = smem_addr(dyn);
+  const uint32_t sq = sp + static_cast<uint32_t>(a.slice) * E;
+  const int lo = rank * a.slice;
+  const int len = max(0, min(a.V, lo + a.slice) - lo);
+  const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
+  int round = 0;
+  for (int64_t g = cid; g < nodes; g += ncl) {
+    const int b = static_cast<int>(g / a.N), j = static_cast<int>(g % a.N);
+    const int32_t* par = a.parents + static_cast<size_t>(b) * a.N;
+    const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
+    TreeRec* rec = a.recs + g;
+    if (threadIdx.x == 0) {
+      int d = 0, v = j, att = 1;
+      while (v != 0) {  // parents strictly decrease, so this ends within j steps
+        const int pv = par[v];
+        if (pv < 0 || pv >= v) {
+          att = 0;
+          break;
+        }
+        v = pv;
+        ++d;
+      }
+      sh.depth = d;
+      sh.attached = att;
+      if (rank == 0) {
+        uint32_t st = 0;
+        if (j == 0 ? par[0] != -1 : (par[j] < 0 || par[j] >= j)) st |= SPEC_STATUS_BAD_PARENT;
+        if (j > 0 && (tok[j] < 0 || tok[j] >= a.V)) st |= SPEC_STATUS_BAD_TOKEN;
+        if (st) atomicOr(a.status, st);
+      }
+    }
+    __syncthreads();
+    uint32_t rflags = 0;
+    int accepted = -1;
+    bool cz = true;
+    float fa = 1.f, fb = 0.f, nmp = 0.f, nmq = 0.f;
+    if (!sh.attached) {
+      rflags = kRecDetached;
+    } else {
+      const bool testable = sh.depth < a.max_depth;
+      collect_children(a, sh, par, tok, j, testable);
+      const int nk = sh.nk;
+      if (sh.has_child && !testable) rflags |= kRecDepth;
+      const bool with_q = nk > 0;
+      const size_t rowoff = (static_cast<size_t>(g) * a.V + lo) * E;
+      const unsigned char* prow = static_cast<const unsigned char*>(a.logits) + rowoff;
+      const unsigned char* qrow = static_cast<const unsigned char*>(a.draft) + rowoff;
+      int slot = round++ & 1;
+      load_slices<DT>(a, sh, prow, qrow, len, with_q, sp, sq, slot);
+      cluster_combine(sh, slot, 4, true);
+      const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[1]);
+      const bool bad = sh.got[2] != 0.0 || mp == -INFINITY || (with_q && (sh.got[3] != 0.0 || mq == -INFINITY));
+      if (bad) {
+        rflags |= kRecBad;
+      } else {
+        nmp = -mp * a.c;
+        nmq = with_q ? -mq * a.c : 0.f;
+        slice_pass<DT, 0>(sh, sp, sq, len, a.wchunk, with_q, a.c, nmp, nmq, 0.f, 0.f);
+        slot = round++ & 1;
+        if (threadIdx.x == 0) {
+          double z0 = 0.0, z1 = 0.0;
+          for (int w = 0; w < kWarps; ++w) {
+            sh.zc[w] = sh.wsum[w][0];
+            z0 += sh.wsum[w][0];
+            z1 += sh.wsum[w][1];
+          }
+          sh.red[slot][0] = z0;
+          sh.red[slot][1] = z1;
+        }
+        cluster_combine(sh, slot, 2, false);
+        const double zp = sh.got[0], zq = sh.got[1];
+        const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
+        const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
+        double cc = 0.0, W = 1.0;
+        for (int i = 0; i < nk; ++i) {
+          const int child = sh.kids[i];
+          if (threadIdx.x == 0) {
+            const int x = tok[child];
+            const double px =
+                static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(pfull, x)), a.c, nmp))) / zp;
+            const double qx =
+                static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(qfull, x)), a.c, nmq))) / zq;
+            const double u = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N + child]);
+            sh.accept = u * qx * W < px - cc * qx;
+          }
+          __syncthreads();
+          if (sh.accept) {
+            accepted = child;
+            break;
+          }
+          cc += W;
+          fa = static_cast<float>(1.0 / zp);
+          fb = static_cast<float>(cc / zq);
+          slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+          slot = round++ & 1;
+          if (threadIdx.x == 0) {
+            double s = 0.0;
+            for (int w = 0; w < kWarps; ++w) {
+              sh.wc[w] = sh.wsum[w][0];
+              s += sh.wsum[w][0];
+            }
+            sh.red[slot][0] = s;
+          }
+          cluster_combine(sh, slot, 1, false);
+          const double wn = sh.got[0];
+          if (wn > 0.0) {
+            W = wn;
+            cz = false;
+          } else {  // residual of mass zero: back to p
+            W = 1.0;
+            cc = 0.0;
+            cz = true;
+          }
+        }
+        if (accepted < 0 && threadIdx.x < kWarps)
+          rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] : sh.wc[threadIdx.x];
+      }
+    }
+    if (rank == 0 && threadIdx.x == 0) {
+      rec->accepted = accepted;
+      rec->flags = rflags;
+      rec->nmp = nmp;
+      rec->nmq = nmq;
+      rec->fa = cz ? 1.f : fa;
+      rec->fb = cz ? 0.f : fb;
+    }
+    __threadfence();
+    cluster.sync();
+    if (rank == 0) {
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t t = atomicAdd(&a.tickets[b], 1u);
+        sh.last = t == static_cast<uint32_t>(a.N - 1);
+        if (sh.last) atomicExch(&a.tickets[b], 0u);  // every node of the tree has counted in
+      }
+      __syncthreads();
+      if (sh.last) {
+        __threadfence();
+        tree_draw<DT>(a, sh, b);
+      }
+    }
+  }
+  cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
+template <int DT>
+int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
+  static int cached_smem[2] = {-1, -1}, cached_clusters[2] = {0, 0}, cached_dev[2] = {-1, -1};
+  const size_t smem = tree_smem_bytes(DT, a.slice);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto kern = tree_node_kernel<DT>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTreeCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cached_smem[DT] != static_cast<int>(smem) || cached_dev[DT] != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(kTreeCl);
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (ncl < 1) return cudaErrorInvalidConfiguration;
+    cached_smem[DT] = static_cast<int>(smem);
+    cached_clusters[DT] = ncl;
+    cached_dev[DT] = dev;
+  }
+  const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
+  const int clusters = static_cast<int>(nodes < cached_clusters[DT] ? nodes : cached_clusters[DT]);
+  cfg.gridDim = dim3(clusters * kTreeCl);
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+size_t tree_smem_bytes(int dtype, int slice) {
+  return 2 * static_cast<size_t>(slice) * (dtype == DT_BF16 ? 2 : 4);
+}
+
+int launch_tree_sample(const TreeSampleArgs& a, int dtype, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return dtype == DT_BF16 ? launch_tree_t<DT_BF16>(a, st) : launch_tree_t<DT_F32>(a, st);
+}
+
+}  // namespace specv

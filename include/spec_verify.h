@@ -96,7 +96,8 @@ typedef struct {
 
 /*
  * Workspace bytes needed by spec_verify_sample / spec_verify_greedy for B
- * sequences of k drafts, and by spec_verify_tree_greedy with k = N - 1 and
+ * sequences of k drafts, by spec_verify_tree_greedy and spec_verify_tree_sample
+ * with k = N - 1, and by
  * spec_transform_probs with B = R rows and k = 0.  Returns 0 for sizes
  * outside the limits.
  */
@@ -189,6 +190,49 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
 int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
                             const int32_t* parents, int B, int N, int V, int max_depth,
                             spec_dtype dtype, int32_t* out_tokens, int32_t* out_path,
+                            int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream);
+
+/*
+ * Token-tree sampling verification ([EIN] "One decode round, end to end":
+ * the accept-or-correct rule of "The core idea: draft, then check" applied
+ * down the branches).  Per tree, from the root (node 0):
+ *   p = softmax(node_logits[v] / T), q = softmax(draft_logits[v] / T), r = p;
+ *   for each child j of v (parents[j] == v) in ascending node order:
+ *     accept j iff u_j * q(x_j) < r(x_j)  -> commit x_j, v = j, start again;
+ *     else r = max(0, r - q) / sum(max(0, r - q))  (r = p if that sum is 0);
+ *   no child accepted: draw one token from r with u_0 (smallest index whose
+ *   running sum exceeds u_0 * S) and stop.
+ * The pages give the rule for a chain; the sibling rule above is the reading
+ * taken for several children (each rejected child removes q from the
+ * residual), which keeps the output distributed as p when the children of a
+ * node are independent draws from q.  Temperature only (no top-k / top-p).
+ *   node_logits   [B][N][V] dtype  target row of every node (row j: the
+ *                                  distribution of the token after node j)
+ *   draft_logits  [B][N][V] dtype  draft row of every node (row j: the
+ *                                  distribution the children of j were drawn
+ *                                  from; rows of leaves are not read)
+ *   node_tokens, parents [B][N]    as for spec_verify_tree_greedy
+ *   uniforms      [B][N] float     in [0, 1): u_0 the final draw, u_j (j >= 1)
+ *                                  the accept test of node j
+ *   temperature   T > 0
+ *   out_tokens    [B][max_depth+1] path tokens (root excluded), the drawn
+ *                                  token, then -1
+ *   out_path      [B][max_depth+1] path node ids, -1 padded (the KV keep list)
+ *   out_num_accepted [B]           accepted nodes n (n + 1 tokens committed)
+ * Children of a node at depth max_depth are not tested (SPEC_STATUS_DEPTH if
+ * the walk stops there).  A child whose token is outside [0, V) is skipped
+ * and sets SPEC_STATUS_BAD_TOKEN; a malformed parent entry detaches that node
+ * and sets SPEC_STATUS_BAD_PARENT; a non-finite row on the walk ends it with
+ * drawn token -1 and SPEC_STATUS_BAD_ROW.
+ * Workspace: spec_verify_workspace_size(B, N - 1, V, dtype), left zeroed.
+ * Returns SPEC_ERR_UNSUPPORTED when a CTA's share of the two rows, 2 *
+ * ceil(V / 8) elements, exceeds 200 KiB of shared memory (V > 204800 f32 or
+ * 409600 bf16).
+ */
+int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, const int32_t* node_tokens,
+                            const int32_t* parents, const float* uniforms, int B, int N, int V, int max_depth,
+                            spec_dtype dtype, float temperature, int32_t* out_tokens, int32_t* out_path,
                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                             void* cuda_stream);
 
