@@ -321,13 +321,14 @@ int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, c
   a.max_depth = max_depth;
   a.c = 1.4426950408889634f / temperature;  // log2(e) / T, as in the chain kernels
   a.slice = slice;
-  a.wchunk = ((slice + kWarps - 1) / kWarps + 31) / 32 * 32;
+  // warp chunks are whole rounds of 32 lanes x one 16-byte vector
+  const int round_elems = 32 * vec_elems(dtype);
+  a.wchunk = ((slice + kWarps - 1) / kWarps + round_elems - 1) / round_elems * round_elems;
   a.aligned = rows_aligned(node_logits, V, dtype) && rows_aligned(draft_logits, V, dtype);
   a.out_tokens = out_tokens;
   a.out_path = out_path;
   a.out_n = out_num_accepted;
   a.status = reinterpret_cast<uint32_t*>(w + L.status);
-  a.tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
   a.recs = reinterpret_cast<TreeRec*>(w + L.trecs);
   if (launch_tree_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, cuda_stream) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)

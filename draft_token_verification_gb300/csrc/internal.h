@@ -81,13 +81,15 @@ constexpr int kChunkRec = 4 + 2 * kWarps;  // floats
 // of the node's target and draft rows in shared memory, and warp w of it the
 // chunk [w*wchunk, (w+1)*wchunk) of that slice.  A node leaves one TreeRec:
 // the first accepted child, or the residual it stops with and that
-// residual's per-chunk sums (the draw's first level).
+// residual's per-chunk sums (the draw's first level); a node without children
+// to test leaves only its flags.
 constexpr int kTreeCl = 8;
 constexpr int kTreeChunks = kTreeCl * kWarps;
 constexpr size_t kTreeSmemMax = 200 * 1024;  // dynamic shared memory of one tree CTA
 constexpr uint32_t kRecBad = 1u;        // a non-finite row at this node
 constexpr uint32_t kRecDepth = 2u;      // children not tested: the node is at max_depth
 constexpr uint32_t kRecDetached = 4u;   // a malformed parent on the way to the root
+constexpr uint32_t kRecDefer = 8u;      // no child to test: the stop residual is p, summed by the walk
 struct TreeRec {
   int32_t accepted;      // node id of the accepted child, or -1
   uint32_t flags;        // kRec*
@@ -188,13 +190,12 @@ struct TreeSampleArgs {
   int B, N, V, max_depth;
   float c;                     // log2(e) / T
   int slice;                   // elements per CTA slice (multiple of 8)
-  int wchunk;                  // elements per warp chunk (multiple of 32)
+  int wchunk;                  // elements per warp chunk (multiple of 32 vectors)
   int aligned;                 // rows start on 16-byte boundaries
   int32_t* out_tokens;         // [B][max_depth+1]
   int32_t* out_path;           // [B][max_depth+1]
   int32_t* out_n;              // [B]
   uint32_t* status;
-  uint32_t* tickets;           // [B] nodes finished per tree
   TreeRec* recs;               // [B][N]
 };
 

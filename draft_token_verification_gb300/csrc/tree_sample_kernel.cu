@@ -14,16 +14,18 @@
 //
 // Which children a node accepts depends only on that node's rows, its
 // children's tokens and their uniforms, never on how the walk reached the
-// node.  So every node is decided independently and in parallel: one
-// thread-block cluster of kTreeCl CTAs per node holds the node's target and
-// draft rows in shared memory (CTA r a 1/kTreeCl slice of each), reduces the
-// row maxima and sums through distributed shared memory, then runs the
-// sibling loop, one residual-mass pass over the shared-memory slices per
-// rejected child.  A node that accepts no child records its stop residual's
-// per-chunk sums.  The cluster that finishes the last node of a tree (a
-// per-tree ticket) walks the accepted children from the root and draws the
-// correction at the stop node: chunk from the records, then the element
-// within the chunk from the rows.
+// node.  So every node with children to test is decided independently and in
+// parallel (tree_node_kernel): one thread-block cluster of kTreeCl CTAs per
+// node copies the node's target and draft rows into shared memory (bulk
+// copies, CTA r a 1/kTreeCl slice of each), reduces the row maxima and masses
+// through distributed shared memory, then runs the sibling loop, one
+// residual-mass pass over the shared-memory slices per rejected child.  A
+// node that accepts no child records its stop residual's per-chunk sums.
+// Nodes without children to test are only marked: their stop distribution
+// is p itself.  tree_walk_kernel (one cluster per tree) then follows the
+// accepted children from the root; if the walk stops at a marked node, the
+// cluster computes that node's p chunk sums, and the correction is drawn:
+// the chunk from the sums, the element within it from the rows.
 //
 // Masses are 2^(l c + nm) with c = log2(e)/T and nm = -max * c, one ex2 per
 // element; sums are float per lane and double across lanes, warps and CTAs,
@@ -42,7 +44,11 @@ namespace specv {
 
 namespace {
 
+constexpr uint32_t kPiece = 16384;  // bytes per bulk copy
+constexpr int16_t kNoParent = -2;   // a parent entry outside [-1, N)
+
 struct TreeShm {
+  uint64_t bar[2];           // bulk-copy completion: target slice, draft slice
   double red[2][4];          // per-CTA values handed to the cluster, by round parity
   double got[4];             // their cluster-wide combination
   double wsum[kWarps][2];    // per-warp sums of the current pass
@@ -51,8 +57,9 @@ struct TreeShm {
   float fmax[kWarps][2];
   int bad[kWarps];
   int16_t kids[kMaxTreeNodes];
+  int16_t par[kMaxTreeNodes];
   int nk_w[kWarps];
-  int nk, has_child, depth, attached, accept, last;
+  int nk, has_child, depth, attached, accept, timed_out;
   int walk_v, walk_n, walk_ok, draw_w;
   double draw_rem;
 };
@@ -115,13 +122,12 @@ __device__ void cluster_combine(TreeShm& sh, int slot, int nv, bool is_max) {
 
 // Children of node j that are tested, in ascending node order, into sh.kids
 // (sh.nk of them); sh.has_child tells whether j has any child at all.
-__device__ void collect_children(const TreeSampleArgs& a, TreeShm& sh, const int32_t* par, const int32_t* tok,
-                                 int j, bool testable) {
+__device__ void collect_children(const TreeSampleArgs& a, TreeShm& sh, const int32_t* tok, int j, bool testable) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int nk = 0, any = 0;
   for (int base = j + 1; base < a.N; base += kThreads) {
     const int jj = base + static_cast<int>(threadIdx.x);
-    const bool child = jj < a.N && par[jj] == j;
+    const bool child = jj < a.N && sh.par[jj] == j;
     const bool ok = child && testable && tok[jj] >= 0 && tok[jj] < a.V;
     any |= __syncthreads_or(child);
     const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ok);
@@ -143,55 +149,62 @@ __device__ void collect_children(const TreeSampleArgs& a, TreeShm& sh, const int
   __syncthreads();
 }
 
+// Thread 0: `bytes` from global src to shared dst by bulk copies completing on bar.
+__device__ __forceinline__ void bulk_issue(uint64_t* bar, uint32_t dst, const unsigned char* src, uint32_t bytes) {
+  mbar_arrive_expect_tx(bar, bytes);
+  for (uint32_t off = 0; off < bytes; off += kPiece)
+    bulk_copy_g2s_addr(dst + off, src + off, bytes - off < kPiece ? bytes - off : kPiece, bar);
+}
+
 // Copies elements [lo, lo+len) of the target row (and of the draft row when
-// with_q) into shared memory and leaves this CTA's maxima and bad-value flags
-// in sh.red[slot] (thread 0): {max p, max q, bad p, bad q}.
+// with_q) into shared memory -- bulk copies for 16-byte aligned rows, plain
+// loads otherwise -- and leaves this CTA's maxima and bad-value flags in
+// sh.red[slot] (thread 0): {max p, max q, bad p, bad q}.  A copy that does
+// not complete within the bounded wait marks the slice bad and sets
+// SPEC_STATUS_TIMEOUT; that CTA copies nothing more.
 template <int DT>
-__device__ void load_slices(const TreeSampleArgs& a, TreeShm& sh, const unsigned char* prow,
-                            const unsigned char* qrow, int len, bool with_q, uint32_t sp, uint32_t sq,
-                            int slot) {
+__device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned char* prow,
+                           const unsigned char* qrow, int len, bool with_q, uint32_t sp, uint32_t sq,
+                           uint32_t& php, uint32_t& phq, int slot) {
   constexpr int E = Elt<DT>::kBytes;
   constexpr int PV = Elt<DT>::kPerVec;
-  constexpr int kB = 4;  // vectors in flight per row and thread
   float mp = -INFINITY, mq = -INFINITY;
-  int bp = 0, bq = 0;
+  int bp = 0, bq = 0, tmo = 0;
   if (a.aligned) {
-    const int nv = len / PV;  // aligned rows: len is a whole number of vectors
-    const uint4* ps = reinterpret_cast<const uint4*>(prow);
-    const uint4* qs = reinterpret_cast<const uint4*>(qrow);
-    for (int base = threadIdx.x; base < nv; base += kThreads * kB) {
-      uint4 vp[kB], vq[kB];
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int i = base + u * kThreads;
-        if (i < nv) {
-          vp[u] = ldg_stream(ps + i);
-          if (with_q) vq[u] = ldg_stream(qs + i);
-        }
+    const bool skip = sh.timed_out != 0;
+    if (threadIdx.x == 0 && !skip) {
+      fence_proxy_async_smem();  // earlier reads of these slices come before the copies' writes
+      bulk_issue(&sh.bar[0], sp, prow, static_cast<uint32_t>(len) * E);
+      if (with_q) bulk_issue(&sh.bar[1], sq, qrow, static_cast<uint32_t>(len) * E);
+    }
+    bool ok = !skip;
+    if (ok) {
+      ok = mbar_wait_bounded(&sh.bar[0], php);
+      php ^= 1u;
+      if (with_q) {
+        ok = mbar_wait_bounded(&sh.bar[1], phq) && ok;
+        phq ^= 1u;
       }
+    }
+    if (!ok) {
+      tmo = 1;
+    } else {
+      const int nv = len / PV;  // aligned rows: len is a whole number of vectors
+      for (int v = threadIdx.x; v < nv; v += kThreads) {
+        const uint4 x = lds128(sp + 16u * v);
 #pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int i = base + u * kThreads;
-        if (i < nv) {
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sp + 16u * i), "r"(vp[u].x), "r"(vp[u].y),
-                       "r"(vp[u].z), "r"(vp[u].w)
-                       : "memory");
+        for (int e = 0; e < PV; ++e) {
+          const uint32_t bits = Elt<DT>::bits_of(x, e);
+          bp |= bad_bits<DT>(bits);
+          mp = fmaxf(mp, Elt<DT>::value(bits));
+        }
+        if (with_q) {
+          const uint4 y = lds128(sq + 16u * v);
 #pragma unroll
           for (int e = 0; e < PV; ++e) {
-            const uint32_t bits = Elt<DT>::bits_of(vp[u], e);
-            bp |= bad_bits<DT>(bits);
-            mp = fmaxf(mp, Elt<DT>::value(bits));
-          }
-          if (with_q) {
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sq + 16u * i), "r"(vq[u].x), "r"(vq[u].y),
-                         "r"(vq[u].z), "r"(vq[u].w)
-                         : "memory");
-#pragma unroll
-            for (int e = 0; e < PV; ++e) {
-              const uint32_t bits = Elt<DT>::bits_of(vq[u], e);
-              bq |= bad_bits<DT>(bits);
-              mq = fmaxf(mq, Elt<DT>::value(bits));
-            }
+            const uint32_t bits = Elt<DT>::bits_of(y, e);
+            bq |= bad_bits<DT>(bits);
+            mq = fmaxf(mq, Elt<DT>::value(bits));
           }
         }
       }
@@ -215,10 +228,11 @@ __device__ void load_slices(const TreeSampleArgs& a, TreeShm& sh, const unsigned
   mq = warp_max_f32(mq);
   bp = __any_sync(0xFFFFFFFFu, bp);
   bq = __any_sync(0xFFFFFFFFu, bq);
+  tmo = __any_sync(0xFFFFFFFFu, tmo);
   if (lane == 0) {
     sh.fmax[warp][0] = mp;
     sh.fmax[warp][1] = mq;
-    sh.bad[warp] = bp | (bq << 1);
+    sh.bad[warp] = bp | (bq << 1) | (tmo << 2);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -229,6 +243,11 @@ __device__ void load_slices(const TreeSampleArgs& a, TreeShm& sh, const unsigned
       m1 = fmaxf(m1, sh.fmax[w][1]);
       bd |= sh.bad[w];
     }
+    if ((bd & 4) || (a.aligned && sh.timed_out)) {  // no data this time: the slice counts as bad
+      if (!sh.timed_out) atomicOr(a.status, SPEC_STATUS_TIMEOUT);
+      sh.timed_out = 1;
+      bd |= 1;
+    }
     sh.red[slot][0] = m0;
     sh.red[slot][1] = m1;
     sh.red[slot][2] = bd & 1;
@@ -236,23 +255,32 @@ __device__ void load_slices(const TreeSampleArgs& a, TreeShm& sh, const unsigned
   }
 }
 
-// Sums over this CTA's slice, per warp chunk (lanes interleaved, float per
-// lane, double across lanes).  MODE 0: target and draft masses
-// (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
+// Sums over this CTA's slice, per warp chunk (16-byte vectors, lanes
+// interleaved, float per lane, double across lanes).  MODE 0: target and
+// draft masses (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
 template <int DT, int MODE>
 __device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
                            float nmp, float nmq, float fa, float fb) {
+  constexpr int PV = Elt<DT>::kPerVec;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wlo = warp * wchunk;
   const int whi = min(len, wlo + wchunk);
   float s0 = 0.f, s1 = 0.f;
-  for (int i = wlo + lane; i < whi; i += 32) {
-    const float l = smem_val<DT>(sp, i);
-    if (MODE == 0) {
-      s0 += ex2_approx(fmaf(l, c, nmp));
-      if (with_q) s1 += ex2_approx(fmaf(smem_val<DT>(sq, i), c, nmq));
-    } else {
-      s0 += resid_weight(l, smem_val<DT>(sq, i), c, nmp, nmq, fa, fb);
+  for (int i0 = wlo + lane * PV; i0 < whi; i0 += 32 * PV) {
+    const uint4 x = lds128(sp + 16u * static_cast<uint32_t>(i0 / PV));
+    uint4 y = make_uint4(0u, 0u, 0u, 0u);
+    if (MODE == 1 || with_q) y = lds128(sq + 16u * static_cast<uint32_t>(i0 / PV));
+#pragma unroll
+    for (int e = 0; e < PV; ++e) {
+      if (i0 + e < whi) {
+        const float l = Elt<DT>::value(Elt<DT>::bits_of(x, e));
+        if (MODE == 0) {
+          s0 += ex2_approx(fmaf(l, c, nmp));
+          if (with_q) s1 += ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_of(y, e)), c, nmq));
+        } else {
+          s0 += resid_weight(l, Elt<DT>::value(Elt<DT>::bits_of(y, e)), c, nmp, nmq, fa, fb);
+        }
+      }
     }
   }
   const double d0 = warp_sum_f64(static_cast<double>(s0));
@@ -264,63 +292,41 @@ __device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int w
   __syncthreads();
 }
 
-// The walk and the draw of tree b, by the whole CTA that finished the tree's
-// last node: follow the accepted children from the root, then draw from the
-// stop node's residual -- the chunk from its records (double prefix), the
-// warp sub-range and the element from its rows.
+// Parents of tree b into sh.par (entries outside [-1, N) become kNoParent),
+// then, by thread 0, the depth of node j and whether its path reaches the root.
+__device__ void tree_header(const TreeSampleArgs& a, TreeShm& sh, int b, int j) {
+  const int32_t* par = a.parents + static_cast<size_t>(b) * a.N;
+  for (int i = threadIdx.x; i < a.N; i += kThreads) {
+    const int p = par[i];
+    sh.par[i] = static_cast<int16_t>(p >= -1 && p < a.N ? p : kNoParent);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int d = 0, v = j, att = 1;
+    while (v != 0) {  // parents strictly decrease, so this ends within j steps
+      const int pv = sh.par[v];
+      if (pv < 0 || pv >= v) {
+        att = 0;
+        break;
+      }
+      v = pv;
+      ++d;
+    }
+    sh.depth = d;
+    sh.attached = att;
+  }
+  __syncthreads();
+}
+
+// The correction drawn at stop node v of tree b (n nodes accepted) by one
+// CTA: the chunk from the node's record (double prefix over its chunk sums),
+// the warp sub-range and the element from the node's rows.
 template <int DT>
-__device__ void tree_draw(const TreeSampleArgs& a, TreeShm& sh, int b) {
+__device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int n) {
   constexpr int E = Elt<DT>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int D = a.max_depth + 1;
   int32_t* otok = a.out_tokens + static_cast<size_t>(b) * D;
-  int32_t* opath = a.out_path + static_cast<size_t>(b) * D;
-  const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
-  if (tid == 0) {
-    int v = 0, n = 0, ok = 1;
-    uint32_t st = 0;
-    for (int it = 0; it <= a.max_depth; ++it) {
-      const TreeRec* r = a.recs + static_cast<size_t>(b) * a.N + v;
-      const uint32_t fl = __ldcg(&r->flags);
-      const int acc = __ldcg(&r->accepted);
-      if (fl & (kRecBad | kRecDetached)) {
-        ok = 0;
-        st |= SPEC_STATUS_BAD_ROW;
-        break;
-      }
-      if (acc >= 0) {
-        if (n >= a.max_depth) {  // not reachable: children at max_depth are never tested
-          ok = 0;
-          break;
-        }
-        opath[n] = acc;
-        otok[n] = tok[acc];
-        ++n;
-        v = acc;
-        continue;
-      }
-      if (fl & kRecDepth) st |= SPEC_STATUS_DEPTH;
-      break;
-    }
-    if (st) atomicOr(a.status, st);
-    sh.walk_v = v;
-    sh.walk_n = n;
-    sh.walk_ok = ok;
-  }
-  __syncthreads();
-  const int v = sh.walk_v, n = sh.walk_n;
-  for (int i = tid; i < D; i += kThreads) {
-    if (i > n) otok[i] = -1;
-    if (i >= n) opath[i] = -1;
-  }
-  if (!sh.walk_ok) {
-    if (tid == 0) {
-      otok[n] = -1;
-      a.out_n[b] = n;
-    }
-    __syncthreads();
-    return;
-  }
   const size_t g = static_cast<size_t>(b) * a.N + v;
   const TreeRec* r = a.recs + g;
   const float nmp = __ldcg(&r->nmp), nmq = __ldcg(&r->nmq), fa = __ldcg(&r->fa), fb = __ldcg(&r->fb);
@@ -446,10 +452,12 @@ __device__ void tree_draw(const TreeSampleArgs& a, TreeShm& sh, int b) {
   __syncthreads();
 }
 
+
 // One cluster of kTreeCl CTAs per node, clusters looping over the B*N nodes.
+// Nodes with children to test run the sibling loop; the others are marked.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSampleArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn[];
+  extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ TreeShm sh;
   constexpr int E = Elt<DT>::kBytes;
   cg::cluster_group cluster = cg::this_cluster();
@@ -461,33 +469,27 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
   const int lo = rank * a.slice;
   const int len = max(0, min(a.V, lo + a.slice) - lo);
   const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.bar[0], 1);
+    mbar_init(&sh.bar[1], 1);
+    fence_mbar_init();
+    sh.timed_out = 0;
+  }
+  __syncthreads();
+  uint32_t php = 0, phq = 0;
   int round = 0;
   for (int64_t g = cid; g < nodes; g += ncl) {
     const int b = static_cast<int>(g / a.N), j = static_cast<int>(g % a.N);
-    const int32_t* par = a.parents + static_cast<size_t>(b) * a.N;
     const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
     TreeRec* rec = a.recs + g;
-    if (threadIdx.x == 0) {
-      int d = 0, v = j, att = 1;
-      while (v != 0) {  // parents strictly decrease, so this ends within j steps
-        const int pv = par[v];
-        if (pv < 0 || pv >= v) {
-          att = 0;
-          break;
-        }
-        v = pv;
-        ++d;
-      }
-      sh.depth = d;
-      sh.attached = att;
-      if (rank == 0) {
-        uint32_t st = 0;
-        if (j == 0 ? par[0] != -1 : (par[j] < 0 || par[j] >= j)) st |= SPEC_STATUS_BAD_PARENT;
-        if (j > 0 && (tok[j] < 0 || tok[j] >= a.V)) st |= SPEC_STATUS_BAD_TOKEN;
-        if (st) atomicOr(a.status, st);
-      }
+    tree_header(a, sh, b, j);
+    if (rank == 0 && threadIdx.x == 0) {
+      uint32_t st = 0;
+      const int pj = sh.par[j];
+      if (j == 0 ? pj != -1 : (pj < 0 || pj >= j)) st |= SPEC_STATUS_BAD_PARENT;
+      if (j > 0 && (tok[j] < 0 || tok[j] >= a.V)) st |= SPEC_STATUS_BAD_TOKEN;
+      if (st) atomicOr(a.status, st);
     }
-    __syncthreads();
     uint32_t rflags = 0;
     int accepted = -1;
     bool cz = true;
@@ -496,82 +498,83 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
       rflags = kRecDetached;
     } else {
       const bool testable = sh.depth < a.max_depth;
-      collect_children(a, sh, par, tok, j, testable);
+      collect_children(a, sh, tok, j, testable);
       const int nk = sh.nk;
       if (sh.has_child && !testable) rflags |= kRecDepth;
-      const bool with_q = nk > 0;
-      const size_t rowoff = (static_cast<size_t>(g) * a.V + lo) * E;
-      const unsigned char* prow = static_cast<const unsigned char*>(a.logits) + rowoff;
-      const unsigned char* qrow = static_cast<const unsigned char*>(a.draft) + rowoff;
-      int slot = round++ & 1;
-      load_slices<DT>(a, sh, prow, qrow, len, with_q, sp, sq, slot);
-      cluster_combine(sh, slot, 4, true);
-      const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[1]);
-      const bool bad = sh.got[2] != 0.0 || mp == -INFINITY || (with_q && (sh.got[3] != 0.0 || mq == -INFINITY));
-      if (bad) {
-        rflags |= kRecBad;
+      if (nk == 0) {
+        rflags |= kRecDefer;  // stop distribution p: summed only if the walk ends here
       } else {
-        nmp = -mp * a.c;
-        nmq = with_q ? -mq * a.c : 0.f;
-        slice_pass<DT, 0>(sh, sp, sq, len, a.wchunk, with_q, a.c, nmp, nmq, 0.f, 0.f);
-        slot = round++ & 1;
-        if (threadIdx.x == 0) {
-          double z0 = 0.0, z1 = 0.0;
-          for (int w = 0; w < kWarps; ++w) {
-            sh.zc[w] = sh.wsum[w][0];
-            z0 += sh.wsum[w][0];
-            z1 += sh.wsum[w][1];
-          }
-          sh.red[slot][0] = z0;
-          sh.red[slot][1] = z1;
-        }
-        cluster_combine(sh, slot, 2, false);
-        const double zp = sh.got[0], zq = sh.got[1];
-        const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
-        const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
-        double cc = 0.0, W = 1.0;
-        for (int i = 0; i < nk; ++i) {
-          const int child = sh.kids[i];
-          if (threadIdx.x == 0) {
-            const int x = tok[child];
-            const double px =
-                static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(pfull, x)), a.c, nmp))) / zp;
-            const double qx =
-                static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(qfull, x)), a.c, nmq))) / zq;
-            const double u = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N + child]);
-            sh.accept = u * qx * W < px - cc * qx;
-          }
-          __syncthreads();
-          if (sh.accept) {
-            accepted = child;
-            break;
-          }
-          cc += W;
-          fa = static_cast<float>(1.0 / zp);
-          fb = static_cast<float>(cc / zq);
-          slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+        const size_t rowoff = (static_cast<size_t>(g) * a.V + lo) * E;
+        int slot = round++ & 1;
+        stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + rowoff,
+                       static_cast<const unsigned char*>(a.draft) + rowoff, len, true, sp, sq, php, phq, slot);
+        cluster_combine(sh, slot, 4, true);
+        const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[1]);
+        if (sh.got[2] != 0.0 || sh.got[3] != 0.0 || mp == -INFINITY || mq == -INFINITY) {
+          rflags |= kRecBad;
+        } else {
+          nmp = -mp * a.c;
+          nmq = -mq * a.c;
+          slice_pass<DT, 0>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, 0.f, 0.f);
           slot = round++ & 1;
           if (threadIdx.x == 0) {
-            double s = 0.0;
+            double z0 = 0.0, z1 = 0.0;
             for (int w = 0; w < kWarps; ++w) {
-              sh.wc[w] = sh.wsum[w][0];
-              s += sh.wsum[w][0];
+              sh.zc[w] = sh.wsum[w][0];
+              z0 += sh.wsum[w][0];
+              z1 += sh.wsum[w][1];
             }
-            sh.red[slot][0] = s;
+            sh.red[slot][0] = z0;
+            sh.red[slot][1] = z1;
           }
-          cluster_combine(sh, slot, 1, false);
-          const double wn = sh.got[0];
-          if (wn > 0.0) {
-            W = wn;
-            cz = false;
-          } else {  // residual of mass zero: back to p
-            W = 1.0;
-            cc = 0.0;
-            cz = true;
+          cluster_combine(sh, slot, 2, false);
+          const double zp = sh.got[0], zq = sh.got[1];
+          const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
+          const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
+          double cc = 0.0, W = 1.0;
+          for (int i = 0; i < nk; ++i) {
+            const int child = sh.kids[i];
+            if (threadIdx.x == 0) {
+              const int x = tok[child];
+              const double px =
+                  static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(pfull, x)), a.c, nmp))) / zp;
+              const double qx =
+                  static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(qfull, x)), a.c, nmq))) / zq;
+              const double u = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N + child]);
+              sh.accept = u * qx * W < px - cc * qx;
+            }
+            __syncthreads();
+            if (sh.accept) {
+              accepted = child;
+              break;
+            }
+            cc += W;
+            fa = static_cast<float>(1.0 / zp);
+            fb = static_cast<float>(cc / zq);
+            slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+            slot = round++ & 1;
+            if (threadIdx.x == 0) {
+              double s = 0.0;
+              for (int w = 0; w < kWarps; ++w) {
+                sh.wc[w] = sh.wsum[w][0];
+                s += sh.wsum[w][0];
+              }
+              sh.red[slot][0] = s;
+            }
+            cluster_combine(sh, slot, 1, false);
+            const double wn = sh.got[0];
+            if (wn > 0.0) {
+              W = wn;
+              cz = false;
+            } else {  // residual of mass zero: back to p
+              W = 1.0;
+              cc = 0.0;
+              cz = true;
+            }
           }
+          if (accepted < 0 && threadIdx.x < kWarps)
+            rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] : sh.wc[threadIdx.x];
         }
-        if (accepted < 0 && threadIdx.x < kWarps)
-          rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] : sh.wc[threadIdx.x];
       }
     }
     if (rank == 0 && threadIdx.x == 0) {
@@ -582,35 +585,121 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
       rec->fa = cz ? 1.f : fa;
       rec->fb = cz ? 0.f : fb;
     }
+    __syncthreads();  // every read of this node's slices and of sh.par is done
+  }
+  if (sh.timed_out && threadIdx.x == 0) {  // let copies still in flight land before the CTA leaves
+    mbar_wait_bounded(&sh.bar[0], php ^ 1u);
+    mbar_wait_bounded(&sh.bar[1], phq ^ 1u);
+  }
+  cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
+// One cluster per tree: follow the accepted children from the root (every
+// CTA walks the same records), sum the stop node's p if its node pass left
+// that to the walk, then rank 0 draws the correction.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSampleArgs a) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ TreeShm sh;
+  constexpr int E = Elt<DT>::kBytes;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / kTreeCl;
+  const int tid = threadIdx.x;
+  const int D = a.max_depth + 1;
+  int32_t* otok = a.out_tokens + static_cast<size_t>(b) * D;
+  int32_t* opath = a.out_path + static_cast<size_t>(b) * D;
+  const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
+  if (tid == 0) {
+    mbar_init(&sh.bar[0], 1);
+    mbar_init(&sh.bar[1], 1);
+    fence_mbar_init();
+    sh.timed_out = 0;
+    sh.has_child = 0;
+    int v = 0, n = 0, ok = 1;
+    uint32_t st = 0;
+    for (int it = 0; it <= a.max_depth; ++it) {
+      const TreeRec* r = a.recs + static_cast<size_t>(b) * a.N + v;
+      const uint32_t fl = r->flags;
+      const int acc = r->accepted;
+      if (fl & (kRecBad | kRecDetached)) {
+        ok = 0;
+        st |= SPEC_STATUS_BAD_ROW;
+        break;
+      }
+      if (acc >= 0) {
+        if (n >= a.max_depth) {  // not reachable: children at max_depth are never tested
+          ok = 0;
+          break;
+        }
+        if (rank == 0) {
+          opath[n] = acc;
+          otok[n] = tok[acc];
+        }
+        ++n;
+        v = acc;
+        continue;
+      }
+      if (fl & kRecDepth) st |= SPEC_STATUS_DEPTH;
+      sh.has_child = (fl & kRecDefer) != 0;
+      break;
+    }
+    if (rank == 0 && st) atomicOr(a.status, st);
+    sh.walk_v = v;
+    sh.walk_n = n;
+    sh.walk_ok = ok;
+  }
+  __syncthreads();
+  const int v = sh.walk_v, n = sh.walk_n;
+  bool ok = sh.walk_ok != 0;
+  if (rank == 0)
+    for (int i = tid; i < D; i += kThreads) {
+      if (i > n) otok[i] = -1;
+      if (i >= n) opath[i] = -1;
+    }
+  if (ok && sh.has_child) {  // stop distribution p of a node whose pass only marked it
+    const size_t g = static_cast<size_t>(b) * a.N + v;
+    TreeRec* rec = a.recs + g;
+    const uint32_t sp = smem_addr(dyn);
+    const int lo = rank * a.slice;
+    const int len = max(0, min(a.V, lo + a.slice) - lo);
+    uint32_t php = 0, phq = 0;
+    stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + (g * a.V + lo) * E, nullptr, len, false,
+                   sp, sp, php, phq, 0);
+    cluster_combine(sh, 0, 4, true);
+    const float mp = static_cast<float>(sh.got[0]);
+    if (sh.got[2] != 0.0 || mp == -INFINITY) {
+      ok = false;
+      if (rank == 0 && tid == 0) atomicOr(a.status, SPEC_STATUS_BAD_ROW);
+    } else {
+      const float nmp = -mp * a.c;
+      slice_pass<DT, 0>(sh, sp, sp, len, a.wchunk, false, a.c, nmp, 0.f, 0.f, 0.f);
+      if (tid < kWarps) rec->chunk[rank * kWarps + tid] = sh.wsum[tid][0];
+      if (rank == 0 && tid == 0) {
+        rec->nmp = nmp;
+        rec->nmq = 0.f;
+        rec->fa = 1.f;
+        rec->fb = 0.f;
+      }
+    }
+    if (sh.timed_out && tid == 0) mbar_wait_bounded(&sh.bar[0], php ^ 1u);
     __threadfence();
-    cluster.sync();
-    if (rank == 0) {
-      if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t t = atomicAdd(&a.tickets[b], 1u);
-        sh.last = t == static_cast<uint32_t>(a.N - 1);
-        if (sh.last) atomicExch(&a.tickets[b], 0u);  // every node of the tree has counted in
-      }
-      __syncthreads();
-      if (sh.last) {
-        __threadfence();
-        tree_draw<DT>(a, sh, b);
-      }
+    cluster.sync();  // every CTA's chunk sums are written
+  }
+  if (rank == 0) {
+    if (ok) {
+      __threadfence();
+      draw_at<DT>(a, sh, b, v, n);
+    } else if (tid == 0) {
+      otok[n] = -1;
+      a.out_n[b] = n;
     }
   }
   cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
-template <int DT>
-int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
-  static int cached_smem[2] = {-1, -1}, cached_clusters[2] = {0, 0}, cached_dev[2] = {-1, -1};
-  const size_t smem = tree_smem_bytes(DT, a.slice);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  auto kern = tree_node_kernel<DT>;
+cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kTreeCl;
   attr[0].val.clusterDim.y = 1;
@@ -620,12 +709,28 @@ int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int DT>
+int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
+  static int cached_smem[2] = {-1, -1}, cached_clusters[2] = {0, 0}, cached_dev[2] = {-1, -1};
+  const size_t smem = tree_smem_bytes(DT, a.slice);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto node_k = tree_node_kernel<DT>;
+  auto walk_k = tree_walk_kernel<DT>;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(attr, smem, st);
   if (cached_smem[DT] != static_cast<int>(smem) || cached_dev[DT] != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(node_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(walk_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(kTreeCl);
     int ncl = 0;
-    e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&ncl, node_k, &cfg);
     if (e != cudaSuccess) return e;
     if (ncl < 1) return cudaErrorInvalidConfiguration;
     cached_smem[DT] = static_cast<int>(smem);
@@ -635,7 +740,10 @@ int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
   const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
   const int clusters = static_cast<int>(nodes < cached_clusters[DT] ? nodes : cached_clusters[DT]);
   cfg.gridDim = dim3(clusters * kTreeCl);
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  e = cudaLaunchKernelEx(&cfg, node_k, a);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kTreeCl);
+  return cudaLaunchKernelEx(&cfg, walk_k, a);
 }
 
 }  // namespace
