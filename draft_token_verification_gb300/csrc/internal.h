@@ -116,6 +116,7 @@ struct WsLayout {
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
   size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
   size_t trecs;       // TreeRec[B*(k+1)]  tree sampling: one record per node
+  size_t tlist;       // uint32 count (zero between calls), then int32[B*(k+1)] nodes with children to test
   size_t total;
 };
 
@@ -139,7 +140,8 @@ constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   w.g_slots = align_up(w.csums + sizeof(float) * kChunkRec * static_cast<size_t>(kMaxDrawChunks) * B, 256);
   w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
   w.trecs = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
-  w.total = align_up(w.trecs + sizeof(TreeRec) * units, 256);
+  w.tlist = align_up(w.trecs + sizeof(TreeRec) * units, 256);
+  w.total = align_up(w.tlist + 16 + sizeof(int32_t) * units, 256);
   return w;
 }
 constexpr WsLayout ws_layout(int B, int k) {
@@ -197,6 +199,8 @@ struct TreeSampleArgs {
   int32_t* out_n;              // [B]
   uint32_t* status;
   TreeRec* recs;               // [B][N]
+  uint32_t* work_count;        // nodes in work_list (zero between calls)
+  int32_t* work_list;          // node ids b*N + j with children to test
 };
 
 struct ArgmaxArgs {

@@ -45,12 +45,13 @@ namespace specv {
 namespace {
 
 constexpr uint32_t kPiece = 16384;  // bytes per bulk copy
+constexpr int kPre = 32;            // children whose logits are fetched ahead of the sibling loop
 constexpr int16_t kNoParent = -2;   // a parent entry outside [-1, N)
 
 struct TreeShm {
   uint64_t bar[2];           // bulk-copy completion: target slice, draft slice
-  double red[2][4];          // per-CTA values handed to the cluster, by round parity
-  double got[4];             // their cluster-wide combination
+  double red[2][8];          // per-CTA values handed to the cluster, by round parity
+  double got[8];             // their cluster-wide combination
   double wsum[kWarps][2];    // per-warp sums of the current pass
   double zc[kWarps];         // per-warp sums of 2^(l c + nmp) (the c = 0 residual)
   double wc[kWarps];         // per-warp sums of the last residual pass
@@ -59,6 +60,9 @@ struct TreeShm {
   int16_t kids[kMaxTreeNodes];
   int16_t par[kMaxTreeNodes];
   int nk_w[kWarps];
+  float kl[kPre], kd[kPre], ku[kPre];  // the first children's target / draft logits and uniforms
+  float mloc[2];             // this CTA's maxima (target, draft)
+  int badloc;               // this CTA's slices hold NaN / +inf (or did not arrive)
   int nk, has_child, depth, attached, accept, timed_out;
   int walk_v, walk_n, walk_ok, draw_w;
   double draw_rem;
@@ -99,23 +103,68 @@ __device__ __forceinline__ float warp_max_f32(float v) {
   return v;
 }
 
+// Loads value i (< 8) of every rank's sh.red[slot] in one round of
+// distributed-shared-memory reads: lane l holds value l/8 and l/8 + 4 of rank
+// l%8.  Warp 0 only.
+__device__ __forceinline__ void cluster_gather(TreeShm& sh, int slot, int nv, double& x0, double& x1) {
+  const int lane = threadIdx.x & 31, r = lane & (kTreeCl - 1), i = lane / kTreeCl;
+  x0 = i < nv ? ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i]), r)) : 0.0;
+  x1 = i + 4 < nv ? ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i + 4]), r)) : 0.0;
+}
+
+// Value i of rank r from the gathered registers (all lanes take part).
+__device__ __forceinline__ double gathered(double x0, double x1, int i, int r) {
+  const double a = __shfl_sync(0xFFFFFFFFu, x0, (i & 3) * kTreeCl + r);
+  const double b = __shfl_sync(0xFFFFFFFFu, x1, (i & 3) * kTreeCl + r);
+  return i < 4 ? a : b;
+}
+
 // Combines the nv values thread 0 of every CTA left in sh.red[slot] across the
 // cluster, in rank order (sum, or max when is_max), into sh.got.  Every CTA
 // computes the same result bit for bit.
 __device__ void cluster_combine(TreeShm& sh, int slot, int nv, bool is_max) {
   cg::this_cluster().sync();
   if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+    double x0, x1;
+    cluster_gather(sh, slot, nv, x0, x1);
     for (int i = 0; i < nv; ++i) {
-      double x = 0.0;
-      if (lane < kTreeCl) x = ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i]), lane));
-      double acc = __shfl_sync(0xFFFFFFFFu, x, 0);
+      double acc = gathered(x0, x1, i, 0);
       for (int r = 1; r < kTreeCl; ++r) {
-        const double y = __shfl_sync(0xFFFFFFFFu, x, r);
+        const double y = gathered(x0, x1, i, r);
         acc = is_max ? fmax(acc, y) : acc + y;
       }
-      if (lane == 0) sh.got[i] = acc;
+      if (threadIdx.x == 0) sh.got[i] = acc;
     }
+  }
+  __syncthreads();
+}
+
+// Row statistics from per-CTA ones: sh.red[slot] = {max p, mass p, max q,
+// mass q, bad} with masses relative to the CTA's own maxima.  sh.got = {max p,
+// mass p, max q, mass q, bad}, masses relative to the cluster maxima
+// (each CTA's mass scaled by 2^((m_r - m) c), summed in rank order).
+__device__ void cluster_combine_stats(TreeShm& sh, int slot, float c) {
+  cg::this_cluster().sync();
+  if (threadIdx.x < 32) {
+    double x0, x1;
+    cluster_gather(sh, slot, 5, x0, x1);
+    for (int k = 0; k < 2; ++k) {
+      float m = -INFINITY;
+      for (int r = 0; r < kTreeCl; ++r) m = fmaxf(m, static_cast<float>(gathered(x0, x1, 2 * k, r)));
+      double z = 0.0;
+      for (int r = 0; r < kTreeCl; ++r) {
+        const float mr = static_cast<float>(gathered(x0, x1, 2 * k, r));
+        const double zr = gathered(x0, x1, 2 * k + 1, r);
+        if (zr > 0.0) z += zr * static_cast<double>(ex2_approx((mr - m) * c));
+      }
+      if (threadIdx.x == 0) {
+        sh.got[2 * k] = m;
+        sh.got[2 * k + 1] = z;
+      }
+    }
+    double bad = 0.0;
+    for (int r = 0; r < kTreeCl; ++r) bad = fmax(bad, gathered(x0, x1, 4, r));
+    if (threadIdx.x == 0) sh.got[4] = bad;
   }
   __syncthreads();
 }
@@ -156,27 +205,32 @@ __device__ __forceinline__ void bulk_issue(uint64_t* bar, uint32_t dst, const un
     bulk_copy_g2s_addr(dst + off, src + off, bytes - off < kPiece ? bytes - off : kPiece, bar);
 }
 
-// Copies elements [lo, lo+len) of the target row (and of the draft row when
-// with_q) into shared memory -- bulk copies for 16-byte aligned rows, plain
-// loads otherwise -- and leaves this CTA's maxima and bad-value flags in
-// sh.red[slot] (thread 0): {max p, max q, bad p, bad q}.  A copy that does
-// not complete within the bounded wait marks the slice bad and sets
+// Thread 0: starts the bulk copies of this CTA's slices (16-byte aligned rows).
+__device__ __forceinline__ void stage_issue(TreeShm& sh, const unsigned char* prow, const unsigned char* qrow,
+                                            uint32_t bytes, bool with_q, uint32_t sp, uint32_t sq) {
+  if (sh.timed_out) return;
+  fence_proxy_async_smem();  // earlier reads of these slices come before the copies' writes
+  bulk_issue(&sh.bar[0], sp, prow, bytes);
+  if (with_q) bulk_issue(&sh.bar[1], sq, qrow, bytes);
+}
+
+// Brings elements [lo, lo+len) of the target row (and of the draft row when
+// with_q) into shared memory -- bulk copies for 16-byte aligned rows (started
+// here unless `issued`), plain loads otherwise -- and leaves this CTA's maxima
+// in sh.mloc and its bad-value flag in sh.badloc.  A copy that does not
+// complete within the bounded wait marks the slice bad and sets
 // SPEC_STATUS_TIMEOUT; that CTA copies nothing more.
 template <int DT>
 __device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned char* prow,
                            const unsigned char* qrow, int len, bool with_q, uint32_t sp, uint32_t sq,
-                           uint32_t& php, uint32_t& phq, int slot) {
+                           uint32_t& php, uint32_t& phq, bool issued) {
   constexpr int E = Elt<DT>::kBytes;
   constexpr int PV = Elt<DT>::kPerVec;
   float mp = -INFINITY, mq = -INFINITY;
   int bp = 0, bq = 0, tmo = 0;
   if (a.aligned) {
     const bool skip = sh.timed_out != 0;
-    if (threadIdx.x == 0 && !skip) {
-      fence_proxy_async_smem();  // earlier reads of these slices come before the copies' writes
-      bulk_issue(&sh.bar[0], sp, prow, static_cast<uint32_t>(len) * E);
-      if (with_q) bulk_issue(&sh.bar[1], sq, qrow, static_cast<uint32_t>(len) * E);
-    }
+    if (threadIdx.x == 0 && !issued) stage_issue(sh, prow, qrow, static_cast<uint32_t>(len) * E, with_q, sp, sq);
     bool ok = !skip;
     if (ok) {
       ok = mbar_wait_bounded(&sh.bar[0], php);
@@ -248,12 +302,20 @@ __device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned 
       sh.timed_out = 1;
       bd |= 1;
     }
-    sh.red[slot][0] = m0;
-    sh.red[slot][1] = m1;
-    sh.red[slot][2] = bd & 1;
-    sh.red[slot][3] = (bd >> 1) & 1;
+    sh.mloc[0] = m0;
+    sh.mloc[1] = m1;
+    sh.badloc = (bd & 1) | (with_q ? (bd >> 1) & 1 : 0);
   }
+  __syncthreads();
 }
+
+// This CTA's masses relative to its own maxima (one pass), handed to the
+// cluster with the maxima: sh.red[slot] = {max p, mass p, max q, mass q, bad};
+// sh.zc keeps the per-warp target masses.  Then the cluster-wide statistics
+// in sh.got (cluster_combine_stats).
+template <int DT>
+__device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
+                            int slot);
 
 // Sums over this CTA's slice, per warp chunk (16-byte vectors, lanes
 // interleaved, float per lane, double across lanes).  MODE 0: target and
@@ -290,6 +352,29 @@ __device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int w
     sh.wsum[warp][1] = d1;
   }
   __syncthreads();
+}
+
+template <int DT>
+__device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
+                            int slot) {
+  const float m0 = sh.mloc[0], m1 = with_q ? sh.mloc[1] : -INFINITY;
+  const float nm0 = m0 == -INFINITY ? 0.f : -m0 * c;  // an empty or all -inf slice has no mass
+  const float nm1 = m1 == -INFINITY ? 0.f : -m1 * c;
+  slice_pass<DT, 0>(sh, sp, sq, len, wchunk, with_q, c, nm0, nm1, 0.f, 0.f);
+  if (threadIdx.x == 0) {
+    double z0 = 0.0, z1 = 0.0;
+    for (int w = 0; w < kWarps; ++w) {
+      sh.zc[w] = sh.wsum[w][0];
+      z0 += sh.wsum[w][0];
+      z1 += sh.wsum[w][1];
+    }
+    sh.red[slot][0] = m0;
+    sh.red[slot][1] = z0;
+    sh.red[slot][2] = m1;
+    sh.red[slot][3] = z1;
+    sh.red[slot][4] = sh.badloc;
+  }
+  cluster_combine_stats(sh, slot, c);
 }
 
 // Parents of tree b into sh.par (entries outside [-1, N) become kNoParent),
@@ -385,6 +470,7 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
   {
     const int wlo = min(chi, clo + warp * sub), whi = min(chi, clo + (warp + 1) * sub);
     float s = 0.f;
+#pragma unroll 8
     for (int t = wlo + lane; t < whi; t += 32)
       s += resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
                         fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp, nmq, fa, fb);
@@ -421,26 +507,38 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
       const double rem = sh.draw_rem;
       const int wlo = min(chi, clo + pick * sub), whi = min(chi, clo + (pick + 1) * sub);
       double acc = 0.0;
-      for (int base = wlo; base < whi; base += 32) {
-        const int t = base + lane;
-        float w = 0.f;
-        if (t < whi)
-          w = resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
-                           fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp, nmq, fa, fb);
-        double incl = static_cast<double>(w);
+      constexpr int kAhead = 8;  // rounds of 32 elements fetched before they are scanned
+      bool found = false;
+      for (int base0 = wlo; base0 < whi && !found; base0 += 32 * kAhead) {
+        float w[kAhead];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
+        for (int k = 0; k < kAhead; ++k) {
+          const int t = base0 + 32 * k + lane;
+          w[k] = t < whi ? resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
+                                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp,
+                                        nmq, fa, fb)
+                         : 0.f;
         }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, w > 0.f && acc + incl > rem);
-        const uint32_t pos = __ballot_sync(0xFFFFFFFFu, w > 0.f);
-        if (pos) token = base + 31 - __clz(pos);
-        if (hit) {
-          token = base + __ffs(hit) - 1;
-          break;
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+          const int base = base0 + 32 * k;
+          double incl = static_cast<double>(w[k]);
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const uint32_t hit = __ballot_sync(0xFFFFFFFFu, w[k] > 0.f && acc + incl > rem);
+          const uint32_t pos = __ballot_sync(0xFFFFFFFFu, w[k] > 0.f);
+          if (!found) {
+            if (pos) token = base + 31 - __clz(pos);
+            if (hit) {
+              token = base + __ffs(hit) - 1;
+              found = true;
+            }
+          }
+          acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
     if (lane == 0) {
@@ -453,8 +551,79 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
 }
 
 
-// One cluster of kTreeCl CTAs per node, clusters looping over the B*N nodes.
-// Nodes with children to test run the sibling loop; the others are marked.
+// One CTA per tree: validates the parents, finds every node's depth, and
+// lists the nodes with at least one child to test (attached, above
+// max_depth, a child whose token is in [0, V)) for tree_node_kernel; the
+// others get their final record here (detached, or stop residual p).
+__global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArgs a) {
+  __shared__ int16_t par[kMaxTreeNodes];
+  __shared__ int16_t dep[kMaxTreeNodes];
+  __shared__ uint8_t has_child[kMaxTreeNodes];
+  __shared__ uint8_t testable_child[kMaxTreeNodes];
+  __shared__ int16_t list[kMaxTreeNodes];
+  __shared__ int cnt, base;
+  const int b = blockIdx.x, tid = threadIdx.x, N = a.N;
+  const int32_t* pg = a.parents + static_cast<size_t>(b) * N;
+  const int32_t* tok = a.tokens + static_cast<size_t>(b) * N;
+  uint32_t st = 0;
+  for (int i = tid; i < N; i += kThreads) {
+    const int p = pg[i];
+    par[i] = static_cast<int16_t>(p >= -1 && p < N ? p : kNoParent);
+    has_child[i] = 0;
+    testable_child[i] = 0;
+    if (i == 0 ? p != -1 : (p < 0 || p >= i)) st |= SPEC_STATUS_BAD_PARENT;
+    if (i > 0 && (tok[i] < 0 || tok[i] >= a.V)) st |= SPEC_STATUS_BAD_TOKEN;
+  }
+  if (tid == 0) cnt = 0;
+  __syncthreads();
+  for (int i = tid; i < N; i += kThreads) {
+    int d = 0, v = i;
+    while (v != 0) {  // parents strictly decrease, so this ends within i steps
+      const int pv = par[v];
+      if (pv < 0 || pv >= v) {
+        d = -1;
+        break;
+      }
+      v = pv;
+      ++d;
+    }
+    dep[i] = static_cast<int16_t>(d);
+  }
+  __syncthreads();
+  for (int i = tid + 1; i < N; i += kThreads) {
+    const int p = par[i];
+    if (p >= 0 && p < i && dep[p] >= 0) {
+      has_child[p] = 1;
+      if (dep[p] < a.max_depth && tok[i] >= 0 && tok[i] < a.V) testable_child[p] = 1;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < N; i += kThreads) {
+    if (testable_child[i]) {
+      list[atomicAdd(&cnt, 1)] = static_cast<int16_t>(i);
+    } else {
+      TreeRec* rec = a.recs + static_cast<size_t>(b) * N + i;
+      uint32_t fl = kRecDetached;
+      if (dep[i] >= 0) fl = kRecDefer | (has_child[i] && dep[i] >= a.max_depth ? kRecDepth : 0u);
+      rec->accepted = -1;
+      rec->flags = fl;
+      rec->nmp = 0.f;
+      rec->nmq = 0.f;
+      rec->fa = 1.f;
+      rec->fb = 0.f;
+    }
+  }
+  if (st) atomicOr(a.status, st);
+  __syncthreads();
+  if (tid == 0) base = static_cast<int>(atomicAdd(a.work_count, static_cast<uint32_t>(cnt)));
+  __syncthreads();
+  const int cap = a.B * N;  // the list's length; the count is zero on entry
+  for (int i = tid; i < cnt; i += kThreads)
+    if (base + i < cap) a.work_list[base + i] = b * N + list[i];
+}
+
+// One cluster of kTreeCl CTAs per node with children to test (the list
+// tree_plan_kernel built), clusters looping over the list.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSampleArgs a) {
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -468,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
   const uint32_t sq = sp + static_cast<uint32_t>(a.slice) * E;
   const int lo = rank * a.slice;
   const int len = max(0, min(a.V, lo + a.slice) - lo);
-  const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
+  const int total = min(static_cast<int>(*a.work_count), a.B * a.N);
   if (threadIdx.x == 0) {
     mbar_init(&sh.bar[0], 1);
     mbar_init(&sh.bar[1], 1);
@@ -478,103 +647,96 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
   __syncthreads();
   uint32_t php = 0, phq = 0;
   int round = 0;
-  for (int64_t g = cid; g < nodes; g += ncl) {
+  for (int idx = cid; idx < total; idx += ncl) {
+    const int64_t g = a.work_list[idx];
+    if (g < 0 || g >= static_cast<int64_t>(a.B) * a.N) continue;  // uniform across the cluster
     const int b = static_cast<int>(g / a.N), j = static_cast<int>(g % a.N);
     const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
+    const float* uni = a.uniforms + static_cast<size_t>(b) * a.N;
     TreeRec* rec = a.recs + g;
+    const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
+    const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
+    // both rows are needed: start their copies before the tree bookkeeping
+    if (a.aligned && threadIdx.x == 0)
+      stage_issue(sh, pfull + static_cast<size_t>(lo) * E, qfull + static_cast<size_t>(lo) * E,
+                  static_cast<uint32_t>(len) * E, true, sp, sq);
     tree_header(a, sh, b, j);
-    if (rank == 0 && threadIdx.x == 0) {
-      uint32_t st = 0;
-      const int pj = sh.par[j];
-      if (j == 0 ? pj != -1 : (pj < 0 || pj >= j)) st |= SPEC_STATUS_BAD_PARENT;
-      if (j > 0 && (tok[j] < 0 || tok[j] >= a.V)) st |= SPEC_STATUS_BAD_TOKEN;
-      if (st) atomicOr(a.status, st);
+    collect_children(a, sh, tok, j, true);
+    const int nk = sh.nk;
+    for (int i = threadIdx.x; i < min(nk, kPre); i += kThreads) {
+      const int x = tok[sh.kids[i]];
+      sh.kl[i] = Elt<DT>::value(Elt<DT>::bits_at(pfull, x));
+      sh.kd[i] = Elt<DT>::value(Elt<DT>::bits_at(qfull, x));
+      sh.ku[i] = uni[sh.kids[i]];
     }
+    stage_rows<DT>(a, sh, pfull + static_cast<size_t>(lo) * E, qfull + static_cast<size_t>(lo) * E, len, true,
+                   sp, sq, php, phq, true);
+    int slot = round++ & 1;
+    slice_stats<DT>(sh, sp, sq, len, a.wchunk, true, a.c, slot);
     uint32_t rflags = 0;
     int accepted = -1;
     bool cz = true;
     float fa = 1.f, fb = 0.f, nmp = 0.f, nmq = 0.f;
-    if (!sh.attached) {
-      rflags = kRecDetached;
+    const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[2]);
+    if (sh.got[4] != 0.0 || mp == -INFINITY || mq == -INFINITY) {
+      rflags |= kRecBad;
     } else {
-      const bool testable = sh.depth < a.max_depth;
-      collect_children(a, sh, tok, j, testable);
-      const int nk = sh.nk;
-      if (sh.has_child && !testable) rflags |= kRecDepth;
-      if (nk == 0) {
-        rflags |= kRecDefer;  // stop distribution p: summed only if the walk ends here
-      } else {
-        const size_t rowoff = (static_cast<size_t>(g) * a.V + lo) * E;
-        int slot = round++ & 1;
-        stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + rowoff,
-                       static_cast<const unsigned char*>(a.draft) + rowoff, len, true, sp, sq, php, phq, slot);
-        cluster_combine(sh, slot, 4, true);
-        const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[1]);
-        if (sh.got[2] != 0.0 || sh.got[3] != 0.0 || mp == -INFINITY || mq == -INFINITY) {
-          rflags |= kRecBad;
-        } else {
-          nmp = -mp * a.c;
-          nmq = -mq * a.c;
-          slice_pass<DT, 0>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, 0.f, 0.f);
-          slot = round++ & 1;
-          if (threadIdx.x == 0) {
-            double z0 = 0.0, z1 = 0.0;
-            for (int w = 0; w < kWarps; ++w) {
-              sh.zc[w] = sh.wsum[w][0];
-              z0 += sh.wsum[w][0];
-              z1 += sh.wsum[w][1];
-            }
-            sh.red[slot][0] = z0;
-            sh.red[slot][1] = z1;
+      nmp = -mp * a.c;
+      nmq = -mq * a.c;
+      const double zp = sh.got[1], zq = sh.got[3];
+      double cc = 0.0, W = 1.0;
+      for (int i = 0; i < nk; ++i) {
+        const int child = sh.kids[i];
+        if (threadIdx.x == 0) {
+          float lx, dx, uf;
+          if (i < kPre) {
+            lx = sh.kl[i];
+            dx = sh.kd[i];
+            uf = sh.ku[i];
+          } else {
+            const int x = tok[child];
+            lx = Elt<DT>::value(Elt<DT>::bits_at(pfull, x));
+            dx = Elt<DT>::value(Elt<DT>::bits_at(qfull, x));
+            uf = uni[child];
           }
-          cluster_combine(sh, slot, 2, false);
-          const double zp = sh.got[0], zq = sh.got[1];
-          const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
-          const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
-          double cc = 0.0, W = 1.0;
-          for (int i = 0; i < nk; ++i) {
-            const int child = sh.kids[i];
-            if (threadIdx.x == 0) {
-              const int x = tok[child];
-              const double px =
-                  static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(pfull, x)), a.c, nmp))) / zp;
-              const double qx =
-                  static_cast<double>(ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_at(qfull, x)), a.c, nmq))) / zq;
-              const double u = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N + child]);
-              sh.accept = u * qx * W < px - cc * qx;
-            }
-            __syncthreads();
-            if (sh.accept) {
-              accepted = child;
-              break;
-            }
-            cc += W;
-            fa = static_cast<float>(1.0 / zp);
-            fb = static_cast<float>(cc / zq);
-            slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
-            slot = round++ & 1;
-            if (threadIdx.x == 0) {
-              double s = 0.0;
-              for (int w = 0; w < kWarps; ++w) {
-                sh.wc[w] = sh.wsum[w][0];
-                s += sh.wsum[w][0];
-              }
-              sh.red[slot][0] = s;
-            }
-            cluster_combine(sh, slot, 1, false);
-            const double wn = sh.got[0];
-            if (wn > 0.0) {
-              W = wn;
-              cz = false;
-            } else {  // residual of mass zero: back to p
-              W = 1.0;
-              cc = 0.0;
-              cz = true;
-            }
-          }
-          if (accepted < 0 && threadIdx.x < kWarps)
-            rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] : sh.wc[threadIdx.x];
+          const double px = static_cast<double>(ex2_approx(fmaf(lx, a.c, nmp))) / zp;
+          const double qx = static_cast<double>(ex2_approx(fmaf(dx, a.c, nmq))) / zq;
+          sh.accept = static_cast<double>(uf) * qx * W < px - cc * qx;
         }
+        __syncthreads();
+        if (sh.accept) {
+          accepted = child;
+          break;
+        }
+        cc += W;
+        fa = static_cast<float>(1.0 / zp);
+        fb = static_cast<float>(cc / zq);
+        slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+        slot = round++ & 1;
+        if (threadIdx.x == 0) {
+          double sum = 0.0;
+          for (int w = 0; w < kWarps; ++w) {
+            sh.wc[w] = sh.wsum[w][0];
+            sum += sh.wsum[w][0];
+          }
+          sh.red[slot][0] = sum;
+        }
+        cluster_combine(sh, slot, 1, false);
+        const double wn = sh.got[0];
+        if (wn > 0.0) {
+          W = wn;
+          cz = false;
+        } else {  // residual of mass zero: back to p
+          W = 1.0;
+          cc = 0.0;
+          cz = true;
+        }
+      }
+      if (accepted < 0 && threadIdx.x < kWarps) {
+        // the c = 0 residual: this CTA's target masses, rescaled to the row maximum
+        const float m0 = sh.mloc[0];
+        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * a.c));
+        rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] * scale : sh.wc[threadIdx.x];
       }
     }
     if (rank == 0 && threadIdx.x == 0) {
@@ -665,18 +827,20 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
     const int len = max(0, min(a.V, lo + a.slice) - lo);
     uint32_t php = 0, phq = 0;
     stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + (g * a.V + lo) * E, nullptr, len, false,
-                   sp, sp, php, phq, 0);
-    cluster_combine(sh, 0, 4, true);
+                   sp, sp, php, phq, false);
+    slice_stats<DT>(sh, sp, sp, len, a.wchunk, false, a.c, 0);
     const float mp = static_cast<float>(sh.got[0]);
-    if (sh.got[2] != 0.0 || mp == -INFINITY) {
+    if (sh.got[4] != 0.0 || mp == -INFINITY) {
       ok = false;
       if (rank == 0 && tid == 0) atomicOr(a.status, SPEC_STATUS_BAD_ROW);
     } else {
-      const float nmp = -mp * a.c;
-      slice_pass<DT, 0>(sh, sp, sp, len, a.wchunk, false, a.c, nmp, 0.f, 0.f, 0.f);
-      if (tid < kWarps) rec->chunk[rank * kWarps + tid] = sh.wsum[tid][0];
+      if (tid < kWarps) {
+        const float m0 = sh.mloc[0];
+        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * a.c));
+        rec->chunk[rank * kWarps + tid] = sh.zc[tid] * scale;
+      }
       if (rank == 0 && tid == 0) {
-        rec->nmp = nmp;
+        rec->nmp = -mp * a.c;
         rec->nmq = 0.f;
         rec->fa = 1.f;
         rec->fb = 0.f;
@@ -695,6 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
       a.out_n[b] = n;
     }
   }
+  if (blockIdx.x == 0 && tid == 0) *a.work_count = 0;  // the node pass has read it; zero for the next call
   cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
@@ -737,13 +902,19 @@ int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
     cached_clusters[DT] = ncl;
     cached_dev[DT] = dev;
   }
+  tree_plan_kernel<<<a.B, kThreads, 0, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
   const int clusters = static_cast<int>(nodes < cached_clusters[DT] ? nodes : cached_clusters[DT]);
   cfg.gridDim = dim3(clusters * kTreeCl);
   e = cudaLaunchKernelEx(&cfg, node_k, a);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kTreeCl);
-  return cudaLaunchKernelEx(&cfg, walk_k, a);
+  if (e == cudaSuccess) {
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kTreeCl);
+    e = cudaLaunchKernelEx(&cfg, walk_k, a);
+  }
+  if (e != cudaSuccess) cudaMemsetAsync(a.work_count, 0, sizeof(uint32_t), st);  // the walk did not reset it
+  return e;
 }
 
 }  // namespace
