@@ -56,6 +56,47 @@ def tree_bytes():
     return TREE["B"] * TREE["N"] * TREE["V"] * 2
 
 
+def tree_sample_bytes(case, n, path):
+    """Bytes the tree-sampling kernels must read: both rows of every node with a
+    child to test, plus the target row of a stop node without one."""
+    total = 0
+    for b in range(case.B):
+        par = case.parents[b]
+        dep = np.zeros(case.N, int)
+        for j in range(1, case.N):
+            dep[j] = dep[par[j]] + 1
+        internal = {int(par[j]) for j in range(1, case.N)
+                    if dep[par[j]] < case.max_depth and 0 <= case.node_tokens[b, j] < case.V}
+        stop = 0 if n[b] == 0 else int(path[b, n[b] - 1])
+        total += (2 * len(internal) + (stop not in internal)) * case.V * 2
+    return total
+
+
+def time_tree_sample(sv, dev, ws, stream, seed, iters=20):
+    """Token-tree sampling verification, timed alone outside the step: 8 trees
+    of 60 nodes, depth <= 6, V = 128256, bf16, children drawn from their
+    parents' draft rows.  An L2-sized buffer is written before every timed call
+    (the rows it reads fit in L2)."""
+    import torch
+
+    c = W.tree_sample_case(TREE["B"], TREE["N"], TREE["V"], TREE["depth"], seed=seed)
+    args = [to_torch(x, dev) for x in (c.logits, c.draft, c.node_tokens, c.parents, c.uniforms)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        out = sv.spec_verify_tree_sample(*args, TREE["depth"], workspace=ws, stream=stream)
+    ts = []
+    for _ in range(iters):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        out = sv.spec_verify_tree_sample(*args, TREE["depth"], workspace=ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    n, path = out[2].cpu().numpy(), out[1].cpu().numpy()
+    return float(np.median(ts)), tree_sample_bytes(c, n, path), float(n.mean())
+
+
 KERNEL_SOURCES = {
     "sample": ("sample_kernel.cu", "device_common.cuh", "internal.h"),
     "argmax": ("argmax_kernel.cu", "device_common.cuh", "internal.h"),
@@ -304,49 +345,61 @@ def run_gpu(args, rank, world):
     if dist:
         e2e_ms = max_over_ranks(e2e_ms, dev)
     status |= sv.spec_get_status(ws)
+    ts_us, ts_bytes, ts_mal = time_tree_sample(sv, dev, ws, stream, seed=4 + rank)
+    status |= sv.spec_get_status(ws)
 
     return dict(elapsed_ms=elapsed_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
-                h2d=h2d, d2h=d2h, mal=float(n_acc.mean()), greedy_mal=float(gn.mean()))
+                h2d=h2d, d2h=d2h, mal=float(n_acc.mean()), greedy_mal=float(gn.mean()),
+                tree_sample=(ts_us, ts_bytes, ts_mal))
 
 
 # ------------------------------------------------------------ CPU leg
 
 
-def cpu_baseline(sample_seqs: int = 4, trees: int = 2, threads: int | None = None):
+def cpu_baseline(passes: int = 4, threads: int | None = None):
     """The float64 oracle, as it stands, on a bounded sample of the same
-    workload: `sample_seqs` sampling + greedy sequences and `trees` trees."""
+    workload: `passes` passes over the whole benchmark batch (64 sampling and
+    64 greedy sequences, 8 trees), about 15-20 s of CPU work, spread over the
+    host's cores one sequence or tree per task."""
     import oracle
 
     s, t = make_inputs()
     cores = threads or len(os.sched_getaffinity(0))
     jobs = []
-    for b in range(sample_seqs):
-        jobs.append(("sample", b))
-        jobs.append(("greedy", b))
-    for b in range(trees):
-        jobs.append(("tree", b))
+    for _ in range(passes):
+        for b in range(SAMPLE["B"]):
+            jobs.append(("sample", b))
+            jobs.append(("greedy", b))
+        for b in range(TREE["B"]):
+            jobs.append(("tree", b))
 
     def run(job):
         kind, b = job
         sl = slice(b, b + 1)
+        t0 = time.perf_counter()
         if kind == "sample":
             oracle.verify_sample(s.target[sl], s.draft[sl], s.tokens[sl], s.uniforms[sl], SAMPLE["T"],
                                  SAMPLE["top_k"], SAMPLE["top_p"], all_rows=False)
-            return SAMPLE["k"]
-        if kind == "greedy":
+            n = SAMPLE["k"]
+        elif kind == "greedy":
             oracle.verify_greedy(s.target[sl], s.tokens[sl])
-            return SAMPLE["k"]
-        oracle.verify_tree_greedy(t.logits[sl], t.node_tokens[sl], t.parents[sl], t.max_depth)
-        return TREE["N"] - 1
+            n = SAMPLE["k"]
+        else:
+            oracle.verify_tree_greedy(t.logits[sl], t.node_tokens[sl], t.parents[sl], t.max_depth)
+            n = TREE["N"] - 1
+        return n, time.perf_counter() - t0
 
     oracle.build()
     t0 = time.perf_counter()
     with ThreadPoolExecutor(cores) as pool:
-        positions = sum(pool.map(run, jobs))
+        done = list(pool.map(run, jobs))
     dt = time.perf_counter() - t0
+    positions = sum(n for n, _ in done)
+    cpu_s = sum(d for _, d in done)
     return {"value": positions / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{sample_seqs} sampling + {sample_seqs} greedy sequences (k=8, V=128256) and {trees} trees "
-                      f"(60 nodes) of the benchmark batch; {positions} positions in {dt:.2f} s"}
+            "sample": f"{passes} passes over the benchmark batch (64 sampling + 64 greedy sequences, k=8, "
+                      f"V=128256, and 8 trees of 60 nodes): {positions} positions, {cpu_s:.1f} s of CPU work, "
+                      f"{dt:.2f} s on {cores} threads"}
 
 
 # ------------------------------------------------------------------ main
@@ -417,6 +470,14 @@ def main():
                      "GB/s": tree_bytes() / (float(per[:, 2].mean()) / 1e3) / 1e9,
                      "frac": tree_bytes() / (float(per[:, 2].mean()) / 1e3) / 1e9 / peak,
                      "algorithmic_bytes": tree_bytes(), "traffic": recorded_traffic("argmax_tree")},
+        },
+        "outside_step": {
+            "tree_sample": {"us": r["tree_sample"][0], "algorithmic_bytes": r["tree_sample"][1],
+                            "GB/s": r["tree_sample"][1] / r["tree_sample"][0] / 1e3,
+                            "frac": r["tree_sample"][1] / r["tree_sample"][0] / 1e3 / peak,
+                            "mean_accepted": r["tree_sample"][2],
+                            "what": "token-tree sampling verification, 8 trees x 60 nodes, depth <= 6, "
+                                    "V=128256 bf16, T=1; plan + node + walk kernels, timed alone after an L2 flush"},
         },
         "acceptance": {"sample_mal": r["mal"], "greedy_mal": r["greedy_mal"], "k": SAMPLE["k"]},
         "status_bits": r["status"],
