@@ -33,6 +33,7 @@
 // decisions.
 
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -88,8 +89,114 @@ __device__ __forceinline__ float resid_weight(float l, float d, float c, float n
   const float ep = ex2_approx(fmaf(l, c, nmp));
   if (fb == 0.f) return ep;
   const float eq = ex2_approx(fmaf(d, c, nmq));
-  return fmaxf(0.f, fmaf(ep, fa, -(eq * fb)));
+  return fmaxf(0.f, fmaf(ep, fa, eq * -fb));
 }
+
+// ------------------------------------------------ packed float pairs (f32x2)
+using u64 = unsigned long long;
+__device__ __forceinline__ u64 pk2(uint32_t x, uint32_t y) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(x), "r"(y));
+  return r;
+}
+__device__ __forceinline__ u64 pkf(float x, float y) { return pk2(__float_as_uint(x), __float_as_uint(y)); }
+__device__ __forceinline__ void upk(u64 r, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+  u64 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Masses 2^(l c + nm) of two elements: per half the same fma and ex2 as the
+// scalar form in resid_weight.
+__device__ __forceinline__ u64 mass2(u64 l2, u64 c2, u64 nm2) {
+  float x, y;
+  upk(fma2(l2, c2, nm2), x, y);
+  return pkf(ex2_approx(x), ex2_approx(y));
+}
+// Residual weights of two elements: per half resid_weight with fb != 0.
+__device__ __forceinline__ u64 resid2(u64 lp2, u64 lq2, u64 c2, u64 np2, u64 nq2, u64 fa2, u64 nfb2) {
+  float x, y;
+  upk(fma2(mass2(lp2, c2, np2), fa2, mul2(mass2(lq2, c2, nq2), nfb2)), x, y);
+  return pkf(fmaxf(0.f, x), fmaxf(0.f, y));
+}
+// The element pairs of one 16-byte vector as float pairs.
+template <int DT>
+__device__ __forceinline__ u64 pair_of(const uint4& v, int h);
+template <>
+__device__ __forceinline__ u64 pair_of<DT_BF16>(const uint4& v, int h) {
+  const uint32_t w = h == 0 ? v.x : h == 1 ? v.y : h == 2 ? v.z : v.w;
+  return pk2(w << 16, w & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ u64 pair_of<DT_F32>(const uint4& v, int h) {
+  return h == 0 ? pk2(v.x, v.y) : pk2(v.z, v.w);
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Running maximum of a slice's 16-byte vectors, and whether it holds NaN or
+// +inf.  bf16: four packed accumulators whose maximum propagates NaN, so one
+// check at the end finds a bad value; f32: per element.
+template <int DT>
+struct VecMax;
+template <>
+struct VecMax<DT_BF16> {
+  __nv_bfloat162 m[4];
+  __device__ static __forceinline__ __nv_bfloat162 b2(uint32_t w) {
+    __nv_bfloat162 r;
+    *reinterpret_cast<uint32_t*>(&r) = w;
+    return r;
+  }
+  __device__ __forceinline__ VecMax() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = b2(0xFF80FF80u);
+  }
+  __device__ __forceinline__ void add(const uint4& v) {
+    m[0] = __hmax2_nan(m[0], b2(v.x));
+    m[1] = __hmax2_nan(m[1], b2(v.y));
+    m[2] = __hmax2_nan(m[2], b2(v.z));
+    m[3] = __hmax2_nan(m[3], b2(v.w));
+  }
+  __device__ __forceinline__ void finish(float& mx, int& bad) const {
+    const __nv_bfloat162 t = __hmax2_nan(__hmax2_nan(m[0], m[1]), __hmax2_nan(m[2], m[3]));
+    const float r = max_nan(__low2float(t), __high2float(t));
+    if (r != r || r == INFINITY) bad = 1;
+    else mx = fmaxf(mx, r);
+  }
+};
+template <>
+struct VecMax<DT_F32> {
+  float mx = -INFINITY;
+  int bad = 0;
+  __device__ __forceinline__ void add(const uint4& v) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t bits = Elt<DT_F32>::bits_of(v, e);
+      bad |= bad_bits<DT_F32>(bits);
+      mx = fmaxf(mx, __uint_as_float(bits));
+    }
+  }
+  __device__ __forceinline__ void finish(float& m_out, int& bad_out) const {
+    bad_out |= bad;
+    m_out = fmaxf(m_out, mx);
+  }
+};
 
 __device__ __forceinline__ double warp_sum_f64(double v) {
 #pragma unroll
@@ -244,24 +351,13 @@ __device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned 
       tmo = 1;
     } else {
       const int nv = len / PV;  // aligned rows: len is a whole number of vectors
+      VecMax<DT> xp, xq;
       for (int v = threadIdx.x; v < nv; v += kThreads) {
-        const uint4 x = lds128(sp + 16u * v);
-#pragma unroll
-        for (int e = 0; e < PV; ++e) {
-          const uint32_t bits = Elt<DT>::bits_of(x, e);
-          bp |= bad_bits<DT>(bits);
-          mp = fmaxf(mp, Elt<DT>::value(bits));
-        }
-        if (with_q) {
-          const uint4 y = lds128(sq + 16u * v);
-#pragma unroll
-          for (int e = 0; e < PV; ++e) {
-            const uint32_t bits = Elt<DT>::bits_of(y, e);
-            bq |= bad_bits<DT>(bits);
-            mq = fmaxf(mq, Elt<DT>::value(bits));
-          }
-        }
+        xp.add(lds128(sp + 16u * v));
+        if (with_q) xq.add(lds128(sq + 16u * v));
       }
+      xp.finish(mp, bp);
+      if (with_q) xq.finish(mq, bq);
     }
   } else {
     for (int i = threadIdx.x; i < len; i += kThreads) {
@@ -274,6 +370,18 @@ __device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned 
         bq |= bad_bits<DT>(b2);
         mq = fmaxf(mq, Elt<DT>::value(b2));
         if (E == 2) sts_u16(sq + 2u * i, b2); else sts_u32(sq + 4u * i, b2);
+      }
+    }
+    // pad the last vector with -inf: the passes read whole vectors
+    const int pad = (len + PV - 1) / PV * PV - len;
+    if (static_cast<int>(threadIdx.x) < pad) {
+      const int i = len + threadIdx.x;
+      if (E == 2) {
+        sts_u16(sp + 2u * i, 0xFF80u);
+        if (with_q) sts_u16(sq + 2u * i, 0xFF80u);
+      } else {
+        sts_u32(sp + 4u * i, 0xFF800000u);
+        if (with_q) sts_u32(sq + 4u * i, 0xFF800000u);
       }
     }
   }
@@ -317,42 +425,60 @@ template <int DT>
 __device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
                             int slot);
 
-// Sums over this CTA's slice, per warp chunk (16-byte vectors, lanes
-// interleaved, float per lane, double across lanes).  MODE 0: target and
-// draft masses (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
+// Sums over this CTA's slice, per warp chunk: 16-byte vectors, lanes
+// interleaved, float pairs per lane (two accumulators), double across lanes.
+// The slice is whole vectors (lenv elements; an unaligned slice is padded
+// with -inf, which has no mass and no weight).  MODE 0: target and draft
+// masses (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
 template <int DT, int MODE>
-__device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
+__device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int lenv, int wchunk, bool with_q, float c,
                            float nmp, float nmq, float fa, float fb) {
   constexpr int PV = Elt<DT>::kPerVec;
+  constexpr int NP = PV / 2;  // element pairs per vector
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wlo = warp * wchunk;
-  const int whi = min(len, wlo + wchunk);
-  float s0 = 0.f, s1 = 0.f;
+  const int whi = min(lenv, wlo + wchunk);
+  const u64 c2 = pkf(c, c), np2 = pkf(nmp, nmp), nq2 = pkf(nmq, nmq), fa2 = pkf(fa, fa), nfb2 = pkf(-fb, -fb);
+  u64 a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
   for (int i0 = wlo + lane * PV; i0 < whi; i0 += 32 * PV) {
-    const uint4 x = lds128(sp + 16u * static_cast<uint32_t>(i0 / PV));
-    uint4 y = make_uint4(0u, 0u, 0u, 0u);
-    if (MODE == 1 || with_q) y = lds128(sq + 16u * static_cast<uint32_t>(i0 / PV));
+    const uint32_t off = 16u * static_cast<uint32_t>(i0 / PV);
+    const uint4 x = lds128(sp + off);
+    if (MODE == 0) {
 #pragma unroll
-    for (int e = 0; e < PV; ++e) {
-      if (i0 + e < whi) {
-        const float l = Elt<DT>::value(Elt<DT>::bits_of(x, e));
-        if (MODE == 0) {
-          s0 += ex2_approx(fmaf(l, c, nmp));
-          if (with_q) s1 += ex2_approx(fmaf(Elt<DT>::value(Elt<DT>::bits_of(y, e)), c, nmq));
-        } else {
-          s0 += resid_weight(l, Elt<DT>::value(Elt<DT>::bits_of(y, e)), c, nmp, nmq, fa, fb);
+      for (int h = 0; h < NP; ++h) {
+        if (h & 1) a1 = add2(a1, mass2(pair_of<DT>(x, h), c2, np2));
+        else a0 = add2(a0, mass2(pair_of<DT>(x, h), c2, np2));
+      }
+      if (with_q) {
+        const uint4 y = lds128(sq + off);
+#pragma unroll
+        for (int h = 0; h < NP; ++h) {
+          if (h & 1) b1 = add2(b1, mass2(pair_of<DT>(y, h), c2, nq2));
+          else b0 = add2(b0, mass2(pair_of<DT>(y, h), c2, nq2));
         }
+      }
+    } else {
+      const uint4 y = lds128(sq + off);
+#pragma unroll
+      for (int h = 0; h < NP; ++h) {
+        const u64 r2 = resid2(pair_of<DT>(x, h), pair_of<DT>(y, h), c2, np2, nq2, fa2, nfb2);
+        if (h & 1) a1 = add2(a1, r2);
+        else a0 = add2(a0, r2);
       }
     }
   }
-  const double d0 = warp_sum_f64(static_cast<double>(s0));
-  const double d1 = MODE == 0 ? warp_sum_f64(static_cast<double>(s1)) : 0.0;
+  float x0, y0, x1, y1;
+  upk(add2(a0, a1), x0, y0);
+  upk(add2(b0, b1), x1, y1);
+  const double d0 = warp_sum_f64(static_cast<double>(x0) + static_cast<double>(y0));
+  const double d1 = MODE == 0 ? warp_sum_f64(static_cast<double>(x1) + static_cast<double>(y1)) : 0.0;
   if (lane == 0) {
     sh.wsum[warp][0] = d0;
     sh.wsum[warp][1] = d1;
   }
   __syncthreads();
 }
+
 
 template <int DT>
 __device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
@@ -637,6 +763,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
   const uint32_t sq = sp + static_cast<uint32_t>(a.slice) * E;
   const int lo = rank * a.slice;
   const int len = max(0, min(a.V, lo + a.slice) - lo);
+  const int lenv = (len + Elt<DT>::kPerVec - 1) / Elt<DT>::kPerVec * Elt<DT>::kPerVec;  // whole vectors
   const int total = min(static_cast<int>(*a.work_count), a.B * a.N);
   if (threadIdx.x == 0) {
     mbar_init(&sh.bar[0], 1);
@@ -672,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     stage_rows<DT>(a, sh, pfull + static_cast<size_t>(lo) * E, qfull + static_cast<size_t>(lo) * E, len, true,
                    sp, sq, php, phq, true);
     int slot = round++ & 1;
-    slice_stats<DT>(sh, sp, sq, len, a.wchunk, true, a.c, slot);
+    slice_stats<DT>(sh, sp, sq, lenv, a.wchunk, true, a.c, slot);
     uint32_t rflags = 0;
     int accepted = -1;
     bool cz = true;
@@ -711,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
         cc += W;
         fa = static_cast<float>(1.0 / zp);
         fb = static_cast<float>(cc / zq);
-        slice_pass<DT, 1>(sh, sp, sq, len, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+        slice_pass<DT, 1>(sh, sp, sq, lenv, a.wchunk, true, a.c, nmp, nmq, fa, fb);
         slot = round++ & 1;
         if (threadIdx.x == 0) {
           double sum = 0.0;
@@ -828,7 +955,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
     uint32_t php = 0, phq = 0;
     stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + (g * a.V + lo) * E, nullptr, len, false,
                    sp, sp, php, phq, false);
-    slice_stats<DT>(sh, sp, sp, len, a.wchunk, false, a.c, 0);
+    slice_stats<DT>(sh, sp, sp, (len + Elt<DT>::kPerVec - 1) / Elt<DT>::kPerVec * Elt<DT>::kPerVec, a.wchunk, false,
+                    a.c, 0);
     const float mp = static_cast<float>(sh.got[0]);
     if (sh.got[4] != 0.0 || mp == -INFINITY) {
       ok = false;
