@@ -100,6 +100,7 @@ def time_tree_sample(sv, dev, ws, stream, seed, iters=20):
 KERNEL_SOURCES = {
     "sample": ("sample_kernel.cu", "device_common.cuh", "internal.h"),
     "argmax": ("argmax_kernel.cu", "device_common.cuh", "internal.h"),
+    "tree_sample": ("tree_sample_kernel.cu", "device_common.cuh", "internal.h"),
 }
 
 
@@ -356,10 +357,10 @@ def run_gpu(args, rank, world):
 # ------------------------------------------------------------ CPU leg
 
 
-def cpu_baseline(passes: int = 4, threads: int | None = None):
+def cpu_baseline(passes: int = 6, threads: int | None = None):
     """The float64 oracle, as it stands, on a bounded sample of the same
     workload: `passes` passes over the whole benchmark batch (64 sampling and
-    64 greedy sequences, 8 trees), about 15-20 s of CPU work, spread over the
+    64 greedy sequences, 8 trees), about 10-30 s of CPU work, spread over the
     host's cores one sequence or tree per task."""
     import oracle
 
@@ -475,7 +476,7 @@ def main():
             "tree_sample": {"us": r["tree_sample"][0], "algorithmic_bytes": r["tree_sample"][1],
                             "GB/s": r["tree_sample"][1] / r["tree_sample"][0] / 1e3,
                             "frac": r["tree_sample"][1] / r["tree_sample"][0] / 1e3 / peak,
-                            "mean_accepted": r["tree_sample"][2],
+                            "mean_accepted": r["tree_sample"][2], "traffic": recorded_traffic("tree_sample"),
                             "what": "token-tree sampling verification, 8 trees x 60 nodes, depth <= 6, "
                                     "V=128256 bf16, T=1; plan + node + walk kernels, timed alone after an L2 flush"},
         },

@@ -145,3 +145,57 @@ def test_repeat_calls_identical():
     b = run_gpu(case)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def _custom_case(parents, V, seed, dtype=W.F32, noise=1.5, T=1.0, max_depth=None):
+    """A tree with the given parent arrays [B][N]; rows and tokens as in
+    tree_sample_case (children drawn from their parents' draft rows)."""
+    parents = np.asarray(parents, np.int32)
+    B, N = parents.shape
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0.0, 3.0, size=(B, N, V)).astype(np.float32)
+    d = (x + rng.normal(0.0, noise, size=x.shape)).astype(np.float32)
+    logits = W.bf16_bits(x) if dtype == W.BF16 else x
+    draft = W.bf16_bits(d) if dtype == W.BF16 else d
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        rows = W.as_f32(draft[b]).astype(np.float64) / T
+        for j in range(1, N):
+            g = -np.log(-np.log(rng.random(V).clip(1e-300, None)))
+            tokens[b, j] = int(np.argmax(rows[parents[b, j]] + g))
+    depth = max_depth
+    if depth is None:
+        dep = np.zeros((B, N), int)
+        for b in range(B):
+            for j in range(1, N):
+                dep[b, j] = dep[b, parents[b, j]] + 1
+        depth = max(1, int(dep.max()))
+    return W.TreeSampleCase("custom", dtype, logits, draft, tokens, parents,
+                            rng.random((B, N), dtype=np.float32), depth, T, seed)
+
+
+def test_many_siblings_past_the_prefetched_ones():
+    """A root with 70 children (only the first 32 have their logits fetched
+    ahead) and a far draft, so that many siblings are rejected in turn."""
+    N = 71
+    par = np.tile(np.array([-1] + [0] * (N - 1), np.int32), (6, 1))
+    case = _custom_case(par, 2000, seed=31, noise=4.0)
+    case.uniforms[:, 1:] = np.float32(0.999)  # reject nearly every child
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_deep_chain_tree():
+    """A chain of 200 nodes: a depth walk of up to 199 steps per node."""
+    N = 200
+    par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (3, 1))
+    case = _custom_case(par, 512, seed=32, dtype=W.BF16, noise=0.05)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_unaligned_pointers():
+    sv = lib()
+    case = W.tree_sample_case(4, 20, 4000, 4, seed=33, dtype=W.BF16)
+    flat = np.concatenate([np.zeros(1, np.uint16), case.logits.ravel()])
+    L = to_dev(flat)[1:].view(case.logits.shape)
+    assert L.data_ptr() % 16 != 0
+    compare(case, run_gpu(case, logits=L), run_oracle(case))
