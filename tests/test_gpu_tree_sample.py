@@ -199,3 +199,20 @@ def test_unaligned_pointers():
     L = to_dev(flat)[1:].view(case.logits.shape)
     assert L.data_ptr() % 16 != 0
     compare(case, run_gpu(case, logits=L), run_oracle(case))
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_masked_vocabulary(dtype):
+    """-inf logits in both rows (30% of tokens, and whole chunks of some rows)."""
+    case = W.tree_sample_case(6, 24, 20000, 4, seed=34, dtype=W.F32, noise=1.0)
+    rng = np.random.default_rng(35)
+    L, Dr = case.logits.copy(), case.draft.copy()
+    for arr in (L, Dr):
+        arr[rng.random(arr.shape) < 0.3] = -np.inf
+        arr[:, ::3, 2000:9000] = -np.inf
+        arr[:, :, 0] = 0.0
+    if dtype == W.BF16:
+        L, Dr = W.bf16_bits(L), W.bf16_bits(Dr)
+    case = W.TreeSampleCase("masked", dtype, L, Dr, case.node_tokens, case.parents, case.uniforms,
+                            case.max_depth, case.temperature, case.seed)
+    compare(case, run_gpu(case), run_oracle(case))

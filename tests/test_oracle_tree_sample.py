@@ -283,3 +283,24 @@ def test_paths_are_root_paths(dtype):
         assert (out["path"][b, n:] == -1).all() and (out["tokens"][b, n + 1:] == -1).all()
     # with a draft close to the target most trees accept at least one node
     assert (out["n"] > 0).mean() > 0.5
+
+
+def test_masked_tokens_are_never_drawn_or_accepted_from_zero_mass():
+    """Tokens with target logit -inf have p = 0: the residual max(0, r - q) is 0
+    there too, so no draw lands on them; a child whose token has p = 0 is never
+    accepted (u * q(x) < 0 fails for every u >= 0)."""
+    rng = np.random.default_rng(41)
+    case = W.tree_sample_case(40, 15, 64, 3, seed=41, dtype=W.F32, noise=1.0)
+    L = case.logits.copy()
+    mask = rng.random(L.shape) < 0.3
+    mask[:, :, 0] = False  # every row keeps a finite entry
+    L[mask] = -np.inf
+    out = oracle.verify_tree_sample(L, case.draft, case.node_tokens, case.parents, case.uniforms, case.max_depth)
+    for b in range(case.B):
+        n = out["n"][b]
+        prev = 0
+        for d in range(n):
+            node = out["path"][b, d]
+            assert not mask[b, prev, case.node_tokens[b, node]]
+            prev = node
+        assert not mask[b, prev, out["tokens"][b, n]]
