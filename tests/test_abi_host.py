@@ -111,6 +111,24 @@ def test_greedy_and_tree_reject_bad_arguments(L):
     assert L.spec_get_status(None, ctypes.byref(st), None) == sv.SPEC_ERR_INVALID_ARG
 
 
+def test_tree_sample_rejects_bad_arguments(L):
+    ts = L.spec_verify_tree_sample
+
+    def call(nl=FAKE, dl=FAKE, uni=FAKE, B=2, N=60, V=100, depth=6, dt=1, T=1.0, wsb=1 << 30):
+        return ts(nl, dl, FAKE, FAKE, uni, B, N, V, depth, dt, T, FAKE, FAKE, FAKE, FAKE, wsb, None)
+
+    assert call(dt=9) == sv.SPEC_ERR_DTYPE
+    assert call(dl=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(N=1025) == sv.SPEC_ERR_INVALID_ARG
+    assert call(depth=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(T=0.0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(T=float("nan")) == sv.SPEC_ERR_INVALID_ARG
+    assert call(uni=ctypes.c_void_p(4098)) == sv.SPEC_ERR_INVALID_ARG  # float needs 4-byte alignment
+    assert call(wsb=8) == sv.SPEC_ERR_WORKSPACE
+    # a CTA's share of both rows must fit its shared memory: V = 300000 f32 does not
+    assert call(V=300000, dt=0) == sv.SPEC_ERR_UNSUPPORTED
+
+
 def test_calculator_helpers_match_golden(L):
     with open(os.path.join(ROOT, "tests", "golden", "closed_forms.json")) as f:
         g = json.load(f)
