@@ -331,6 +331,7 @@ int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, c
   a.status = reinterpret_cast<uint32_t*>(w + L.status);
   a.recs = reinterpret_cast<TreeRec*>(w + L.trecs);
   a.work_count = reinterpret_cast<uint32_t*>(w + L.tlist);
+  a.work_next = reinterpret_cast<uint32_t*>(w + L.tlist + 4);
   a.work_list = reinterpret_cast<int32_t*>(w + L.tlist + 16);
   if (launch_tree_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, cuda_stream) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)

@@ -116,7 +116,8 @@ struct WsLayout {
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
   size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
   size_t trecs;       // TreeRec[B*(k+1)]  tree sampling: one record per node
-  size_t tlist;       // uint32 count (zero between calls), then int32[B*(k+1)] nodes with children to test
+  size_t tlist;       // uint32 count and uint32 claimed items (zero between calls), then
+                      // int32[B*(k+1)] nodes with children to test
   size_t total;
 };
 
@@ -200,6 +201,7 @@ struct TreeSampleArgs {
   uint32_t* status;
   TreeRec* recs;               // [B][N]
   uint32_t* work_count;        // nodes in work_list (zero between calls)
+  uint32_t* work_next;         // node-kernel work items claimed past the first round (zero between calls)
   int32_t* work_list;          // node ids b*N + j with children to test
 };
 

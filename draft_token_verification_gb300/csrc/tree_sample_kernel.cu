@@ -65,6 +65,8 @@ struct TreeShm {
   float mloc[2];             // this CTA's maxima (target, draft)
   int badloc;               // this CTA's slices hold NaN / +inf (or did not arrive)
   int nk, has_child, depth, attached, accept, timed_out;
+  int next[2];               // rank 0: the next work item claimed, by node parity
+  int nextl;                 // that item, read by every CTA of the cluster
   int walk_v, walk_n, walk_ok, draw_w;
   double draw_rem;
 };
@@ -685,7 +687,8 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   __shared__ int16_t par[kMaxTreeNodes];
   __shared__ int16_t dep[kMaxTreeNodes];
   __shared__ uint8_t has_child[kMaxTreeNodes];
-  __shared__ uint8_t testable_child[kMaxTreeNodes];
+  __shared__ int testable_child[kMaxTreeNodes];  // children to test, per node
+  __shared__ int16_t raw[kMaxTreeNodes];
   __shared__ int16_t list[kMaxTreeNodes];
   __shared__ int cnt, base;
   const int b = blockIdx.x, tid = threadIdx.x, N = a.N;
@@ -720,13 +723,13 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
     const int p = par[i];
     if (p >= 0 && p < i && dep[p] >= 0) {
       has_child[p] = 1;
-      if (dep[p] < a.max_depth && tok[i] >= 0 && tok[i] < a.V) testable_child[p] = 1;
+      if (dep[p] < a.max_depth && tok[i] >= 0 && tok[i] < a.V) atomicAdd(&testable_child[p], 1);
     }
   }
   __syncthreads();
   for (int i = tid; i < N; i += kThreads) {
     if (testable_child[i]) {
-      list[atomicAdd(&cnt, 1)] = static_cast<int16_t>(i);
+      raw[atomicAdd(&cnt, 1)] = static_cast<int16_t>(i);
     } else {
       TreeRec* rec = a.recs + static_cast<size_t>(b) * N + i;
       uint32_t fl = kRecDetached;
@@ -741,6 +744,16 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   }
   if (st) atomicOr(a.status, st);
   __syncthreads();
+  // order: more children to test first (more possible residual passes), then node index
+  for (int i = tid; i < cnt; i += kThreads) {
+    const int ni = raw[i], ci = testable_child[ni];
+    int r = 0;
+    for (int t = 0; t < cnt; ++t) {
+      const int nt = raw[t], ct = testable_child[nt];
+      r += (ct > ci || (ct == ci && nt < ni)) ? 1 : 0;
+    }
+    list[r] = static_cast<int16_t>(ni);
+  }
   if (tid == 0) base = static_cast<int>(atomicAdd(a.work_count, static_cast<uint32_t>(cnt)));
   __syncthreads();
   const int cap = a.B * N;  // the list's length; the count is zero on entry
@@ -774,9 +787,12 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
   __syncthreads();
   uint32_t php = 0, phq = 0;
   int round = 0;
-  for (int idx = cid; idx < total; idx += ncl) {
+  // the first round takes items cid; later items are claimed from a shared
+  // counter, one ahead, during each node's first cluster round
+  int kpar = 0;
+  for (int idx = cid; idx < total; ++kpar) {
     const int64_t g = a.work_list[idx];
-    if (g < 0 || g >= static_cast<int64_t>(a.B) * a.N) continue;  // uniform across the cluster
+    if (g < 0 || g >= static_cast<int64_t>(a.B) * a.N) break;  // uniform across the cluster
     const int b = static_cast<int>(g / a.N), j = static_cast<int>(g % a.N);
     const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
     const float* uni = a.uniforms + static_cast<size_t>(b) * a.N;
@@ -799,7 +815,10 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     stage_rows<DT>(a, sh, pfull + static_cast<size_t>(lo) * E, qfull + static_cast<size_t>(lo) * E, len, true,
                    sp, sq, php, phq, true);
     int slot = round++ & 1;
-    slice_stats<DT>(sh, sp, sq, lenv, a.wchunk, true, a.c, slot);
+    if (rank == 0 && threadIdx.x == 0) sh.next[kpar & 1] = ncl + static_cast<int>(atomicAdd(a.work_next, 1u));
+    slice_stats<DT>(sh, sp, sq, lenv, a.wchunk, true, a.c, slot);  // (its cluster barrier publishes sh.next)
+    if (threadIdx.x == 0)
+      sh.nextl = static_cast<int>(ld_cluster_u32(mapa_shared(smem_addr(&sh.next[kpar & 1]), 0)));
     uint32_t rflags = 0;
     int accepted = -1;
     bool cz = true;
@@ -875,6 +894,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
       rec->fb = cz ? 0.f : fb;
     }
     __syncthreads();  // every read of this node's slices and of sh.par is done
+    idx = sh.nextl;
   }
   if (sh.timed_out && threadIdx.x == 0) {  // let copies still in flight land before the CTA leaves
     mbar_wait_bounded(&sh.bar[0], php ^ 1u);
@@ -987,7 +1007,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
       a.out_n[b] = n;
     }
   }
-  if (blockIdx.x == 0 && tid == 0) *a.work_count = 0;  // the node pass has read it; zero for the next call
+  if (blockIdx.x == 0 && tid == 0) {  // the node pass has read both: zero for the next call
+    *a.work_count = 0u;
+    *a.work_next = 0u;
+  }
   cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
@@ -1041,7 +1064,7 @@ int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
     cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kTreeCl);
     e = cudaLaunchKernelEx(&cfg, walk_k, a);
   }
-  if (e != cudaSuccess) cudaMemsetAsync(a.work_count, 0, sizeof(uint32_t), st);  // the walk did not reset it
+  if (e != cudaSuccess) cudaMemsetAsync(a.work_count, 0, 2 * sizeof(uint32_t), st);  // the walk did not reset them
   return e;
 }
 
