@@ -121,9 +121,10 @@ def test_nonfinite_row_on_the_walk():
 
 
 def test_workspace_shared_with_other_entry_points():
-    """Tree sampling leaves its tickets zeroed: chain sampling, greedy tree and
-    tree sampling calls on one workspace all keep their parity."""
-    from parity_utils import compare_sample, run_sample_gpu, run_sample_oracle, run_tree_gpu
+    """Tree sampling leaves its work counts zeroed and the other entry points'
+    regions untouched: chain sampling, greedy tree and tree sampling calls on
+    one workspace all keep their parity."""
+    from parity_utils import compare_sample, run_sample_gpu, run_sample_oracle
 
     sv = lib()
     ws = sv.Workspace()
