@@ -176,3 +176,59 @@ def first_token_law(p: Dist, q: Dist, k: int) -> Dict[int, Fraction]:
             t = toks[idx] if kind == "accept" else idx
             out[t] = out.get(t, Fraction(0)) + pr * m
     return out
+
+
+def tree_pass_law(P: Table, Q: Table, prefix: Tuple[int, ...], fanout: Sequence[int]) -> Dict[Tuple[int, ...], Fraction]:
+    """Law of the tokens one tree-verification pass commits after ``prefix``.
+
+    The draft tree has ``fanout[d]`` children under every node at depth d
+    (leaves at depth len(fanout)); the children of the node reached by path
+    ``acc`` are independent draws from Q(prefix + acc).  At each node the
+    children are checked with :func:`sibling_law` against P(prefix + acc);
+    an accepted child moves the walk into its subtree, a node that accepts
+    none commits its draw, and a leaf commits a bonus token from its P.
+    """
+    law: Dict[Tuple[int, ...], Fraction] = {}
+
+    def node(acc: Tuple[int, ...], mass: Fraction, depth: int) -> None:
+        ctx = prefix + acc
+        p = P(ctx)
+        if depth == len(fanout):
+            for t, pt in enumerate(p):
+                if pt:
+                    key = acc + (t,)
+                    law[key] = law.get(key, Fraction(0)) + mass * pt
+            return
+        q = Q(ctx)
+        V = len(p)
+        for toks in product(range(V), repeat=fanout[depth]):
+            pr = Fraction(1)
+            for x in toks:
+                pr *= q[x]
+            if pr == 0:
+                continue
+            for (kind, idx), m in sibling_law(p, q, toks).items():
+                if kind == "accept":
+                    node(acc + (toks[idx],), mass * pr * m, depth + 1)
+                else:
+                    key = acc + (idx,)
+                    law[key] = law.get(key, Fraction(0)) + mass * pr * m
+
+    node((), Fraction(1), 0)
+    return law
+
+
+def tree_sequence_law(P: Table, Q: Table, fanout: Sequence[int], m: int) -> Dict[Tuple[int, ...], Fraction]:
+    """Law of the first ``m`` tokens when tree passes are repeated from the empty prefix."""
+    out: Dict[Tuple[int, ...], Fraction] = {}
+
+    def run(prefix: Tuple[int, ...], mass: Fraction) -> None:
+        if len(prefix) >= m:
+            key = prefix[:m]
+            out[key] = out.get(key, Fraction(0)) + mass
+            return
+        for emitted, pr in tree_pass_law(P, Q, prefix, fanout).items():
+            run(prefix + emitted, mass * pr)
+
+    run((), Fraction(1))
+    return out

@@ -42,6 +42,8 @@ MUTATIONS = [
     ("tree residual left unnormalised", "for (t = 0; t < V; ++t) r[t] /= s;", "s = s;"),
     ("tree final draw from p", "drawn = inverse_cdf(r, V, (double)u[0], &mg);",
      "drawn = inverse_cdf(p, V, (double)u[0], &mg);"),
+    ("tree walk keeps the parent's rows after an acceptance", "        v = accepted;\n        continue;",
+     "        (void)accepted;\n        continue;"),
 ]
 
 PIN_FILES = ("test_oracle_pins.py", "test_oracle_tree_sample.py")

@@ -304,3 +304,77 @@ def test_masked_tokens_are_never_drawn_or_accepted_from_zero_mass():
             assert not mask[b, prev, case.node_tokens[b, node]]
             prev = node
         assert not mask[b, prev, out["tokens"][b, n]]
+
+
+# ------------------------------------------------ multi-level trees, exact law
+
+
+def _table(seed, V, zero=False):
+    """A prefix-dependent distribution table with memoised random rational rows."""
+    rng = np.random.default_rng(seed)
+    cache = {}
+
+    def f(ctx):
+        if ctx not in cache:
+            w = [Fraction(int(x)) for x in rng.integers(1, 9, size=V)]
+            if zero:
+                w[int(rng.integers(0, V))] = Fraction(0)
+            s = sum(w)
+            cache[ctx] = [x / s for x in w]
+        return cache[ctx]
+
+    return f
+
+
+@pytest.mark.parametrize("fanout,V,m,seed", [([1], 3, 3, 0), ([2], 3, 3, 1), ([2, 2], 3, 3, 2),
+                                             ([3, 1], 2, 3, 3), ([1, 1, 1], 3, 3, 4), ([2, 1], 3, 2, 5)])
+def test_repeated_tree_passes_give_the_target_sequence_law(fanout, V, m, seed):
+    """Tree passes repeated from the empty prefix, children drawn from their
+    node's draft table: the committed text has exactly the target's law."""
+    P = _table(100 + seed, V)
+    Q = _table(200 + seed, V, zero=(seed % 2 == 1))
+    assert exact.tree_sequence_law(P, Q, fanout, m) == exact.product_law(P, V, m)
+
+
+def test_c_oracle_tree_pass_follows_the_exact_law():
+    """Two-level tree (2 children, 2 grandchildren each), V = 3: the C
+    oracle's committed tokens over random child draws and uniforms follow
+    exact.tree_pass_law (chi-square over all committed sequences)."""
+    from scipy import stats
+
+    V, S = 3, 40000
+    P, Q = _table(7, V), _table(8, V)
+    ctxs = [()] + [(a,) for a in range(V)] + [(a, c) for a in range(V) for c in range(V)]
+    lp = {c: np.log(np.array([float(x) for x in P(c)])).astype(np.float32) for c in ctxs}
+    lq = {c: np.log(np.array([float(x) for x in Q(c)])).astype(np.float32) for c in ctxs}
+    qf = {c: np.array([float(x) for x in Q(c)]) for c in ctxs}
+    rng = np.random.default_rng(9)
+    N = 7  # root; 1, 2 under the root; 3, 4 under 1; 5, 6 under 2
+    par = np.tile(np.array([-1, 0, 0, 1, 1, 2, 2], np.int32), (S, 1))
+    toks = np.zeros((S, N), np.int32)
+    toks[:, 1] = rng.choice(V, size=S, p=qf[()])
+    toks[:, 2] = rng.choice(V, size=S, p=qf[()])
+    L = np.empty((S, N, V), np.float32)
+    D = np.empty((S, N, V), np.float32)
+    for s in range(S):
+        c1, c2 = (int(toks[s, 1]),), (int(toks[s, 2]),)
+        toks[s, 3:5] = rng.choice(V, size=2, p=qf[c1])
+        toks[s, 5:7] = rng.choice(V, size=2, p=qf[c2])
+        ctx = [(), c1, c2, c1 + (int(toks[s, 3]),), c1 + (int(toks[s, 4]),), c2 + (int(toks[s, 5]),),
+               c2 + (int(toks[s, 6]),)]
+        for j in range(N):
+            L[s, j] = lp[ctx[j]] if len(ctx[j]) < 3 else 0.0
+            D[s, j] = lq[ctx[j]] if len(ctx[j]) < 3 else 0.0
+    u = rng.random((S, N), dtype=np.float32)
+    out = oracle.verify_tree_sample(L, D, toks, par, u, 2)
+    law = exact.tree_pass_law(P, Q, (), [2, 2])
+    keys = sorted(law)
+    index = {k: i for i, k in enumerate(keys)}
+    counts = np.zeros(len(keys))
+    for s in range(S):
+        n = int(out["n"][s])
+        counts[index[tuple(int(x) for x in out["tokens"][s, :n + 1])]] += 1
+    expected = np.array([float(law[k]) for k in keys]) * S
+    assert abs(sum(float(law[k]) for k in keys) - 1.0) < 1e-12
+    _, pval = stats.chisquare(counts, expected)
+    assert pval > 1e-4, list(zip(keys, counts, expected))
