@@ -217,3 +217,9 @@ def test_masked_vocabulary(dtype):
     case = W.TreeSampleCase("masked", dtype, L, Dr, case.node_tokens, case.parents, case.uniforms,
                             case.max_depth, case.temperature, case.seed)
     compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_maximum_tree_size():
+    """N = 1024 nodes (the limit), up to 4 children per node, depth <= 12."""
+    case = W.tree_sample_case(2, 1024, 2048, 12, seed=36, dtype=W.BF16, noise=0.7)
+    compare(case, run_gpu(case), run_oracle(case))
