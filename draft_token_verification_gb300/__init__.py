@@ -106,7 +106,7 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_greedy.restype = I
             L.spec_verify_tree_greedy.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, SZ, P]
             L.spec_verify_tree_greedy.restype = I
-            L.spec_verify_tree_sample.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P, P, P, P, SZ, P]
+            L.spec_verify_tree_sample.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.spec_verify_tree_sample.restype = I
             L.spec_transform_probs.argtypes = [P, I, I, I, P, P, P, SZ, P]
             L.spec_transform_probs.restype = I
@@ -349,11 +349,12 @@ def spec_verify_tree_greedy(node_logits: torch.Tensor, node_tokens: torch.Tensor
 
 def spec_verify_tree_sample(node_logits: torch.Tensor, draft_logits: torch.Tensor, node_tokens: torch.Tensor,
                             parents: torch.Tensor, uniforms: torch.Tensor, max_depth: int,
-                            temperature: float = 1.0, out_tokens=None, out_path=None, out_num_accepted=None,
-                            workspace=None, stream=None):
+                            temperature: float = 1.0, temperature_per_tree: Optional[torch.Tensor] = None,
+                            out_tokens=None, out_path=None, out_num_accepted=None, workspace=None, stream=None):
     """Token-tree sampling verification.  node_logits / draft_logits [B][N][V],
     node_tokens / parents [B][N] int32, uniforms [B][N] float32 (u_0 the final
-    draw, u_j the test of node j).  Returns (tokens, path [B][max_depth+1], n [B])."""
+    draw, u_j the test of node j); temperature_per_tree [B] float32 or None.
+    Returns (tokens, path [B][max_depth+1], n [B])."""
     B, N, V = node_logits.shape
     if tuple(draft_logits.shape) != (B, N, V) or draft_logits.dtype != node_logits.dtype:
         raise ValueError("draft_logits must match node_logits in shape and dtype")
@@ -371,6 +372,7 @@ def spec_verify_tree_sample(node_logits: torch.Tensor, draft_logits: torch.Tenso
         _dev(node_logits, "node_logits"), _dev(draft_logits, "draft_logits"),
         _dev(node_tokens, "node_tokens", torch.int32), _dev(parents, "parents", torch.int32),
         _dev(uniforms, "uniforms", torch.float32), B, N, V, int(max_depth), dt, float(temperature),
+        _dev(temperature_per_tree, "temperature_per_tree", torch.float32),
         _dev(out_tokens, "out_tokens", torch.int32), _dev(out_path, "out_path", torch.int32),
         _dev(out_num_accepted, "out_num_accepted", torch.int32), ws.data_ptr(), ws.numel(), _stream(stream),
     )

@@ -288,7 +288,8 @@ int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
 
 int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, const int32_t* node_tokens,
                             const int32_t* parents, const float* uniforms, int B, int N, int V, int max_depth,
-                            spec_dtype dtype, float temperature, int32_t* out_tokens, int32_t* out_path,
+                            spec_dtype dtype, float temperature, const float* temperature_per_tree,
+                            int32_t* out_tokens, int32_t* out_path,
                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                             void* cuda_stream) {
   if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
@@ -297,10 +298,11 @@ int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, c
     return SPEC_ERR_INVALID_ARG;
   if (B < 1 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V || max_depth < 1)
     return SPEC_ERR_INVALID_ARG;
-  if (!(temperature > 0.f && isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  if (!temperature_per_tree && !(temperature > 0.f && isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
   const size_t es = elt_bytes(dtype);
   if (!aligned_to(node_logits, es) || !aligned_to(draft_logits, es) || !aligned_to(node_tokens, 4) ||
-      !aligned_to(parents, 4) || !aligned_to(uniforms, 4))
+      !aligned_to(parents, 4) || !aligned_to(uniforms, 4) ||
+      (temperature_per_tree && !aligned_to(temperature_per_tree, 4)))
     return SPEC_ERR_INVALID_ARG;
   const int rc = check_workspace(workspace, workspace_bytes, B, N - 1);
   if (rc != SPEC_OK) return rc;
@@ -319,7 +321,8 @@ int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, c
   a.N = N;
   a.V = V;
   a.max_depth = max_depth;
-  a.c = 1.4426950408889634f / temperature;  // log2(e) / T, as in the chain kernels
+  a.c = temperature_per_tree ? 0.f : 1.4426950408889634f / temperature;  // log2(e) / T, as in the chain kernels
+  a.temps = temperature_per_tree;
   a.slice = slice;
   // warp chunks are whole rounds of 32 lanes x one 16-byte vector
   const int round_elems = 32 * vec_elems(dtype);

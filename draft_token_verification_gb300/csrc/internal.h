@@ -191,7 +191,8 @@ struct TreeSampleArgs {
   const int32_t* parents;      // [B][N]
   const float* uniforms;       // [B][N]
   int B, N, V, max_depth;
-  float c;                     // log2(e) / T
+  float c;                     // log2(e) / T (scalar temperature)
+  const float* temps;          // [B] per-tree temperatures, or null
   int slice;                   // elements per CTA slice (multiple of 8)
   int wchunk;                  // elements per warp chunk (multiple of 32 vectors)
   int aligned;                 // rows start on 16-byte boundaries

@@ -200,6 +200,12 @@ struct VecMax<DT_F32> {
   }
 };
 
+// log2(e) / T of tree b: the scalar temperature's factor, or the tree's own
+// (the same float division as on the host).
+__device__ __forceinline__ float tree_c(const TreeSampleArgs& a, int b) {
+  return a.temps ? kLog2e / a.temps[b] : a.c;
+}
+
 __device__ __forceinline__ double warp_sum_f64(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
@@ -601,7 +607,7 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
 #pragma unroll 8
     for (int t = wlo + lane; t < whi; t += 32)
       s += resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
-                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp, nmq, fa, fb);
+                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), tree_c(a, b), nmp, nmq, fa, fb);
     const double ws = warp_sum_f64(static_cast<double>(s));
     if (lane == 0) sh.wsum[warp][0] = ws;
   }
@@ -643,7 +649,7 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
         for (int k = 0; k < kAhead; ++k) {
           const int t = base0 + 32 * k + lane;
           w[k] = t < whi ? resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
-                                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), a.c, nmp,
+                                        fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), tree_c(a, b), nmp,
                                         nmq, fa, fb)
                          : 0.f;
         }
@@ -692,6 +698,8 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   __shared__ int16_t list[kMaxTreeNodes];
   __shared__ int cnt, base;
   const int b = blockIdx.x, tid = threadIdx.x, N = a.N;
+  // a tree temperature that gives no distribution: every node bad, nothing listed
+  const bool bad_t = a.temps != nullptr && !(a.temps[b] > 0.f && isfinite(a.temps[b]));
   const int32_t* pg = a.parents + static_cast<size_t>(b) * N;
   const int32_t* tok = a.tokens + static_cast<size_t>(b) * N;
   uint32_t st = 0;
@@ -728,12 +736,13 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   }
   __syncthreads();
   for (int i = tid; i < N; i += kThreads) {
-    if (testable_child[i]) {
+    if (testable_child[i] && !bad_t) {
       raw[atomicAdd(&cnt, 1)] = static_cast<int16_t>(i);
     } else {
       TreeRec* rec = a.recs + static_cast<size_t>(b) * N + i;
       uint32_t fl = kRecDetached;
       if (dep[i] >= 0) fl = kRecDefer | (has_child[i] && dep[i] >= a.max_depth ? kRecDepth : 0u);
+      if (bad_t) fl = kRecBad;
       rec->accepted = -1;
       rec->flags = fl;
       rec->nmp = 0.f;
@@ -796,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     const int b = static_cast<int>(g / a.N), j = static_cast<int>(g % a.N);
     const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
     const float* uni = a.uniforms + static_cast<size_t>(b) * a.N;
+    const float c = tree_c(a, b);
     TreeRec* rec = a.recs + g;
     const unsigned char* pfull = static_cast<const unsigned char*>(a.logits) + static_cast<size_t>(g) * a.V * E;
     const unsigned char* qfull = static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(g) * a.V * E;
@@ -816,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
                    sp, sq, php, phq, true);
     int slot = round++ & 1;
     if (rank == 0 && threadIdx.x == 0) sh.next[kpar & 1] = ncl + static_cast<int>(atomicAdd(a.work_next, 1u));
-    slice_stats<DT>(sh, sp, sq, lenv, a.wchunk, true, a.c, slot);  // (its cluster barrier publishes sh.next)
+    slice_stats<DT>(sh, sp, sq, lenv, a.wchunk, true, c, slot);  // (its cluster barrier publishes sh.next)
     if (threadIdx.x == 0)
       sh.nextl = static_cast<int>(ld_cluster_u32(mapa_shared(smem_addr(&sh.next[kpar & 1]), 0)));
     uint32_t rflags = 0;
@@ -827,8 +837,8 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     if (sh.got[4] != 0.0 || mp == -INFINITY || mq == -INFINITY) {
       rflags |= kRecBad;
     } else {
-      nmp = -mp * a.c;
-      nmq = -mq * a.c;
+      nmp = -mp * c;
+      nmq = -mq * c;
       const double zp = sh.got[1], zq = sh.got[3];
       double cc = 0.0, W = 1.0;
       for (int i = 0; i < nk; ++i) {
@@ -845,8 +855,8 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
             dx = Elt<DT>::value(Elt<DT>::bits_at(qfull, x));
             uf = uni[child];
           }
-          const double px = static_cast<double>(ex2_approx(fmaf(lx, a.c, nmp))) / zp;
-          const double qx = static_cast<double>(ex2_approx(fmaf(dx, a.c, nmq))) / zq;
+          const double px = static_cast<double>(ex2_approx(fmaf(lx, c, nmp))) / zp;
+          const double qx = static_cast<double>(ex2_approx(fmaf(dx, c, nmq))) / zq;
           sh.accept = static_cast<double>(uf) * qx * W < px - cc * qx;
         }
         __syncthreads();
@@ -857,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
         cc += W;
         fa = static_cast<float>(1.0 / zp);
         fb = static_cast<float>(cc / zq);
-        slice_pass<DT, 1>(sh, sp, sq, lenv, a.wchunk, true, a.c, nmp, nmq, fa, fb);
+        slice_pass<DT, 1>(sh, sp, sq, lenv, a.wchunk, true, c, nmp, nmq, fa, fb);
         slot = round++ & 1;
         if (threadIdx.x == 0) {
           double sum = 0.0;
@@ -881,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
       if (accepted < 0 && threadIdx.x < kWarps) {
         // the c = 0 residual: this CTA's target masses, rescaled to the row maximum
         const float m0 = sh.mloc[0];
-        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * a.c));
+        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * c));
         rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] * scale : sh.wc[threadIdx.x];
       }
     }
@@ -976,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
     stage_rows<DT>(a, sh, static_cast<const unsigned char*>(a.logits) + (g * a.V + lo) * E, nullptr, len, false,
                    sp, sp, php, phq, false);
     slice_stats<DT>(sh, sp, sp, (len + Elt<DT>::kPerVec - 1) / Elt<DT>::kPerVec * Elt<DT>::kPerVec, a.wchunk, false,
-                    a.c, 0);
+                    tree_c(a, b), 0);
     const float mp = static_cast<float>(sh.got[0]);
     if (sh.got[4] != 0.0 || mp == -INFINITY) {
       ok = false;
@@ -984,11 +994,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
     } else {
       if (tid < kWarps) {
         const float m0 = sh.mloc[0];
-        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * a.c));
+        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * tree_c(a, b)));
         rec->chunk[rank * kWarps + tid] = sh.zc[tid] * scale;
       }
       if (rank == 0 && tid == 0) {
-        rec->nmp = -mp * a.c;
+        rec->nmp = -mp * tree_c(a, b);
         rec->nmq = 0.f;
         rec->fa = 1.f;
         rec->fb = 0.f;

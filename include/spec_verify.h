@@ -215,7 +215,10 @@ int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
  *   node_tokens, parents [B][N]    as for spec_verify_tree_greedy
  *   uniforms      [B][N] float     in [0, 1): u_0 the final draw, u_j (j >= 1)
  *                                  the accept test of node j
- *   temperature   T > 0
+ *   temperature   T > 0, used when temperature_per_tree is NULL
+ *   temperature_per_tree  device float[B] (T of every tree) or NULL; a tree whose
+ *                 T is not finite and positive ends at its root with drawn
+ *                 token -1 and SPEC_STATUS_BAD_ROW
  *   out_tokens    [B][max_depth+1] path tokens (root excluded), the drawn
  *                                  token, then -1
  *   out_path      [B][max_depth+1] path node ids, -1 padded (the KV keep list)
@@ -232,9 +235,9 @@ int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens,
  */
 int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, const int32_t* node_tokens,
                             const int32_t* parents, const float* uniforms, int B, int N, int V, int max_depth,
-                            spec_dtype dtype, float temperature, int32_t* out_tokens, int32_t* out_path,
-                            int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
-                            void* cuda_stream);
+                            spec_dtype dtype, float temperature, const float* temperature_per_tree,
+                            int32_t* out_tokens, int32_t* out_path, int32_t* out_num_accepted,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
  * The filtered, normalised distribution the accept test uses, written out

@@ -70,7 +70,7 @@ def _load():
             lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P]
             lib.oracle_verify_greedy.restype = I
             lib.oracle_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P]
-            lib.oracle_verify_tree_sample.argtypes = [P, P, I, P, P, P, I, I, I, I, D, P, P, P, P, P]
+            lib.oracle_verify_tree_sample.argtypes = [P, P, I, P, P, P, I, I, I, I, D, P, P, P, P, P, P]
             lib.oracle_verify_tree_greedy.restype = I
             for name in ("oracle_expected_tokens_series", "oracle_expected_tokens_closed"):
                 getattr(lib, name).argtypes = [D, I]
@@ -188,11 +188,12 @@ def verify_tree_greedy(logits, node_tokens, parents, max_depth):
 
 
 def verify_tree_sample(logits, draft_logits, node_tokens, parents, uniforms, max_depth,
-                       temperature=1.0):
+                       temperature=1.0, temperature_per_tree=None):
     """Token-tree sampling verification.
 
     logits, draft_logits [B][N][V] (same dtype); node_tokens, parents [B][N];
-    uniforms [B][N] float32 (u_0 the final draw, u_j the test of node j).
+    uniforms [B][N] float32 (u_0 the final draw, u_j the test of node j);
+    temperature_per_tree [B] float32 or None (then the scalar temperature).
     Returns tokens / path [B][max_depth+1], n [B], flags [B], margin [B].
     """
     logits = np.ascontiguousarray(logits)
@@ -202,13 +203,14 @@ def verify_tree_sample(logits, draft_logits, node_tokens, parents, uniforms, max
     node_tokens = np.ascontiguousarray(node_tokens, dtype=np.int32)
     parents = np.ascontiguousarray(parents, dtype=np.int32)
     uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    tpt = None if temperature_per_tree is None else np.ascontiguousarray(temperature_per_tree, dtype=np.float32)
     B, N, V = logits.shape
     D = max_depth + 1
     out = dict(tokens=np.empty((B, D), np.int32), path=np.empty((B, D), np.int32),
                n=np.empty(B, np.int32), flags=np.empty(B, np.uint32), margin=np.empty(B, np.float64))
     rc = _load().oracle_verify_tree_sample(
         _ptr(logits), _ptr(draft_logits), _dtype_code(logits), _ptr(node_tokens), _ptr(parents),
-        _ptr(uniforms), B, N, V, int(max_depth), float(temperature), _ptr(out["tokens"]),
+        _ptr(uniforms), B, N, V, int(max_depth), float(temperature), _ptr(tpt), _ptr(out["tokens"]),
         _ptr(out["path"]), _ptr(out["n"]), _ptr(out["flags"]), _ptr(out["margin"]),
     )
     if rc != 0:

@@ -577,21 +577,24 @@ int oracle_verify_tree_greedy(const void* logits, int dtype, const int32_t* node
  * Outputs: out_tokens [B][max_depth+1] (path tokens, the drawn token, then
  * -1), out_path [B][max_depth+1] (path node ids, root excluded, -1 padded),
  * out_n [B] (accepted nodes), out_flags [B] (OFLAG_*), out_margin [B] (the
- * smallest accept / draw margin met; may be NULL).
+ * smallest accept / draw margin met; may be NULL).  temperature_per_tree [B]
+ * (or NULL for the scalar temperature) gives every tree its own T; a T that
+ * is not finite and positive ends that tree's walk at the root (drawn -1).
  * A node whose parent entry is malformed is never a child of anything; a
  * non-finite row at a visited node ends the walk there with drawn token -1.
  */
 int oracle_verify_tree_sample(const void* node_logits, const void* draft_logits, int dtype,
                               const int32_t* node_tokens, const int32_t* parents,
                               const float* uniforms, int B, int N, int V, int max_depth,
-                              double temperature, int32_t* out_tokens, int32_t* out_path,
+                              double temperature, const float* temperature_per_tree,
+                              int32_t* out_tokens, int32_t* out_path,
                               int32_t* out_n, uint32_t* out_flags, double* out_margin) {
   size_t es = (dtype == ORACLE_BF16) ? 2 : 4;
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
   int b, j, t;
-  if (N < 1 || max_depth < 1 || !(temperature > 0.0)) {
+  if (N < 1 || max_depth < 1 || (!temperature_per_tree && !(temperature > 0.0))) {
     free(p);
     free(q);
     free(r);
@@ -605,6 +608,7 @@ int oracle_verify_tree_sample(const void* node_logits, const void* draft_logits,
     uint32_t flags = 0;
     double margin = INFINITY;
     int v = 0, n = 0, drawn = -1;
+    const double T = temperature_per_tree ? (double)temperature_per_tree[b] : temperature;
     if (par[0] != -1) flags |= OFLAG_BAD_PARENT;
     for (j = 1; j < N; ++j) {
       if (par[j] < 0 || par[j] >= j) flags |= OFLAG_BAD_PARENT;
@@ -616,6 +620,10 @@ int oracle_verify_tree_sample(const void* node_logits, const void* draft_logits,
     }
     for (;;) {
       const char* prow = (const char*)node_logits + ((size_t)b * N + v) * (size_t)V * es;
+      if (!(T > 0.0) || isinf(T)) { /* a temperature that gives no distribution */
+        flags |= OFLAG_BAD_ROW;
+        break;
+      }
       const char* qrow = (const char*)draft_logits + ((size_t)b * N + v) * (size_t)V * es;
       int has_child = 0, n_test = 0, accepted = -1;
       for (j = v + 1; j < N; ++j)
@@ -624,12 +632,12 @@ int oracle_verify_tree_sample(const void* node_logits, const void* draft_logits,
           if (tok[j] >= 0 && tok[j] < V && n < max_depth) ++n_test;
         }
       if (has_child && n >= max_depth) flags |= OFLAG_DEPTH;
-      if (row_probs_adj(prow, dtype, V, temperature, 0, 1.0, 0, p, NULL, NULL, NULL, NULL, NULL) != 0) {
+      if (row_probs_adj(prow, dtype, V, T, 0, 1.0, 0, p, NULL, NULL, NULL, NULL, NULL) != 0) {
         flags |= OFLAG_BAD_ROW;
         break;
       }
       if (n_test > 0 &&
-          row_probs_adj(qrow, dtype, V, temperature, 0, 1.0, 0, q, NULL, NULL, NULL, NULL, NULL) != 0) {
+          row_probs_adj(qrow, dtype, V, T, 0, 1.0, 0, q, NULL, NULL, NULL, NULL, NULL) != 0) {
         flags |= OFLAG_BAD_ROW;
         break;
       }

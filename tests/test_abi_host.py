@@ -114,8 +114,8 @@ def test_greedy_and_tree_reject_bad_arguments(L):
 def test_tree_sample_rejects_bad_arguments(L):
     ts = L.spec_verify_tree_sample
 
-    def call(nl=FAKE, dl=FAKE, uni=FAKE, B=2, N=60, V=100, depth=6, dt=1, T=1.0, wsb=1 << 30):
-        return ts(nl, dl, FAKE, FAKE, uni, B, N, V, depth, dt, T, FAKE, FAKE, FAKE, FAKE, wsb, None)
+    def call(nl=FAKE, dl=FAKE, uni=FAKE, B=2, N=60, V=100, depth=6, dt=1, T=1.0, tpt=None, wsb=1 << 30):
+        return ts(nl, dl, FAKE, FAKE, uni, B, N, V, depth, dt, T, tpt, FAKE, FAKE, FAKE, FAKE, wsb, None)
 
     assert call(dt=9) == sv.SPEC_ERR_DTYPE
     assert call(dl=None) == sv.SPEC_ERR_INVALID_ARG
@@ -125,6 +125,9 @@ def test_tree_sample_rejects_bad_arguments(L):
     assert call(T=float("nan")) == sv.SPEC_ERR_INVALID_ARG
     assert call(uni=ctypes.c_void_p(4098)) == sv.SPEC_ERR_INVALID_ARG  # float needs 4-byte alignment
     assert call(wsb=8) == sv.SPEC_ERR_WORKSPACE
+    # per-tree temperatures replace the scalar one (checked on the device, per tree)
+    assert call(T=0.0, tpt=FAKE, wsb=8) == sv.SPEC_ERR_WORKSPACE
+    assert call(tpt=ctypes.c_void_p(4098)) == sv.SPEC_ERR_INVALID_ARG
     # a CTA's share of both rows must fit its shared memory: V = 300000 f32 does not
     assert call(V=300000, dt=0) == sv.SPEC_ERR_UNSUPPORTED
 

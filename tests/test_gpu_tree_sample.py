@@ -223,3 +223,22 @@ def test_maximum_tree_size():
     """N = 1024 nodes (the limit), up to 4 children per node, depth <= 12."""
     case = W.tree_sample_case(2, 1024, 2048, 12, seed=36, dtype=W.BF16, noise=0.7)
     compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_per_tree_temperatures():
+    sv = lib()
+    case = W.tree_sample_case(8, 30, 20000, 5, seed=37, dtype=W.BF16)
+    temps = np.random.default_rng(38).uniform(0.5, 1.2, size=case.B).astype(np.float32)
+    temps[5] = 0.0  # no distribution: that tree ends at its root
+    ws = sv.Workspace()
+    sv.spec_get_status(ws)
+    out = sv.spec_verify_tree_sample(to_dev(case.logits), to_dev(case.draft), to_dev(case.node_tokens),
+                                     to_dev(case.parents), to_dev(case.uniforms), case.max_depth,
+                                     temperature_per_tree=to_dev(temps), workspace=ws)
+    torch.cuda.synchronize()
+    gpu = [o.cpu().numpy() for o in out]
+    assert sv.spec_get_status(ws) & sv.SPEC_STATUS_BAD_ROW
+    orc = oracle.verify_tree_sample(case.logits, case.draft, case.node_tokens, case.parents, case.uniforms,
+                                    case.max_depth, temperature_per_tree=temps)
+    compare(case, gpu, orc)
+    assert gpu[2][5] == 0 and gpu[0][5, 0] == -1

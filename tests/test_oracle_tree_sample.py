@@ -378,3 +378,21 @@ def test_c_oracle_tree_pass_follows_the_exact_law():
     assert abs(sum(float(law[k]) for k in keys) - 1.0) < 1e-12
     _, pval = stats.chisquare(counts, expected)
     assert pval > 1e-4, list(zip(keys, counts, expected))
+
+
+def test_per_tree_temperature_equals_separate_runs():
+    case = W.tree_sample_case(6, 20, 300, 4, seed=42, dtype=W.F32)
+    temps = np.array([0.5, 0.8, 1.0, 1.3, 2.0, 0.7], np.float32)
+    out = oracle.verify_tree_sample(case.logits, case.draft, case.node_tokens, case.parents, case.uniforms,
+                                    case.max_depth, temperature_per_tree=temps)
+    for b in range(case.B):
+        sl = slice(b, b + 1)
+        one = oracle.verify_tree_sample(case.logits[sl], case.draft[sl], case.node_tokens[sl], case.parents[sl],
+                                        case.uniforms[sl], case.max_depth, temperature=float(temps[b]))
+        assert out["n"][b] == one["n"][0]
+        np.testing.assert_array_equal(out["tokens"][b], one["tokens"][0])
+    bad = temps.copy()
+    bad[2] = 0.0
+    out = oracle.verify_tree_sample(case.logits, case.draft, case.node_tokens, case.parents, case.uniforms,
+                                    case.max_depth, temperature_per_tree=bad)
+    assert out["n"][2] == 0 and out["tokens"][2, 0] == -1 and out["flags"][2] & oracle.FLAG_BAD_ROW
