@@ -44,6 +44,11 @@ MUTATIONS = [
      "drawn = inverse_cdf(p, V, (double)u[0], &mg);"),
     ("tree walk keeps the parent's rows after an acceptance", "        v = accepted;\n        continue;",
      "        (void)accepted;\n        continue;"),
+    ("tree siblings tried from the last", "for (j = v + 1; j < N && n_test > 0; ++j) {",
+     "for (j = N - 1; j > v && n_test > 0; --j) {"),
+    ("tree degenerate residual not put back to p",
+     "flags |= OFLAG_DEGENERATE;\n          for (t = 0; t < V; ++t) r[t] = p[t];",
+     "flags |= OFLAG_DEGENERATE;"),
 ]
 
 PIN_FILES = ("test_oracle_pins.py", "test_oracle_tree_sample.py")

@@ -396,3 +396,17 @@ def test_per_tree_temperature_equals_separate_runs():
     out = oracle.verify_tree_sample(case.logits, case.draft, case.node_tokens, case.parents, case.uniforms,
                                     case.max_depth, temperature_per_tree=bad)
     assert out["n"][2] == 0 and out["tokens"][2, 0] == -1 and out["flags"][2] & oracle.FLAG_BAD_ROW
+
+
+def test_degenerate_residual_goes_back_to_p():
+    """p = q = (1, 0): the first child's token has no mass in either row, so it
+    is rejected and the residual max(0, p - q) has mass 0; it goes back to p,
+    against which the second child (token 0) is accepted for any u."""
+    P = np.array([[[0.0, -np.inf], [0.0, 0.0], [0.0, 0.0]]], np.float32)  # log of (1, 0), (.5, .5), (.5, .5)
+    Q = P.copy()
+    toks = np.array([[0, 1, 0]], np.int32)
+    par = np.array([[-1, 0, 0]], np.int32)
+    for u2 in (0.0, 0.5, 0.999):
+        out = oracle.verify_tree_sample(P, Q, toks, par, np.array([[0.3, 0.2, u2]], np.float32), 1)
+        assert out["n"][0] == 1 and out["path"][0, 0] == 2 and out["tokens"][0, 0] == 0
+        assert out["flags"][0] & oracle.FLAG_DEGENERATE
