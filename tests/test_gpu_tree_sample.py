@@ -242,3 +242,24 @@ def test_per_tree_temperatures():
                                     case.max_depth, temperature_per_tree=temps)
     compare(case, gpu, orc)
     assert gpu[2][5] == 0 and gpu[0][5, 0] == -1
+
+
+def test_degenerate_residual_goes_back_to_p():
+    """p = q = (1, 0) at the root; the first child's token has no mass, its
+    rejection leaves a residual of mass 0, which goes back to p: the second
+    child (token 0) is accepted for any u, then the leaf's (.5, .5) row is
+    drawn with u_0 = 0.3 (token 0).  Oracle-flagged as degenerate, so the
+    outcome is checked here directly."""
+    B = 4
+    P = np.tile(np.array([[[0.0, -np.inf], [0.0, 0.0], [0.0, 0.0]]], np.float32), (B, 1, 1))
+    toks = np.tile(np.array([[0, 1, 0]], np.int32), (B, 1))
+    par = np.tile(np.array([[-1, 0, 0]], np.int32), (B, 1))
+    u = np.array([[0.3, 0.2, x] for x in (0.0, 0.5, 0.9, 0.999)], np.float32)
+    case = W.TreeSampleCase("degenerate", W.F32, P, P.copy(), toks, par, u, 1, 1.0)
+    tok, path, n = run_gpu(case)
+    orc = run_oracle(case)
+    assert (orc["flags"] & oracle.FLAG_DEGENERATE).all()
+    np.testing.assert_array_equal(n, orc["n"])
+    np.testing.assert_array_equal(tok, orc["tokens"])
+    np.testing.assert_array_equal(path, orc["path"])
+    assert (n == 1).all() and (path[:, 0] == 2).all() and (tok[:, :2] == 0).all()
