@@ -29,7 +29,12 @@
  *   - the inverse CDF picks the smallest index j whose running sum (in
  *     ascending index order) exceeds u * S;
  *   - a residual of total mass 0 after a rejection (reachable only through
- *     rounding) is replaced by the target row itself.
+ *     rounding) is replaced by the target row itself;
+ *   - token trees (sampling): the children of a node are tried in ascending
+ *     node order, each rejected child replaces the residual r by
+ *     max(0, r - q) renormalised (q unchanged), the next child is tested
+ *     against it, and the node where the walk stops draws from its current
+ *     residual; temperature only (scalar or per tree), no top-k / top-p.
  */
 #include <math.h>
 #include <stdint.h>
