@@ -21,8 +21,6 @@ bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 size_t elt_bytes(spec_dtype d) { return d == SPEC_BF16 ? 2 : 4; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-// Elements of one 16-byte vector.
-int vec_elems(spec_dtype d) { return 16 / static_cast<int>(elt_bytes(d)); }
 
 // Rows start on 16-byte boundaries: the bulk-copy / vector-load fast path.
 int rows_aligned(const void* base, int V, spec_dtype d) {
@@ -78,19 +76,16 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.status = reinterpret_cast<uint32_t*>(w + L.status);
   a.seq_tickets = reinterpret_cast<uint32_t*>(w + L.s_tickets);
   a.draw_tickets = reinterpret_cast<uint32_t*>(w + L.d_tickets);
-  a.tie_tickets = reinterpret_cast<uint32_t*>(w + L.t_tickets);
-  a.work = reinterpret_cast<uint32_t*>(w + L.work);
-  a.ready = reinterpret_cast<uint32_t*>(w + L.ready);
+  a.hdrs = reinterpret_cast<RowHdr*>(w + L.hdrs);
+  a.tags = reinterpret_cast<uint32_t*>(w + L.tags);
   a.pubs = reinterpret_cast<RowPub*>(w + L.pubs);
   a.csums = reinterpret_cast<float*>(w + L.csums);
-  a.tcnt = reinterpret_cast<int32_t*>(w + L.tcnt);
-  a.tcut = reinterpret_cast<int32_t*>(w + L.tcut);
+  a.work = reinterpret_cast<uint32_t*>(w + L.work);
   a.launch_mode = g_launch_mode.load();
-  // whole-row draws: one chunk per 512 row vectors, at most kMaxDrawChunks
-  {
-    const int nv = (V + vec_elems(dtype) - 1) / vec_elems(dtype);
-    a.chunks = nv / 512 < 1 ? 1 : (nv / 512 > kMaxDrawChunks ? kMaxDrawChunks : nv / 512);
-  }
+  a.done = reinterpret_cast<uint32_t*>(w + L.done);
+  // the draw at the first rejection: a few chunks over listed vectors, more
+  // over whole rows (no filter)
+  a.chunks = (a.top_k > 0 || a.top_p < 1.f) ? 8 : kMaxDrawChunks;
   a.aligned_target = rows_aligned(target, V, dtype);
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
@@ -98,6 +93,9 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }
+
+// Elements of one 16-byte vector.
+int vec_elems(spec_dtype d) { return 16 / static_cast<int>(elt_bytes(d)); }
 
 // ------------------------------------------------ allocation-free sampling
 // Fixed scratch for spec_verify_sample_noalloc: a bound on the workspace
@@ -168,10 +166,9 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
   int rc = noalloc_scratch(&scratch);
   if (rc != SPEC_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  // The array keeps whatever the previous call left: the status word, the
-  // tickets, counters and draw queue must start at zero (everything else is
-  // written before it is read).
-  if (cudaMemsetAsync(scratch, 0, L.pubs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  // The array keeps whatever the previous call left: the status word and the
+  // tickets must start at zero (everything else is written before it is read).
+  if (cudaMemsetAsync(scratch, 0, L.hdrs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
   rc = run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                   out_num_accepted, out_p_draft, out_q_draft, nullptr, scratch, kNoAllocBytes, cuda_stream,
                   MODE_SAMPLE);

@@ -14,52 +14,52 @@ constexpr int DT_BF16 = 1;
 
 constexpr int kThreads = 256;           // threads per CTA in every kernel
 constexpr int kWarps = kThreads / 32;
+constexpr int kWindow = 512;            // exact-value histogram bins per row
 constexpr int kMaxK = 31;
 constexpr int kMaxTreeNodes = 1024;
 
 constexpr int MODE_SAMPLE = 0;          // speculative-sampling verification
 constexpr int MODE_PROBS = 1;           // write filtered probabilities
 
-// ---------------------------------------------------------------- sampling
-// Each row is streamed once by one CTA.  Vectors whose maximum reaches the
-// row's window bottom are queued per warp and counted, element by element,
-// into a histogram of exact values (a ring of kRing slots over the value
-// key); the window spans at most kWinKeys keys below its anchor (the largest
-// key seen at the last window update), and keys up to kFreeKeys above the
-// anchor are counted before the window moves.  The first kListCap candidate
-// vectors are kept (index and data) for the tie cut and the kept-vector list.
-constexpr int kRing = 4096;
-constexpr int kWinKeys = 1024;
-constexpr int kFreeKeys = 1536;
-static_assert(kFreeKeys <= (kRing - kWinKeys) / 2, "a window move must not reach slots still being cleared");
-constexpr int kQCap = 64;               // candidate vectors queued per warp
-constexpr int kListCap = 1024;          // candidate vectors kept per row
-constexpr int kStreamU = 4;             // 16-byte loads in flight per thread (double-buffered)
-constexpr int kSyncEvery = 4;           // stream iterations between window updates
-
 // The kept set and normaliser of one filtered row: token j of key (value
-// order) `key` is kept iff all_kept, or key > kstar, or key == kstar and it
-// is among the `keep` lowest-index tokens of that value (of `total`), i.e.
-// j < tie_cut when tie_cut >= 0; tie_cut < 0 means that index is not known
-// yet (the consumer finds it).  Its probability is 2^(l c - K) * inv_z.
+// order) `key` is kept iff all_kept, or key > kstar, or key == kstar and
+// j < tie_cut; its probability is 2^(l c - K) * inv_z.
 struct RowState {
   float c;               // log2(e) / T
   float K;               // lattice exponent (an integer) of the row
   float m;               // row maximum
   uint32_t kmax;         // key of m
   uint32_t kstar;
-  int32_t keep;
-  int32_t total;
   int32_t tie_cut;
   float inv_z;           // 1 / mass of the kept set
   float zkept;
   int32_t all_kept;
+  int32_t covered;       // the kept set was decided from candidate vectors
   int32_t bad;
 };
 
-// One row after its CTA: its kept set, its probability at the draft token and,
-// for target rows, the row vectors holding kept tokens in index order
-// (nlist = kPubReread when they are not listed).
+// Sampling runs as three launches.  The stream kernel reads every row once
+// and leaves a RowHdr and its candidate tags; the tail kernel decides each
+// row's kept set from them (RowPub) and, in the last CTA of a sequence, the
+// accepted prefix n; the draw kernel draws the token at position n.
+constexpr int kTagsPerWarp = 1024;      // candidate tags per warp segment handed to the tail kernel
+constexpr int kRowTags = kWarps * kTagsPerWarp;
+
+// One row after the stream kernel.
+struct RowHdr {
+  float m;               // row maximum
+  float K;               // lattice exponent
+  float zhi, zlo;        // sum of 2^(l c - K) over the row, as a double-float
+  uint32_t kmax;         // key of m
+  uint32_t klo;          // every tag list is complete at and above this key
+  uint32_t xbits;        // the row's value at the draft token (draft positions)
+  int32_t bad;           // bad temperature, no finite maximum, or |m c| >= 2^30
+  uint32_t ntags[kWarps];  // tags at or above klo handed over per warp segment
+};
+
+// One row after the tail kernel: its kept set, its probability at the draft
+// token and, for target rows, the row vectors holding its kept tokens in
+// index order (nlist = kPubReread when they are not listed).
 constexpr int kPubList = 1024;
 constexpr uint32_t kPubReread = 0xFFFFFFFFu;
 struct RowPub {
@@ -70,10 +70,9 @@ struct RowPub {
   uint32_t list[kPubList];
 };
 
-// The draw at the first rejection over whole rows runs in chunks, one CTA
-// each.  A chunk's record: its residual and p sums (two double-floats), then
-// its per-warp sums (kWarps residual, kWarps p).  Rows whose tie index is not
-// known first count their tokens of value kstar per chunk.
+// Chunks of the draw at the first rejection: one CTA each.  A chunk's record:
+// its residual and p sums (two double-floats), then its per-warp sums
+// (kWarps residual, kWarps p).
 constexpr int kMaxDrawChunks = 16;
 constexpr int kChunkRec = 4 + 2 * kWarps;  // floats
 
@@ -101,22 +100,19 @@ struct TreeRec {
 };
 
 // Workspace layout (byte offsets), identical for every call with the same
-// (B, k).  Everything before `pubs` must be zero when a call starts and every
-// call leaves it zero again (the status word collects sticky bits until
-// spec_get_status clears it); everything after it is written before it is
-// read within a call.
+// (B, k).  Tickets are zero between calls; everything else is written before
+// it is read within a call (the status word collects sticky bits until
+// spec_get_status clears it).
 struct WsLayout {
   size_t status;      // uint32 status word (sticky bits)
-  size_t s_tickets;   // uint32[B]  rows finished per sequence
-  size_t d_tickets;   // uint32[B]  draw chunks summed per sequence
-  size_t t_tickets;   // uint32[B]  draw chunks that counted their ties per sequence
-  size_t work;        // uint32[8]  sampling counters (row items, draw items, CTAs done, sequences
-                      //            done, queued draws)
-  size_t ready;       // uint32[B]  queued whole-row draws: sequence + 1, 0 = not yet queued
+  size_t s_tickets;   // uint32[B]  rows finished per sequence, tail kernel
+  size_t d_tickets;   // uint32[B]  chunks finished per sequence, draw kernel
+  size_t work;        // uint32[2]  fused stream/tail kernel: next work item, CTAs finished
+  size_t done;        // uint32[rows]  fused kernel: a row's stream part is published
+  size_t hdrs;        // RowHdr[rows]
+  size_t tags;        // uint32[rows][kRowTags]
   size_t pubs;        // RowPub[rows]
   size_t csums;       // float[B][kMaxDrawChunks][kChunkRec]  per-chunk draw sums
-  size_t tcnt;        // int32[B][kMaxDrawChunks][2]  tokens of value kstar per chunk (target, draft)
-  size_t tcut;        // int32[B][kMaxDrawChunks][2]  each chunk's tie index bound (target, draft)
   size_t g_slots;     // uint64[B*(k+1)]  packed (value key, ~index) per row
   size_t g_tickets;   // uint32[B]  row vectors folded per sequence / tree, argmax kernel
   size_t trecs;       // TreeRec[B*(k+1)]  tree sampling: one record per node
@@ -135,17 +131,16 @@ constexpr WsLayout ws_layout_of(size_t B, size_t rows, size_t units) {
   WsLayout w{};
   w.status = 0;
   w.s_tickets = 256;
-  w.d_tickets = align_up(w.s_tickets + sizeof(uint32_t) * B, 256);
-  w.t_tickets = align_up(w.d_tickets + sizeof(uint32_t) * B, 256);
-  w.work = align_up(w.t_tickets + sizeof(uint32_t) * B, 256);
-  w.ready = w.work + 256;
-  w.pubs = align_up(w.ready + sizeof(uint32_t) * B, 256);
+  w.d_tickets = align_up(w.s_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.work = align_up(w.d_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
+  w.done = w.work + 2 * sizeof(uint32_t);
+  w.hdrs = align_up(w.done + sizeof(uint32_t) * rows, 256);
+  w.tags = align_up(w.hdrs + sizeof(RowHdr) * rows, 256);
+  w.pubs = align_up(w.tags + sizeof(uint32_t) * kRowTags * rows, 256);
   w.csums = align_up(w.pubs + sizeof(RowPub) * rows, 256);
-  w.tcnt = align_up(w.csums + sizeof(float) * kChunkRec * static_cast<size_t>(kMaxDrawChunks) * B, 256);
-  w.tcut = align_up(w.tcnt + sizeof(int32_t) * 2 * static_cast<size_t>(kMaxDrawChunks) * B, 256);
-  w.g_slots = align_up(w.tcut + sizeof(int32_t) * 2 * static_cast<size_t>(kMaxDrawChunks) * B, 256);
+  w.g_slots = align_up(w.csums + sizeof(float) * kChunkRec * static_cast<size_t>(kMaxDrawChunks) * B, 256);
   w.g_tickets = align_up(w.g_slots + sizeof(uint64_t) * units, 256);
-  w.trecs = align_up(w.g_tickets + sizeof(uint32_t) * B, 256);
+  w.trecs = align_up(w.g_tickets + sizeof(uint32_t) * static_cast<size_t>(B), 256);
   w.tlist = align_up(w.trecs + sizeof(TreeRec) * units, 256);
   w.total = align_up(w.tlist + 16 + sizeof(int32_t) * units, 256);
   return w;
@@ -175,27 +170,19 @@ struct SampleArgs {
   uint32_t* status;
   uint32_t* seq_tickets;       // [B]
   uint32_t* draw_tickets;      // [B]
-  uint32_t* tie_tickets;       // [B]
-  uint32_t* work;              // [8]
-  uint32_t* ready;             // [B]
+  RowHdr* hdrs;                // [rows]
+  uint32_t* tags;              // [rows][kRowTags]
   RowPub* pubs;                // [rows]
   float* csums;                // [B][kMaxDrawChunks][kChunkRec]
-  int32_t* tcnt;               // [B][kMaxDrawChunks][2]
-  int32_t* tcut;               // [B][kMaxDrawChunks][2]
   int chunks;                  // draw chunks per sequence (<= kMaxDrawChunks)
+  uint32_t* work;              // [2] fused kernel work counters
+  uint32_t* done;              // [rows] fused kernel row flags
   int launch_mode;             // SPEC_LAUNCH_*
-  int poll_limit;              // fused kernel: polls before a wait gives up
+  int poll_limit;              // fused kernel: polls before a tail part gives up
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;
 };
-
-// Indices into SampleArgs::work.
-constexpr int WK_ROWS = 0;      // row items claimed
-constexpr int WK_DRAWS = 1;     // draw items claimed
-constexpr int WK_EXIT = 2;      // CTAs finished
-constexpr int WK_SEQS = 3;      // sequences finished
-constexpr int WK_QUEUED = 4;    // sequences queued for a whole-row draw
 
 struct TreeSampleArgs {
   const void* logits;          // [B][N][V] target row of every node

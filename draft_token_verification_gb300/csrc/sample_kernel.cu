@@ -8,32 +8,44 @@
 // p_i(x_i); at the first rejection n one token is drawn from
 // max(0, p_n - q_n) with u_{k+1}, else a bonus token from p_k with u_k.
 //
-// How (one GPU, memory-bound).  One persistent cooperative launch takes work
-// items from a counter: every row of every sequence (sequence by sequence),
-// then the chunks of the draws that need whole rows.  A row's CTA reads the
-// row from HBM once, 16-byte non-allocating loads, four in flight per thread:
-//   - masses sit on a power-of-two lattice: with c = log2(e) / T and an
-//     integer K >= max(l) * c (raised, with an exact power-of-two rescale,
-//     whenever the row maximum seen so far rises), mass(l) = 2^(l c - K),
-//     one packed f32x2 fma and one ex2 per element; 2^(l c - K) / Z is the
-//     softmax of l / T.
-//   - a vector whose maximum reaches the window bottom (kDelta octaves of
-//     mass below the row maximum seen so far) is queued in its warp; full
-//     queues are counted element by element, 32 vectors at a time, into a
-//     histogram of exact values (a ring over the value key), and their
-//     first kListCap vectors are kept with their index.
-// The tail scans the histogram from the top for the top-k and top-p cut (a
-// token is kept while the mass ranked before it is below top_p times the
-// top-k mass), the number of tokens of the cut value that are kept (lowest
-// indices first) and the kept normaliser.  The kept vectors give the index
-// bound of that tie and, for target rows, the row vectors holding kept
-// tokens in index order.  A row whose cut lies below the window (or an fp32
-// row, whose values are not counted exactly) takes an exact search that
-// re-reads it.  The last row of a sequence to finish (ticket, no wait) tests
+// How (one GPU, memory-bound).  Every row (the target and draft rows of
+// each draft position (b, i), then the bonus target rows (b, k)) has a stream
+// part and a tail part, run by one CTA each: as work items of one
+// cooperative launch (every stream part, then every tail part; a tail part
+// polls, bounded, for its row's stream part) or as two launches.
+// The stream part reads its row from HBM once, 16-byte non-allocating loads
+// by warp segments in index order:
+//   - masses are taken on a power-of-two lattice: with c = log2(e) / T and
+//     an integer k_t >= max(l) * c held per thread, mass(l) = 2^(l c - k_t)
+//     (one packed f32x2 fma and one ex2 per element).  Raising k_t rescales
+//     the running sum by an exact power of two, so the row sum
+//     Z = sum 2^(l c - K) (K the CTA-wide k) carries no rescaling error;
+//     2^(l c - K) / Z is the softmax of l / T.
+//   - candidate vectors: a lane tags every 16-byte vector whose maximum is
+//     within kTheta octaves of mass of the best maximum it knows (its own
+//     running maximum, or the CTA's, exchanged at fixed stream steps).  A tag
+//     is the vector's index in the warp segment and the bf16 pattern of its
+//     maximum.  A lane list short of room drops the tags below its current
+//     bound and, if still short, raises the lane's floor above its smallest
+//     tag; each list is complete above max(bound, floor).
+// It hands over a row header (maximum, lattice exponent, row sum, window
+// bottom) and the tags at or above the window bottom.
+// The tail part bounds the cut from the tagged maxima (vector maxima are
+// tokens of the row, so the mass or count above a value is at least that of
+// the maxima above it), gathers the tagged vectors at or above the bound in
+// index order, counts their elements in a histogram of exact values and
+// scans it for the cut, its tie count and the kept normaliser.  A row the
+// candidates do not decide re-reads itself in windows of exact values from
+// the maximum down, and past a few windows (flat rows crossing zero, 32-bit
+// keys) by a bitwise search.  Each row publishes its state, its probability
+// at the draft token and, for target rows, its vectors holding kept tokens.
+// The last row of a sequence to finish (ticket, no spin-wait) tests
 // u_i q_i(x_i) < p_i(x_i) at every position, takes the first rejection n,
-// commits the accepted prefix and draws the token at n over the target row's
-// listed kept vectors; rows without such a list (no filter, dense kept sets)
-// are queued for a draw over whole rows in chunks.
+// commits the accepted prefix and, when row n's kept vectors are listed,
+// draws the token at n from max(0, p_n - q_n) (or from p_k when n = k) over
+// them.  A draw over whole rows (no filter, or a row the candidates did not
+// decide) is left to the draw kernel, which splits the rows into chunks.
+// Only the first rejection is drawn: no residual is computed speculatively.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -50,24 +62,20 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 using u64 = unsigned long long;
 
-constexpr float kDelta = 16.f;      // octaves of mass below the row maximum the histogram window spans
-constexpr int kTieCap = 1024;       // tokens of the cut value gathered to find the tie's index bound
-constexpr int kTieRankMax = 256;    // above this many, the bound is found by a pass over the row
-constexpr int kMaxPolls = 1 << 22;  // polls before a wait of the fused kernel gives up
-
-// Dynamic shared memory of a row CTA (filtered bf16 rows): the histogram
-// ring, the per-warp candidate queues (data, index) and the kept candidate
-// list (data, index).  After the stream the histogram holds the tie tokens
-// and the draw scratch, and the queues the kept-vector bitmap.
-constexpr size_t kHistBytes = sizeof(uint32_t) * kRing;
-constexpr size_t kQDataOff = kHistBytes;
-constexpr size_t kQIdxOff = kQDataOff + sizeof(uint4) * kWarps * kQCap;
-constexpr size_t kListOff = kQIdxOff + sizeof(uint32_t) * kWarps * kQCap;
-constexpr size_t kListIdxOff = kListOff + sizeof(uint4) * kListCap;
-constexpr size_t kRowSmem = kListIdxOff + sizeof(uint32_t) * kListCap;
-constexpr size_t kBitmapBytes = kListOff - kQDataOff;  // kept-vector bitmap in the queues' place
-static_assert(kHistBytes >= sizeof(uint32_t) * 3 * kPubList, "draw scratch in the histogram's place");
-static_assert(kHistBytes >= sizeof(uint32_t) * kTieCap, "tie tokens in the histogram's place");
+constexpr int kLaneTags = 32;                       // candidate vector tags per lane per row
+constexpr int kBmapWords = 128;                     // gather bitmap words per warp per row (4096 vectors)
+constexpr int kGather = kLaneTags * 32;             // gathered vectors per warp per row (in the lane tags' place)
+constexpr int kSyncEvery = 4;                       // stream iterations between CTA maximum exchanges
+constexpr float kTheta = 13.f;                      // octaves of mass kept as candidates
+constexpr uint32_t kSlotMask = static_cast<uint32_t>(kWindow) - 1u;
+// Histogram slot of a key (any kWindow consecutive keys take distinct
+// slots): the low bits are mixed with bits 4.. so that the scan's lanes,
+// which read keys 16 apart, fall in distinct shared-memory banks.
+__device__ __forceinline__ uint32_t hslot(uint32_t key) { return (key & kSlotMask) ^ ((key >> 4) & 15u); }
+constexpr int kGroups = kWindow / 4;                // aligned groups of four keys
+constexpr int kScanWarps = 4;                       // warps that scan one row's histogram
+constexpr int kVecCacheAt = 256;                    // gathered tags before, cached vectors after (words)
+constexpr int kVecCache = (kGather - kVecCacheAt) / 4;  // cached gathered vectors per warp (192)
 
 // ------------------------------------------------------- packed f32x2 math
 
@@ -294,43 +302,46 @@ struct CutOut {
   DF zkept;              // mass of the kept set
 };
 
-// Shared state of one CTA (static shared memory).
+// Row-wide values after the stream (the same for every thread).
+struct RowG {
+  float m;               // row maximum
+  float K;               // lattice exponent
+  uint32_t kmax;         // key of m
+  uint32_t klo;          // lowest key of the scanned window
+  DF z;                  // sum of masses 2^(l c - K)
+  uint32_t c0;           // tokens above the window (keys > kmax)
+  DF m0;                 // their mass
+  int active;            // the row takes part in the current scan
+};
+
 struct Shm {
-  float w_s[kWarps];           // per-warp sums (reductions, draw weights)
+  float w_m[kWarps][2];
+  int w_k[kWarps][2];
+  float w_z[kWarps][2];
+  uint32_t w_floor[kWarps][2]; // key above which a warp's tag list is complete
+  uint32_t w_over[kWarps][2];  // a warp's gather overflowed
+  float w_s[kWarps];
   float w_sp[kWarps];
   uint32_t w_u[kWarps][2];
-  uint32_t wm[2][kWarps];      // per-warp running maxima at window updates (double-buffered)
-  DF wz[kWarps];               // per-warp row sums
-  uint32_t sc_cnt[kWarps];     // key scan: per-warp counts and masses
-  double sc_mass[kWarps];
-  int nlist;                   // candidate vectors appended to the list (may exceed kListCap)
-  int ntie;                    // tokens of the cut value gathered
-  int nkept;                   // kept vectors of a target row
-  // row results passed between the threads of the CTA
-  uint32_t mbits;              // bits of the row maximum
-  float K;                     // lattice exponent at the end of the stream
-  DF z;                        // row sum
-  int corrupt;                 // the histogram window is not valid
-  uint32_t kb;                 // lowest key counted by the histogram
-  uint32_t vk;                 // top-k cut: key, kept tokens of that value, tokens of that value
-  int ck, cnt_vk;
-  double zk;                   // mass of the top-k set
-  uint32_t vstar;              // top-p cut: key, kept, total, kept mass
-  int jstar, cnt_vstar;
-  double zkept;
-  int found;
-  int tie_idx;
-  uint32_t xbits;              // the row's value at the draft token
-  int second;                  // the last row of its sequence / the last chunk of its draw
-  int item;
-  int flag;
-  // the draw
+  float x_m[2][kWarps][2];     // running maxima exchanged while streaming (double-buffered)
+  uint32_t xbits[2];           // the draft token's value in the target and draft rows
+  uint32_t s_C[2][kScanWarps];
+  DF s_M[2][kScanWarps];
+  RowG g[2];
+  CutOut cutk[2];
+  CutOut cut[2];
+  int tie_warp[2];
+  uint32_t tie_j[2];
+  int tie_cut[2];
+  int lead;                    // the warp that runs one-warp steps for this row
+  RowStat rs[2];
   int draw_warp;
   float draw_base;
+  int second;                  // this CTA is the last of its sequence (tail, draw kernels)
+  int draw_chunk;              // the chunk holding the draw target, or -1
+  int draw_useq;               // the draw weights are max(0, p - q)
   int draw_token;
-  int draw_useq;
-  int draw_chunk;
-  DF draw_target;
+  DF draw_target;              // the draw target within its chunk
 };
 
 // 16-byte vector v of a row (elements v*kPerVec ...), -inf beyond n.
@@ -500,6 +511,378 @@ __device__ __noinline__ CutOut search_cut(Shm& sh, const unsigned char* row, int
   return co;
 }
 
+// ------------------------------------------------------ segments & lists
+
+// Warp w owns vectors [beg, end) of a row: consecutive vectors in index
+// order (iteration, lane, element).
+struct Seg {
+  int beg, end, iters;
+};
+__device__ __forceinline__ int seg_vectors(int nvec) { return ((nvec + kWarps - 1) / kWarps + 31) / 32 * 32; }
+__device__ __forceinline__ Seg warp_seg(int nvec, int warp) {
+  const int vpw = seg_vectors(nvec);
+  Seg s;
+  s.beg = min(nvec, warp * vpw);
+  s.end = min(nvec, s.beg + vpw);
+  s.iters = (s.end - s.beg + 31) / 32;
+  return s;
+}
+
+// Tag of a candidate vector: its index within the warp segment (high 16
+// bits) and the bf16 pattern of its maximum (low 16 bits).
+__device__ __forceinline__ uint32_t tag_make(uint32_t local, uint32_t key) { return (local << 16) | key; }
+__device__ __forceinline__ uint32_t tag_local(uint32_t t) { return t >> 16; }
+// (the tag keeps the maximum's bf16 pattern; its key orders the values)
+__device__ __forceinline__ uint32_t tag_key(uint32_t t) { return Elt<DT_BF16>::key(t & 0xFFFFu); }
+
+// Lane tag lists: every lane keeps the tags of the candidate vectors it
+// streamed (stream order), kLaneTags per row; tag q of a lane sits at
+// [row][warp][q][lane] (conflict-free).
+__device__ __forceinline__ uint32_t lane_tags_purge(uint32_t* L, uint32_t n, uint32_t kthr) {
+  uint32_t out = 0;
+  for (uint32_t q = 0; q < n; ++q) {
+    const uint32_t t = L[32 * q];
+    if (tag_key(t) >= kthr) L[32 * (out++)] = t;
+  }
+  return out;
+}
+__device__ __forceinline__ uint32_t lane_tags_min_key(const uint32_t* L, uint32_t n) {
+  uint32_t k = 0xFFFFFFFFu;
+  for (uint32_t q = 0; q < n; ++q) k = min(k, tag_key(L[32 * q]));
+  return k;
+}
+
+// The gathered vectors of one warp and row: its tags at or above the bound
+// (index order); the vectors themselves are read from the row on demand.
+struct GList {
+  const uint32_t* tags;
+  const unsigned char* row;
+  const uint4* vc;  // the gathered vectors themselves (same order), or null: read from the row
+};
+
+
+// The cut of the row from a histogram of exact keys (slot key & (kWindow -
+// 1), keys g.klo .. g.kmax), scanned by one warp from the top: lane l holds
+// the 16 keys below 4 * (kmax >> 2) + 3 - 16 l, their counts and lattice
+// masses summed, then one warp-wide prefix (count, double-float mass).
+// Top-k: where the running count reaches top_k (sh.cutk); top-p (on the
+// top-k set, if any): where the running mass reaches top_p * Z, a token being
+// kept while the mass ranked before it is below the target (sh.cut).  The
+// lane holding a crossing walks its 16 keys.  A cut below the window leaves
+// found = 0.  The count and mass above the window (g.c0, g.m0) start the
+// running sums; the window's own totals are left in sh.s_C[0][0], sh.s_M[0][0].
+// With given_k the top-k cut in sh.cutk is taken as found earlier and only
+// top-p is scanned.  Whole CTA (one barrier).
+template <int DT, int NR>
+__device__ __noinline__ void cut_scan(Shm& sh, const uint32_t* hist, float c, int top_k, float top_p,
+                                      bool given_k = false) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  if (warp == sh.lead) {
+    const RowG g = sh.g[0];
+    CutOut ck = sh.cutk[0];
+    if (!given_k) ck.found = 0;
+    __syncwarp();
+    if (lane == 0) {
+      sh.cut[0].found = 0;
+      if (!given_k) sh.cutk[0].found = 0;
+    }
+    __syncwarp();
+    const uint32_t gtop = g.kmax >> 2;
+    const uint32_t span = 4u * gtop + 3u;  // keys 0 .. span; lane l takes span - 16 l down to span - 16 l - 15
+    const uint32_t top = span - 16u * static_cast<uint32_t>(lane);
+    const bool live = g.active && span >= 16u * static_cast<uint32_t>(lane);
+    uint32_t Cl = 0u;
+    float Ml = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {  // (selects, no branches)
+      const uint32_t key = top - static_cast<uint32_t>(j);
+      const bool in = live && 16u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(j) <= span &&
+                      key <= g.kmax && key >= g.klo;
+      const uint32_t n = in ? hist[hslot(key)] : 0u;
+      const float ms = lat_mass(value_of_key<DT>(key), c, g.K);
+      Cl += n;
+      Ml += n ? static_cast<float>(n) * ms : 0.f;
+    }
+    const uint32_t Craw = warp_incl_scan_u32(Cl);
+    const DF Mraw = warp_incl_scan_df(DF{Ml, 0.f});
+    const uint32_t Cin = Craw + g.c0, Cex = Cin - Cl;
+    const DF Min = df_add2(g.m0, Mraw);
+    DF Mex = df_shfl_up(Min, 1);
+    if (lane == 0) Mex = g.m0;
+    if (lane == 31) {  // the window's own totals
+      sh.s_C[0][0] = Craw;
+      sh.s_M[0][0] = Mraw;
+    }
+    if (lane > 0 && lane < kScanWarps) {
+      sh.s_C[0][lane] = 0u;
+      sh.s_M[0][lane] = DF{0.f, 0.f};
+    }
+    // The crossing lane's 16 keys resolved by the warp: lane j < 16 takes
+    // its key j (count, mass), then one warp prefix over them.
+    auto lane_keys = [&](int xl, uint32_t& key, uint32_t& n, float& ms) {
+      const uint32_t topx = span - 16u * static_cast<uint32_t>(xl);
+      const uint32_t jj = static_cast<uint32_t>(lane);
+      key = topx - jj;
+      const bool in = lane < 16 && 16u * static_cast<uint32_t>(xl) + jj <= span && key <= g.kmax && key >= g.klo;
+      n = in ? hist[hslot(key)] : 0u;
+      ms = lat_mass(value_of_key<DT>(key), c, g.K);
+    };
+    if (topk_on && !given_k) {  // the value where the running count reaches top_k
+      const uint32_t Kc = static_cast<uint32_t>(top_k);
+      const unsigned bal = __ballot_sync(kFull, live && Cin >= Kc && Cex < Kc);
+      if (bal) {  // (warp-uniform)
+        const int xl = __ffs(bal) - 1;
+        uint32_t key, n;
+        float ms;
+        lane_keys(xl, key, n, ms);
+        const uint32_t run0 = __shfl_sync(kFull, Cex, xl);
+        const DF mb0 = DF{__shfl_sync(kFull, Mex.hi, xl), __shfl_sync(kFull, Mex.lo, xl)};
+        const uint32_t ci = warp_incl_scan_u32(n);
+        const DF mi = warp_incl_scan_df(DF{n ? static_cast<float>(n) * ms : 0.f, 0.f});
+        DF me = df_shfl_up(mi, 1);
+        if (lane == 0) me = DF{0.f, 0.f};
+        const uint32_t before = run0 + ci - n;
+        const unsigned hit = __ballot_sync(kFull, n > 0u && before < Kc && before + n >= Kc);
+        if (hit && lane == __ffs(hit) - 1) {
+          ck.kstar = key;
+          ck.keep = Kc - before;
+          ck.total = n;
+          ck.found = 1;
+          ck.zkept = df_add(df_add2(mb0, me), static_cast<float>(Kc - before) * ms);
+          sh.cutk[0] = ck;
+          if (!topp_on) sh.cut[0] = ck;
+        }
+        const int src = hit ? __ffs(hit) - 1 : 0;
+        ck.found = __shfl_sync(kFull, hit ? 1 : 0, src);
+        ck.kstar = __shfl_sync(kFull, ck.kstar, src);
+        ck.keep = __shfl_sync(kFull, ck.keep, src);
+        ck.total = __shfl_sync(kFull, ck.total, src);
+        ck.zkept = DF{__shfl_sync(kFull, ck.zkept.hi, src), __shfl_sync(kFull, ck.zkept.lo, src)};
+      }
+    }
+    if (topp_on && (!topk_on || ck.found)) {
+      const DF target = df_mul_f(topk_on ? ck.zkept : g.z, top_p);
+      // the first lane whose running mass reaches the target (a window
+      // holding less than the target leaves the cut unfound)
+      const unsigned bal = __ballot_sync(kFull, live && !df_lt(Min, target));
+      const int xl = bal ? __ffs(bal) - 1 : 0;
+      const DF mb0 = DF{__shfl_sync(kFull, Mex.hi, xl), __shfl_sync(kFull, Mex.lo, xl)};
+      if (bal && df_lt(mb0, target)) {  // (warp-uniform)
+        uint32_t key, n;
+        float ms;
+        lane_keys(xl, key, n, ms);
+        uint32_t ce = n;
+        if (topk_on) ce = key < ck.kstar ? 0u : (key == ck.kstar ? ck.keep : ce);
+        const DF mi = warp_incl_scan_df(DF{ce ? static_cast<float>(ce) * ms : 0.f, 0.f});
+        DF me = df_shfl_up(mi, 1);
+        if (lane == 0) me = DF{0.f, 0.f};
+        const DF before = df_add2(mb0, me), after = df_add2(mb0, mi);
+        const unsigned hit = __ballot_sync(kFull, ce > 0u && !df_lt(after, target));
+        // (rounding may leave the crossing past these keys: then all of the last one)
+        const unsigned pos = __ballot_sync(kFull, ce > 0u);
+        const int jc = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        if (jc >= 0 && lane == jc) {
+          CutOut cp;
+          uint32_t keep = ce;
+          if (hit) {
+            const float need = df_float(df_add(target, -before.hi)) - before.lo;
+            keep = static_cast<uint32_t>(ceilf(need / ms));
+            keep = max(1u, min(keep, ce));
+          }
+          cp.kstar = key;
+          cp.keep = keep;
+          cp.total = n;
+          cp.found = 1;
+          cp.zkept = df_add(before, static_cast<float>(keep) * ms);
+          sh.cut[0] = cp;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Exact counts of the row's tokens with keys in [klo, khi] (klo .. klo +
+// kWindow - 1, slot hslot(key)), by one re-read of the row with four loads
+// in flight per thread.  Whole CTA.
+template <int DT>
+__device__ __noinline__ void window_pass(uint32_t* hist, const unsigned char* row, int V, bool aligned,
+                                         uint32_t klo, uint32_t khi, uint32_t* priv) {
+  using E = Elt<DT>;
+  constexpr int kU = 4;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  // each warp counts into its own copy when priv is given (fewer colliding
+  // atomics on the common values), then the copies are summed
+  uint32_t* const mine = priv ? priv + (threadIdx.x >> 5) * kWindow : hist;
+  for (int t = threadIdx.x; t < kWindow; t += kThreads) hist[t] = 0u;
+  if (priv)
+    for (int t = threadIdx.x; t < kWarps * kWindow; t += kThreads) priv[t] = 0u;
+  __syncthreads();
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kU * kThreads) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = v0 + u * kThreads;
+      x[u] = v < nvec ? load_vec<DT>(row, v, V, aligned) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int t0 = (v0 + u * kThreads) * E::kPerVec;
+#pragma unroll
+      for (int j = 0; j < E::kPerVec; ++j) {
+        const uint32_t k = E::key(E::bits_of(x[u], j));
+        if (t0 + j < V && k >= klo && k <= khi) red_add_shared(smem_addr(mine + hslot(k)), 1u);
+      }
+    }
+  }
+  __syncthreads();
+  if (priv) {
+    for (int t = threadIdx.x; t < kWindow; t += kThreads) {
+      uint32_t sum = 0u;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) sum += priv[w * kWindow + t];
+      hist[t] = sum;
+    }
+    __syncthreads();
+  }
+}
+
+constexpr int kSlowWindows = 8;  // windows of kWindow keys tried before the bitwise search
+
+// The exact cut of a row that the candidate vectors do not decide: windows
+// of kWindow consecutive keys from the row maximum down, each counted by a
+// re-read of the row and scanned with the count and mass above it carried,
+// until the window holding the cut.  Top-k first; top-p then scans the same
+// windows on the top-k set.  A cut more than kSlowWindows windows down
+// takes the bitwise search.  Whole CTA; sh.g[0] is left as it was.
+template <int DT>
+__device__ __noinline__ CutOut window_cut(Shm& sh, uint32_t* hist, const unsigned char* row, int V, bool aligned,
+                                          int top_k, float top_p, const RowStat& rs, double zfull,
+                                          uint32_t* priv) {
+  // (32-bit keys are too fine for windows of kWindow keys)
+  if (Elt<DT>::kKeyBits > 16) return search_cut<DT>(sh, row, V, aligned, top_k, top_p, rs, zfull);
+  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
+  const RowG g0 = sh.g[0];
+  bool ok = true;
+#pragma unroll 1
+  for (int phase = 0; phase < 2 && ok; ++phase) {
+    const bool kphase = phase == 0;
+    if (kphase ? !topk_on : !topp_on) continue;
+    uint32_t hi = g0.kmax, c0 = 0u;
+    DF m0{0.f, 0.f};
+    bool found = false;
+#pragma unroll 1
+    for (int w = 0; w < kSlowWindows && !found; ++w) {
+      const uint32_t gt = hi >> 2;
+      const uint32_t lo = gt >= static_cast<uint32_t>(kGroups - 1) ? 4u * (gt - static_cast<uint32_t>(kGroups - 1)) : 0u;
+      window_pass<DT>(hist, row, V, aligned, lo, hi, priv);
+      if (threadIdx.x == 0) {
+        RowG g = g0;
+        g.kmax = hi;
+        g.klo = lo;
+        g.c0 = c0;
+        g.m0 = m0;
+        g.active = 1;
+        sh.g[0] = g;
+      }
+      __syncthreads();
+      cut_scan<DT, 1>(sh, hist, rs.c, top_k, kphase ? 1.f : top_p, !kphase);
+      found = (kphase ? sh.cutk[0].found : sh.cut[0].found) != 0;
+      if (!found) {
+#pragma unroll
+        for (int q = 0; q < kScanWarps; ++q) {
+          c0 += sh.s_C[0][q];
+          m0 = df_add2(m0, sh.s_M[0][q]);
+        }
+        if (lo == 0u) break;
+        hi = lo - 1u;
+      }
+      __syncthreads();
+    }
+    ok = found;
+  }
+  CutOut co = sh.cut[0];
+  __syncthreads();
+  if (threadIdx.x == 0) sh.g[0] = g0;
+  __syncthreads();
+  if (!ok) co = search_cut<DT>(sh, row, V, aligned, top_k, top_p, rs, zfull);
+  return co;
+}
+
+// Tie cut of a row: tokens of value kstar are kept in index order, the
+// first `keep` of them.  Every warp counts its tokens (in its gathered
+// vectors, or in its segment of the row re-read), the warp holding token
+// number `keep` (0-based) finds its row index.  Whole CTA.
+template <int DT, bool FROM_LIST>
+__device__ __noinline__ int tie_cut_of(Shm& sh, const GList& L, uint32_t len, const unsigned char* row, int V,
+                                       bool aligned, uint32_t kstar, uint32_t keep) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const uint32_t thr = H::thr_pack(E::bits_of_key(kstar));
+  const int rounds = FROM_LIST ? static_cast<int>((len + 31) / 32) : sg.iters;
+  auto vec_at = [&](int it, uint4& x) -> int {
+    if (FROM_LIST) {
+      const uint32_t i = it * 32 + lane;
+      if (i >= len) return -1;
+      const int v = sg.beg + static_cast<int>(tag_local(L.tags[i]));
+      x = L.vc ? L.vc[i] : load_vec<DT>(L.row, v, V, aligned);
+      return v;
+    }
+    const int v = sg.beg + it * 32 + lane;
+    if (v >= sg.end) return -1;
+    x = load_vec<DT>(row, v, V, aligned);
+    return v;
+  };
+  uint32_t c = 0;
+  for (int it = 0; it < rounds; ++it) {
+    uint4 x;
+    const int v = vec_at(it, x);
+    if (v >= 0) c += __popc(H::mask_eq(x, thr) & vmask<DT>(v, V));
+  }
+  c = warp_sum_u32(c);
+  if (lane == 0) sh.w_u[warp][0] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t run = 0;
+    sh.tie_warp[0] = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      if (run + sh.w_u[w][0] > keep) { sh.tie_warp[0] = w; sh.tie_j[0] = keep - run; break; }
+      run += sh.w_u[w][0];
+    }
+    sh.tie_cut[0] = V;  // all kept (only if the counts disagree)
+  }
+  __syncthreads();
+  if (warp == sh.tie_warp[0]) {
+    uint32_t jj = sh.tie_j[0];
+    for (int it = 0; it < rounds; ++it) {
+      uint4 x;
+      const int v = vec_at(it, x);
+      const uint32_t msk = v >= 0 ? (H::mask_eq(x, thr) & vmask<DT>(v, V)) : 0u;
+      const uint32_t cc = __popc(msk);
+      const uint32_t incl = warp_incl_scan_u32(cc);
+      const uint32_t tot = __shfl_sync(kFull, incl, 31);
+      if (jj < tot) {
+        if (incl > jj && incl - cc <= jj) {
+          uint32_t mm = msk;
+          for (uint32_t q = jj - (incl - cc); q > 0; --q) mm &= mm - 1u;
+          sh.tie_cut[0] = v * E::kPerVec + (__ffs(mm) - 1);
+        }
+        break;
+      }
+      jj -= tot;
+    }
+  }
+  __syncthreads();
+  const int r = sh.tie_cut[0];
+  __syncthreads();
+  return r;
+}
+
+// The filtered, normalised probabilities of a row, written out.
 template <int DT>
 __device__ __noinline__ void write_probs(const unsigned char* row, int V, bool aligned, const RowStat& rp_in,
                                          float* out) {
@@ -544,6 +927,54 @@ __device__ __forceinline__ float vec_weights(const RowStat& rp, const RowStat& r
   }
   *ps = sp;
   return s;
+}
+
+}  // namespace
+
+constexpr int ROLE_P = 0;      // target row of a draft position
+constexpr int ROLE_Q = 1;      // draft row of a draft position
+constexpr int ROLE_BONUS = 2;  // target row after the last draft
+constexpr int ROLE_PROBS = 3;  // one row of spec_transform_probs
+
+// The row of CTA `cta` in the stream and tail kernels: the target (even) and
+// draft (odd) rows of every draft position, then the bonus target rows
+// (MODE_PROBS: row cta).
+struct RowRef {
+  int role, b, pos;
+  const unsigned char* row;
+  bool aligned;
+};
+template <int DT>
+__device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int cta) {
+  using E = Elt<DT>;
+  const unsigned char* tgt = static_cast<const unsigned char*>(a.target);
+  const size_t rb = static_cast<size_t>(a.V) * E::kBytes;
+  RowRef r;
+  if (a.mode == MODE_PROBS) {
+    r.role = ROLE_PROBS;
+    r.b = cta;
+    r.pos = 0;
+    r.row = tgt + static_cast<size_t>(cta) * rb;
+    r.aligned = a.aligned_target != 0;
+    return r;
+  }
+  const int k = a.k, npairs = a.B * k;
+  if (cta < 2 * npairs) {
+    const int pair = cta >> 1;
+    r.role = (cta & 1) ? ROLE_Q : ROLE_P;
+    r.b = pair / k;
+    r.pos = pair % k;
+    r.row = r.role == ROLE_P ? tgt + static_cast<size_t>(r.b * (k + 1) + r.pos) * rb
+                             : static_cast<const unsigned char*>(a.draft) + static_cast<size_t>(pair) * rb;
+    r.aligned = (r.role == ROLE_P ? a.aligned_target : a.aligned_draft) != 0;
+  } else {
+    r.role = ROLE_BONUS;
+    r.b = cta - 2 * npairs;
+    r.pos = k;
+    r.row = tgt + static_cast<size_t>(r.b * (k + 1) + k) * rb;
+    r.aligned = a.aligned_target != 0;
+  }
+  return r;
 }
 
 // -------------------------------------------------------------- the draw
@@ -840,821 +1271,466 @@ __device__ __forceinline__ RowStat ldcg_rowstat(const RowStat* p) {
   return r;
 }
 
-
-// ------------------------------------------------------------ work items
-constexpr int ROLE_P = 0;      // target row of a draft position
-constexpr int ROLE_Q = 1;      // draft row of a draft position
-constexpr int ROLE_BONUS = 2;  // target row after the last draft
-constexpr int ROLE_PROBS = 3;  // one row of spec_transform_probs
-
-// Row item `item`: sequence by sequence, the target and draft rows of each
-// draft position, then the bonus target row (MODE_PROBS: row `item`).
-// `pub` is the row's record: 2 (b k + i) + role for draft positions, 2 B k + b
-// for the bonus rows.
-struct RowRef {
-  int role, b, pos, pub;
-  const unsigned char* row;
-  bool aligned;
-};
-template <int DT>
-__device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int item) {
-  using E = Elt<DT>;
-  const unsigned char* tgt = static_cast<const unsigned char*>(a.target);
-  const size_t rb = static_cast<size_t>(a.V) * E::kBytes;
-  RowRef r;
-  if (a.mode == MODE_PROBS) {
-    r.role = ROLE_PROBS;
-    r.b = item;
-    r.pos = 0;
-    r.pub = item;
-    r.row = tgt + static_cast<size_t>(item) * rb;
-    r.aligned = a.aligned_target != 0;
-    return r;
-  }
-  const int k = a.k;
-  r.b = item / (2 * k + 1);
-  const int j = item - r.b * (2 * k + 1);
-  if (j < 2 * k) {
-    r.role = (j & 1) ? ROLE_Q : ROLE_P;
-    r.pos = j >> 1;
-    r.pub = 2 * (r.b * k + r.pos) + (j & 1);
-    r.row = r.role == ROLE_P ? tgt + (static_cast<size_t>(r.b) * (k + 1) + r.pos) * rb
-                             : static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(r.b) * k + r.pos) * rb;
-    r.aligned = (r.role == ROLE_P ? a.aligned_target : a.aligned_draft) != 0;
-  } else {
-    r.role = ROLE_BONUS;
-    r.pos = k;
-    r.pub = 2 * a.B * k + r.b;
-    r.row = tgt + (static_cast<size_t>(r.b) * (k + 1) + k) * rb;
-    r.aligned = a.aligned_target != 0;
-  }
-  return r;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_shared_u32(uint32_t a) {
-  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Running maximum of a thread, as bits: bf16x2 (both halves), or f32.
-template <int DT>
-struct RunMax;
-template <>
-struct RunMax<DT_BF16> {
-  static constexpr uint32_t kNeg = 0xFF80FF80u;
-  __device__ static __forceinline__ uint32_t vec(const uint4& x) {
-    const uint32_t m = hmax2(hmax2(x.x, x.y), hmax2(x.z, x.w));
-    return hmax2(m, __byte_perm(m, 0, 0x1032));
-  }
-  __device__ static __forceinline__ uint32_t join(uint32_t a, uint32_t b) { return hmax2(a, b); }
-  __device__ static __forceinline__ uint32_t bits(uint32_t m) { return m & 0xFFFFu; }
-  __device__ static __forceinline__ float value(uint32_t m) { return __uint_as_float(m & 0xFFFF0000u); }
-};
-template <>
-struct RunMax<DT_F32> {
-  static constexpr uint32_t kNeg = 0xFF800000u;
-  __device__ static __forceinline__ uint32_t vec(const uint4& x) {
-    return __float_as_uint(max_nan(max_nan(__uint_as_float(x.x), __uint_as_float(x.y)),
-                                   max_nan(__uint_as_float(x.z), __uint_as_float(x.w))));
-  }
-  __device__ static __forceinline__ uint32_t join(uint32_t a, uint32_t b) {
-    return __float_as_uint(max_nan(__uint_as_float(a), __uint_as_float(b)));
-  }
-  __device__ static __forceinline__ uint32_t bits(uint32_t m) { return m; }
-  __device__ static __forceinline__ float value(uint32_t m) { return __uint_as_float(m); }
-};
-
-// ---------------------------------------------------------------- stream
-// One row streamed once by the CTA (see the file comment).  Leaves in sh:
-// mbits (row maximum), K, z (row sum of 2^(l c - K)), and for FILT the
-// histogram window (kb, corrupt), the candidate list (nlist) and their data
-// in dsm.
-template <int DT, bool FILT>
-__device__ __noinline__ void stream_row(const unsigned char* row, int V, bool aligned, float c, Shm& sh,
-                                        unsigned char* dsm) {
-  using E = Elt<DT>;
-  using M = RunMax<DT>;
-  constexpr int U = kStreamU;
-  constexpr int PV = E::kPerVec;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = (V + PV - 1) / PV;
-  constexpr int kStep = kThreads * U;
-  const int iters = (nvec + kStep - 1) / kStep;
-  const uint32_t hbase = smem_addr(dsm);
-  const uint32_t qd = smem_addr(dsm + kQDataOff) + warp * kQCap * 16;
-  const uint32_t qi = smem_addr(dsm + kQIdxOff) + warp * kQCap * 4;
-  uint4* const ldata = reinterpret_cast<uint4*>(dsm + kListOff);
-  uint32_t* const lidx = reinterpret_cast<uint32_t*>(dsm + kListIdxOff);
-  const uint4 pad = make_uint4(Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad);
-  if (FILT) {
-    uint32_t* hist = reinterpret_cast<uint32_t*>(dsm);
-    for (int i = tid; i < kRing; i += kThreads) hist[i] = 0u;
-    if (tid == 0) {
-      sh.nlist = 0;
-      sh.corrupt = 0;
-    }
-  }
-  uint4 cur[U], nxt[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int v = u * kThreads + tid;
-    cur[u] = v < nvec ? load_vec<DT>(row, v, V, aligned) : pad;
-  }
-  uint32_t mx = M::kNeg;
-#pragma unroll
-  for (int u = 0; u < U; ++u) mx = M::join(mx, M::vec(cur[u]));
-
-  // window and lattice state (the same in every thread)
-  float K = 0.f, lbf = __int_as_float(0x7F800000);  // +inf: nothing is a candidate until anchored
-  bool anchored = false, lbpos = false;
-  uint32_t ktop = 0u, kb = 0u;
-  int corrupt = 0;
-  u64 nk2 = pkf(-0.f, -0.f);
-  const u64 c2 = pkf(c, c);
-  u64 acc0 = pkf(0.f, 0.f), acc1 = pkf(0.f, 0.f);
-  int par = 0;
-  uint32_t qn = 0u, qf = 0u;
-  const uint32_t ltmask = (1u << lane) - 1u;
-
-  // The window update: every thread takes the CTA maximum seen so far; a
-  // higher maximum raises K (exact rescale of the partial sums), the window
-  // bottom (its departing slots cleared) and the anchor.
-  auto update = [&]() {
-    uint32_t m1 = mx;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m1 = M::join(m1, __shfl_xor_sync(kFull, m1, o));
-    if (lane == 0) sh.wm[par][warp] = m1;
-    __syncthreads();
-    uint32_t m = sh.wm[par][0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) m = M::join(m, sh.wm[par][w]);
-    par ^= 1;
-    const uint32_t mb = M::bits(m);
-    const float mv = M::value(m);
-    if (!isfinite(mv) || !(fabsf(mv * c) < 1073741824.f)) return;  // (bad rows are found at the end)
-    const uint32_t nt = E::key(mb);
-    if (anchored && nt <= ktop) return;
-    const float nK = ceilf(mv * c);
-    if (anchored) {
-      const float s = exp2i(static_cast<int>(K - nK));
-      const u64 s2 = pkf(s, s);
-      acc0 = mul2(acc0, s2);
-      acc1 = mul2(acc1, s2);
-      if (FILT && nt > ktop + static_cast<uint32_t>(kFreeKeys)) corrupt = 1;
-    }
-    K = nK;
-    nk2 = pkf(-K, -K);
-    if (FILT && DT == DT_BF16) {
-      uint32_t nkb = E::key(bits_round_up<DT>(mv - kDelta / c));
-      if (nt >= static_cast<uint32_t>(kWinKeys - 1)) nkb = max(nkb, nt - static_cast<uint32_t>(kWinKeys - 1));
-      if (anchored && nkb > kb) {  // departing keys: their slots are cleared (their masses stay in the sums)
-        uint32_t* hist = reinterpret_cast<uint32_t*>(dsm);
-        const uint32_t end = min(nkb, kb + static_cast<uint32_t>(kRing));
-        for (uint32_t kk = kb + tid; kk < end; kk += kThreads) hist[kk & (kRing - 1)] = 0u;
-      }
-      if (!anchored || nkb > kb) {
-        kb = nkb;
-        lbf = value_of_key<DT>(kb);
-        lbpos = lbf > 0.f;
-      }
-    }
-    ktop = nt;
-    anchored = true;
-  };
-
-  // Count queued vectors [e, e + 32) of this warp (lanes at or past `cnt`
-  // idle) into the histogram and append them to the candidate list.
-  auto flush = [&](uint32_t e0, uint32_t cnt) {
-    __syncwarp();
-    const bool has = static_cast<uint32_t>(lane) < cnt;
-    uint4 d = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t vi = 0u;
-    if (has) {
-      const uint32_t slot = (e0 + lane) & (kQCap - 1);
-      d = lds128(qd + slot * 16);
-      vi = lds_u32(qi + slot * 4);
-      const uint32_t w4[4] = {d.x, d.y, d.z, d.w};
-      if (lbpos) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t w = w4[j];
-          if (__uint_as_float(w << 16) >= lbf) red_shared_u32(hbase + ((w << 2) & ((kRing - 1) << 2)));
-          if (__uint_as_float(w & 0xFFFF0000u) >= lbf) red_shared_u32(hbase + ((w >> 14) & ((kRing - 1) << 2)));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t bj = (j & 1) ? (w4[j >> 1] >> 16) : (w4[j >> 1] & 0xFFFFu);
-          if (E::value(bj) >= lbf) red_shared_u32(hbase + ((E::key(bj) & (kRing - 1)) << 2));
-        }
-      }
-    }
-    __syncwarp();
-    int base = 0;
-    if (lane == 0) base = atomicAdd(&sh.nlist, static_cast<int>(cnt));
-    base = __shfl_sync(kFull, base, 0);
-    if (has && base + lane < kListCap) {
-      ldata[base + lane] = d;
-      lidx[base + lane] = vi;
-    }
-  };
-
-  if (FILT && DT == DT_BF16) update();
-  else {
-    // (unfiltered rows only need the lattice exponent: one update)
-    update();
-  }
-
-  for (int it = 0; it < iters; ++it) {
-    if (it + 1 < iters) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = (it + 1) * kStep + u * kThreads + tid;
-        nxt[u] = v < nvec ? load_vec<DT>(row, v, V, aligned) : pad;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint4 x = cur[u];
-      const uint32_t vm = M::vec(x);
-      mx = M::join(mx, vm);
-      Hot<DT>::mass_vec(x, c2, nk2, acc0, acc1);
-      if (FILT && DT == DT_BF16) {
-        const bool cand = M::value(vm) >= lbf;
-        const uint32_t bal = __ballot_sync(kFull, cand);
-        if (bal) {
-          const uint32_t pos = qn + __popc(bal & ltmask);
-          if (cand) {
-            const uint32_t slot = pos & (kQCap - 1);
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qd + slot * 16), "r"(x.x), "r"(x.y), "r"(x.z),
-                         "r"(x.w)
-                         : "memory");
-            sts_u32(qi + slot * 4, static_cast<uint32_t>(it * kStep + u * kThreads + tid));
-          }
-          qn += __popc(bal);
-          if (qn - qf >= 32u) {
-            flush(qf, 32u);
-            qf += 32u;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) cur[u] = nxt[u];
-    if (((it + 1) % kSyncEvery) == 0 && it + 1 < iters) update();
-  }
-  if (FILT && DT == DT_BF16 && qn != qf) flush(qf, qn - qf);
-
-  // the row maximum and sum
-  {
-    uint32_t m1 = mx;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m1 = M::join(m1, __shfl_xor_sync(kFull, m1, o));
-    float a0, a1, a2, a3;
-    upk(acc0, a0, a1);
-    upk(acc1, a2, a3);
-    DF z{(a0 + a1) + (a2 + a3), 0.f};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z = df_add2(z, DF{__shfl_xor_sync(kFull, z.hi, o), __shfl_xor_sync(kFull, z.lo, o)});
-    if (lane == 0) {
-      sh.wm[par][warp] = m1;
-      sh.wz[warp] = z;
-    }
-    if (FILT && tid == 0) {
-      sh.kb = kb;
-      if (!anchored) corrupt = 1;
-      sh.corrupt = corrupt;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t m = sh.wm[par][0];
-      DF t{0.f, 0.f};
-      for (int w = 0; w < kWarps; ++w) {
-        m = M::join(m, sh.wm[par][w]);
-        t = df_add2(t, sh.wz[w]);
-      }
-      const float mv = M::value(m);
-      float Kf = K;
-      if (isfinite(mv) && fabsf(mv * c) < 1073741824.f) {
-        Kf = ceilf(mv * c);
-        if (Kf > K) {  // elements above the last anchor: exact rescale to the final exponent
-          const float s = exp2i(static_cast<int>(K - Kf));
-          t = DF{t.hi * s, t.lo * s};
-        }
-        if (FILT && (!anchored || E::key(M::bits(m)) > ktop + static_cast<uint32_t>(kFreeKeys))) sh.corrupt = 1;
-      }
-      sh.mbits = M::bits(m);
-      sh.K = Kf;
-      sh.z = t;
-    }
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------- the cut from the ring
-// Exclusive CTA scan (thread order) of a count and a mass; totals too.
-__device__ __forceinline__ void block_scan_cm(Shm& sh, uint32_t c, double m, uint32_t& cb, double& mb, uint32_t& ct,
-                                              double& mt) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t ci = c;
-  double mi = m;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t co = __shfl_up_sync(kFull, ci, o);
-    const double mo = __shfl_up_sync(kFull, mi, o);
-    if (lane >= o) {
-      ci += co;
-      mi += mo;
-    }
-  }
-  if (lane == 31) {
-    sh.sc_cnt[warp] = ci;
-    sh.sc_mass[warp] = mi;
-  }
-  __syncthreads();
-  uint32_t wc = 0u, tc = 0u;
-  double wmass = 0.0, tm = 0.0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) {
-      wc += sh.sc_cnt[w];
-      wmass += sh.sc_mass[w];
-    }
-    tc += sh.sc_cnt[w];
-    tm += sh.sc_mass[w];
-  }
-  __syncthreads();
-  cb = wc + ci - c;
-  mb = wmass + (mi - m);
-  ct = tc;
-  mt = tm;
-}
-
-// The top-k / top-p cut from the histogram ring (keys kb .. kmax).  Fills
-// rs.kstar, rs.keep, rs.total and *zkept.  False when the cut may lie below
-// the window (the caller then searches the whole row).  Whole CTA.
-template <int DT>
-__device__ __noinline__ bool cut_from_hist(Shm& sh, const uint32_t* hist, RowStat& rs, int top_k, float top_p,
-                                           double zfull, uint32_t kb, double* zkept) {
-  const int tid = threadIdx.x;
-  const bool topk_on = top_k > 0, topp_on = top_p < 1.f;
-  const uint32_t kmax = rs.kmax;
-  if (kmax < kb) return false;
-  const int nk = static_cast<int>(kmax - kb) + 1;
-  if (nk > kRing) return false;
-  const int per = (nk + kThreads - 1) / kThreads;
-  const int i0 = min(nk, tid * per), i1 = min(nk, i0 + per);
-  uint32_t cnt = 0u;
-  double mass = 0.0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = kmax - static_cast<uint32_t>(i);
-    const uint32_t n = hist[key & (kRing - 1)];
-    if (n) {
-      cnt += n;
-      mass += static_cast<double>(n) * static_cast<double>(lat_mass(value_of_key<DT>(key), rs.c, rs.K));
-    }
-  }
-  if (tid == 0) sh.found = 0;
-  uint32_t cb, ct;
-  double mb, mt;
-  block_scan_cm(sh, cnt, mass, cb, mb, ct, mt);
-  // top-k: the value holding the top_k-th token
-  double zk = zfull;
-  uint32_t vk = 0u;
-  int ck = 0;
-  if (topk_on) {
-    if (ct < static_cast<uint32_t>(top_k)) return false;  // (uniform: every thread has the totals)
-    if (cb < static_cast<uint32_t>(top_k) && cb + cnt >= static_cast<uint32_t>(top_k)) {
-      uint32_t rc = cb;
-      double rm = mb;
-      for (int i = i0; i < i1; ++i) {
-        const uint32_t key = kmax - static_cast<uint32_t>(i);
-        const uint32_t n = hist[key & (kRing - 1)];
-        if (!n) continue;
-        const double w = static_cast<double>(lat_mass(value_of_key<DT>(key), rs.c, rs.K));
-        if (rc + n >= static_cast<uint32_t>(top_k)) {
-          sh.vk = key;
-          sh.ck = top_k - static_cast<int>(rc);
-          sh.cnt_vk = static_cast<int>(n);
-          sh.zk = rm + static_cast<double>(top_k - static_cast<int>(rc)) * w;
-          break;
-        }
-        rc += n;
-        rm += static_cast<double>(n) * w;
-      }
-    }
-    __syncthreads();
-    zk = sh.zk;
-    vk = sh.vk;
-    ck = sh.ck;
-  }
-  if (!topp_on) {
-    rs.kstar = vk;
-    rs.keep = ck;
-    rs.total = sh.cnt_vk;
-    *zkept = zk;
-    return true;
-  }
-  // top-p on the top-k set: the first value at which the mass ranked at or
-  // above it reaches top_p * zk; its tokens are kept while the mass before
-  // them is below that target
-  const double target = static_cast<double>(top_p) * zk;
-  if (!topk_on && mt < target) return false;
-  if (mb < target && mb + mass >= target) {
-    double rm = mb;
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t key = kmax - static_cast<uint32_t>(i);
-      const uint32_t n = hist[key & (kRing - 1)];
-      if (!n) continue;
-      const double w = static_cast<double>(lat_mass(value_of_key<DT>(key), rs.c, rs.K));
-      if (rm + static_cast<double>(n) * w >= target || (topk_on && key <= vk)) {
-        uint32_t vs = key, avail = n, tot = n;
-        double before = rm;
-        if (topk_on && key <= vk) {  // the crossing is at the top-k cut value, within its kept tokens
-          const double wk = static_cast<double>(lat_mass(value_of_key<DT>(vk), rs.c, rs.K));
-          vs = vk;
-          avail = static_cast<uint32_t>(ck);
-          tot = static_cast<uint32_t>(sh.cnt_vk);
-          before = zk - static_cast<double>(ck) * wk;
-        }
-        const double ws = static_cast<double>(lat_mass(value_of_key<DT>(vs), rs.c, rs.K));
-        double need = ws > 0.0 ? ceil((target - before) / ws) : static_cast<double>(avail);
-        if (!(need >= 1.0)) need = 1.0;
-        const uint32_t j = need >= static_cast<double>(avail) ? avail : static_cast<uint32_t>(need);
-        sh.vstar = vs;
-        sh.jstar = static_cast<int>(j);
-        sh.cnt_vstar = static_cast<int>(tot);
-        sh.zkept = before + static_cast<double>(j) * ws;
-        sh.found = 1;
-        break;
-      }
-      rm += static_cast<double>(n) * w;
-    }
-  }
-  __syncthreads();
-  if (!sh.found) return false;
-  rs.kstar = sh.vstar;
-  rs.keep = sh.jstar;
-  rs.total = sh.cnt_vstar;
-  *zkept = sh.zkept;
-  return true;
-}
-
-// ------------------------------------------------ tokens of one value
-// Tokens of key `kstar` among vectors [e0, e1) of a row with index < jmax.
-// Whole CTA; every thread gets the count.
-template <int DT>
-__device__ __noinline__ uint32_t count_equal(Shm& sh, const unsigned char* row, int V, bool aligned, int e0, int e1,
-                                             uint32_t kstar, int jmax) {
-  using E = Elt<DT>;
-  uint32_t cnt = 0u;
-  constexpr int kU = 4;
-  for (int v0 = e0 + static_cast<int>(threadIdx.x); v0 < e1; v0 += kU * kThreads) {
-    uint4 xs[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int v = v0 + u * kThreads;
-      xs[u] = v < e1 ? load_vec<DT>(row, v, V, aligned) : make_uint4(Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad);
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int v = v0 + u * kThreads;
-#pragma unroll
-      for (int j = 0; j < E::kPerVec; ++j) {
-        const int t = v * E::kPerVec + j;
-        if (v < e1 && t < jmax && t < V && E::key(E::bits_of(xs[u], j)) == kstar) ++cnt;
-      }
-    }
-  }
-  return block_sum_u32(cnt, sh);
-}
-
-// Index of the m-th (1-based) token of key `kstar` among vectors [e0, e1) in
-// index order, or -1.  Whole CTA: per-warp counts over equal parts, then the
-// warp holding it walks its part 32 vectors at a time.
-template <int DT>
-__device__ __noinline__ int find_nth_equal(Shm& sh, const unsigned char* row, int V, bool aligned, int e0, int e1,
-                                           uint32_t kstar, int m) {
-  using E = Elt<DT>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const Part pt = warp_part(e0, e1, warp);
-  uint32_t cnt = 0u;
-  for (int v = pt.beg + lane; v < pt.end; v += 32) {
-    const uint4 x = load_vec<DT>(row, v, V, aligned);
-#pragma unroll
-    for (int j = 0; j < E::kPerVec; ++j)
-      if (v * E::kPerVec + j < V && E::key(E::bits_of(x, j)) == kstar) ++cnt;
-  }
-  cnt = warp_sum_u32(cnt);
-  if (lane == 0) sh.w_u[warp][0] = cnt;
-  if (threadIdx.x == 0) sh.tie_idx = -1;
-  __syncthreads();
-  uint32_t before = 0u;
-  for (int w = 0; w < warp; ++w) before += sh.w_u[w][0];
-  if (before < static_cast<uint32_t>(m) && before + cnt >= static_cast<uint32_t>(m)) {
-    uint32_t run = before;
-    for (int v0 = pt.beg; v0 < pt.end; v0 += 32) {
-      const int v = v0 + lane;
-      uint4 x = make_uint4(Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad, Hot<DT>::kPad);
-      if (v < pt.end) x = load_vec<DT>(row, v, V, aligned);
-      uint32_t bits = 0u;
-#pragma unroll
-      for (int j = 0; j < E::kPerVec; ++j)
-        if (v < pt.end && v * E::kPerVec + j < V && E::key(E::bits_of(x, j)) == kstar) bits |= 1u << j;
-      const uint32_t lc = __popc(bits);
-      const uint32_t incl = warp_incl_scan_u32(lc);
-      const uint32_t tot = __shfl_sync(kFull, incl, 31);
-      if (run + tot >= static_cast<uint32_t>(m)) {
-        const uint32_t excl = incl - lc;
-        if (run + excl < static_cast<uint32_t>(m) && run + incl >= static_cast<uint32_t>(m)) {
-          uint32_t need = static_cast<uint32_t>(m) - run - excl;  // 1-based within this lane's vector
-          int idx = -1;
-#pragma unroll
-          for (int j = 0; j < E::kPerVec; ++j)
-            if (((bits >> j) & 1u) && idx < 0 && --need == 0u) idx = v * E::kPerVec + j;
-          sh.tie_idx = idx;
-        }
-        break;
-      }
-      run += tot;
-    }
-  }
-  __syncthreads();
-  return sh.tie_idx;
-}
-
-// The index bound of a row's tie from its candidate list (every token of the
-// cut value lies in a listed vector): the keep-th lowest index of the listed
-// tokens of key kstar, plus one.  -1 when the list cannot tell.  Whole CTA.
-template <int DT>
-__device__ __noinline__ int tie_cut_from_list(Shm& sh, const unsigned char* dsm, uint32_t* tix, int nlist,
-                                              uint32_t kstar, int keep, int total) {
-  using E = Elt<DT>;
-  const uint4* ldata = reinterpret_cast<const uint4*>(dsm + kListOff);
-  const uint32_t* lidx = reinterpret_cast<const uint32_t*>(dsm + kListIdxOff);
-  if (threadIdx.x == 0) {
-    sh.ntie = 0;
-    sh.tie_idx = -1;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < nlist; e += kThreads) {
-    const uint4 d = ldata[e];
-    const uint32_t v = lidx[e];
-#pragma unroll
-    for (int j = 0; j < E::kPerVec; ++j) {
-      if (E::key(E::bits_of(d, j)) == kstar) {
-        const int p = atomicAdd(&sh.ntie, 1);
-        if (p < kTieCap) tix[p] = v * E::kPerVec + j;
-      }
-    }
-  }
-  __syncthreads();
-  const int n = sh.ntie;
-  if (n != total || n > kTieRankMax) return -1;
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const uint32_t mine = tix[i];
-    int r = 0;
-    for (int j = 0; j < n; ++j) r += tix[j] < mine ? 1 : 0;
-    if (r == keep - 1) sh.tie_idx = static_cast<int>(mine);
-  }
-  __syncthreads();
-  return sh.tie_idx < 0 ? -1 : sh.tie_idx + 1;
-}
-
-// The vectors of a target row holding a token at or above value key kstar,
-// in index order, from its candidate list (a bitmap over the row's vectors
-// in the queues' place).  Returns their count (> kPubList: not listed).
-template <int DT>
-__device__ __noinline__ int kept_vectors(Shm& sh, unsigned char* dsm, int nlist, int nvec, uint32_t kstar,
-                                         uint32_t* out) {
-  using M = RunMax<DT>;
-  const uint4* ldata = reinterpret_cast<const uint4*>(dsm + kListOff);
-  const uint32_t* lidx = reinterpret_cast<const uint32_t*>(dsm + kListIdxOff);
-  uint32_t* bm = reinterpret_cast<uint32_t*>(dsm + kQDataOff);
-  const int nw = (nvec + 31) / 32;
-  if (nw * 4 > static_cast<int>(kBitmapBytes)) return kPubList + 1;
-  for (int i = threadIdx.x; i < nw; i += kThreads) bm[i] = 0u;
-  __syncthreads();
-  const float vs = value_of_key<DT>(kstar);
-  for (int e = threadIdx.x; e < nlist; e += kThreads) {
-    if (M::value(M::vec(ldata[e])) >= vs) {
-      const uint32_t v = lidx[e];
-      atomicOr(&bm[v >> 5], 1u << (v & 31u));
-    }
-  }
-  __syncthreads();
-  // ordered compaction: thread t takes words [t * per, (t + 1) * per)
-  const int per = (nw + kThreads - 1) / kThreads;
-  const int w0 = min(nw, static_cast<int>(threadIdx.x) * per), w1 = min(nw, w0 + per);
-  uint32_t c = 0u;
-  for (int i = w0; i < w1; ++i) c += __popc(bm[i]);
-  uint32_t cb, ct;
-  double mb, mt;
-  block_scan_cm(sh, c, 0.0, cb, mb, ct, mt);
-  if (ct <= static_cast<uint32_t>(kPubList)) {
-    uint32_t o = cb;
-    for (int i = w0; i < w1; ++i) {
-      uint32_t bits = bm[i];
-      while (bits) {
-        const int l = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        out[o++] = static_cast<uint32_t>(i * 32 + l);
-      }
-    }
-  }
-  return static_cast<int>(ct);
-}
-
-// ------------------------------------------------------------ one row
-template <int DT>
-__device__ __noinline__ void process_row(const SampleArgs& a, Shm& sh, unsigned char* dsm, const int item);
-
-// The records sequence b's rows published (headers and kept-vector lists)
-// and, with draw_recs, its whole-row draw records, zeroed once every reader
-// is done: the workspace is left zero for the next call whatever its shape.
-// Whole CTA.
-__device__ __noinline__ void clear_sequence(const SampleArgs& a, int b, bool draw_recs) {
+// The records of sequence b's rows (pubs) zeroed for the next call, whatever
+// its shape.  Whole CTA; every read of them is done.
+// nl_pre: the rows' list lengths already in shared memory, or null.
+__device__ __noinline__ void clear_sequence_pubs(const SampleArgs& a, int b, const uint32_t* nl_pre) {
+  __shared__ uint32_t s_nl[2 * kMaxK + 1];
   const int k = a.k, nrows = 2 * k + 1, tid = threadIdx.x;
-  auto pub_of = [&](int r) {
-    return r < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + r : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
-  };
+  auto row_pub = [&](int r) { return r < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + r
+                                                 : a.pubs + 2 * static_cast<size_t>(a.B) * k + b; };
   __syncthreads();
+  if (!nl_pre && tid < nrows) s_nl[tid] = __ldcg(&row_pub(tid)->nlist);
+  __syncthreads();
+  const uint32_t* const nls = nl_pre ? nl_pre : s_nl;
   for (int r = 0; r < nrows; ++r) {
-    RowPub* p = pub_of(r);
-    const uint32_t nl = __ldcg(&p->nlist);
+    const uint32_t nl = nls[r];
     if (nl != kPubReread)
-      for (uint32_t i = tid; i < nl && i < static_cast<uint32_t>(kPubList); i += kThreads) p->list[i] = 0u;
+      for (uint32_t i = tid; i < nl && i < static_cast<uint32_t>(kPubList); i += kThreads) row_pub(r)->list[i] = 0u;
   }
-  __syncthreads();
   constexpr int kHdrWords = static_cast<int>(offsetof(RowPub, list) / 4);
   for (int i = tid; i < nrows * kHdrWords; i += kThreads)
-    reinterpret_cast<uint32_t*>(pub_of(i / kHdrWords))[i % kHdrWords] = 0u;
-  if (draw_recs) {
-    float* cs = a.csums + static_cast<size_t>(b) * kMaxDrawChunks * kChunkRec;
-    for (int i = tid; i < kMaxDrawChunks * kChunkRec; i += kThreads) cs[i] = 0.f;
-    for (int i = tid; i < 2 * kMaxDrawChunks; i += kThreads) {
-      a.tcnt[static_cast<size_t>(b) * kMaxDrawChunks * 2 + i] = 0;
-      a.tcut[static_cast<size_t>(b) * kMaxDrawChunks * 2 + i] = 0;
-    }
-  }
+    reinterpret_cast<uint32_t*>(row_pub(i / kHdrWords))[i % kHdrWords] = 0u;
 }
 
-// The first-rejection rule and the draw for sequence b, run by the CTA that
-// finished its last row.
-template <int DT>
-__device__ __noinline__ void finish_sequence(const SampleArgs& a, Shm& sh, unsigned char* dsm, const int b) {
-  using E = Elt<DT>;
-  const int k = a.k, V = a.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
-  __threadfence();
-  int rej = k;
-  if (tid < k) {
-    const RowPub* pp = a.pubs + 2 * (static_cast<size_t>(b) * k + tid);
-    const float px = __ldcg(&pp[0].xprob), qx = __ldcg(&pp[1].xprob);
-    const int bp = __ldcg(&pp[0].rs.bad), bq = __ldcg(&pp[1].rs.bad);
-    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + tid];
-    const bool xok = x[tid] >= 0 && x[tid] < V;
-    if (!(!bp && !bq && xok && u * qx < px)) rej = tid;
-  }
-  if (warp == 0) {  // k <= 31: the first warp holds every position
-    const unsigned rb = __ballot_sync(kFull, rej < k);
-    if (lane == 0) sh.draw_chunk = rb ? __ffs(rb) - 1 : k;
-  }
-  __syncthreads();
-  const int n = sh.draw_chunk;
-  int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
-  if (tid < n) out[tid] = x[tid];
-  else if (tid <= k) out[tid] = -1;  // out[n]: written by the draw below or by the whole-row draw
-  if (tid == 0) {
-    a.out_n[b] = n;
-    a.seq_tickets[b] = 0u;  // left zeroed for the next call
-  }
-  const bool want_q = n < k;
-  const RowPub* const pp = want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
-  const RowStat rp = ldcg_rowstat(&pp[0].rs);
-  const RowStat rq = want_q ? ldcg_rowstat(&pp[1].rs) : rp;
-  const uint32_t nlist = __ldcg(&pp[0].nlist);
-  const bool bad = rp.bad || (want_q && rq.bad);
-  const bool q_known = !want_q || rq.all_kept || rq.tie_cut >= 0;
-  const bool listed = !bad && !rp.all_kept && nlist != kPubReread && rp.tie_cut >= 0 && q_known;
-  if (listed) {
-    const size_t rb = static_cast<size_t>(V) * E::kBytes;
-    const unsigned char* const rowp =
-        static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + n) * rb;
-    const unsigned char* const rowq =
-        want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
-    const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
-    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
-    uint32_t* const idx = reinterpret_cast<uint32_t*>(dsm);
-    float* const ew = reinterpret_cast<float*>(dsm + sizeof(uint32_t) * kPubList);
-    const int token = draw_listed<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, pp[0].list, static_cast<int>(nlist), u,
-                                      idx, ew);
-    if (tid == 0) out[n] = token;
-    clear_sequence(a, b, false);
-  } else if (bad || a.launch_mode == SPEC_LAUNCH_FUSED_WAIT_TEST) {
-    // nothing to draw (a non-finite row: token -1), or, in the wait test, a
-    // draw whose queue entry is withheld so that its waits run out
-    if (tid == 0 && !bad) atomicAdd(a.work + WK_QUEUED, 1u);
-    clear_sequence(a, b, false);
-  } else if (tid == 0) {
-    // queued for the draw over whole rows (the queue counter first, so that a
-    // claimer that sees every sequence finished sees the final count)
-    const uint32_t e = atomicAdd(a.work + WK_QUEUED, 1u);
-    st_release_u32(a.ready + e, static_cast<uint32_t>(b) + 1u);
-  }
-  if (tid == 0) {
-    __threadfence();
-    atomicAdd(a.work + WK_SEQS, 1u);
-  }
-}
+constexpr uint32_t kDrawnInTail = 0x80000000u;  // draw ticket flag: the tail kernel drew the token
 
+// ---------------------------------------------------------- stream kernel
+// One CTA per row: stream it once (lattice masses, maximum, candidate tags),
+// then hand over the row header and the tags at or above klo.
 template <int DT>
-__device__ __noinline__ void process_row(const SampleArgs& a, Shm& sh, unsigned char* dsm, const int item) {
+__device__ __forceinline__ void stream_row(const SampleArgs& a, Shm& sh, uint32_t* dsm, const int cta) {
   using E = Elt<DT>;
-  const RowRef rr = row_ref<DT>(a, item);
+  using H = Hot<DT>;
+  uint32_t* const ltags = dsm;  // lane tags [kWarps][kLaneTags][32]
+  const RowRef rr = row_ref<DT>(a, cta);
   const int role = rr.role, b = rr.b, pos = rr.pos;
   const unsigned char* const row = rr.row;
   const bool aligned = rr.aligned;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = a.V;
   const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
-  const bool bad_t = !(T > 0.f) || isinf(T) || isnan(T);
-  const float c = bad_t ? 1.f : kLog2e / T;
+  const bool bad_t = !(T > 0.f) || isinf(T);
+  const float c = kLog2e / T;
+  const u64 c2 = pkf(c, c);
   const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
-  const bool topk_on = a.top_k > 0, topp_on = a.top_p < 1.f;
-  const bool filt = topk_on || topp_on;
+  const Seg sg = warp_seg(nvec, warp);
+  const bool filt = a.top_k > 0 || a.top_p < 1.f;
+  const int kq = a.k;
   const bool paired = role == ROLE_P || role == ROLE_Q;
-  const int xtok = paired ? a.tokens[static_cast<size_t>(b) * a.k + pos] : -1;
-  const bool xok = xtok >= 0 && xtok < V;
-  if (tid == 0) sh.xbits = xok ? E::bits_at(row, xtok) : 0u;  // (read early: its latency hides behind the stream)
-  const bool hist_on = DT == DT_BF16 && filt && !bad_t;
-  if (hist_on) stream_row<DT, true>(row, V, aligned, c, sh, dsm);
-  else stream_row<DT, false>(row, V, aligned, c, sh, dsm);
+  const int xtok = paired ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
+  // candidate tags: bf16 rows with a cut, segments short enough to index
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
+  const float dtheta = kTheta / c;  // kTheta octaves of mass, in logit units
+  uint32_t* const myl = ltags + warp * kLaneTags * 32 + lane;
 
-  RowStat rs;
-  rs.c = c;
-  rs.K = sh.K;
-  rs.m = E::value(sh.mbits);
-  rs.kmax = E::key(sh.mbits);
-  rs.kstar = 0u;
-  rs.keep = 0;
-  rs.total = 0;
-  rs.tie_cut = V;
-  rs.all_kept = filt ? 0 : 1;
-  DF z = sh.z;
-  double zfull = df_double(z);
-  const bool bad = bad_t || !isfinite(rs.m) || !(fabsf(rs.m * c) < 1073741824.f);
-  rs.bad = bad ? 1 : 0;
-  double zk = zfull;
-  int nlist = 0;
-  bool from_list = false;
-  if (filt && !bad) {
-    bool done = false;
-    if (hist_on && !sh.corrupt && isfinite(zfull) && zfull > 0.0) {
-      done = cut_from_hist<DT>(sh, reinterpret_cast<const uint32_t*>(dsm), rs, a.top_k, a.top_p, zfull, sh.kb, &zk);
-      nlist = sh.nlist;
-      from_list = done && nlist <= kListCap;
+  if (tid == 0) sh.xbits[0] = 0u;
+  __syncthreads();
+
+  // --------------------------------------------------- phase 1: stream
+  float mt = -INFINITY;     // thread maximum
+  int kt = -(1 << 30);      // thread lattice exponent
+  u64 acc0 = 0ull, acc1 = 0ull;  // thread sums of 2^(l c - kt)
+  float mw = -INFINITY;     // CTA maximum of the last exchange
+  uint32_t cnt = 0u;        // lane tag list length
+  uint32_t lfl = 0u;        // lane floor: the lane list is complete above it
+  float lflv = -INFINITY;   // its value
+  float lthr = -3.0e38f;    // lane bound: kTheta octaves below mw, at least the lane floor
+                            // (finite: the -inf padding past a segment is never tagged)
+  int sync_no = 0;
+  // every warp runs the same number of iterations (the CTA barriers below)
+  const int iters_all = seg_vectors(nvec) / 32;
+  // whole 16-byte vectors: every vector below the segment end is full
+  const bool whole = aligned && (V % E::kPerVec) == 0;
+  for (int it = 0; it < iters_all; it += 4) {
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = sg.beg + (it + u) * 32 + lane;
+      x[u] = make_uint4(H::kPad, H::kPad, H::kPad, H::kPad);
+      if (v < sg.end) x[u] = whole ? ldg_stream(row + 16 * static_cast<size_t>(v)) : load_vec<DT>(row, v, V, aligned);
     }
-    if (!done) {
-      if (!(isfinite(zfull) && zfull > 0.0)) zfull = row_pass<DT>(sh, row, V, aligned, PASS_MASS_GT, 0u, rs);
-      const CutOut co = search_cut<DT>(sh, row, V, aligned, a.top_k, a.top_p, rs, zfull);
-      rs.kstar = co.kstar;
-      rs.keep = static_cast<int>(co.keep);
-      rs.total = static_cast<int>(co.total);
-      zk = df_double(co.zkept);
-    }
-    if (rs.keep < rs.total) {
-      rs.tie_cut = from_list ? tie_cut_from_list<DT>(sh, dsm, reinterpret_cast<uint32_t*>(dsm), nlist, rs.kstar,
-                                                      rs.keep, rs.total)
-                             : -1;
-      // rows that searched the whole row find the bound now; rows whose
-      // candidate list overflowed leave it to whoever needs it
-      if (rs.tie_cut < 0 && (!hist_on || !done || role == ROLE_PROBS)) {
-        const int idx = find_nth_equal<DT>(sh, row, V, aligned, 0, nvec, rs.kstar, rs.keep);
-        rs.tie_cut = idx < 0 ? V : idx + 1;
+    // the four vectors' maxima: one lattice-exponent check and one bound
+    // update per four vectors
+    float vmx[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) vmx[u] = H::vmax(x[u]);
+    const float gm = max_nan(max_nan(vmx[0], vmx[1]), max_nan(vmx[2], vmx[3]));
+    {
+      const float L = gm * c;
+      if (L > static_cast<float>(kt) && L < 1073741824.f) {  // raise the lattice exponent (rare)
+        const int knew = static_cast<int>(ceilf(L));
+        const float s = exp2i(kt - knew);
+        acc0 = mul2(acc0, pkf(s, s));
+        acc1 = mul2(acc1, pkf(s, s));
+        kt = knew;
       }
     }
-  } else if (!bad && !(isfinite(zfull) && zfull > 0.0)) {
-    zfull = row_pass<DT>(sh, row, V, aligned, PASS_MASS_GT, 0u, rs);
-    zk = zfull;
+    const float nk = -static_cast<float>(kt);
+    const u64 nk2 = pkf(nk, nk);
+    mt = max_nan(mt, gm);
+    // lane bound lthr: kTheta octaves below the larger of this lane's running
+    // maximum and the CTA maximum of the last exchange (both at most the row
+    // maximum), never below the lane floor
+    lthr = fmaxf(lthr, gm - dtheta);
+    if (use_lists && cnt > static_cast<uint32_t>(kLaneTags - 4)) {
+      // (rare) room for this group's four candidates: drop the tags below the
+      // bound, then while still short of room raise the lane's floor above its
+      // smallest tag; the list stays complete above max(bound, floor)
+      cnt = lane_tags_purge(myl, cnt, E::key(bits_round_down<DT>(lthr)));
+      while (cnt > static_cast<uint32_t>(kLaneTags - 4)) {
+        lfl = lane_tags_min_key(myl, cnt) + 1u;
+        lflv = value_of_key<DT>(lfl);
+        cnt = lane_tags_purge(myl, cnt, lfl);
+      }
+      lthr = fmaxf(lthr, lflv);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = sg.beg + (it + u) * 32 + lane;
+      H::mass_vec(x[u], c2, nk2, acc0, acc1);
+      // a candidate: one predicated store, no branch
+      const bool take = use_lists && vmx[u] >= lthr;
+      if (take) myl[32 * cnt] = (static_cast<uint32_t>(v - sg.beg) << 16) | (__float_as_uint(vmx[u]) >> 16);
+      cnt += take ? 1u : 0u;
+    }
+    const int li = it >> 2;  // loop iteration
+    if (use_lists && (li < kSyncEvery ? (li & (li + 1)) == 0 : (li % kSyncEvery) == kSyncEvery - 1)) {
+      // share the running maxima across the CTA (fixed points, denser at the
+      // start where they rise fastest: deterministic)
+      const int slot = (sync_no++) & 1;
+      const float wm = warp_max_nan(mt);
+      if (lane == 0) sh.x_m[slot][warp][0] = fmaxf(mw, wm);
+      __syncthreads();
+      float mm = mw;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sh.x_m[slot][w][0]);
+      if (mm > mw) {
+        mw = mm;
+        lthr = fmaxf(lthr, mw - dtheta);
+      }
+    }
   }
-  rs.zkept = static_cast<float>(zk);
-  rs.inv_z = static_cast<float>(1.0 / zk);
+
+  // the row's value at the draft token
+  if (tid == 0 && xtok >= 0 && xtok < V) sh.xbits[0] = E::bits_at(row, xtok);
+
+  // ------------------------------------------ phase 2: row maximum and sum
+  {
+    float s0, s1, s2, s3;
+    upk(acc0, s0, s1);
+    upk(acc1, s2, s3);
+    float zt = (s0 + s1) + (s2 + s3);
+    const int kw = warp_max_i32(kt);
+    zt *= exp2i(kt - kw);
+    zt = warp_sum_f32(zt);
+    const float mx = warp_max_nan(mt);
+    const uint32_t fl = warp_max_u32(lfl);
+    if (lane == 0) {
+      sh.w_m[warp][0] = mx;
+      sh.w_k[warp][0] = kw;
+      sh.w_z[warp][0] = zt;
+      sh.w_floor[warp][0] = fl;
+      sh.w_over[warp][0] = 0u;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float mx = -INFINITY;
+    int kk = -(1 << 30);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mx = max_nan(mx, sh.w_m[w][0]);
+      kk = max(kk, sh.w_k[w][0]);
+    }
+    DF z{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) z = df_add(z, sh.w_z[w][0] * exp2i(sh.w_k[w][0] - kk));
+    RowG g;
+    g.m = mx;
+    g.K = static_cast<float>(kk);
+    g.kmax = key_of_float<DT>(mx);
+    g.z = z;
+    g.c0 = 0u;
+    g.m0 = DF{0.f, 0.f};
+    // every vector whose maximum reaches klo is tagged
+    const float tv = mx - dtheta;
+    uint32_t kl = tv > -3.0e38f ? E::key(bits_round_up<DT>(tv)) : 0u;
+    const uint32_t gtop = g.kmax >> 2;
+    if (gtop >= static_cast<uint32_t>(kGroups - 1)) kl = max(kl, 4u * (gtop - static_cast<uint32_t>(kGroups - 1)));
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) kl = max(kl, sh.w_floor[w][0]);
+    g.klo = kl;
+    g.active = use_lists ? 1 : 0;
+    sh.g[0] = g;
+  }
+  __syncthreads();
+  // the lattice exponent must stay an int: |max| log2(e) / T < 2^30
+  const bool bad = bad_t || !isfinite(sh.g[0].m) || !(fabsf(sh.g[0].m * c) < 1073741824.f);
+
+  // ------------- hand over: the row header and its tags at or above klo
+  {
+    const bool lists = use_lists && !bad;
+    const uint32_t kl = sh.g[0].klo;
+    uint32_t mine = 0u;
+    if (lists)
+      for (uint32_t q = 0; q < cnt; ++q) mine += tag_key(myl[32 * q]) >= kl ? 1u : 0u;
+    const uint32_t incl = warp_incl_scan_u32(mine);
+    if (lists) {
+      uint32_t* dst = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
+      uint32_t o = incl - mine;  // (at most kLaneTags * 32 = kTagsPerWarp in all)
+      for (uint32_t q = 0; q < cnt; ++q) {
+        const uint32_t t = myl[32 * q];
+        if (tag_key(t) >= kl) dst[o++] = t;
+      }
+    }
+    if (lane == 31) sh.w_u[warp][0] = lists ? incl : 0u;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const RowG g = sh.g[0];
+    RowHdr h;
+    h.m = g.m;
+    h.K = g.K;
+    h.zhi = g.z.hi;
+    h.zlo = g.z.lo;
+    h.kmax = g.kmax;
+    h.klo = g.klo;
+    h.xbits = sh.xbits[0];
+    h.bad = bad ? 1 : 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) h.ntags[w] = sh.w_u[w][0];
+    a.hdrs[cta] = h;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) stream_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  stream_row<DT>(a, sh, dsm, static_cast<int>(blockIdx.x));
+}
+
+// ------------------------------------------------------------ tail kernel
+// One CTA per row, after the stream kernel: the kept set of the row from its
+// header and tags (or by re-reading the row), published with its probability
+// at the draft token and, for target rows, its kept vectors.  The last row
+// of a sequence to finish applies the first-rejection rule.
+// timed_out: the row's header never arrived (fused kernel): the row is
+// published as bad without reading it.
+template <int DT>
+__device__ __forceinline__ void tail_row(const SampleArgs& a, Shm& sh, uint32_t* dsm, const int cta,
+                                         const bool timed_out) {
+  using E = Elt<DT>;
+  using H = Hot<DT>;
+  // dynamic shared memory: tags [kWarps][kTagsPerWarp] (then the gathered
+  // tags in their place), histogram [kWindow], gather bitmaps
+  // [kWarps][kBmapWords]
+  uint32_t* const ltags = dsm;
+  uint32_t* const hist = ltags + kRowTags;
+  uint32_t* const bmap = hist + kWindow;
+  const RowRef rr = row_ref<DT>(a, cta);
+  const int role = rr.role, b = rr.b, pos = rr.pos;
+  const unsigned char* const row = rr.row;
+  const bool aligned = rr.aligned;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V;
+  const float T = a.temperature_per_seq ? a.temperature_per_seq[b] : a.temperature;
+  const bool bad_t = !(T > 0.f) || isinf(T);
+  const float c = kLog2e / T;
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const Seg sg = warp_seg(nvec, warp);
+  const bool topk_on = a.top_k > 0;
+  const bool topp_on = a.top_p < 1.f;
+  const bool filt = topk_on || topp_on;
+  const int kq = a.k;
+  const bool paired = role == ROLE_P || role == ROLE_Q;
+  const int xtok = paired ? a.tokens[static_cast<size_t>(b) * kq + pos] : -1;
+  const bool use_lists = DT == DT_BF16 && filt && !bad_t && seg_vectors(nvec) <= kBmapWords * 32;
+  // a warp's tags, then its gathered vectors (index order)
+  uint32_t* const wg = ltags + warp * kGather;
+  uint32_t* const wb = bmap + warp * kBmapWords;
+  GList gl;
+  gl.tags = wg;
+  gl.row = row;
+  gl.vc = nullptr;
+  // gathered vectors cached after the first kVecCacheAt words of the warp's region
+  uint4* const vc = reinterpret_cast<uint4*>(wg + kVecCacheAt);
+
+  // The header and the first tags are read together (the tag area beyond a
+  // warp's count holds zeros), so one memory round trip covers most rows.
+  // (read past L1: written by another CTA when the kernels are fused)
+  const RowHdr* const hp = a.hdrs + cta;
+  uint32_t* const src = a.tags + static_cast<size_t>(cta) * kRowTags + warp * kTagsPerWarp;
+  constexpr int kSpec = 8;  // tags per lane read ahead of the count
+  uint32_t t8[kSpec];
+  if (use_lists && !timed_out) {
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) t8[u] = __ldcg(src + 32 * u + lane);
+  }
+  const bool bad = timed_out || __ldcg(&hp->bad) != 0;
+  const uint32_t ntag = use_lists && !bad ? __ldcg(&hp->ntags[warp]) : 0u;
+  if (tid == 0) {
+    RowG g;
+    g.m = timed_out ? 0.f : __ldcg(&hp->m);
+    g.K = timed_out ? 0.f : __ldcg(&hp->K);
+    g.kmax = timed_out ? 0u : __ldcg(&hp->kmax);
+    g.klo = timed_out ? 0u : __ldcg(&hp->klo);
+    g.z = timed_out ? DF{1.f, 0.f} : DF{__ldcg(&hp->zhi), __ldcg(&hp->zlo)};
+    g.c0 = 0u;
+    g.m0 = DF{0.f, 0.f};
+    g.active = use_lists ? 1 : 0;
+    sh.g[0] = g;
+    sh.xbits[0] = timed_out ? 0u : __ldcg(&hp->xbits);
+    // one-warp steps of co-resident CTAs spread over the SM's schedulers
+    // (warp w issues from scheduler w % 4): a hashed warp per row
+    sh.lead = static_cast<int>((static_cast<uint32_t>(cta) * 2654435761u) >> 29);
+  }
+  if (filt)
+    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
+  {  // (the handed-over tags and header are left zeroed for the next call)
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) {
+      const uint32_t i = 32 * u + lane;
+      if (i < ntag) {
+        wg[i] = t8[u];
+        src[i] = 0u;
+      }
+    }
+    for (uint32_t i0 = 32 * kSpec; i0 < ntag; i0 += 32 * 8) {  // the rest, eight loads in flight per lane
+      uint32_t r8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = i0 + 32 * u + lane;
+        r8[u] = i < ntag ? __ldcg(src + i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = i0 + 32 * u + lane;
+        if (i < ntag) {
+          wg[i] = r8[u];
+          src[i] = 0u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < static_cast<int>(sizeof(RowHdr) / 4)) reinterpret_cast<uint32_t*>(a.hdrs + cta)[tid] = 0u;
+
+  // ---------- phase 3: a bound on the cut from the tagged vector maxima
+  // The tags hold every vector whose maximum reaches klo.  Vector maxima
+  // are tokens of the row, so the mass (or count) of the row above a value is
+  // at least that of the maxima above it: where the maxima reach the top-p
+  // target (or top_k), the row's cut lies at or above.
+  int ngat = 0;
+  bool fast = false;
+  if (use_lists && !bad) {
+    {
+      const uint32_t kl = sh.g[0].klo;
+      for (uint32_t i = lane; i < ntag; i += 32) {
+        const uint32_t k = tag_key(wg[i]);
+        if (k >= kl) red_add_shared(smem_addr(hist + hslot(k)), 1u);
+      }
+    }
+    __syncthreads();
+    cut_scan<DT, 1>(sh, hist, c, a.top_k, a.top_p);
+    // bound (top-k: its own cut; top-p alone: the maxima's crossing)
+    const CutOut bo = topk_on ? sh.cutk[0] : sh.cut[0];
+    fast = bo.found != 0;
+    const uint32_t tau = bo.kstar;
+    __syncthreads();
+    for (int t = tid; t < kWindow; t += kThreads) hist[t] = 0u;
+    // the gathered vectors: the warp's tags at or above the bound, marked in
+    // its bitmap and read back in index order (in the tags' place)
+    if (fast) {
+      const int nwords = seg_vectors(nvec) / 32;
+      for (int w2 = lane; w2 < nwords; w2 += 32) wb[w2] = 0u;
+      __syncwarp();
+      for (uint32_t i = lane; i < ntag; i += 32) {
+        const uint32_t t = wg[i];
+        if (tag_key(t) >= tau) atomicOr(&wb[tag_local(t) >> 5], 1u << (tag_local(t) & 31u));
+      }
+      __syncwarp();
+      uint32_t base = 0u;
+      for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w2 = w0 + lane;
+        const uint32_t bits = w2 < nwords ? wb[w2] : 0u;
+        const uint32_t cb = __popc(bits);
+        const uint32_t incl = warp_incl_scan_u32(cb);
+        uint32_t o = base + incl - cb;
+        uint32_t bb = bits;
+        while (bb) {
+          const uint32_t j = __ffs(bb) - 1u;
+          bb &= bb - 1u;
+          if (o < static_cast<uint32_t>(kGather)) wg[o] = tag_make(static_cast<uint32_t>(w2) * 32u + j, 0u);
+          ++o;
+        }
+        base += __shfl_sync(kFull, incl, 31);
+      }
+      ngat = static_cast<int>(min(base, static_cast<uint32_t>(kGather)));
+      if (lane == 0) sh.w_over[warp][0] = base > static_cast<uint32_t>(kGather) ? 1u : 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) fast = fast && sh.w_over[w][0] == 0u;
+    // exact histogram of the gathered elements at or above the bound
+    if (fast) {
+      const uint32_t thr = H::thr_pack(E::bits_of_key(tau));
+      const bool cache = ngat <= kVecCache;
+      for (int i = lane; i < ngat; i += 32) {
+        const int v = sg.beg + static_cast<int>(tag_local(wg[i]));
+        const uint4 x = load_vec<DT>(row, v, V, aligned);
+        if (cache) vc[i] = x;
+        wg[i] = tag_make(tag_local(wg[i]), __float_as_uint(H::vmax(x)) >> 16);  // keep its maximum
+        uint32_t msk = H::mask_ge(x, thr) & vmask<DT>(v, V);
+        while (msk) {
+          const int j = __ffs(msk) - 1;
+          msk &= msk - 1u;
+          red_add_shared(smem_addr(hist + hslot(E::key(E::bits_of(x, j)))), 1u);
+        }
+      }
+    }
+    if (tid == 0) {
+      sh.g[0].klo = tau;
+      sh.g[0].active = fast ? 1 : 0;
+    }
+    __syncthreads();
+    cut_scan<DT, 1>(sh, hist, c, a.top_k, a.top_p);
+    fast = fast && sh.cut[0].found != 0;
+    if (fast && ngat <= kVecCache) gl.vc = vc;
+  }
+
+
+  // ------------------------------------------ phase 4: kept set of the row
+  RowStat rs;
+  {
+    const RowG g = sh.g[0];
+    rs.c = c;
+    rs.K = g.K;
+    rs.m = g.m;
+    rs.kmax = g.kmax;
+    rs.bad = bad ? 1 : 0;
+    rs.all_kept = filt ? 0 : 1;
+    rs.covered = fast ? 1 : 0;
+    rs.kstar = 0u;
+    rs.tie_cut = V;
+    float zk = df_float(g.z);
+    if (filt && !bad) {
+      const CutOut co = fast ? sh.cut[0] : window_cut<DT>(sh, hist, row, V, aligned, a.top_k, a.top_p, rs, df_double(g.z),
+                                                          use_lists ? ltags : nullptr);
+      rs.kstar = co.kstar;
+      zk = df_float(co.zkept);
+      if (co.keep < co.total)
+        rs.tie_cut = fast ? tie_cut_of<DT, true>(sh, gl, static_cast<uint32_t>(ngat), row, V, aligned, co.kstar, co.keep)
+                          : tie_cut_of<DT, false>(sh, gl, 0u, row, V, aligned, co.kstar, co.keep);
+    }
+    rs.zkept = zk;
+    rs.inv_z = 1.f / zk;
+  }
+
 
   if (role == ROLE_PROBS) {
-    float* out = a.out_probs + static_cast<size_t>(item) * V;
+    float* out = a.out_probs + static_cast<size_t>(cta) * V;
     if (bad) {
       for (int t = tid; t < V; t += kThreads) out[t] = 0.f;
       if (tid == 0) set_status(a.status, SPEC_STATUS_BAD_ROW);
@@ -1664,151 +1740,234 @@ __device__ __noinline__ void process_row(const SampleArgs& a, Shm& sh, unsigned 
     return;
   }
 
-  // the probability at the draft token (its rank among ties found by a pass
-  // over the row before it when the bound is not known)
-  bool xkept = false;
-  float xp = 0.f;
-  if (paired && xok && !bad) {
-    const uint32_t xk = E::key(sh.xbits);
-    if (rs.all_kept || xk > rs.kstar) xkept = true;
-    else if (xk == rs.kstar) {
-      if (rs.tie_cut >= 0) xkept = xtok < rs.tie_cut;
-      else xkept = count_equal<DT>(sh, row, V, aligned, 0, xtok / E::kPerVec + 1, rs.kstar, xtok) <
-                   static_cast<uint32_t>(rs.keep);
-    }
-    if (xkept) xp = lat_mass(E::value(sh.xbits), rs.c, rs.K) * rs.inv_z;
-  }
-
   // ------------------------------------------------------------- publish
-  RowPub* const pub = a.pubs + rr.pub;
-  if (role == ROLE_P || role == ROLE_BONUS) {
-    uint32_t nl = kPubReread;
-    if (from_list && !bad && rs.tie_cut >= 0) {
-      const int nkv = kept_vectors<DT>(sh, dsm, nlist, nvec, rs.kstar, pub->list);
-      if (nkv <= kPubList) nl = static_cast<uint32_t>(nkv);
-    }
-    if (tid == 0) pub->nlist = nl;
-  }
+  RowPub* const pub = a.pubs + cta;
   if (tid == 0) {
+    const bool xok = xtok >= 0 && xtok < V;
+    const float xp = (!bad && paired && xok) ? prob_of<DT>(rs, sh.xbits[0], xtok) : 0.f;
     pub->rs = rs;
     pub->xprob = xp;
-    if (role == ROLE_P && a.out_p) a.out_p[static_cast<size_t>(b) * a.k + pos] = xp;
-    if (role == ROLE_Q && a.out_q) a.out_q[static_cast<size_t>(b) * a.k + pos] = xp;
+    if (role == ROLE_P && a.out_p) a.out_p[static_cast<size_t>(b) * kq + pos] = xp;
+    if (role == ROLE_Q && a.out_q) a.out_q[static_cast<size_t>(b) * kq + pos] = xp;
     const uint32_t st = (bad ? SPEC_STATUS_BAD_ROW : 0u) | ((role == ROLE_P && !xok) ? SPEC_STATUS_BAD_TOKEN : 0u);
     if (st) set_status(a.status, st);
   }
+  if (role == ROLE_P || role == ROLE_BONUS) {  // the vectors holding kept tokens, in index order
+    uint32_t mine = 0u, nk = 0u;
+    if (fast) {
+      for (int i0 = 0; i0 < ngat; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t t = i < ngat ? wg[i] : 0u;
+        const bool keep = i < ngat && tag_key(t) >= rs.kstar;
+        const unsigned ball = __ballot_sync(kFull, keep);
+        if (keep) wg[nk + __popc(ball & ((1u << lane) - 1u))] = t;
+        nk += __popc(ball);
+        __syncwarp();
+      }
+      mine = nk;
+    }
+    if (lane == 0) sh.w_u[warp][0] = mine;
+    __syncthreads();
+    uint32_t off = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) off += sh.w_u[w][0];
+      tot += sh.w_u[w][0];
+    }
+    const bool listed = fast && !rs.all_kept && !bad && tot <= static_cast<uint32_t>(kPubList);
+    if (listed)
+      for (uint32_t i = lane; i < mine; i += 32) pub->list[off + i] = static_cast<uint32_t>(sg.beg) + tag_local(wg[i]);
+    if (tid == 0) pub->nlist = listed ? tot : kPubReread;
+  }
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    sh.second = atomicAdd(a.seq_tickets + b, 1u) == static_cast<uint32_t>(2 * a.k) ? 1 : 0;
+    sh.second = atomicAdd(a.seq_tickets + b, 1u) == static_cast<uint32_t>(2 * kq) ? 1 : 0;
   }
   __syncthreads();
-  if (sh.second) finish_sequence<DT>(a, sh, dsm, b);
-}
+  if (!sh.second) return;
 
-// ----------------------------------------------------- whole-row draws
-// Queue entry e (sequence b, first rejection n) is drawn in a.chunks chunks
-// of the rows' vectors, one CTA each: (1) rows whose tie bound is not known
-// count their tokens of value kstar per chunk; (2) each chunk, knowing how
-// many such tokens come before it, sets its own bound and sums its draw
-// weights; the last chunk to finish picks the chunk holding u * S and walks
-// it.
-struct DrawRows {
-  int n;
-  bool want_q, bad, need_p, need_q;
-  RowStat rp, rq;
-  const unsigned char *rowp, *rowq;
-  bool ap, aq;
-};
-template <int DT>
-__device__ __forceinline__ DrawRows draw_rows(const SampleArgs& a, int b) {
-  using E = Elt<DT>;
-  DrawRows d;
-  const int k = a.k;
-  d.n = min(max(__ldcg(a.out_n + b), 0), k);
-  d.want_q = d.n < k;
-  const RowPub* const pp =
-      d.want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + d.n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
-  d.rp = ldcg_rowstat(&pp[0].rs);
-  d.rq = d.want_q ? ldcg_rowstat(&pp[1].rs) : d.rp;
-  d.bad = d.rp.bad || (d.want_q && d.rq.bad);
-  d.need_p = !d.rp.all_kept && d.rp.tie_cut < 0;
-  d.need_q = d.want_q && !d.rq.all_kept && d.rq.tie_cut < 0;
-  const size_t rb = static_cast<size_t>(a.V) * E::kBytes;
-  d.rowp = static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + d.n) * rb;
-  d.rowq = d.want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + d.n) * rb : d.rowp;
-  d.ap = a.aligned_target != 0;
-  d.aq = d.want_q ? a.aligned_draft != 0 : d.ap;
-  return d;
-}
-__device__ __forceinline__ int chunk_beg(int nvec, int S, int cc) {
-  return static_cast<int>(static_cast<long long>(nvec) * cc / S);
-}
-
-// Stage 1: tokens of value kstar in chunk s (rows whose bound is unknown).
-template <int DT>
-__device__ __noinline__ void draw_count(const SampleArgs& a, Shm& sh, int b, int s) {
-  using E = Elt<DT>;
-  const DrawRows d = draw_rows<DT>(a, b);
-  if (d.bad || !(d.need_p || d.need_q)) return;
-  const int nvec = (a.V + E::kPerVec - 1) / E::kPerVec, S = a.chunks;
-  const int e0 = chunk_beg(nvec, S, s), e1 = chunk_beg(nvec, S, s + 1);
-  const uint32_t cp = d.need_p ? count_equal<DT>(sh, d.rowp, a.V, d.ap, e0, e1, d.rp.kstar, a.V) : 0u;
-  const uint32_t cq = d.need_q ? count_equal<DT>(sh, d.rowq, a.V, d.aq, e0, e1, d.rq.kstar, a.V) : 0u;
-  if (threadIdx.x == 0) {
-    int32_t* t = a.tcnt + (static_cast<size_t>(b) * kMaxDrawChunks + s) * 2;
-    t[0] = static_cast<int32_t>(cp);
-    t[1] = static_cast<int32_t>(cq);
-    __threadfence();
-    atomicAdd(a.tie_tickets + b, 1u);
-  }
-}
-template <int DT>
-__device__ __forceinline__ bool draw_needs_counts(const SampleArgs& a, int b) {
-  const DrawRows d = draw_rows<DT>(a, b);
-  return !d.bad && (d.need_p || d.need_q);
-}
-
-// The bound of one row's tie inside chunk s, from the per-chunk counts.
-template <int DT>
-__device__ __forceinline__ int chunk_tie_cut(const SampleArgs& a, Shm& sh, int b, int s, int which, const RowStat& r,
-                                             const unsigned char* row, bool al, int e0, int e1) {
-  int before = 0;
-  for (int cc = 0; cc < s; ++cc) before += __ldcg(a.tcnt + (static_cast<size_t>(b) * kMaxDrawChunks + cc) * 2 + which);
-  const int mine = __ldcg(a.tcnt + (static_cast<size_t>(b) * kMaxDrawChunks + s) * 2 + which);
-  if (before + mine <= r.keep) return 0x7FFFFFFF;  // every such token of this chunk is kept
-  if (before >= r.keep) return 0;                  // none is
-  const int idx = find_nth_equal<DT>(sh, row, a.V, al, e0, e1, r.kstar, r.keep - before);
-  return idx < 0 ? 0 : idx + 1;
-}
-
-// Stage 2 of chunk s; the last chunk picks and walks.  e: the queue entry.
-template <int DT>
-__device__ __noinline__ void draw_sum(const SampleArgs& a, Shm& sh, int b, int s, int e) {
-  using E = Elt<DT>;
-  const int tid = threadIdx.x, S = a.chunks, k = a.k;
-  DrawRows d = draw_rows<DT>(a, b);
-  const int nvec = (a.V + E::kPerVec - 1) / E::kPerVec;
-  const int e0 = chunk_beg(nvec, S, s), e1 = chunk_beg(nvec, S, s + 1);
-  const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (d.want_q ? k + 1 : k)];
-  RowStat rp = d.rp, rq = d.rq;
-  if (!d.bad) {
-    __threadfence();
-    if (d.need_p) rp.tie_cut = chunk_tie_cut<DT>(a, sh, b, s, 0, d.rp, d.rowp, d.ap, e0, e1);
-    if (d.need_q) rq.tie_cut = chunk_tie_cut<DT>(a, sh, b, s, 1, d.rq, d.rowq, d.aq, e0, e1);
-    if (tid == 0) {
-      int32_t* t = a.tcut + (static_cast<size_t>(b) * kMaxDrawChunks + s) * 2;
-      t[0] = rp.tie_cut;
-      t[1] = rq.tie_cut;
+  // ------------- the last row of sequence b: the first-rejection rule
+  // (every position tested by its own thread, so the reads overlap)
+  __threadfence();
+  {
+    const int k = kq;
+    const int32_t* x = a.tokens + static_cast<size_t>(b) * k;
+    int rej = k;  // this thread's position if it is rejected
+    if (tid < k) {
+      const RowPub* pp = a.pubs + 2 * (static_cast<size_t>(b) * k + tid);
+      const float px = __ldcg(&pp[0].xprob), qx = __ldcg(&pp[1].xprob);
+      const int bp = __ldcg(&pp[0].rs.bad), bq = __ldcg(&pp[1].rs.bad);
+      const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + tid];
+      const bool xok = x[tid] >= 0 && x[tid] < V;
+      const bool acc = !bp && !bq && xok && u * qx < px;
+      if (!acc) rej = tid;
     }
-    range_sums<DT>(sh, rp, rq, d.rowp, d.rowq, d.ap, d.aq, a.V, d.want_q, nullptr, e0, e1);
-  } else {
-    if (tid < kWarps) {
-      sh.w_s[tid] = 0.f;
-      sh.w_sp[tid] = 0.f;
+    // k <= 31: the first warp holds every position
+    if (warp == 0) {
+      const unsigned rb = __ballot_sync(kFull, rej < k);
+      if (lane == 0) sh.draw_chunk = rb ? __ffs(rb) - 1 : k;
     }
     __syncthreads();
+    const int n = sh.draw_chunk;
+    int32_t* out = a.out_tokens + static_cast<size_t>(b) * (k + 1);
+    if (tid < n) out[tid] = x[tid];
+    else if (tid > n && tid <= k) out[tid] = -1;  // out[n]: drawn below, or by the draw kernel
+    if (tid == 0) {
+      a.out_n[b] = n;
+      a.seq_tickets[b] = 0u;  // left zeroed for the next call
+    }
   }
+
+  // ------- the draw at n, here when the target row's kept vectors are listed
+  {
+    const int k = kq, n = sh.draw_chunk;
+    const bool want_q = n < k;
+    const RowPub* const pp = want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
+    const RowStat rp = ldcg_rowstat(&pp[0].rs);
+    const RowStat rq = want_q ? ldcg_rowstat(&pp[1].rs) : rp;
+    const uint32_t nlist = __ldcg(&pp[0].nlist);
+    const bool listed = !rp.bad && !(want_q && rq.bad) && nlist != kPubReread && !rp.all_kept;
+    if (!listed) return;  // the draw kernel draws over the whole rows
+    const size_t rb = static_cast<size_t>(V) * E::kBytes;
+    const unsigned char* const rowp =
+        static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + n) * rb;
+    const unsigned char* const rowq =
+        want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
+    const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
+    const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
+    uint32_t* const idx = ltags;  // (the tags region is free now)
+    float* const ew = reinterpret_cast<float*>(ltags + kPubList);
+    uint32_t* const nls = ltags + 3 * kPubList;
+    if (tid < 2 * k + 1)
+      nls[tid] = __ldcg(&(tid < 2 * k ? a.pubs + 2 * static_cast<size_t>(b) * k + tid
+                                        : a.pubs + 2 * static_cast<size_t>(a.B) * k + b)->nlist);
+    const int token = draw_listed<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, pp[0].list, static_cast<int>(nlist), u,
+                                      idx, ew);
+    if (tid == 0) {
+      a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
+      a.draw_tickets[b] = kDrawnInTail;
+    }
+    clear_sequence_pubs(a, b, nls);
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) tail_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  tail_row<DT>(a, sh, dsm, static_cast<int>(blockIdx.x), false);
+}
+
+// ----------------------------------------------------- fused stream + tail
+// One cooperative launch of as many CTAs as fit on the GPU at once, taking
+// work items in order from a counter: the stream part of every row, then the
+// tail part of every row.  A tail item waits for its row's stream item,
+// which a running CTA took earlier and finishes without waiting on anyone;
+// the tails of the first rows thus run beside the streams of the last ones,
+// and no CTA slot idles between the two.  (Interleaving the two kinds
+// earlier measured slower.)  The wait is bounded (about kMaxPolls polls):
+// past it the row is published as bad and SPEC_STATUS_TIMEOUT is set.
+constexpr int kMaxPolls = 1 << 22;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) {
+  __shared__ Shm sh;
+  __shared__ int s_item, s_ok;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  const int R = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
+  const int tid = threadIdx.x;
+  for (;;) {
+    __syncthreads();  // the previous item is done with shared memory
+    if (tid == 0) s_item = static_cast<int>(atomicAdd(a.work, 1u));
+    __syncthreads();
+    const int item = s_item;
+    if (item >= 2 * R) break;
+    // item -> (stream or tail, row)
+    const int kind = item < R ? 0 : 1;
+    const int rowi = item < R ? item : item - R;
+    if (kind == 0) {
+      const int item_row = rowi;
+      stream_row<DT>(a, sh, dsm, item_row);
+      __syncthreads();
+      if (tid == 0 && a.launch_mode != SPEC_LAUNCH_FUSED_WAIT_TEST) {
+        __threadfence();
+        st_release_u32(a.done + item_row, 1u);
+      }
+    } else {
+      const int r = rowi;
+      if (tid == 0) {
+        int ok = 0;
+        for (int i = 0; i < a.poll_limit; ++i) {
+          if (ld_acquire_u32(a.done + r)) {
+            ok = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!ok) set_status(a.status, SPEC_STATUS_TIMEOUT);
+        a.done[r] = 0u;  // left zeroed for the next call
+        s_ok = ok;
+      }
+      __syncthreads();
+      tail_row<DT>(a, sh, dsm, r, s_ok == 0);
+    }
+  }
+  // the last CTA out leaves the counters zeroed for the next call
+  if (tid == 0 && atomicAdd(a.work + 1, 1u) == gridDim.x - 1) {
+    a.work[0] = 0u;
+    a.work[1] = 0u;
+  }
+}
+
+// ------------------------------------------------------------ draw kernel
+// After the tail kernel: sequence b's token at its first rejection n when the
+// tail kernel could not draw it from listed vectors (no filter, a row the
+// candidates did not decide, a non-finite row): drawn from max(0, p_n - q_n)
+// with u_{k+1} (n < k) or from p_k with u_k (n = k), falling back to p_n
+// when the residual has no mass.  a.chunks CTAs each sum one chunk of the
+// whole rows; the last of them picks the chunk holding u * S from the chunk
+// sums in order and walks it.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) draw_kernel(const SampleArgs a) {
+  using E = Elt<DT>;
+  __shared__ Shm sh;
+  const int S = a.chunks;
+  const int b = static_cast<int>(blockIdx.x) / S, s = static_cast<int>(blockIdx.x) % S;
+  const int k = a.k, V = a.V, tid = threadIdx.x;
+  if (__ldcg(a.draw_tickets + b) & kDrawnInTail) {  // drawn in the tail kernel: the last CTA resets the flag
+    if (tid == 0) {
+      const uint32_t old = atomicAdd(a.draw_tickets + b, 1u);
+      if ((old & ~kDrawnInTail) == static_cast<uint32_t>(S - 1)) a.draw_tickets[b] = 0u;
+    }
+    return;
+  }
+  const int nvec = (V + E::kPerVec - 1) / E::kPerVec;
+  const int n = min(max(a.out_n[b], 0), k);  // (written by the tail kernel; kept in range regardless)
+  const bool want_q = n < k;
+  const RowPub* const pp = want_q ? a.pubs + 2 * (static_cast<size_t>(b) * k + n) : a.pubs + 2 * static_cast<size_t>(a.B) * k + b;
+  const RowStat rp = pp[0].rs;
+  const RowStat rq = want_q ? pp[1].rs : rp;
+  const size_t rb = static_cast<size_t>(V) * E::kBytes;
+  const unsigned char* const rowp = static_cast<const unsigned char*>(a.target) + (static_cast<size_t>(b) * (k + 1) + n) * rb;
+  const unsigned char* const rowq =
+      want_q ? static_cast<const unsigned char*>(a.draft) + (static_cast<size_t>(b) * k + n) * rb : rowp;
+  const bool ap = a.aligned_target != 0, aq = want_q ? a.aligned_draft != 0 : ap;
+  const bool bad = rp.bad || (want_q && rq.bad);
+  const float u = a.uniforms[static_cast<size_t>(b) * (k + 2) + (want_q ? k + 1 : k)];
+  const int N = bad ? 0 : nvec;
+  auto chunk_beg = [&](int cc) { return static_cast<int>(static_cast<long long>(N) * cc / S); };
+
+  range_sums<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, want_q, nullptr, chunk_beg(s), chunk_beg(s + 1));
   if (tid == 0) {
     DF sr{0.f, 0.f}, spp{0.f, 0.f};
 #pragma unroll
@@ -1822,7 +1981,7 @@ __device__ __noinline__ void draw_sum(const SampleArgs& a, Shm& sh, int b, int s
     cs[2] = spp.hi;
     cs[3] = spp.lo;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kWarps; ++w) {  // kept for the walk of the chosen chunk
       cs[4 + w] = sh.w_s[w];
       cs[4 + kWarps + w] = sh.w_sp[w];
     }
@@ -1832,7 +1991,7 @@ __device__ __noinline__ void draw_sum(const SampleArgs& a, Shm& sh, int b, int s
   __syncthreads();
   if (!sh.second) return;
 
-  // ---------------------------------------- the last chunk: pick one, walk it
+  // ------------------------ the last chunk of sequence b: pick one, walk it
   __shared__ float s_cs[kMaxDrawChunks * 4];
   __threadfence();
   if (tid < 4 * S) s_cs[tid] = __ldcg(a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + tid / 4) * kChunkRec + tid % 4);
@@ -1844,29 +2003,20 @@ __device__ __noinline__ void draw_sum(const SampleArgs& a, Shm& sh, int b, int s
       tr = df_add2(tr, DF{cs[4 * cc], cs[4 * cc + 1]});
       tp = df_add2(tp, DF{cs[4 * cc + 2], cs[4 * cc + 3]});
     }
-    const bool use_q = d.want_q && tr.hi > 0.f;  // a residual with no mass: draw from p
+    const bool use_q = want_q && tr.hi > 0.f;  // a residual with no mass: draw from p
     const DF target = df_mul_f(use_q ? tr : tp, u);
     DF run{0.f, 0.f}, base{0.f, 0.f}, lbase{0.f, 0.f};
     int csel = -1, clast = -1;
     const int o = use_q ? 0 : 2;
     for (int cc = 0; cc < S; ++cc) {
       const DF sc{cs[4 * cc + o], cs[4 * cc + o + 1]};
-      const DF nx = df_add2(run, sc);
-      if (sc.hi > 0.f) {
-        clast = cc;
-        lbase = run;
-      }
-      if (csel < 0 && sc.hi > 0.f && df_lt(target, nx)) {
-        csel = cc;
-        base = run;
-      }
-      run = nx;
+      const DF nxt = df_add2(run, sc);
+      if (sc.hi > 0.f) { clast = cc; lbase = run; }
+      if (csel < 0 && sc.hi > 0.f && df_lt(target, nxt)) { csel = cc; base = run; }
+      run = nxt;
     }
-    if (csel < 0) {
-      csel = clast;
-      base = lbase;
-    }
-    sh.draw_chunk = d.bad ? -1 : csel;
+    if (csel < 0) { csel = clast; base = lbase; }
+    sh.draw_chunk = bad ? -1 : csel;
     sh.draw_useq = use_q ? 1 : 0;
     sh.draw_target = df_add2(target, df_neg(base));
   }
@@ -1875,155 +2025,29 @@ __device__ __noinline__ void draw_sum(const SampleArgs& a, Shm& sh, int b, int s
   int token = -1;
   if (cs >= 0) {
     const bool use_q = sh.draw_useq != 0;
-    if (tid < 2 * kWarps) {
+    // the chosen chunk's per-warp sums, as its CTA recorded them
+    if (cs != s && tid < 2 * kWarps) {
       const float v = __ldcg(a.csums + (static_cast<size_t>(b) * kMaxDrawChunks + cs) * kChunkRec + 4 + tid);
       if (tid < kWarps) sh.w_s[tid] = v;
       else sh.w_sp[tid - kWarps] = v;
     }
-    RowStat wp = d.rp, wq = d.rq;
-    if (d.need_p) wp.tie_cut = __ldcg(a.tcut + (static_cast<size_t>(b) * kMaxDrawChunks + cs) * 2);
-    if (d.need_q) wq.tie_cut = __ldcg(a.tcut + (static_cast<size_t>(b) * kMaxDrawChunks + cs) * 2 + 1);
     __syncthreads();
-    token = range_walk<DT>(sh, wp, wq, d.rowp, d.rowq, d.ap, d.aq, a.V, use_q, sh.draw_target, nullptr,
-                           chunk_beg(nvec, S, cs), chunk_beg(nvec, S, cs + 1));
+    token = range_walk<DT>(sh, rp, rq, rowp, rowq, ap, aq, V, use_q, sh.draw_target, nullptr, chunk_beg(cs),
+                           chunk_beg(cs + 1));
   }
-  if (tid == 0) {
-    a.out_tokens[static_cast<size_t>(b) * (k + 1) + d.n] = token;
-    // left zeroed for the next call
-    a.draw_tickets[b] = 0u;
-    a.tie_tickets[b] = 0u;
-    a.ready[e] = 0u;
-  }
-  clear_sequence(a, b, true);
-}
-
-}  // namespace
-
-// ------------------------------------------------------------------ kernels
-// One row per CTA (the separate-launch mode).
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) rows_kernel(const SampleArgs a) {
-  __shared__ Shm sh;
-  extern __shared__ __align__(16) unsigned char dsm[];
-  process_row<DT>(a, sh, dsm, static_cast<int>(blockIdx.x));
-}
-// Whole-row draws, separate-launch mode: counts, then sums and walks.
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) draw1_kernel(const SampleArgs a) {
-  __shared__ Shm sh;
-  const int e = static_cast<int>(blockIdx.x) / a.chunks, s = static_cast<int>(blockIdx.x) % a.chunks;
-  if (e >= static_cast<int>(__ldcg(a.work + WK_QUEUED))) return;
-  const int b = static_cast<int>(__ldcg(a.ready + e)) - 1;
-  if (b < 0) return;
-  draw_count<DT>(a, sh, b, s);
-}
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) draw2_kernel(const SampleArgs a) {
-  __shared__ Shm sh;
-  const int e = static_cast<int>(blockIdx.x) / a.chunks, s = static_cast<int>(blockIdx.x) % a.chunks;
-  if (e < static_cast<int>(__ldcg(a.work + WK_QUEUED))) {
-    const int b = static_cast<int>(__ldcg(a.ready + e)) - 1;
-    if (b >= 0) draw_sum<DT>(a, sh, b, s, e);
-  }
-  // the last CTA out leaves the counters zeroed for the next call
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(a.work + WK_EXIT, 1u) == gridDim.x - 1) {
-    a.work[WK_QUEUED] = 0u;
-    a.work[WK_SEQS] = 0u;
-    a.work[WK_EXIT] = 0u;
-  }
-}
-// Separate-launch mode of spec_transform_probs and of sampling calls with
-// no whole-row draw to run: the counters the finishers bump are reset here.
-__global__ void reset_kernel(uint32_t* work) {
-  if (threadIdx.x < 8) work[threadIdx.x] = 0u;
-}
-
-// One cooperative launch of as many CTAs as fit on the GPU, taking work items
-// in order from counters: every row, then the whole-row draw chunks.  A draw
-// chunk waits (bounded polls) for its queue entry and, when ties must be
-// counted, for the other chunks of its entry to count theirs; the awaited
-// work was taken earlier by running CTAs and waits on nothing it could block,
-// so every wait ends.  Past the poll limit the wait gives up and sets
-// SPEC_STATUS_TIMEOUT (that token stays -1).
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) fused_kernel(const SampleArgs a) {
-  __shared__ Shm sh;
-  extern __shared__ __align__(16) unsigned char dsm[];
-  const int R = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
-  const int tid = threadIdx.x;
-  for (;;) {
-    __syncthreads();
-    if (tid == 0) sh.item = static_cast<int>(atomicAdd(a.work + WK_ROWS, 1u));
-    __syncthreads();
-    const int item = sh.item;
-    if (item >= R) break;
-    process_row<DT>(a, sh, dsm, item);
-  }
-  if (a.mode == MODE_SAMPLE) {
-    const int S = a.chunks;
-    for (;;) {
-      __syncthreads();
-      if (tid == 0) {
-        const int d = static_cast<int>(atomicAdd(a.work + WK_DRAWS, 1u));
-        const int e = d / S;
-        int bb = -2;  // -2: no more queued draws; -1: the wait gave up
-        if (e < a.B) {
-          bb = -1;
-          for (int i = 0; i < a.poll_limit; ++i) {
-            const uint32_t v = ld_acquire_u32(a.ready + e);
-            if (v) {
-              bb = static_cast<int>(v) - 1;
-              break;
-            }
-            if (ld_acquire_u32(a.work + WK_SEQS) == static_cast<uint32_t>(a.B) &&
-                ld_acquire_u32(a.work + WK_QUEUED) <= static_cast<uint32_t>(e)) {
-              bb = -2;
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (bb == -1) set_status(a.status, SPEC_STATUS_TIMEOUT);
-        }
-        sh.item = d;
-        sh.flag = bb;
-      }
-      __syncthreads();
-      const int bb = sh.flag;
-      if (bb == -2) break;
-      if (bb < 0) continue;
-      const int e = sh.item / S, s = sh.item % S;
-      if (draw_needs_counts<DT>(a, bb)) {
-        draw_count<DT>(a, sh, bb, s);
-        if (tid == 0) {
-          int ok = 0;
-          for (int i = 0; i < a.poll_limit; ++i) {
-            if (ld_acquire_u32(a.tie_tickets + bb) >= static_cast<uint32_t>(S)) {
-              ok = 1;
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (!ok) set_status(a.status, SPEC_STATUS_TIMEOUT);
-          sh.flag = ok;
-        }
-        __syncthreads();
-        if (!sh.flag) continue;
-      }
-      draw_sum<DT>(a, sh, bb, s, e);
-    }
-  }
-  // the last CTA out leaves the counters zeroed for the next call
-  __syncthreads();
-  if (tid == 0 && atomicAdd(a.work + WK_EXIT, 1u) == gridDim.x - 1) {
-    for (int i = 0; i < 8; ++i) a.work[i] = 0u;
-  }
+  if (tid == 0) a.out_tokens[static_cast<size_t>(b) * (k + 1) + n] = token;
+  // leave the workspace zeroed for the next call, whatever its shape
+  for (int i = tid; i < kChunkRec * S; i += kThreads) a.csums[static_cast<size_t>(b) * kMaxDrawChunks * kChunkRec + i] = 0.f;
+  if (tid == 0) a.draw_tickets[b] = 0u;
+  clear_sequence_pubs(a, b, nullptr);
 }
 
 // ------------------------------------------------------------------ launch
 
+size_t stream_smem_bytes(bool filter) { return filter ? kWarps * kLaneTags * 32 * sizeof(uint32_t) : 16; }
 size_t sample_smem_bytes(int dtype, bool filter) {
-  return (dtype == DT_BF16 && filter) ? kRowSmem : sizeof(uint32_t) * 3 * kPubList;
+  (void)dtype;
+  return filter ? (kRowTags + kWindow + kWarps * kBmapWords) * sizeof(uint32_t) : 16;
 }
 
 template <int DT>
@@ -2032,34 +2056,29 @@ static int launch_all(const SampleArgs& args, cudaStream_t st) {
   a.poll_limit = a.launch_mode == SPEC_LAUNCH_FUSED_WAIT_TEST ? 64 : kMaxPolls;
   const bool filter = a.top_k > 0 || a.top_p < 1.f;
   const int rows = a.mode == MODE_SAMPLE ? a.B * (2 * a.k + 1) : a.B;
-  const size_t smem = sample_smem_bytes(DT, filter);
+  const size_t s1 = stream_smem_bytes(filter), s2 = sample_smem_bytes(DT, filter);
+  static_assert(kRowTags * 4 + (kWindow + kWarps * kBmapWords) * 4 <= 48 * 1024, "tail kernel shared memory");
+  // stream and tail fused in one cooperative launch when the GPU allows it
   bool fused = false;
   if (a.launch_mode != SPEC_LAUNCH_SEPARATE) {
+    const size_t sf = s1 > s2 ? s1 : s2;
     int per_sm = 0, dev = 0, coop = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
-        cudaFuncSetAttribute(fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
-            cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<DT>, kThreads, smem) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<DT>, kThreads, sf) == cudaSuccess &&
         per_sm > 0) {
-      const int items = rows + (a.mode == MODE_SAMPLE ? a.B * a.chunks : 0);
-      const int grid = std::min(per_sm * num_sms(), items);
+      const int grid = std::min(per_sm * num_sms(), 2 * rows);
       void* params[] = {&a};
       fused = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_kernel<DT>), dim3(grid), dim3(kThreads),
-                                          params, smem, st) == cudaSuccess;
+                                          params, sf, st) == cudaSuccess;
     }
-    if (!fused) (void)cudaGetLastError();  // (clear a refused launch; the separate launches stand in)
+    if (!fused) (void)cudaGetLastError();  // (clear a refused launch; the two launches below stand in)
   }
   if (!fused) {
-    cudaFuncSetAttribute(rows_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    rows_kernel<DT><<<rows, kThreads, smem, st>>>(a);
-    if (a.mode == MODE_SAMPLE) {
-      draw1_kernel<DT><<<a.B * a.chunks, kThreads, 0, st>>>(a);
-      draw2_kernel<DT><<<a.B * a.chunks, kThreads, 0, st>>>(a);
-    } else {
-      reset_kernel<<<1, 32, 0, st>>>(a.work);
-    }
+    stream_kernel<DT><<<rows, kThreads, s1, st>>>(a);
+    tail_kernel<DT><<<rows, kThreads, s2, st>>>(a);
   }
+  if (a.mode == MODE_SAMPLE) draw_kernel<DT><<<a.B * a.chunks, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

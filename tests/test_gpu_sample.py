@@ -249,31 +249,25 @@ def test_fused_and_separate_launches_agree(label):
         assert np.array_equal(x, y)
 
 
-# Failure detection without a fault: in the fused launch, a draw over whole
-# rows (here every sequence's: no filter) waits, with a bounded poll, for its
-# sequence to be queued.  With the queue entries withheld every such wait
-# runs out: the call still ends with the accepted prefixes and counts
-# committed, the drawn tokens left at -1 and SPEC_STATUS_TIMEOUT set, and the
-# next call on the same workspace and context is correct.
+# Failure detection without a fault: with the stream parts' completion flags
+# withheld, every tail part's bounded wait runs out; the call still ends,
+# publishes every row as non-finite and sets SPEC_STATUS_TIMEOUT, and the next
+# call on the same workspace and context is correct.
 def test_fused_wait_runs_out_and_context_stays_usable():
     sv = lib()
-    case = W.random_sample_case(6, 3, 5000, seed=24, top_p=1.0)
+    case = W.random_sample_case(6, 3, 5000, seed=24, top_p=0.9)
     ws = sv.Workspace()
     sv.spec_get_status(ws)
     good = run_sample_gpu(case, workspace=ws)
     assert sv.spec_get_status(ws) == 0
     prev = sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_FUSED_WAIT_TEST)
     try:
-        tok, n, p, q = run_sample_gpu(case, workspace=ws)
+        tok, n, _, _ = run_sample_gpu(case, workspace=ws)
     finally:
         sv.spec_sample_launch_mode(prev)
     st = sv.spec_get_status(ws)
-    assert st & sv.SPEC_STATUS_TIMEOUT
-    assert np.array_equal(n, good[1])
-    for b in range(case.B):
-        nb = int(n[b])
-        assert np.array_equal(tok[b, :nb], good[0][b, :nb]) and np.all(tok[b, nb:] == -1)
-    assert np.array_equal(p, good[2]) and np.array_equal(q, good[3])
+    assert st & sv.SPEC_STATUS_TIMEOUT and st & sv.SPEC_STATUS_BAD_ROW
+    assert np.all(n == 0) and np.all(tok == -1)
     again = run_sample_gpu(case, workspace=ws)
     assert sv.spec_get_status(ws) == 0
     for x, y in zip(good, again):
