@@ -46,12 +46,20 @@ MUTATIONS = [
      "        (void)accepted;\n        continue;"),
     ("tree siblings tried from the last", "for (j = v + 1; j < N && n_test > 0; ++j) {",
      "for (j = N - 1; j > v && n_test > 0; --j) {"),
+    ("boundary flags 10x wider", "#define BOUNDARY_EPS 1e-6", "#define BOUNDARY_EPS 1e-5"),
+    ("boundary flags 10x narrower", "#define BOUNDARY_EPS 1e-6", "#define BOUNDARY_EPS 1e-7"),
+    ("top-p cut re-scan skipped", "if (differs) o.flags |= OFLAG_CUT_BOUNDARY;", "(void)differs;"),
+    ("top-p cut flagged whether or not it matters", "if (differs) o.flags |= OFLAG_CUT_BOUNDARY;",
+     "o.flags |= OFLAG_CUT_BOUNDARY;"),
+    ("accept flag tested on q/p", "double mg = fabs((double)u[i] - px / qx);", "double mg = fabs((double)u[i] - qx / px);"),
+    ("draw flag measured against the far edge only", "if (margin) *margin = (a < b ? a : b) / s;",
+     "if (margin) *margin = b / s;"),
     ("tree degenerate residual not put back to p",
      "flags |= OFLAG_DEGENERATE;\n          for (t = 0; t < V; ++t) r[t] = p[t];",
      "flags |= OFLAG_DEGENERATE;"),
 ]
 
-PIN_FILES = ("test_oracle_pins.py", "test_oracle_tree_sample.py")
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_tree_sample.py", "test_oracle_boundary_pins.py")
 
 
 def _run_mutated(tmp_root, src, idx, name, old, new):
