@@ -41,6 +41,7 @@ SPEC_STATUS_BAD_ROW = 2
 SPEC_STATUS_BAD_PARENT = 4
 SPEC_STATUS_DEPTH = 8
 SPEC_STATUS_TIMEOUT = 16
+SPEC_STATUS_BAD_KV = 32
 
 SPEC_MAX_K = 31
 SPEC_MAX_TREE_NODES = 1024
@@ -125,6 +126,8 @@ def lib() -> ctypes.CDLL:
             L.spec_best_gamma.argtypes = [D, D, I, ctypes.POINTER(D)]
             L.spec_best_gamma.restype = I
             L.spec_first_draft_check.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
+            L.spec_kv_compact.argtypes = [P, I, P, P, P, I, I, I, I, P, P, P, P, P, P]
+            L.spec_kv_compact.restype = I
             L.spec_first_draft_check.restype = I
             _lib = L
     return _lib
@@ -378,6 +381,35 @@ def spec_verify_tree_sample(node_logits: torch.Tensor, draft_logits: torch.Tenso
     )
     _check(rc, "spec_verify_tree_sample")
     return out_tokens, out_path, out_num_accepted
+
+
+def spec_kv_compact(num_accepted: torch.Tensor, kv_base: torch.Tensor, path: Optional[torch.Tensor] = None,
+                    block_table: Optional[torch.Tensor] = None, block_size: int = 0, max_keep: Optional[int] = None,
+                    out_status: Optional[torch.Tensor] = None, stream=None):
+    """KV-cache keep list after verification: (src [B][max_keep], dst [B][max_keep],
+    new_len [B], num_moves [B]) slots of the kept entries before and after the
+    cut.  path [B][S] (tree out_path) or None for a chain; block_table [B][M]
+    maps logical blocks of block_size entries to physical ones, or None."""
+    B = num_accepted.shape[0]
+    dev = num_accepted.device
+    if max_keep is None:
+        max_keep = (path.shape[1] + 1) if path is not None else None
+        if max_keep is None:
+            raise ValueError("max_keep is required for a chain (k + 1)")
+    src = torch.empty((B, max_keep), dtype=torch.int32, device=dev)
+    dst = torch.empty((B, max_keep), dtype=torch.int32, device=dev)
+    new_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    moves = torch.empty((B,), dtype=torch.int32, device=dev)
+    rc = lib().spec_kv_compact(
+        _dev(path, "path", torch.int32), path.shape[1] if path is not None else 0,
+        _dev(num_accepted, "num_accepted", torch.int32), _dev(kv_base, "kv_base", torch.int32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1] if block_table is not None else 0,
+        block_size, B, max_keep, _dev(src, "out_src"), _dev(dst, "out_dst"), _dev(new_len, "out_new_len"),
+        _dev(moves, "out_num_moves"), _dev(out_status, "out_status", torch.int32) if out_status is not None else None,
+        _stream(stream),
+    )
+    _check(rc, "spec_kv_compact")
+    return src, dst, new_len, moves
 
 
 def spec_transform_probs(logits: torch.Tensor, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,

@@ -185,6 +185,37 @@ int spec_sample_launch_mode(int mode) {
   return g_launch_mode.exchange(mode);
 }
 
+int spec_kv_compact(const int32_t* path, int path_stride, const int32_t* num_accepted, const int32_t* kv_base,
+                    const int32_t* block_table, int max_blocks, int block_size, int B, int max_keep,
+                    int32_t* out_src, int32_t* out_dst, int32_t* out_new_len, int32_t* out_num_moves,
+                    uint32_t* out_status, void* cuda_stream) {
+  if (!num_accepted || !kv_base || !out_src || !out_dst || !out_new_len) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || max_keep < 1) return SPEC_ERR_INVALID_ARG;
+  if (path && path_stride < 1) return SPEC_ERR_INVALID_ARG;
+  if (block_table && (block_size < 1 || max_blocks < 1)) return SPEC_ERR_INVALID_ARG;
+  const void* ptrs[] = {path, num_accepted, kv_base, block_table, out_src, out_dst, out_new_len, out_num_moves,
+                        out_status};
+  for (const void* q : ptrs)
+    if (q && !aligned_to(q, 4)) return SPEC_ERR_INVALID_ARG;
+  KvArgs a = {};
+  a.path = path;
+  a.n = num_accepted;
+  a.base = kv_base;
+  a.block_table = block_table;
+  a.path_stride = path ? path_stride : 0;
+  a.max_blocks = block_table ? max_blocks : 0;
+  a.block_size = block_table ? block_size : 0;
+  a.B = B;
+  a.max_keep = max_keep;
+  a.out_src = out_src;
+  a.out_dst = out_dst;
+  a.out_new_len = out_new_len;
+  a.out_moves = out_num_moves;
+  a.status = out_status;
+  if (launch_kv_compact(a, cuda_stream) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
 int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype, const spec_sampling_params* params,
                          float* out_probs, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return run_sample(logits, nullptr, nullptr, nullptr, R, 0, V, dtype, params, nullptr, nullptr, nullptr, nullptr,

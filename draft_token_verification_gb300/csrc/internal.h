@@ -224,11 +224,25 @@ struct ArgmaxArgs {
   uint32_t* tickets;
 };
 
+struct KvArgs {
+  const int32_t* path;         // [B][path_stride] or nullptr (chain)
+  const int32_t* n;            // [B]
+  const int32_t* base;         // [B]
+  const int32_t* block_table;  // [B][max_blocks] or nullptr
+  int path_stride, max_blocks, block_size, B, max_keep;
+  int32_t* out_src;
+  int32_t* out_dst;
+  int32_t* out_new_len;
+  int32_t* out_moves;          // or nullptr
+  uint32_t* status;            // or nullptr
+};
+
 // Launchers (return a cudaError_t as int).  launch_sample issues the stream
 // and tail kernels, and the draw kernel in MODE_SAMPLE.
 int launch_sample(const SampleArgs& a, int dtype, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
 int launch_tree_sample(const TreeSampleArgs& a, int dtype, void* stream);
+int launch_kv_compact(const KvArgs& a, void* stream);
 // Shared-memory bytes of one tree-sampling CTA for slice `slice`.
 size_t tree_smem_bytes(int dtype, int slice);
 size_t sample_smem_bytes(int dtype, bool filter);

@@ -68,6 +68,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_PARENT 4u  /* parents[0] != -1 or parents[j] not in [0, j) */
 #define SPEC_STATUS_DEPTH 8u       /* an agreed tree node deeper than max_depth */
 #define SPEC_STATUS_TIMEOUT 16u    /* a bounded device wait gave up             */
+#define SPEC_STATUS_BAD_KV 32u     /* spec_kv_compact: a path, length or block
+                                      lookup out of range (sequence left out)   */
 
 /* Limits. */
 #define SPEC_MAX_K 31              /* drafts per sequence                       */
@@ -238,6 +240,52 @@ int spec_verify_tree_sample(const void* node_logits, const void* draft_logits, c
                             spec_dtype dtype, float temperature, const float* temperature_per_tree,
                             int32_t* out_tokens, int32_t* out_path, int32_t* out_num_accepted,
                             void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * KV-cache bookkeeping after a verification pass ([TGTG] section 2.4,
+ * KV-cached regime: on rejection the cache is cut back to the accepted
+ * prefix; [EIN] "One decode round, end to end": the longest agreed path is
+ * committed and the other branches collapse).
+ *
+ * The verification pass wrote one cache entry per input position of
+ * sequence b: node j of its flattened tree (node 0 the root, the last
+ * committed token) at logical position kv_base[b] + j.  A chain of k drafts
+ * is the tree whose node j (1 <= j <= k) is draft j - 1; pass path = NULL.
+ * With n accepted nodes the cache keeps the root's entry and those of the
+ * path's nodes, in path order, at logical positions kv_base[b] + d,
+ * d = 0..n, and ends there: every other entry of the pass is dropped.  The
+ * committed correction token has no entry yet (the next pass writes it).
+ *
+ *   path          [B][path_stride] int32 device: node ids of the accepted
+ *                 path, root excluded (out_path of spec_verify_tree_greedy /
+ *                 spec_verify_tree_sample), or NULL for a chain
+ *   num_accepted  [B] int32 device: n
+ *   kv_base       [B] int32 device: logical position of node 0's entry
+ *   block_table   [B][max_blocks] int32 device: physical block of every
+ *                 logical block of the sequence (paged cache, block_size
+ *                 entries per block), or NULL: slots are logical positions
+ *   out_src, out_dst  [B][max_keep] int32 device: slot of the d-th kept
+ *                 entry now (src) and after the cut (dst), d = 0..n; -1 after
+ *   out_new_len   [B] int32 device: kv_base + n + 1 (logical length)
+ *   out_num_moves [B] int32 device or NULL: kept entries with src != dst.
+ *                 Path node ids increase along a path and are >= their
+ *                 depth, so the moves are a suffix of the list and each
+ *                 dst is below its src: copying entry by entry in
+ *                 ascending d overwrites no source still to be read.
+ *   out_status    [1] uint32 device or NULL: SPEC_STATUS_BAD_KV is OR-ed
+ *                 in (the caller clears it) when a sequence's n is
+ *                 negative, n + 1 > max_keep, a path entry is not above the
+ *                 one before it (or below 1), kv_base is negative, a
+ *                 position exceeds INT32_MAX, or a block lookup falls
+ *                 outside [0, max_blocks) or reads a negative block; that
+ *                 sequence gets -1 everywhere and 0 moves.
+ * B >= 1, max_keep >= 1, path_stride >= 1 when path is set, block_size >= 1
+ * and max_blocks >= 1 when block_table is set.  No workspace; one launch.
+ */
+int spec_kv_compact(const int32_t* path, int path_stride, const int32_t* num_accepted, const int32_t* kv_base,
+                    const int32_t* block_table, int max_blocks, int block_size, int B, int max_keep,
+                    int32_t* out_src, int32_t* out_dst, int32_t* out_new_len, int32_t* out_num_moves,
+                    uint32_t* out_status, void* cuda_stream);
 
 /*
  * The filtered, normalised distribution the accept test uses, written out

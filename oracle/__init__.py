@@ -239,3 +239,71 @@ def best_gamma(alpha: float, c: float, gamma_max: int = 12):
     best = ctypes.c_double()
     g = _load().oracle_best_gamma(float(alpha), float(c), int(gamma_max), ctypes.byref(best))
     return g, best.value
+
+
+def kv_compact(num_accepted, kv_base, path=None, block_table=None, block_size=0, max_keep=None):
+    """KV-cache keep list after a verification pass, written out per sequence.
+
+    "Towards Green Text Generation: Memory-Based Speculative Decoding",
+    section 2.4 (KV-cached regime): on rejection the cache is cut back to the
+    accepted prefix.  Edge Inference Notes, "One decode round, end to end": the
+    longest agreed path is committed and the other branches collapse.  Reading
+    taken: the pass wrote node j's entry (node 0 the root, the last committed
+    token; a chain's node j is its draft j - 1) at logical position base + j;
+    the kept entries are the root's and the path's, in path order, and go to
+    positions base, base + 1, ..., base + n.  A paged cache maps position p
+    to block_table[p // block_size] * block_size + p % block_size.
+
+    Returns (src [B][max_keep], dst [B][max_keep], new_len [B], moves [B],
+    bad [B]); a sequence whose path is not strictly increasing from the root,
+    whose n does not fit, or whose lookups fall outside its table is bad and
+    gets -1 everywhere and 0 moves.
+    """
+    n_all = np.asarray(num_accepted, np.int64)
+    base_all = np.asarray(kv_base, np.int64)
+    B = len(n_all)
+    if max_keep is None:
+        max_keep = np.asarray(path).shape[1] + 1
+    src = np.full((B, max_keep), -1, np.int32)
+    dst = np.full((B, max_keep), -1, np.int32)
+    new_len = np.full(B, -1, np.int32)
+    moves = np.zeros(B, np.int32)
+    bad = np.zeros(B, bool)
+    int_max = 2**31 - 1
+
+    for b in range(B):
+        n, base = int(n_all[b]), int(base_all[b])
+
+        def slot(pos):
+            if block_table is None:
+                return pos if pos <= int_max else None
+            row = block_table[b]
+            blk = pos // block_size
+            if blk >= len(row) or int(row[blk]) < 0:
+                return None
+            s = int(row[blk]) * block_size + pos % block_size
+            return s if s <= int_max else None
+
+        ok = n >= 0 and n + 1 <= max_keep and base >= 0 and base + n + 1 <= int_max
+        if ok and path is not None and n > np.asarray(path).shape[1]:
+            ok = False
+        kept = []
+        if ok:
+            kept = [0] + ([int(path[b][d]) for d in range(n)] if path is not None else list(range(1, n + 1)))
+            ok = all(kept[d] > kept[d - 1] for d in range(1, n + 1))
+        pairs = []
+        if ok:
+            for d in range(n + 1):
+                s, t = slot(base + kept[d]), slot(base + d)
+                if s is None or t is None:
+                    ok = False
+                    break
+                pairs.append((s, t))
+        if not ok:
+            bad[b] = True
+            continue
+        for d, (s, t) in enumerate(pairs):
+            src[b, d], dst[b, d] = s, t
+        new_len[b] = base + n + 1
+        moves[b] = sum(1 for d in range(n + 1) if kept[d] != d)
+    return src, dst, new_len, moves, bad

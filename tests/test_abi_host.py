@@ -132,6 +132,23 @@ def test_tree_sample_rejects_bad_arguments(L):
     assert call(V=300000, dt=0) == sv.SPEC_ERR_UNSUPPORTED
 
 
+def test_kv_compact_rejects_bad_arguments(L):
+    kv = L.spec_kv_compact
+
+    def call(path=FAKE, stride=7, n=FAKE, base=FAKE, table=None, mb=0, bs=0, B=4, keep=8, moves=None, st=None):
+        return kv(path, stride, n, base, table, mb, bs, B, keep, FAKE, FAKE, FAKE, moves, st, None)
+
+    assert call(n=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(base=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(B=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(keep=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(stride=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(table=FAKE, mb=4, bs=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(table=FAKE, mb=0, bs=16) == sv.SPEC_ERR_INVALID_ARG
+    assert call(st=ctypes.c_void_p(4098)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(moves=ctypes.c_void_p(4098)) == sv.SPEC_ERR_INVALID_ARG
+
+
 def test_calculator_helpers_match_golden(L):
     with open(os.path.join(ROOT, "tests", "golden", "closed_forms.json")) as f:
         g = json.load(f)

@@ -194,14 +194,15 @@ def _finish_sample(name, dtype, L, D, T, top_k, top_p, ss, tps=None, mask_fn=Non
                       tps, seed, meta or {})
 
 
-def config1(mask_fn: Optional[MaskFn] = None) -> SampleCase:
-    """C1: B=1, k=4, V=32000, fp32, T=1, no filter, everything from seed 0."""
-    B, k, V = 1, 4, 32000
-    ss = np.random.SeedSequence(0)
+def config1(mask_fn: Optional[MaskFn] = None, seed: int = 0, B: int = 1) -> SampleCase:
+    """C1: B=1, k=4, V=32000, fp32, T=1, no filter, everything from seed 0
+    (other seeds and batch sizes give more sequences of the same recipe)."""
+    k, V = 4, 32000
+    ss = np.random.SeedSequence(seed)
     s_l, s_d, s_tok, s_u = ss.spawn(4)
     L = _rng(s_l).normal(0.0, 2.0, size=(B, k + 1, V)).astype(np.float32)
     D = (L[:, :k] + _rng(s_d).normal(0.0, 1.0, size=(B, k, V))).astype(np.float32)
-    return _finish_sample("C1", F32, L, D, 1.0, 0, 1.0, (s_tok, s_u), mask_fn=mask_fn, seed=0)
+    return _finish_sample("C1", F32, L, D, 1.0, 0, 1.0, (s_tok, s_u), mask_fn=mask_fn, seed=seed)
 
 
 def config2(seed: int = 2, mask_fn: Optional[MaskFn] = None, B: int = 16) -> SampleCase:
@@ -362,3 +363,40 @@ def tree_sample_case(B: int, N: int, V: int, max_depth: int, seed: int = 0, dtyp
     uniforms = _rng(s_u).random((B, N), dtype=np.float32)
     return TreeSampleCase(f"tree-sample-B{B}-N{N}-V{V}", dtype, logits, draft, tokens, parents, uniforms,
                           max_depth, float(temperature), seed)
+
+
+@dataclass
+class KvCase:
+    """Inputs of the KV keep-list step: accept counts, cache positions of the
+    roots, accepted paths (None for chains) and an optional block table."""
+    num_accepted: np.ndarray
+    kv_base: np.ndarray
+    path: Optional[np.ndarray]
+    block_table: Optional[np.ndarray]
+    block_size: int
+    max_keep: int
+    entries: int          # cache entries the pass wrote per sequence (N, or k + 1)
+
+
+def kv_case(B: int, N: int, max_depth: int, seed: int = 0, chain: bool = False, block_size: int = 0,
+            base_max: int = 4000) -> KvCase:
+    """B sequences whose pass wrote N entries each (a chain: N = k + 1).
+    n ~ U{0..max_depth}; a tree path is n distinct node ids from 1..N-1 in
+    increasing order (the shape every root-to-node path of a tree whose
+    parents precede their children has), -1 padded to max_depth + 1 entries;
+    roots at positions U{0..base_max}.  With block_size > 0 every sequence
+    gets ceil((base_max + N) / block_size) logical blocks mapped to distinct
+    physical blocks of one shared pool, in random order."""
+    rng = _rng(np.random.SeedSequence(seed))
+    n = rng.integers(0, max_depth + 1, B).astype(np.int32)
+    base = rng.integers(0, base_max + 1, B).astype(np.int32)
+    path = None
+    if not chain:
+        path = np.full((B, max_depth + 1), -1, np.int32)
+        for b in range(B):
+            path[b, :n[b]] = np.sort(rng.choice(np.arange(1, N), size=n[b], replace=False))
+    table = None
+    if block_size > 0:
+        M = -(-(base_max + N) // block_size)
+        table = rng.permutation(B * M).astype(np.int32).reshape(B, M)
+    return KvCase(n, base, path, table, block_size, (N if chain else max_depth + 1), N)
