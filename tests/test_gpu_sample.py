@@ -1,8 +1,9 @@
 """GPU parity of speculative-sampling verification against the float64 oracle.
 
 Bar (per sequence): identical accept count and committed tokens, except for
-sequences the oracle flags as within 1e-6 of a decision edge (counted; must
-stay under 1e-5 of all draws); p_i(x_i), q_i(x_i) within 1e-5 absolute.
+sequences the oracle flags as within 1e-6 of a decision edge (counted, and
+held against the rate the oracle alone gives on the same recipes);
+p_i(x_i), q_i(x_i) within 1e-5 absolute.
 """
 import numpy as np
 import pytest
@@ -10,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from parity_utils import (BOUNDARY_BUDGET, compare_sample, lib, q_support_mask, run_sample_gpu,
+from parity_utils import (compare_sample, lib, q_support_mask, run_sample_gpu,
                           run_sample_oracle, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -18,21 +19,35 @@ pytestmark = pytest.mark.gpu
 # Boundary draws (oracle decision within 1e-6 of an edge), per kind of input:
 # "config" = workloads C1-C3, "sweep" = C5 points, "edge" = constructed edge
 # cases (flat rows, quantised ties), where edges are dense by construction.
-_BOUNDARY = {kind: {"count": 0, "draws": 0} for kind in ("config", "sweep", "edge")}
+_BOUNDARY = {kind: {"count": 0, "draws": 0, "expect": 0.0} for kind in ("config", "sweep", "edge")}
 
 
-def _check(case, seqs=None, kind="edge"):
+def _oracle_rates():
+    """Boundary sequences per decision that the oracle alone finds on many
+    seeded batches of each recipe (written by tests/golden/boundary_rates.py)."""
+    import json
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "boundary_rates.json")
+    return {k: v["rate"] for k, v in json.load(open(path))["configs"].items()}
+
+
+def _check(case, seqs=None, kind="edge", recipe=None):
     gpu = run_sample_gpu(case)
     orc = run_sample_oracle(case, seqs)
     nb, draws = compare_sample(case, gpu, orc, seqs)
     _BOUNDARY[kind]["count"] += nb
     _BOUNDARY[kind]["draws"] += draws
+    if recipe is not None:
+        rate = _oracle_rates().get(recipe)
+        assert rate is not None, f"tests/golden/boundary_rates.json has no rate for {recipe}"
+        _BOUNDARY[kind]["expect"] += rate * draws
     return gpu, orc
 
 
 def test_config1_fp32_no_filter():
     case = W.config1()
-    gpu, orc = _check(case, kind="config")
+    gpu, orc = _check(case, kind="config", recipe="C1")
     # the same logits through greedy mode
     g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
     o = oracle.verify_greedy(case.target, case.tokens)
@@ -41,24 +56,33 @@ def test_config1_fp32_no_filter():
 
 def test_config2_topk50_bf16():
     case = W.config2(mask_fn=q_support_mask(50, 1.0))
-    _check(case, kind="config")
+    _check(case, kind="config", recipe="C2")
 
 
 @pytest.mark.parametrize("per_seq", [False, True])
-def test_config3_topp_full_size_sampled(per_seq):
+def test_config3_topp_full_size(per_seq):
+    """C3 at full size: every one of the 64 sequences against the oracle."""
     case = W.config3(per_seq_temperature=per_seq)
-    seqs = list(range(0, case.B, 4))  # the oracle checks every 4th sequence of the full launch
-    _check(case, seqs, kind="config")
+    _check(case, kind="config", recipe="C3")
 
 
-@pytest.mark.parametrize("B,k,sigma", [(1, 1, 0.5), (4, 12, 2.0), (16, 4, 4.0), (64, 8, 0.5), (128, 2, 2.0)])
+C5_POINTS = ([(1, 1, 0.5), (4, 12, 2.0), (16, 4, 4.0), (64, 8, 0.5), (128, 2, 2.0)]
+             + [(256, k, s) for k in (8, 12) for s in (0.5, 2.0, 4.0)]
+             + [(B, 12, s) for B in (64, 128) for s in (0.5, 4.0)])
+
+
+@pytest.mark.parametrize("B,k,sigma", C5_POINTS)
 def test_config5_sweep_points(B, k, sigma):
+    """Sweep points of C5 (V = 152064, top-p 0.95): at least 32 sequences of
+    every point (all of them up to B = 32) against the oracle, and greedy mode
+    on the same target rows against the oracle's argmax chain."""
     case = W.config5(B, k, sigma)
-    seqs = list(range(0, B, max(1, B // 8)))
-    _check(case, seqs, kind="sweep")
-    o = oracle.verify_greedy(case.target, case.tokens)
+    seqs = list(range(0, B, max(1, B // 32)))
+    _check(case, seqs, kind="sweep", recipe=f"C5s{sigma:g}")
+    sl = np.asarray(seqs)
+    o = oracle.verify_greedy(case.target[sl], case.tokens[sl])
     g_tok, g_n = lib().spec_verify_greedy(to_dev(case.target), to_dev(case.tokens))
-    assert np.array_equal(g_tok.cpu().numpy(), o["tokens"]) and np.array_equal(g_n.cpu().numpy(), o["n"])
+    assert np.array_equal(g_tok.cpu().numpy()[sl], o["tokens"]) and np.array_equal(g_n.cpu().numpy()[sl], o["n"])
 
 
 EDGE = [
@@ -211,18 +235,24 @@ def test_transform_probs_within_tolerance(dtype, top_k, top_p, V):
         assert abs(got[r].sum() - 1.0) < 1e-4
 
 
-def test_boundary_draws_under_budget():
-    """Runs last in this module.  Boundary draws are counted and reported per
-    kind of input; on the concentrated workloads C1-C3 they must stay under
-    1e-5 of all draws.  (For deep nuclei such as C5's and for the constructed
-    flat / tied rows, the share of draws whose uniform lies within 1e-6 of an
-    interval edge is a property of the inputs, fixed by the oracle alone.)"""
+def test_boundary_draws_reported():
+    """Runs after the configuration and sweep cases of this module.  The
+    sequences left out of the exact comparison (an oracle decision within
+    1e-6 of its edge) are counted per kind of input and held against the rate
+    the oracle alone gives on many seeded batches of the same recipes.  That
+    rate is a property of the inputs and of the 1e-6 width, not of the GPU
+    path: an unfiltered draw over 128k tokens picks a token whose own
+    interval is often narrower than 1e-5 of the total, so C1's rate is about
+    1e-2 by the definition alone.  The count seen here must stay within what
+    those rates allow (mean + 5 sigma + 3), so that a flag gone wrong cannot
+    silently shrink what parity compares."""
     for kind, c in _BOUNDARY.items():
-        print(f"boundary draws [{kind}]: {c['count']} of {c['draws']}")
-    c = _BOUNDARY["config"]
-    if c["draws"] == 0:
-        pytest.skip("no configuration cases ran")
-    assert c["count"] == 0 or c["count"] / c["draws"] < BOUNDARY_BUDGET
+        print(f"boundary sequences [{kind}]: {c['count']} of {c['draws']} decisions "
+              f"(oracle rate expects {c['expect']:.2f})")
+        if kind == "edge" or c["draws"] == 0:
+            continue  # constructed flat / tied rows: edges dense by design
+        e = c["expect"]
+        assert c["count"] <= e + 5.0 * e ** 0.5 + 3, (kind, c)
 
 
 # The stream and tail parts of sampling run fused in one cooperative launch

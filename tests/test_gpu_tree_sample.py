@@ -63,9 +63,11 @@ def test_tree_sample_parity(B, N, V, depth, dtype, noise, T):
 
 
 def test_tree_sample_parity_full_size():
-    """8 trees of 60 nodes, depth <= 6, V = 128256, bf16."""
+    """8 trees of 60 nodes, depth <= 6, V = 128256, bf16.  One tree of this
+    seeded batch ends with an unfiltered draw 3.7e-7 from its interval's edge
+    (the oracle flags it); at most one boundary tree is allowed."""
     case = W.tree_sample_case(8, 60, 128256, 6, seed=4)
-    compare(case, run_gpu(case), run_oracle(case), max_boundary=0.25)
+    assert compare(case, run_gpu(case), run_oracle(case)) <= 1
 
 
 def test_tree_sample_many_small_trees():
