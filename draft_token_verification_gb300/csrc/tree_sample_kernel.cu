@@ -35,6 +35,8 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 #include <math.h>
 #include <stdint.h>
 
@@ -1038,36 +1040,51 @@ cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, size_t smem, cudaSt
   return cfg;
 }
 
+// Shared-memory opt-in and cluster occupancy of the node kernel, per device
+// and dtype: the last shared-memory size set and the clusters that fit.
+constexpr int kTreeMaxDevices = 64;
+struct TreeLaunchCache {
+  int smem = -1;
+  int clusters = 0;
+};
+std::mutex g_tree_mu;
+TreeLaunchCache g_tree_cache[kTreeMaxDevices][2];
+
 template <int DT>
 int launch_tree_t(const TreeSampleArgs& a, cudaStream_t st) {
-  static int cached_smem[2] = {-1, -1}, cached_clusters[2] = {0, 0}, cached_dev[2] = {-1, -1};
   const size_t smem = tree_smem_bytes(DT, a.slice);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kTreeMaxDevices) return cudaErrorInvalidDevice;
   auto node_k = tree_node_kernel<DT>;
   auto walk_k = tree_walk_kernel<DT>;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(attr, smem, st);
-  if (cached_smem[DT] != static_cast<int>(smem) || cached_dev[DT] != dev) {
-    e = cudaFuncSetAttribute(node_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(walk_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(kTreeCl);
-    int ncl = 0;
-    e = cudaOccupancyMaxActiveClusters(&ncl, node_k, &cfg);
-    if (e != cudaSuccess) return e;
-    if (ncl < 1) return cudaErrorInvalidConfiguration;
-    cached_smem[DT] = static_cast<int>(smem);
-    cached_clusters[DT] = ncl;
-    cached_dev[DT] = dev;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_tree_mu);
+    TreeLaunchCache& c = g_tree_cache[dev][DT];
+    if (c.smem != static_cast<int>(smem)) {
+      e = cudaFuncSetAttribute(node_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(walk_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3(kTreeCl);
+      int ncl = 0;
+      e = cudaOccupancyMaxActiveClusters(&ncl, node_k, &cfg);
+      if (e != cudaSuccess) return e;
+      if (ncl < 1) return cudaErrorInvalidConfiguration;
+      c.smem = static_cast<int>(smem);
+      c.clusters = ncl;
+    }
+    max_clusters = c.clusters;
   }
   tree_plan_kernel<<<a.B, kThreads, 0, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nodes = static_cast<int64_t>(a.B) * a.N;
-  const int clusters = static_cast<int>(nodes < cached_clusters[DT] ? nodes : cached_clusters[DT]);
+  const int clusters = static_cast<int>(nodes < max_clusters ? nodes : max_clusters);
   cfg.gridDim = dim3(clusters * kTreeCl);
   e = cudaLaunchKernelEx(&cfg, node_k, a);
   if (e == cudaSuccess) {
