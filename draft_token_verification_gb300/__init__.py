@@ -57,6 +57,7 @@ EXPORTS = (
 SPEC_LAUNCH_SEPARATE = 0
 SPEC_LAUNCH_FUSED = 1
 SPEC_LAUNCH_FUSED_WAIT_TEST = 2
+SPEC_LAUNCH_ROWS = 3
 
 
 class SpecSamplingParams(ctypes.Structure):
@@ -385,7 +386,8 @@ def spec_verify_tree_sample(node_logits: torch.Tensor, draft_logits: torch.Tenso
 
 def spec_kv_compact(num_accepted: torch.Tensor, kv_base: torch.Tensor, path: Optional[torch.Tensor] = None,
                     block_table: Optional[torch.Tensor] = None, block_size: int = 0, max_keep: Optional[int] = None,
-                    out_status: Optional[torch.Tensor] = None, stream=None):
+                    out_status: Optional[torch.Tensor] = None, out_src=None, out_dst=None, out_new_len=None,
+                    out_num_moves=None, stream=None):
     """KV-cache keep list after verification: (src [B][max_keep], dst [B][max_keep],
     new_len [B], num_moves [B]) slots of the kept entries before and after the
     cut.  path [B][S] (tree out_path) or None for a chain; block_table [B][M]
@@ -396,16 +398,18 @@ def spec_kv_compact(num_accepted: torch.Tensor, kv_base: torch.Tensor, path: Opt
         max_keep = (path.shape[1] + 1) if path is not None else None
         if max_keep is None:
             raise ValueError("max_keep is required for a chain (k + 1)")
-    src = torch.empty((B, max_keep), dtype=torch.int32, device=dev)
-    dst = torch.empty((B, max_keep), dtype=torch.int32, device=dev)
-    new_len = torch.empty((B,), dtype=torch.int32, device=dev)
-    moves = torch.empty((B,), dtype=torch.int32, device=dev)
+    src = out_src if out_src is not None else torch.empty((B, max_keep), dtype=torch.int32, device=dev)
+    dst = out_dst if out_dst is not None else torch.empty((B, max_keep), dtype=torch.int32, device=dev)
+    new_len = out_new_len if out_new_len is not None else torch.empty((B,), dtype=torch.int32, device=dev)
+    moves = out_num_moves if out_num_moves is not None else torch.empty((B,), dtype=torch.int32, device=dev)
+    if src.shape != (B, max_keep) or dst.shape != (B, max_keep) or new_len.shape != (B,) or moves.shape != (B,):
+        raise ValueError("spec_kv_compact: output shapes must be [B][max_keep] and [B]")
     rc = lib().spec_kv_compact(
         _dev(path, "path", torch.int32), path.shape[1] if path is not None else 0,
         _dev(num_accepted, "num_accepted", torch.int32), _dev(kv_base, "kv_base", torch.int32),
         _dev(block_table, "block_table", torch.int32), block_table.shape[1] if block_table is not None else 0,
-        block_size, B, max_keep, _dev(src, "out_src"), _dev(dst, "out_dst"), _dev(new_len, "out_new_len"),
-        _dev(moves, "out_num_moves"), _dev(out_status, "out_status", torch.int32) if out_status is not None else None,
+        block_size, B, max_keep, _dev(src, "out_src", torch.int32), _dev(dst, "out_dst", torch.int32),
+        _dev(new_len, "out_new_len", torch.int32), _dev(moves, "out_num_moves", torch.int32), _dev(out_status, "out_status", torch.int32) if out_status is not None else None,
         _stream(stream),
     )
     _check(rc, "spec_kv_compact")

@@ -89,7 +89,16 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.aligned_target = rows_aligned(target, V, dtype);
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
-  const int e = launch_sample(a, dtype == SPEC_BF16 ? DT_BF16 : DT_F32, stream);
+  const int dt = dtype == SPEC_BF16 ? DT_BF16 : DT_F32;
+  const bool rows = a.launch_mode == SPEC_LAUNCH_ROWS || a.launch_mode == SPEC_LAUNCH_FUSED_WAIT_TEST;
+  if (rows && row_supported(a, dt)) {
+    a.poll_limit = 64;  // (used only by the failure-detection mode)
+    const int e = launch_rows(a, dt, stream);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
+    return SPEC_OK;
+  }
+  if (a.launch_mode == SPEC_LAUNCH_ROWS) a.launch_mode = SPEC_LAUNCH_FUSED;
+  const int e = launch_sample(a, dt, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }
@@ -180,7 +189,8 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
 }
 
 int spec_sample_launch_mode(int mode) {
-  if (mode != SPEC_LAUNCH_FUSED && mode != SPEC_LAUNCH_SEPARATE && mode != SPEC_LAUNCH_FUSED_WAIT_TEST)
+  if (mode != SPEC_LAUNCH_FUSED && mode != SPEC_LAUNCH_SEPARATE && mode != SPEC_LAUNCH_FUSED_WAIT_TEST &&
+      mode != SPEC_LAUNCH_ROWS)
     return SPEC_ERR_INVALID_ARG;
   return g_launch_mode.exchange(mode);
 }

@@ -98,6 +98,8 @@ struct TreeRec {
   int32_t pad[2];
   double chunk[kTreeChunks];  // sums of that weight per (CTA, warp) chunk
 };
+// The tree draw scans the chunk sums with one warp, two chunks per lane.
+static_assert(kTreeChunks == 2 * 32, "the tree draw reads exactly two chunk sums per lane of one warp");
 
 // Workspace layout (byte offsets), identical for every call with the same
 // (B, k).  Tickets are zero between calls; everything else is written before
@@ -243,6 +245,10 @@ int launch_sample(const SampleArgs& a, int dtype, void* stream);
 int launch_argmax(const ArgmaxArgs& a, int dtype, bool tree, void* stream);
 int launch_tree_sample(const TreeSampleArgs& a, int dtype, void* stream);
 int launch_kv_compact(const KvArgs& a, void* stream);
+// Sampling verification with one CTA per row streamed through a ring of
+// bulk-copy stages: bf16 rows with or without a filter, f32 rows without one.
+bool row_supported(const SampleArgs& a, int dtype);
+int launch_rows(const SampleArgs& a, int dtype, void* stream);
 // Shared-memory bytes of one tree-sampling CTA for slice `slice`.
 size_t tree_smem_bytes(int dtype, int slice);
 size_t sample_smem_bytes(int dtype, bool filter);

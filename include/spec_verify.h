@@ -342,22 +342,42 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
                                float* out_q_draft, uint32_t* out_status, void* cuda_stream);
 
 /*
- * How the sampling entry points launch their stream and tail parts, for the
- * whole process (a setting, not a request of the pages):
- *   SPEC_LAUNCH_FUSED     one cooperative launch whose CTAs take every row's
- *                         stream part, then every row's tail part (the default;
- *                         the separate launches stand in when the GPU refuses it)
+ * How the sampling entry points launch, for the whole process (a setting,
+ * not a request of the pages):
+ *   SPEC_LAUNCH_ROWS      one launch with one CTA per row: the row streams
+ *                         through shared memory by bulk copies; the values
+ *                         within 2^-12 of the running maximum's mass are
+ *                         listed as candidates, from which the filter's cut,
+ *                         its ties and the draw are decided (rows whose kept
+ *                         set outgrows the list are searched again from L2);
+ *                         the second CTA of each (target, draft) pair takes
+ *                         the accept test and draws at a rejection.  Used for
+ *                         bf16 rows with or without a filter and for f32 rows
+ *                         without one, up to V * element bytes = 512 KiB; other
+ *                         shapes take SPEC_LAUNCH_FUSED.  Faster than the
+ *                         fused launch where the kept set is wide
+ *                         (top-p near 1 over flat rows) or the temperature
+ *                         varies per sequence.
+ *   SPEC_LAUNCH_FUSED     (the default) one cooperative launch whose CTAs
+ *                         take every row's stream part, then every row's
+ *                         tail part (the separate launches stand in when the
+ *                         GPU refuses it)
  *   SPEC_LAUNCH_SEPARATE  a stream launch, then a tail launch
- *   SPEC_LAUNCH_FUSED_WAIT_TEST  the fused launch with the stream parts'
- *                         completion flags withheld and a short poll limit:
- *                         every tail part's bounded wait runs out, every row
- *                         is published as non-finite and SPEC_STATUS_TIMEOUT
- *                         is set (exercises the timeout path without a fault)
+ *   SPEC_LAUNCH_FUSED_WAIT_TEST  failure detection without a fault: the
+ *                         SPEC_LAUNCH_ROWS launch with its bulk copies withheld and a
+ *                         short poll limit (or, for shapes it does not take,
+ *                         the fused launch with its completion flags
+ *                         withheld): every bounded wait runs out, every row
+ *                         is treated as non-finite and SPEC_STATUS_TIMEOUT is
+ *                         set; nothing is left in flight
+ * spec_transform_probs always takes the stream and tail kernels.  Every mode
+ * gives the same results outside decisions within rounding of their edge.
  * Returns the previous mode, or SPEC_ERR_INVALID_ARG for an unknown one.
  */
 #define SPEC_LAUNCH_FUSED 1
 #define SPEC_LAUNCH_SEPARATE 0
 #define SPEC_LAUNCH_FUSED_WAIT_TEST 2
+#define SPEC_LAUNCH_ROWS 3
 int spec_sample_launch_mode(int mode);
 
 /* Static description of a return code. */
