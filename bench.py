@@ -9,8 +9,14 @@ One step = one pass of the whole verification hot path over one batch:
     V = 128256, bf16.
 Metric: verified draft positions per second (64*8 + 64*8 + 8*59 per step).
 
+Each step also lists the KV-cache keep entries of the sampled chains and of
+the trees (spec_kv_compact), the bookkeeping a decode loop needs next.
+
 Default: python bench.py [--gpus N --steps K --warmup W]; prints one JSON line.
 --impl reference times the float64 CPU oracle on a bounded sample instead.
+--sweep times sampling and greedy verification over the V = 152064 sweep
+(B in 1..256, k in 1..12, three draft noise levels) and the draft-length scan
+fed with the measured verification cost; it prints one JSON line.
 Under torchrun every rank runs its own batch on its own GPU (weak scaling,
 no collective on the data path); rank 0 prints the line.
 """
@@ -75,13 +81,13 @@ def tree_sample_bytes(case, n, path):
 def time_tree_sample(sv, dev, ws, stream, seed, iters=20):
     """Token-tree sampling verification, timed alone outside the step: 8 trees
     of 60 nodes, depth <= 6, V = 128256, bf16, children drawn from their
-    parents' draft rows.  An L2-sized buffer is written before every timed call
+    parents' draft rows.  A 512 MB buffer (4x L2) is written before every timed call
     (the rows it reads fit in L2)."""
     import torch
 
     c = W.tree_sample_case(TREE["B"], TREE["N"], TREE["V"], TREE["depth"], seed=seed)
     args = [to_torch(x, dev) for x in (c.logits, c.draft, c.node_tokens, c.parents, c.uniforms)]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(3):
         out = sv.spec_verify_tree_sample(*args, TREE["depth"], workspace=ws, stream=stream)
     ts = []
@@ -95,6 +101,29 @@ def time_tree_sample(sv, dev, ws, stream, seed, iters=20):
         ts.append(e0.elapsed_time(e1) * 1e3)
     n, path = out[2].cpu().numpy(), out[1].cpu().numpy()
     return float(np.median(ts)), tree_sample_bytes(c, n, path), float(n.mean())
+
+
+def time_per_seq_temperature(sv, dev, ws, stream, seed, iters=20):
+    """Sampling verification of the main workload with a temperature per
+    sequence (T_b ~ U(0.5, 1.2)), timed alone: the same 64 x 8 x 128256 bf16
+    rows as the step with a per-sequence temperature array.  The rows (279 MB)
+    exceed L2, so every call reads them from HBM."""
+    import torch
+
+    c = W.config3(seed=seed, per_seq_temperature=True, B=SAMPLE["B"], k=SAMPLE["k"], V=SAMPLE["V"])
+    args = [to_torch(x, dev) for x in (c.target, c.draft, c.tokens, c.uniforms)]
+    tps = to_torch(c.temperature_per_seq, dev)
+    for _ in range(3):
+        out = sv.spec_verify_sample(*args, SAMPLE["T"], 0, SAMPLE["top_p"], tps, workspace=ws, stream=stream)
+    ts = []
+    for _ in range(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        out = sv.spec_verify_sample(*args, SAMPLE["T"], 0, SAMPLE["top_p"], tps, workspace=ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return float(np.median(ts)), float(out[1].float().mean().item())
 
 
 KERNEL_SOURCES = {
@@ -260,6 +289,20 @@ def run_gpu(args, rank, world):
         "tpath": torch.empty((t.B, t.max_depth + 1), dtype=torch.int32, device=dev),
         "tn": torch.empty(t.B, dtype=torch.int32, device=dev),
     }
+    # KV keep lists: chains from cache position 1000 + 100 b, trees from 2000 + 100 b
+    kv = {"sbase": torch.arange(B, dtype=torch.int32, device=dev) * 100 + 1000,
+          "tbase": torch.arange(t.B, dtype=torch.int32, device=dev) * 100 + 2000}
+    for name, rows, keep in (("s", B, k + 1), ("t", t.B, t.max_depth + 2)):
+        for f in ("src", "dst"):
+            kv[name + f] = torch.empty((rows, keep), dtype=torch.int32, device=dev)
+        kv[name + "len"] = torch.empty(rows, dtype=torch.int32, device=dev)
+        kv[name + "moves"] = torch.empty(rows, dtype=torch.int32, device=dev)
+    kv_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def kv_compact(path, n, base, prefix, rows, keep):
+        sv.spec_kv_compact(n, base, path, max_keep=keep, out_status=kv_status, out_src=kv[prefix + "src"],
+                           out_dst=kv[prefix + "dst"], out_new_len=kv[prefix + "len"],
+                           out_num_moves=kv[prefix + "moves"], stream=stream)
     ws = sv.Workspace(dev)
     stream = torch.cuda.current_stream()
 
@@ -268,6 +311,7 @@ def run_gpu(args, rank, world):
             ev[0].record(stream)
         sv.spec_verify_sample(inputs["target"], inputs["draft"], inputs["tokens"], inputs["uniforms"], SAMPLE["T"],
                               SAMPLE["top_k"], SAMPLE["top_p"], None, o["tok"], o["n"], o["p"], o["q"], ws, stream)
+        kv_compact(None, o["n"], kv["sbase"], "s", B, k + 1)
         if ev is not None:
             ev[1].record(stream)
         sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws, stream)
@@ -275,6 +319,7 @@ def run_gpu(args, rank, world):
             ev[2].record(stream)
         sv.spec_verify_tree_greedy(inputs["tree_logits"], inputs["tree_tokens"], inputs["parents"], TREE["depth"],
                                    o["ttok"], o["tpath"], o["tn"], ws, stream)
+        kv_compact(o["tpath"], o["tn"], kv["tbase"], "t", t.B, t.max_depth + 2)
         if ev is not None:
             ev[3].record(stream)
 
@@ -348,10 +393,13 @@ def run_gpu(args, rank, world):
     status |= sv.spec_get_status(ws)
     ts_us, ts_bytes, ts_mal = time_tree_sample(sv, dev, ws, stream, seed=4 + rank)
     status |= sv.spec_get_status(ws)
+    tb_us, tb_mal = time_per_seq_temperature(sv, dev, ws, stream, seed=3 + rank)
+    status |= sv.spec_get_status(ws) | int(kv_status.item())
 
     return dict(elapsed_ms=elapsed_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
                 h2d=h2d, d2h=d2h, mal=float(n_acc.mean()), greedy_mal=float(gn.mean()),
-                tree_sample=(ts_us, ts_bytes, ts_mal))
+                tree_sample=(ts_us, ts_bytes, ts_mal), per_seq_t=(tb_us, tb_mal),
+                kv_moves=int(kv["tmoves"].sum().item()))
 
 
 # ------------------------------------------------------------ CPU leg
@@ -403,6 +451,109 @@ def cpu_baseline(passes: int = 6, threads: int | None = None):
                       f"{dt:.2f} s on {cores} threads"}
 
 
+# ------------------------------------------------------------ sweep
+
+
+def run_sweep(args):
+    """Sampling and greedy verification over the V = 152064 sweep: every B in
+    1..256, k in 1..12 and draft noise sigma in {0.5, 2, 4} (T = 1, top-p 0.95
+    for sampling).  Each call is timed alone with CUDA events after a 512 MB
+    write that evicts L2, median of `iters`.  The draft-length scan of the
+    Speedup Calculator (steps 1-3) is then fed with measured numbers: the
+    acceptance rate alpha seen at each (B, sigma), and the verification cost
+    per pass, fitted as a + b k over the five k and expressed in target
+    forward passes of t_T = 2 bytes x target parameters / measured HBM
+    bandwidth (one decode pass reads every weight once).  Adding a + b gamma
+    to the calculator's cost gamma c + 1 divides the speedup by a constant and
+    replaces c by (c + b) / (1 + a), so the best gamma is the calculator's
+    scan at that effective c."""
+    import torch
+
+    import draft_token_verification_gb300 as sv
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    sv.build()
+    stream = torch.cuda.current_stream()
+    ws = sv.Workspace(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peaks()
+    V = 152064
+    iters = args.sweep_iters
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            out = fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return float(np.median(ts)), out
+
+    points = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for sigma in W.C5_SIGMAS:
+        for k in W.C5_DRAFTS:
+            Bmax = max(W.C5_BATCHES)
+            tgt, drf, tok, uni = W.config5_device(Bmax, k, sigma, device=dev, V=V)
+            for B in W.C5_BATCHES:
+                t, d, x, u = tgt[:B], drf[:B], tok[:B], uni[:B]
+                us_s, out = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
+                                                                stream=stream, want_probs=False))
+                n = out[1].cpu().numpy().astype(np.int64)
+                us_g, gout = timed(lambda: sv.spec_verify_greedy(t, x, workspace=ws, stream=stream))
+                gn = gout[1].cpu().numpy()
+                sb, gb = B * (2 * k + 1) * V * 2, B * (k + 1) * V * 2
+                points.append({
+                    "B": B, "k": k, "sigma": sigma,
+                    "sample": {"us": us_s, "positions_per_s": B * k / us_s * 1e6, "sequences_per_s": B / us_s * 1e6,
+                               "GB/s": sb / us_s / 1e3, "frac": sb / us_s / 1e3 / peak,
+                               "mal": float(n.mean()), "accepted": int(n.sum()),
+                               "tests": int(np.minimum(n + 1, k).sum())},
+                    "greedy": {"us": us_g, "positions_per_s": B * k / us_g * 1e6, "sequences_per_s": B / us_g * 1e6,
+                               "GB/s": gb / us_g / 1e3, "frac": gb / us_g / 1e3 / peak, "mal": float(gn.mean())},
+                })
+            del tgt, drf, tok, uni
+            torch.cuda.empty_cache()
+    clk = clocks.stop()
+    status = sv.spec_get_status(ws)
+
+    # the draft-length scan on measured numbers
+    t_target_us = 2.0 * args.target_params / (peak * 1e9) * 1e6
+    scan = []
+    for B in W.C5_BATCHES:
+        ks = np.array(W.C5_DRAFTS, float)
+        us = np.array([np.median([p["sample"]["us"] for p in points if p["B"] == B and p["k"] == k])
+                       for k in W.C5_DRAFTS])
+        b, a = np.polyfit(ks, us, 1)  # us = a + b k
+        for sigma in W.C5_SIGMAS:
+            sel = [p for p in points if p["B"] == B and p["sigma"] == sigma]
+            alpha = sum(p["sample"]["accepted"] for p in sel) / max(1, sum(p["sample"]["tests"] for p in sel))
+            v0, v1 = a / t_target_us, b / t_target_us
+            c_eff = (args.draft_cost + v1) / (1.0 + v0)
+            g_calc, f_calc = sv.spec_best_gamma(alpha, args.draft_cost, 12)
+            g_meas, f_meas = sv.spec_best_gamma(alpha, c_eff, 12)
+            scan.append({"B": B, "sigma": sigma, "alpha": alpha, "verify_us": {"a": a, "b_per_draft": b},
+                         "v0": v0, "v1": v1, "c_draft": args.draft_cost, "c_eff": c_eff,
+                         "best_gamma_calculator": g_calc, "speedup_calculator": f_calc,
+                         "best_gamma_measured_verify": g_meas, "speedup_measured_verify": f_meas / (1.0 + v0)})
+    line = {"metric": "sweep: verified draft positions/s and sequences/s, V=152064 bf16", "unit": "positions/s",
+            "dtype": "bf16", "data": "synthetic", "config": {
+                "workload": "C5 sweep: B in 1,4,16,64,128,256; k in 1,2,4,8,12; sigma in 0.5,2,4; V=152064 bf16; "
+                            "T=1, top-p 0.95 (sampling); greedy on the same rows",
+                "l2": "512 MB written before every timed call", "iters": iters,
+                "target_forward_us": t_target_us, "target_params": args.target_params,
+                "draft_cost_c": args.draft_cost, "peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs"},
+            "clocks": clk, "status_bits": status, "points": points, "gamma_scan": scan}
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------------ main
 
 
@@ -413,9 +564,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the V=152064 sweep instead of the step")
+    ap.add_argument("--sweep-iters", type=int, default=10)
+    ap.add_argument("--target-params", type=float, default=8.03e9,
+                    help="target model parameters for the gamma scan (default: an 8B target)")
+    ap.add_argument("--draft-cost", type=float, default=0.05,
+                    help="draft forward / target forward time for the gamma scan")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -456,7 +618,13 @@ def main():
         "clocks": r["clk"],
         "e2e": {"value": pos * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 4 * K,  # sampling: fused stream+tail and draw kernels; greedy; tree
+        "sequences_per_s": {
+            "step": (2 * SAMPLE["B"] + TREE["B"]) * world * K / (r["elapsed_ms"] / 1e3),
+            "sample": SAMPLE["B"] / t_sample, "greedy": SAMPLE["B"] / (float(per[:, 1].mean()) / 1e3),
+            "tree": TREE["B"] / (float(per[:, 2].mean()) / 1e3),
+            "what": "sequences (chains or trees) verified per second: the whole step (64 sampled + 64 greedy "
+                    "chains + 8 trees per GPU), and each kernel alone from its own events"},
+        "gpu_launches": 6 * K,  # sampling: fused stream+tail and draw kernels; greedy; tree; two KV keep lists
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic("sample"), "kernel": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together",
                      "peak_source": f"{peak_kind} hbm_gbs"},
@@ -479,8 +647,17 @@ def main():
                             "mean_accepted": r["tree_sample"][2], "traffic": recorded_traffic("tree_sample"),
                             "what": "token-tree sampling verification, 8 trees x 60 nodes, depth <= 6, "
                                     "V=128256 bf16, T=1; plan + node + walk kernels, timed alone after an L2 flush"},
+            "sample_per_seq_temperature": {
+                "us": r["per_seq_t"][0], "GB/s": sample_bytes() / r["per_seq_t"][0] / 1e3,
+                "frac": sample_bytes() / r["per_seq_t"][0] / 1e3 / peak,
+                "sequences_per_s": SAMPLE["B"] / (r["per_seq_t"][0] / 1e6), "mean_accepted": r["per_seq_t"][1],
+                "what": "the step's sampling workload with T_b ~ U(0.5, 1.2) per sequence, timed alone "
+                        "(median of 20; rows exceed L2)"},
         },
         "acceptance": {"sample_mal": r["mal"], "greedy_mal": r["greedy_mal"], "k": SAMPLE["k"]},
+        "boundary_rate": boundary_rates(),
+        "kv_keep": {"tree_entries_moved_last_step": r["kv_moves"],
+                    "what": "spec_kv_compact after the sampled chains and after the trees, inside every step"},
         "status_bits": r["status"],
     }
     if not args.no_cpu_baseline:
@@ -490,6 +667,18 @@ def main():
         import torch.distributed as tdist
 
         tdist.destroy_process_group()
+
+
+def boundary_rates():
+    """Share of oracle decisions within 1e-6 of their edge on each recipe,
+    from the committed oracle-only count (tests/golden/boundary_rates.json)."""
+    path = os.path.join(ROOT, "tests", "golden", "boundary_rates.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: {"rate": v["rate"], "decisions": v["decisions"]} for k, v in d["configs"].items()}
+    except Exception:
+        return None
 
 
 def workload_config(world: int = 1):

@@ -239,6 +239,28 @@ def config5(B: int, k: int, sigma: float, seed: int = 5, mask_fn: Optional[MaskF
                           mask_fn=mask_fn, seed=seed, meta=dict(sigma=sigma))
 
 
+def config5_device(B: int, k: int, sigma: float, seed: int = 5, device="cuda", V: int = 152064):
+    """C5 sweep point drawn on the device (torch's Philox generator), for the
+    benchmark's sweep, where numpy would take minutes: the recipe of config5
+    (L ~ N(0, 3^2), D = L + N(0, sigma^2), both rounded to bf16, drafts by
+    Gumbel-max on the bf16 draft rows at T = 1, uniforms U[0, 1)) from other
+    random streams.  Returns (target, draft, tokens, uniforms) torch tensors."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(np.random.SeedSequence([seed, B, k, int(round(sigma * 100))]).generate_state(1)[0]))
+    target = (torch.randn((B, k + 1, V), generator=g, device=device) * 3.0)
+    draft = (target[:, :k] + sigma * torch.randn((B, k, V), generator=g, device=device)).to(torch.bfloat16)
+    target = target.to(torch.bfloat16)
+    tokens = torch.empty((B, k), dtype=torch.int32, device=device)
+    for b in range(B):  # one sequence at a time keeps the noise buffer small
+        u = torch.rand((k, V), generator=g, device=device, dtype=torch.float64).clamp_min(1e-300)
+        score = draft[b].double() - torch.log(-torch.log(u))
+        tokens[b] = score.argmax(dim=-1).to(torch.int32)
+    uniforms = torch.rand((B, k + 2), generator=g, device=device, dtype=torch.float32)
+    return target, draft, tokens, uniforms
+
+
 C5_BATCHES = (1, 4, 16, 64, 128, 256)
 C5_DRAFTS = (1, 2, 4, 8, 12)
 C5_SIGMAS = (0.5, 2.0, 4.0)
