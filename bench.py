@@ -507,6 +507,10 @@ def run_sweep(args):
                 us_s, out = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
                                                                 stream=stream, want_probs=False))
                 n = out[1].cpu().numpy().astype(np.int64)
+                prev = sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_ROWS)
+                us_r, rout = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
+                                                                 stream=stream, want_probs=False))
+                sv.spec_sample_launch_mode(prev)
                 us_g, gout = timed(lambda: sv.spec_verify_greedy(t, x, workspace=ws, stream=stream))
                 gn = gout[1].cpu().numpy()
                 sb, gb = B * (2 * k + 1) * V * 2, B * (k + 1) * V * 2
@@ -516,6 +520,8 @@ def run_sweep(args):
                                "GB/s": sb / us_s / 1e3, "frac": sb / us_s / 1e3 / peak,
                                "mal": float(n.mean()), "accepted": int(n.sum()),
                                "tests": int(np.minimum(n + 1, k).sum())},
+                    "sample_rows": {"us": us_r, "GB/s": sb / us_r / 1e3, "frac": sb / us_r / 1e3 / peak,
+                                    "what": "the same call with SPEC_LAUNCH_ROWS (one CTA per row)"},
                     "greedy": {"us": us_g, "positions_per_s": B * k / us_g * 1e6, "sequences_per_s": B / us_g * 1e6,
                                "GB/s": gb / us_g / 1e3, "frac": gb / us_g / 1e3 / peak, "mal": float(gn.mean())},
                 })

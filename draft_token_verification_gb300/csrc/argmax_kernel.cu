@@ -31,6 +31,13 @@ namespace {
 
 constexpr int kUnroll = 8;  // 16-byte loads in flight per thread
 
+// NaN-propagating maximum of two bf16 pairs.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
@@ -208,9 +215,15 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
         for (int u = 0; u < kUnroll; ++u) {
           const int v = v0 + u * kThreads;
           if (v < v_hi) {
-            float vm = E::value(E::bits_of(x[u], 0));
+            float vm;
+            if constexpr (DT == DT_BF16) {  // packed: three bf16x2 maxima, then the two halves
+              const uint32_t m2 = bmax2_nan(bmax2_nan(x[u].x, x[u].y), bmax2_nan(x[u].z, x[u].w));
+              vm = max_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+            } else {
+              vm = E::value(E::bits_of(x[u], 0));
 #pragma unroll
-            for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x[u], j)));
+              for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x[u], j)));
+            }
             if (vm != vm) {
               nan_seen = 1u;
             } else if (best_pos < 0 || vm > best) {
