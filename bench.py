@@ -273,6 +273,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     sv.build()
+    if args.sample_launch == "rows":
+        sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_ROWS)
     s, t = make_inputs(seed_offset=rank)
     d = {
         "target": to_torch(s.target, dev), "draft": to_torch(s.draft, dev), "tokens": to_torch(s.tokens, dev),
@@ -307,21 +309,24 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
 
     def step(ev=None, inputs=d):
+        # events bracket each verification call alone; the KV keep lists run between them
         if ev is not None:
             ev[0].record(stream)
         sv.spec_verify_sample(inputs["target"], inputs["draft"], inputs["tokens"], inputs["uniforms"], SAMPLE["T"],
                               SAMPLE["top_k"], SAMPLE["top_p"], None, o["tok"], o["n"], o["p"], o["q"], ws, stream)
-        kv_compact(None, o["n"], kv["sbase"], "s", B, k + 1)
         if ev is not None:
             ev[1].record(stream)
-        sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws, stream)
+        kv_compact(None, o["n"], kv["sbase"], "s", B, k + 1)
         if ev is not None:
             ev[2].record(stream)
-        sv.spec_verify_tree_greedy(inputs["tree_logits"], inputs["tree_tokens"], inputs["parents"], TREE["depth"],
-                                   o["ttok"], o["tpath"], o["tn"], ws, stream)
-        kv_compact(o["tpath"], o["tn"], kv["tbase"], "t", t.B, t.max_depth + 2)
+        sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws, stream)
         if ev is not None:
             ev[3].record(stream)
+        sv.spec_verify_tree_greedy(inputs["tree_logits"], inputs["tree_tokens"], inputs["parents"], TREE["depth"],
+                                   o["ttok"], o["tpath"], o["tn"], ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        kv_compact(o["tpath"], o["tn"], kv["tbase"], "t", t.B, t.max_depth + 2)
 
     dist = world > 1
     if dist:
@@ -332,7 +337,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     status = sv.spec_get_status(ws)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if dist:
         tdist.barrier()
@@ -350,7 +355,7 @@ def run_gpu(args, rank, world):
     if dist:
         tdist.barrier()
     elapsed_ms = start.elapsed_time(end)
-    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])] for e in evs])
+    per = np.array([[e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3]), e[3].elapsed_time(e[4])] for e in evs])
     if dist:
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
@@ -572,6 +577,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the V=152064 sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
+    ap.add_argument("--sample-launch", default="fused", choices=["fused", "rows"],
+                    help="sampling kernels: fused stream + tail items (default) or one CTA per row")
     ap.add_argument("--target-params", type=float, default=8.03e9,
                     help="target model parameters for the gamma scan (default: an 8B target)")
     ap.add_argument("--draft-cost", type=float, default=0.05,
@@ -630,13 +637,17 @@ def main():
             "tree": TREE["B"] / (float(per[:, 2].mean()) / 1e3),
             "what": "sequences (chains or trees) verified per second: the whole step (64 sampled + 64 greedy "
                     "chains + 8 trees per GPU), and each kernel alone from its own events"},
-        "gpu_launches": 6 * K,  # sampling: fused stream+tail and draw kernels; greedy; tree; two KV keep lists
+        # sampling: fused stream+tail and draw kernels (rows: one row kernel); greedy; tree; two KV keep lists
+        "gpu_launches": (6 if args.sample_launch == "fused" else 5) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic("sample"), "kernel": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together",
+                     "traffic": recorded_traffic("sample") if args.sample_launch == "fused" else None,
+                     "kernel": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together"
+                     if args.sample_launch == "fused" else "sampling verify: row_kernel<bf16> (one CTA per row)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels": {
             "sample": {"us": t_sample * 1e6, "GB/s": achieved, "frac": achieved / peak,
-                       "algorithmic_bytes": sample_bytes(), "traffic": recorded_traffic("sample")},
+                       "algorithmic_bytes": sample_bytes(),
+                       "traffic": recorded_traffic("sample") if args.sample_launch == "fused" else None},
             "greedy": {"us": float(per[:, 1].mean()) * 1e3,
                        "GB/s": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9,
                        "frac": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9 / peak,
@@ -666,6 +677,7 @@ def main():
                     "what": "spec_kv_compact after the sampled chains and after the trees, inside every step"},
         "status_bits": r["status"],
     }
+    line["config"]["sample_launch"] = args.sample_launch
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

@@ -29,6 +29,9 @@ def _greedy_case(B, k, V, dtype, seed, quantize=None, agree=0.7):
     (1, 4, 32000, W.F32, None), (16, 5, 32000, W.BF16, None), (64, 8, 128256, W.BF16, None),
     (7, 3, 1, W.BF16, None), (9, 2, 7, W.F32, None), (5, 31, 33, W.BF16, 1.0), (12, 6, 1001, W.BF16, 0.5),
     (4, 12, 152064, W.BF16, None), (256, 1, 152064, W.BF16, None), (3, 4, 100003, W.F32, 1.0),
+    # aligned rows of a few vectors (many row pieces per CTA) and rows one vector past a
+    # shared-memory stage (a chunk cut at every row's end)
+    (40, 3, 64, W.BF16, 1.0), (33, 7, 4104, W.BF16, 1.0), (10, 2, 2052, W.F32, 0.5), (2, 3, 8, W.BF16, None),
 ])
 def test_greedy_parity(B, k, V, dtype, quantize):
     target, tokens = _greedy_case(B, k, V, dtype, seed=B * 100 + k, quantize=quantize)
@@ -76,6 +79,7 @@ def test_config4_tree_full_size():
 @pytest.mark.parametrize("B,N,V,depth,dtype,quantize,children", [
     (5, 1, 100, 1, W.BF16, None, 4), (7, 2, 9, 1, W.F32, None, 4), (6, 40, 50, 6, W.BF16, 1.0, 4),
     (4, 1024, 300, 12, W.BF16, 1.0, 3), (3, 200, 20000, 8, W.F32, None, 2), (8, 60, 128256, 6, W.BF16, 2.0, 4),
+    (5, 100, 64, 6, W.BF16, 1.0, 4), (3, 30, 4104, 6, W.F32, 1.0, 3),
 ])
 def test_tree_parity(B, N, V, depth, dtype, quantize, children):
     case = W.random_tree_case(B, N, V, depth, seed=N + V, dtype=dtype, quantize=quantize, max_children=children)
