@@ -273,8 +273,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     sv.build()
-    if args.sample_launch == "rows":
-        sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_ROWS)
+    sv.spec_sample_launch_mode({"auto": sv.SPEC_LAUNCH_AUTO, "fused": sv.SPEC_LAUNCH_FUSED, "rows": sv.SPEC_LAUNCH_ROWS,
+                                "split": sv.SPEC_LAUNCH_SPLIT}[args.sample_launch])
     s, t = make_inputs(seed_offset=rank)
     d = {
         "target": to_torch(s.target, dev), "draft": to_torch(s.draft, dev), "tokens": to_torch(s.tokens, dev),
@@ -515,6 +515,9 @@ def run_sweep(args):
                 prev = sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_ROWS)
                 us_r, rout = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
                                                                  stream=stream, want_probs=False))
+                sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_FUSED)
+                us_f, fout = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
+                                                                 stream=stream, want_probs=False))
                 sv.spec_sample_launch_mode(prev)
                 us_g, gout = timed(lambda: sv.spec_verify_greedy(t, x, workspace=ws, stream=stream))
                 gn = gout[1].cpu().numpy()
@@ -527,6 +530,8 @@ def run_sweep(args):
                                "tests": int(np.minimum(n + 1, k).sum())},
                     "sample_rows": {"us": us_r, "GB/s": sb / us_r / 1e3, "frac": sb / us_r / 1e3 / peak,
                                     "what": "the same call with SPEC_LAUNCH_ROWS (one CTA per row)"},
+                    "sample_fused": {"us": us_f, "GB/s": sb / us_f / 1e3, "frac": sb / us_f / 1e3 / peak,
+                                     "what": "the same call with SPEC_LAUNCH_FUSED (stream + tail items, draw)"},
                     "greedy": {"us": us_g, "positions_per_s": B * k / us_g * 1e6, "sequences_per_s": B / us_g * 1e6,
                                "GB/s": gb / us_g / 1e3, "frac": gb / us_g / 1e3 / peak, "mal": float(gn.mean())},
                 })
@@ -577,8 +582,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the V=152064 sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
-    ap.add_argument("--sample-launch", default="fused", choices=["fused", "rows"],
-                    help="sampling kernels: fused stream + tail items (default) or one CTA per row")
+    ap.add_argument("--sample-launch", default="auto", choices=["auto", "fused", "rows", "split"],
+                    help="sampling kernels: the library's choice per call (default), fused stream + tail items, "
+                         "one CTA per row, or stream / row / draw launches")
     ap.add_argument("--target-params", type=float, default=8.03e9,
                     help="target model parameters for the gamma scan (default: an 8B target)")
     ap.add_argument("--draft-cost", type=float, default=0.05,
@@ -619,6 +625,8 @@ def main():
         return
     K = args.steps
     per = r["per"]
+    # the step's sampling call: top-p 0.9 with one temperature, which the library's own choice runs fused
+    step_launch = "fused" if args.sample_launch == "auto" else args.sample_launch
     pos = positions_per_step() * world
     value = job_rate(positions_per_step(), world, K, r["elapsed_ms"])
     peak, peak_kind = measured_peaks()
@@ -638,16 +646,18 @@ def main():
             "what": "sequences (chains or trees) verified per second: the whole step (64 sampled + 64 greedy "
                     "chains + 8 trees per GPU), and each kernel alone from its own events"},
         # sampling: fused stream+tail and draw kernels (rows: one row kernel); greedy; tree; two KV keep lists
-        "gpu_launches": (6 if args.sample_launch == "fused" else 5) * K,
+        "gpu_launches": {"fused": 6, "rows": 5, "split": 7}[step_launch] * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic("sample") if args.sample_launch == "fused" else None,
-                     "kernel": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together"
-                     if args.sample_launch == "fused" else "sampling verify: row_kernel<bf16> (one CTA per row)",
+                     "traffic": recorded_traffic("sample") if step_launch == "fused" else None,
+                     "kernel": {"fused": "sampling verify: fused_kernel (stream + tail) + draw_kernel<bf16>, timed together",
+                                "rows": "sampling verify: row_kernel<bf16> (one CTA per row)",
+                                "split": "sampling verify: split_stream_kernel + split_row_kernel + "
+                                         "split_draw_kernel<bf16>, timed together"}[step_launch],
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels": {
             "sample": {"us": t_sample * 1e6, "GB/s": achieved, "frac": achieved / peak,
                        "algorithmic_bytes": sample_bytes(),
-                       "traffic": recorded_traffic("sample") if args.sample_launch == "fused" else None},
+                       "traffic": recorded_traffic("sample") if step_launch == "fused" else None},
             "greedy": {"us": float(per[:, 1].mean()) * 1e3,
                        "GB/s": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9,
                        "frac": greedy_bytes() / (float(per[:, 1].mean()) / 1e3) / 1e9 / peak,
@@ -668,7 +678,8 @@ def main():
                 "us": r["per_seq_t"][0], "GB/s": sample_bytes() / r["per_seq_t"][0] / 1e3,
                 "frac": sample_bytes() / r["per_seq_t"][0] / 1e3 / peak,
                 "sequences_per_s": SAMPLE["B"] / (r["per_seq_t"][0] / 1e6), "mean_accepted": r["per_seq_t"][1],
-                "what": "the step's sampling workload with T_b ~ U(0.5, 1.2) per sequence, timed alone "
+                "what": "the step's sampling workload with T_b ~ U(0.5, 1.2) per sequence (the library's choice "
+                        "for a temperature per sequence: the split launch), timed alone "
                         "(median of 20; rows exceed L2)"},
         },
         "acceptance": {"sample_mal": r["mal"], "greedy_mal": r["greedy_mal"], "k": SAMPLE["k"]},
@@ -677,7 +688,7 @@ def main():
                     "what": "spec_kv_compact after the sampled chains and after the trees, inside every step"},
         "status_bits": r["status"],
     }
-    line["config"]["sample_launch"] = args.sample_launch
+    line["config"]["sample_launch"] = args.sample_launch + (" (fused for this call)" if args.sample_launch == "auto" else "")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

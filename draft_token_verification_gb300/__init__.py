@@ -58,6 +58,8 @@ SPEC_LAUNCH_SEPARATE = 0
 SPEC_LAUNCH_FUSED = 1
 SPEC_LAUNCH_FUSED_WAIT_TEST = 2
 SPEC_LAUNCH_ROWS = 3
+SPEC_LAUNCH_SPLIT = 4
+SPEC_LAUNCH_AUTO = 5
 
 
 class SpecSamplingParams(ctypes.Structure):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "sample_kernel.cu", "argmax_kernel.cu", "tree_sample_kernel.cu", "kv_kernel.cu", "row_kernel.cu"]
+SOURCES = ["api.cu", "sample_kernel.cu", "argmax_kernel.cu", "tree_sample_kernel.cu", "kv_kernel.cu", "row_kernel.cu", "split_kernel.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -15,7 +15,7 @@ using namespace specv;
 
 namespace {
 
-std::atomic<int> g_launch_mode{SPEC_LAUNCH_FUSED};
+std::atomic<int> g_launch_mode{SPEC_LAUNCH_AUTO};
 
 bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 size_t elt_bytes(spec_dtype d) { return d == SPEC_BF16 ? 2 : 4; }
@@ -36,7 +36,8 @@ int check_workspace(void* ws, size_t bytes, int B, int k) {
 
 int run_sample(const void* target, const void* draft, const int32_t* tokens, const float* uniforms, int B, int k,
                int V, spec_dtype dtype, const spec_sampling_params* sp, int32_t* out_tokens, int32_t* out_n,
-               float* out_p, float* out_q, float* out_probs, void* ws, size_t ws_bytes, void* stream, int mode) {
+               float* out_p, float* out_q, float* out_probs, void* ws, size_t ws_bytes, void* stream, int mode,
+               bool auto_split) {
   if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
   if (!sp || !target || B < 1 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
   if (mode == MODE_SAMPLE) {
@@ -82,6 +83,12 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.csums = reinterpret_cast<float*>(w + L.csums);
   a.work = reinterpret_cast<uint32_t*>(w + L.work);
   a.launch_mode = g_launch_mode.load();
+  if (a.launch_mode == SPEC_LAUNCH_AUTO) {
+    // the split launch where the nucleus reaches deep below the row maximum
+    // (top-p >= 0.95) or the temperature varies per sequence; else fused
+    const bool deep = a.top_p >= 0.95f && a.top_p < 1.f;
+    a.launch_mode = (auto_split && (deep || a.temperature_per_seq)) ? SPEC_LAUNCH_SPLIT : SPEC_LAUNCH_FUSED;
+  }
   a.done = reinterpret_cast<uint32_t*>(w + L.done);
   // the draw at the first rejection: a few chunks over listed vectors, more
   // over whole rows (no filter)
@@ -90,6 +97,14 @@ int run_sample(const void* target, const void* draft, const int32_t* tokens, con
   a.aligned_draft = draft ? rows_aligned(draft, V, dtype) : 0;
   a.mode = mode;
   const int dt = dtype == SPEC_BF16 ? DT_BF16 : DT_F32;
+  if (a.launch_mode == SPEC_LAUNCH_SPLIT) {
+    if (split_supported(a, dt)) {
+      const int e = launch_split(a, dt, stream);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
+      return SPEC_OK;
+    }
+    a.launch_mode = SPEC_LAUNCH_FUSED;
+  }
   const bool rows = a.launch_mode == SPEC_LAUNCH_ROWS || a.launch_mode == SPEC_LAUNCH_FUSED_WAIT_TEST;
   if (rows && row_supported(a, dt)) {
     a.poll_limit = 64;  // (used only by the failure-detection mode)
@@ -158,7 +173,7 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, cons
                        void* cuda_stream) {
   return run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                     out_num_accepted, out_p_draft, out_q_draft, nullptr, workspace, workspace_bytes, cuda_stream,
-                    MODE_SAMPLE);
+                    MODE_SAMPLE, true);
 }
 
 int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
@@ -180,7 +195,7 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
   if (cudaMemsetAsync(scratch, 0, L.hdrs, st) != cudaSuccess) return SPEC_ERR_LAUNCH;
   rc = run_sample(target_logits, draft_logits, draft_tokens, uniforms, B, k, V, dtype, params, out_tokens,
                   out_num_accepted, out_p_draft, out_q_draft, nullptr, scratch, kNoAllocBytes, cuda_stream,
-                  MODE_SAMPLE);
+                  MODE_SAMPLE, false);
   if (rc != SPEC_OK) return rc;
   if (out_status && cudaMemcpyAsync(out_status, scratch + L.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
                                     st) != cudaSuccess)
@@ -190,7 +205,7 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
 
 int spec_sample_launch_mode(int mode) {
   if (mode != SPEC_LAUNCH_FUSED && mode != SPEC_LAUNCH_SEPARATE && mode != SPEC_LAUNCH_FUSED_WAIT_TEST &&
-      mode != SPEC_LAUNCH_ROWS)
+      mode != SPEC_LAUNCH_ROWS && mode != SPEC_LAUNCH_SPLIT && mode != SPEC_LAUNCH_AUTO)
     return SPEC_ERR_INVALID_ARG;
   return g_launch_mode.exchange(mode);
 }
@@ -229,7 +244,7 @@ int spec_kv_compact(const int32_t* path, int path_stride, const int32_t* num_acc
 int spec_transform_probs(const void* logits, int R, int V, spec_dtype dtype, const spec_sampling_params* params,
                          float* out_probs, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return run_sample(logits, nullptr, nullptr, nullptr, R, 0, V, dtype, params, nullptr, nullptr, nullptr, nullptr,
-                    out_probs, workspace, workspace_bytes, cuda_stream, MODE_PROBS);
+                    out_probs, workspace, workspace_bytes, cuda_stream, MODE_PROBS, false);
 }
 
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int k, int V,

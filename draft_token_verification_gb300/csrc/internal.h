@@ -184,6 +184,7 @@ struct SampleArgs {
   int aligned_target;          // rows start on 16-byte boundaries
   int aligned_draft;
   int mode;
+  int split_grid;              // split launch: CTAs of the stream kernel
 };
 
 struct TreeSampleArgs {
@@ -249,6 +250,8 @@ int launch_kv_compact(const KvArgs& a, void* stream);
 // bulk-copy stages: bf16 rows with or without a filter, f32 rows without one.
 bool row_supported(const SampleArgs& a, int dtype);
 int launch_rows(const SampleArgs& a, int dtype, void* stream);
+bool split_supported(const SampleArgs& a, int dtype);
+int launch_split(SampleArgs a, int dtype, void* stream);
 // Shared-memory bytes of one tree-sampling CTA for slice `slice`.
 size_t tree_smem_bytes(int dtype, int slice);
 size_t sample_smem_bytes(int dtype, bool filter);

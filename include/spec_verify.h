@@ -358,7 +358,27 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
  *                         fused launch where the kept set is wide
  *                         (top-p near 1 over flat rows) or the temperature
  *                         varies per sequence.
- *   SPEC_LAUNCH_FUSED     (the default) one cooperative launch whose CTAs
+ *   SPEC_LAUNCH_AUTO      (the default) SPEC_LAUNCH_SPLIT for calls whose
+ *                         nucleus reaches deep below the row maximum
+ *                         (0.95 <= top_p < 1) or whose temperature varies per
+ *                         sequence, where the split launch is the faster one;
+ *                         SPEC_LAUNCH_FUSED for the others.  For
+ *                         spec_verify_sample_noalloc and spec_transform_probs
+ *                         it means SPEC_LAUNCH_FUSED.
+ *   SPEC_LAUNCH_SPLIT     three launches: a stream kernel reads every row
+ *                         once in one wave of equal ranges, keeping per row
+ *                         piece its maximum, its softmax mass and exact
+ *                         counts of the 512 bf16 values below its maximum;
+ *                         a row kernel merges the pieces and decides each
+ *                         row's kept set and p(x) or q(x) (searching the row
+ *                         again when the cut lies below those 512 values);
+ *                         a draw kernel (one 8-CTA cluster per sequence)
+ *                         finds n and draws at n from the two rows.  Used
+ *                         for rows that start on 16-byte boundaries and hold
+ *                         whole 16-byte vectors, bf16 with or without a
+ *                         filter and f32 without one; other calls take
+ *                         SPEC_LAUNCH_FUSED.
+ *   SPEC_LAUNCH_FUSED     one cooperative launch whose CTAs
  *                         take every row's stream part, then every row's
  *                         tail part (the separate launches stand in when the
  *                         GPU refuses it)
@@ -378,6 +398,8 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
 #define SPEC_LAUNCH_SEPARATE 0
 #define SPEC_LAUNCH_FUSED_WAIT_TEST 2
 #define SPEC_LAUNCH_ROWS 3
+#define SPEC_LAUNCH_SPLIT 4
+#define SPEC_LAUNCH_AUTO 5
 int spec_sample_launch_mode(int mode);
 
 /* Static description of a return code. */
