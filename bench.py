@@ -503,11 +503,17 @@ def run_sweep(args):
     points = []
     clocks = ClockSampler(0)
     clocks.start()
+    only = None
+    if args.sweep_points:
+        only = {(int(b), int(kk), float(sg)) for b, kk, sg in (p.split(":") for p in args.sweep_points.split(","))}
     for sigma in W.C5_SIGMAS:
         for k in W.C5_DRAFTS:
-            Bmax = max(W.C5_BATCHES)
+            batches = [B for B in W.C5_BATCHES if only is None or (B, k, float(sigma)) in only]
+            if not batches:
+                continue
+            Bmax = max(batches)
             tgt, drf, tok, uni = W.config5_device(Bmax, k, sigma, device=dev, V=V)
-            for B in W.C5_BATCHES:
+            for B in batches:
                 t, d, x, u = tgt[:B], drf[:B], tok[:B], uni[:B]
                 us_s, out = timed(lambda: sv.spec_verify_sample(t, d, x, u, 1.0, 0, 0.95, None, workspace=ws,
                                                                 stream=stream, want_probs=False))
@@ -544,9 +550,12 @@ def run_sweep(args):
     t_target_us = 2.0 * args.target_params / (peak * 1e9) * 1e6
     scan = []
     for B in W.C5_BATCHES:
-        ks = np.array(W.C5_DRAFTS, float)
+        kdone = [k for k in W.C5_DRAFTS if any(p["B"] == B and p["k"] == k for p in points)]
+        if len(kdone) < 2:  # (a partial sweep: no fit for this batch)
+            continue
+        ks = np.array(kdone, float)
         us = np.array([np.median([p["sample"]["us"] for p in points if p["B"] == B and p["k"] == k])
-                       for k in W.C5_DRAFTS])
+                       for k in kdone])
         b, a = np.polyfit(ks, us, 1)  # us = a + b k
         for sigma in W.C5_SIGMAS:
             sel = [p for p in points if p["B"] == B and p["sigma"] == sigma]
@@ -582,6 +591,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the V=152064 sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
+    ap.add_argument("--sweep-points", default=None,
+                    help="only these sweep points, as B:k:sigma separated by commas (e.g. 64:8:2,256:12:4)")
     ap.add_argument("--sample-launch", default="auto", choices=["auto", "fused", "rows", "split"],
                     help="sampling kernels: the library's choice per call (default), fused stream + tail items, "
                          "one CTA per row, or stream / row / draw launches")
