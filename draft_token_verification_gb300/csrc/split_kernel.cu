@@ -988,6 +988,12 @@ struct DrawShm {
   uint32_t wt[kDrawWarps][2];  // per warp: tokens of the cut keys
   DF ws[kDrawWarps];           // per warp: residual mass
   float pick_hi, pick_lo;  // residual mass before the picked warp
+  float all_hi[kDrawCl], all_lo[kDrawCl];  // every CTA's residual mass
+  // per warp: vectors that hold a token of P's kept set, in index order, with
+  // the ranks of their first cut-key tokens (slice vector, rank in P, rank in Q)
+  uint32_t lv[kDrawWarps][64];
+  uint32_t lr[kDrawWarps][64][2];
+  uint32_t cta_ties[2];    // cut-key tokens before this CTA
   int n;
   int pick_warp;
   int token;
@@ -1027,10 +1033,51 @@ __device__ __forceinline__ void pair_weights(const uint4& vp_, const uint4& vq_,
 template <int DT>
 __device__ __forceinline__ uint32_t ties_of(const uint4& v, uint32_t kstar) {
   using E = Elt<DT>;
-  uint32_t n = 0u;
+  if constexpr (DT == DT_BF16) {
+    // tokens whose value equals the cut value: equal 16-bit patterns, and
+    // for the value 0 both signed zeros
+    const uint32_t kb = E::bits_of_key(kstar);
+    const uint32_t k2 = kb | (kb << 16);
+    const bool zero = (kb & 0x7FFFu) == 0u;
+    uint32_t n = 0u;
 #pragma unroll
-  for (int j = 0; j < E::kPerVec; ++j) n += E::key(E::bits_of(v, j)) == kstar ? 1u : 0u;
-  return n;
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t wd = word_of(v, w);
+      uint32_t eq = __vcmpeq2(wd, k2);
+      if (zero) eq |= __vcmpeq2(wd, 0u) | __vcmpeq2(wd, 0x80008000u);
+      n += __popc(eq);
+    }
+    return n >> 4;
+  } else {
+    uint32_t n = 0u;
+#pragma unroll
+    for (int j = 0; j < E::kPerVec; ++j) n += E::key(E::bits_of(v, j)) == kstar ? 1u : 0u;
+    return n;
+  }
+}
+
+// Exclusive ranks of this lane's cut-key tokens within one round of 32
+// vectors (one per lane), both rows packed 16 + 16 bits, and the round's
+// totals: a ballot when no lane holds more than one, else a scan.
+__device__ __forceinline__ void round_ranks(uint32_t lp, uint32_t lq, uint32_t& ep, uint32_t& eq, uint32_t& tp,
+                                            uint32_t& tq) {
+  const int lane = threadIdx.x & 31;
+  if (__any_sync(kFullMask, lp > 1u || lq > 1u)) {
+    const uint32_t both = lp | (lq << 16);
+    const uint32_t incl = warp_incl_scan_u(both);
+    const uint32_t ex = incl - both, tot = __shfl_sync(kFullMask, incl, 31);
+    ep = ex & 0xFFFFu;
+    eq = ex >> 16;
+    tp = tot & 0xFFFFu;
+    tq = tot >> 16;
+  } else {
+    const unsigned bp = __ballot_sync(kFullMask, lp != 0u), bq = __ballot_sync(kFullMask, lq != 0u);
+    const unsigned lt = (1u << lane) - 1u;
+    ep = __popc(bp & lt);
+    eq = __popc(bq & lt);
+    tp = __popc(bp);
+    tq = __popc(bq);
+  }
 }
 
 // Largest value of a 16-byte vector (NaN-propagating).
@@ -1042,6 +1089,65 @@ __device__ __forceinline__ float vec_max(const uint4& v) {
   } else {
     return max_nan(max_nan(__uint_as_float(v.x), __uint_as_float(v.y)), max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
+}
+
+// Walks a warp's segment [s0, s1) of the slice in rounds of 32 vectors,
+// keeping the ranks of the two cut keys' tokens in index order, and lists the
+// vectors that can hold a token of P's kept set (maximum at or above pcut);
+// every 32 listed vectors (and the rest at the end) go to f(n, v, rp, rq) as
+// one batch, lane l holding the l-th (v: slice vector; rp, rq: ranks of its
+// first cut-key tokens) if l < n.  f returns true to stop.  The weights of the
+// other vectors are 0, so only the listed ones are evaluated.
+template <int DT, typename F>
+__device__ __forceinline__ void walk_listed(uint32_t* lv, uint32_t (*lr)[2], uint32_t sp, uint32_t sq, int s0, int s1,
+                                            bool pt, bool qt, const SRow& P, const SRow& Q, bool use_q, float pcut,
+                                            uint32_t rp, uint32_t rq, F&& f) {
+  const int lane = threadIdx.x & 31;
+  int cnt = 0;
+  bool stop = false;
+  for (int v0 = s0; v0 < s1 && !stop; v0 += 32) {
+    const int v = v0 + lane;
+    uint32_t lp = 0u, lq = 0u;
+    bool keep = false;
+    if (v < s1) {
+      const uint4 xp = lds128(sp + 16u * v);
+      if (pt) lp = ties_of<DT>(xp, P.kstar);
+      if (use_q && qt) lq = ties_of<DT>(lds128(sq + 16u * v), Q.kstar);
+      keep = vec_max<DT>(xp) >= pcut;
+    }
+    uint32_t ep = 0u, eq = 0u, tp = 0u, tq = 0u;
+    if (pt || qt) round_ranks(lp, lq, ep, eq, tp, tq);
+    const unsigned bal = __ballot_sync(kFullMask, keep);
+    if (keep) {
+      const int o = cnt + __popc(bal & ((1u << lane) - 1u));
+      lv[o] = static_cast<uint32_t>(v);
+      lr[o][0] = rp + ep;
+      lr[o][1] = rq + eq;
+    }
+    cnt += __popc(bal);
+    rp += tp;
+    rq += tq;
+    __syncwarp();
+    if (cnt >= 32) {
+      const bool in = true;
+      stop = f(32, in ? lv[lane] : 0u, lr[lane][0], lr[lane][1]);
+      __syncwarp();
+      cnt -= 32;
+      if (lane < cnt) {  // (at most 31 left: move them to the front)
+        const uint32_t a0 = lv[32 + lane], a1 = lr[32 + lane][0], a2 = lr[32 + lane][1];
+        __syncwarp(__activemask());
+        lv[lane] = a0;
+        lr[lane][0] = a1;
+        lr[lane][1] = a2;
+      }
+      __syncwarp();
+    }
+  }
+  if (!stop && cnt > 0) {
+    const uint32_t a0 = lane < cnt ? lv[lane] : 0u, a1 = lane < cnt ? lr[lane][0] : 0u, a2 = lane < cnt ? lr[lane][1] : 0u;
+    f(cnt, a0, a1, a2);
+  }
+  __syncwarp();
 }
 
 // Vectors of a CTA's slice (the largest slice of the cluster).
@@ -1148,10 +1254,18 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
   }
   cluster.sync();
   if (ties) {
-    for (int r = 0; r < rank; ++r) {
-      base_p += ld_cluster_u32(mapa_shared(smem_addr(&sh.ties[0]), static_cast<uint32_t>(r)));
-      base_q += ld_cluster_u32(mapa_shared(smem_addr(&sh.ties[1]), static_cast<uint32_t>(r)));
+    if (tid == 0) {  // the tokens before this CTA, read once from the cluster
+      uint32_t cp = 0u, cq = 0u;
+      for (int r = 0; r < rank; ++r) {
+        cp += ld_cluster_u32(mapa_shared(smem_addr(&sh.ties[0]), static_cast<uint32_t>(r)));
+        cq += ld_cluster_u32(mapa_shared(smem_addr(&sh.ties[1]), static_cast<uint32_t>(r)));
+      }
+      sh.cta_ties[0] = cp;
+      sh.cta_ties[1] = cq;
     }
+    __syncthreads();
+    base_p = sh.cta_ties[0];
+    base_q = sh.cta_ties[1];
     for (int w = 0; w < warp; ++w) {
       base_p += sh.wt[w][0];
       base_q += sh.wt[w][1];
@@ -1165,29 +1279,20 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
   for (int pass = 0; pass < 2; ++pass) {
     DF wsum = df_make(0.f);
     if (!bad) {
-      uint32_t rp = base_p, rq = base_q;
-      for (int v0 = s0; v0 < s1; v0 += 32) {
-        const int v = v0 + lane;
-        float ls = 0.f;
-        uint32_t lp = 0u, lq = 0u;
-        uint4 xp = make_uint4(0u, 0u, 0u, 0u), xq = xp;
-        if (v < s1) {
-          xp = lds128(sp + 16u * v);
-          if (mode == 1) xq = lds128(sq + 16u * v);
-          if (pt) lp = ties_of<DT>(xp, P.kstar);
-          if (mode == 1 && qt) lq = ties_of<DT>(xq, Q.kstar);
-        }
-        const uint32_t ip = warp_incl_scan_u(lp), iq = warp_incl_scan_u(lq);
-        if (v < s1 && vec_max<DT>(xp) >= pcut) {
-          float w[PV];
-          pair_weights<DT>(xp, xq, P, Q, mode == 1, rp + ip - lp, rq + iq - lq, w);
+      walk_listed<DT>(sh.lv[warp], sh.lr[warp], sp, sq, s0, s1, pt, qt, P, Q, mode == 1, pcut, base_p, base_q,
+                      [&](int nb, uint32_t v, uint32_t rpv, uint32_t rqv) {
+                        if (lane < nb) {
+                          float w[PV];
+                          const uint4 xp = lds128(sp + 16u * v);
+                          const uint4 xq = mode == 1 ? lds128(sq + 16u * v) : xp;
+                          pair_weights<DT>(xp, xq, P, Q, mode == 1, rpv, rqv, w);
+                          float ls = 0.f;
 #pragma unroll
-          for (int j = 0; j < PV; ++j) ls += w[j];
-        }
-        rp += __shfl_sync(kFullMask, ip, 31);
-        rq += __shfl_sync(kFullMask, iq, 31);
-        wsum = df_add(wsum, ls);
-      }
+                          for (int j = 0; j < PV; ++j) ls += w[j];
+                          wsum = df_add(wsum, ls);
+                        }
+                        return false;
+                      });
     }
     wsum = warp_sum_df(wsum);
     if (lane == 0) sh.ws[warp] = wsum;
@@ -1200,11 +1305,15 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
       sh.sum_lo = t.lo;
     }
     cluster.sync();
+    if (tid < kDrawCl) {  // every CTA's mass, read once from the cluster
+      sh.all_hi[tid] = ld_cluster_f32(mapa_shared(smem_addr(&sh.sum_hi), static_cast<uint32_t>(tid)));
+      sh.all_lo[tid] = ld_cluster_f32(mapa_shared(smem_addr(&sh.sum_lo), static_cast<uint32_t>(tid)));
+    }
+    __syncthreads();
     total = df_make(0.f);
     before = df_make(0.f);
     for (int r = 0; r < kDrawCl; ++r) {
-      const DF o{ld_cluster_f32(mapa_shared(smem_addr(&sh.sum_hi), static_cast<uint32_t>(r))),
-                 ld_cluster_f32(mapa_shared(smem_addr(&sh.sum_lo), static_cast<uint32_t>(r)))};
+      const DF o{sh.all_hi[r], sh.all_lo[r]};
       if (r < rank) before = df_add(before, o);
       total = df_add(total, o);
     }
@@ -1224,8 +1333,7 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
   bool mine = !bad && mysum.hi > 0.f && !df_lt(tgt, before) && df_lt(tgt, after);
   if (!bad && mysum.hi > 0.f && !df_lt(tgt, after)) {
     bool later = false;
-    for (int r = rank + 1; r < kDrawCl; ++r)
-      later = later || ld_cluster_f32(mapa_shared(smem_addr(&sh.sum_hi), static_cast<uint32_t>(r))) > 0.f;
+    for (int r = rank + 1; r < kDrawCl; ++r) later = later || sh.all_hi[r] > 0.f;
     mine = !later;
   }
   if (tid == 0) {
@@ -1250,59 +1358,54 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
     __syncthreads();
     if (warp == sh.pick_warp) {
       DF cm{sh.pick_hi, sh.pick_lo};
-      uint32_t rp = base_p, rq = base_q;
       int token = -1, last_tok = -1;  // (last_tok: the last token with mass, for a target past the end)
-      for (int v0 = s0; v0 < s1 && token < 0; v0 += 32) {
-        const int v = v0 + lane;
-        float w[PV];
-        float ls = 0.f;
-        uint32_t lp = 0u, lq = 0u;
-        uint4 xp = make_uint4(0u, 0u, 0u, 0u), xq = xp;
-        if (v < s1) {
-          xp = lds128(sp + 16u * v);
-          if (mode == 1) xq = lds128(sq + 16u * v);
-          if (pt) lp = ties_of<DT>(xp, P.kstar);
-          if (mode == 1 && qt) lq = ties_of<DT>(xq, Q.kstar);
-        }
-        const uint32_t ip = warp_incl_scan_u(lp), iq = warp_incl_scan_u(lq);
+      walk_listed<DT>(sh.lv[warp], sh.lr[warp], sp, sq, s0, s1, pt, qt, P, Q, mode == 1, pcut, base_p, base_q,
+                      [&](int nb, uint32_t v, uint32_t rpv, uint32_t rqv) -> bool {
+                        float w[PV];
 #pragma unroll
-        for (int j = 0; j < PV; ++j) w[j] = 0.f;
-        if (v < s1 && vec_max<DT>(xp) >= pcut) pair_weights<DT>(xp, xq, P, Q, mode == 1, rp + ip - lp, rq + iq - lq, w);
+                        for (int j = 0; j < PV; ++j) w[j] = 0.f;
+                        if (lane < nb) {
+                          const uint4 xp = lds128(sp + 16u * v);
+                          const uint4 xq = mode == 1 ? lds128(sq + 16u * v) : xp;
+                          pair_weights<DT>(xp, xq, P, Q, mode == 1, rpv, rqv, w);
+                        }
+                        float ls = 0.f;
 #pragma unroll
-        for (int j = 0; j < PV; ++j) ls += w[j];
-        rp += __shfl_sync(kFullMask, ip, 31);
-        rq += __shfl_sync(kFullMask, iq, 31);
-        // lanes in index order: the first lane whose running total passes the target
-        const DF li = warp_incl_scan_df(df_make(ls));
-        const DF lend = df_norm(df_add(cm, li));
-        const unsigned hit = __ballot_sync(kFullMask, ls > 0.f && df_lt(tgt, lend));
-        const unsigned any = __ballot_sync(kFullMask, ls > 0.f);
-        if (any) {
-          const int ll = 31 - __clz(any);
-          int lj = -1;
-          for (int j = 0; j < PV; ++j)
-            if (w[j] > 0.f) lj = j;
-          lj = __shfl_sync(kFullMask, lj, ll);
-          last_tok = (c0 + v0 + ll) * PV + lj;
-        }
-        if (hit) {
-          const int pl = __ffs(hit) - 1;
-          if (lane == pl) {
-            DF cc = df_norm(df_add(lend, df_neg(df_make(ls))));  // before this lane
-            int jl = -1;
-            for (int j = 0; j < PV; ++j) {
-              if (w[j] <= 0.f) continue;
-              jl = j;
-              const DF nc = df_norm(df_add(cc, w[j]));
-              if (df_lt(tgt, nc)) break;
-              cc = nc;
-            }
-            token = (c0 + v) * PV + jl;
-          }
-          token = __shfl_sync(kFullMask, token, pl);
-        }
-        cm = df_norm(df_add(cm, shfl_df(li, 31)));
-      }
+                        for (int j = 0; j < PV; ++j) ls += w[j];
+                        // lanes in index order: the first lane whose running total passes the target
+                        const DF li = warp_incl_scan_df(df_make(ls));
+                        const DF lend = df_norm(df_add(cm, li));
+                        const unsigned hit = __ballot_sync(kFullMask, ls > 0.f && df_lt(tgt, lend));
+                        const unsigned any = __ballot_sync(kFullMask, ls > 0.f);
+                        if (any) {
+                          const int ll = 31 - __clz(any);
+                          int lj = -1;
+                          for (int j = 0; j < PV; ++j)
+                            if (w[j] > 0.f) lj = j;
+                          lj = __shfl_sync(kFullMask, lj, ll);
+                          const uint32_t vl = __shfl_sync(kFullMask, v, ll);
+                          last_tok = (c0 + static_cast<int>(vl)) * PV + lj;
+                        }
+                        if (hit) {
+                          const int pl = __ffs(hit) - 1;
+                          if (lane == pl) {
+                            DF cc = df_norm(df_add(lend, df_neg(df_make(ls))));  // before this lane
+                            int jl = -1;
+                            for (int j = 0; j < PV; ++j) {
+                              if (w[j] <= 0.f) continue;
+                              jl = j;
+                              const DF nc = df_norm(df_add(cc, w[j]));
+                              if (df_lt(tgt, nc)) break;
+                              cc = nc;
+                            }
+                            token = (c0 + static_cast<int>(v)) * PV + jl;
+                          }
+                          token = __shfl_sync(kFullMask, token, pl);
+                          return true;
+                        }
+                        cm = df_norm(df_add(cm, shfl_df(li, 31)));
+                        return false;
+                      });
       if (lane == 0) sh.token = token >= 0 ? token : last_tok;
     }
     __syncthreads();
