@@ -301,32 +301,54 @@ def run_gpu(args, rank, world):
         kv[name + "moves"] = torch.empty(rows, dtype=torch.int32, device=dev)
     kv_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def kv_compact(path, n, base, prefix, rows, keep):
+    def kv_compact(path, n, base, prefix, rows, keep, st):
         sv.spec_kv_compact(n, base, path, max_keep=keep, out_status=kv_status, out_src=kv[prefix + "src"],
                            out_dst=kv[prefix + "dst"], out_new_len=kv[prefix + "len"],
-                           out_num_moves=kv[prefix + "moves"], stream=stream)
+                           out_num_moves=kv[prefix + "moves"], stream=st)
     ws = sv.Workspace(dev)
     stream = torch.cuda.current_stream()
+    # --streams 3: the greedy chain and the greedy tree run on streams (and
+    # workspaces) of their own beside the sampling call, joined at the end of
+    # every step
+    ws_g3, ws_t3 = sv.Workspace(dev), sv.Workspace(dev)
+    s_g3, s_t3 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    conc = {"on": args.streams == 3}
 
     def step(ev=None, inputs=d):
-        # events bracket each verification call alone; the KV keep lists run between them
+        # events bracket each verification call alone (on its own stream); the
+        # KV keep lists run between them
+        if conc["on"]:
+            ws_g, ws_t, s_g, s_t = ws_g3, ws_t3, s_g3, s_t3
+        else:
+            ws_g, ws_t, s_g, s_t = ws, ws, stream, stream
+        if conc["on"]:
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            s_g.wait_event(fork)
+            s_t.wait_event(fork)
         if ev is not None:
             ev[0].record(stream)
         sv.spec_verify_sample(inputs["target"], inputs["draft"], inputs["tokens"], inputs["uniforms"], SAMPLE["T"],
                               SAMPLE["top_k"], SAMPLE["top_p"], None, o["tok"], o["n"], o["p"], o["q"], ws, stream)
         if ev is not None:
             ev[1].record(stream)
-        kv_compact(None, o["n"], kv["sbase"], "s", B, k + 1)
+        kv_compact(None, o["n"], kv["sbase"], "s", B, k + 1, stream)
         if ev is not None:
-            ev[2].record(stream)
-        sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws, stream)
+            ev[2].record(s_g)
+        sv.spec_verify_greedy(inputs["greedy_target"], inputs["tokens"], o["gtok"], o["gn"], ws_g, s_g)
         if ev is not None:
-            ev[3].record(stream)
+            ev[3].record(s_g)
+            ev[5].record(s_t)
         sv.spec_verify_tree_greedy(inputs["tree_logits"], inputs["tree_tokens"], inputs["parents"], TREE["depth"],
-                                   o["ttok"], o["tpath"], o["tn"], ws, stream)
+                                   o["ttok"], o["tpath"], o["tn"], ws_t, s_t)
         if ev is not None:
-            ev[4].record(stream)
-        kv_compact(o["tpath"], o["tn"], kv["tbase"], "t", t.B, t.max_depth + 2)
+            ev[4].record(s_t)
+        kv_compact(o["tpath"], o["tn"], kv["tbase"], "t", t.B, t.max_depth + 2, s_t)
+        if conc["on"]:
+            for st in (s_g, s_t):
+                join = torch.cuda.Event()
+                join.record(st)
+                stream.wait_event(join)
 
     dist = world > 1
     if dist:
@@ -337,7 +359,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     status = sv.spec_get_status(ws)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if dist:
         tdist.barrier()
@@ -355,7 +377,25 @@ def run_gpu(args, rank, world):
     if dist:
         tdist.barrier()
     elapsed_ms = start.elapsed_time(end)
-    per = np.array([[e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3]), e[3].elapsed_time(e[4])] for e in evs])
+    per = np.array([[e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3]), e[5].elapsed_time(e[4])] for e in evs])
+    # the same K steps with the other stream layout (reported beside the main line)
+    conc["on"] = args.streams != 3
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    alt0 = torch.cuda.Event(enable_timing=True)
+    alt1 = torch.cuda.Event(enable_timing=True)
+    alt0.record(stream)
+    for i in range(args.steps):
+        step()
+    alt1.record(stream)
+    torch.cuda.synchronize()
+    alt_ms = alt0.elapsed_time(alt1)
+    if dist:
+        alt_ms = max_over_ranks(alt_ms, dev)
+    conc["on"] = args.streams == 3
     if dist:
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
@@ -372,36 +412,56 @@ def run_gpu(args, rank, world):
     h2d = sum(v.numel() * v.element_size() for v in h.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-    def e2e_step():
-        for key, v in h.items():
-            d[key].copy_(v, non_blocking=True)
-        d_in = dict(d)
-        d_in["greedy_target"] = d["target"]
+    # Two sets of device inputs: the next step's host-to-device copy runs on its
+    # own stream while this step verifies (the link, about 210 GB/s here, is the
+    # bound); every step still copies all of its inputs in and its results out.
+    d_sets = [d, {key: torch.empty_like(d[key]) for key in h}]
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step(i):
+        b = i % 2
+        ds = d_sets[b]
+        copy_stream.wait_event(freed[b])  # the set's previous step has finished with it
+        with torch.cuda.stream(copy_stream):
+            for key, v in h.items():
+                ds[key].copy_(v, non_blocking=True)
+        copied[b].record(copy_stream)
+        stream.wait_event(copied[b])
+        d_in = dict(ds)
+        d_in["greedy_target"] = ds["target"]
         step(None, d_in)
+        freed[b].record(stream)
         for key, v in host_out.items():
             v.copy_(o[key], non_blocking=True)
 
-    e2e_step()
+    for ev in freed:
+        ev.record(stream)
+    e2e_step(0)
+    e2e_step(1)
     torch.cuda.synchronize()
     if dist:
         tdist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    for ev in freed:
+        ev.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if dist:
         e2e_ms = max_over_ranks(e2e_ms, dev)
-    status |= sv.spec_get_status(ws)
+    status |= sv.spec_get_status(ws) | sv.spec_get_status(ws_g3) | sv.spec_get_status(ws_t3)
     ts_us, ts_bytes, ts_mal = time_tree_sample(sv, dev, ws, stream, seed=4 + rank)
     status |= sv.spec_get_status(ws)
     tb_us, tb_mal = time_per_seq_temperature(sv, dev, ws, stream, seed=3 + rank)
     status |= sv.spec_get_status(ws) | int(kv_status.item())
 
-    return dict(elapsed_ms=elapsed_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
+    return dict(elapsed_ms=elapsed_ms, alt_ms=alt_ms, per=per, clk=clk, status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
                 h2d=h2d, d2h=d2h, mal=float(n_acc.mean()), greedy_mal=float(gn.mean()),
                 tree_sample=(ts_us, ts_bytes, ts_mal), per_seq_t=(tb_us, tb_mal),
                 kv_moves=int(kv["tmoves"].sum().item()))
@@ -591,6 +651,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the V=152064 sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
+    ap.add_argument("--streams", type=int, default=1, choices=[1, 3],
+                    help="1: the step's calls in order on one stream; 3: greedy chain and greedy tree on streams "
+                         "of their own beside the sampling call")
     ap.add_argument("--sweep-points", default=None,
                     help="only these sweep points, as B:k:sigma separated by commas (e.g. 64:8:2,256:12:4)")
     ap.add_argument("--sample-launch", default="auto", choices=["auto", "fused", "rows", "split"],
@@ -649,7 +712,10 @@ def main():
         "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
         "clocks": r["clk"],
         "e2e": {"value": pos * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "what": "through the C ABI from pinned host buffers: every step copies its inputs in and its results "
+                        "out; the next step's copy (its own stream, a second set of device inputs) overlaps this "
+                        "step's verification"},
         "sequences_per_s": {
             "step": (2 * SAMPLE["B"] + TREE["B"]) * world * K / (r["elapsed_ms"] / 1e3),
             "sample": SAMPLE["B"] / t_sample, "greedy": SAMPLE["B"] / (float(per[:, 1].mean()) / 1e3),
@@ -693,6 +759,12 @@ def main():
                         "for a temperature per sequence: the split launch), timed alone "
                         "(median of 20; rows exceed L2)"},
         },
+        "step_other_streams": {
+            "value": job_rate(positions_per_step(), world, K, r["alt_ms"]), "unit": UNIT,
+            "ms_per_step": r["alt_ms"] / K,
+            "what": ("the same K steps with greedy chain and greedy tree on streams (and workspaces) of their own "
+                     "beside the sampling call, joined at the end of every step" if args.streams == 1 else
+                     "the same K steps with every call in order on one stream")},
         "acceptance": {"sample_mal": r["mal"], "greedy_mal": r["greedy_mal"], "k": SAMPLE["k"]},
         "boundary_rate": boundary_rates(),
         "kv_keep": {"tree_entries_moved_last_step": r["kv_moves"],
@@ -700,6 +772,9 @@ def main():
         "status_bits": r["status"],
     }
     line["config"]["sample_launch"] = args.sample_launch + (" (fused for this call)" if args.sample_launch == "auto" else "")
+    line["config"]["streams"] = ("the step's calls in order on one stream" if args.streams == 1 else
+                                 "greedy chain and greedy tree on streams of their own beside the sampling call, "
+                                 "joined at the end of every step")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))
