@@ -1005,6 +1005,13 @@ __device__ __forceinline__ bool kept_tok(const SRow& r, uint32_t key, uint32_t r
   return r.all_kept || key > r.kstar || (key == r.kstar && rank < static_cast<uint32_t>(r.keep));
 }
 
+// max(0, p - q) of one token from its two masses and the rows' inverse kept
+// masses, rounded step by step (no contraction): the sums over the cluster and
+// the walk to the token use this one function, so they agree bit for bit.
+__device__ __forceinline__ float resid_weight(float mp, float izp, float mq, float izq) {
+  return fmaxf(__fsub_rn(__fmul_rn(mp, izp), __fmul_rn(mq, izq)), 0.f);
+}
+
 // Residual weights of the tokens of one vector pair, in index order; rp / rq:
 // ranks of this vector's first cut-key token in each row.
 template <int DT>
@@ -1018,18 +1025,49 @@ __device__ __forceinline__ void pair_weights(const uint4& vp_, const uint4& vq_,
     const uint32_t kp = E::key(bp);
     const bool kpk = kept_tok(P, kp, rp);
     rp += (kp == P.kstar) ? 1u : 0u;
-    const float p = kpk ? mass(E::value(bp), P.c, nmp) * P.izk : 0.f;
-    float q = 0.f;
+    const float mp = kpk ? mass(E::value(bp), P.c, nmp) : 0.f;
+    float mq = 0.f;
     if (use_q) {
       const uint32_t bq = E::bits_of(vq_, j);
       const uint32_t kq = E::key(bq);
       const bool kqk = kept_tok(Q, kq, rq);
       rq += (kq == Q.kstar) ? 1u : 0u;
-      q = kqk ? mass(E::value(bq), Q.c, nmq) * Q.izk : 0.f;
+      mq = kqk ? mass(E::value(bq), Q.c, nmq) : 0.f;
     }
-    w[j] = fmaxf(p - q, 0.f);
+    w[j] = kpk ? resid_weight(mp, P.izk, mq, Q.izk) : 0.f;
   }
 }
+// Sum of the residual weights of one vector pair (the same values as
+// pair_weights, added in index order): P's kept tokens are found by value
+// first, and only they are weighed.
+template <int DT>
+__device__ __forceinline__ float pair_sum(const uint4& vp_, const uint4& vq_, const SRow& P, const SRow& Q, bool use_q,
+                                          uint32_t rp, uint32_t rq) {
+  using E = Elt<DT>;
+  uint32_t kmask = 0u, qmask = 0u;  // P's kept tokens; Q's kept tokens
+#pragma unroll
+  for (int j = 0; j < E::kPerVec; ++j) {
+    const uint32_t kp = E::key(E::bits_of(vp_, j));
+    kmask |= kept_tok(P, kp, rp) ? (1u << j) : 0u;
+    rp += (kp == P.kstar) ? 1u : 0u;
+    if (use_q) {
+      const uint32_t kq = E::key(E::bits_of(vq_, j));
+      qmask |= kept_tok(Q, kq, rq) ? (1u << j) : 0u;
+      rq += (kq == Q.kstar) ? 1u : 0u;
+    }
+  }
+  const float nmp = -P.m * P.c, nmq = use_q ? -Q.m * Q.c : 0.f;
+  float sum = 0.f;
+  while (kmask) {
+    const int j = __ffs(kmask) - 1;
+    kmask &= kmask - 1u;
+    const float mp = mass(E::value(E::bits_of(vp_, j)), P.c, nmp);
+    const float mq = ((qmask >> j) & 1u) ? mass(E::value(E::bits_of(vq_, j)), Q.c, nmq) : 0.f;
+    sum += resid_weight(mp, P.izk, mq, Q.izk);
+  }
+  return sum;
+}
+
 template <int DT>
 __device__ __forceinline__ uint32_t ties_of(const uint4& v, uint32_t kstar) {
   using E = Elt<DT>;
@@ -1282,14 +1320,9 @@ __global__ void __launch_bounds__(kDrawThreads) split_draw_kernel(const SampleAr
       walk_listed<DT>(sh.lv[warp], sh.lr[warp], sp, sq, s0, s1, pt, qt, P, Q, mode == 1, pcut, base_p, base_q,
                       [&](int nb, uint32_t v, uint32_t rpv, uint32_t rqv) {
                         if (lane < nb) {
-                          float w[PV];
                           const uint4 xp = lds128(sp + 16u * v);
                           const uint4 xq = mode == 1 ? lds128(sq + 16u * v) : xp;
-                          pair_weights<DT>(xp, xq, P, Q, mode == 1, rpv, rqv, w);
-                          float ls = 0.f;
-#pragma unroll
-                          for (int j = 0; j < PV; ++j) ls += w[j];
-                          wsum = df_add(wsum, ls);
+                          wsum = df_add(wsum, pair_sum<DT>(xp, xq, P, Q, mode == 1, rpv, rqv));
                         }
                         return false;
                       });
