@@ -147,3 +147,22 @@ def test_split_repeat_calls_and_other_modes_share_the_workspace():
             assert np.array_equal(a, b) if a.dtype.kind in "iu" else np.allclose(a, b, rtol=1e-5, atol=1e-7)
     sv.spec_sample_launch_mode(sv.SPEC_LAUNCH_SPLIT)
     assert sv.spec_get_status(ws) == 0
+
+
+# Calls the split launches do not take run the fused launch instead, with the
+# same results: rows that are not whole 16-byte vectors, rows that do not start
+# on a 16-byte boundary, f32 rows with a filter, rows over 512 KiB.
+@pytest.mark.parametrize("B,k,V,dtype,top_k,top_p", [(5, 3, 1001, W.BF16, 0, 0.95), (4, 2, 4100, W.F32, 10, 0.9),
+                                                     (2, 2, 270000, W.BF16, 0, 0.95)])
+def test_split_falls_back_for_shapes_it_does_not_take(B, k, V, dtype, top_k, top_p):
+    _check(W.random_sample_case(B, k, V, dtype=dtype, seed=V, top_k=top_k, top_p=top_p))
+
+
+def test_split_unaligned_rows_fall_back():
+    sv = lib()
+    case = W.random_sample_case(4, 3, 4096, seed=5, top_p=0.95)
+    t = to_dev(np.concatenate([np.zeros(1, np.uint16), case.target.ravel()]))[1:].view(case.target.shape)
+    d = to_dev(np.concatenate([np.zeros(1, np.uint16), case.draft.ravel()]))[1:].view(case.draft.shape)
+    assert t.data_ptr() % 16 == 2
+    out = sv.spec_verify_sample(t, d, to_dev(case.tokens), to_dev(case.uniforms), 1.0, 0, 0.95)
+    compare_sample(case, [o.cpu().numpy() for o in out], run_sample_oracle(case))
