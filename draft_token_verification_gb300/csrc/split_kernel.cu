@@ -16,11 +16,13 @@
 //           vectors and cut into one equal range per CTA (one wave).  Per
 //           row piece every warp keeps its running maximum, its mass sum
 //           2^((v - m) c) (c = log2(e)/T) and, with a filter, exact counts
-//           of the bf16 keys in a window of kSW keys below its running
-//           maximum (a ring indexed by key mod kSW, cleared as the maximum
-//           rises).  Counts of tokens before the position's draft token and
-//           from it on are kept apart.  A piece leaves a record: its
-//           maximum, its mass and the counts below its own maximum key.
+//           of the bf16 keys in a window below its running maximum: at most
+//           kSW keys and kBandOct octaves of mass (a ring indexed by key mod
+//           kSW, cleared as the maximum rises).  The vectors holding such
+//           values are listed in shared memory and counted 32 at a time.
+//           Counts of tokens before the position's draft token and from it
+//           on are kept apart.  A piece leaves a record: its maximum, its
+//           mass and the counts below its own maximum key.
 //   row     One CTA per row merges the records of the row's pieces: the
 //           maximum, Z, and the window counts of the row.  The cut of top-k
 //           (a count) and top-p (a mass, over the top-k set) is the group of
