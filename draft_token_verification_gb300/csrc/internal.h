@@ -96,7 +96,7 @@ struct TreeRec {
   float nmp, nmq;        // -max * log2(e) / T of the target and draft rows
   float fa, fb;          // stop residual weight: max(0, 2^(l c + nmp) fa - 2^(d c + nmq) fb)
   int32_t pad[2];
-  double chunk[kTreeChunks];  // sums of that weight per (CTA, warp) chunk
+  float chunk[kTreeChunks][2];  // sums of that weight per (CTA, warp) chunk, double-float (hi, lo)
 };
 // The tree draw scans the chunk sums with one warp, two chunks per lane.
 static_assert(kTreeChunks == 2 * 32, "the tree draw reads exactly two chunk sums per lane of one warp");

@@ -28,9 +28,12 @@
 // the chunk from the sums, the element within it from the rows.
 //
 // Masses are 2^(l c + nm) with c = log2(e)/T and nm = -max * c, one ex2 per
-// element; sums are float per lane and double across lanes, warps and CTAs,
-// always in the same order, so every CTA of a cluster takes the same
-// decisions.
+// element.  Sums are float per lane and double-float (an unevaluated sum of
+// two floats) across lanes, warps and CTAs: this GPU's fp64 pipe is narrow,
+// and every fp64 instruction on a reduction or a decision sits on a chain
+// that one thread waits for.  They are always taken in the same order, so
+// every CTA of a cluster takes the same decisions; the accept test and the
+// draw compare double-float values.
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -51,13 +54,63 @@ constexpr uint32_t kPiece = 16384;  // bytes per bulk copy
 constexpr int kPre = 32;            // children whose logits are fetched ahead of the sibling loop
 constexpr int16_t kNoParent = -2;   // a parent entry outside [-1, N)
 
+// ------------------------------------------------ double-float arithmetic
+// A value hi + lo with |lo| at most half an ulp of hi: TwoSum for additions,
+// an fma for the rounding error of a product.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_norm(DF a) {  // Fast2Sum
+  const float s = a.hi + a.lo;
+  return DF{s, a.lo - (s - a.hi)};
+}
+__device__ __forceinline__ DF df_two(float x, float y) {  // x + y exactly
+  const float s = x + y;
+  const float bp = s - x;
+  return DF{s, (x - (s - bp)) + (y - bp)};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = df_two(a.hi, b.hi);
+  return df_norm(DF{s.hi, s.lo + (a.lo + b.lo)});
+}
+__device__ __forceinline__ DF df_sub(DF a, DF b) { return df_add(a, DF{-b.hi, -b.lo}); }
+__device__ __forceinline__ DF df_mulf(DF a, float f) {
+  const float p = a.hi * f;
+  return df_norm(DF{p, fmaf(a.lo, f, fmaf(a.hi, f, -p))});
+}
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = a.hi * b.hi;
+  return df_norm(DF{p, fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, fmaf(a.hi, b.hi, -p)))});
+}
+__device__ __forceinline__ bool df_gt(DF a, DF b) { return df_sub(a, b).hi > 0.f; }
+__device__ __forceinline__ bool df_pos(DF a) { return a.hi > 0.f; }  // of a normalised value
+__device__ __forceinline__ float df_f(DF a) { return a.hi + a.lo; }
+__device__ __forceinline__ DF shfl_df(DF a, int src) {
+  return DF{__shfl_sync(0xFFFFFFFFu, a.hi, src), __shfl_sync(0xFFFFFFFFu, a.lo, src)};
+}
+__device__ __forceinline__ DF shfl_up_df(DF a, int d) {
+  return DF{__shfl_up_sync(0xFFFFFFFFu, a.hi, d), __shfl_up_sync(0xFFFFFFFFu, a.lo, d)};
+}
+__device__ __forceinline__ DF shfl_down_df(DF a, int d) {
+  return DF{__shfl_down_sync(0xFFFFFFFFu, a.hi, d), __shfl_down_sync(0xFFFFFFFFu, a.lo, d)};
+}
+// Sum over the warp, valid in lane 0.
+__device__ __forceinline__ DF warp_sum_df(DF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_down_df(v, o));
+  return v;
+}
+
 struct TreeShm {
   uint64_t bar[2];           // bulk-copy completion: target slice, draft slice
-  double red[2][8];          // per-CTA values handed to the cluster, by round parity
-  double got[8];             // their cluster-wide combination
-  double wsum[kWarps][2];    // per-warp sums of the current pass
-  double zc[kWarps];         // per-warp sums of 2^(l c + nmp) (the c = 0 residual)
-  double wc[kWarps];         // per-warp sums of the last residual pass
+  float red[2][8];           // per-CTA values handed to the cluster, by round parity
+  float gm[2];               // cluster-wide maxima (target, draft)
+  DF gz[2];                  // cluster-wide masses relative to them
+  DF gsum;                   // cluster-wide sum of the last residual pass
+  int gbad;                  // a slice of the cluster holds NaN / +inf (or did not arrive)
+  DF wsum[kWarps][2];        // per-warp sums of the current pass
+  DF zc[kWarps];             // per-warp sums of 2^(l c + nmp) (the c = 0 residual)
+  DF wc[kWarps];             // per-warp sums of the last residual pass
   float fmax[kWarps][2];
   int bad[kWarps];
   int16_t kids[kMaxTreeNodes];
@@ -66,11 +119,11 @@ struct TreeShm {
   float kl[kPre], kd[kPre], ku[kPre];  // the first children's target / draft logits and uniforms
   float mloc[2];             // this CTA's maxima (target, draft)
   int badloc;               // this CTA's slices hold NaN / +inf (or did not arrive)
-  int nk, has_child, depth, attached, accept, timed_out;
+  int nk, has_child, accept, timed_out;
   int next[2];               // rank 0: the next work item claimed, by node parity
   int nextl;                 // that item, read by every CTA of the cluster
-  int walk_v, walk_n, walk_ok, draw_w;
-  double draw_rem;
+  int walk_v, walk_n, walk_ok, draw_w, draw_past;
+  DF draw_rem;
 };
 
 template <int DT>
@@ -208,80 +261,73 @@ __device__ __forceinline__ float tree_c(const TreeSampleArgs& a, int b) {
   return a.temps ? kLog2e / a.temps[b] : a.c;
 }
 
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
-  return v;  // lane 0
-}
-
 __device__ __forceinline__ float warp_max_f32(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
-// Loads value i (< 8) of every rank's sh.red[slot] in one round of
-// distributed-shared-memory reads: lane l holds value l/8 and l/8 + 4 of rank
-// l%8.  Warp 0 only.
-__device__ __forceinline__ void cluster_gather(TreeShm& sh, int slot, int nv, double& x0, double& x1) {
-  const int lane = threadIdx.x & 31, r = lane & (kTreeCl - 1), i = lane / kTreeCl;
-  x0 = i < nv ? ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i]), r)) : 0.0;
-  x1 = i + 4 < nv ? ld_cluster_f64(mapa_shared(smem_addr(&sh.red[slot][i + 4]), r)) : 0.0;
+// Warp 0, after a cluster barrier: lane l reads the first nv values that rank
+// l % kTreeCl left in sh.red[slot] (one round of distributed-shared-memory
+// reads, all lanes at once).
+template <int NV>
+__device__ __forceinline__ void cluster_read(TreeShm& sh, int slot, float (&v)[NV]) {
+  const uint32_t base = mapa_shared(smem_addr(&sh.red[slot][0]), static_cast<int>(threadIdx.x) & (kTreeCl - 1));
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = ld_cluster_f32(base + 4u * i);
 }
 
-// Value i of rank r from the gathered registers (all lanes take part).
-__device__ __forceinline__ double gathered(double x0, double x1, int i, int r) {
-  const double a = __shfl_sync(0xFFFFFFFFu, x0, (i & 3) * kTreeCl + r);
-  const double b = __shfl_sync(0xFFFFFFFFu, x1, (i & 3) * kTreeCl + r);
-  return i < 4 ? a : b;
+// The sum of one double-float per rank (lane r holds rank r's), in rank
+// order.  Every lane adds the same shuffled values in the same order, so
+// every lane, and every CTA of the cluster, holds the same bits.
+__device__ __forceinline__ DF rank_sum(DF x) {
+  DF s = shfl_df(x, 0);
+#pragma unroll
+  for (int r = 1; r < kTreeCl; ++r) s = df_add(s, shfl_df(x, r));
+  return s;
 }
 
-// Combines the nv values thread 0 of every CTA left in sh.red[slot] across the
-// cluster, in rank order (sum, or max when is_max), into sh.got.  Every CTA
-// computes the same result bit for bit.
-__device__ void cluster_combine(TreeShm& sh, int slot, int nv, bool is_max) {
+// The maximum over ranks (lanes that differ in their low bits).
+__device__ __forceinline__ float rank_max(float x) {
+#pragma unroll
+  for (int o = 1; o < kTreeCl; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+// The cluster-wide sum of the double-float thread 0 of every CTA left in
+// sh.red[slot][0..1], into sh.gsum.
+__device__ void cluster_sum(TreeShm& sh, int slot) {
   cg::this_cluster().sync();
   if (threadIdx.x < 32) {
-    double x0, x1;
-    cluster_gather(sh, slot, nv, x0, x1);
-    for (int i = 0; i < nv; ++i) {
-      double acc = gathered(x0, x1, i, 0);
-      for (int r = 1; r < kTreeCl; ++r) {
-        const double y = gathered(x0, x1, i, r);
-        acc = is_max ? fmax(acc, y) : acc + y;
-      }
-      if (threadIdx.x == 0) sh.got[i] = acc;
-    }
+    float v[2];
+    cluster_read(sh, slot, v);
+    const DF s = rank_sum(DF{v[0], v[1]});
+    if (threadIdx.x == 0) sh.gsum = s;
   }
   __syncthreads();
 }
 
-// Row statistics from per-CTA ones: sh.red[slot] = {max p, mass p, max q,
-// mass q, bad} with masses relative to the CTA's own maxima.  sh.got = {max p,
-// mass p, max q, mass q, bad}, masses relative to the cluster maxima
-// (each CTA's mass scaled by 2^((m_r - m) c), summed in rank order).
+// Row statistics from per-CTA ones: sh.red[slot] = {max p, mass p (hi, lo),
+// max q, mass q (hi, lo), bad} with masses relative to the CTA's own maxima.
+// Into sh.gm / sh.gz / sh.gbad: the cluster maxima, and the masses relative
+// to them (each CTA's mass scaled by 2^((m_r - m) c), summed in rank order).
 __device__ void cluster_combine_stats(TreeShm& sh, int slot, float c) {
   cg::this_cluster().sync();
   if (threadIdx.x < 32) {
-    double x0, x1;
-    cluster_gather(sh, slot, 5, x0, x1);
-    for (int k = 0; k < 2; ++k) {
-      float m = -INFINITY;
-      for (int r = 0; r < kTreeCl; ++r) m = fmaxf(m, static_cast<float>(gathered(x0, x1, 2 * k, r)));
-      double z = 0.0;
-      for (int r = 0; r < kTreeCl; ++r) {
-        const float mr = static_cast<float>(gathered(x0, x1, 2 * k, r));
-        const double zr = gathered(x0, x1, 2 * k + 1, r);
-        if (zr > 0.0) z += zr * static_cast<double>(ex2_approx((mr - m) * c));
-      }
-      if (threadIdx.x == 0) {
-        sh.got[2 * k] = m;
-        sh.got[2 * k + 1] = z;
-      }
+    float v[7];
+    cluster_read(sh, slot, v);
+    const float mp = rank_max(v[0]), mq = rank_max(v[3]), bad = rank_max(v[6]);
+    // a CTA without mass (an empty or all -inf slice) adds nothing, and no 0 * NaN
+    const DF zp = v[1] > 0.f ? df_mulf(DF{v[1], v[2]}, ex2_approx((v[0] - mp) * c)) : DF{0.f, 0.f};
+    const DF zq = v[4] > 0.f ? df_mulf(DF{v[4], v[5]}, ex2_approx((v[3] - mq) * c)) : DF{0.f, 0.f};
+    const DF sp = rank_sum(zp), sq = rank_sum(zq);
+    if (threadIdx.x == 0) {
+      sh.gm[0] = mp;
+      sh.gm[1] = mq;
+      sh.gz[0] = sp;
+      sh.gz[1] = sq;
+      sh.gbad = bad != 0.f;
     }
-    double bad = 0.0;
-    for (int r = 0; r < kTreeCl; ++r) bad = fmax(bad, gathered(x0, x1, 4, r));
-    if (threadIdx.x == 0) sh.got[4] = bad;
   }
   __syncthreads();
 }
@@ -428,15 +474,16 @@ __device__ void stage_rows(const TreeSampleArgs& a, TreeShm& sh, const unsigned 
 }
 
 // This CTA's masses relative to its own maxima (one pass), handed to the
-// cluster with the maxima: sh.red[slot] = {max p, mass p, max q, mass q, bad};
-// sh.zc keeps the per-warp target masses.  Then the cluster-wide statistics
-// in sh.got (cluster_combine_stats).
+// cluster with the maxima (the layout cluster_combine_stats reads); sh.zc
+// keeps the per-warp target masses.  Then the cluster-wide statistics in
+// sh.gm, sh.gz and sh.gbad.
 template <int DT>
 __device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int wchunk, bool with_q, float c,
                             int slot);
 
 // Sums over this CTA's slice, per warp chunk: 16-byte vectors, lanes
-// interleaved, float pairs per lane (two accumulators), double across lanes.
+// interleaved, float pairs per lane (two accumulators), double-float across
+// lanes.
 // The slice is whole vectors (lenv elements; an unaligned slice is padded
 // with -inf, which has no mass and no weight).  MODE 0: target and draft
 // masses (sh.wsum[w][0], [1]);  MODE 1: residual weights (sh.wsum[w][0]).
@@ -480,8 +527,8 @@ __device__ void slice_pass(TreeShm& sh, uint32_t sp, uint32_t sq, int lenv, int 
   float x0, y0, x1, y1;
   upk(add2(a0, a1), x0, y0);
   upk(add2(b0, b1), x1, y1);
-  const double d0 = warp_sum_f64(static_cast<double>(x0) + static_cast<double>(y0));
-  const double d1 = MODE == 0 ? warp_sum_f64(static_cast<double>(x1) + static_cast<double>(y1)) : 0.0;
+  const DF d0 = warp_sum_df(df_two(x0, y0));
+  const DF d1 = MODE == 0 ? warp_sum_df(df_two(x1, y1)) : DF{0.f, 0.f};
   if (lane == 0) {
     sh.wsum[warp][0] = d0;
     sh.wsum[warp][1] = d1;
@@ -498,49 +545,38 @@ __device__ void slice_stats(TreeShm& sh, uint32_t sp, uint32_t sq, int len, int 
   const float nm1 = m1 == -INFINITY ? 0.f : -m1 * c;
   slice_pass<DT, 0>(sh, sp, sq, len, wchunk, with_q, c, nm0, nm1, 0.f, 0.f);
   if (threadIdx.x == 0) {
-    double z0 = 0.0, z1 = 0.0;
-    for (int w = 0; w < kWarps; ++w) {
+    DF z0 = sh.wsum[0][0], z1 = sh.wsum[0][1];
+    sh.zc[0] = z0;
+    for (int w = 1; w < kWarps; ++w) {
       sh.zc[w] = sh.wsum[w][0];
-      z0 += sh.wsum[w][0];
-      z1 += sh.wsum[w][1];
+      z0 = df_add(z0, sh.wsum[w][0]);
+      z1 = df_add(z1, sh.wsum[w][1]);
     }
     sh.red[slot][0] = m0;
-    sh.red[slot][1] = z0;
-    sh.red[slot][2] = m1;
-    sh.red[slot][3] = z1;
-    sh.red[slot][4] = sh.badloc;
+    sh.red[slot][1] = z0.hi;
+    sh.red[slot][2] = z0.lo;
+    sh.red[slot][3] = m1;
+    sh.red[slot][4] = z1.hi;
+    sh.red[slot][5] = z1.lo;
+    sh.red[slot][6] = static_cast<float>(sh.badloc);
   }
   cluster_combine_stats(sh, slot, c);
 }
 
-// Parents of tree b into sh.par (entries outside [-1, N) become kNoParent),
-// then, by thread 0, the depth of node j and whether its path reaches the root.
-__device__ void tree_header(const TreeSampleArgs& a, TreeShm& sh, int b, int j) {
+// Parents of tree b into sh.par (entries outside [-1, N) become kNoParent).
+// The plan kernel has already checked that every listed node is attached
+// below max_depth.
+__device__ void stage_parents(const TreeSampleArgs& a, TreeShm& sh, int b) {
   const int32_t* par = a.parents + static_cast<size_t>(b) * a.N;
   for (int i = threadIdx.x; i < a.N; i += kThreads) {
     const int p = par[i];
     sh.par[i] = static_cast<int16_t>(p >= -1 && p < a.N ? p : kNoParent);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int d = 0, v = j, att = 1;
-    while (v != 0) {  // parents strictly decrease, so this ends within j steps
-      const int pv = sh.par[v];
-      if (pv < 0 || pv >= v) {
-        att = 0;
-        break;
-      }
-      v = pv;
-      ++d;
-    }
-    sh.depth = d;
-    sh.attached = att;
-  }
-  __syncthreads();
 }
 
 // The correction drawn at stop node v of tree b (n nodes accepted) by one
-// CTA: the chunk from the node's record (double prefix over its chunk sums),
+// CTA: the chunk from the node's record (double-float prefix over its chunk sums),
 // the warp sub-range and the element from the node's rows.
 template <int DT>
 __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int n) {
@@ -555,31 +591,33 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
   const unsigned char* drow = static_cast<const unsigned char*>(a.draft) + g * a.V * E;
   if (warp == 0) {
     // chunk: lane L holds chunks 2L and 2L+1
-    const double c0 = __ldcg(&r->chunk[2 * lane]), c1 = __ldcg(&r->chunk[2 * lane + 1]);
-    double incl = c0 + c1;
+    const DF c0{__ldcg(&r->chunk[2 * lane][0]), __ldcg(&r->chunk[2 * lane][1])};
+    const DF c1{__ldcg(&r->chunk[2 * lane + 1][0]), __ldcg(&r->chunk[2 * lane + 1][1])};
+    const DF own = df_add(c0, c1);
+    DF incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
+      const DF y = shfl_up_df(incl, o);
+      if (lane >= o) incl = df_add(incl, y);
     }
-    const double total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    const double target = static_cast<double>(a.uniforms[static_cast<size_t>(b) * a.N]) * total;
-    const uint32_t over = __ballot_sync(0xFFFFFFFFu, incl > target);
-    const uint32_t pos = __ballot_sync(0xFFFFFFFFu, c0 > 0.0 || c1 > 0.0);
+    const DF total = shfl_df(incl, 31);
+    const DF target = df_mulf(total, a.uniforms[static_cast<size_t>(b) * a.N]);
+    const uint32_t over = __ballot_sync(0xFFFFFFFFu, df_gt(incl, target));
+    const uint32_t pos = __ballot_sync(0xFFFFFFFFu, df_pos(c0) || df_pos(c1));
     int l = -1;
     if (over) l = __ffs(over) - 1;
     else if (pos) l = 31 - __clz(pos);
     int ci = -1;
-    double rem = 0.0;
+    DF rem{0.f, 0.f};
     if (l >= 0) {
-      const double ex = __shfl_sync(0xFFFFFFFFu, incl - (c0 + c1), l);
-      const double a0 = __shfl_sync(0xFFFFFFFFu, c0, l), a1 = __shfl_sync(0xFFFFFFFFu, c1, l);
+      const DF ex = shfl_df(df_sub(incl, own), l);
+      const DF a0 = shfl_df(c0, l), a1 = shfl_df(c1, l);
       if (over) {
-        ci = (ex + a0 > target || a1 <= 0.0) ? 2 * l : 2 * l + 1;
+        ci = (df_gt(df_add(ex, a0), target) || !df_pos(a1)) ? 2 * l : 2 * l + 1;
       } else {
-        ci = a1 > 0.0 ? 2 * l + 1 : 2 * l;
+        ci = df_pos(a1) ? 2 * l + 1 : 2 * l;
       }
-      rem = target - (ci & 1 ? ex + a0 : ex);
+      rem = df_sub(target, ci & 1 ? df_add(ex, a0) : ex);
     }
     if (lane == 0) {
       sh.draw_w = ci;
@@ -610,29 +648,26 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
     for (int t = wlo + lane; t < whi; t += 32)
       s += resid_weight(Elt<DT>::value(Elt<DT>::bits_at(lrow, t)),
                         fb == 0.f ? 0.f : Elt<DT>::value(Elt<DT>::bits_at(drow, t)), tree_c(a, b), nmp, nmq, fa, fb);
-    const double ws = warp_sum_f64(static_cast<double>(s));
+    const DF ws = warp_sum_df(DF{s, 0.f});
     if (lane == 0) sh.wsum[warp][0] = ws;
   }
   __syncthreads();
   if (tid == 0) {
-    const double rem = sh.draw_rem;
-    double cum = 0.0;
+    const DF rem = sh.draw_rem;
+    DF cum{0.f, 0.f};
     int pick = -1, lastpos = -1;
     for (int w = 0; w < kWarps; ++w) {
-      const double s = sh.wsum[w][0];
-      if (s > 0.0) lastpos = w;
-      if (cum + s > rem && s > 0.0) {
+      const DF s = sh.wsum[w][0];
+      if (df_pos(s)) lastpos = w;
+      if (df_pos(s) && df_gt(df_add(cum, s), rem)) {
         pick = w;
         break;
       }
-      cum += s;
+      cum = df_add(cum, s);
     }
-    if (pick < 0) {
-      pick = lastpos;
-      sh.draw_rem = INFINITY;  // past every element: the last positive one
-    } else {
-      sh.draw_rem = rem - cum;
-    }
+    sh.draw_past = pick < 0;  // past every element: the last positive one
+    if (pick < 0) pick = lastpos;
+    else sh.draw_rem = df_sub(rem, cum);
     sh.walk_v = pick;
   }
   __syncthreads();
@@ -640,9 +675,10 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
   if (warp == (pick < 0 ? 0 : pick)) {
     int token = -1;
     if (pick >= 0) {
-      const double rem = sh.draw_rem;
+      const DF rem = sh.draw_rem;
+      const bool past = sh.draw_past != 0;
       const int wlo = min(chi, clo + pick * sub), whi = min(chi, clo + (pick + 1) * sub);
-      double acc = 0.0;
+      DF acc{0.f, 0.f};
       constexpr int kAhead = 8;  // rounds of 32 elements fetched before they are scanned
       bool found = false;
       for (int base0 = wlo; base0 < whi && !found; base0 += 32 * kAhead) {
@@ -658,13 +694,9 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
 #pragma unroll
         for (int k = 0; k < kAhead; ++k) {
           const int base = base0 + 32 * k;
-          double incl = static_cast<double>(w[k]);
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const uint32_t hit = __ballot_sync(0xFFFFFFFFu, w[k] > 0.f && acc + incl > rem);
+          // 32 weights: a float prefix, added to the double-float sum before them
+          const float incl = warp_incl_scan(w[k]);
+          const uint32_t hit = __ballot_sync(0xFFFFFFFFu, w[k] > 0.f && !past && df_gt(df_add(acc, DF{incl, 0.f}), rem));
           const uint32_t pos = __ballot_sync(0xFFFFFFFFu, w[k] > 0.f);
           if (!found) {
             if (pos) token = base + 31 - __clz(pos);
@@ -673,7 +705,7 @@ __device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int 
               found = true;
             }
           }
-          acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+          acc = df_add(acc, DF{__shfl_sync(0xFFFFFFFFu, incl, 31), 0.f});
         }
       }
     }
@@ -815,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     if (a.aligned && threadIdx.x == 0)
       stage_issue(sh, pfull + static_cast<size_t>(lo) * E, qfull + static_cast<size_t>(lo) * E,
                   static_cast<uint32_t>(len) * E, true, sp, sq);
-    tree_header(a, sh, b, j);
+    stage_parents(a, sh, b);
     collect_children(a, sh, tok, j, true);
     const int nk = sh.nk;
     for (int i = threadIdx.x; i < min(nk, kPre); i += kThreads) {
@@ -835,14 +867,14 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
     int accepted = -1;
     bool cz = true;
     float fa = 1.f, fb = 0.f, nmp = 0.f, nmq = 0.f;
-    const float mp = static_cast<float>(sh.got[0]), mq = static_cast<float>(sh.got[2]);
-    if (sh.got[4] != 0.0 || mp == -INFINITY || mq == -INFINITY) {
+    const float mp = sh.gm[0], mq = sh.gm[1];
+    if (sh.gbad || mp == -INFINITY || mq == -INFINITY) {
       rflags |= kRecBad;
     } else {
       nmp = -mp * c;
       nmq = -mq * c;
-      const double zp = sh.got[1], zq = sh.got[3];
-      double cc = 0.0, W = 1.0;
+      const DF zp = sh.gz[0], zq = sh.gz[1];  // each at least 1: the maximum's own mass
+      DF cc{0.f, 0.f}, W{1.f, 0.f};
       for (int i = 0; i < nk; ++i) {
         const int child = sh.kids[i];
         if (threadIdx.x == 0) {
@@ -857,44 +889,51 @@ __global__ void __launch_bounds__(kThreads, 3) tree_node_kernel(const TreeSample
             dx = Elt<DT>::value(Elt<DT>::bits_at(qfull, x));
             uf = uni[child];
           }
-          const double px = static_cast<double>(ex2_approx(fmaf(lx, c, nmp))) / zp;
-          const double qx = static_cast<double>(ex2_approx(fmaf(dx, c, nmq))) / zq;
-          sh.accept = static_cast<double>(uf) * qx * W < px - cc * qx;
+          // u q(x) W < p(x) - cc q(x) with p(x) = ep / zp and q(x) = eq / zq,
+          // both sides multiplied by zp zq > 0
+          const float ep = ex2_approx(fmaf(lx, c, nmp)), eq = ex2_approx(fmaf(dx, c, nmq));
+          const DF lhs = df_mulf(df_mulf(df_mul(W, zp), uf), eq);
+          const DF rhs = df_sub(df_mulf(zq, ep), df_mulf(df_mul(cc, zp), eq));
+          sh.accept = df_gt(rhs, lhs);
         }
         __syncthreads();
         if (sh.accept) {
           accepted = child;
           break;
         }
-        cc += W;
-        fa = static_cast<float>(1.0 / zp);
-        fb = static_cast<float>(cc / zq);
+        cc = df_add(cc, W);
+        fa = __frcp_rn(df_f(zp));
+        fb = __fdiv_rn(df_f(cc), df_f(zq));
         slice_pass<DT, 1>(sh, sp, sq, lenv, a.wchunk, true, c, nmp, nmq, fa, fb);
         slot = round++ & 1;
         if (threadIdx.x == 0) {
-          double sum = 0.0;
-          for (int w = 0; w < kWarps; ++w) {
+          DF sum = sh.wsum[0][0];
+          sh.wc[0] = sum;
+          for (int w = 1; w < kWarps; ++w) {
             sh.wc[w] = sh.wsum[w][0];
-            sum += sh.wsum[w][0];
+            sum = df_add(sum, sh.wsum[w][0]);
           }
-          sh.red[slot][0] = sum;
+          sh.red[slot][0] = sum.hi;
+          sh.red[slot][1] = sum.lo;
         }
-        cluster_combine(sh, slot, 1, false);
-        const double wn = sh.got[0];
-        if (wn > 0.0) {
+        cluster_sum(sh, slot);
+        const DF wn = sh.gsum;
+        if (df_pos(wn)) {
           W = wn;
           cz = false;
         } else {  // residual of mass zero: back to p
-          W = 1.0;
-          cc = 0.0;
+          W = DF{1.f, 0.f};
+          cc = DF{0.f, 0.f};
           cz = true;
         }
       }
       if (accepted < 0 && threadIdx.x < kWarps) {
         // the c = 0 residual: this CTA's target masses, rescaled to the row maximum
         const float m0 = sh.mloc[0];
-        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * c));
-        rec->chunk[rank * kWarps + threadIdx.x] = cz ? sh.zc[threadIdx.x] * scale : sh.wc[threadIdx.x];
+        const float scale = m0 == -INFINITY ? 0.f : ex2_approx((m0 - mp) * c);
+        const DF w = cz ? df_mulf(sh.zc[threadIdx.x], scale) : sh.wc[threadIdx.x];
+        rec->chunk[rank * kWarps + threadIdx.x][0] = w.hi;
+        rec->chunk[rank * kWarps + threadIdx.x][1] = w.lo;
       }
     }
     if (rank == 0 && threadIdx.x == 0) {
@@ -989,15 +1028,17 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
                    sp, sp, php, phq, false);
     slice_stats<DT>(sh, sp, sp, (len + Elt<DT>::kPerVec - 1) / Elt<DT>::kPerVec * Elt<DT>::kPerVec, a.wchunk, false,
                     tree_c(a, b), 0);
-    const float mp = static_cast<float>(sh.got[0]);
-    if (sh.got[4] != 0.0 || mp == -INFINITY) {
+    const float mp = sh.gm[0];
+    if (sh.gbad || mp == -INFINITY) {
       ok = false;
       if (rank == 0 && tid == 0) atomicOr(a.status, SPEC_STATUS_BAD_ROW);
     } else {
       if (tid < kWarps) {
         const float m0 = sh.mloc[0];
-        const double scale = m0 == -INFINITY ? 0.0 : static_cast<double>(ex2_approx((m0 - mp) * tree_c(a, b)));
-        rec->chunk[rank * kWarps + tid] = sh.zc[tid] * scale;
+        const float scale = m0 == -INFINITY ? 0.f : ex2_approx((m0 - mp) * tree_c(a, b));
+        const DF w = df_mulf(sh.zc[tid], scale);
+        rec->chunk[rank * kWarps + tid][0] = w.hi;
+        rec->chunk[rank * kWarps + tid][1] = w.lo;
       }
       if (rank == 0 && tid == 0) {
         rec->nmp = -mp * tree_c(a, b);
