@@ -576,23 +576,40 @@ __device__ void stage_parents(const TreeSampleArgs& a, TreeShm& sh, int b) {
 }
 
 // The correction drawn at stop node v of tree b (n nodes accepted) by one
-// CTA: the chunk from the node's record (double-float prefix over its chunk sums),
-// the warp sub-range and the element from the node's rows.
+// CTA: the chunk by a double-float prefix over the node's chunk sums, then
+// the warp sub-range and the element from the node's rows.  The chunk sums
+// and the residual's parameters come from the node's record, or, for a stop
+// node whose p the walk's cluster has just summed (`local`), from every
+// CTA's sh.wc by distributed-shared-memory reads and from the arguments.
 template <int DT>
-__device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int n) {
+__device__ void draw_at(const TreeSampleArgs& a, TreeShm& sh, int b, int v, int n, bool local, float nmp,
+                        float nmq, float fa, float fb) {
   constexpr int E = Elt<DT>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int D = a.max_depth + 1;
   int32_t* otok = a.out_tokens + static_cast<size_t>(b) * D;
   const size_t g = static_cast<size_t>(b) * a.N + v;
   const TreeRec* r = a.recs + g;
-  const float nmp = __ldcg(&r->nmp), nmq = __ldcg(&r->nmq), fa = __ldcg(&r->fa), fb = __ldcg(&r->fb);
+  if (!local) {
+    nmp = __ldcg(&r->nmp);
+    nmq = __ldcg(&r->nmq);
+    fa = __ldcg(&r->fa);
+    fb = __ldcg(&r->fb);
+  }
   const unsigned char* lrow = static_cast<const unsigned char*>(a.logits) + g * a.V * E;
   const unsigned char* drow = static_cast<const unsigned char*>(a.draft) + g * a.V * E;
   if (warp == 0) {
-    // chunk: lane L holds chunks 2L and 2L+1
-    const DF c0{__ldcg(&r->chunk[2 * lane][0]), __ldcg(&r->chunk[2 * lane][1])};
-    const DF c1{__ldcg(&r->chunk[2 * lane + 1][0]), __ldcg(&r->chunk[2 * lane + 1][1])};
+    // chunk: lane L holds chunks 2L and 2L+1 (chunk i is warp i % kWarps of rank i / kWarps)
+    DF c0, c1;
+    if (local) {
+      const int rk = 2 * lane / kWarps, w0 = 2 * lane % kWarps;
+      const uint32_t p0 = mapa_shared(smem_addr(&sh.wc[w0]), rk), p1 = mapa_shared(smem_addr(&sh.wc[w0 + 1]), rk);
+      c0 = DF{ld_cluster_f32(p0), ld_cluster_f32(p0 + 4u)};
+      c1 = DF{ld_cluster_f32(p1), ld_cluster_f32(p1 + 4u)};
+    } else {
+      c0 = DF{__ldcg(&r->chunk[2 * lane][0]), __ldcg(&r->chunk[2 * lane][1])};
+      c1 = DF{__ldcg(&r->chunk[2 * lane + 1][0]), __ldcg(&r->chunk[2 * lane + 1][1])};
+    }
     const DF own = df_add(c0, c1);
     DF incl = own;
 #pragma unroll
@@ -970,18 +987,30 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
   int32_t* otok = a.out_tokens + static_cast<size_t>(b) * D;
   int32_t* opath = a.out_path + static_cast<size_t>(b) * D;
   const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.N;
+  // every node's outcome in one round of loads; thread 0 then walks them here
+  __shared__ int16_t w_acc[kMaxTreeNodes];
+  __shared__ uint8_t w_fl[kMaxTreeNodes];
+  __shared__ int16_t w_path[kMaxTreeNodes];
+  const TreeRec* trec = a.recs + static_cast<size_t>(b) * a.N;
+  for (int i = tid; i < a.N; i += kThreads) {
+    const int acc = trec[i].accepted;
+    w_acc[i] = static_cast<int16_t>(acc > i && acc < a.N ? acc : -1);  // a child's id exceeds its parent's
+    w_fl[i] = static_cast<uint8_t>(trec[i].flags | (acc >= 0 && !(acc > i && acc < a.N) ? kRecBad : 0u));
+  }
   if (tid == 0) {
     mbar_init(&sh.bar[0], 1);
     mbar_init(&sh.bar[1], 1);
     fence_mbar_init();
     sh.timed_out = 0;
     sh.has_child = 0;
+  }
+  __syncthreads();
+  if (tid == 0) {
     int v = 0, n = 0, ok = 1;
     uint32_t st = 0;
     for (int it = 0; it <= a.max_depth; ++it) {
-      const TreeRec* r = a.recs + static_cast<size_t>(b) * a.N + v;
-      const uint32_t fl = r->flags;
-      const int acc = r->accepted;
+      const uint32_t fl = w_fl[v];
+      const int acc = w_acc[v];
       if (fl & (kRecBad | kRecDetached)) {
         ok = 0;
         st |= SPEC_STATUS_BAD_ROW;
@@ -992,11 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
           ok = 0;
           break;
         }
-        if (rank == 0) {
-          opath[n] = acc;
-          otok[n] = tok[acc];
-        }
-        ++n;
+        w_path[n++] = static_cast<int16_t>(acc);
         v = acc;
         continue;
       }
@@ -1014,12 +1039,18 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
   bool ok = sh.walk_ok != 0;
   if (rank == 0)
     for (int i = tid; i < D; i += kThreads) {
-      if (i > n) otok[i] = -1;
-      if (i >= n) opath[i] = -1;
+      if (i < n) {
+        opath[i] = w_path[i];
+        otok[i] = tok[w_path[i]];
+      } else {
+        opath[i] = -1;
+        if (i > n) otok[i] = -1;
+      }
     }
-  if (ok && sh.has_child) {  // stop distribution p of a node whose pass only marked it
+  const bool local = ok && sh.has_child;
+  float nmp_l = 0.f;
+  if (local) {  // stop distribution p of a node whose pass only marked it
     const size_t g = static_cast<size_t>(b) * a.N + v;
-    TreeRec* rec = a.recs + g;
     const uint32_t sp = smem_addr(dyn);
     const int lo = rank * a.slice;
     const int len = max(0, min(a.V, lo + a.slice) - lo);
@@ -1033,28 +1064,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeSample
       ok = false;
       if (rank == 0 && tid == 0) atomicOr(a.status, SPEC_STATUS_BAD_ROW);
     } else {
-      if (tid < kWarps) {
+      if (tid < kWarps) {  // this CTA's chunk sums, rescaled to the row maximum, for rank 0's draw
         const float m0 = sh.mloc[0];
         const float scale = m0 == -INFINITY ? 0.f : ex2_approx((m0 - mp) * tree_c(a, b));
-        const DF w = df_mulf(sh.zc[tid], scale);
-        rec->chunk[rank * kWarps + tid][0] = w.hi;
-        rec->chunk[rank * kWarps + tid][1] = w.lo;
+        sh.wc[tid] = df_mulf(sh.zc[tid], scale);
       }
-      if (rank == 0 && tid == 0) {
-        rec->nmp = -mp * tree_c(a, b);
-        rec->nmq = 0.f;
-        rec->fa = 1.f;
-        rec->fb = 0.f;
-      }
+      nmp_l = -mp * tree_c(a, b);
     }
     if (sh.timed_out && tid == 0) mbar_wait_bounded(&sh.bar[0], php ^ 1u);
-    __threadfence();
-    cluster.sync();  // every CTA's chunk sums are written
+    cluster.sync();  // every CTA's chunk sums are in its shared memory
   }
   if (rank == 0) {
     if (ok) {
-      __threadfence();
-      draw_at<DT>(a, sh, b, v, n);
+      draw_at<DT>(a, sh, b, v, n, local, nmp_l, 0.f, 1.f, 0.f);
     } else if (tid == 0) {
       otok[n] = -1;
       a.out_n[b] = n;
