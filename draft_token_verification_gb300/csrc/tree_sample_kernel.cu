@@ -747,6 +747,7 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   __shared__ int testable_child[kMaxTreeNodes];  // children to test, per node
   __shared__ int16_t raw[kMaxTreeNodes];
   __shared__ int16_t list[kMaxTreeNodes];
+  __shared__ int order_key[kMaxTreeNodes];
   __shared__ int cnt, base;
   const int b = blockIdx.x, tid = threadIdx.x, N = a.N;
   // a tree temperature that gives no distribution: every node bad, nothing listed
@@ -804,15 +805,19 @@ __global__ void __launch_bounds__(kThreads) tree_plan_kernel(const TreeSampleArg
   }
   if (st) atomicOr(a.status, st);
   __syncthreads();
-  // order: more children to test first (more possible residual passes), then node index
+  // order: more children to test first (more possible residual passes), then
+  // node index -- one key per listed node, larger first, all keys distinct
   for (int i = tid; i < cnt; i += kThreads) {
-    const int ni = raw[i], ci = testable_child[ni];
+    const int ni = raw[i];
+    order_key[i] = testable_child[ni] * kMaxTreeNodes + (kMaxTreeNodes - 1 - ni);
+  }
+  __syncthreads();
+  for (int i = tid; i < cnt; i += kThreads) {
+    const int mine = order_key[i];
     int r = 0;
-    for (int t = 0; t < cnt; ++t) {
-      const int nt = raw[t], ct = testable_child[nt];
-      r += (ct > ci || (ct == ci && nt < ni)) ? 1 : 0;
-    }
-    list[r] = static_cast<int16_t>(ni);
+#pragma unroll 8
+    for (int t = 0; t < cnt; ++t) r += order_key[t] > mine ? 1 : 0;
+    list[r] = raw[i];
   }
   if (tid == 0) base = static_cast<int>(atomicAdd(a.work_count, static_cast<uint32_t>(cnt)));
   __syncthreads();
