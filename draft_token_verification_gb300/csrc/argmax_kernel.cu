@@ -204,7 +204,41 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
     uint32_t nan_seen = 0;
     if (a.aligned) {  // whole 16-byte vectors (V is a multiple of kPerVec)
       const uint4* vp = reinterpret_cast<const uint4*>(base);
-      for (int v0 = v_lo + tid; v0 < v_hi; v0 += kThreads * kUnroll) {
+      // Branch-free fold: the first vector whose maximum is the largest so
+      // far (strictly, so an earlier vector keeps a tie) is kept with its
+      // bits; the element's place in it is found once at the end.  A vector
+      // holding NaN is never kept and leaves nan_acc NaN.
+      float bv = -INFINITY, nan_acc = 0.f;
+      int bidx = -1;
+      uint4 bx = make_uint4(0u, 0u, 0u, 0u);
+      auto fold = [&](const uint4& x, int v) {
+        float vm;
+        if constexpr (DT == DT_BF16) {  // packed: three bf16x2 maxima, then the two halves
+          const uint32_t m2 = bmax2_nan(bmax2_nan(x.x, x.y), bmax2_nan(x.z, x.w));
+          vm = max_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+        } else {
+          vm = E::value(E::bits_of(x, 0));
+#pragma unroll
+          for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x, j)));
+        }
+        nan_acc = max_nan(nan_acc, vm);
+        const bool take = vm > bv || (bidx < 0 && vm == vm);
+        bv = take ? vm : bv;
+        bidx = take ? v : bidx;
+        bx.x = take ? x.x : bx.x;
+        bx.y = take ? x.y : bx.y;
+        bx.z = take ? x.z : bx.z;
+        bx.w = take ? x.w : bx.w;
+      };
+      int v0 = v_lo + tid;
+      for (; v0 + (kUnroll - 1) * kThreads < v_hi; v0 += kThreads * kUnroll) {  // every load in range
+        uint4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) x[u] = ldg_stream(vp + v0 + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) fold(x[u], v0 + u * kThreads);
+      }
+      if (v0 < v_hi) {  // the last batch, in part
         uint4 x[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -212,30 +246,17 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const ArgmaxArgs a) {
           x[u] = v < v_hi ? ldg_stream(vp + v) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * kThreads;
-          if (v < v_hi) {
-            float vm;
-            if constexpr (DT == DT_BF16) {  // packed: three bf16x2 maxima, then the two halves
-              const uint32_t m2 = bmax2_nan(bmax2_nan(x[u].x, x[u].y), bmax2_nan(x[u].z, x[u].w));
-              vm = max_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
-            } else {
-              vm = E::value(E::bits_of(x[u], 0));
+        for (int u = 0; u < kUnroll; ++u)
+          if (v0 + u * kThreads < v_hi) fold(x[u], v0 + u * kThreads);
+      }
+      nan_seen = nan_acc != nan_acc ? 1u : 0u;
+      if (bidx >= 0) {
+        int j0 = E::kPerVec - 1;
 #pragma unroll
-              for (int j = 1; j < E::kPerVec; ++j) vm = max_nan(vm, E::value(E::bits_of(x[u], j)));
-            }
-            if (vm != vm) {
-              nan_seen = 1u;
-            } else if (best_pos < 0 || vm > best) {
-              int j0 = E::kPerVec - 1;
-#pragma unroll
-              for (int j = E::kPerVec - 1; j >= 0; --j)
-                if (E::value(E::bits_of(x[u], j)) == vm) j0 = j;
-              best = vm;
-              best_pos = v * E::kPerVec + j0;
-            }
-          }
-        }
+        for (int j = E::kPerVec - 1; j >= 0; --j)
+          if (E::value(E::bits_of(bx, j)) == bv) j0 = j;
+        best = bv;
+        best_pos = bidx * E::kPerVec + j0;
       }
     } else {
       const int hi = min(V, v_hi * E::kPerVec);
