@@ -306,6 +306,10 @@ int spec_first_draft_check(const void* prev_rows, const int32_t* draft0, int B, 
   return SPEC_OK;
 }
 
+// The tree kernels stage one tree's parents, tokens and outcomes in shared
+// arrays of kMaxTreeNodes entries; the largest N the entry points accept fits.
+static_assert(SPEC_MAX_TREE_NODES <= kMaxTreeNodes, "a tree of SPEC_MAX_TREE_NODES nodes must fit the tree kernels");
+
 int spec_verify_tree_greedy(const void* node_logits, const int32_t* node_tokens, const int32_t* parents, int B,
                             int N, int V, int max_depth, spec_dtype dtype, int32_t* out_tokens, int32_t* out_path,
                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
